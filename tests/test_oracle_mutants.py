@@ -1,0 +1,48 @@
+"""Plants one mistake at a time in a copy of the oracle (on the CPU) and checks that the
+pins in test_oracle_pins.py reject every such copy."""
+import inspect
+
+import pytest
+
+import oracle
+import tests.test_oracle_pins as pins
+
+# (name, text in anchor_oracle.c, replacement): each a plausible slip.
+MUTANTS = [
+    ("scale dropped", "a[j] = scale * s;", "a[j] = s;"),
+    ("scale applied twice", "a[j] = scale * s;", "a[j] = scale * scale * s;"),
+    ("max subtracted with wrong sign", "a[j] = exp(a[j] - mx);", "a[j] = exp(mx - a[j]);"),
+    ("row not normalised", "for (long j = 0; j < m; ++j) a[j] /= z;", ";"),
+    ("Delta^-1 dropped", "Wp[j * d + k] = delta[j] != 0.0 ? s / delta[j] : 0.0;", "Wp[j * d + k] = s;"),
+    ("Delta from the first token only", "for (long i = 0; i < n; ++i) s += A[i * m + j];", "s = A[j];"),
+    ("value column reversed", "s += A[i * m + j] * V[i * d + k];", "s += A[i * m + j] * V[i * d + (d - 1 - k)];"),
+    ("first anchor dropped in the apply", "for (long j = 0; j < m; ++j) s += a[j] * Wp[j * d + k];",
+     "for (long j = 1; j < m; ++j) s += a[j] * Wp[j * d + k];"),
+    ("anchors indexed by batch", "U + (size_t)h * (size_t)m * (size_t)d", "U + (size_t)((b + h) % heads) * (size_t)m * (size_t)d"),
+    ("query/anchor dims crossed", "s += Q[i * d + k] * U[j * d + k];", "s += Q[i * d + k] * U[k % m * d + j % d];"),
+]
+
+
+def _run_pins(mut) -> list:
+    failed = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_") or name == "test_bad_arguments_raise":
+            continue
+        params = inspect.signature(fn).parameters
+        cases = [{}]
+        if "case" in params:
+            cases = [{"case": c} for c in ("m1", "identical_anchors", "zero_queries")]
+        for kw in cases:
+            try:
+                fn(mut, **kw)
+            except (AssertionError, ValueError, FloatingPointError, ZeroDivisionError):
+                failed.append(name)
+    return failed
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_reject_planted_mistake(tmp_path, name, old, new):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
+    mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    assert _run_pins(mut), f"no pin rejects the planted mistake '{name}'"
