@@ -1,0 +1,108 @@
+/*
+ * anchor_attn.h - C ABI of the GB300 (sm_103a) anchor-attention forward.
+ *
+ * The operation (AnchorFormer, arXiv 2505.16463; pith.science verdict on 2505.16463,
+ * "core_discovery", "key_machinery" and the referee summary of Eq. 11/12):
+ *
+ *   A[i][j] = softmax over j of ( scale * q_i . u_j )      n x m, rows sum to one
+ *   Delta   = diag( sum_i A[i][j] )                        m x m, the anchor degrees
+ *   H       = A Delta^{-1} A^T V                           n x d
+ *
+ * evaluated as A (Delta^{-1} (A^T V)), so no n x n matrix exists anywhere (the reordering
+ * B^T V -> Delta^{-1}(B^T V) -> B(Delta^{-1} B^T V) of the referee summary, B == A).
+ * Each (batch, head) pair - a "slice" - is independent (the construction is per head).
+ * An anchor that no token reaches (Delta_j == 0 after underflow) contributes nothing.
+ *
+ * Layout (row-major, dense, no padding):
+ *   Q, V, H : [B][heads][n][d]
+ *   U       : [heads][m][d]    one set of m learnable anchor keys per head, shared by
+ *                              every batch entry
+ * Every pointer is a DEVICE pointer, 16-byte aligned.  The caller owns all buffers.
+ * H must not overlap Q, U or V (the forward reads Q twice).
+ *
+ * Calls are asynchronous and ordered on `stream` (a cudaStream_t passed as void*;
+ * NULL = the legacy default stream).  No host synchronisation happens inside.
+ * Workspace, where a variant needs one, is taken with cudaMallocAsync on `stream` and
+ * released with cudaFreeAsync on the same stream before the call returns.
+ * Results are bit-identical from run to run on the same device and library build.
+ *
+ * Shapes: B, heads, n >= 0 (a zero makes the call a no-op that returns OK and accepts NULL
+ * pointers); m >= 1; d in {16, 32, 64, 128}; m * d <= 16384 (so m <= 256 for d <= 64 and
+ * m <= 128 for d = 128); B * heads * n * d < 2^63.  scale must be finite.
+ *
+ * Errors are returned, never thrown or printed; a failed call launches nothing unless the
+ * status is ANCHOR_ATTN_ERR_CUDA.
+ */
+#ifndef ANCHOR_ATTN_H
+#define ANCHOR_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ANCHOR_ATTN_API __attribute__((visibility("default")))
+#else
+#define ANCHOR_ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ANCHOR_ATTN_OK = 0,
+    ANCHOR_ATTN_ERR_INVALID_ARG = 1, /* NULL or misaligned pointer, negative size, m < 1,
+                                        non-finite scale, size overflow                   */
+    ANCHOR_ATTN_ERR_UNSUPPORTED = 2, /* d not in {16,32,64,128}, or m * d > 16384         */
+    ANCHOR_ATTN_ERR_ALIAS = 3,       /* H overlaps Q, U or V                               */
+    ANCHOR_ATTN_ERR_ALLOC = 4,       /* workspace allocation failed                        */
+    ANCHOR_ATTN_ERR_CUDA = 5         /* a CUDA launch or runtime call failed               */
+} anchor_attn_status_t;
+
+/*
+ * bf16 forward: Q, U, V, H are bf16 (uint16 bit patterns of bfloat16); scores, softmax,
+ * Delta and every contraction accumulate in fp32; H is rounded to bf16 (nearest even).
+ * On d in {64, 128} with 32 <= m <= 128 the three n x m x d contractions run on the
+ * tensor cores (tcgen05, bf16 operands, fp32 accumulators in tensor memory); elsewhere on
+ * CUDA-core fp32 FMA.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward(const void *Q, const void *U, const void *V, void *H,
+                                         int B, int heads, int n, int m, int d, float scale,
+                                         void *stream);
+
+/*
+ * fp32 forward: float in, float out, fp32 CUDA-core arithmetic throughout (expf, fixed-order
+ * fp32 sums).  Same layout, shapes and errors as anchor_attn_forward.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, const float *U, const float *V,
+                                             float *H, int B, int heads, int n, int m, int d,
+                                             float scale, void *stream);
+
+/* Static description of what one call with these arguments launches (no GPU access). */
+typedef struct {
+    int variant;              /* ANCHOR_ATTN_VARIANT_*                                  */
+    int kernels_per_call;     /* kernel launches one call makes                        */
+    int splits;               /* token chunks per slice whose partials are reduced     */
+    int reserved;
+    size_t workspace_bytes;   /* device workspace one call allocates (0 if none)       */
+} anchor_attn_plan_t;
+
+enum {
+    ANCHOR_ATTN_VARIANT_EMPTY = 0,        /* nothing to do                                   */
+    ANCHOR_ATTN_VARIANT_SIMT_SLICE = 1,   /* one CTA per slice, CUDA-core FMA                */
+    ANCHOR_ATTN_VARIANT_SIMT_SPLIT = 2,   /* token chunks + fixed-order reduction, FMA       */
+    ANCHOR_ATTN_VARIANT_UMMA = 3          /* tcgen05 tensor-core path                        */
+};
+
+/* dtype: 0 = bf16 (anchor_attn_forward), 1 = fp32 (anchor_attn_forward_f32). */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, int m, int d,
+                                            anchor_attn_plan_t *plan);
+
+/* Human-readable name of a status code (static storage). */
+ANCHOR_ATTN_API const char *anchor_attn_status_string(anchor_attn_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ANCHOR_ATTN_H */

@@ -1,0 +1,155 @@
+"""Anchor-attention forward H = A Delta^{-1} A^T V on GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI in include/anchor_attn.h (libanchor_attn.so, built
+in-tree by ``_build.build()``).  This module only marshals arguments: every step of the
+forward runs in the library's CUDA kernels.  PyTorch supplies device memory and the current
+stream.  There is no CPU fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "LIB_PATH", "load", "forward", "anchor_attn_forward", "anchor_attn_forward_f32",
+    "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "query_plan", "status_string",
+    "AnchorAttnError", "STATUS", "VARIANTS",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libanchor_attn.so")
+
+STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_ALIAS", 4: "ERR_ALLOC", 5: "ERR_CUDA"}
+VARIANTS = {0: "empty", 1: "simt_slice", 2: "simt_split", 3: "umma"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AnchorAttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"anchor_attn: {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("kernels_per_call", ctypes.c_int), ("splits", ctypes.c_int),
+                ("reserved", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"anchor_attn CUDA library not built ({p}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        for name in ("anchor_attn_forward", "anchor_attn_forward_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
+            fn.restype = ctypes.c_int
+        lib.anchor_attn_query_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(_Plan)]
+        lib.anchor_attn_query_plan.restype = ctypes.c_int
+        lib.anchor_attn_status_string.argtypes = [ctypes.c_int]
+        lib.anchor_attn_status_string.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().anchor_attn_status_string(int(status)).decode()
+
+
+def _raise(st: int, what: str) -> None:
+    if st != 0:
+        raise AnchorAttnError(st, f"{what}: {status_string(st)}")
+
+
+def anchor_attn_forward_ptr(Q: int, U: int, V: int, H: int, B: int, heads: int, n: int, m: int, d: int,
+                            scale: float, stream: int = 0) -> int:
+    """Raw C-ABI call (bf16 device pointers as integers); returns the status code."""
+    return load().anchor_attn_forward(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
+
+
+def anchor_attn_forward_f32_ptr(Q: int, U: int, V: int, H: int, B: int, heads: int, n: int, m: int,
+                                d: int, scale: float, stream: int = 0) -> int:
+    """Raw C-ABI call (fp32 device pointers as integers); returns the status code."""
+    return load().anchor_attn_forward_f32(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
+
+
+def query_plan(dtype: str, B: int, heads: int, n: int, m: int, d: int) -> dict:
+    """What one call launches: variant, kernels per call, splits, workspace bytes."""
+    pl = _Plan()
+    st = load().anchor_attn_query_plan(1 if dtype == "f32" else 0, B, heads, n, m, d, ctypes.byref(pl))
+    _raise(st, "query_plan")
+    return {"variant": VARIANTS.get(pl.variant, pl.variant), "kernels_per_call": pl.kernels_per_call,
+            "splits": pl.splits, "workspace_bytes": pl.workspace_bytes}
+
+
+def _check_tensors(Q, U, V, H, dtype):
+    import torch
+    for name, t in (("Q", Q), ("U", U), ("V", V), ("H", H)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if Q.dim() != 4 or U.dim() != 3:
+        raise ValueError("Q, V, H are [B, heads, n, d]; U is [heads, m, d]")
+    if V.shape != Q.shape or H.shape != Q.shape:
+        raise ValueError("V and H must have Q's shape")
+    if U.shape[0] != Q.shape[1] or U.shape[2] != Q.shape[3]:
+        raise ValueError("U must be [heads, m, d] matching Q")
+
+
+def forward(Q, U, V, H=None, scale: float | None = None, stream=None):
+    """H = A Delta^{-1} A^T V for torch CUDA tensors (bf16 or fp32).
+
+    Q, V: [B, heads, n, d]; U: [heads, m, d].  scale defaults to 1/sqrt(d).  Runs on
+    ``stream`` (a torch.cuda.Stream) or the current stream; asynchronous.
+    """
+    import torch
+    if H is None:
+        H = torch.empty_like(Q)
+    _check_tensors(Q, U, V, H, Q.dtype)
+    B, heads, n, d = Q.shape
+    m = U.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    s = stream if stream is not None else torch.cuda.current_stream(Q.device)
+    with torch.cuda.device(Q.device):
+        if Q.dtype == torch.bfloat16:
+            st = anchor_attn_forward_ptr(Q.data_ptr(), U.data_ptr(), V.data_ptr(), H.data_ptr(), B, heads, n, m,
+                                         d, scale, s.cuda_stream)
+        elif Q.dtype == torch.float32:
+            st = anchor_attn_forward_f32_ptr(Q.data_ptr(), U.data_ptr(), V.data_ptr(), H.data_ptr(), B, heads,
+                                             n, m, d, scale, s.cuda_stream)
+        else:
+            raise TypeError("Q must be bfloat16 or float32")
+    _raise(st, "forward")
+    return H
+
+
+def anchor_attn_forward(Q, U, V, H=None, scale=None, stream=None):
+    """bf16 entry point (see ``forward``)."""
+    import torch
+    if Q.dtype != torch.bfloat16:
+        raise TypeError("anchor_attn_forward takes bfloat16 tensors")
+    return forward(Q, U, V, H, scale, stream)
+
+
+def anchor_attn_forward_f32(Q, U, V, H=None, scale=None, stream=None):
+    """fp32 entry point (see ``forward``)."""
+    import torch
+    if Q.dtype != torch.float32:
+        raise TypeError("anchor_attn_forward_f32 takes float32 tensors")
+    return forward(Q, U, V, H, scale, stream)

@@ -1,0 +1,145 @@
+// C ABI of the anchor-attention forward: argument checks, variant choice, workspace, launch.
+// The operation and the argument contract are documented in include/anchor_attn.h.
+#include "anchor_attn.h"
+#include "common.cuh"
+
+#include <math.h>
+#include <stdlib.h>
+
+namespace {
+
+using anchor::Problem;
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// Shape-only checks (shared by the plan query and the forward calls).
+anchor_attn_status_t check_shape(int B, int heads, int n, int m, int d) {
+    if (B < 0 || heads < 0 || n < 0 || m < 1 || d < 1) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (!supported_d(d) || (long long)m * d > 16384) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    const long long slices = (long long)B * heads;
+    // element counts must fit in 63 bits, and the SIMT grids (slices x tiles) in 2^31 - 1
+    if (slices > 0 && n > 0) {
+        if ((long long)n * d > (1LL << 62) / slices) return ANCHOR_ATTN_ERR_INVALID_ARG;
+        const long long tiles = (n + anchor::kSimtTile - 1) / anchor::kSimtTile;
+        if (slices * tiles > 0x7fffffffLL) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    }
+    return ANCHOR_ATTN_OK;
+}
+
+struct Plan {
+    int variant = ANCHOR_ATTN_VARIANT_EMPTY;
+    int kernels = 0;
+    int splits = 0;
+    size_t workspace = 0;
+};
+
+Plan make_plan(const Problem &p) {
+    Plan pl;
+    if (p.slices() == 0 || p.n == 0) return pl;
+    if (p.n <= 512 && anchor::simt_slice_smem_bytes(p.n, p.m, p.d) <= kMaxSmem) {
+        pl.variant = ANCHOR_ATTN_VARIANT_SIMT_SLICE;
+        pl.kernels = 1;
+        pl.splits = 1;
+        return pl;
+    }
+    pl.variant = ANCHOR_ATTN_VARIANT_SIMT_SPLIT;
+    pl.kernels = 3;
+    pl.splits = (p.n + anchor::kSimtChunk - 1) / anchor::kSimtChunk;
+    pl.workspace = anchor::simt_split_workspace_bytes(p, pl.splits);
+    return pl;
+}
+
+anchor_attn_status_t run(const Problem &p, void *stream_v) {
+    anchor_attn_status_t st = check_shape(p.B, p.heads, p.n, p.m, p.d);
+    if (st != ANCHOR_ATTN_OK) return st;
+    if (!isfinite(p.scale)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (p.slices() == 0 || p.n == 0) return ANCHOR_ATTN_OK;
+    if (!p.Q || !p.U || !p.V || !p.H) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (!aligned16(p.Q) || !aligned16(p.U) || !aligned16(p.V) || !aligned16(p.H))
+        return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const size_t es = p.f32 ? 4 : 2;
+    const size_t xbytes = (size_t)p.slices() * p.n * p.d * es;
+    const size_t ubytes = (size_t)p.heads * p.m * p.d * es;
+    if (overlaps(p.H, xbytes, p.Q, xbytes) || overlaps(p.H, xbytes, p.V, xbytes) ||
+        overlaps(p.H, xbytes, p.U, ubytes))
+        return ANCHOR_ATTN_ERR_ALIAS;
+
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    const Plan pl = make_plan(p);
+    cudaError_t e = cudaSuccess;
+    switch (pl.variant) {
+    case ANCHOR_ATTN_VARIANT_SIMT_SLICE:
+        e = anchor::launch_simt_slice(p, stream);
+        break;
+    case ANCHOR_ATTN_VARIANT_SIMT_SPLIT: {
+        void *ws = nullptr;
+        if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
+        if (cudaMallocAsync(&ws, pl.workspace, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return ANCHOR_ATTN_ERR_ALLOC;
+        }
+        e = anchor::launch_simt_split(p, pl.splits, (float *)ws, stream);
+        const cudaError_t ef = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess) e = ef;
+        break;
+    }
+    default:
+        return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? ANCHOR_ATTN_OK : ANCHOR_ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+anchor_attn_status_t anchor_attn_forward(const void *Q, const void *U, const void *V, void *H, int B,
+                                         int heads, int n, int m, int d, float scale, void *stream) {
+    const Problem p{Q, U, V, H, B, heads, n, m, d, scale, false};
+    return run(p, stream);
+}
+
+anchor_attn_status_t anchor_attn_forward_f32(const float *Q, const float *U, const float *V, float *H,
+                                             int B, int heads, int n, int m, int d, float scale,
+                                             void *stream) {
+    const Problem p{Q, U, V, H, B, heads, n, m, d, scale, true};
+    return run(p, stream);
+}
+
+anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, int m, int d,
+                                            anchor_attn_plan_t *plan) {
+    if (!plan || (dtype != 0 && dtype != 1)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const anchor_attn_status_t st = check_shape(B, heads, n, m, d);
+    if (st != ANCHOR_ATTN_OK) return st;
+    const Problem p{nullptr, nullptr, nullptr, nullptr, B, heads, n, m, d, 1.f, dtype == 1};
+    const Plan pl = make_plan(p);
+    plan->variant = pl.variant;
+    plan->kernels_per_call = pl.kernels;
+    plan->splits = pl.splits;
+    plan->reserved = 0;
+    plan->workspace_bytes = pl.workspace;
+    return ANCHOR_ATTN_OK;
+}
+
+const char *anchor_attn_status_string(anchor_attn_status_t s) {
+    switch (s) {
+    case ANCHOR_ATTN_OK: return "ok";
+    case ANCHOR_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ANCHOR_ATTN_ERR_UNSUPPORTED: return "unsupported shape";
+    case ANCHOR_ATTN_ERR_ALIAS: return "output overlaps an input";
+    case ANCHOR_ATTN_ERR_ALLOC: return "workspace allocation failed";
+    case ANCHOR_ATTN_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

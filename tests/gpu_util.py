@@ -1,0 +1,46 @@
+"""Helpers shared by the GPU tests: move generator output to the device, run the oracle on
+the same (dtype-rounded) inputs, and apply the parity bar.
+
+Parity bar (the forward's stated tolerances):
+  fp32 : max relative error 1e-5, read elementwise as |g - o| <= 1e-5 * max(|o|, rms(o)):
+         an output far below the slice's typical magnitude is a cancellation whose rounding
+         error scales with its summands (~rms), not with itself.
+  bf16 : |g - o| <= 1e-2 + 2e-2 |o| elementwise (2e-2 relative / 1e-2 absolute).
+"""
+import numpy as np
+
+import gen
+
+
+def to_device(x: np.ndarray, dtype: str, torch, device="cuda"):
+    if dtype == "f32":
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint16).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def to_host64(t) -> np.ndarray:
+    return t.detach().double().cpu().numpy()
+
+
+def bound(ref: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f32":
+        rms = float(np.sqrt((ref ** 2).mean())) if ref.size else 0.0
+        return 1e-5 * np.maximum(np.abs(ref), max(rms, 1e-30))
+    return 1e-2 + 2e-2 * np.abs(ref)
+
+
+def assert_parity(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "") -> float:
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    b = bound(ref, dtype)
+    bad = err > b
+    if bad.any():
+        idx = np.unravel_index(np.argmax(err - b), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {err.size} outside the {dtype} bar; worst at {idx}: "
+                             f"got {got[idx]!r} oracle {ref[idx]!r} (bound {b[idx]:.3e})")
+    return float(err.max()) if err.size else 0.0
+
+
+def widen(x: dict, dtype: str) -> dict:
+    return {k: gen.to_float64(v, dtype) for k, v in x.items()}

@@ -1,0 +1,96 @@
+"""The C ABI library without a GPU: it loads, exports what include/anchor_attn.h declares,
+and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    from linear_complexity_anchor_gb300 import _build
+    _build.build()
+    import linear_complexity_anchor_gb300 as p
+    p.load()
+    return p
+
+
+def _declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^ANCHOR_ATTN_API[^;(]*?\b(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_exports_every_declared_symbol(pkg):
+    names = _declared_symbols()
+    assert "anchor_attn_forward" in names and "anchor_attn_forward_f32" in names
+    lib = ctypes.CDLL(pkg.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+A = 1 << 20  # a 16-byte aligned fake address; never dereferenced by the rejected calls
+
+
+def _call(pkg, f32=False, Q=A, U=2 * A, V=3 * A, H=4 * A, B=1, heads=1, n=8, m=4, d=16, scale=0.25):
+    f = pkg.anchor_attn_forward_f32_ptr if f32 else pkg.anchor_attn_forward_ptr
+    return f(Q, U, V, H, B, heads, n, m, d, scale, 0)
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_argument_validation(pkg, f32):
+    c = lambda **kw: _call(pkg, f32=f32, **kw)
+    INVALID, UNSUP, ALIAS = 1, 2, 3
+    assert c(Q=0) == INVALID
+    assert c(H=0) == INVALID
+    assert c(V=3 * A + 4) == INVALID                       # misaligned
+    assert c(B=-1) == INVALID
+    assert c(n=-5) == INVALID
+    assert c(m=0) == INVALID
+    assert c(scale=float("nan")) == INVALID
+    assert c(scale=float("inf")) == INVALID
+    assert c(d=48) == UNSUP
+    assert c(d=128, m=129) == UNSUP                        # m * d > 16384
+    assert c(d=64, m=257) == UNSUP
+    assert c(H=A + 64) == ALIAS                            # H inside Q
+    assert c(H=3 * A - 16) == ALIAS                        # H runs into V
+    assert c(U=4 * A + 32, B=2) == ALIAS                   # U inside H
+    # empty problems are valid no-ops and accept NULL pointers
+    assert c(B=0, Q=0, U=0, V=0, H=0) == 0
+    assert c(n=0, Q=0, U=0, V=0, H=0) == 0
+    assert c(heads=0, Q=0, U=0, V=0, H=0) == 0
+
+
+def test_status_strings(pkg):
+    for code in range(6):
+        assert pkg.status_string(code)
+    assert pkg.status_string(99) == "unknown status"
+
+
+def test_plans(pkg):
+    p = pkg.query_plan("f32", 1, 1, 196, 16, 64)
+    assert p["variant"] == "simt_slice" and p["kernels_per_call"] == 1 and p["workspace_bytes"] == 0
+    p = pkg.query_plan("bf16", 1, 2, 1100, 20, 64)
+    assert p["variant"] == "simt_split" and p["splits"] == 3 and p["workspace_bytes"] > 0
+    assert pkg.query_plan("bf16", 0, 2, 100, 20, 64)["variant"] == "empty"
+    with pytest.raises(pkg.AnchorAttnError):
+        pkg.query_plan("bf16", 1, 1, 10, 4, 48)
+
+
+def test_alloc_failure_is_reported(pkg, monkeypatch):
+    """Host-side fault injection: the workspace allocation reports failure."""
+    monkeypatch.setenv("ANCHOR_ATTN_TEST_FAIL_ALLOC", "1")
+    assert pkg.query_plan("bf16", 1, 1, 2000, 20, 64)["workspace_bytes"] > 0
+    assert _call(pkg, n=2000, m=20, d=64) == 4
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import linear_complexity_anchor_gb300 as p
+    with pytest.raises(RuntimeError, match="not built"):
+        p.load(str(tmp_path / "nope.so"))

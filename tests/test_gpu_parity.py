@@ -1,0 +1,194 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element,
+on the same seeded inputs."""
+import math
+
+import numpy as np
+import pytest
+
+import gen
+from tests.conftest import gpu_available
+from tests.gpu_util import assert_parity, to_device, to_host64, widen
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not gpu_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module")
+def env(oracle_mod):
+    import torch
+    import linear_complexity_anchor_gb300 as pkg
+    pkg.load()
+    return pkg, torch, oracle_mod
+
+
+def _run(env, w: gen.Workload, x: dict, scale=None, stream=None):
+    pkg, torch, _ = env
+    t = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    H = pkg.forward(t["Q"], t["U"], t["V"], scale=w.scale if scale is None else scale, stream=stream)
+    torch.cuda.synchronize()
+    return H
+
+
+def _check_full(env, w, seed=0, x=None, scale=None):
+    pkg, torch, orc = env
+    x = gen.make_inputs(w, seed=seed) if x is None else x
+    H = _run(env, w, x, scale)
+    xx = widen(x, w.dtype)
+    ref = orc.forward(xx["Q"], xx["U"], xx["V"], w.scale if scale is None else scale)
+    return assert_parity(to_host64(H), ref, w.dtype, f"{w.name} {w.B}x{w.heads}x{w.n} m={w.m} d={w.d}")
+
+
+# ------------------------------------------------------------------ the five workloads
+
+@pytest.mark.parametrize("name", ["vit14_f32", "deit_small"])
+def test_workload_full(env, name):
+    _check_full(env, gen.WORKLOADS[name])
+
+
+@pytest.mark.parametrize("name,nslices", [("deit_base", 24), ("det_800x1344", 6), ("long_16k", 3)])
+def test_workload_sampled_slices(env, name, nslices):
+    """Full-size launch (the bench's configuration); the oracle checks a spread of whole
+    slices, and a size-independent property checks every slice: each column of H sums to
+    the same column of V (S_t is doubly stochastic)."""
+    pkg, torch, orc = env
+    w = gen.WORKLOADS[name]
+    x = gen.make_inputs(w, seed=0)
+    H = _run(env, w, x)
+    U = gen.to_float64(x["U"], w.dtype)
+    rng = np.random.default_rng(123)
+    picks = sorted({0, w.slices - 1, *rng.choice(w.slices, nslices - 2, replace=False).tolist()})
+    for s in picks:
+        b, h = divmod(s, w.heads)
+        Qs = gen.to_float64(x["Q"][b, h], w.dtype)
+        Vs = gen.to_float64(x["V"][b, h], w.dtype)
+        ref = orc.slice_forward(Qs, U[h], Vs, w.scale)["H"]
+        assert_parity(to_host64(H[b, h]), ref, w.dtype, f"{name} slice ({b},{h})")
+    Hs = H.double().sum(dim=2)
+    Vt = to_device(x["V"], w.dtype, torch).double()
+    tol = 1e-3 * Vt.abs().sum(dim=2) + 1e-2
+    assert ((Hs - Vt.sum(dim=2)).abs() <= tol).all(), "column sums of H differ from those of V"
+
+
+# ------------------------------------------------------------------ edge shapes
+
+_MD = [(1, 16), (2, 64), (15, 32), (16, 64), (30, 64), (31, 16), (32, 64), (33, 64), (49, 64), (64, 64),
+       (64, 128), (100, 128), (128, 64), (128, 128), (256, 64), (200, 32)]
+_N = [1, 2, 7, 8, 127, 128, 129, 197, 513, 1100]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("m,d", _MD)
+def test_edge_shapes(env, dtype, m, d):
+    for i, n in enumerate(_N):
+        B, heads = (2, 3) if n <= 129 else (1, 2)
+        w = gen.WORKLOADS["vit14_f32"].with_(name="edge", B=B, heads=heads, n=n, m=m, d=d, dtype=dtype)
+        _check_full(env, w, seed=1000 + 17 * i + m + d)
+
+
+# ------------------------------------------------------------------ degenerate cases
+
+def _small(dtype, **kw):
+    base = dict(name="degenerate", B=2, heads=2, n=300, m=40, d=64, dtype=dtype)
+    base.update(kw)
+    return gen.WORKLOADS["vit14_f32"].with_(**base)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("m,n", [(40, 300), (20, 2000), (64, 700)])
+def test_constant_value_is_fixed(env, dtype, m, n):
+    """S_t 1 = 1: a V with constant columns comes back unchanged."""
+    w = _small(dtype, m=m, n=n)
+    x = gen.make_inputs(w, seed=5)
+    col = x["V"][:, :, :1, :]
+    x["V"] = np.ascontiguousarray(np.broadcast_to(col, x["V"].shape))
+    H = _run(env, w, x)
+    assert_parity(to_host64(H), gen.to_float64(x["V"], dtype), dtype, "constant V")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", ["m1", "zero_q", "zero_scale", "identical_anchors"])
+def test_degenerate_means(env, dtype, case):
+    """One anchor, Q = 0, scale = 0 or identical anchors: every H row is the mean of V."""
+    w = _small(dtype, m=1 if case == "m1" else 40)
+    x = gen.make_inputs(w, seed=6)
+    if case == "zero_q":
+        x["Q"] = np.zeros_like(x["Q"])
+    if case == "identical_anchors":
+        x["U"] = np.ascontiguousarray(np.broadcast_to(x["U"][:, :1, :], x["U"].shape))
+    H = _run(env, w, x, scale=0.0 if case == "zero_scale" else None)
+    V = gen.to_float64(x["V"], dtype)
+    ref = np.broadcast_to(V.mean(axis=2, keepdims=True), V.shape)
+    assert_parity(to_host64(H), ref, dtype, case)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_unreached_anchor_drops_out(env, dtype):
+    """An anchor whose scores underflow for every token (Delta_j = 0) contributes nothing."""
+    w = _small(dtype, m=33)
+    x = gen.make_inputs(w, seed=7)
+    Q = gen.to_float64(x["Q"], dtype)
+    U = gen.to_float64(x["U"], dtype)
+    # anchor 5 of every head: score = -2000 * q_0 * scale <= -250 while the others stay
+    # within a few units, so its A column underflows to exactly 0 in fp32
+    U[:, 5, :] = 0.0
+    U[:, 5, 0] = -2000.0
+    x["Q"] = np.where(np.arange(w.d) == 0, np.abs(Q) + 1.0, Q)
+    x["Q"] = x["Q"].astype(np.float32) if dtype == "f32" else gen.round_bf16(x["Q"])
+    x["U"] = U.astype(np.float32) if dtype == "f32" else gen.round_bf16(U)
+    _check_full(env, w, x=x)
+
+
+# ------------------------------------------------------------------ run-time properties
+
+@pytest.mark.parametrize("shape", [(1, 1, 196, 16, 64, "f32"), (2, 3, 2000, 20, 64, "bf16"),
+                                   (4, 6, 197, 30, 64, "bf16"), (2, 4, 700, 64, 64, "bf16"),
+                                   (1, 4, 1500, 128, 128, "bf16")])
+def test_bit_stable(env, shape):
+    pkg, torch, _ = env
+    B, heads, n, m, d, dtype = shape
+    w = _small(dtype, B=B, heads=heads, n=n, m=m, d=d)
+    x = gen.make_inputs(w, seed=8)
+    H1 = _run(env, w, x)
+    H2 = _run(env, w, x)
+    assert torch.equal(H1.view(torch.int16) if dtype == "bf16" else H1.view(torch.int32),
+                       H2.view(torch.int16) if dtype == "bf16" else H2.view(torch.int32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("n,m,d", [(197, 30, 64), (1100, 20, 64), (700, 64, 64), (333, 128, 128)])
+def test_guard_bands_untouched(env, dtype, n, m, d):
+    """Sentinels before and after H stay intact (no write outside the output)."""
+    pkg, torch, orc = env
+    w = _small(dtype, B=2, heads=2, n=n, m=m, d=d)
+    x = gen.make_inputs(w, seed=9)
+    t = {k: to_device(x[k], dtype, torch) for k in "QUV"}
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    pad = 4096
+    buf = torch.full((pad + t["Q"].numel() + pad,), -4096.0, dtype=tdt, device="cuda")
+    H = buf[pad:pad + t["Q"].numel()].view(t["Q"].shape)
+    pkg.forward(t["Q"], t["U"], t["V"], H=H, scale=w.scale)
+    torch.cuda.synchronize()
+    assert (buf[:pad] == -4096.0).all() and (buf[-pad:] == -4096.0).all()
+    xx = widen(x, dtype)
+    assert_parity(to_host64(H), orc.forward(xx["Q"], xx["U"], xx["V"], w.scale), dtype, "guarded")
+
+
+def test_empty_problems_are_noops(env):
+    pkg, torch, _ = env
+    for shape in [(0, 2, 10, 4, 64), (2, 0, 10, 4, 64), (2, 2, 0, 4, 64)]:
+        B, heads, n, m, d = shape
+        Q = torch.zeros((B, heads, n, d), dtype=torch.bfloat16, device="cuda")
+        U = torch.zeros((heads, m, d), dtype=torch.bfloat16, device="cuda")
+        H = pkg.forward(Q, U, Q.clone())
+        assert H.shape == Q.shape
+
+
+def test_runs_on_the_given_stream(env):
+    pkg, torch, orc = env
+    w = _small("bf16", n=900, m=48)
+    x = gen.make_inputs(w, seed=10)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        H = _run(env, w, x, stream=s)
+    s.synchronize()
+    xx = widen(x, "bf16")
+    assert_parity(to_host64(H), orc.forward(xx["Q"], xx["U"], xx["V"], w.scale), "bf16", "side stream")
