@@ -61,6 +61,17 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, device, world: int):
+    """Element-wise max of per-rank floats (the timed region's length is the slowest rank's)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -258,10 +269,7 @@ def run_ours(args) -> None:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
     call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    if world > 1:
-        t = torch.tensor([elapsed_ms, call_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, call_ms = t.tolist()
+    elapsed_ms, call_ms = max_over_ranks([elapsed_ms, call_ms], dev, world)
 
     units = world * w.slices * w.n * K
     value = units / (elapsed_ms / 1e3)
@@ -285,10 +293,7 @@ def run_ours(args) -> None:
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev, world)
     e2e_value = world * w.slices * w.n * E / (e2e_ms / 1e3)
     elem = 4 if w.dtype == "f32" else 2
     h2d = (hQ.numel() + hU.numel() + hV.numel()) * elem

@@ -98,6 +98,16 @@ enum {
 ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, int m, int d,
                                             anchor_attn_plan_t *plan);
 
+/*
+ * Failure detection for the tensor-core variant.  Its kernel never waits without a bound:
+ * a wait on the tensor-memory pipeline or on another CTA's reduction gives up after 2 s,
+ * sets a bit in a device-wide error word and lets the CTA leave, so the context stays
+ * usable.  This call synchronises the device, copies that word to *code and clears it
+ * (bit 0: a pipeline wait timed out, bit 1: a wait for a slice's reduction timed out;
+ * 0: no failure since the last read).  Returns ANCHOR_ATTN_ERR_CUDA if the copy fails.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_device_error(unsigned *code);
+
 /* Human-readable name of a status code (static storage). */
 ANCHOR_ATTN_API const char *anchor_attn_status_string(anchor_attn_status_t status);
 

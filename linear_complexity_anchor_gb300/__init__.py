@@ -14,7 +14,7 @@ import threading
 
 __all__ = [
     "LIB_PATH", "load", "forward", "anchor_attn_forward", "anchor_attn_forward_f32",
-    "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "query_plan", "status_string",
+    "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "device_error", "query_plan", "status_string",
     "AnchorAttnError", "STATUS", "VARIANTS",
 ]
 
@@ -55,6 +55,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         lib.anchor_attn_query_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(_Plan)]
         lib.anchor_attn_query_plan.restype = ctypes.c_int
+        lib.anchor_attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.anchor_attn_device_error.restype = ctypes.c_int
         lib.anchor_attn_status_string.argtypes = [ctypes.c_int]
         lib.anchor_attn_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -81,6 +83,13 @@ def anchor_attn_forward_f32_ptr(Q: int, U: int, V: int, H: int, B: int, heads: i
                                 d: int, scale: float, stream: int = 0) -> int:
     """Raw C-ABI call (fp32 device pointers as integers); returns the status code."""
     return load().anchor_attn_forward_f32(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
+
+
+def device_error() -> int:
+    """Synchronise and return (and clear) the tensor-core kernel's device error word."""
+    code = ctypes.c_uint(0)
+    _raise(load().anchor_attn_device_error(ctypes.byref(code)), "device_error")
+    return int(code.value)
 
 
 def query_plan(dtype: str, B: int, heads: int, n: int, m: int, d: int) -> dict:

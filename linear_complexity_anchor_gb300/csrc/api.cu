@@ -6,12 +6,9 @@
 #include <math.h>
 #include <stdlib.h>
 
+namespace anchor {
+
 namespace {
-
-using anchor::Problem;
-
-constexpr size_t kMaxSmem = 227 * 1024;
-
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
@@ -20,8 +17,8 @@ bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
 }
 
 bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+}  // namespace
 
-// Shape-only checks (shared by the plan query and the forward calls).
 anchor_attn_status_t check_shape(int B, int heads, int n, int m, int d) {
     if (B < 0 || heads < 0 || n < 0 || m < 1 || d < 1) return ANCHOR_ATTN_ERR_INVALID_ARG;
     if (!supported_d(d) || (long long)m * d > 16384) return ANCHOR_ATTN_ERR_UNSUPPORTED;
@@ -35,6 +32,32 @@ anchor_attn_status_t check_shape(int B, int heads, int n, int m, int d) {
     return ANCHOR_ATTN_OK;
 }
 
+anchor_attn_status_t check_problem(const Problem &p) {
+    anchor_attn_status_t st = check_shape(p.B, p.heads, p.n, p.m, p.d);
+    if (st != ANCHOR_ATTN_OK) return st;
+    if (!isfinite(p.scale)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (p.slices() == 0 || p.n == 0) return ANCHOR_ATTN_OK;
+    if (!p.Q || !p.U || !p.V || !p.H) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (!aligned16(p.Q) || !aligned16(p.U) || !aligned16(p.V) || !aligned16(p.H))
+        return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const size_t es = p.f32 ? 4 : 2;
+    const size_t xbytes = (size_t)p.slices() * p.n * p.d * es;
+    const size_t ubytes = (size_t)p.heads * p.m * p.d * es;
+    if (overlaps(p.H, xbytes, p.Q, xbytes) || overlaps(p.H, xbytes, p.V, xbytes) ||
+        overlaps(p.H, xbytes, p.U, ubytes))
+        return ANCHOR_ATTN_ERR_ALIAS;
+    return ANCHOR_ATTN_OK;
+}
+
+}  // namespace anchor
+
+namespace {
+
+using anchor::Problem;
+using anchor::check_shape;
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
 struct Plan {
     int variant = ANCHOR_ATTN_VARIANT_EMPTY;
     int kernels = 0;
@@ -45,6 +68,14 @@ struct Plan {
 Plan make_plan(const Problem &p) {
     Plan pl;
     if (p.slices() == 0 || p.n == 0) return pl;
+    if (anchor::umma_supported(p)) {
+        const anchor::UmmaPlan u = anchor::umma_plan(p);
+        pl.variant = ANCHOR_ATTN_VARIANT_UMMA;
+        pl.kernels = 1;
+        pl.splits = u.C1;
+        pl.workspace = u.workspace_bytes;
+        return pl;
+    }
     if (p.n <= 512 && anchor::simt_slice_smem_bytes(p.n, p.m, p.d) <= kMaxSmem) {
         pl.variant = ANCHOR_ATTN_VARIANT_SIMT_SLICE;
         pl.kernels = 1;
@@ -59,19 +90,9 @@ Plan make_plan(const Problem &p) {
 }
 
 anchor_attn_status_t run(const Problem &p, void *stream_v) {
-    anchor_attn_status_t st = check_shape(p.B, p.heads, p.n, p.m, p.d);
+    const anchor_attn_status_t st = anchor::check_problem(p);
     if (st != ANCHOR_ATTN_OK) return st;
-    if (!isfinite(p.scale)) return ANCHOR_ATTN_ERR_INVALID_ARG;
     if (p.slices() == 0 || p.n == 0) return ANCHOR_ATTN_OK;
-    if (!p.Q || !p.U || !p.V || !p.H) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    if (!aligned16(p.Q) || !aligned16(p.U) || !aligned16(p.V) || !aligned16(p.H))
-        return ANCHOR_ATTN_ERR_INVALID_ARG;
-    const size_t es = p.f32 ? 4 : 2;
-    const size_t xbytes = (size_t)p.slices() * p.n * p.d * es;
-    const size_t ubytes = (size_t)p.heads * p.m * p.d * es;
-    if (overlaps(p.H, xbytes, p.Q, xbytes) || overlaps(p.H, xbytes, p.V, xbytes) ||
-        overlaps(p.H, xbytes, p.U, ubytes))
-        return ANCHOR_ATTN_ERR_ALIAS;
 
     cudaStream_t stream = (cudaStream_t)stream_v;
     const Plan pl = make_plan(p);
@@ -88,6 +109,19 @@ anchor_attn_status_t run(const Problem &p, void *stream_v) {
             return ANCHOR_ATTN_ERR_ALLOC;
         }
         e = anchor::launch_simt_split(p, pl.splits, (float *)ws, stream);
+        const cudaError_t ef = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess) e = ef;
+        break;
+    }
+    case ANCHOR_ATTN_VARIANT_UMMA: {
+        const anchor::UmmaPlan u = anchor::umma_plan(p);
+        void *ws = nullptr;
+        if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
+        if (cudaMallocAsync(&ws, u.workspace_bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return ANCHOR_ATTN_ERR_ALLOC;
+        }
+        e = anchor::launch_umma(p, u, ws, stream);
         const cudaError_t ef = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = ef;
         break;
@@ -128,6 +162,11 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
     plan->reserved = 0;
     plan->workspace_bytes = pl.workspace;
     return ANCHOR_ATTN_OK;
+}
+
+anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
+    if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    return anchor::umma_read_and_clear_error(code) == cudaSuccess ? ANCHOR_ATTN_OK : ANCHOR_ATTN_ERR_CUDA;
 }
 
 const char *anchor_attn_status_string(anchor_attn_status_t s) {

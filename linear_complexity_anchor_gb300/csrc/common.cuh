@@ -6,6 +6,10 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <algorithm>
+
+#include "anchor_attn.h"
+
 namespace anchor {
 
 // One forward problem as the C ABI received it (device pointers, validated).
@@ -19,6 +23,10 @@ struct Problem {
     bool f32;  // element type of Q, U, V, H: float (true) or bf16 (false)
     long long slices() const { return (long long)B * heads; }
 };
+
+// Argument checks of the C ABI (see include/anchor_attn.h); no device access.
+anchor_attn_status_t check_shape(int B, int heads, int n, int m, int d);
+anchor_attn_status_t check_problem(const Problem &p);
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -52,5 +60,22 @@ constexpr int kSimtChunk = 512;      // tokens per split (chunk) in the split va
 size_t simt_split_smem_bytes(int m, int d);
 size_t simt_split_workspace_bytes(const Problem &p, int splits);
 cudaError_t launch_simt_split(const Problem &p, int splits, float *workspace, cudaStream_t stream);
+
+// --- tensor-core (tcgen05) variant ---------------------------------------------------
+constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA
+constexpr int kUmmaP1Tiles = 8;      // target tiles per pass-1 chunk
+constexpr int kUmmaP2Tiles = 4;      // target tiles per pass-2 chunk
+struct UmmaPlan {
+    int MP = 0;              // anchors padded to 64 or 128
+    int NT = 0;              // 128-token tiles per slice
+    int C1 = 0, C2 = 0;      // chunks per slice in pass 1 / pass 2 (C1 == 1: whole slice per CTA)
+    int total_items = 0;
+    size_t header_bytes = 0; // zeroed part of the workspace (ticket, counters, flags)
+    size_t workspace_bytes = 0;
+};
+bool umma_supported(const Problem &p);
+UmmaPlan umma_plan(const Problem &p);
+cudaError_t launch_umma(const Problem &p, const UmmaPlan &plan, void *workspace, cudaStream_t stream);
+cudaError_t umma_read_and_clear_error(unsigned *out);
 
 }  // namespace anchor

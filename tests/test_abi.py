@@ -69,7 +69,7 @@ def test_argument_validation(pkg, f32):
 
 def test_status_strings(pkg):
     for code in range(6):
-        assert pkg.status_string(code)
+        assert pkg.status_string(code) != "unknown status"
     assert pkg.status_string(99) == "unknown status"
 
 
@@ -79,6 +79,14 @@ def test_plans(pkg):
     p = pkg.query_plan("bf16", 1, 2, 1100, 20, 64)
     assert p["variant"] == "simt_split" and p["splits"] == 3 and p["workspace_bytes"] > 0
     assert pkg.query_plan("bf16", 0, 2, 100, 20, 64)["variant"] == "empty"
+    # tensor-core variant: d in {64, 128}, 32 <= m <= 128, bf16 only
+    p = pkg.query_plan("bf16", 8, 12, 4200, 64, 64)
+    assert p["variant"] == "umma" and p["kernels_per_call"] == 1 and p["splits"] == 5
+    p = pkg.query_plan("bf16", 256, 12, 197, 49, 64)
+    assert p["variant"] == "umma" and p["splits"] == 1 and p["workspace_bytes"] == 256
+    assert pkg.query_plan("f32", 8, 12, 4200, 64, 64)["variant"] == "simt_split"
+    assert pkg.query_plan("bf16", 1, 1, 4200, 31, 64)["variant"] == "simt_split"
+    assert pkg.query_plan("bf16", 1, 1, 4200, 64, 32)["variant"] == "simt_split"
     with pytest.raises(pkg.AnchorAttnError):
         pkg.query_plan("bf16", 1, 1, 10, 4, 48)
 
@@ -87,7 +95,8 @@ def test_alloc_failure_is_reported(pkg, monkeypatch):
     """Host-side fault injection: the workspace allocation reports failure."""
     monkeypatch.setenv("ANCHOR_ATTN_TEST_FAIL_ALLOC", "1")
     assert pkg.query_plan("bf16", 1, 1, 2000, 20, 64)["workspace_bytes"] > 0
-    assert _call(pkg, n=2000, m=20, d=64) == 4
+    assert _call(pkg, n=2000, m=20, d=64) == 4     # CUDA-core split variant
+    assert _call(pkg, n=2000, m=64, d=64) == 4     # tensor-core variant
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -39,6 +39,17 @@ def _check_full(env, w, seed=0, x=None, scale=None):
 
 # ------------------------------------------------------------------ the five workloads
 
+EXPECTED_VARIANT = {"vit14_f32": "simt_slice", "deit_small": "simt_slice", "deit_base": "umma",
+                    "det_800x1344": "umma", "long_16k": "umma"}
+
+
+@pytest.mark.parametrize("name", sorted(EXPECTED_VARIANT))
+def test_workload_variant(env, name):
+    pkg, _, _ = env
+    w = gen.WORKLOADS[name]
+    assert pkg.query_plan(w.dtype, w.B, w.heads, w.n, w.m, w.d)["variant"] == EXPECTED_VARIANT[name]
+
+
 @pytest.mark.parametrize("name", ["vit14_f32", "deit_small"])
 def test_workload_full(env, name):
     _check_full(env, gen.WORKLOADS[name])
@@ -66,6 +77,7 @@ def test_workload_sampled_slices(env, name, nslices):
     Vt = to_device(x["V"], w.dtype, torch).double()
     tol = 1e-3 * Vt.abs().sum(dim=2) + 1e-2
     assert ((Hs - Vt.sum(dim=2)).abs() <= tol).all(), "column sums of H differ from those of V"
+    assert pkg.device_error() == 0
 
 
 # ------------------------------------------------------------------ edge shapes
@@ -170,6 +182,11 @@ def test_guard_bands_untouched(env, dtype, n, m, d):
     assert (buf[:pad] == -4096.0).all() and (buf[-pad:] == -4096.0).all()
     xx = widen(x, dtype)
     assert_parity(to_host64(H), orc.forward(xx["Q"], xx["U"], xx["V"], w.scale), dtype, "guarded")
+
+
+def test_no_device_error_after_runs(env):
+    pkg, _, _ = env
+    assert pkg.device_error() == 0
 
 
 def test_empty_problems_are_noops(env):
