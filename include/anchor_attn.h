@@ -56,7 +56,9 @@ typedef enum {
     ANCHOR_ATTN_ERR_UNSUPPORTED = 2, /* d not in {16,32,64,128}, or m * d > 16384         */
     ANCHOR_ATTN_ERR_ALIAS = 3,       /* H overlaps Q, U or V                               */
     ANCHOR_ATTN_ERR_ALLOC = 4,       /* workspace allocation failed                        */
-    ANCHOR_ATTN_ERR_CUDA = 5         /* a CUDA launch or runtime call failed               */
+    ANCHOR_ATTN_ERR_CUDA = 5,        /* a CUDA launch or runtime call failed               */
+    ANCHOR_ATTN_ERR_SCRATCH_LIMIT = 6 /* the problem needs more scratch than the fixed
+                                         array of anchor_attn_forward_static_scratch holds */
 } anchor_attn_status_t;
 
 /*
@@ -77,6 +79,34 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward(const void *Q, const vo
 ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, const float *U, const float *V,
                                              float *H, int B, int heads, int n, int m, int d,
                                              float scale, void *stream);
+
+/*
+ * Allocation-free variant of anchor_attn_forward (bf16 in and out, same layout, shapes and
+ * errors).  The paper has no counterpart to this call: it exists for callers that may not
+ * allocate device memory while they run - e.g. a plugin's enqueue step inside an inference
+ * engine that owns all device memory, or a loop with a fixed memory budget - and so cannot
+ * use anchor_attn_forward, which takes a workspace with cudaMallocAsync on every call.
+ *
+ * It always runs the token-chunk CUDA-core variant (fp32 FMA, fixed-order reduction), whose
+ * partial sums live in a fixed array compiled into the library:
+ *   - limit: anchor_attn_static_scratch_bytes() (16 MiB); a problem needing more returns
+ *     ANCHOR_ATTN_ERR_SCRATCH_LIMIT before anything is launched.  It needs
+ *     4 * B * heads * (ceil(n / 512) * (m * d + m) + m * d) bytes.
+ *   - the array exists on every GPU that loads the library, until the process exits;
+ *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture;
+ *   - every call shares the array and it keeps the last call's contents (nothing needs to
+ *     start at zero); calls whose kernels overlap on the GPU (other streams or host threads)
+ *     race on it and must be serialised by the caller.
+ * Calls no cudaMalloc, cudaMallocAsync, cudaFree or allocating library routine.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_static_scratch(const void *Q, const void *U,
+                                                                        const void *V, void *H, int B,
+                                                                        int heads, int n, int m, int d,
+                                                                        float scale, void *stream);
+
+/* Size in bytes of the fixed scratch array behind anchor_attn_forward_static_scratch. */
+ANCHOR_ATTN_API size_t anchor_attn_static_scratch_bytes(void);
 
 /* Static description of what one call with these arguments launches (no GPU access). */
 typedef struct {

@@ -14,13 +14,15 @@ import threading
 
 __all__ = [
     "LIB_PATH", "load", "forward", "anchor_attn_forward", "anchor_attn_forward_f32",
-    "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "device_error", "query_plan", "status_string",
+    "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "anchor_attn_forward_static_scratch_ptr",
+    "static_scratch_bytes", "device_error", "query_plan", "status_string",
     "AnchorAttnError", "STATUS", "VARIANTS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libanchor_attn.so")
 
-STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_ALIAS", 4: "ERR_ALLOC", 5: "ERR_CUDA"}
+STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_ALIAS", 4: "ERR_ALLOC", 5: "ERR_CUDA",
+          6: "ERR_SCRATCH_LIMIT"}
 VARIANTS = {0: "empty", 1: "simt_slice", 2: "simt_split", 3: "umma"}
 
 _lock = threading.Lock()
@@ -49,12 +51,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
             raise RuntimeError(f"anchor_attn CUDA library not built ({p}); run __graft_entry__.build()")
         lib = ctypes.CDLL(p)
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        for name in ("anchor_attn_forward", "anchor_attn_forward_f32"):
+        for name in ("anchor_attn_forward", "anchor_attn_forward_f32", "anchor_attn_forward_static_scratch"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
             fn.restype = ctypes.c_int
         lib.anchor_attn_query_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(_Plan)]
         lib.anchor_attn_query_plan.restype = ctypes.c_int
+        lib.anchor_attn_static_scratch_bytes.argtypes = []
+        lib.anchor_attn_static_scratch_bytes.restype = ctypes.c_size_t
         lib.anchor_attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.anchor_attn_device_error.restype = ctypes.c_int
         lib.anchor_attn_status_string.argtypes = [ctypes.c_int]
@@ -83,6 +87,16 @@ def anchor_attn_forward_f32_ptr(Q: int, U: int, V: int, H: int, B: int, heads: i
                                 d: int, scale: float, stream: int = 0) -> int:
     """Raw C-ABI call (fp32 device pointers as integers); returns the status code."""
     return load().anchor_attn_forward_f32(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
+
+
+def anchor_attn_forward_static_scratch_ptr(Q: int, U: int, V: int, H: int, B: int, heads: int, n: int,
+                                           m: int, d: int, scale: float, stream: int = 0) -> int:
+    """Raw C-ABI call of the allocation-free variant (bf16 device pointers); returns the status."""
+    return load().anchor_attn_forward_static_scratch(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
+
+
+def static_scratch_bytes() -> int:
+    return int(load().anchor_attn_static_scratch_bytes())
 
 
 def device_error() -> int:

@@ -177,6 +177,7 @@ const char *anchor_attn_status_string(anchor_attn_status_t s) {
     case ANCHOR_ATTN_ERR_ALIAS: return "output overlaps an input";
     case ANCHOR_ATTN_ERR_ALLOC: return "workspace allocation failed";
     case ANCHOR_ATTN_ERR_CUDA: return "CUDA error";
+    case ANCHOR_ATTN_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch array";
     }
     return "unknown status";
 }

@@ -68,7 +68,7 @@ def test_argument_validation(pkg, f32):
 
 
 def test_status_strings(pkg):
-    for code in range(6):
+    for code in range(7):
         assert pkg.status_string(code) != "unknown status"
     assert pkg.status_string(99) == "unknown status"
 
