@@ -63,17 +63,22 @@ struct Layout {
     static constexpr int kUB = MP * D * 2;
     static constexpr int kAB = kT * 128 * 2;           // A tile, 128 anchor columns
     static constexpr int kOnesB = 16 * kT * 2;         // 16 x 128 ones (bf16)
+    static constexpr int kNS = 2;                      // TMA stages (each: a Q and a V tile)
     static constexpr int offU = 0;
-    static constexpr int offQ = offU + kUB;            // 2 stages
-    static constexpr int offV = offQ + 2 * kQB;        // 2 stages; W' image in pass 2
-    static constexpr int offA = offV + 2 * kQB;
+    static constexpr int offQ = offU + kUB;            // kNS Q tiles
+    static constexpr int offV = offQ + kNS * kQB;      // kNS V tiles; in pass 2: W' image, H staging
+    static constexpr int offA = offV + kNS * kQB;
     static constexpr int offOnes = offA + kAB;
     static constexpr int offBar = offOnes + kOnesB;
     static constexpr int kBytes = offBar + 256;
     static constexpr int kSmem = kBytes + 1024;        // slack for 1024-byte alignment
-    static constexpr int colS = 0, colW = MP, colD = MP + D;
-    static constexpr int kTmemCols = (MP + D + 16) <= 256 ? 256 : 512;
-    static_assert(D * MP * 2 <= 2 * kQB, "W' image must fit in the V stages");
+    // TMEM columns: pass 1 uses S0 S1 W Delta, pass 2 uses S0 S1 H0 H1
+    static constexpr int colS0 = 0, colS1 = MP, colW = 2 * MP, colD = 2 * MP + D;
+    static constexpr int colH0 = 2 * MP, colH1 = 2 * MP + D;
+    static constexpr int kColsNeeded = (2 * MP + D + 16) > (2 * MP + 2 * D) ? (2 * MP + D + 16) : (2 * MP + 2 * D);
+    static constexpr int kTmemCols = kColsNeeded <= 256 ? 256 : 512;
+    static_assert(kColsNeeded <= 512, "TMEM budget");
+    static_assert(D * MP * 2 <= kQB, "W' image must fit in one V tile buffer");
     static_assert(offU % 1024 == 0 && offQ % 1024 == 0 && offV % 1024 == 0 && offA % 1024 == 0 &&
                   offOnes % 1024 == 0, "operand blocks must be 1024-byte aligned");
 };
@@ -119,43 +124,53 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Row softmax of one S row (TMEM lane = this thread's token) into the A tile (bf16).
+// 2^x on the multi-function unit (PTX ex2.approx, flush-to-zero): one instruction.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Row softmax of one S row (TMEM lane = this thread's token), packed to bf16 pairs.
 // Rows past the end of the slice become zero rows; anchors >= m get probability 0.
+// The max and the sum run as 8 interleaved partial chains (fixed order: deterministic).
 template <int MP>
-__device__ __forceinline__ void softmax_row(uint32_t taddr_s, bool valid, int m, float c, uint8_t *sA, int row) {
+__device__ __forceinline__ void softmax_row(uint32_t taddr_s, bool valid, int m, float c, uint32_t (&pk)[MP / 2]) {
     float v[MP];
 #pragma unroll
     for (int q = 0; q < MP / 32; ++q) tmem_ld32(taddr_s + q * 32, v + q * 32);
     tmem_ld_wait();
-    if (!valid) {
+    float mx8[8];
 #pragma unroll
-        for (int c8 = 0; c8 < MP / 8; ++c8)
-            *reinterpret_cast<uint4 *>(sA + sw_off(row, c8, kT)) = make_uint4(0u, 0u, 0u, 0u);
-        return;
-    }
-    float mx = -INFINITY;
+    for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
 #pragma unroll
     for (int j = 0; j < MP; ++j) {
         v[j] *= c;
-        if (j < m) mx = fmaxf(mx, v[j]);
+        if (j < m) mx8[j & 7] = fmaxf(mx8[j & 7], v[j]);
     }
-    float z = 0.f;
+    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+    float z8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) z8[i] = 0.f;
 #pragma unroll
     for (int j = 0; j < MP; ++j) {
-        const float e = (j < m) ? exp2f(v[j] - mx) : 0.f;
+        const float e = (j < m) ? ex2_approx(v[j] - mx) : 0.f;
         v[j] = e;
-        z += e;
+        z8[j & 7] += e;
     }
-    const float inv = 1.f / z;
+    const float z = ((z8[0] + z8[1]) + (z8[2] + z8[3])) + ((z8[4] + z8[5]) + (z8[6] + z8[7]));
+    const float inv = valid ? 1.f / z : 0.f;
 #pragma unroll
-    for (int c8 = 0; c8 < MP / 8; ++c8) {
-        uint4 u;
-        u.x = pack_bf16x2(v[8 * c8 + 0] * inv, v[8 * c8 + 1] * inv);
-        u.y = pack_bf16x2(v[8 * c8 + 2] * inv, v[8 * c8 + 3] * inv);
-        u.z = pack_bf16x2(v[8 * c8 + 4] * inv, v[8 * c8 + 5] * inv);
-        u.w = pack_bf16x2(v[8 * c8 + 6] * inv, v[8 * c8 + 7] * inv);
-        *reinterpret_cast<uint4 *>(sA + sw_off(row, c8, kT)) = u;
-    }
+    for (int j = 0; j < MP / 2; ++j) pk[j] = pack_bf16x2(v[2 * j] * inv, v[2 * j + 1] * inv);
+}
+
+template <int MP>
+__device__ __forceinline__ void store_a_row(const uint32_t (&pk)[MP / 2], uint8_t *sA, int row) {
+#pragma unroll
+    for (int c8 = 0; c8 < MP / 8; ++c8)
+        *reinterpret_cast<uint4 *>(sA + sw_off(row, c8, kT)) =
+            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
 }
 
 template <int D, int MP>
@@ -164,6 +179,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                    const __grid_constant__ CUtensorMap tu, const __grid_constant__ CUtensorMap th,
                    const UParams p) {
     using LY = Layout<D, MP>;
+    constexpr int NS = LY::kNS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sU = sm + LY::offU;
@@ -171,14 +187,17 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint8_t *sV = sm + LY::offV;
     uint8_t *sA = sm + LY::offA;
     uint8_t *sOnes = sm + LY::offOnes;
+    uint8_t *sW = sV;                 // pass 2: W' operand image (V buffer 0)
+    uint8_t *sH = sV + LY::kQB;       // pass 2: H staging for the TMA store (V buffer 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::offBar);
-    uint64_t *bar_q = bars;        // [2] Q (or Q+V) tile landed
-    uint64_t *bar_v = bars + 2;    // [2] V tile landed
-    uint64_t *bar_u = bars + 4;    // U landed
-    // Two commit barriers, so that neither runs more than one phase ahead of its waiters:
-    uint64_t *bar_s = bars + 5;    // scores S = Q U^T (and every MMA before them) complete
-    uint64_t *bar_w = bars + 6;    // A^T V / A^T 1 (pass 1) or A W' (pass 2) complete
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 7);
+    uint64_t *bar_q = bars;           // [NS] Q tile landed
+    uint64_t *bar_v = bars + NS;      // [NS] V tile landed
+    uint64_t *bar_u = bars + 2 * NS;  // U landed
+    // MMA completion barriers; each has at most one phase in flight ahead of its waiters.
+    uint64_t *bar_s = bars + 2 * NS + 1;  // [2] scores into S buffer 0 / 1 (and all MMAs before)
+    uint64_t *bar_w = bars + 2 * NS + 3;  // A^T V + A^T 1 (pass 1) or A W' (pass 2)
+    constexpr int kNumBars = 2 * NS + 4;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + kNumBars);
     int *s_item = reinterpret_cast<int *>(s_tmem + 1);
     int *s_last = s_item + 1;
 
@@ -186,7 +205,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const int row = tid;  // token row of a tile / anchor row of W
 
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < kNumBars; ++i) mbar_init(bars + i, 1);
         fence_mbar_init();
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tv);
@@ -204,7 +223,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
 
     const uint32_t sQa = smem_u32(sQ), sVa = smem_u32(sV), sUa = smem_u32(sU), sAa = smem_u32(sA);
-    const uint32_t sOa = smem_u32(sOnes);
+    const uint32_t sOa = smem_u32(sOnes), sWa = smem_u32(sW);
     constexpr uint32_t kIdS = idesc_bf16_f32(128, MP, false, false);
     constexpr uint32_t kIdW = idesc_bf16_f32(128, D, true, true);
     constexpr uint32_t kIdD = idesc_bf16_f32(128, 16, true, false);
@@ -212,7 +231,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_stream = policy_evict_first();
 
-    uint32_t ph_q[2] = {0u, 0u}, ph_v[2] = {0u, 0u}, ph_u = 0u, ph_s = 0u, ph_w = 0u;
+    // phases: TMA barriers are waited on by thread 0 only; MMA barriers by every thread
+    uint32_t ph_q[NS], ph_v[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) ph_q[i] = ph_v[i] = 0u;
+    uint32_t ph_u = 0u, ph_s[2] = {0u, 0u}, ph_w = 0u;
     bool ok = true;
     int cur_head = -1;
 
@@ -220,28 +243,60 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         ok = mbar_wait(bar, ph, kWaitNs) && ok;
         ph ^= 1u;
     };
-    // TMA of tile `tile` of slice s: Q (and V) into stage st.
-    auto load_tile = [&](int s, int tile, int st, bool with_v) {
+    // TMA of the Q / V tile `tile` of slice s into ring stage st.  Thread 0 only.  Tile k of
+    // an item lives in stage (k - first tile) % NS of each ring; a stage is refilled once its
+    // reader is done (Q: the score MMA, V: the A^T V MMA).
+    auto load_q = [&](int s, int tile, int st) {
         mbar_arrive_expect_tx(bar_q + st, LY::kQB);
 #pragma unroll
         for (int b = 0; b < D / 64; ++b)
             tma_load_3d(sQ + st * LY::kQB + b * kT * 128, &tq, bar_q + st, 64 * b, tile * kT, s, pol_keep);
-        if (with_v) {
-            mbar_arrive_expect_tx(bar_v + st, LY::kQB);
-#pragma unroll
-            for (int b = 0; b < D / 64; ++b)
-                tma_load_3d(sV + st * LY::kQB + b * kT * 128, &tv, bar_v + st, 64 * b, tile * kT, s, pol_stream);
-        }
     };
-    auto issue_scores = [&](int st) {  // S = Q U^T
+    auto load_v = [&](int s, int tile, int st) {
+        mbar_arrive_expect_tx(bar_v + st, LY::kQB);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b)
+            tma_load_3d(sV + st * LY::kQB + b * kT * 128, &tv, bar_v + st, 64 * b, tile * kT, s, pol_stream);
+    };
+    // Thread 0: wait for the Q tile in stage st, then S[buf] = Q U^T.
+    auto issue_scores = [&](int st, int buf) {
+        ok = mbar_wait(bar_q + st, ph_q[st], kWaitNs) && ok;
+        ph_q[st] ^= 1u;
         tc_fence_after();
+        const uint32_t dcol = buf ? LY::colS1 : LY::colS0;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t a = smem_desc_sw128(sQa + st * LY::kQB + (kk >> 2) * kT * 128 + (kk & 3) * 32, 16, 1024);
             const uint64_t b = smem_desc_sw128(sUa + (kk >> 2) * MP * 128 + (kk & 3) * 32, 16, 1024);
-            umma_bf16(tmem + LY::colS, a, b, kIdS, kk > 0);
+            umma_bf16(tmem + dcol, a, b, kIdS, kk > 0);
         }
-        umma_commit(bar_s);
+        umma_commit(bar_s + buf);
+    };
+    // All threads: H row of TMEM buffer `hcol` -> bf16 -> staging -> TMA store of tile `tile`.
+    auto h_epilogue = [&](int s, int tile, uint32_t hcol) {
+        uint32_t pk[D / 2];
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+            float v[32];
+            tmem_ld32(trow + hcol + q * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[q * 16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        }
+        if (tid == 0) bulk_wait_group_read0();  // the previous store has read the staging buffer
+        __syncthreads();
+#pragma unroll
+        for (int c8 = 0; c8 < D / 8; ++c8)
+            *reinterpret_cast<uint4 *>(sH + sw_off(row, c8, kT)) =
+                make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int bb = 0; bb < D / 64; ++bb)
+                tma_store_3d(&th, sH + bb * kT * 128, 64 * bb, tile * kT, s, pol_stream);
+            bulk_commit_group();
+        }
     };
 
     for (;;) {
@@ -268,21 +323,34 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (it.kind != 1) {
             const int a = it.kind == 2 ? 0 : (int)((long long)it.chunk * p.NT / p.C1);
             const int b = it.kind == 2 ? p.NT : (int)((long long)(it.chunk + 1) * p.NT / p.C1);
-            if (tid == 0) load_tile(s, a, 0, true);
-            int st = 0;
-            for (int tile = a; tile < b; ++tile, st ^= 1) {
-                wait(bar_q + st, ph_q[st]);
-                if (tid == 0) issue_scores(st);
-                wait(bar_s, ph_s);               // S(tile), and W(tile-1) issued before it
-                if (tile > a) wait(bar_w, ph_w); // consume W(tile-1)'s phase (already complete)
+            if (tid == 0) {
+                for (int k = 0; k < NS && a + k < b; ++k) {
+                    load_q(s, a + k, k);
+                    load_v(s, a + k, k);
+                }
+                issue_scores(0, 0);
+            }
+            for (int tile = a; tile < b; ++tile) {
+                const int i = tile - a, buf = i & 1, st = i % NS;
+                wait(bar_s + buf, ph_s[buf]);          // S(tile) done: its Q stage is free
                 tc_fence_after();
-                if (tid == 0 && tile + 1 < b) load_tile(s, tile + 1, st ^ 1, true);
-                softmax_row<MP>(trow + LY::colS, tile * kT + row < p.n, p.m, p.c, sA, row);
+                if (tid == 0) {
+                    if (tile + NS < b) load_q(s, tile + NS, st);
+                    if (tile + 1 < b) issue_scores((i + 1) % NS, buf ^ 1);
+                }
+                uint32_t pk[MP / 2];
+                softmax_row<MP>(trow + (buf ? LY::colS1 : LY::colS0), tile * kT + row < p.n, p.m, p.c, pk);
+                if (i > 0) {
+                    wait(bar_w, ph_w);                 // W(tile-1) done: A tile and V stage of tile-1 free
+                    if (tid == 0 && tile - 1 + NS < b) load_v(s, tile - 1 + NS, (i - 1) % NS);
+                }
+                store_a_row<MP>(pk, sA, row);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 if (__syncthreads_or(!ok)) goto abort;
-                wait(bar_v + st, ph_v[st]);
                 if (tid == 0) {
+                    ok = mbar_wait(bar_v + st, ph_v[st], kWaitNs) && ok;
+                    ph_v[st] ^= 1u;
                     tc_fence_after();
 #pragma unroll
                     for (int kt = 0; kt < kT / 16; ++kt) {
@@ -374,7 +442,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const float wp = dj != 0.f ? v[i] / dj : 0.f;
-                            *reinterpret_cast<uint16_t *>(sV + wimg_off<D>(row, q * 32 + i)) =
+                            *reinterpret_cast<uint16_t *>(sW + wimg_off<D>(row, q * 32 + i)) =
                                 __bfloat16_as_ushort(__float2bfloat16_rn(wp));
                         }
                     }
@@ -399,7 +467,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             if (__syncthreads_or(!ok)) goto abort;
             const uint4 *src = reinterpret_cast<const uint4 *>(p.wimg + (size_t)s * (D * MP));
             for (int i = tid; i < D * MP * 2 / 16; i += kThreads)
-                reinterpret_cast<uint4 *>(sV)[i] = __ldcg(src + i);
+                reinterpret_cast<uint4 *>(sW)[i] = __ldcg(src + i);
             fence_proxy_async_smem();
             __syncthreads();
         }
@@ -409,65 +477,47 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             const int a = it.kind == 2 ? 0 : (int)((long long)it.chunk * p.NT / p.C2);
             const int b = it.kind == 2 ? p.NT : (int)((long long)(it.chunk + 1) * p.NT / p.C2);
             if (tid == 0) {
-                bulk_wait_group_read0();
-                load_tile(s, a, 0, false);
+                for (int k = 0; k < NS && a + k < b; ++k) load_q(s, a + k, k);
+                issue_scores(0, 0);
             }
-            int st = 0;
-            for (int tile = a; tile < b; ++tile, st ^= 1) {
-                if (tid == 0 && tile + 1 < b) {
-                    bulk_wait_group_read0();  // stage st^1 may still feed the previous H store
-                    load_tile(s, tile + 1, st ^ 1, false);
-                }
-                wait(bar_q + st, ph_q[st]);
-                if (tid == 0) issue_scores(st);
-                wait(bar_s, ph_s);
+            for (int tile = a; tile < b; ++tile) {
+                const int i = tile - a, buf = i & 1;
+                wait(bar_s + buf, ph_s[buf]);          // S(tile) ready (and H(tile-1)'s inputs)
                 tc_fence_after();
-                softmax_row<MP>(trow + LY::colS, tile * kT + row < p.n, p.m, p.c, sA, row);
+                if (tid == 0) {
+                    if (tile + NS < b) load_q(s, tile + NS, i % NS);  // Q(tile) consumed
+                    if (tile + 1 < b) issue_scores((i + 1) % NS, buf ^ 1);
+                }
+                uint32_t pk[MP / 2];
+                softmax_row<MP>(trow + (buf ? LY::colS1 : LY::colS0), tile * kT + row < p.n, p.m, p.c, pk);
+                if (i > 0) wait(bar_w, ph_w);          // H(tile-1) done: A tile free
+                store_a_row<MP>(pk, sA, row);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 if (__syncthreads_or(!ok)) goto abort;
                 if (tid == 0) {
                     tc_fence_after();
+                    const uint32_t hcol = buf ? LY::colH1 : LY::colH0;
 #pragma unroll
                     for (int kj = 0; kj < MP / 16; ++kj) {
                         const uint64_t ad = smem_desc_sw128(sAa + (kj >> 2) * 16384 + (kj & 3) * 32, 16, 1024);
-                        const uint64_t wd = smem_desc_sw128(sVa + (kj >> 2) * D * 128 + (kj & 3) * 32, 16, 1024);
-                        umma_bf16(tmem + LY::colW, ad, wd, kIdH, kj > 0);
+                        const uint64_t wd = smem_desc_sw128(sWa + (kj >> 2) * D * 128 + (kj & 3) * 32, 16, 1024);
+                        umma_bf16(tmem + hcol, ad, wd, kIdH, kj > 0);
                     }
                     umma_commit(bar_w);
                 }
-                wait(bar_w, ph_w);
-                tc_fence_after();
-                // H row -> bf16 -> the Q buffer of this stage (Q was consumed by S) -> TMA store
-                {
-                    float v[32];
-                    uint8_t *stg = sQ + st * LY::kQB;
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        tmem_ld32(trow + LY::colW + q * 32, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            uint4 u;
-                            u.x = pack_bf16x2(v[8 * c4 + 0], v[8 * c4 + 1]);
-                            u.y = pack_bf16x2(v[8 * c4 + 2], v[8 * c4 + 3]);
-                            u.z = pack_bf16x2(v[8 * c4 + 4], v[8 * c4 + 5]);
-                            u.w = pack_bf16x2(v[8 * c4 + 6], v[8 * c4 + 7]);
-                            *reinterpret_cast<uint4 *>(stg + sw_off(row, q * 4 + c4, kT)) = u;
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncthreads();
-                if (tid == 0) {
-#pragma unroll
-                    for (int bb = 0; bb < D / 64; ++bb)
-                        tma_store_3d(&th, sQ + st * LY::kQB + bb * kT * 128, 64 * bb, tile * kT, s, pol_stream);
-                    bulk_commit_group();
+                if (i > 0) {  // store H(tile-1) while the tensor core works on tile
+                    tc_fence_after();
+                    h_epilogue(s, tile - 1, buf ? LY::colH0 : LY::colH1);
                 }
             }
+            wait(bar_w, ph_w);
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) goto abort;
+            h_epilogue(s, b - 1, ((b - 1 - a) & 1) ? LY::colH1 : LY::colH0);
+            tc_fence_before();
             if (tid == 0) bulk_wait_group_read0();
+            __syncthreads();
         }
     }
     goto done;
@@ -513,6 +563,8 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
     using LY = Layout<D, MP>;
     auto kern = anchor_umma_kernel<D, MP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
