@@ -33,8 +33,8 @@
 
 namespace anchor {
 
-// Device-wide error word: bit 0 = an mbarrier wait timed out, bit 1 = a wait for another
-// CTA's reduction timed out.  Read and cleared by anchor_attn_device_error().
+// Device-wide error word: bit 0 = a wait inside the kernel timed out, bit 1 = a wait for
+// another CTA's reduction timed out.  Read and cleared by anchor_attn_device_error().
 __device__ unsigned int g_umma_error;
 
 namespace {
@@ -42,69 +42,116 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 128;                         // tokens per tile (UMMA M)
-constexpr int kThreads = 128;                   // one thread per token row / TMEM lane
+constexpr int kThreads = 192;                   // warps 0-3 softmax/epilogue, 4 producer, 5 MMA
+constexpr int kIQ = 4;                          // item queue depth
 constexpr uint64_t kWaitNs = 2000000000ull;     // every wait gives up after 2 s
+constexpr double kL2QBudget = 48.0 * 1024 * 1024; // L2 share for Q between its two reads
 
 struct UParams {
-    int slices, heads, n, m;
+    int slices, heads, B, n, m;
     float c;                  // scale * log2(e)
-    int NT, C1, C2, L, total; // tiles per slice, P1 / P2 chunks per slice, lag, items
-    float *part;              // [slices][C1][D][MP]  W partials (anchor index fastest)
+    int NT, C1, C2;           // tiles per slice, P1 / P2 chunks per slice (C1 == 1: whole slices)
+    float *part;              // [slices][C1][MP][D]  W partials, one row per anchor
     float *pdelta;            // [slices][C1][MP]     Delta partials
-    uint16_t *wimg;           // [slices][D * MP]     W' operand images (bf16)
-    unsigned *counts;         // [slices] finished P1 chunks
-    unsigned *flags;          // [slices] W' ready
-    unsigned *ticket;         // item counter
+    uint16_t *wimg;           // [slices][D * MP]     W' operand images (bf16, swizzled)
+    unsigned *flags;          // [slices * 32] W' published (one 128-byte line per slice)
+    unsigned *p2c;            // [slices * 32] P2 chunks of the slice claimed so far
+    unsigned *tree;           // [slices][C1] arrivals at the nodes of the reduction tree
+    unsigned *next;           // next P1 chunk (or whole slice) to claim
+    unsigned *head;           // first slice (schedule order) whose P2 chunks are not all claimed
+    int K;                    // P1 may run at most K slices ahead of the P2 head
 };
 
 template <int D, int MP>
 struct Layout {
-    static constexpr int kQB = kT * D * 2;             // one Q / V / H tile
+    static constexpr int kQB = kT * D * 2;             // one Q or V tile: one ring slot
     static constexpr int kUB = MP * D * 2;
     static constexpr int kAB = kT * 128 * 2;           // A tile, 128 anchor columns
+    static constexpr int kWB = D * MP * 2;             // W' operand image
     static constexpr int kOnesB = 16 * kT * 2;         // 16 x 128 ones (bf16)
-    static constexpr int kNS = 2;                      // TMA stages (each: a Q and a V tile)
+    static constexpr int kBarB = 1024;
+    static constexpr int kMaxDyn = 227 * 1024 - 1024;  // minus the alignment slack
+    // double-buffer the anchors and the A tile when that still leaves a 6-slot ring
+    static constexpr bool kRoomy = (2 * kUB + 2 * kAB + kWB + kOnesB + kBarB + 6 * kQB) <= kMaxDyn;
+    static constexpr int kNU = kRoomy ? 2 : 1;
+    static constexpr int kNA = kRoomy ? 2 : 1;
+    static constexpr int kFixed = kNU * kUB + kNA * kAB + kWB + kOnesB + kBarB;
+    static constexpr int kSlotsFit = (kMaxDyn - kFixed) / kQB;
+    static constexpr int kNSlot = kSlotsFit > 8 ? 8 : kSlotsFit;
     static constexpr int offU = 0;
-    static constexpr int offQ = offU + kUB;            // kNS Q tiles
-    static constexpr int offV = offQ + kNS * kQB;      // kNS V tiles; in pass 2: W' image, H staging
-    static constexpr int offA = offV + kNS * kQB;
-    static constexpr int offOnes = offA + kAB;
+    static constexpr int offA = offU + kNU * kUB;
+    static constexpr int offW = offA + kNA * kAB;
+    static constexpr int offRing = offW + kWB;
+    static constexpr int offOnes = offRing + kNSlot * kQB;
     static constexpr int offBar = offOnes + kOnesB;
-    static constexpr int kBytes = offBar + 256;
-    static constexpr int kSmem = kBytes + 1024;        // slack for 1024-byte alignment
-    // TMEM columns: pass 1 uses S0 S1 W Delta, pass 2 uses S0 S1 H0 H1
-    static constexpr int colS0 = 0, colS1 = MP, colW = 2 * MP, colD = 2 * MP + D;
-    static constexpr int colH0 = 2 * MP, colH1 = 2 * MP + D;
-    static constexpr int kColsNeeded = (2 * MP + D + 16) > (2 * MP + 2 * D) ? (2 * MP + D + 16) : (2 * MP + 2 * D);
-    static constexpr int kTmemCols = kColsNeeded <= 256 ? 256 : 512;
-    static_assert(kColsNeeded <= 512, "TMEM budget");
-    static_assert(D * MP * 2 <= kQB, "W' image must fit in one V tile buffer");
-    static_assert(offU % 1024 == 0 && offQ % 1024 == 0 && offV % 1024 == 0 && offA % 1024 == 0 &&
+    static constexpr int kBytes = offBar + kBarB;
+    static constexpr int kSmem = kBytes + 1024;
+    // TMEM: S0 | S1 | B0 (W in pass 1, H0 in pass 2) | B1 (Delta in pass 1, H1 in pass 2)
+    static constexpr int colS0 = 0, colS1 = MP, colB0 = 2 * MP, colB1 = 2 * MP + D;
+    static constexpr int kTmemCols = (2 * MP + 2 * D) <= 256 ? 256 : 512;
+    static_assert(kNSlot >= 3, "ring too shallow");
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static_assert(kUB % 1024 == 0 && offA % 1024 == 0 && offW % 1024 == 0 && offRing % 1024 == 0 &&
                   offOnes % 1024 == 0, "operand blocks must be 1024-byte aligned");
 };
 
+// Work items.  kind: 0 = P1 chunk, 1 = P2 chunk, 2 = whole slice, 3 = FLUSH (no tile follows
+// soon: finish the tile held back for overlap), 4 = end of work.
 struct Item {
-    int kind;   // 0 = P1, 1 = P2, 2 = FULL
-    int slice;
+    int kind;
+    int slice;  // (batch, head) slice index b * heads + h
     int chunk;
 };
+constexpr int kFlush = 3, kEnd = 4;
 
-__device__ __forceinline__ Item decode(int t, const UParams &p) {
-    if (p.C1 == 1) return {2, t, 0};
-    const int S = p.slices, L = p.L, C1 = p.C1, C2 = p.C2;
-    const int a = min(L, S);
-    if (t < a * C1) return {0, t / C1, t % C1};
-    t -= a * C1;
-    if (L < S) {
-        const int per = C1 + C2, nb = S - L;
-        if (t < nb * per) {
-            const int k = t / per, r = t - k * per;
-            return r < C1 ? Item{0, L + k, r} : Item{1, k, r - C1};
-        }
-        t -= nb * per;
-        return {1, (S - L) + t / C2, t % C2};
+// Slices are visited head-major (all batch entries of head 0, then head 1, ...) so that
+// consecutive items usually share the anchors U.
+__device__ __forceinline__ int slice_of(int so, const UParams &p) {
+    const int h = so / p.B, b = so - h * p.B;
+    return b * p.heads + h;
+}
+
+// One 128-token tile of an item, as every role sees it.
+struct TileRef {
+    int slice, tile;
+    int kind;       // 0: pass-1 tile (S, softmax, A^T V);  1: pass-2 tile (S, softmax, A W')
+    bool first;     // first tile of its pass within the item
+    bool last;      // last tile of its pass within the item
+    bool full;      // the item keeps W' on chip (whole slice per CTA)
+    int chunk;      // pass-1 chunk (partials)
+};
+
+__device__ __forceinline__ int item_tiles(const Item &it, const UParams &p, int &a1, int &b1) {
+    if (it.kind == 2) {
+        a1 = 0, b1 = p.NT;
+        return 2 * p.NT;
     }
-    return {1, t / C2, t % C2};
+    const int C = it.kind == 0 ? p.C1 : p.C2;
+    a1 = (int)((long long)it.chunk * p.NT / C);
+    b1 = (int)((long long)(it.chunk + 1) * p.NT / C);
+    return b1 - a1;
+}
+
+__device__ __forceinline__ TileRef tile_at(const Item &it, int a1, int b1, int idx) {
+    TileRef r;
+    r.slice = it.slice;
+    r.chunk = it.chunk;
+    r.full = it.kind == 2;
+    const int n1 = b1 - a1;
+    if (it.kind == 2) {
+        const bool p2 = idx >= n1;
+        const int k = p2 ? idx - n1 : idx;
+        r.kind = p2 ? 1 : 0;
+        r.tile = k;
+        r.first = k == 0;
+        r.last = k == n1 - 1;
+    } else {
+        r.kind = it.kind;
+        r.tile = a1 + idx;
+        r.first = idx == 0;
+        r.last = idx == n1 - 1;
+    }
+    return r;
 }
 
 // byte offset of 16-byte chunk `c` (0 .. cols/8-1) of row `r` in a swizzled [rows][cols]
@@ -130,6 +177,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+
+__device__ __forceinline__ void wg_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Row softmax of one S row (TMEM lane = this thread's token), packed to bf16 pairs.
 // Rows past the end of the slice become zero rows; anchors >= m get probability 0.
@@ -165,370 +214,575 @@ __device__ __forceinline__ void softmax_row(uint32_t taddr_s, bool valid, int m,
     for (int j = 0; j < MP / 2; ++j) pk[j] = pack_bf16x2(v[2 * j] * inv, v[2 * j + 1] * inv);
 }
 
-template <int MP>
-__device__ __forceinline__ void store_a_row(const uint32_t (&pk)[MP / 2], uint8_t *sA, int row) {
-#pragma unroll
-    for (int c8 = 0; c8 < MP / 8; ++c8)
-        *reinterpret_cast<uint4 *>(sA + sw_off(row, c8, kT)) =
-            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-}
-
 template <int D, int MP>
 __global__ void __launch_bounds__(kThreads, 1)
 anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
-                   const __grid_constant__ CUtensorMap tu, const __grid_constant__ CUtensorMap th,
-                   const UParams p) {
+                   const __grid_constant__ CUtensorMap tu, const UParams p, uint16_t *__restrict__ Hout) {
     using LY = Layout<D, MP>;
-    constexpr int NS = LY::kNS;
+    constexpr int NS = LY::kNSlot, NU = LY::kNU, NA = LY::kNA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sU = sm + LY::offU;
-    uint8_t *sQ = sm + LY::offQ;
-    uint8_t *sV = sm + LY::offV;
     uint8_t *sA = sm + LY::offA;
+    uint8_t *sW = sm + LY::offW;
+    uint8_t *sRing = sm + LY::offRing;
     uint8_t *sOnes = sm + LY::offOnes;
-    uint8_t *sW = sV;                 // pass 2: W' operand image (V buffer 0)
-    uint8_t *sH = sV + LY::kQB;       // pass 2: H staging for the TMA store (V buffer 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::offBar);
-    uint64_t *bar_q = bars;           // [NS] Q tile landed
-    uint64_t *bar_v = bars + NS;      // [NS] V tile landed
-    uint64_t *bar_u = bars + 2 * NS;  // U landed
-    // MMA completion barriers; each has at most one phase in flight ahead of its waiters.
-    uint64_t *bar_s = bars + 2 * NS + 1;  // [2] scores into S buffer 0 / 1 (and all MMAs before)
-    uint64_t *bar_w = bars + 2 * NS + 3;  // A^T V + A^T 1 (pass 1) or A W' (pass 2)
-    constexpr int kNumBars = 2 * NS + 4;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + kNumBars);
-    int *s_item = reinterpret_cast<int *>(s_tmem + 1);
-    int *s_last = s_item + 1;
+    // full/empty barrier pairs (arrival counts in brackets)
+    uint64_t *slot_full = bars;                  // [NS] (1 + tx)  TMA landed
+    uint64_t *slot_empty = slot_full + NS;       // [NS] (1)       MMA that read the slot completed
+    uint64_t *s_full = slot_empty + NS;          // [2]  (1)       scores in S buffer
+    uint64_t *s_empty = s_full + 2;              // [2]  (4)       softmax warps read the S buffer
+    uint64_t *a_full = s_empty + 2;              // [NA] (4)       A tile written
+    uint64_t *a_empty = a_full + NA;             // [NA] (1)       MMA reading the A tile completed
+    uint64_t *acc_full = a_empty + NA;           // [2]  (1)       W/Delta or H complete in TMEM
+    uint64_t *acc_empty = acc_full + 2;          // [2]  (4)       epilogue read it
+    uint64_t *u_full = acc_empty + 2;            // [NU] (1 + tx)  U landed
+    uint64_t *u_empty = u_full + NU;             // [NU] (1)       MMAs on that U completed
+    uint64_t *w_full = u_empty + NU;             //      (1 [+ tx]) W' image in place
+    uint64_t *w_empty = w_full + 1;              //      (1)       MMAs reading W' completed
+    uint64_t *iq_full = w_empty + 1;             // [kIQ] (1)      item queue
+    uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (2)
+    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 * NA + 2 + 2 + 2 * NU + 2 + 2 * kIQ;
+    static_assert(kNumBars * 8 + 3 * 4 * kIQ + 64 <= LY::kBarB, "barrier area");
+    int *s_items = reinterpret_cast<int *>(bars + kNumBars);           // [kIQ][3]
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_items + 3 * kIQ);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    int *s_last = reinterpret_cast<int *>(s_tmem + 2);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = tid;  // token row of a tile / anchor row of W
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(slot_full + i, 1);
+            mbar_init(slot_empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + i, 1);
+            mbar_init(s_empty + i, 4);
+            mbar_init(acc_full + i, 1);
+            mbar_init(acc_empty + i, 4);
+        }
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(a_full + i, 4);
+            mbar_init(a_empty + i, 1);
+        }
+        for (int i = 0; i < NU; ++i) {
+            mbar_init(u_full + i, 1);
+            mbar_init(u_empty + i, 1);
+        }
+        mbar_init(w_full, 1);
+        mbar_init(w_empty, 1);
+        for (int i = 0; i < kIQ; ++i) {
+            mbar_init(iq_full + i, 1);
+            mbar_init(iq_empty + i, 2);
+        }
+        *s_abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tu);
-        tma_prefetch_desc(&th);
     }
     for (int i = tid; i < LY::kOnesB / 4; i += kThreads) reinterpret_cast<uint32_t *>(sOnes)[i] = 0x3F803F80u;
-    for (int i = tid; i < LY::kAB / 16; i += kThreads) reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0, 0, 0, 0);
-    if (warp == 0) tmem_alloc(s_tmem, LY::kTmemCols);
+    for (int i = tid; i < NA * LY::kAB / 16; i += kThreads) reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0, 0, 0, 0);
+    if (warp == 5) tmem_alloc(s_tmem, LY::kTmemCols);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
 
-    const uint32_t sQa = smem_u32(sQ), sVa = smem_u32(sV), sUa = smem_u32(sU), sAa = smem_u32(sA);
-    const uint32_t sOa = smem_u32(sOnes), sWa = smem_u32(sW);
-    constexpr uint32_t kIdS = idesc_bf16_f32(128, MP, false, false);
-    constexpr uint32_t kIdW = idesc_bf16_f32(128, D, true, true);
-    constexpr uint32_t kIdD = idesc_bf16_f32(128, 16, true, false);
-    constexpr uint32_t kIdH = idesc_bf16_f32(128, D, false, false);
-    const uint64_t pol_keep = policy_evict_last();
-    const uint64_t pol_stream = policy_evict_first();
-
-    // phases: TMA barriers are waited on by thread 0 only; MMA barriers by every thread
-    uint32_t ph_q[NS], ph_v[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) ph_q[i] = ph_v[i] = 0u;
-    uint32_t ph_u = 0u, ph_s[2] = {0u, 0u}, ph_w = 0u;
-    bool ok = true;
-    int cur_head = -1;
-
-    auto wait = [&](uint64_t *bar, uint32_t &ph) {
-        ok = mbar_wait(bar, ph, kWaitNs) && ok;
-        ph ^= 1u;
-    };
-    // TMA of the Q / V tile `tile` of slice s into ring stage st.  Thread 0 only.  Tile k of
-    // an item lives in stage (k - first tile) % NS of each ring; a stage is refilled once its
-    // reader is done (Q: the score MMA, V: the A^T V MMA).
-    auto load_q = [&](int s, int tile, int st) {
-        mbar_arrive_expect_tx(bar_q + st, LY::kQB);
-#pragma unroll
-        for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(sQ + st * LY::kQB + b * kT * 128, &tq, bar_q + st, 64 * b, tile * kT, s, pol_keep);
-    };
-    auto load_v = [&](int s, int tile, int st) {
-        mbar_arrive_expect_tx(bar_v + st, LY::kQB);
-#pragma unroll
-        for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(sV + st * LY::kQB + b * kT * 128, &tv, bar_v + st, 64 * b, tile * kT, s, pol_stream);
-    };
-    // Thread 0: wait for the Q tile in stage st, then S[buf] = Q U^T.
-    auto issue_scores = [&](int st, int buf) {
-        ok = mbar_wait(bar_q + st, ph_q[st], kWaitNs) && ok;
-        ph_q[st] ^= 1u;
-        tc_fence_after();
-        const uint32_t dcol = buf ? LY::colS1 : LY::colS0;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = smem_desc_sw128(sQa + st * LY::kQB + (kk >> 2) * kT * 128 + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = smem_desc_sw128(sUa + (kk >> 2) * MP * 128 + (kk & 3) * 32, 16, 1024);
-            umma_bf16(tmem + dcol, a, b, kIdS, kk > 0);
-        }
-        umma_commit(bar_s + buf);
-    };
-    // All threads: H row of TMEM buffer `hcol` -> bf16 -> staging -> TMA store of tile `tile`.
-    auto h_epilogue = [&](int s, int tile, uint32_t hcol) {
-        uint32_t pk[D / 2];
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-            float v[32];
-            tmem_ld32(trow + hcol + q * 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[q * 16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-        }
-        if (tid == 0) bulk_wait_group_read0();  // the previous store has read the staging buffer
-        __syncthreads();
-#pragma unroll
-        for (int c8 = 0; c8 < D / 8; ++c8)
-            *reinterpret_cast<uint4 *>(sH + sw_off(row, c8, kT)) =
-                make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-#pragma unroll
-            for (int bb = 0; bb < D / 64; ++bb)
-                tma_store_3d(&th, sH + bb * kT * 128, 64 * bb, tile * kT, s, pol_stream);
-            bulk_commit_group();
+    // Bounded wait that also gives up once another role has given up.
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if (*s_abort) return false;
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                *s_abort = 1;
+                atomicOr(&g_umma_error, 1u);
+                return false;
+            }
         }
     };
+    auto read_item = [&](uint32_t iq) -> Item {
+        const int *e = s_items + 3 * (int)(iq % kIQ);
+        return {e[0], e[1], e[2]};
+    };
 
-    for (;;) {
-        if (tid == 0) *s_item = (int)atomicAdd(p.ticket, 1u);
-        __syncthreads();
-        const int t = *s_item;
-        __syncthreads();
-        if (t >= p.total) break;
-        const Item it = decode(t, p);
-        const int s = it.slice;
-        const int h = s % p.heads;
-
-        if (h != cur_head) {  // anchors of this head (all MMAs of the previous item are done)
-            if (tid == 0) {
-                mbar_arrive_expect_tx(bar_u, LY::kUB);
+    if (warp == 4) {
+        // =========================================================== producer
+        if (lane == 0) {
+            const uint64_t pol_keep = policy_evict_last();
+            const uint64_t pol_stream = policy_evict_first();
+            uint32_t ld_seq = 0, iq = 0, wuse = 0, nu = 0;
+            int u_head = -1;
+            TileRef pend_v;
+            bool has_pend_v = false, ok = true, flushed = true;
+            const unsigned n1 = (unsigned)(p.C1 == 1 ? p.slices : p.slices * p.C1);
+            const unsigned n2 = (unsigned)(p.C1 == 1 ? 0 : p.slices * p.C2);
+            auto load_slot = [&](const CUtensorMap *map, int slice, int tile, uint64_t pol) -> bool {
+                const int st = (int)(ld_seq % NS);
+                if (!wait(slot_empty + st, ((ld_seq / NS) & 1u) ^ 1u)) return false;
+                mbar_arrive_expect_tx(slot_full + st, LY::kQB);
 #pragma unroll
-                for (int b = 0; b < D / 64; ++b) tma_load_3d(sU + b * MP * 128, &tu, bar_u, 64 * b, 0, h, pol_keep);
-            }
-            wait(bar_u, ph_u);
-            cur_head = h;
-        }
-
-        // ------------------------------------------------------------ pass 1
-        if (it.kind != 1) {
-            const int a = it.kind == 2 ? 0 : (int)((long long)it.chunk * p.NT / p.C1);
-            const int b = it.kind == 2 ? p.NT : (int)((long long)(it.chunk + 1) * p.NT / p.C1);
-            if (tid == 0) {
-                for (int k = 0; k < NS && a + k < b; ++k) {
-                    load_q(s, a + k, k);
-                    load_v(s, a + k, k);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(sRing + st * LY::kQB + b * kT * 128, map, slot_full + st, 64 * b, tile * kT, slice, pol);
+                ++ld_seq;
+                return true;
+            };
+            auto push = [&](const Item &it) -> bool {
+                const int qs = (int)(iq % kIQ);
+                if (!wait(iq_empty + qs, ((iq / kIQ) & 1u) ^ 1u)) return false;
+                s_items[3 * qs] = it.kind;
+                s_items[3 * qs + 1] = it.slice;
+                s_items[3 * qs + 2] = it.chunk;
+                mbar_arrive(iq_full + qs);
+                ++iq;
+                return true;
+            };
+            auto vload = [](const unsigned *a) { return *reinterpret_cast<const volatile unsigned *>(a); };
+            // Claim the next item: a P2 chunk of a slice whose W' is published (within a window
+            // of kWin slices from the head), else a P1 chunk if its slice is within K of the head
+            // (or a whole slice).  Readiness is tested with plain loads before any atomic, and
+            // every atomic is an add (no compare-and-swap retry loops).
+            // 1: claimed, 0: nothing claimable yet, -1: no work left.
+            constexpr int kWin = 8;
+            auto claim = [&](Item &it) -> int {
+                if (n2 == 0) {
+                    if (vload(p.next) >= n1) return -1;
+                    const unsigned u = atomicAdd(p.next, 1u);
+                    if (u >= n1) return -1;
+                    it = {2, slice_of((int)u, p), 0};
+                    return 1;
                 }
-                issue_scores(0, 0);
-            }
-            for (int tile = a; tile < b; ++tile) {
-                const int i = tile - a, buf = i & 1, st = i % NS;
-                wait(bar_s + buf, ph_s[buf]);          // S(tile) done: its Q stage is free
-                tc_fence_after();
-                if (tid == 0) {
-                    if (tile + NS < b) load_q(s, tile + NS, st);
-                    if (tile + 1 < b) issue_scores((i + 1) % NS, buf ^ 1);
+                unsigned h = vload(p.head);
+                while (h < (unsigned)p.slices && vload(p.p2c + 32 * slice_of((int)h, p)) >= (unsigned)p.C2) {
+                    atomicMax(p.head, h + 1u);
+                    h = vload(p.head);
                 }
-                uint32_t pk[MP / 2];
-                softmax_row<MP>(trow + (buf ? LY::colS1 : LY::colS0), tile * kT + row < p.n, p.m, p.c, pk);
-                if (i > 0) {
-                    wait(bar_w, ph_w);                 // W(tile-1) done: A tile and V stage of tile-1 free
-                    if (tid == 0 && tile - 1 + NS < b) load_v(s, tile - 1 + NS, (i - 1) % NS);
-                }
-                store_a_row<MP>(pk, sA, row);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                if (__syncthreads_or(!ok)) goto abort;
-                if (tid == 0) {
-                    ok = mbar_wait(bar_v + st, ph_v[st], kWaitNs) && ok;
-                    ph_v[st] ^= 1u;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kt = 0; kt < kT / 16; ++kt) {
-                        const uint64_t ad = smem_desc_sw128(sAa + kt * 2048, 16384, 1024);
-                        const uint64_t vd = smem_desc_sw128(sVa + st * LY::kQB + kt * 2048, 16384, 1024);
-                        const uint64_t od = smem_desc_sw128(sOa + (kt >> 2) * 2048 + (kt & 3) * 32, 16, 1024);
-                        const uint32_t acc = (tile > a || kt > 0) ? 1u : 0u;
-                        umma_bf16(tmem + LY::colW, ad, vd, kIdW, acc);
-                        umma_bf16(tmem + LY::colD, ad, od, kIdD, acc);
-                    }
-                    umma_commit(bar_w);
-                }
-            }
-            wait(bar_w, ph_w);  // W, Delta of the chunk complete
-            tc_fence_after();
-            if (__syncthreads_or(!ok)) goto abort;
-
-            if (it.kind == 0) {
-                // chunk partial -> workspace; the last chunk of the slice reduces
-                float v[32];
-                float *dst = p.part + ((size_t)s * p.C1 + it.chunk) * (size_t)(D * MP);
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    tmem_ld32(trow + LY::colW + q * 32, v);
-                    tmem_ld_wait();
-                    if (row < MP) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) dst[(q * 32 + i) * MP + row] = v[i];
+                if (h >= (unsigned)p.slices) return -1;
+                const unsigned hend = min((unsigned)p.slices, h + (unsigned)kWin);
+                for (unsigned so = h; so < hend; ++so) {
+                    const int sl = slice_of((int)so, p);
+                    if (vload(p.flags + 32 * sl) == 0u || vload(p.p2c + 32 * sl) >= (unsigned)p.C2) continue;
+                    const unsigned u = atomicAdd(p.p2c + 32 * sl, 1u);
+                    if (u < (unsigned)p.C2) {
+                        it = {1, sl, (int)u};
+                        return 1;
                     }
                 }
-                tmem_ld32(trow + LY::colD, v);
-                tmem_ld_wait();
-                if (row < MP) p.pdelta[((size_t)s * p.C1 + it.chunk) * MP + row] = v[0];
-                __threadfence();
-                tc_fence_before();
-                __syncthreads();
-                if (tid == 0) *s_last = (atomicAdd(p.counts + s, 1u) == (unsigned)(p.C1 - 1)) ? 1 : 0;
-                __syncthreads();
-                if (*s_last) {
-                    __threadfence();
-                    // Delta_j = sum over chunks in order; then W'_jk = W_jk / Delta_j
-                    float *sd = reinterpret_cast<float *>(sA);  // A tile lower block is scratch now
-                    if (tid < MP) {
-                        float dsum = 0.f;
-                        for (int cc = 0; cc < p.C1; ++cc) dsum += __ldcg(p.pdelta + ((size_t)s * p.C1 + cc) * MP + tid);
-                        sd[tid] = dsum;
-                    }
-                    __syncthreads();
-                    constexpr int JQ = MP / 4, KG = kThreads / JQ;
-                    const int jq = tid % JQ, kg = tid / JQ;
-                    const float *src = p.part + (size_t)s * p.C1 * (D * MP);
-                    uint16_t *img = p.wimg + (size_t)s * (D * MP);
-                    for (int k = kg; k < D; k += KG) {
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int cc = 0; cc < p.C1; ++cc) {
-                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(src + ((size_t)cc * D + k) * MP) + jq);
-                            acc.x += x.x;
-                            acc.y += x.y;
-                            acc.z += x.z;
-                            acc.w += x.w;
-                        }
-                        const float w4[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int j = 4 * jq + e;
-                            const float dj = sd[j];
-                            const float wp = dj != 0.f ? w4[e] / dj : 0.f;
-                            img[wimg_off<D>(j, k) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(wp));
-                        }
-                    }
-                    __threadfence();
-                    __syncthreads();
-                    if (tid == 0) st_release_gpu(p.flags + s, 1u);
-                    // the next softmax rewrites the lower block of the A tile
-                }
-                continue;
-            }
-            // FULL: W' = Delta^{-1} W straight from TMEM into the pass-2 operand image
-            {
-                float v[32], dj;
-                tmem_ld32(trow + LY::colD, v);
-                tmem_ld_wait();
-                dj = v[0];
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    tmem_ld32(trow + LY::colW + q * 32, v);
-                    tmem_ld_wait();
-                    if (row < MP) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float wp = dj != 0.f ? v[i] / dj : 0.f;
-                            *reinterpret_cast<uint16_t *>(sW + wimg_off<D>(row, q * 32 + i)) =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(wp));
-                        }
+                const unsigned nx = vload(p.next);
+                if (nx < n1 && nx / (unsigned)p.C1 < h + (unsigned)p.K) {
+                    const unsigned u = atomicAdd(p.next, 1u);
+                    if (u < n1) {
+                        const int so = (int)(u / (unsigned)p.C1);
+                        it = {0, slice_of(so, p), (int)(u - (unsigned)so * p.C1)};
+                        return 1;
                     }
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncthreads();
-            }
-        } else {
-            // P2: wait for the slice's W' (published by another CTA), copy it on chip
-            if (tid == 0) {
-                const uint64_t t0 = globaltimer_ns();
-                while (ld_acquire_gpu(p.flags + s) == 0u) {
-                    if (globaltimer_ns() - t0 > kWaitNs) {
-                        ok = false;
+                return 0;
+            };
+            uint64_t idle_since = 0;
+            uint32_t backoff = 256;
+            bool idle = false;
+            while (ok) {
+                Item it;
+                const int r = claim(it);
+                if (r == 0) {  // the remaining P2 chunks wait for reductions still running
+                    if (!idle) {
+                        idle = true;
+                        idle_since = globaltimer_ns();
+                    }
+                    if (!flushed) {
+                        ok = push(Item{kFlush, 0, 0});
+                        if (ok && has_pend_v) ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
+                        has_pend_v = false;
+                        flushed = true;
+                    }
+                    if (*s_abort) break;
+                    if (globaltimer_ns() - idle_since > kWaitNs) {
+                        *s_abort = 1;
                         atomicOr(&g_umma_error, 2u);
                         break;
                     }
-                    __nanosleep(128);
+                    __nanosleep(backoff);
+                    backoff = backoff < 8192 ? 2 * backoff : 8192;
+                    continue;
+                }
+                backoff = 256;
+                idle = false;
+                if (r < 0) {
+                    ok = push(Item{kEnd, 0, 0});
+                    break;
+                }
+                if (!push(it)) break;
+                flushed = false;
+                const int h = it.slice % p.heads;
+                if (h != u_head) {  // U load number nu goes to buffer nu % NU
+                    const int ub = (int)(nu % NU);
+                    if (!wait(u_empty + ub, ((nu / NU) & 1u) ^ 1u)) break;
+                    mbar_arrive_expect_tx(u_full + ub, LY::kUB);
+#pragma unroll
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(sU + ub * LY::kUB + b * MP * 128, &tu, u_full + ub, 64 * b, 0, h, pol_keep);
+                    u_head = h;
+                    ++nu;
+                }
+                int a1, b1;
+                const int nt = item_tiles(it, p, a1, b1);
+                for (int idx = 0; idx < nt && ok; ++idx) {
+                    const TileRef tr = tile_at(it, a1, b1, idx);
+                    ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 ? pol_keep : pol_stream);
+                    if (ok && has_pend_v) {
+                        ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
+                        has_pend_v = false;
+                    }
+                    if (tr.kind == 0) {
+                        pend_v = tr;
+                        has_pend_v = true;
+                    }
+                    if (ok && tr.kind == 1 && tr.first) {
+                        if (!tr.full) {  // W' of a split slice: published (claim checked the flag)
+                            ok = wait(w_empty, (wuse & 1u) ^ 1u);
+                            if (ok) {
+                                (void)ld_acquire_gpu(p.flags + 32 * tr.slice);  // orders the image reads
+                                asm volatile("fence.proxy.async.global;" ::: "memory");
+                                mbar_arrive_expect_tx(w_full, LY::kWB);
+                                bulk_load(sW, p.wimg + (size_t)tr.slice * (D * MP), LY::kWB, w_full);
+                            }
+                        }
+                        ++wuse;
+                    }
                 }
             }
-            if (__syncthreads_or(!ok)) goto abort;
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.wimg + (size_t)s * (D * MP));
-            for (int i = tid; i < D * MP * 2 / 16; i += kThreads)
-                reinterpret_cast<uint4 *>(sW)[i] = __ldcg(src + i);
-            fence_proxy_async_smem();
-            __syncthreads();
+            if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
         }
+    } else if (warp == 5) {
+        // =========================================================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16_f32(128, MP, false, false);
+            constexpr uint32_t kIdW = idesc_bf16_f32(128, D, true, true);
+            constexpr uint32_t kIdD = idesc_bf16_f32(128, 16, true, false);
+            constexpr uint32_t kIdH = idesc_bf16_f32(128, D, false, false);
+            const uint32_t sUa = smem_u32(sU), sAa = smem_u32(sA), sWa = smem_u32(sW);
+            const uint32_t sRa = smem_u32(sRing), sOa = smem_u32(sOnes);
+            uint32_t cons = 0, sidx = 0, iq = 0, nu = 0, xk = 0, wph = 0, p2 = 0;
+            uint32_t accuse[2] = {0u, 0u};
+            int prev_head = -1;
+            TileRef pend;
+            bool has_pend = false, ok = true;
 
-        // ------------------------------------------------------------ pass 2
-        {
-            const int a = it.kind == 2 ? 0 : (int)((long long)it.chunk * p.NT / p.C2);
-            const int b = it.kind == 2 ? p.NT : (int)((long long)(it.chunk + 1) * p.NT / p.C2);
-            if (tid == 0) {
-                for (int k = 0; k < NS && a + k < b; ++k) load_q(s, a + k, k);
-                issue_scores(0, 0);
-            }
-            for (int tile = a; tile < b; ++tile) {
-                const int i = tile - a, buf = i & 1;
-                wait(bar_s + buf, ph_s[buf]);          // S(tile) ready (and H(tile-1)'s inputs)
-                tc_fence_after();
-                if (tid == 0) {
-                    if (tile + NS < b) load_q(s, tile + NS, i % NS);  // Q(tile) consumed
-                    if (tile + 1 < b) issue_scores((i + 1) % NS, buf ^ 1);
-                }
-                uint32_t pk[MP / 2];
-                softmax_row<MP>(trow + (buf ? LY::colS1 : LY::colS0), tile * kT + row < p.n, p.m, p.c, pk);
-                if (i > 0) wait(bar_w, ph_w);          // H(tile-1) done: A tile free
-                store_a_row<MP>(pk, sA, row);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                if (__syncthreads_or(!ok)) goto abort;
-                if (tid == 0) {
+            auto do_x = [&](const TileRef &tr) -> bool {
+                const int ab = (int)(xk % NA);
+                if (!wait(a_full + ab, (xk / NA) & 1u)) return false;
+                const uint32_t sAb = sAa + ab * LY::kAB;
+                if (tr.kind == 0) {
+                    const int vs = (int)(cons % NS);
+                    if (!wait(slot_full + vs, (cons / NS) & 1u)) return false;
+                    ++cons;
+                    if (tr.first) {
+                        if (!wait(acc_empty + 0, (accuse[0] & 1u) ^ 1u)) return false;
+                        if (!wait(acc_empty + 1, (accuse[1] & 1u) ^ 1u)) return false;
+                    }
                     tc_fence_after();
-                    const uint32_t hcol = buf ? LY::colH1 : LY::colH0;
+#pragma unroll
+                    for (int kt = 0; kt < kT / 16; ++kt) {
+                        const uint64_t ad = smem_desc_sw128(sAb + kt * 2048, 16384, 1024);
+                        const uint64_t vd = smem_desc_sw128(sRa + vs * LY::kQB + kt * 2048, 16384, 1024);
+                        const uint64_t od = smem_desc_sw128(sOa + (kt >> 2) * 2048 + (kt & 3) * 32, 16, 1024);
+                        const uint32_t acc = (!tr.first || kt > 0) ? 1u : 0u;
+                        umma_bf16(tmem + LY::colB0, ad, vd, kIdW, acc);
+                        umma_bf16(tmem + LY::colB1, ad, od, kIdD, acc);
+                    }
+                    umma_commit(a_empty + ab);
+                    umma_commit(slot_empty + vs);
+                    if (tr.last) {
+                        umma_commit(acc_full + 0);
+                        umma_commit(acc_full + 1);
+                        ++accuse[0];
+                        ++accuse[1];
+                    }
+                } else {
+                    if (tr.first) {
+                        if (!wait(w_full, wph)) return false;
+                        wph ^= 1u;
+                    }
+                    const int hb = (int)(p2 & 1u);
+                    if (!wait(acc_empty + hb, (accuse[hb] & 1u) ^ 1u)) return false;
+                    tc_fence_after();
+                    const uint32_t dcol = hb ? LY::colB1 : LY::colB0;
 #pragma unroll
                     for (int kj = 0; kj < MP / 16; ++kj) {
-                        const uint64_t ad = smem_desc_sw128(sAa + (kj >> 2) * 16384 + (kj & 3) * 32, 16, 1024);
+                        const uint64_t ad = smem_desc_sw128(sAb + (kj >> 2) * 16384 + (kj & 3) * 32, 16, 1024);
                         const uint64_t wd = smem_desc_sw128(sWa + (kj >> 2) * D * 128 + (kj & 3) * 32, 16, 1024);
-                        umma_bf16(tmem + hcol, ad, wd, kIdH, kj > 0);
+                        umma_bf16(tmem + dcol, ad, wd, kIdH, kj > 0);
                     }
-                    umma_commit(bar_w);
+                    umma_commit(a_empty + ab);
+                    umma_commit(acc_full + hb);
+                    ++accuse[hb];
+                    ++p2;
+                    if (tr.last) umma_commit(w_empty);
                 }
-                if (i > 0) {  // store H(tile-1) while the tensor core works on tile
+                ++xk;
+                return true;
+            };
+
+            while (ok) {
+                if (!wait(iq_full + iq % kIQ, (iq / kIQ) & 1u)) break;
+                const Item it = read_item(iq);
+                mbar_arrive(iq_empty + iq % kIQ);
+                ++iq;
+                if (it.kind == kEnd) break;
+                if (it.kind == kFlush) {
+                    if (has_pend && !do_x(pend)) break;
+                    has_pend = false;
+                    continue;
+                }
+                const int h = it.slice % p.heads;
+                if (h != prev_head) {
+                    if (prev_head >= 0) umma_commit(u_empty + (nu - 1) % NU);  // every S on the old U issued
+                    if (!wait(u_full + nu % NU, (nu / NU) & 1u)) break;
+                    ++nu;
+                    prev_head = h;
+                }
+                const uint32_t sUb = sUa + ((nu - 1) % NU) * LY::kUB;
+                int a1, b1;
+                const int nt = item_tiles(it, p, a1, b1);
+                for (int idx = 0; idx < nt && ok; ++idx) {
+                    const TileRef tr = tile_at(it, a1, b1, idx);
+                    const int qslot = (int)(cons % NS);
+                    if (!wait(slot_full + qslot, (cons / NS) & 1u)) { ok = false; break; }
+                    ++cons;
+                    const int sb = (int)(sidx & 1u);
+                    if (!wait(s_empty + sb, ((sidx >> 1) & 1u) ^ 1u)) { ok = false; break; }
                     tc_fence_after();
-                    h_epilogue(s, tile - 1, buf ? LY::colH0 : LY::colH1);
+                    const uint32_t dcol = sb ? LY::colS1 : LY::colS0;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t a = smem_desc_sw128(sRa + qslot * LY::kQB + (kk >> 2) * kT * 128 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b = smem_desc_sw128(sUb + (kk >> 2) * MP * 128 + (kk & 3) * 32, 16, 1024);
+                        umma_bf16(tmem + dcol, a, b, kIdS, kk > 0);
+                    }
+                    umma_commit(s_full + sb);
+                    umma_commit(slot_empty + qslot);
+                    ++sidx;
+                    if (has_pend && !do_x(pend)) { ok = false; break; }
+                    pend = tr;
+                    has_pend = true;
                 }
             }
-            wait(bar_w, ph_w);
-            tc_fence_after();
-            if (__syncthreads_or(!ok)) goto abort;
-            h_epilogue(s, b - 1, ((b - 1 - a) & 1) ? LY::colH1 : LY::colH0);
-            tc_fence_before();
-            if (tid == 0) bulk_wait_group_read0();
-            __syncthreads();
+            if (ok && has_pend) do_x(pend);
         }
-    }
-    goto done;
+    } else {
+        // =========================================================== softmax / epilogue (warps 0-3)
+        const int row = tid;  // TMEM lane = token row of a tile / anchor row of W
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        uint32_t sidx = 0, ause = 0, iq = 0, p2 = 0, wuse = 0;
+        uint32_t accuse[2] = {0u, 0u};
+        TileRef pend;
+        bool has_pend = false, ok = true;
 
-abort:
-    if (tid == 0) atomicOr(&g_umma_error, 1u);
-done:
-    if (tid == 0) bulk_wait_group0();
+        auto arrive4 = [&](uint64_t *bar) {  // one arrival per warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar);
+        };
+
+        auto epilogue = [&](const TileRef &tr) -> bool {
+            if (tr.kind == 1) {
+                // H tile -> bf16 -> global
+                const int hb = (int)(p2 & 1u);
+                if (!wait(acc_full + hb, accuse[hb] & 1u)) return false;
+                tc_fence_after();
+                const uint32_t hcol = hb ? LY::colB1 : LY::colB0;
+                uint32_t pk[D / 2];
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    float v[32];
+                    tmem_ld32(trow + hcol + q * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[q * 16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                }
+                tc_fence_before();
+                arrive4(acc_empty + hb);
+                ++accuse[hb];
+                ++p2;
+                const int tok = tr.tile * kT + row;
+                if (tok < p.n) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(Hout + ((size_t)tr.slice * p.n + tok) * D);
+#pragma unroll
+                    for (int c8 = 0; c8 < D / 8; ++c8)
+                        __stcs(dst + c8, make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]));
+                }
+                return true;
+            }
+            if (!tr.last) return true;
+            // end of a pass-1 phase: W (anchor row `row`, D columns) and Delta in TMEM
+            if (!wait(acc_full + 0, accuse[0] & 1u)) return false;
+            if (!wait(acc_full + 1, accuse[1] & 1u)) return false;
+            tc_fence_after();
+            float v[32];
+            tmem_ld32(trow + LY::colB1, v);
+            tmem_ld_wait();
+            const float dj = v[0];
+            if (!tr.full) {
+                // this chunk's W row -> workspace (before TMEM is released to the next MMAs)
+                if (row < MP) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.part + (((size_t)tr.slice * p.C1 + tr.chunk) * MP + row) * D);
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        tmem_ld32(trow + LY::colB0 + q * 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[q * 8 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
+                    p.pdelta[((size_t)tr.slice * p.C1 + tr.chunk) * MP + row] = dj;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) tmem_ld32(trow + LY::colB0 + q * 32, v);  // keep the warp converged
+                    tmem_ld_wait();
+                }
+                tc_fence_before();
+                arrive4(acc_empty + 0);
+                arrive4(acc_empty + 1);
+                ++accuse[0];
+                ++accuse[1];
+                // Fixed binary tree over the slice's chunks: node (l, i) covers chunks
+                // [i 2^(l+1), (i+1) 2^(l+1)).  The second of its two children to arrive forms
+                // left + right into the left child's slot and climbs on; the first stops.  The
+                // sums - and so W - do not depend on which CTA arrived first.
+                for (int l = 0; (1 << l) < p.C1; ++l) {
+                    const int left = (tr.chunk >> (l + 1)) << (l + 1), right = left + (1 << l);
+                    if (right >= p.C1) continue;  // no right subtree at this level
+                    __threadfence();
+                    wg_sync();
+                    if (row == 0) *s_last = (int)atomicAdd(p.tree + (size_t)tr.slice * p.C1 + (right - 1), 1u);
+                    wg_sync();
+                    if (*s_last == 0) return true;  // first to arrive: the sibling's CTA goes on
+                    __threadfence();
+                    const bool root = (2 << l) >= p.C1;
+                    if (row < MP) {
+                        const size_t rl = ((size_t)tr.slice * p.C1 + left) * MP + row;
+                        const size_t rr = ((size_t)tr.slice * p.C1 + right) * MP + row;
+                        const float dsum = __ldcg(p.pdelta + rl) + __ldcg(p.pdelta + rr);
+                        const float rinv = dsum != 0.f ? 1.f / dsum : 0.f;
+                        const float4 *sl = reinterpret_cast<const float4 *>(p.part + rl * D);
+                        const float4 *sr = reinterpret_cast<const float4 *>(p.part + rr * D);
+                        float4 *dl = reinterpret_cast<float4 *>(p.part + rl * D);
+                        uint16_t *img = p.wimg + (size_t)tr.slice * (D * MP);
+#pragma unroll 1
+                        for (int q = 0; q < D / 32; ++q) {
+                            float4 xl[8], xr[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                xl[i] = __ldcg(sl + q * 8 + i);
+                                xr[i] = __ldcg(sr + q * 8 + i);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float4 w4 = make_float4(xl[i].x + xr[i].x, xl[i].y + xr[i].y, xl[i].z + xr[i].z,
+                                                              xl[i].w + xr[i].w);
+                                if (!root) {
+                                    dl[q * 8 + i] = w4;
+                                } else {  // every chunk is in: W'_jk = W_jk / Delta_j, bf16 image
+                                    const int k = q * 32 + 4 * i;
+                                    img[wimg_off<D>(row, k) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.x * rinv));
+                                    img[wimg_off<D>(row, k + 1) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.y * rinv));
+                                    img[wimg_off<D>(row, k + 2) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.z * rinv));
+                                    img[wimg_off<D>(row, k + 3) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.w * rinv));
+                                }
+                            }
+                        }
+                        if (!root) p.pdelta[rl] = dsum;
+                    }
+                    if (root) {
+                        __threadfence();
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        wg_sync();
+                        if (row == 0) st_release_gpu(p.flags + 32 * tr.slice, 1u);
+                        return true;
+                    }
+                }
+                return true;
+            }
+            // whole slice on chip: W' = Delta^{-1} W straight into the shared operand image
+            if (!wait(w_empty, (wuse & 1u) ^ 1u)) return false;
+            const float rinv = dj != 0.f ? 1.f / dj : 0.f;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                tmem_ld32(trow + LY::colB0 + q * 32, v);
+                tmem_ld_wait();
+                if (row < MP) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        *reinterpret_cast<uint16_t *>(sW + wimg_off<D>(row, q * 32 + i)) =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(v[i] * rinv));
+                }
+            }
+            tc_fence_before();
+            arrive4(acc_empty + 0);
+            arrive4(acc_empty + 1);
+            ++accuse[0];
+            ++accuse[1];
+            fence_proxy_async_smem();
+            wg_sync();
+            if (row == 0) mbar_arrive(w_full);
+            return true;
+        };
+
+        while (ok) {
+            if (!wait(iq_full + iq % kIQ, (iq / kIQ) & 1u)) break;
+            const Item it = read_item(iq);
+            wg_sync();
+            if (row == 0) mbar_arrive(iq_empty + iq % kIQ);
+            ++iq;
+            if (it.kind == kEnd) break;
+            if (it.kind == kFlush) {
+                if (has_pend && !epilogue(pend)) break;
+                has_pend = false;
+                continue;
+            }
+            int a1, b1;
+            const int nt = item_tiles(it, p, a1, b1);
+            for (int idx = 0; idx < nt && ok; ++idx) {
+                const TileRef tr = tile_at(it, a1, b1, idx);
+                const int sb = (int)(sidx & 1u);
+                if (!wait(s_full + sb, (sidx >> 1) & 1u)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t pk[MP / 2];
+                softmax_row<MP>(trow + (sb ? LY::colS1 : LY::colS0), tr.tile * kT + row < p.n, p.m, p.c, pk);
+                tc_fence_before();
+                arrive4(s_empty + sb);
+                ++sidx;
+                const int ab = (int)(ause % NA);
+                if (!wait(a_empty + ab, ((ause / NA) & 1u) ^ 1u)) { ok = false; break; }
+                uint8_t *sAb = sA + ab * LY::kAB;
+#pragma unroll
+                for (int c8 = 0; c8 < MP / 8; ++c8)
+                    *reinterpret_cast<uint4 *>(sAb + sw_off(row, c8, kT)) =
+                        make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                fence_proxy_async_smem();
+                arrive4(a_full + ab);
+                ++ause;
+                // the epilogue of the previous tile may write the W' image this tile's pass uses
+                if (has_pend && !epilogue(pend)) { ok = false; break; }
+                if (tr.kind == 1 && tr.first) ++wuse;  // W' uses started so far
+                pend = tr;
+                has_pend = true;
+            }
+        }
+        if (ok && has_pend) epilogue(pend);
+    }
+
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, LY::kTmemCols);
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, LY::kTmemCols);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -560,6 +814,7 @@ bool make_map(CUtensorMap *map, const void *base, int cols, int rows, long long 
 
 template <int D, int MP>
 cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream_t stream) {
+    static_assert(Layout<D, MP>::kSmem <= 227 * 1024, "shared memory");
     using LY = Layout<D, MP>;
     auto kern = anchor_umma_kernel<D, MP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem);
@@ -573,28 +828,35 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
         return e;
     per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
 
-    CUtensorMap tq, tv, tu, th;
+    CUtensorMap tq, tv, tu;
     const long long S = pr.slices();
     if (!make_map(&tq, pr.Q, D, pr.n, S, kT) || !make_map(&tv, pr.V, D, pr.n, S, kT) ||
-        !make_map(&th, pr.H, D, pr.n, S, kT) || !make_map(&tu, pr.U, D, pr.m, pr.heads, MP))
+        !make_map(&tu, pr.U, D, pr.m, pr.heads, MP))
         return cudaErrorInvalidValue;
 
     UParams p;
     p.slices = (int)S;
     p.heads = pr.heads;
+    p.B = pr.B;
     p.n = pr.n;
     p.m = pr.m;
     p.c = pr.scale * 1.4426950408889634f;
     p.NT = pl.NT;
     p.C1 = pl.C1;
     p.C2 = pl.C2;
-    p.total = pl.total_items;
     const int grid = (int)std::min<long long>((long long)sms * per_sm, pl.total_items);
-    p.L = pl.C1 == 1 ? 0 : std::max(1, std::min(p.slices, grid / (pl.C1 + pl.C2) + 2));
     uint8_t *w = static_cast<uint8_t *>(ws);
-    p.ticket = reinterpret_cast<unsigned *>(w);
-    p.counts = reinterpret_cast<unsigned *>(w + 256);
-    p.flags = p.counts + S;
+    // header (zeroed each call): next | head | flags[S] and P2 claim counters[S], one 128-byte
+    // line each | tree arrival counters [S][C1]
+    p.next = reinterpret_cast<unsigned *>(w);
+    p.head = reinterpret_cast<unsigned *>(w + 128);
+    p.flags = reinterpret_cast<unsigned *>(w + 256);
+    p.p2c = p.flags + 32 * S;
+    p.tree = p.p2c + 32 * S;
+    // P1 runs at most K slices ahead of P2, so that the Q of the slices in flight (read in
+    // pass 1, read again in pass 2) fits in a share of L2
+    const double q_slice = (double)pr.n * D * 2;
+    p.K = (int)std::max<double>(2.0, std::min<double>((double)S, kL2QBudget / q_slice));
     uint8_t *after = w + pl.header_bytes;
     p.pdelta = reinterpret_cast<float *>(after);
     p.part = p.pdelta + (size_t)S * pl.C1 * MP;
@@ -602,7 +864,7 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
     if (pl.C1 == 1) p.part = p.pdelta = nullptr, p.wimg = nullptr;
 
     if ((e = cudaMemsetAsync(ws, 0, pl.header_bytes, stream)) != cudaSuccess) return e;
-    kern<<<grid, kThreads, LY::kSmem, stream>>>(tq, tv, tu, th, p);
+    kern<<<grid, kThreads, LY::kSmem, stream>>>(tq, tv, tu, p, static_cast<uint16_t *>(pr.H));
     return cudaGetLastError();
 }
 
@@ -625,9 +887,9 @@ UmmaPlan umma_plan(const Problem &p) {
     }
     pl.C2 = (pl.NT + kUmmaP2Tiles - 1) / kUmmaP2Tiles;
     pl.total_items = (int)(S * (pl.C1 + pl.C2));
-    pl.header_bytes = (256 + 8 * (size_t)S + 1023) / 1024 * 1024;
+    pl.header_bytes = (256 + 2 * 128 * (size_t)S + 4 * (size_t)S * pl.C1 + 1023) / 1024 * 1024;
     pl.workspace_bytes = pl.header_bytes + 4 * (size_t)S * pl.C1 * MP + 4 * (size_t)S * pl.C1 * p.d * MP +
-                         2 * (size_t)S * p.d * MP;
+                         2 * (size_t)S * p.d * MP + 1024;
     return pl;
 }
 
