@@ -45,7 +45,7 @@ constexpr int kT = 128;                         // tokens per tile (UMMA M)
 constexpr int kThreads = 192;                   // warps 0-3 softmax/epilogue, 4 producer, 5 MMA
 constexpr int kIQ = 4;                          // item queue depth
 constexpr uint64_t kWaitNs = 2000000000ull;     // every wait gives up after 2 s
-constexpr double kL2QBudget = 48.0 * 1024 * 1024; // L2 share for Q between its two reads
+constexpr double kL2QBudget = 64.0 * 1024 * 1024; // L2 share for Q between its two reads
 
 struct UParams {
     int slices, heads, B, n, m;
@@ -72,16 +72,17 @@ struct Layout {
     static constexpr int kBarB = 1024;
     static constexpr int kMaxDyn = 227 * 1024 - 1024;  // minus the alignment slack
     // double-buffer the anchors and the A tile when that still leaves a 6-slot ring
-    static constexpr bool kRoomy = (2 * kUB + 2 * kAB + kWB + kOnesB + kBarB + 6 * kQB) <= kMaxDyn;
+    static constexpr bool kRoomy = (2 * kUB + 2 * kAB + 2 * kWB + kOnesB + kBarB + 6 * kQB) <= kMaxDyn;
     static constexpr int kNU = kRoomy ? 2 : 1;
     static constexpr int kNA = kRoomy ? 2 : 1;
-    static constexpr int kFixed = kNU * kUB + kNA * kAB + kWB + kOnesB + kBarB;
+    static constexpr int kNW = kRoomy ? 2 : 1;
+    static constexpr int kFixed = kNU * kUB + kNA * kAB + kNW * kWB + kOnesB + kBarB;
     static constexpr int kSlotsFit = (kMaxDyn - kFixed) / kQB;
     static constexpr int kNSlot = kSlotsFit > 8 ? 8 : kSlotsFit;
     static constexpr int offU = 0;
     static constexpr int offA = offU + kNU * kUB;
     static constexpr int offW = offA + kNA * kAB;
-    static constexpr int offRing = offW + kWB;
+    static constexpr int offRing = offW + kNW * kWB;
     static constexpr int offOnes = offRing + kNSlot * kQB;
     static constexpr int offBar = offOnes + kOnesB;
     static constexpr int kBytes = offBar + kBarB;
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
                    const __grid_constant__ CUtensorMap tu, const UParams p, uint16_t *__restrict__ Hout) {
     using LY = Layout<D, MP>;
-    constexpr int NS = LY::kNSlot, NU = LY::kNU, NA = LY::kNA;
+    constexpr int NS = LY::kNSlot, NU = LY::kNU, NA = LY::kNA, NW = LY::kNW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sU = sm + LY::offU;
@@ -239,11 +240,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *acc_empty = acc_full + 2;          // [2]  (4)       epilogue read it
     uint64_t *u_full = acc_empty + 2;            // [NU] (1 + tx)  U landed
     uint64_t *u_empty = u_full + NU;             // [NU] (1)       MMAs on that U completed
-    uint64_t *w_full = u_empty + NU;             //      (1 [+ tx]) W' image in place
-    uint64_t *w_empty = w_full + 1;              //      (1)       MMAs reading W' completed
-    uint64_t *iq_full = w_empty + 1;             // [kIQ] (1)      item queue
+    uint64_t *w_full = u_empty + NU;             // [NW] (1 [+ tx]) W' image in place
+    uint64_t *w_empty = w_full + NW;             // [NW] (1)       MMAs reading W' completed
+    uint64_t *iq_full = w_empty + NW;            // [kIQ] (1)      item queue
     uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (2)
-    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 * NA + 2 + 2 + 2 * NU + 2 + 2 * kIQ;
+    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 * NA + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ;
     static_assert(kNumBars * 8 + 3 * 4 * kIQ + 64 <= LY::kBarB, "barrier area");
     int *s_items = reinterpret_cast<int *>(bars + kNumBars);           // [kIQ][3]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_items + 3 * kIQ);
@@ -271,8 +272,10 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_init(u_full + i, 1);
             mbar_init(u_empty + i, 1);
         }
-        mbar_init(w_full, 1);
-        mbar_init(w_empty, 1);
+        for (int i = 0; i < NW; ++i) {
+            mbar_init(w_full + i, 1);
+            mbar_init(w_empty + i, 1);
+        }
         for (int i = 0; i < kIQ; ++i) {
             mbar_init(iq_full + i, 1);
             mbar_init(iq_empty + i, 2);
@@ -312,153 +315,198 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     };
 
     if (warp == 4) {
-        // =========================================================== producer
-        if (lane == 0) {
-            const uint64_t pol_keep = policy_evict_last();
-            const uint64_t pol_stream = policy_evict_first();
-            uint32_t ld_seq = 0, iq = 0, wuse = 0, nu = 0;
-            int u_head = -1;
-            TileRef pend_v;
-            bool has_pend_v = false, ok = true, flushed = true;
-            const unsigned n1 = (unsigned)(p.C1 == 1 ? p.slices : p.slices * p.C1);
-            const unsigned n2 = (unsigned)(p.C1 == 1 ? 0 : p.slices * p.C2);
-            auto load_slot = [&](const CUtensorMap *map, int slice, int tile, uint64_t pol) -> bool {
-                const int st = (int)(ld_seq % NS);
-                if (!wait(slot_empty + st, ((ld_seq / NS) & 1u) ^ 1u)) return false;
+        // =========================================================== producer (whole warp:
+        // every lane waits and decides alike; lane 0 issues the copies and the queue writes)
+        constexpr unsigned FULLW = 0xffffffffu;
+        const bool L0 = lane == 0;
+        const uint64_t pol_keep = policy_evict_last();
+        const uint64_t pol_stream = policy_evict_first();
+        uint32_t ld_seq = 0, iq = 0, wuse = 0, nu = 0;
+        int u_head = -1;
+        TileRef pend_v;
+        bool has_pend_v = false, ok = true, flushed = true;
+        const unsigned S = (unsigned)p.slices;
+        const unsigned n1 = (unsigned)(p.C1 == 1 ? p.slices : p.slices * p.C1);
+        const unsigned n2 = (unsigned)(p.C1 == 1 ? 0 : p.slices * p.C2);
+        auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(FULLW, wait(bar, parity)) != 0;
+        };
+        auto load_slot = [&](const CUtensorMap *map, int slice, int tile, uint64_t pol) -> bool {
+            const int st = (int)(ld_seq % NS);
+            if (!wwait(slot_empty + st, ((ld_seq / NS) & 1u) ^ 1u)) return false;
+            if (L0) {
                 mbar_arrive_expect_tx(slot_full + st, LY::kQB);
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b)
                     tma_load_3d(sRing + st * LY::kQB + b * kT * 128, map, slot_full + st, 64 * b, tile * kT, slice, pol);
-                ++ld_seq;
-                return true;
-            };
-            auto push = [&](const Item &it) -> bool {
-                const int qs = (int)(iq % kIQ);
-                if (!wait(iq_empty + qs, ((iq / kIQ) & 1u) ^ 1u)) return false;
+            }
+            ++ld_seq;
+            return true;
+        };
+        auto push = [&](const Item &it) -> bool {
+            const int qs = (int)(iq % kIQ);
+            if (!wwait(iq_empty + qs, ((iq / kIQ) & 1u) ^ 1u)) return false;
+            if (L0) {
                 s_items[3 * qs] = it.kind;
                 s_items[3 * qs + 1] = it.slice;
                 s_items[3 * qs + 2] = it.chunk;
                 mbar_arrive(iq_full + qs);
-                ++iq;
-                return true;
-            };
-            auto vload = [](const unsigned *a) { return *reinterpret_cast<const volatile unsigned *>(a); };
-            // Claim the next item: a P2 chunk of a slice whose W' is published (within a window
-            // of kWin slices from the head), else a P1 chunk if its slice is within K of the head
-            // (or a whole slice).  Readiness is tested with plain loads before any atomic, and
-            // every atomic is an add (no compare-and-swap retry loops).
-            // 1: claimed, 0: nothing claimable yet, -1: no work left.
-            constexpr int kWin = 8;
-            auto claim = [&](Item &it) -> int {
-                if (n2 == 0) {
-                    if (vload(p.next) >= n1) return -1;
-                    const unsigned u = atomicAdd(p.next, 1u);
-                    if (u >= n1) return -1;
-                    it = {2, slice_of((int)u, p), 0};
-                    return 1;
-                }
-                unsigned h = vload(p.head);
-                while (h < (unsigned)p.slices && vload(p.p2c + 32 * slice_of((int)h, p)) >= (unsigned)p.C2) {
-                    atomicMax(p.head, h + 1u);
-                    h = vload(p.head);
-                }
-                if (h >= (unsigned)p.slices) return -1;
-                const unsigned hend = min((unsigned)p.slices, h + (unsigned)kWin);
-                for (unsigned so = h; so < hend; ++so) {
-                    const int sl = slice_of((int)so, p);
-                    if (vload(p.flags + 32 * sl) == 0u || vload(p.p2c + 32 * sl) >= (unsigned)p.C2) continue;
-                    const unsigned u = atomicAdd(p.p2c + 32 * sl, 1u);
-                    if (u < (unsigned)p.C2) {
-                        it = {1, sl, (int)u};
-                        return 1;
+            }
+            ++iq;
+            return true;
+        };
+        auto vload = [](const unsigned *a) { return *reinterpret_cast<const volatile unsigned *>(a); };
+        // Claim the next item: a P2 chunk of a slice whose W' is published (the 32 lanes test
+        // 32 slices from the head at once, with plain loads), else a P1 chunk if its slice is
+        // within K of the head, or a whole slice.  Every atomic is an add or a max: no
+        // compare-and-swap retries.  1: claimed, 0: nothing claimable yet, -1: no work left.
+        auto claim = [&](Item &it) -> int {
+            int r = 0;
+            unsigned u = 0;
+            if (n2 == 0) {
+                if (L0) {
+                    if (vload(p.next) >= n1) {
+                        r = -1;
+                    } else {
+                        u = atomicAdd(p.next, 1u);
+                        r = u < n1 ? 1 : -1;
                     }
                 }
-                const unsigned nx = vload(p.next);
-                if (nx < n1 && nx / (unsigned)p.C1 < h + (unsigned)p.K) {
-                    const unsigned u = atomicAdd(p.next, 1u);
-                    if (u < n1) {
-                        const int so = (int)(u / (unsigned)p.C1);
-                        it = {0, slice_of(so, p), (int)(u - (unsigned)so * p.C1)};
-                        return 1;
-                    }
+                r = __shfl_sync(FULLW, r, 0);
+                u = __shfl_sync(FULLW, u, 0);
+                if (r == 1) it = {2, slice_of((int)u, p), 0};
+                return r;
+            }
+            unsigned h = __shfl_sync(FULLW, L0 ? vload(p.head) : 0u, 0);
+            for (;;) {
+                if (h >= S) return -1;
+                const unsigned so = h + (unsigned)lane;
+                bool exhausted = true, ready = false;
+                int sl = 0;
+                if (so < S) {
+                    sl = slice_of((int)so, p);
+                    exhausted = vload(p.p2c + 32 * sl) >= (unsigned)p.C2;
+                    ready = !exhausted && vload(p.flags + 32 * sl) != 0u;
                 }
-                return 0;
-            };
-            uint64_t idle_since = 0;
-            uint32_t backoff = 256;
-            bool idle = false;
-            while (ok) {
-                Item it;
-                const int r = claim(it);
-                if (r == 0) {  // the remaining P2 chunks wait for reductions still running
-                    if (!idle) {
-                        idle = true;
-                        idle_since = globaltimer_ns();
-                    }
-                    if (!flushed) {
-                        ok = push(Item{kFlush, 0, 0});
-                        if (ok && has_pend_v) ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
-                        has_pend_v = false;
-                        flushed = true;
-                    }
-                    if (*s_abort) break;
-                    if (globaltimer_ns() - idle_since > kWaitNs) {
-                        *s_abort = 1;
-                        atomicOr(&g_umma_error, 2u);
-                        break;
-                    }
-                    __nanosleep(backoff);
-                    backoff = backoff < 8192 ? 2 * backoff : 8192;
+                const unsigned ex = __ballot_sync(FULLW, exhausted);
+                if (ex == FULLW) {  // all 32 exhausted: move the head on
+                    h = min(h + 32u, S);
+                    if (L0) atomicMax(p.head, h);
                     continue;
                 }
-                backoff = 256;
-                idle = false;
-                if (r < 0) {
-                    ok = push(Item{kEnd, 0, 0});
+                const unsigned nh = h + (unsigned)(__ffs(~ex) - 1);
+                if (nh > h && L0) atomicMax(p.head, nh);
+                h = nh;
+                unsigned rm = __ballot_sync(FULLW, ready);
+                while (rm) {
+                    const int ln = __ffs(rm) - 1;
+                    unsigned got = 0;
+                    if (lane == ln) got = atomicAdd(p.p2c + 32 * sl, 1u);
+                    got = __shfl_sync(FULLW, got, ln);
+                    const int slr = __shfl_sync(FULLW, sl, ln);
+                    if (got < (unsigned)p.C2) {
+                        it = {1, slr, (int)got};
+                        return 1;
+                    }
+                    rm &= rm - 1u;
+                }
+                break;
+            }
+            if (L0) {
+                const unsigned nx = vload(p.next);
+                if (nx < n1 && nx / (unsigned)p.C1 < h + (unsigned)p.K) {
+                    u = atomicAdd(p.next, 1u);
+                    r = u < n1 ? 1 : 0;
+                }
+            }
+            r = __shfl_sync(FULLW, r, 0);
+            u = __shfl_sync(FULLW, u, 0);
+            if (r == 1) {
+                const int so = (int)(u / (unsigned)p.C1);
+                it = {0, slice_of(so, p), (int)(u - (unsigned)so * p.C1)};
+                return 1;
+            }
+            return 0;
+        };
+        uint64_t idle_since = 0;
+        uint32_t backoff = 256;
+        bool idle = false;
+        while (ok) {
+            Item it;
+            const int r = claim(it);
+            if (r == 0) {  // the remaining P2 chunks wait for reductions still running
+                if (!idle) {
+                    idle = true;
+                    idle_since = globaltimer_ns();
+                }
+                if (!flushed) {
+                    ok = push(Item{kFlush, 0, 0});
+                    if (ok && has_pend_v) ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
+                    has_pend_v = false;
+                    flushed = true;
+                }
+                const bool give_up = __any_sync(FULLW, *s_abort != 0 || globaltimer_ns() - idle_since > kWaitNs);
+                if (give_up) {
+                    if (L0 && !*s_abort) {
+                        *s_abort = 1;
+                        atomicOr(&g_umma_error, 2u);
+                    }
                     break;
                 }
-                if (!push(it)) break;
-                flushed = false;
-                const int h = it.slice % p.heads;
-                if (h != u_head) {  // U load number nu goes to buffer nu % NU
-                    const int ub = (int)(nu % NU);
-                    if (!wait(u_empty + ub, ((nu / NU) & 1u) ^ 1u)) break;
+                __nanosleep(backoff);
+                backoff = backoff < 8192 ? 2 * backoff : 8192;
+                continue;
+            }
+            backoff = 256;
+            idle = false;
+            if (r < 0) {
+                ok = push(Item{kEnd, 0, 0});
+                break;
+            }
+            if (!push(it)) break;
+            flushed = false;
+            const int h = it.slice % p.heads;
+            if (h != u_head) {  // U load number nu goes to buffer nu % NU
+                const int ub = (int)(nu % NU);
+                if (!wwait(u_empty + ub, ((nu / NU) & 1u) ^ 1u)) break;
+                if (L0) {
                     mbar_arrive_expect_tx(u_full + ub, LY::kUB);
 #pragma unroll
                     for (int b = 0; b < D / 64; ++b)
                         tma_load_3d(sU + ub * LY::kUB + b * MP * 128, &tu, u_full + ub, 64 * b, 0, h, pol_keep);
-                    u_head = h;
-                    ++nu;
                 }
-                int a1, b1;
-                const int nt = item_tiles(it, p, a1, b1);
-                for (int idx = 0; idx < nt && ok; ++idx) {
-                    const TileRef tr = tile_at(it, a1, b1, idx);
-                    ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 ? pol_keep : pol_stream);
-                    if (ok && has_pend_v) {
-                        ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
-                        has_pend_v = false;
-                    }
-                    if (tr.kind == 0) {
-                        pend_v = tr;
-                        has_pend_v = true;
-                    }
-                    if (ok && tr.kind == 1 && tr.first) {
-                        if (!tr.full) {  // W' of a split slice: published (claim checked the flag)
-                            ok = wait(w_empty, (wuse & 1u) ^ 1u);
-                            if (ok) {
-                                (void)ld_acquire_gpu(p.flags + 32 * tr.slice);  // orders the image reads
-                                asm volatile("fence.proxy.async.global;" ::: "memory");
-                                mbar_arrive_expect_tx(w_full, LY::kWB);
-                                bulk_load(sW, p.wimg + (size_t)tr.slice * (D * MP), LY::kWB, w_full);
-                            }
+                u_head = h;
+                ++nu;
+            }
+            int a1, b1;
+            const int nt = item_tiles(it, p, a1, b1);
+            for (int idx = 0; idx < nt && ok; ++idx) {
+                const TileRef tr = tile_at(it, a1, b1, idx);
+                ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 ? pol_keep : pol_stream);
+                if (ok && has_pend_v) {
+                    ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
+                    has_pend_v = false;
+                }
+                if (tr.kind == 0) {
+                    pend_v = tr;
+                    has_pend_v = true;
+                }
+                if (ok && tr.kind == 1 && tr.first) {
+                    if (!tr.full) {  // W' of a split slice: published (claim checked the flag)
+                        const int wb = (int)(wuse % NW);
+                        ok = wwait(w_empty + wb, ((wuse / NW) & 1u) ^ 1u);
+                        if (ok && L0) {
+                            (void)ld_acquire_gpu(p.flags + 32 * tr.slice);  // orders the image reads
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            mbar_arrive_expect_tx(w_full + wb, LY::kWB);
+                            bulk_load(sW + wb * LY::kWB, p.wimg + (size_t)tr.slice * (D * MP), LY::kWB, w_full + wb);
                         }
-                        ++wuse;
                     }
+                    ++wuse;
                 }
             }
-            if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
         }
+        if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
     } else if (warp == 5) {
         // =========================================================== MMA issuer
         if (lane == 0) {
@@ -468,7 +516,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             constexpr uint32_t kIdH = idesc_bf16_f32(128, D, false, false);
             const uint32_t sUa = smem_u32(sU), sAa = smem_u32(sA), sWa = smem_u32(sW);
             const uint32_t sRa = smem_u32(sRing), sOa = smem_u32(sOnes);
-            uint32_t cons = 0, sidx = 0, iq = 0, nu = 0, xk = 0, wph = 0, p2 = 0;
+            uint32_t cons = 0, sidx = 0, iq = 0, nu = 0, xk = 0, wuse = 0, p2 = 0;
             uint32_t accuse[2] = {0u, 0u};
             int prev_head = -1;
             TileRef pend;
@@ -505,10 +553,12 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         ++accuse[1];
                     }
                 } else {
+                    const int wb = (int)((tr.first ? wuse : wuse - 1u) % NW);  // this pass-2 phase's W'
                     if (tr.first) {
-                        if (!wait(w_full, wph)) return false;
-                        wph ^= 1u;
+                        if (!wait(w_full + wb, (wuse / NW) & 1u)) return false;
+                        ++wuse;
                     }
+                    const uint32_t sWb = sWa + wb * LY::kWB;
                     const int hb = (int)(p2 & 1u);
                     if (!wait(acc_empty + hb, (accuse[hb] & 1u) ^ 1u)) return false;
                     tc_fence_after();
@@ -516,14 +566,14 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
                     for (int kj = 0; kj < MP / 16; ++kj) {
                         const uint64_t ad = smem_desc_sw128(sAb + (kj >> 2) * 16384 + (kj & 3) * 32, 16, 1024);
-                        const uint64_t wd = smem_desc_sw128(sWa + (kj >> 2) * D * 128 + (kj & 3) * 32, 16, 1024);
+                        const uint64_t wd = smem_desc_sw128(sWb + (kj >> 2) * D * 128 + (kj & 3) * 32, 16, 1024);
                         umma_bf16(tmem + dcol, ad, wd, kIdH, kj > 0);
                     }
                     umma_commit(a_empty + ab);
                     umma_commit(acc_full + hb);
                     ++accuse[hb];
                     ++p2;
-                    if (tr.last) umma_commit(w_empty);
+                    if (tr.last) umma_commit(w_empty + wb);
                 }
                 ++xk;
                 return true;
@@ -709,7 +759,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 return true;
             }
             // whole slice on chip: W' = Delta^{-1} W straight into the shared operand image
-            if (!wait(w_empty, (wuse & 1u) ^ 1u)) return false;
+            const int wb = (int)(wuse % NW);
+            uint8_t *sWb = sW + wb * LY::kWB;
+            if (!wait(w_empty + wb, ((wuse / NW) & 1u) ^ 1u)) return false;
             const float rinv = dj != 0.f ? 1.f / dj : 0.f;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
@@ -718,7 +770,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 if (row < MP) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        *reinterpret_cast<uint16_t *>(sW + wimg_off<D>(row, q * 32 + i)) =
+                        *reinterpret_cast<uint16_t *>(sWb + wimg_off<D>(row, q * 32 + i)) =
                             __bfloat16_as_ushort(__float2bfloat16_rn(v[i] * rinv));
                 }
             }
@@ -729,7 +781,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             ++accuse[1];
             fence_proxy_async_smem();
             wg_sync();
-            if (row == 0) mbar_arrive(w_full);
+            if (row == 0) mbar_arrive(w_full + wb);
             return true;
         };
 
