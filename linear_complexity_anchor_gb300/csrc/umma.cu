@@ -42,7 +42,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 128;                         // tokens per tile (UMMA M)
-constexpr int kThreads = 192;                   // warps 0-3 softmax/epilogue, 4 producer, 5 MMA
+constexpr int kThreads = 320;  // warps 0-3 softmax, 4-7 epilogue, 8 producer, 9 MMA
 constexpr int kIQ = 4;                          // item queue depth
 constexpr uint64_t kWaitNs = 2000000000ull;     // every wait gives up after 2 s
 constexpr double kL2QBudget = 64.0 * 1024 * 1024; // L2 share for Q between its two reads
@@ -179,7 +179,9 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-__device__ __forceinline__ void wg_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barriers of the two 4-warp groups (id 0 is __syncthreads)
+__device__ __forceinline__ void sm_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void ep_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // Row softmax of one S row (TMEM lane = this thread's token), packed to bf16 pairs.
 // Rows past the end of the slice become zero rows; anchors >= m get probability 0.
@@ -243,7 +245,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *w_full = u_empty + NU;             // [NW] (1 [+ tx]) W' image in place
     uint64_t *w_empty = w_full + NW;             // [NW] (1)       MMAs reading W' completed
     uint64_t *iq_full = w_empty + NW;            // [kIQ] (1)      item queue
-    uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (2)
+    uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (3)
     constexpr int kNumBars = 2 * NS + 2 + 2 + 2 * NA + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ;
     static_assert(kNumBars * 8 + 3 * 4 * kIQ + 64 <= LY::kBarB, "barrier area");
     int *s_items = reinterpret_cast<int *>(bars + kNumBars);           // [kIQ][3]
@@ -278,7 +280,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         for (int i = 0; i < kIQ; ++i) {
             mbar_init(iq_full + i, 1);
-            mbar_init(iq_empty + i, 2);
+            mbar_init(iq_empty + i, 3);
         }
         *s_abort = 0;
         fence_mbar_init();
@@ -288,7 +290,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
     for (int i = tid; i < LY::kOnesB / 4; i += kThreads) reinterpret_cast<uint32_t *>(sOnes)[i] = 0x3F803F80u;
     for (int i = tid; i < NA * LY::kAB / 16; i += kThreads) reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0, 0, 0, 0);
-    if (warp == 5) tmem_alloc(s_tmem, LY::kTmemCols);
+    if (warp == 9) tmem_alloc(s_tmem, LY::kTmemCols);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -314,7 +316,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         return {e[0], e[1], e[2]};
     };
 
-    if (warp == 4) {
+    if (warp == 8) {
         // =========================================================== producer (whole warp:
         // every lane waits and decides alike; lane 0 issues the copies and the queue writes)
         constexpr unsigned FULLW = 0xffffffffu;
@@ -507,7 +509,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
         }
         if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // =========================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(128, MP, false, false);
@@ -625,20 +627,62 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
             if (ok && has_pend) do_x(pend);
         }
-    } else {
-        // =========================================================== softmax / epilogue (warps 0-3)
-        const int row = tid;  // TMEM lane = token row of a tile / anchor row of W
+    } else if (warp < 4) {
+        // =========================================================== softmax (warps 0-3)
+        const int row = tid;  // TMEM lane = token row of the tile
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        uint32_t sidx = 0, ause = 0, iq = 0, p2 = 0, wuse = 0;
-        uint32_t accuse[2] = {0u, 0u};
-        TileRef pend;
-        bool has_pend = false, ok = true;
-
+        uint32_t sidx = 0, ause = 0, iq = 0;
+        bool ok = true;
         auto arrive4 = [&](uint64_t *bar) {  // one arrival per warp
             __syncwarp();
             if (lane == 0) mbar_arrive(bar);
         };
-
+        while (ok) {
+            if (!wait(iq_full + iq % kIQ, (iq / kIQ) & 1u)) break;
+            const Item it = read_item(iq);
+            sm_sync();
+            if (row == 0) mbar_arrive(iq_empty + iq % kIQ);
+            ++iq;
+            if (it.kind == kEnd) break;
+            if (it.kind == kFlush) continue;
+            int a1, b1;
+            const int nt = item_tiles(it, p, a1, b1);
+            for (int idx = 0; idx < nt && ok; ++idx) {
+                const TileRef tr = tile_at(it, a1, b1, idx);
+                const int sb = (int)(sidx & 1u);
+                if (!wait(s_full + sb, (sidx >> 1) & 1u)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t pk[MP / 2];
+                softmax_row<MP>(trow + (sb ? LY::colS1 : LY::colS0), tr.tile * kT + row < p.n, p.m, p.c, pk);
+                tc_fence_before();
+                arrive4(s_empty + sb);
+                ++sidx;
+                const int ab = (int)(ause % NA);
+                if (!wait(a_empty + ab, ((ause / NA) & 1u) ^ 1u)) { ok = false; break; }
+                uint8_t *sAb = sA + ab * LY::kAB;
+#pragma unroll
+                for (int c8 = 0; c8 < MP / 8; ++c8)
+                    *reinterpret_cast<uint4 *>(sAb + sw_off(row, c8, kT)) =
+                        make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                fence_proxy_async_smem();
+                arrive4(a_full + ab);
+                ++ause;
+            }
+        }
+    } else {
+        // =========================================================== epilogue (warps 4-7)
+        // H tiles out of TMEM to global; at the end of a pass-1 phase, the chunk partial and
+        // its reduction (or, for whole slices, W' straight into shared memory).
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // TMEM lane: token row (H) / anchor row (W)
+        const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+        uint32_t iq = 0, p2 = 0, wuse = 0;
+        uint32_t accuse[2] = {0u, 0u};
+        bool ok = true;
+        auto arrive4 = [&](uint64_t *bar) {  // one arrival per warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar);
+        };
         auto epilogue = [&](const TileRef &tr) -> bool {
             if (tr.kind == 1) {
                 // H tile -> bf16 -> global
@@ -708,9 +752,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     const int left = (tr.chunk >> (l + 1)) << (l + 1), right = left + (1 << l);
                     if (right >= p.C1) continue;  // no right subtree at this level
                     __threadfence();
-                    wg_sync();
+                    ep_sync();
                     if (row == 0) *s_last = (int)atomicAdd(p.tree + (size_t)tr.slice * p.C1 + (right - 1), 1u);
-                    wg_sync();
+                    ep_sync();
                     if (*s_last == 0) return true;  // first to arrive: the sibling's CTA goes on
                     __threadfence();
                     const bool root = (2 << l) >= p.C1;
@@ -751,7 +795,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     if (root) {
                         __threadfence();
                         asm volatile("fence.proxy.async.global;" ::: "memory");
-                        wg_sync();
+                        ep_sync();
                         if (row == 0) st_release_gpu(p.flags + 32 * tr.slice, 1u);
                         return true;
                     }
@@ -780,7 +824,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             ++accuse[0];
             ++accuse[1];
             fence_proxy_async_smem();
-            wg_sync();
+            ep_sync();
             if (row == 0) mbar_arrive(w_full + wb);
             return true;
         };
@@ -788,50 +832,24 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         while (ok) {
             if (!wait(iq_full + iq % kIQ, (iq / kIQ) & 1u)) break;
             const Item it = read_item(iq);
-            wg_sync();
+            ep_sync();
             if (row == 0) mbar_arrive(iq_empty + iq % kIQ);
             ++iq;
             if (it.kind == kEnd) break;
-            if (it.kind == kFlush) {
-                if (has_pend && !epilogue(pend)) break;
-                has_pend = false;
-                continue;
-            }
+            if (it.kind == kFlush) continue;
             int a1, b1;
             const int nt = item_tiles(it, p, a1, b1);
             for (int idx = 0; idx < nt && ok; ++idx) {
                 const TileRef tr = tile_at(it, a1, b1, idx);
-                const int sb = (int)(sidx & 1u);
-                if (!wait(s_full + sb, (sidx >> 1) & 1u)) { ok = false; break; }
-                tc_fence_after();
-                uint32_t pk[MP / 2];
-                softmax_row<MP>(trow + (sb ? LY::colS1 : LY::colS0), tr.tile * kT + row < p.n, p.m, p.c, pk);
-                tc_fence_before();
-                arrive4(s_empty + sb);
-                ++sidx;
-                const int ab = (int)(ause % NA);
-                if (!wait(a_empty + ab, ((ause / NA) & 1u) ^ 1u)) { ok = false; break; }
-                uint8_t *sAb = sA + ab * LY::kAB;
-#pragma unroll
-                for (int c8 = 0; c8 < MP / 8; ++c8)
-                    *reinterpret_cast<uint4 *>(sAb + sw_off(row, c8, kT)) =
-                        make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-                fence_proxy_async_smem();
-                arrive4(a_full + ab);
-                ++ause;
-                // the epilogue of the previous tile may write the W' image this tile's pass uses
-                if (has_pend && !epilogue(pend)) { ok = false; break; }
+                if (!epilogue(tr)) { ok = false; break; }
                 if (tr.kind == 1 && tr.first) ++wuse;  // W' uses started so far
-                pend = tr;
-                has_pend = true;
             }
         }
-        if (ok && has_pend) epilogue(pend);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, LY::kTmemCols);
     }
