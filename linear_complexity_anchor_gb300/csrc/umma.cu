@@ -60,6 +60,7 @@ struct UParams {
     unsigned *next;           // next P1 chunk (or whole slice) to claim
     unsigned *head;           // first slice (schedule order) whose P2 chunks are not all claimed
     int K;                    // P1 may run at most K slices ahead of the P2 head
+    int p1first;              // every slice's Q fits the L2 budget: take P1 chunks before P2
 };
 
 template <int D, int MP>
@@ -302,7 +303,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (mbar_try_wait(bar, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
         for (;;) {
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
             if (*s_abort) return false;
             if (globaltimer_ns() - t0 > kWaitNs) {
                 *s_abort = 1;
@@ -379,6 +380,25 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 if (r == 1) it = {2, slice_of((int)u, p), 0};
                 return r;
             }
+            auto try_p1 = [&](unsigned limit) -> bool {  // P1 chunk whose slice is below `limit`
+                int got = 0;
+                unsigned v = 0;
+                if (L0) {
+                    const unsigned nx = vload(p.next);
+                    if (nx < n1 && nx / (unsigned)p.C1 < limit) {
+                        v = atomicAdd(p.next, 1u);
+                        got = v < n1 ? 1 : 0;
+                    }
+                }
+                got = __shfl_sync(FULLW, got, 0);
+                v = __shfl_sync(FULLW, v, 0);
+                if (got) {
+                    const int so = (int)(v / (unsigned)p.C1);
+                    it = {0, slice_of(so, p), (int)(v - (unsigned)so * p.C1)};
+                }
+                return got != 0;
+            };
+            if (p.p1first && try_p1(S)) return 1;
             unsigned h = __shfl_sync(FULLW, L0 ? vload(p.head) : 0u, 0);
             for (;;) {
                 if (h >= S) return -1;
@@ -414,28 +434,24 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
                 break;
             }
-            if (L0) {
-                const unsigned nx = vload(p.next);
-                if (nx < n1 && nx / (unsigned)p.C1 < h + (unsigned)p.K) {
-                    u = atomicAdd(p.next, 1u);
-                    r = u < n1 ? 1 : 0;
-                }
-            }
-            r = __shfl_sync(FULLW, r, 0);
-            u = __shfl_sync(FULLW, u, 0);
-            if (r == 1) {
-                const int so = (int)(u / (unsigned)p.C1);
-                it = {0, slice_of(so, p), (int)(u - (unsigned)so * p.C1)};
-                return 1;
-            }
+            if (!p.p1first && try_p1(h + (unsigned)p.K)) return 1;
             return 0;
         };
         uint64_t idle_since = 0;
         uint32_t backoff = 256;
         bool idle = false;
+        Item ahead;
+        bool have_ahead = false;
         while (ok) {
             Item it;
-            const int r = claim(it);
+            int r;
+            if (have_ahead) {
+                it = ahead;
+                have_ahead = false;
+                r = 1;
+            } else {
+                r = claim(it);
+            }
             if (r == 0) {  // the remaining P2 chunks wait for reductions still running
                 if (!idle) {
                     idle = true;
@@ -485,6 +501,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             for (int idx = 0; idx < nt && ok; ++idx) {
                 const TileRef tr = tile_at(it, a1, b1, idx);
                 ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 ? pol_keep : pol_stream);
+                // claim the next item now, while the ring is still full of this one's tiles
+                if (idx == 0 && !have_ahead) have_ahead = claim(ahead) == 1;
                 if (ok && has_pend_v) {
                     ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
                     has_pend_v = false;
@@ -767,22 +785,23 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         const float4 *sr = reinterpret_cast<const float4 *>(p.part + rr * D);
                         float4 *dl = reinterpret_cast<float4 *>(p.part + rl * D);
                         uint16_t *img = p.wimg + (size_t)tr.slice * (D * MP);
+                        constexpr int QV = D / 8;  // float4 per half row
 #pragma unroll 1
-                        for (int q = 0; q < D / 32; ++q) {
-                            float4 xl[8], xr[8];
+                        for (int q = 0; q < 2; ++q) {
+                            float4 xl[QV], xr[QV];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                xl[i] = __ldcg(sl + q * 8 + i);
-                                xr[i] = __ldcg(sr + q * 8 + i);
+                            for (int i = 0; i < QV; ++i) {
+                                xl[i] = __ldcg(sl + q * QV + i);
+                                xr[i] = __ldcg(sr + q * QV + i);
                             }
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
+                            for (int i = 0; i < QV; ++i) {
                                 const float4 w4 = make_float4(xl[i].x + xr[i].x, xl[i].y + xr[i].y, xl[i].z + xr[i].z,
                                                               xl[i].w + xr[i].w);
                                 if (!root) {
-                                    dl[q * 8 + i] = w4;
+                                    dl[q * QV + i] = w4;
                                 } else {  // every chunk is in: W'_jk = W_jk / Delta_j, bf16 image
-                                    const int k = q * 32 + 4 * i;
+                                    const int k = q * (D / 2) + 4 * i;
                                     img[wimg_off<D>(row, k) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.x * rinv));
                                     img[wimg_off<D>(row, k + 1) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.y * rinv));
                                     img[wimg_off<D>(row, k + 2) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.z * rinv));
@@ -927,6 +946,7 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
     // pass 1, read again in pass 2) fits in a share of L2
     const double q_slice = (double)pr.n * D * 2;
     p.K = (int)std::max<double>(2.0, std::min<double>((double)S, kL2QBudget / q_slice));
+    p.p1first = p.K >= S ? 1 : 0;
     uint8_t *after = w + pl.header_bytes;
     p.pdelta = reinterpret_cast<float *>(after);
     p.part = p.pdelta + (size_t)S * pl.C1 * MP;
