@@ -63,8 +63,9 @@ cudaError_t launch_simt_split(const Problem &p, int splits, float *workspace, cu
 
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA
-constexpr int kUmmaP1Tiles = 8;      // target tiles per pass-1 chunk
-constexpr int kUmmaP2Tiles = 4;      // target tiles per pass-2 chunk
+constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)
+constexpr int kUmmaP2Tiles = 8;      // tiles per pass-2 chunk (halved while items are too few)
+constexpr int kUmmaMinTiles = 4;     // smallest chunk either pass is cut into
 struct UmmaPlan {
     int MP = 0;              // anchors padded to 64 or 128
     int NT = 0;              // 128-token tiles per slice

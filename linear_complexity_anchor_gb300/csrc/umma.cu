@@ -45,13 +45,13 @@ constexpr int kT = 128;                         // tokens per tile (UMMA M)
 constexpr int kThreads = 320;  // warps 0-3 softmax, 4-7 epilogue, 8 producer, 9 MMA
 constexpr int kIQ = 4;                          // item queue depth
 constexpr uint64_t kWaitNs = 2000000000ull;     // every wait gives up after 2 s
-constexpr double kL2QBudget = 64.0 * 1024 * 1024; // L2 share for Q between its two reads
+constexpr double kL2QBudget = 96.0 * 1024 * 1024; // L2 share for Q between its two reads
 
 struct UParams {
     int slices, heads, B, n, m;
     float c;                  // scale * log2(e)
     int NT, C1, C2;           // tiles per slice, P1 / P2 chunks per slice (C1 == 1: whole slices)
-    float *part;              // [slices][C1][MP][D]  W partials, one row per anchor
+    float *part;              // [slices][C1][D/4][MP][4]  W partials (anchor-interleaved float4)
     float *pdelta;            // [slices][C1][MP]     Delta partials
     uint16_t *wimg;           // [slices][D * MP]     W' operand images (bf16, swizzled)
     unsigned *flags;          // [slices * 32] W' published (one 128-byte line per slice)
@@ -157,21 +157,30 @@ __device__ __forceinline__ TileRef tile_at(const Item &it, int a1, int b1, int i
 }
 
 // byte offset of 16-byte chunk `c` (0 .. cols/8-1) of row `r` in a swizzled [rows][cols]
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 // bf16 tile stored as 64-column blocks of `rows` x 128 bytes
 __device__ __forceinline__ uint32_t sw_off(int r, int c, int rows) {
     return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// byte offset of element (anchor j, column k) in the W' image [D rows][MP anchors]
-template <int D>
-__device__ __forceinline__ uint32_t wimg_off(int j, int k) {
-    return (uint32_t)((j >> 6) * D * 128 + k * 128 + ((((j & 63) >> 3) ^ (k & 7)) << 4) + (j & 7) * 2);
+// The W' operand image holds W'[anchor j][column k] as MP rows of D bf16, in 64-column
+// blocks of MP rows x 128 bytes, 128-byte swizzled (the layout a TMA load of a row-major
+// [MP][D] tile produces): 8 consecutive columns of one anchor are one 16-byte chunk.
+template <int MP>
+__device__ __forceinline__ uint32_t wimg_chunk_off(int j, int c8) {
+    return sw_off(j, c8, MP);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&h);
+// 8 floats -> 8 bf16 (round to nearest even), scaled by r
+__device__ __forceinline__ uint4 pack8_scaled(const float *x, float r) {
+    return make_uint4(pack_bf16x2(x[0] * r, x[1] * r), pack_bf16x2(x[2] * r, x[3] * r),
+                      pack_bf16x2(x[4] * r, x[5] * r), pack_bf16x2(x[6] * r, x[7] * r));
 }
+
 
 // 2^x on the multi-function unit (PTX ex2.approx, flush-to-zero): one instruction.
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -184,38 +193,57 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ void sm_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 __device__ __forceinline__ void ep_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// Row softmax of one S row (TMEM lane = this thread's token), packed to bf16 pairs.
-// Rows past the end of the slice become zero rows; anchors >= m get probability 0.
-// The max and the sum run as 8 interleaved partial chains (fixed order: deterministic).
-template <int MP>
+// Row softmax of one S row (TMEM lane = this thread's token), packed to bf16 pairs:
+// A_i = softmax_j(scale * S_ij) computed as 2^(c * S_ij - c * max_j S_ij) / sum, c = scale *
+// log2(e) > 0, so the scale folds into one fused multiply-add per element.  Rows past the end
+// of the slice become zero rows.  With MASKED, anchors >= m are set to -inf first (their
+// probability is exactly 0); without it every one of the MP columns is a real anchor.
+// Max and sum run as 8 interleaved partial chains in a fixed order (deterministic); the
+// scale, the sum and the normalisation use the paired fp32 instructions.
+template <int MP, bool MASKED>
 __device__ __forceinline__ void softmax_row(uint32_t taddr_s, bool valid, int m, float c, uint32_t (&pk)[MP / 2]) {
     float v[MP];
 #pragma unroll
     for (int q = 0; q < MP / 32; ++q) tmem_ld32(taddr_s + q * 32, v + q * 32);
     tmem_ld_wait();
+    if (MASKED) {
+#pragma unroll
+        for (int j = 0; j < MP; ++j)
+            if (j >= m) v[j] = -INFINITY;
+    }
     float mx8[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+    for (int i = 0; i < 8; ++i) mx8[i] = v[i];
 #pragma unroll
-    for (int j = 0; j < MP; ++j) {
-        v[j] *= c;
-        if (j < m) mx8[j & 7] = fmaxf(mx8[j & 7], v[j]);
+    for (int j = 8; j < MP; j += 16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            mx8[k] = (j + 8 + k < MP) ? max3_f32(mx8[k], v[j + k], v[j + 8 + k]) : fmaxf(mx8[k], v[j + k]);
     }
-    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-    float z8[8];
+    const float mx = fmaxf(max3_f32(mx8[0], mx8[1], mx8[2]), max3_f32(max3_f32(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+    const float nb = -mx * c;
+    const uint64_t c2 = f32x2(c, c), nb2 = f32x2(nb, nb);
+    uint64_t z4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) z8[i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < MP; ++j) {
-        const float e = (j < m) ? ex2_approx(v[j] - mx) : 0.f;
-        v[j] = e;
-        z8[j & 7] += e;
+    for (int j = 0; j < MP; j += 2) {
+        float a, b;
+        f32x2_split(fma_f32x2(f32x2(v[j], v[j + 1]), c2, nb2), a, b);
+        a = ex2_approx(a);
+        b = ex2_approx(b);
+        v[j] = a;
+        v[j + 1] = b;
+        z4[(j >> 1) & 3] = add_f32x2(z4[(j >> 1) & 3], f32x2(a, b));
     }
-    const float z = ((z8[0] + z8[1]) + (z8[2] + z8[3])) + ((z8[4] + z8[5]) + (z8[6] + z8[7]));
-    const float inv = valid ? 1.f / z : 0.f;
+    float za, zb;
+    f32x2_split(add_f32x2(add_f32x2(z4[0], z4[1]), add_f32x2(z4[2], z4[3])), za, zb);
+    const float inv = valid ? 1.f / (za + zb) : 0.f;
+    const uint64_t inv2 = f32x2(inv, inv);
 #pragma unroll
-    for (int j = 0; j < MP / 2; ++j) pk[j] = pack_bf16x2(v[2 * j] * inv, v[2 * j + 1] * inv);
+    for (int j = 0; j < MP / 2; ++j) {
+        float a, b;
+        f32x2_split(mul_f32x2(f32x2(v[2 * j], v[2 * j + 1]), inv2), a, b);
+        pk[j] = pack_bf16x2(a, b);
+    }
 }
 
 template <int D, int MP>
@@ -419,18 +447,23 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 const unsigned nh = h + (unsigned)(__ffs(~ex) - 1);
                 if (nh > h && L0) atomicMax(p.head, nh);
                 h = nh;
-                unsigned rm = __ballot_sync(FULLW, ready);
-                while (rm) {
-                    const int ln = __ffs(rm) - 1;
-                    unsigned got = 0;
-                    if (lane == ln) got = atomicAdd(p.p2c + 32 * sl, 1u);
-                    got = __shfl_sync(FULLW, got, ln);
-                    const int slr = __shfl_sync(FULLW, sl, ln);
-                    if (got < (unsigned)p.C2) {
-                        it = {1, slr, (int)got};
-                        return 1;
+                // ready slices of the head whose U is already in shared memory go first
+                const unsigned rs = __ballot_sync(FULLW, ready && sl % p.heads == u_head);
+                const unsigned rm = __ballot_sync(FULLW, ready);
+                for (unsigned pass = 0; pass < 2; ++pass) {
+                    unsigned rq = pass == 0 ? rs : rm & ~rs;
+                    while (rq) {
+                        const int ln = __ffs(rq) - 1;
+                        unsigned got = 0;
+                        if (lane == ln) got = atomicAdd(p.p2c + 32 * sl, 1u);
+                        got = __shfl_sync(FULLW, got, ln);
+                        const int slr = __shfl_sync(FULLW, sl, ln);
+                        if (got < (unsigned)p.C2) {
+                            it = {1, slr, (int)got};
+                            return 1;
+                        }
+                        rq &= rq - 1u;
                     }
-                    rm &= rm - 1u;
                 }
                 break;
             }
@@ -472,7 +505,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     break;
                 }
                 __nanosleep(backoff);
-                backoff = backoff < 8192 ? 2 * backoff : 8192;
+                backoff = backoff < 1024 ? 2 * backoff : 1024;
                 continue;
             }
             backoff = 256;
@@ -533,7 +566,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             constexpr uint32_t kIdS = idesc_bf16_f32(128, MP, false, false);
             constexpr uint32_t kIdW = idesc_bf16_f32(128, D, true, true);
             constexpr uint32_t kIdD = idesc_bf16_f32(128, 16, true, false);
-            constexpr uint32_t kIdH = idesc_bf16_f32(128, D, false, false);
+            constexpr uint32_t kIdH = idesc_bf16_f32(128, D, false, true);
             const uint32_t sUa = smem_u32(sU), sAa = smem_u32(sA), sWa = smem_u32(sW);
             const uint32_t sRa = smem_u32(sRing), sOa = smem_u32(sOnes);
             uint32_t cons = 0, sidx = 0, iq = 0, nu = 0, xk = 0, wuse = 0, p2 = 0;
@@ -586,7 +619,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
                     for (int kj = 0; kj < MP / 16; ++kj) {
                         const uint64_t ad = smem_desc_sw128(sAb + (kj >> 2) * 16384 + (kj & 3) * 32, 16, 1024);
-                        const uint64_t wd = smem_desc_sw128(sWb + (kj >> 2) * D * 128 + (kj & 3) * 32, 16, 1024);
+                        const uint64_t wd = smem_desc_sw128(sWb + kj * 2048, MP * 128, 1024);
                         umma_bf16(tmem + dcol, ad, wd, kIdH, kj > 0);
                     }
                     umma_commit(a_empty + ab);
@@ -671,7 +704,10 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 if (!wait(s_full + sb, (sidx >> 1) & 1u)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t pk[MP / 2];
-                softmax_row<MP>(trow + (sb ? LY::colS1 : LY::colS0), tr.tile * kT + row < p.n, p.m, p.c, pk);
+                const uint32_t ts = trow + (sb ? LY::colS1 : LY::colS0);
+                const bool valid = tr.tile * kT + row < p.n;
+                if (p.m == MP) softmax_row<MP, false>(ts, valid, p.m, p.c, pk);
+                else softmax_row<MP, true>(ts, valid, p.m, p.c, pk);
                 tc_fence_before();
                 arrive4(s_empty + sb);
                 ++sidx;
@@ -742,14 +778,15 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             if (!tr.full) {
                 // this chunk's W row -> workspace (before TMEM is released to the next MMAs)
                 if (row < MP) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.part + (((size_t)tr.slice * p.C1 + tr.chunk) * MP + row) * D);
+                    // partial layout [D/4][MP] float4: a warp's 32 anchors write 512 contiguous bytes
+                    float4 *dst = reinterpret_cast<float4 *>(p.part + ((size_t)tr.slice * p.C1 + tr.chunk) * MP * D) + row;
 #pragma unroll
                     for (int q = 0; q < D / 32; ++q) {
                         tmem_ld32(trow + LY::colB0 + q * 32, v);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            dst[q * 8 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                            dst[(q * 8 + i) * MP] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     }
                     p.pdelta[((size_t)tr.slice * p.C1 + tr.chunk) * MP + row] = dj;
                 } else {
@@ -777,39 +814,41 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     __threadfence();
                     const bool root = (2 << l) >= p.C1;
                     if (row < MP) {
-                        const size_t rl = ((size_t)tr.slice * p.C1 + left) * MP + row;
-                        const size_t rr = ((size_t)tr.slice * p.C1 + right) * MP + row;
-                        const float dsum = __ldcg(p.pdelta + rl) + __ldcg(p.pdelta + rr);
+                        const size_t dl_ = ((size_t)tr.slice * p.C1 + left) * MP + row;
+                        const size_t dr_ = ((size_t)tr.slice * p.C1 + right) * MP + row;
+                        const float dsum = __ldcg(p.pdelta + dl_) + __ldcg(p.pdelta + dr_);
+                        const float4 *sl = reinterpret_cast<const float4 *>(p.part + ((size_t)tr.slice * p.C1 + left) * MP * D) + row;
+                        const float4 *sr = reinterpret_cast<const float4 *>(p.part + ((size_t)tr.slice * p.C1 + right) * MP * D) + row;
+                        float4 *dl = reinterpret_cast<float4 *>(p.part + ((size_t)tr.slice * p.C1 + left) * MP * D) + row;
                         const float rinv = dsum != 0.f ? 1.f / dsum : 0.f;
-                        const float4 *sl = reinterpret_cast<const float4 *>(p.part + rl * D);
-                        const float4 *sr = reinterpret_cast<const float4 *>(p.part + rr * D);
-                        float4 *dl = reinterpret_cast<float4 *>(p.part + rl * D);
-                        uint16_t *img = p.wimg + (size_t)tr.slice * (D * MP);
-                        constexpr int QV = D / 8;  // float4 per half row
+                        uint8_t *img = reinterpret_cast<uint8_t *>(p.wimg + (size_t)tr.slice * (D * MP));
+                        // 4 groups of D/16 float4 from each side (8-column chunks stay whole)
+                        constexpr int QV = D / 16;
 #pragma unroll 1
-                        for (int q = 0; q < 2; ++q) {
+                        for (int g = 0; g < 4; ++g) {
                             float4 xl[QV], xr[QV];
 #pragma unroll
                             for (int i = 0; i < QV; ++i) {
-                                xl[i] = __ldcg(sl + q * QV + i);
-                                xr[i] = __ldcg(sr + q * QV + i);
+                                xl[i] = __ldcg(sl + (g * QV + i) * MP);
+                                xr[i] = __ldcg(sr + (g * QV + i) * MP);
                             }
 #pragma unroll
-                            for (int i = 0; i < QV; ++i) {
-                                const float4 w4 = make_float4(xl[i].x + xr[i].x, xl[i].y + xr[i].y, xl[i].z + xr[i].z,
-                                                              xl[i].w + xr[i].w);
-                                if (!root) {
-                                    dl[q * QV + i] = w4;
-                                } else {  // every chunk is in: W'_jk = W_jk / Delta_j, bf16 image
-                                    const int k = q * (D / 2) + 4 * i;
-                                    img[wimg_off<D>(row, k) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.x * rinv));
-                                    img[wimg_off<D>(row, k + 1) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.y * rinv));
-                                    img[wimg_off<D>(row, k + 2) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.z * rinv));
-                                    img[wimg_off<D>(row, k + 3) / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(w4.w * rinv));
+                            for (int i = 0; i < QV; ++i)
+                                xl[i] = make_float4(xl[i].x + xr[i].x, xl[i].y + xr[i].y, xl[i].z + xr[i].z, xl[i].w + xr[i].w);
+                            if (!root) {
+#pragma unroll
+                                for (int i = 0; i < QV; ++i) dl[(g * QV + i) * MP] = xl[i];
+                            } else {  // every chunk is in: W'_jk = W_jk / Delta_j, bf16 image
+#pragma unroll
+                                for (int i = 0; i < QV; i += 2) {
+                                    const float w8[8] = {xl[i].x, xl[i].y, xl[i].z, xl[i].w,
+                                                         xl[i + 1].x, xl[i + 1].y, xl[i + 1].z, xl[i + 1].w};
+                                    *reinterpret_cast<uint4 *>(img + wimg_chunk_off<MP>(row, (g * QV + i) / 2)) =
+                                        pack8_scaled(w8, rinv);
                                 }
                             }
                         }
-                        if (!root) p.pdelta[rl] = dsum;
+                        if (!root) p.pdelta[dl_] = dsum;
                     }
                     if (root) {
                         __threadfence();
@@ -832,9 +871,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 tmem_ld_wait();
                 if (row < MP) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        *reinterpret_cast<uint16_t *>(sWb + wimg_off<D>(row, q * 32 + i)) =
-                            __bfloat16_as_ushort(__float2bfloat16_rn(v[i] * rinv));
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(sWb + wimg_chunk_off<MP>(row, q * 4 + c)) = pack8_scaled(v + 8 * c, rinv);
                 }
             }
             tc_fence_before();
@@ -960,13 +998,31 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
 
 }  // namespace
 
+// SMs of the current device (152 on GB300 when no device can be queried: plans are also
+// asked for on machines without one)
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
 UmmaPlan umma_plan(const Problem &p) {
     UmmaPlan pl;
     const int MP = p.m <= 64 ? 64 : 128;
     pl.MP = MP;
     pl.NT = (p.n + kT - 1) / kT;
     const long long S = p.slices();
-    pl.C1 = (pl.NT + kUmmaP1Tiles - 1) / kUmmaP1Tiles;
+    // Chunk sizes: long chunks mean fewer partials to reduce and fewer anchor reloads, but
+    // every SM needs work: halve a pass's chunk while the pass has fewer than two items per SM.
+    const long long want = 2LL * sm_count();
+    int t1 = kUmmaP1Tiles, t2 = kUmmaP2Tiles;
+    while (t1 > kUmmaMinTiles && S * ((pl.NT + t1 - 1) / t1) < want) t1 /= 2;
+    while (t2 > kUmmaMinTiles && S * ((pl.NT + t2 - 1) / t2) < want) t2 /= 2;
+    pl.C1 = (pl.NT + t1 - 1) / t1;
     if (pl.NT <= kUmmaFullTiles || pl.C1 == 1) {
         pl.C1 = 1;
         pl.C2 = 0;
@@ -975,7 +1031,7 @@ UmmaPlan umma_plan(const Problem &p) {
         pl.workspace_bytes = 256;
         return pl;
     }
-    pl.C2 = (pl.NT + kUmmaP2Tiles - 1) / kUmmaP2Tiles;
+    pl.C2 = (pl.NT + t2 - 1) / t2;
     pl.total_items = (int)(S * (pl.C1 + pl.C2));
     pl.header_bytes = (256 + 2 * 128 * (size_t)S + 4 * (size_t)S * pl.C1 + 1023) / 1024 * 1024;
     pl.workspace_bytes = pl.header_bytes + 4 * (size_t)S * pl.C1 * MP + 4 * (size_t)S * pl.C1 * p.d * MP +
@@ -984,7 +1040,8 @@ UmmaPlan umma_plan(const Problem &p) {
 }
 
 bool umma_supported(const Problem &p) {
-    return !p.f32 && (p.d == 64 || p.d == 128) && p.m >= 32 && p.m <= 128 &&
+    // scale > 0: the softmax takes the row maximum of the raw scores
+    return !p.f32 && (p.d == 64 || p.d == 128) && p.m >= 32 && p.m <= 128 && p.scale > 0.f &&
            p.slices() * ((p.n + kT - 1) / kT) * 3 < 0x7fffffffLL;
 }
 
