@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch count (a smaller case for profiling)")
     return ap.parse_args(argv)
 
 
@@ -222,6 +224,8 @@ def run_ours(args) -> None:
     dev = torch.device("cuda", local)
     pkg.load()
     w = gen.WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = w.with_(B=args.batch)
     tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     plan = pkg.query_plan(w.dtype, w.B, w.heads, w.n, w.m, w.d)
 

@@ -64,7 +64,7 @@ cudaError_t launch_simt_split(const Problem &p, int splits, float *workspace, cu
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA
 constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)
-constexpr int kUmmaP2Tiles = 8;      // tiles per pass-2 chunk (halved while items are too few)
+constexpr int kUmmaP2Tiles = 16;     // tiles per pass-2 chunk (halved while items are too few)
 constexpr int kUmmaMinTiles = 4;     // smallest chunk either pass is cut into
 struct UmmaPlan {
     int MP = 0;              // anchors padded to 64 or 128
@@ -72,6 +72,8 @@ struct UmmaPlan {
     int C1 = 0, C2 = 0;      // chunks per slice in pass 1 / pass 2 (C1 == 1: whole slice per CTA)
     int total_items = 0;
     size_t header_bytes = 0; // zeroed part of the workspace (ticket, counters, flags)
+    size_t abuf_offset = 0;  // the A copy pass 2 reads: [slices][n][MP] bf16 (split slices only)
+    bool store_a = false;    // pass 2 loads the A copy (else it recomputes A from Q)
     size_t workspace_bytes = 0;
 };
 bool umma_supported(const Problem &p);

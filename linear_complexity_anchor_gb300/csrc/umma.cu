@@ -3,28 +3,34 @@
 // (AnchorFormer, arXiv 2505.16463; pith.science verdict: "key_machinery", "core_discovery"
 // and the referee summary of Eq. 11/12: B^T V -> Delta^{-1}(B^T V) -> B(Delta^{-1} B^T V)).
 //
-// One persistent kernel per call.  Work is cut into items handed out in a fixed ticket
-// order by an atomic counter:
+// One persistent kernel per call; work is cut into items that CTAs claim at run time:
 //   P1(s, c)  pass 1 over token chunk c of slice s: per 128-token tile, S = Q U^T on the
 //             tensor core (TMEM accumulator), row softmax in registers (one thread per
 //             token), A tile -> shared memory as bf16, then W += A^T V and Delta += A^T 1
-//             on the tensor core (both from the same rounded A).  The chunk's (W, Delta)
-//             goes to a workspace partial.  The last chunk of a slice to finish sums the
-//             partials in chunk order (fixed: the result does not depend on which CTA ran
-//             what), forms W' = Delta^{-1} W as a bf16 operand image and publishes it.
-//   P2(s, c)  pass 2 over token chunk c: waits for the slice's W', recomputes A exactly as
-//             P1 did, H = A W' on the tensor core, TMA store of the bf16 tile.
-//   FULL(s)   short slices: P1 and P2 of a whole slice in one CTA, W' kept on chip.
-// P2 items of slice s are issued L slices after its P1 items, so a P2 item only waits on
-// items with smaller tickets, which are already held by running CTAs: no deadlock for any
-// grid size, and Q is usually still in L2 when pass 2 re-reads it.
+//             on the tensor core (both from the same rounded A).  The A tile also goes to
+//             a workspace copy (TMA store, kept in L2).  The chunk's (W, Delta) goes to a
+//             workspace partial; partials meet in a fixed binary tree (the second of two
+//             siblings to arrive adds them: the sums do not depend on which CTA ran what),
+//             and the root forms W' = Delta^{-1} W as a bf16 operand image and publishes it.
+//   P2(s, c)  pass 2 over token chunk c, once the slice's W' is published: the stored A
+//             tile comes back from L2, H = A W' on the tensor core, bf16 H rows to global
+//             memory; the A lines are then dropped from L2 without a write-back.
+//   FULL(s)   short slices: P1 and P2 of a whole slice in one CTA, W' kept on chip; pass 2
+//             recomputes A instead of storing it.
+// A CTA takes a P2 chunk of a slice whose W' is ready, else a P1 chunk of a slice at most K
+// slices past the oldest slice with unclaimed P2 chunks (K: the A copies of the slices in
+// flight fit a share of L2).  A P2 chunk only waits on P1 chunks already held by running
+// CTAs, so no grid size can deadlock.
+//
+// Roles (warp-specialised, one CTA per SM): warps 0-3 softmax, 4-7 epilogue (H rows,
+// partials, tree, W'), warp 8 TMA producer and work claiming, warp 9 MMA issue.
 //
 // Operand layouts (shared memory, 128-byte swizzle, 1024-byte aligned blocks of 64 columns):
-//   Q, V, H tiles  [128 tokens][D]   K-major for S = Q U^T; MN-major (N = d) for A^T V
+//   Q, V tiles     [128 tokens][D]   K-major for S = Q U^T; MN-major (N = d) for A^T V
 //   U              [MP anchors][D]   K-major
 //   A tile         [128 tokens][128 anchors] MN-major as A^T (M = anchors) in pass 1,
 //                  K-major as A (M = tokens) in pass 2; anchors >= MP stay zero
-//   W' image       [D][MP]           K-major B operand of H = A W'
+//   W' image       [MP][D]           MN-major B operand of H = A W'
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -42,10 +48,15 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 128;                         // tokens per tile (UMMA M)
-constexpr int kThreads = 320;  // warps 0-3 softmax, 4-7 epilogue, 8 producer, 9 MMA
+// warps 0-7 softmax (two groups of four, each on half of the anchors of the same 128 rows),
+// 8-11 epilogue, 12 producer, 13 MMA
+constexpr int kThreads = 448;
+constexpr int kWarpProducer = 12, kWarpMma = 13;
 constexpr int kIQ = 4;                          // item queue depth
+constexpr int kPrefetch = 0;                    // tiles of an item brought into L2 ahead of their load
 constexpr uint64_t kWaitNs = 2000000000ull;     // every wait gives up after 2 s
-constexpr double kL2QBudget = 96.0 * 1024 * 1024; // L2 share for Q between its two reads
+constexpr double kL2ABudget = 256.0 * 1024 * 1024; // bytes kept for pass 2 (A or Q) of the slices in flight
+constexpr double kStoreABudget = 64.0 * 1024 * 1024; // largest A copy kept for pass 2
 
 struct UParams {
     int slices, heads, B, n, m;
@@ -54,38 +65,44 @@ struct UParams {
     float *part;              // [slices][C1][D/4][MP][4]  W partials (anchor-interleaved float4)
     float *pdelta;            // [slices][C1][MP]     Delta partials
     uint16_t *wimg;           // [slices][D * MP]     W' operand images (bf16, swizzled)
+    uint16_t *abuf;           // [slices][n][MP]      A (bf16) written in pass 1, read in pass 2
     unsigned *flags;          // [slices * 32] W' published (one 128-byte line per slice)
     unsigned *p2c;            // [slices * 32] P2 chunks of the slice claimed so far
     unsigned *tree;           // [slices][C1] arrivals at the nodes of the reduction tree
     unsigned *next;           // next P1 chunk (or whole slice) to claim
     unsigned *head;           // first slice (schedule order) whose P2 chunks are not all claimed
     int K;                    // P1 may run at most K slices ahead of the P2 head
-    int p1first;              // every slice's Q fits the L2 budget: take P1 chunks before P2
+    int p1first;              // take every P1 chunk before any P2 chunk
+    int store_a;              // pass 2 of split slices loads pass 1's A copy (else recomputes A)
 };
 
 template <int D, int MP>
 struct Layout {
-    static constexpr int kQB = kT * D * 2;             // one Q or V tile: one ring slot
+    static constexpr int kQB = kT * D * 2;             // one Q or V tile
+    static constexpr int kATB = kT * MP * 2;           // one stored A tile (pass-2 operand)
+    static constexpr int kSlotB = kQB > kATB ? kQB : kATB;  // ring slot: any of the three
     static constexpr int kUB = MP * D * 2;
     static constexpr int kAB = kT * 128 * 2;           // A tile, 128 anchor columns
     static constexpr int kWB = D * MP * 2;             // W' operand image
     static constexpr int kOnesB = 16 * kT * 2;         // 16 x 128 ones (bf16)
+    static constexpr int kXchB = 2 * 2 * kT * 8;        // softmax halves' (max, sum), by tile parity
     static constexpr int kBarB = 1024;
     static constexpr int kMaxDyn = 227 * 1024 - 1024;  // minus the alignment slack
     // double-buffer the anchors and the A tile when that still leaves a 6-slot ring
-    static constexpr bool kRoomy = (2 * kUB + 2 * kAB + 2 * kWB + kOnesB + kBarB + 6 * kQB) <= kMaxDyn;
+    static constexpr bool kRoomy = (2 * kUB + 2 * kAB + 2 * kWB + kOnesB + kXchB + kBarB + 6 * kSlotB) <= kMaxDyn;
     static constexpr int kNU = kRoomy ? 2 : 1;
     static constexpr int kNA = kRoomy ? 2 : 1;
     static constexpr int kNW = kRoomy ? 2 : 1;
-    static constexpr int kFixed = kNU * kUB + kNA * kAB + kNW * kWB + kOnesB + kBarB;
-    static constexpr int kSlotsFit = (kMaxDyn - kFixed) / kQB;
+    static constexpr int kFixed = kNU * kUB + kNA * kAB + kNW * kWB + kOnesB + kXchB + kBarB;
+    static constexpr int kSlotsFit = (kMaxDyn - kFixed) / kSlotB;
     static constexpr int kNSlot = kSlotsFit > 8 ? 8 : kSlotsFit;
     static constexpr int offU = 0;
     static constexpr int offA = offU + kNU * kUB;
     static constexpr int offW = offA + kNA * kAB;
     static constexpr int offRing = offW + kNW * kWB;
-    static constexpr int offOnes = offRing + kNSlot * kQB;
-    static constexpr int offBar = offOnes + kOnesB;
+    static constexpr int offOnes = offRing + kNSlot * kSlotB;
+    static constexpr int offXch = offOnes + kOnesB;
+    static constexpr int offBar = offXch + kXchB;
     static constexpr int kBytes = offBar + kBarB;
     static constexpr int kSmem = kBytes + 1024;
     // TMEM: S0 | S1 | B0 (W in pass 1, H0 in pass 2) | B1 (Delta in pass 1, H1 in pass 2)
@@ -120,6 +137,7 @@ struct TileRef {
     bool first;     // first tile of its pass within the item
     bool last;      // last tile of its pass within the item
     bool full;      // the item keeps W' on chip (whole slice per CTA)
+    bool stored;    // pass-2 tile whose A is loaded from pass 1's copy instead of recomputed
     int chunk;      // pass-1 chunk (partials)
 };
 
@@ -134,11 +152,12 @@ __device__ __forceinline__ int item_tiles(const Item &it, const UParams &p, int 
     return b1 - a1;
 }
 
-__device__ __forceinline__ TileRef tile_at(const Item &it, int a1, int b1, int idx) {
+__device__ __forceinline__ TileRef tile_at(const Item &it, int a1, int b1, int idx, bool store_a) {
     TileRef r;
     r.slice = it.slice;
     r.chunk = it.chunk;
     r.full = it.kind == 2;
+    r.stored = it.kind == 1 && store_a;
     const int n1 = b1 - a1;
     if (it.kind == 2) {
         const bool p2 = idx >= n1;
@@ -156,12 +175,12 @@ __device__ __forceinline__ TileRef tile_at(const Item &it, int a1, int b1, int i
     return r;
 }
 
-// byte offset of 16-byte chunk `c` (0 .. cols/8-1) of row `r` in a swizzled [rows][cols]
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// byte offset of 16-byte chunk `c` (0 .. cols/8-1) of row `r` in a swizzled [rows][cols]
 // bf16 tile stored as 64-column blocks of `rows` x 128 bytes
 __device__ __forceinline__ uint32_t sw_off(int r, int c, int rows) {
     return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
@@ -190,42 +209,43 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // named barriers of the two 4-warp groups (id 0 is __syncthreads)
-__device__ __forceinline__ void sm_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void sm_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ void ep_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// Row softmax of one S row (TMEM lane = this thread's token), packed to bf16 pairs:
-// A_i = softmax_j(scale * S_ij) computed as 2^(c * S_ij - c * max_j S_ij) / sum, c = scale *
-// log2(e) > 0, so the scale folds into one fused multiply-add per element.  Rows past the end
-// of the slice become zero rows.  With MASKED, anchors >= m are set to -inf first (their
-// probability is exactly 0); without it every one of the MP columns is a real anchor.
-// Max and sum run as 8 interleaved partial chains in a fixed order (deterministic); the
-// scale, the sum and the normalisation use the paired fp32 instructions.
+// Half of a row softmax: this thread's token row, anchors [col0, col0 + MP/2) of the S row.
+// A_ij = softmax_j(scale * S_ij) = 2^(c S_ij - c max_j S_ij) / sum, c = scale * log2(e) > 0.
+// The two halves of a row (two threads in the two softmax groups) each produce
+//   e_j = 2^(c S_j - c mg)  with mg = their own maximum, and zg = sum of their e_j;
+// the row then combines them: max M = max(mg0, mg1), sum z = zg0 2^(c(mg0 - M)) + zg1 2^(c(mg1 - M)),
+// and A_j = e_j 2^(c(mg - M)) / z.  With MASKED, anchors >= m are -inf (probability 0).
+// Max and sum run as 8 interleaved chains in a fixed order (deterministic).
 template <int MP, bool MASKED>
-__device__ __forceinline__ void softmax_row(uint32_t taddr_s, bool valid, int m, float c, uint32_t (&pk)[MP / 2]) {
-    float v[MP];
+__device__ __forceinline__ void softmax_half(uint32_t taddr, int col0, int m, float c, float (&v)[MP / 2], float &mg,
+                                             float &zg) {
+    constexpr int HM = MP / 2;
 #pragma unroll
-    for (int q = 0; q < MP / 32; ++q) tmem_ld32(taddr_s + q * 32, v + q * 32);
+    for (int q = 0; q < HM / 32; ++q) tmem_ld32(taddr + q * 32, v + q * 32);
     tmem_ld_wait();
     if (MASKED) {
 #pragma unroll
-        for (int j = 0; j < MP; ++j)
-            if (j >= m) v[j] = -INFINITY;
+        for (int j = 0; j < HM; ++j)
+            if (col0 + j >= m) v[j] = -INFINITY;
     }
     float mx8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) mx8[i] = v[i];
 #pragma unroll
-    for (int j = 8; j < MP; j += 16) {
+    for (int j = 8; j < HM; j += 16) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            mx8[k] = (j + 8 + k < MP) ? max3_f32(mx8[k], v[j + k], v[j + 8 + k]) : fmaxf(mx8[k], v[j + k]);
+            mx8[k] = (j + 8 + k < HM) ? max3_f32(mx8[k], v[j + k], v[j + 8 + k]) : fmaxf(mx8[k], v[j + k]);
     }
-    const float mx = fmaxf(max3_f32(mx8[0], mx8[1], mx8[2]), max3_f32(max3_f32(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-    const float nb = -mx * c;
+    mg = fmaxf(max3_f32(mx8[0], mx8[1], mx8[2]), max3_f32(max3_f32(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+    const float nb = mg == -INFINITY ? 0.f : -mg * c;  // a fully masked half: every e_j = 0
     const uint64_t c2 = f32x2(c, c), nb2 = f32x2(nb, nb);
     uint64_t z4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-    for (int j = 0; j < MP; j += 2) {
+    for (int j = 0; j < HM; j += 2) {
         float a, b;
         f32x2_split(fma_f32x2(f32x2(v[j], v[j + 1]), c2, nb2), a, b);
         a = ex2_approx(a);
@@ -236,20 +256,15 @@ __device__ __forceinline__ void softmax_row(uint32_t taddr_s, bool valid, int m,
     }
     float za, zb;
     f32x2_split(add_f32x2(add_f32x2(z4[0], z4[1]), add_f32x2(z4[2], z4[3])), za, zb);
-    const float inv = valid ? 1.f / (za + zb) : 0.f;
-    const uint64_t inv2 = f32x2(inv, inv);
-#pragma unroll
-    for (int j = 0; j < MP / 2; ++j) {
-        float a, b;
-        f32x2_split(mul_f32x2(f32x2(v[2 * j], v[2 * j + 1]), inv2), a, b);
-        pk[j] = pack_bf16x2(a, b);
-    }
+    zg = za + zb;
 }
 
 template <int D, int MP>
 __global__ void __launch_bounds__(kThreads, 1)
 anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
-                   const __grid_constant__ CUtensorMap tu, const UParams p, uint16_t *__restrict__ Hout) {
+                   const __grid_constant__ CUtensorMap tu, const __grid_constant__ CUtensorMap ta_st,
+                   const __grid_constant__ CUtensorMap ta_ld, const __grid_constant__ CUtensorMap th_st,
+                   const UParams p, uint16_t *__restrict__ Hout) {
     using LY = Layout<D, MP>;
     constexpr int NS = LY::kNSlot, NU = LY::kNU, NA = LY::kNA, NW = LY::kNW;
     extern __shared__ uint8_t smem_raw[];
@@ -259,13 +274,14 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint8_t *sW = sm + LY::offW;
     uint8_t *sRing = sm + LY::offRing;
     uint8_t *sOnes = sm + LY::offOnes;
+    float2 *sXch = reinterpret_cast<float2 *>(sm + LY::offXch);  // [tile parity][group][row]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::offBar);
     // full/empty barrier pairs (arrival counts in brackets)
     uint64_t *slot_full = bars;                  // [NS] (1 + tx)  TMA landed
     uint64_t *slot_empty = slot_full + NS;       // [NS] (1)       MMA that read the slot completed
     uint64_t *s_full = slot_empty + NS;          // [2]  (1)       scores in S buffer
-    uint64_t *s_empty = s_full + 2;              // [2]  (4)       softmax warps read the S buffer
-    uint64_t *a_full = s_empty + 2;              // [NA] (4)       A tile written
+    uint64_t *s_empty = s_full + 2;              // [2]  (8)       softmax warps read the S buffer
+    uint64_t *a_full = s_empty + 2;              // [NA] (1)       A tile written
     uint64_t *a_empty = a_full + NA;             // [NA] (1)       MMA reading the A tile completed
     uint64_t *acc_full = a_empty + NA;           // [2]  (1)       W/Delta or H complete in TMEM
     uint64_t *acc_empty = acc_full + 2;          // [2]  (4)       epilogue read it
@@ -281,6 +297,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_items + 3 * kIQ);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_last = reinterpret_cast<int *>(s_tmem + 2);
+    uint32_t *s_ast = s_tmem + 3;  // softmax-warp chunk ends whose A stores are complete
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -291,12 +308,12 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + i, 1);
-            mbar_init(s_empty + i, 4);
+            mbar_init(s_empty + i, 8);
             mbar_init(acc_full + i, 1);
             mbar_init(acc_empty + i, 4);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(a_full + i, 4);
+            mbar_init(a_full + i, 1);
             mbar_init(a_empty + i, 1);
         }
         for (int i = 0; i < NU; ++i) {
@@ -312,14 +329,18 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_init(iq_empty + i, 3);
         }
         *s_abort = 0;
+        *s_ast = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tu);
+        tma_prefetch_desc(&ta_st);
+        tma_prefetch_desc(&ta_ld);
+        tma_prefetch_desc(&th_st);
     }
     for (int i = tid; i < LY::kOnesB / 4; i += kThreads) reinterpret_cast<uint32_t *>(sOnes)[i] = 0x3F803F80u;
     for (int i = tid; i < NA * LY::kAB / 16; i += kThreads) reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0, 0, 0, 0);
-    if (warp == 9) tmem_alloc(s_tmem, LY::kTmemCols);
+    if (warp == kWarpMma) tmem_alloc(s_tmem, LY::kTmemCols);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -345,7 +366,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         return {e[0], e[1], e[2]};
     };
 
-    if (warp == 8) {
+    if (warp == kWarpProducer) {
         // =========================================================== producer (whole warp:
         // every lane waits and decides alike; lane 0 issues the copies and the queue writes)
         constexpr unsigned FULLW = 0xffffffffu;
@@ -362,14 +383,14 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
             return __all_sync(FULLW, wait(bar, parity)) != 0;
         };
-        auto load_slot = [&](const CUtensorMap *map, int slice, int tile, uint64_t pol) -> bool {
+        // one 128-row tile of `cols` columns (D for Q and V, MP for a stored A tile)
+        auto load_slot = [&](const CUtensorMap *map, int slice, int tile, uint64_t pol, int cols) -> bool {
             const int st = (int)(ld_seq % NS);
             if (!wwait(slot_empty + st, ((ld_seq / NS) & 1u) ^ 1u)) return false;
             if (L0) {
-                mbar_arrive_expect_tx(slot_full + st, LY::kQB);
-#pragma unroll
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(sRing + st * LY::kQB + b * kT * 128, map, slot_full + st, 64 * b, tile * kT, slice, pol);
+                mbar_arrive_expect_tx(slot_full + st, (uint32_t)(kT * cols * 2));
+                for (int b = 0; b < cols / 64; ++b)
+                    tma_load_3d(sRing + st * LY::kSlotB + b * kT * 128, map, slot_full + st, 64 * b, tile * kT, slice, pol);
             }
             ++ld_seq;
             return true;
@@ -492,7 +513,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
                 if (!flushed) {
                     ok = push(Item{kFlush, 0, 0});
-                    if (ok && has_pend_v) ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
+                    if (ok && has_pend_v) ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream, D);
                     has_pend_v = false;
                     flushed = true;
                 }
@@ -517,7 +538,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             if (!push(it)) break;
             flushed = false;
             const int h = it.slice % p.heads;
-            if (h != u_head) {  // U load number nu goes to buffer nu % NU
+            // U load number nu goes to buffer nu % NU (pass 2 on a stored A needs no U)
+            if ((it.kind != 1 || !p.store_a) && h != u_head) {
                 const int ub = (int)(nu % NU);
                 if (!wwait(u_empty + ub, ((nu / NU) & 1u) ^ 1u)) break;
                 if (L0) {
@@ -531,13 +553,30 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
             int a1, b1;
             const int nt = item_tiles(it, p, a1, b1);
+            // L2 prefetch of the tiles a few loads ahead: the ring alone holds too few bytes
+            // in flight to cover the memory latency
+            auto prefetch = [&](int j) {
+                if (!L0 || j >= nt) return;
+                const TileRef tf = tile_at(it, a1, b1, j, p.store_a != 0);
+                if (tf.stored) {
+                    for (int b = 0; b < MP / 64; ++b) tma_prefetch_l2_3d(&ta_ld, 64 * b, tf.tile * kT, tf.slice);
+                } else {
+                    for (int b = 0; b < D / 64; ++b) tma_prefetch_l2_3d(&tq, 64 * b, tf.tile * kT, tf.slice);
+                    if (tf.kind == 0)
+                        for (int b = 0; b < D / 64; ++b) tma_prefetch_l2_3d(&tv, 64 * b, tf.tile * kT, tf.slice);
+                }
+            };
+            for (int j = 0; j < kPrefetch; ++j) prefetch(j);
             for (int idx = 0; idx < nt && ok; ++idx) {
-                const TileRef tr = tile_at(it, a1, b1, idx);
-                ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 ? pol_keep : pol_stream);
+                const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                prefetch(idx + kPrefetch);
+                // a pass-1 Q tile is read again by pass 2 unless pass 2 loads the stored A
+                if (tr.stored) ok = load_slot(&ta_ld, tr.slice, tr.tile, pol_stream, MP);
+                else ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 && (tr.full || !p.store_a) ? pol_keep : pol_stream, D);
                 // claim the next item now, while the ring is still full of this one's tiles
                 if (idx == 0 && !have_ahead) have_ahead = claim(ahead) == 1;
                 if (ok && has_pend_v) {
-                    ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
+                    ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream, D);
                     has_pend_v = false;
                 }
                 if (tr.kind == 0) {
@@ -559,8 +598,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
             }
         }
-        if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream);
-    } else if (warp == 9) {
+        if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream, D);
+    } else if (warp == kWarpMma) {
         // =========================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(128, MP, false, false);
@@ -591,7 +630,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
                     for (int kt = 0; kt < kT / 16; ++kt) {
                         const uint64_t ad = smem_desc_sw128(sAb + kt * 2048, 16384, 1024);
-                        const uint64_t vd = smem_desc_sw128(sRa + vs * LY::kQB + kt * 2048, 16384, 1024);
+                        const uint64_t vd = smem_desc_sw128(sRa + vs * LY::kSlotB + kt * 2048, 16384, 1024);
                         const uint64_t od = smem_desc_sw128(sOa + (kt >> 2) * 2048 + (kt & 3) * 32, 16, 1024);
                         const uint32_t acc = (!tr.first || kt > 0) ? 1u : 0u;
                         umma_bf16(tmem + LY::colB0, ad, vd, kIdW, acc);
@@ -644,7 +683,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     continue;
                 }
                 const int h = it.slice % p.heads;
-                if (h != prev_head) {
+                if ((it.kind != 1 || !p.store_a) && h != prev_head) {
                     if (prev_head >= 0) umma_commit(u_empty + (nu - 1) % NU);  // every S on the old U issued
                     if (!wait(u_full + nu % NU, (nu / NU) & 1u)) break;
                     ++nu;
@@ -654,22 +693,52 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 int a1, b1;
                 const int nt = item_tiles(it, p, a1, b1);
                 for (int idx = 0; idx < nt && ok; ++idx) {
-                    const TileRef tr = tile_at(it, a1, b1, idx);
+                    const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
                     const int qslot = (int)(cons % NS);
                     if (!wait(slot_full + qslot, (cons / NS) & 1u)) { ok = false; break; }
                     ++cons;
+                    if (tr.stored) {
+                        // pass 2 of a split slice: the slot holds the A tile pass 1 stored
+                        // (the ring has it ahead of the pending pass-1 tile's V)
+                        if (has_pend && !do_x(pend)) { ok = false; break; }
+                        has_pend = false;
+                        const int wb = (int)((tr.first ? wuse : wuse - 1u) % NW);
+                        if (tr.first) {
+                            if (!wait(w_full + wb, (wuse / NW) & 1u)) { ok = false; break; }
+                            ++wuse;
+                        }
+                        const uint32_t sWb = sWa + wb * LY::kWB;
+                        const int hb = (int)(p2 & 1u);
+                        if (!wait(acc_empty + hb, (accuse[hb] & 1u) ^ 1u)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t dcol = hb ? LY::colB1 : LY::colB0;
+                        const uint32_t sAt = sRa + qslot * LY::kSlotB;
+#pragma unroll
+                        for (int kj = 0; kj < MP / 16; ++kj) {
+                            const uint64_t ad = smem_desc_sw128(sAt + (kj >> 2) * kT * 128 + (kj & 3) * 32, 16, 1024);
+                            const uint64_t wd = smem_desc_sw128(sWb + kj * 2048, MP * 128, 1024);
+                            umma_bf16(tmem + dcol, ad, wd, kIdH, kj > 0);
+                        }
+                        // the slot is released by the epilogue, which stages the H tile in it
+                        umma_commit(acc_full + hb);
+                        ++accuse[hb];
+                        ++p2;
+                        if (tr.last) umma_commit(w_empty + wb);
+                        continue;
+                    }
                     const int sb = (int)(sidx & 1u);
                     if (!wait(s_empty + sb, ((sidx >> 1) & 1u) ^ 1u)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t dcol = sb ? LY::colS1 : LY::colS0;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t a = smem_desc_sw128(sRa + qslot * LY::kQB + (kk >> 2) * kT * 128 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t a = smem_desc_sw128(sRa + qslot * LY::kSlotB + (kk >> 2) * kT * 128 + (kk & 3) * 32, 16, 1024);
                         const uint64_t b = smem_desc_sw128(sUb + (kk >> 2) * MP * 128 + (kk & 3) * 32, 16, 1024);
                         umma_bf16(tmem + dcol, a, b, kIdS, kk > 0);
                     }
                     umma_commit(s_full + sb);
-                    umma_commit(slot_empty + qslot);
+                    // a pass-2 tile's Q slot stays held: the epilogue stages the H tile there
+                    if (tr.kind == 0) umma_commit(slot_empty + qslot);
                     ++sidx;
                     if (has_pend && !do_x(pend)) { ok = false; break; }
                     pend = tr;
@@ -678,13 +747,18 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
             if (ok && has_pend) do_x(pend);
         }
-    } else if (warp < 4) {
-        // =========================================================== softmax (warps 0-3)
-        const int row = tid;  // TMEM lane = token row of the tile
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    } else if (warp < 8) {
+        // =========================================================== softmax (warps 0-7)
+        // Group g = warp / 4 takes anchors [g MP/2, (g+1) MP/2) of the rows of TMEM lane
+        // quadrant warp % 4; the two halves of a row meet through shared memory.
+        const int g = warp >> 2, quad = warp & 3;
+        const int row = quad * 32 + lane;  // TMEM lane = token row of the tile
+        const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+        constexpr int HM = MP / 2;
+        const uint64_t pol_keep = policy_evict_last();
         uint32_t sidx = 0, ause = 0, iq = 0;
         bool ok = true;
-        auto arrive4 = [&](uint64_t *bar) {  // one arrival per warp
+        auto arrive_w = [&](uint64_t *bar) {  // one arrival per warp
             __syncwarp();
             if (lane == 0) mbar_arrive(bar);
         };
@@ -692,78 +766,148 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             if (!wait(iq_full + iq % kIQ, (iq / kIQ) & 1u)) break;
             const Item it = read_item(iq);
             sm_sync();
-            if (row == 0) mbar_arrive(iq_empty + iq % kIQ);
+            if (tid == 0) mbar_arrive(iq_empty + iq % kIQ);
             ++iq;
             if (it.kind == kEnd) break;
             if (it.kind == kFlush) continue;
             int a1, b1;
             const int nt = item_tiles(it, p, a1, b1);
             for (int idx = 0; idx < nt && ok; ++idx) {
-                const TileRef tr = tile_at(it, a1, b1, idx);
+                const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                if (tr.stored) continue;  // pass 2 of a split slice has no softmax
                 const int sb = (int)(sidx & 1u);
                 if (!wait(s_full + sb, (sidx >> 1) & 1u)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t pk[MP / 2];
-                const uint32_t ts = trow + (sb ? LY::colS1 : LY::colS0);
-                const bool valid = tr.tile * kT + row < p.n;
-                if (p.m == MP) softmax_row<MP, false>(ts, valid, p.m, p.c, pk);
-                else softmax_row<MP, true>(ts, valid, p.m, p.c, pk);
+                float v[HM], mg, zg;
+                const uint32_t ts = trow + (sb ? LY::colS1 : LY::colS0) + g * HM;
+                if (p.m == MP) softmax_half<MP, false>(ts, g * HM, p.m, p.c, v, mg, zg);
+                else softmax_half<MP, true>(ts, g * HM, p.m, p.c, v, mg, zg);
                 tc_fence_before();
-                arrive4(s_empty + sb);
+                arrive_w(s_empty + sb);
+                // the last A store of this group has read its rows before anyone rewrites them
+                if (g == 0 && lane == 0) bulk_wait_group_read0();
+                float2 *xc = sXch + (size_t)(sb * 2) * kT;
+                xc[g * kT + row] = make_float2(mg, zg);
+                sm_sync();
+                const float2 o = xc[(g ^ 1) * kT + row];
                 ++sidx;
+                const float mrow = fmaxf(mg, o.x);
+                const float own = ex2_approx((mg - mrow) * p.c), other = ex2_approx((o.x - mrow) * p.c);
+                const bool valid = tr.tile * kT + row < p.n;
+                const float scale = valid ? own / (zg * own + o.y * other) : 0.f;
+                uint32_t pk[HM / 2];
+                const uint64_t sc2 = f32x2(scale, scale);
+#pragma unroll
+                for (int j = 0; j < HM / 2; ++j) {
+                    float x0, x1;
+                    f32x2_split(mul_f32x2(f32x2(v[2 * j], v[2 * j + 1]), sc2), x0, x1);
+                    pk[j] = pack_bf16x2(x0, x1);
+                }
                 const int ab = (int)(ause % NA);
                 if (!wait(a_empty + ab, ((ause / NA) & 1u) ^ 1u)) { ok = false; break; }
                 uint8_t *sAb = sA + ab * LY::kAB;
 #pragma unroll
-                for (int c8 = 0; c8 < MP / 8; ++c8)
-                    *reinterpret_cast<uint4 *>(sAb + sw_off(row, c8, kT)) =
+                for (int c8 = 0; c8 < HM / 8; ++c8)
+                    *reinterpret_cast<uint4 *>(sAb + sw_off(row, g * (HM / 8) + c8, kT)) =
                         make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
                 fence_proxy_async_smem();
-                arrive4(a_full + ab);
+                sm_sync();  // both halves of every row are in place
+                if (tid == 0) mbar_arrive(a_full + ab);
                 ++ause;
+                const bool store = tr.kind == 0 && !tr.full && p.store_a;  // pass 2 reads A back
+                if (g == 0 && store && lane == 0) {
+                    if (tr.tile * kT + quad * 32 < p.n) {
+                        // this quadrant's 32 rows; rows past the end of the slice are not written
+#pragma unroll
+                        for (int b = 0; b < MP / 64; ++b)
+                            tma_store_3d(&ta_st, sAb + b * kT * 128 + quad * 32 * 128, 64 * b, tr.tile * kT + quad * 32,
+                                         tr.slice, pol_keep);
+                        bulk_commit_group();
+                    }
+                    if (tr.last) {
+                        // end of a chunk: its A rows are in global memory before the chunk is
+                        // published (the epilogue waits for all four storing warps)
+                        bulk_wait_group0();
+                        fence_proxy_async_global();
+                        red_release_cta_add(s_ast, 1u);
+                    }
+                }
             }
         }
     } else {
-        // =========================================================== epilogue (warps 4-7)
+        // =========================================================== epilogue (warps 8-11)
         // H tiles out of TMEM to global; at the end of a pass-1 phase, the chunk partial and
         // its reduction (or, for whole slices, W' straight into shared memory).
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // TMEM lane: token row (H) / anchor row (W)
         const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint32_t iq = 0, p2 = 0, wuse = 0;
+        uint32_t iq = 0, p2 = 0, wuse = 0, chunks = 0, lseq = 0;
+        bool lpend = false;
         uint32_t accuse[2] = {0u, 0u};
         bool ok = true;
         auto arrive4 = [&](uint64_t *bar) {  // one arrival per warp
             __syncwarp();
             if (lane == 0) mbar_arrive(bar);
         };
-        auto epilogue = [&](const TileRef &tr) -> bool {
+        // bounded wait until the four softmax warps have stored the A rows of `target / 4`
+        // chunks (a monotonic counter: no phase to alias)
+        auto wait_ast = [&](uint32_t target) -> bool {
+            if (ld_acquire_cta(s_ast) >= target) return true;
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_cta(s_ast) < target) {
+                if (*s_abort) return false;
+                if (globaltimer_ns() - t0 > kWaitNs) {
+                    *s_abort = 1;
+                    atomicOr(&g_umma_error, 1u);
+                    return false;
+                }
+                __nanosleep(64);
+            }
+            return true;
+        };
+        const uint64_t pol_stream = policy_evict_first();
+        auto epilogue = [&](const TileRef &tr, int aslot) -> bool {
             if (tr.kind == 1) {
-                // H tile -> bf16 -> global
+                // H tile -> bf16 -> the ring slot that held this tile's A or Q (the MMAs have
+                // read it) -> one TMA store per warp (32 rows), then the slot is released
                 const int hb = (int)(p2 & 1u);
                 if (!wait(acc_full + hb, accuse[hb] & 1u)) return false;
                 tc_fence_after();
                 const uint32_t hcol = hb ? LY::colB1 : LY::colB0;
-                uint32_t pk[D / 2];
+                uint8_t *stage = sRing + aslot * LY::kSlotB;
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     float v[32];
                     tmem_ld32(trow + hcol + q * 32, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[q * 16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(stage + sw_off(row, q * 4 + c, kT)) = pack8_scaled(v + 8 * c, 1.f);
                 }
                 tc_fence_before();
                 arrive4(acc_empty + hb);
                 ++accuse[hb];
                 ++p2;
-                const int tok = tr.tile * kT + row;
-                if (tok < p.n) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(Hout + ((size_t)tr.slice * p.n + tok) * D);
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int r0 = tr.tile * kT + quarter * 32;
+                if (lane == 0 && r0 < p.n) {
 #pragma unroll
-                    for (int c8 = 0; c8 < D / 8; ++c8)
-                        __stcs(dst + c8, make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]));
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_store_3d(&th_st, stage + b * kT * 128 + quarter * 32 * 128, 64 * b, r0, tr.slice, pol_stream);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
                 }
+                const int tok = tr.tile * kT + row;
+                if (tr.stored && tok < p.n) {
+                    // the H MMA has read this A row: nothing reads it again, so its L2 lines
+                    // are dropped instead of being written back to memory
+                    const uint8_t *arow = reinterpret_cast<const uint8_t *>(p.abuf + ((size_t)tr.slice * p.n + tok) * MP);
+#pragma unroll
+                    for (int l = 0; l < MP * 2 / 128; ++l) discard_l2_line(arow + 128 * l);
+                }
+                ep_sync();
+                if (row == 0) mbar_arrive(slot_empty + aslot);
                 return true;
             }
             if (!tr.last) return true;
@@ -799,6 +943,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 arrive4(acc_empty + 1);
                 ++accuse[0];
                 ++accuse[1];
+                ++chunks;
+                bool published = false;
                 // Fixed binary tree over the slice's chunks: node (l, i) covers chunks
                 // [i 2^(l+1), (i+1) 2^(l+1)).  The second of its two children to arrive forms
                 // left + right into the left child's slot and climbs on; the first stops.  The
@@ -808,7 +954,13 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     if (right >= p.C1) continue;  // no right subtree at this level
                     __threadfence();
                     ep_sync();
-                    if (row == 0) *s_last = (int)atomicAdd(p.tree + (size_t)tr.slice * p.C1 + (right - 1), 1u);
+                    if (row == 0) {
+                        // this chunk's A rows must be in memory before the chunk is published;
+                        // if that wait gives up (abort), stop here as if first to arrive
+                        const bool go = published || !p.store_a || wait_ast(4u * chunks);
+                        published = true;
+                        *s_last = go ? (int)atomicAdd(p.tree + (size_t)tr.slice * p.C1 + (right - 1), 1u) : 0;
+                    }
                     ep_sync();
                     if (*s_last == 0) return true;  // first to arrive: the sibling's CTA goes on
                     __threadfence();
@@ -893,12 +1045,22 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             if (row == 0) mbar_arrive(iq_empty + iq % kIQ);
             ++iq;
             if (it.kind == kEnd) break;
-            if (it.kind == kFlush) continue;
+            // the ring positions, replayed from the item stream exactly as the producer fills
+            // them: one slot per tile (Q, or the stored A), then the previous pass-1 tile's V
+            if (it.kind == kFlush) {
+                if (lpend) ++lseq;
+                lpend = false;
+                continue;
+            }
             int a1, b1;
             const int nt = item_tiles(it, p, a1, b1);
             for (int idx = 0; idx < nt && ok; ++idx) {
-                const TileRef tr = tile_at(it, a1, b1, idx);
-                if (!epilogue(tr)) { ok = false; break; }
+                const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                const int aslot = (int)(lseq % NS);
+                ++lseq;
+                if (lpend) ++lseq;
+                lpend = tr.kind == 0;
+                if (!epilogue(tr, aslot)) { ok = false; break; }
                 if (tr.kind == 1 && tr.first) ++wuse;  // W' uses started so far
             }
         }
@@ -906,7 +1068,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, LY::kTmemCols);
     }
@@ -955,7 +1117,7 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
         return e;
     per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
 
-    CUtensorMap tq, tv, tu;
+    CUtensorMap tq, tv, tu, ta_st, ta_ld;
     const long long S = pr.slices();
     if (!make_map(&tq, pr.Q, D, pr.n, S, kT) || !make_map(&tv, pr.V, D, pr.n, S, kT) ||
         !make_map(&tu, pr.U, D, pr.m, pr.heads, MP))
@@ -980,19 +1142,30 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
     p.flags = reinterpret_cast<unsigned *>(w + 256);
     p.p2c = p.flags + 32 * S;
     p.tree = p.p2c + 32 * S;
-    // P1 runs at most K slices ahead of P2, so that the Q of the slices in flight (read in
-    // pass 1, read again in pass 2) fits in a share of L2
-    const double q_slice = (double)pr.n * D * 2;
-    p.K = (int)std::max<double>(2.0, std::min<double>((double)S, kL2QBudget / q_slice));
+    // P1 runs at most K slices ahead of P2, so that the A tiles of the slices in flight
+    // (written in pass 1, read in pass 2) fit in a share of L2
+    p.store_a = pl.store_a ? 1 : 0;
+    const double kept_slice = (double)pr.n * (pl.store_a ? MP : D) * 2;  // A copy, or Q for its re-read
+    p.K = (int)std::max<double>(2.0, std::min<double>((double)S, kL2ABudget / kept_slice));
     p.p1first = p.K >= S ? 1 : 0;
     uint8_t *after = w + pl.header_bytes;
     p.pdelta = reinterpret_cast<float *>(after);
     p.part = p.pdelta + (size_t)S * pl.C1 * MP;
     p.wimg = reinterpret_cast<uint16_t *>(p.part + (size_t)S * pl.C1 * D * MP);
+    p.abuf = reinterpret_cast<uint16_t *>(w + pl.abuf_offset);
     if (pl.C1 == 1) p.part = p.pdelta = nullptr, p.wimg = nullptr;
+    if (!pl.store_a) p.abuf = nullptr;
+    // the stored A: row-major [S][n][MP]; pass 1 stores 32-row slabs (one per softmax warp),
+    // pass 2 loads 128-row tiles.  Whole-slice plans have no stored A: the maps then point
+    // at Q, which is never touched through them.
+    const void *abase = p.abuf ? static_cast<const void *>(p.abuf) : pr.Q;
+    if (!make_map(&ta_st, abase, MP, pr.n, p.abuf ? S : 1, 32) || !make_map(&ta_ld, abase, MP, pr.n, p.abuf ? S : 1, kT))
+        return cudaErrorInvalidValue;
+    CUtensorMap th_st;  // H rows, 32-row boxes (one per epilogue warp)
+    if (!make_map(&th_st, pr.H, D, pr.n, S, 32)) return cudaErrorInvalidValue;
 
     if ((e = cudaMemsetAsync(ws, 0, pl.header_bytes, stream)) != cudaSuccess) return e;
-    kern<<<grid, kThreads, LY::kSmem, stream>>>(tq, tv, tu, p, static_cast<uint16_t *>(pr.H));
+    kern<<<grid, kThreads, LY::kSmem, stream>>>(tq, tv, tu, ta_st, ta_ld, th_st, p, static_cast<uint16_t *>(pr.H));
     return cudaGetLastError();
 }
 
@@ -1034,8 +1207,13 @@ UmmaPlan umma_plan(const Problem &p) {
     pl.C2 = (pl.NT + t2 - 1) / t2;
     pl.total_items = (int)(S * (pl.C1 + pl.C2));
     pl.header_bytes = (256 + 2 * 128 * (size_t)S + 4 * (size_t)S * pl.C1 + 1023) / 1024 * 1024;
-    pl.workspace_bytes = pl.header_bytes + 4 * (size_t)S * pl.C1 * MP + 4 * (size_t)S * pl.C1 * p.d * MP +
-                         2 * (size_t)S * p.d * MP + 1024;
+    const size_t reduce_bytes = 4 * (size_t)S * pl.C1 * MP + 4 * (size_t)S * pl.C1 * p.d * MP + 2 * (size_t)S * p.d * MP;
+    pl.abuf_offset = (pl.header_bytes + reduce_bytes + 1023) / 1024 * 1024;
+    // Pass 2 reuses pass 1's A only when every slice's copy fits in L2 together; otherwise
+    // the copy would make a round trip through memory, and recomputing A costs less traffic
+    // (one re-read of Q) than storing it (a write and a read of A).
+    pl.store_a = 2.0 * (double)S * p.n * MP <= kStoreABudget;
+    pl.workspace_bytes = pl.abuf_offset + (pl.store_a ? 2 * (size_t)S * p.n * MP : 0);
     return pl;
 }
 
