@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "linear_complexity_anchor_gb300", "csrc", f)
-                  for f in ("umma.cu", "simt.cu", "api.cu", "common.cuh")]
+                  for f in ("umma.cu", "simt.cu", "api.cu", "common.cuh", "ptx.cuh")]
 
 
 def parse_args(argv=None):

@@ -49,9 +49,9 @@ using namespace ptx;
 
 constexpr int kT = 128;                         // tokens per tile (UMMA M)
 // warps 0-7 softmax (two groups of four, each on half of the anchors of the same 128 rows),
-// 8-11 epilogue, 12 producer, 13 MMA
-constexpr int kThreads = 448;
-constexpr int kWarpProducer = 12, kWarpMma = 13;
+// 8-11 epilogue, 12 producer, 13 issues S = Q U^T, 14 issues W, Delta and H
+constexpr int kThreads = 480;
+constexpr int kWarpProducer = 12, kWarpMmaS = 13, kWarpMmaX = 14;
 constexpr int kIQ = 4;                          // item queue depth
 constexpr int kPrefetch = 0;                    // tiles of an item brought into L2 ahead of their load
 constexpr uint64_t kWaitNs = 2000000000ull;     // every wait gives up after 2 s
@@ -290,14 +290,18 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *w_full = u_empty + NU;             // [NW] (1 [+ tx]) W' image in place
     uint64_t *w_empty = w_full + NW;             // [NW] (1)       MMAs reading W' completed
     uint64_t *iq_full = w_empty + NW;            // [kIQ] (1)      item queue
-    uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (3)
+    uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (4)
     constexpr int kNumBars = 2 * NS + 2 + 2 + 2 * NA + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ;
-    static_assert(kNumBars * 8 + 3 * 4 * kIQ + 64 <= LY::kBarB, "barrier area");
+    static_assert(kNumBars * 8 + 3 * 4 * kIQ + 16 + 4 * NS <= LY::kBarB, "barrier area");
     int *s_items = reinterpret_cast<int *>(bars + kNumBars);           // [kIQ][3]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_items + 3 * kIQ);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_last = reinterpret_cast<int *>(s_tmem + 2);
     uint32_t *s_ast = s_tmem + 3;  // softmax-warp chunk ends whose A stores are complete
+    // ring slot tags: the load sequence number a slot was last filled with.  Two threads
+    // consume the ring, each skipping the other's slots, so a parity wait alone could match a
+    // phase two loads old; a consumer first sees its own tag, then waits for the phase.
+    uint32_t *s_slot_seq = s_tmem + 4;  // [NS]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -326,10 +330,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         for (int i = 0; i < kIQ; ++i) {
             mbar_init(iq_full + i, 1);
-            mbar_init(iq_empty + i, 3);
+            mbar_init(iq_empty + i, 4);
         }
         *s_abort = 0;
         *s_ast = 0;
+        for (int i = 0; i < NS; ++i) s_slot_seq[i] = 0xffffffffu;
         fence_mbar_init();
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tv);
@@ -340,7 +345,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
     for (int i = tid; i < LY::kOnesB / 4; i += kThreads) reinterpret_cast<uint32_t *>(sOnes)[i] = 0x3F803F80u;
     for (int i = tid; i < NA * LY::kAB / 16; i += kThreads) reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0, 0, 0, 0);
-    if (warp == kWarpMma) tmem_alloc(s_tmem, LY::kTmemCols);
+    if (warp == kWarpMmaS) tmem_alloc(s_tmem, LY::kTmemCols);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -360,6 +365,23 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 return false;
             }
         }
+    };
+    // wait for ring load number `seq` (see s_slot_seq)
+    auto wait_slot = [&](uint32_t seq) -> bool {
+        uint32_t *tag = s_slot_seq + seq % NS;
+        if (ld_acquire_cta(tag) != seq) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_cta(tag) != seq) {
+                if (*s_abort) return false;
+                if (globaltimer_ns() - t0 > kWaitNs) {
+                    *s_abort = 1;
+                    atomicOr(&g_umma_error, 1u);
+                    return false;
+                }
+                __nanosleep(32);
+            }
+        }
+        return wait(slot_full + seq % NS, (seq / NS) & 1u);
     };
     auto read_item = [&](uint32_t iq) -> Item {
         const int *e = s_items + 3 * (int)(iq % kIQ);
@@ -388,6 +410,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             const int st = (int)(ld_seq % NS);
             if (!wwait(slot_empty + st, ((ld_seq / NS) & 1u) ^ 1u)) return false;
             if (L0) {
+                st_release_cta(s_slot_seq + st, ld_seq);
                 mbar_arrive_expect_tx(slot_full + st, (uint32_t)(kT * cols * 2));
                 for (int b = 0; b < cols / 64; ++b)
                     tma_load_3d(sRing + st * LY::kSlotB + b * kT * 128, map, slot_full + st, 64 * b, tile * kT, slice, pol);
@@ -599,153 +622,172 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
         }
         if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream, D);
-    } else if (warp == kWarpMma) {
-        // =========================================================== MMA issuer
+    } else if (warp == kWarpMmaS || warp == kWarpMmaX) {
+        // =========================================================== MMA issue
+        // Two issuing threads, so that neither kind of MMA waits behind the other: warp 13
+        // issues S = Q U^T as soon as a Q tile and an S buffer are there; warp 14 issues
+        // W += A^T V, Delta += A^T 1 and H = A W' as soon as their A tile is written.  Both
+        // replay the producer's ring order from the item stream: per tile one slot (Q, or a
+        // stored A), then the previous pass-1 tile's V.  Descriptors advance by adding the
+        // K-step offset to the start-address field.
         if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_bf16_f32(128, MP, false, false);
-            constexpr uint32_t kIdW = idesc_bf16_f32(128, D, true, true);
-            constexpr uint32_t kIdD = idesc_bf16_f32(128, 16, true, false);
-            constexpr uint32_t kIdH = idesc_bf16_f32(128, D, false, true);
-            const uint32_t sUa = smem_u32(sU), sAa = smem_u32(sA), sWa = smem_u32(sW);
-            const uint32_t sRa = smem_u32(sRing), sOa = smem_u32(sOnes);
-            uint32_t cons = 0, sidx = 0, iq = 0, nu = 0, xk = 0, wuse = 0, p2 = 0;
-            uint32_t accuse[2] = {0u, 0u};
-            int prev_head = -1;
-            TileRef pend;
-            bool has_pend = false, ok = true;
-
-            auto do_x = [&](const TileRef &tr) -> bool {
-                const int ab = (int)(xk % NA);
-                if (!wait(a_full + ab, (xk / NA) & 1u)) return false;
-                const uint32_t sAb = sAa + ab * LY::kAB;
-                if (tr.kind == 0) {
-                    const int vs = (int)(cons % NS);
-                    if (!wait(slot_full + vs, (cons / NS) & 1u)) return false;
-                    ++cons;
-                    if (tr.first) {
-                        if (!wait(acc_empty + 0, (accuse[0] & 1u) ^ 1u)) return false;
-                        if (!wait(acc_empty + 1, (accuse[1] & 1u) ^ 1u)) return false;
+            const uint32_t sRa = smem_u32(sRing);
+            uint32_t lseq = 0, iq = 0;
+            bool lpend = false, ok = true;
+            if (warp == kWarpMmaS) {
+                constexpr uint32_t kIdS = idesc_bf16_f32(128, MP, false, false);
+                const uint32_t sUa = smem_u32(sU);
+                uint32_t sidx = 0, nu = 0;
+                int prev_head = -1;
+                while (ok) {
+                    if (!wait(iq_full + iq % kIQ, (iq / kIQ) & 1u)) break;
+                    const Item it = read_item(iq);
+                    mbar_arrive(iq_empty + iq % kIQ);
+                    ++iq;
+                    if (it.kind == kEnd) break;
+                    if (it.kind == kFlush) {
+                        if (lpend) ++lseq;
+                        lpend = false;
+                        continue;
                     }
-                    tc_fence_after();
+                    const int h = it.slice % p.heads;
+                    if ((it.kind != 1 || !p.store_a) && h != prev_head) {
+                        if (prev_head >= 0) umma_commit(u_empty + (nu - 1) % NU);  // every S on the old U issued
+                        if (!wait(u_full + nu % NU, (nu / NU) & 1u)) break;
+                        ++nu;
+                        prev_head = h;
+                    }
+                    const uint64_t bdesc = smem_desc_sw128(sUa + ((nu - 1) % NU) * LY::kUB, 16, 1024);
+                    int a1, b1;
+                    const int nt = item_tiles(it, p, a1, b1);
+                    for (int idx = 0; idx < nt && ok; ++idx) {
+                        const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                        const uint32_t mseq = lseq++;
+                        if (lpend) ++lseq;
+                        lpend = tr.kind == 0;
+                        if (tr.stored) continue;
+                        const int qslot = (int)(mseq % NS);
+                        if (!wait_slot(mseq)) { ok = false; break; }
+                        const int sb = (int)(sidx & 1u);
+                        if (!wait(s_empty + sb, ((sidx >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t dcol = sb ? LY::colS1 : LY::colS0;
+                        const uint64_t adesc = smem_desc_sw128(sRa + qslot * LY::kSlotB, 16, 1024);
 #pragma unroll
-                    for (int kt = 0; kt < kT / 16; ++kt) {
-                        const uint64_t ad = smem_desc_sw128(sAb + kt * 2048, 16384, 1024);
-                        const uint64_t vd = smem_desc_sw128(sRa + vs * LY::kSlotB + kt * 2048, 16384, 1024);
-                        const uint64_t od = smem_desc_sw128(sOa + (kt >> 2) * 2048 + (kt & 3) * 32, 16, 1024);
-                        const uint32_t acc = (!tr.first || kt > 0) ? 1u : 0u;
-                        umma_bf16(tmem + LY::colB0, ad, vd, kIdW, acc);
-                        umma_bf16(tmem + LY::colB1, ad, od, kIdD, acc);
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            umma_bf16(tmem + dcol, adesc + (uint64_t)((((kk >> 2) * kT * 128) + (kk & 3) * 32) >> 4),
+                                      bdesc + (uint64_t)((((kk >> 2) * MP * 128) + (kk & 3) * 32) >> 4), kIdS, kk > 0);
+                        umma_commit(s_full + sb);
+                        // a pass-2 tile's Q slot stays held: the epilogue stages the H tile there
+                        if (tr.kind == 0) umma_commit(slot_empty + qslot);
+                        ++sidx;
                     }
-                    umma_commit(a_empty + ab);
-                    umma_commit(slot_empty + vs);
-                    if (tr.last) {
-                        umma_commit(acc_full + 0);
-                        umma_commit(acc_full + 1);
-                        ++accuse[0];
-                        ++accuse[1];
-                    }
-                } else {
+                }
+            } else {
+                constexpr uint32_t kIdW = idesc_bf16_f32(128, D, true, true);
+                constexpr uint32_t kIdD = idesc_bf16_f32(128, 16, true, false);
+                constexpr uint32_t kIdH = idesc_bf16_f32(128, D, false, true);
+                const uint32_t sAa = smem_u32(sA), sWa = smem_u32(sW);
+                const uint64_t odesc = smem_desc_sw128(smem_u32(sOnes), 16, 1024);
+                uint32_t xk = 0, wuse = 0, p2 = 0;
+                uint32_t accuse[2] = {0u, 0u};
+                TileRef pv;
+                // H = A W' from A at `adesc` (K-major) into the next H buffer
+                auto issue_h = [&](const TileRef &tr, uint64_t adesc) -> bool {
                     const int wb = (int)((tr.first ? wuse : wuse - 1u) % NW);  // this pass-2 phase's W'
                     if (tr.first) {
                         if (!wait(w_full + wb, (wuse / NW) & 1u)) return false;
                         ++wuse;
                     }
-                    const uint32_t sWb = sWa + wb * LY::kWB;
                     const int hb = (int)(p2 & 1u);
                     if (!wait(acc_empty + hb, (accuse[hb] & 1u) ^ 1u)) return false;
                     tc_fence_after();
+                    const uint64_t wdesc = smem_desc_sw128(sWa + wb * LY::kWB, MP * 128, 1024);
                     const uint32_t dcol = hb ? LY::colB1 : LY::colB0;
 #pragma unroll
-                    for (int kj = 0; kj < MP / 16; ++kj) {
-                        const uint64_t ad = smem_desc_sw128(sAb + (kj >> 2) * 16384 + (kj & 3) * 32, 16, 1024);
-                        const uint64_t wd = smem_desc_sw128(sWb + kj * 2048, MP * 128, 1024);
-                        umma_bf16(tmem + dcol, ad, wd, kIdH, kj > 0);
-                    }
-                    umma_commit(a_empty + ab);
+                    for (int kj = 0; kj < MP / 16; ++kj)
+                        umma_bf16(tmem + dcol, adesc + (uint64_t)((((kj >> 2) * kT * 128) + (kj & 3) * 32) >> 4),
+                                  wdesc + (uint64_t)(kj * 128), kIdH, kj > 0);
                     umma_commit(acc_full + hb);
                     ++accuse[hb];
                     ++p2;
                     if (tr.last) umma_commit(w_empty + wb);
-                }
-                ++xk;
-                return true;
-            };
-
-            while (ok) {
-                if (!wait(iq_full + iq % kIQ, (iq / kIQ) & 1u)) break;
-                const Item it = read_item(iq);
-                mbar_arrive(iq_empty + iq % kIQ);
-                ++iq;
-                if (it.kind == kEnd) break;
-                if (it.kind == kFlush) {
-                    if (has_pend && !do_x(pend)) break;
-                    has_pend = false;
-                    continue;
-                }
-                const int h = it.slice % p.heads;
-                if ((it.kind != 1 || !p.store_a) && h != prev_head) {
-                    if (prev_head >= 0) umma_commit(u_empty + (nu - 1) % NU);  // every S on the old U issued
-                    if (!wait(u_full + nu % NU, (nu / NU) & 1u)) break;
-                    ++nu;
-                    prev_head = h;
-                }
-                const uint32_t sUb = sUa + ((nu - 1) % NU) * LY::kUB;
-                int a1, b1;
-                const int nt = item_tiles(it, p, a1, b1);
-                for (int idx = 0; idx < nt && ok; ++idx) {
-                    const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
-                    const int qslot = (int)(cons % NS);
-                    if (!wait(slot_full + qslot, (cons / NS) & 1u)) { ok = false; break; }
-                    ++cons;
-                    if (tr.stored) {
-                        // pass 2 of a split slice: the slot holds the A tile pass 1 stored
-                        // (the ring has it ahead of the pending pass-1 tile's V)
-                        if (has_pend && !do_x(pend)) { ok = false; break; }
-                        has_pend = false;
-                        const int wb = (int)((tr.first ? wuse : wuse - 1u) % NW);
+                    return true;
+                };
+                // the softmax's A tile of `tr`: pass 1 (W, Delta; V at ring position vseq) or
+                // pass 2 recomputed (H)
+                auto do_x = [&](const TileRef &tr, uint32_t vseq) -> bool {
+                    const int ab = (int)(xk % NA);
+                    if (!wait(a_full + ab, (xk / NA) & 1u)) return false;
+                    const uint32_t sAb = sAa + ab * LY::kAB;
+                    if (tr.kind == 0) {
+                        const int vs = (int)(vseq % NS);
+                        if (!wait_slot(vseq)) return false;
                         if (tr.first) {
-                            if (!wait(w_full + wb, (wuse / NW) & 1u)) { ok = false; break; }
-                            ++wuse;
+                            if (!wait(acc_empty + 0, (accuse[0] & 1u) ^ 1u)) return false;
+                            if (!wait(acc_empty + 1, (accuse[1] & 1u) ^ 1u)) return false;
                         }
-                        const uint32_t sWb = sWa + wb * LY::kWB;
-                        const int hb = (int)(p2 & 1u);
-                        if (!wait(acc_empty + hb, (accuse[hb] & 1u) ^ 1u)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t dcol = hb ? LY::colB1 : LY::colB0;
-                        const uint32_t sAt = sRa + qslot * LY::kSlotB;
+                        const uint64_t adesc = smem_desc_sw128(sAb, 16384, 1024);
+                        const uint64_t vdesc = smem_desc_sw128(sRa + vs * LY::kSlotB, 16384, 1024);
 #pragma unroll
-                        for (int kj = 0; kj < MP / 16; ++kj) {
-                            const uint64_t ad = smem_desc_sw128(sAt + (kj >> 2) * kT * 128 + (kj & 3) * 32, 16, 1024);
-                            const uint64_t wd = smem_desc_sw128(sWb + kj * 2048, MP * 128, 1024);
-                            umma_bf16(tmem + dcol, ad, wd, kIdH, kj > 0);
+                        for (int kt = 0; kt < kT / 16; ++kt) {
+                            const uint32_t acc = (!tr.first || kt > 0) ? 1u : 0u;
+                            umma_bf16(tmem + LY::colB0, adesc + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), kIdW, acc);
+                            umma_bf16(tmem + LY::colB1, adesc + (uint64_t)(kt * 128),
+                                      odesc + (uint64_t)((((kt >> 2) * 2048) + (kt & 3) * 32) >> 4), kIdD, acc);
                         }
-                        // the slot is released by the epilogue, which stages the H tile in it
-                        umma_commit(acc_full + hb);
-                        ++accuse[hb];
-                        ++p2;
-                        if (tr.last) umma_commit(w_empty + wb);
+                        umma_commit(a_empty + ab);
+                        umma_commit(slot_empty + vs);
+                        if (tr.last) {
+                            umma_commit(acc_full + 0);
+                            umma_commit(acc_full + 1);
+                            ++accuse[0];
+                            ++accuse[1];
+                        }
+                    } else {
+                        if (!issue_h(tr, smem_desc_sw128(sAb, 16, 1024))) return false;
+                        umma_commit(a_empty + ab);
+                    }
+                    ++xk;
+                    return true;
+                };
+                while (ok) {
+                    if (!wait(iq_full + iq % kIQ, (iq / kIQ) & 1u)) break;
+                    const Item it = read_item(iq);
+                    mbar_arrive(iq_empty + iq % kIQ);
+                    ++iq;
+                    if (it.kind == kEnd) break;
+                    if (it.kind == kFlush) {  // the producer loads the held-back V now
+                        if (lpend && !do_x(pv, lseq++)) break;
+                        lpend = false;
                         continue;
                     }
-                    const int sb = (int)(sidx & 1u);
-                    if (!wait(s_empty + sb, ((sidx >> 1) & 1u) ^ 1u)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t dcol = sb ? LY::colS1 : LY::colS0;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t a = smem_desc_sw128(sRa + qslot * LY::kSlotB + (kk >> 2) * kT * 128 + (kk & 3) * 32, 16, 1024);
-                        const uint64_t b = smem_desc_sw128(sUb + (kk >> 2) * MP * 128 + (kk & 3) * 32, 16, 1024);
-                        umma_bf16(tmem + dcol, a, b, kIdS, kk > 0);
+                    int a1, b1;
+                    const int nt = item_tiles(it, p, a1, b1);
+                    for (int idx = 0; idx < nt && ok; ++idx) {
+                        const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                        const uint32_t mseq = lseq++;
+                        if (lpend) {  // the previous pass-1 tile's V follows this tile's first slot
+                            if (!do_x(pv, lseq++)) { ok = false; break; }
+                            lpend = false;
+                        }
+                        if (tr.kind == 0) {
+                            pv = tr;
+                            lpend = true;
+                        } else if (tr.stored) {
+                            // the slot holds the A tile pass 1 stored; the epilogue releases it
+                            const int aslot = (int)(mseq % NS);
+                            if (!wait_slot(mseq)) { ok = false; break; }
+                            if (!issue_h(tr, smem_desc_sw128(sRa + aslot * LY::kSlotB, 16, 1024))) { ok = false; break; }
+                        } else if (!do_x(tr, 0)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                    umma_commit(s_full + sb);
-                    // a pass-2 tile's Q slot stays held: the epilogue stages the H tile there
-                    if (tr.kind == 0) umma_commit(slot_empty + qslot);
-                    ++sidx;
-                    if (has_pend && !do_x(pend)) { ok = false; break; }
-                    pend = tr;
-                    has_pend = true;
                 }
+                if (ok && lpend) do_x(pv, lseq++);  // after the end marker the producer loads the last V
             }
-            if (ok && has_pend) do_x(pend);
         }
     } else if (warp < 8) {
         // =========================================================== softmax (warps 0-7)
@@ -1068,7 +1110,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kWarpMmaS) {
         tc_fence_after();
         tmem_dealloc(tmem, LY::kTmemCols);
     }
