@@ -280,8 +280,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *slot_full = bars;                  // [NS] (1 + tx)  TMA landed
     uint64_t *slot_empty = slot_full + NS;       // [NS] (1)       MMA that read the slot completed
     uint64_t *s_full = slot_empty + NS;          // [2]  (1)       scores in S buffer
-    uint64_t *s_empty = s_full + 2;              // [2]  (8)       softmax warps read the S buffer
-    uint64_t *a_full = s_empty + 2;              // [NA] (1)       A tile written
+    uint64_t *s_empty = s_full + 2;              // [2]  (1)       S buffer free (read, or its P consumed)
+    uint64_t *p_full = s_empty + 2;              // [2]  (1)       pass-2 A (P) written over the S buffer
+    uint64_t *a_full = p_full + 2;               // [NA] (1)       A tile written
     uint64_t *a_empty = a_full + NA;             // [NA] (1)       MMA reading the A tile completed
     uint64_t *acc_full = a_empty + NA;           // [2]  (1)       W/Delta or H complete in TMEM
     uint64_t *acc_empty = acc_full + 2;          // [2]  (4)       epilogue read it
@@ -291,7 +292,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *w_empty = w_full + NW;             // [NW] (1)       MMAs reading W' completed
     uint64_t *iq_full = w_empty + NW;            // [kIQ] (1)      item queue
     uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (4)
-    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 * NA + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ;
+    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 + 2 * NA + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ;
     static_assert(kNumBars * 8 + 3 * 4 * kIQ + 16 + 4 * NS <= LY::kBarB, "barrier area");
     int *s_items = reinterpret_cast<int *>(bars + kNumBars);           // [kIQ][3]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_items + 3 * kIQ);
@@ -312,7 +313,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + i, 1);
-            mbar_init(s_empty + i, 8);
+            mbar_init(s_empty + i, 1);
+            mbar_init(p_full + i, 1);
             mbar_init(acc_full + i, 1);
             mbar_init(acc_empty + i, 4);
         }
@@ -692,8 +694,10 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 uint32_t xk = 0, wuse = 0, p2 = 0;
                 uint32_t accuse[2] = {0u, 0u};
                 TileRef pv;
-                // H = A W' from A at `adesc` (K-major) into the next H buffer
-                auto issue_h = [&](const TileRef &tr, uint64_t adesc) -> bool {
+                uint32_t xs = 0, pcnt[2] = {0u, 0u};  // S tiles seen; pass-2 A's seen per S buffer
+                // H = A W' into the next H buffer; A at `adesc` (K-major, shared memory) or, with
+                // from_tmem, in tensor memory at a_tmem
+                auto issue_h = [&](const TileRef &tr, uint64_t adesc, uint32_t a_tmem, bool from_tmem) -> bool {
                     const int wb = (int)((tr.first ? wuse : wuse - 1u) % NW);  // this pass-2 phase's W'
                     if (tr.first) {
                         if (!wait(w_full + wb, (wuse / NW) & 1u)) return false;
@@ -704,18 +708,23 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     tc_fence_after();
                     const uint64_t wdesc = smem_desc_sw128(sWa + wb * LY::kWB, MP * 128, 1024);
                     const uint32_t dcol = hb ? LY::colB1 : LY::colB0;
+                    if (from_tmem) {
 #pragma unroll
-                    for (int kj = 0; kj < MP / 16; ++kj)
-                        umma_bf16(tmem + dcol, adesc + (uint64_t)((((kj >> 2) * kT * 128) + (kj & 3) * 32) >> 4),
-                                  wdesc + (uint64_t)(kj * 128), kIdH, kj > 0);
+                        for (int kj = 0; kj < MP / 16; ++kj)
+                            umma_bf16_tmem_a(tmem + dcol, a_tmem + kj * 8, wdesc + (uint64_t)(kj * 128), kIdH, kj > 0);
+                    } else {
+#pragma unroll
+                        for (int kj = 0; kj < MP / 16; ++kj)
+                            umma_bf16(tmem + dcol, adesc + (uint64_t)((((kj >> 2) * kT * 128) + (kj & 3) * 32) >> 4),
+                                      wdesc + (uint64_t)(kj * 128), kIdH, kj > 0);
+                    }
                     umma_commit(acc_full + hb);
                     ++accuse[hb];
                     ++p2;
                     if (tr.last) umma_commit(w_empty + wb);
                     return true;
                 };
-                // the softmax's A tile of `tr`: pass 1 (W, Delta; V at ring position vseq) or
-                // pass 2 recomputed (H)
+                // pass 1: W += A^T V, Delta += A^T 1 from the softmax's A tile (V at ring position vseq)
                 auto do_x = [&](const TileRef &tr, uint32_t vseq) -> bool {
                     const int ab = (int)(xk % NA);
                     if (!wait(a_full + ab, (xk / NA) & 1u)) return false;
@@ -745,9 +754,6 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                             ++accuse[0];
                             ++accuse[1];
                         }
-                    } else {
-                        if (!issue_h(tr, smem_desc_sw128(sAb, 16, 1024))) return false;
-                        umma_commit(a_empty + ab);
                     }
                     ++xk;
                     return true;
@@ -772,6 +778,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                             if (!do_x(pv, lseq++)) { ok = false; break; }
                             lpend = false;
                         }
+                        const int sbx = (int)(xs & 1u);  // this tile's S buffer (tiles with an S only)
+                        if (!tr.stored) ++xs;
                         if (tr.kind == 0) {
                             pv = tr;
                             lpend = true;
@@ -779,10 +787,13 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                             // the slot holds the A tile pass 1 stored; the epilogue releases it
                             const int aslot = (int)(mseq % NS);
                             if (!wait_slot(mseq)) { ok = false; break; }
-                            if (!issue_h(tr, smem_desc_sw128(sRa + aslot * LY::kSlotB, 16, 1024))) { ok = false; break; }
-                        } else if (!do_x(tr, 0)) {
-                            ok = false;
-                            break;
+                            if (!issue_h(tr, smem_desc_sw128(sRa + aslot * LY::kSlotB, 16, 1024), 0u, false)) { ok = false; break; }
+                        } else {
+                            // recomputed pass-2 A, written by the softmax over its S buffer
+                            if (!wait(p_full + sbx, pcnt[sbx] & 1u)) { ok = false; break; }
+                            ++pcnt[sbx];
+                            if (!issue_h(tr, 0ull, tmem + (sbx ? LY::colS1 : LY::colS0), true)) { ok = false; break; }
+                            umma_commit(s_empty + sbx);
                         }
                     }
                 }
@@ -825,12 +836,14 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 if (p.m == MP) softmax_half<MP, false>(ts, g * HM, p.m, p.c, v, mg, zg);
                 else softmax_half<MP, true>(ts, g * HM, p.m, p.c, v, mg, zg);
                 tc_fence_before();
-                arrive_w(s_empty + sb);
                 // the last A store of this group has read its rows before anyone rewrites them
                 if (g == 0 && lane == 0) bulk_wait_group_read0();
                 float2 *xc = sXch + (size_t)(sb * 2) * kT;
                 xc[g * kT + row] = make_float2(mg, zg);
-                sm_sync();
+                sm_sync();  // both halves have read the S buffer
+                // pass 1 frees the S buffer now; pass 2 writes its A over it, and the MMA that
+                // consumes that A frees it
+                if (tr.kind == 0 && tid == 0) mbar_arrive(s_empty + sb);
                 const float2 o = xc[(g ^ 1) * kT + row];
                 ++sidx;
                 const float mrow = fmaxf(mg, o.x);
@@ -844,6 +857,17 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     float x0, x1;
                     f32x2_split(mul_f32x2(f32x2(v[2 * j], v[2 * j + 1]), sc2), x0, x1);
                     pk[j] = pack_bf16x2(x0, x1);
+                }
+                if (tr.kind == 1) {
+                    // pass 2: A (bf16 pairs) into the first MP/2 columns of the S buffer, the
+                    // A operand of H = A W' straight from tensor memory
+                    if (HM / 2 == 32) tmem_st32(ts - g * HM + g * (HM / 2), pk);
+                    else tmem_st16(ts - g * HM + g * (HM / 2), pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    sm_sync();
+                    if (tid == 0) mbar_arrive(p_full + sb);
+                    continue;
                 }
                 const int ab = (int)(ause % NA);
                 if (!wait(a_empty + ab, ((ause / NA) & 1u) ^ 1u)) { ok = false; break; }
