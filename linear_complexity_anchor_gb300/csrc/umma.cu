@@ -1018,18 +1018,18 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 for (int l = 0; (1 << l) < p.C1; ++l) {
                     const int left = (tr.chunk >> (l + 1)) << (l + 1), right = left + (1 << l);
                     if (right >= p.C1) continue;  // no right subtree at this level
-                    __threadfence();
+                    // the group's partial writes are ordered before thread 0's release by the
+                    // barrier; its acquire orders the sibling's partial before the group's reads
                     ep_sync();
                     if (row == 0) {
                         // this chunk's A rows must be in memory before the chunk is published;
                         // if that wait gives up (abort), stop here as if first to arrive
                         const bool go = published || !p.store_a || wait_ast(4u * chunks);
                         published = true;
-                        *s_last = go ? (int)atomicAdd(p.tree + (size_t)tr.slice * p.C1 + (right - 1), 1u) : 0;
+                        *s_last = go ? (int)atom_add_acq_rel_gpu(p.tree + (size_t)tr.slice * p.C1 + (right - 1), 1u) : 0;
                     }
                     ep_sync();
                     if (*s_last == 0) return true;  // first to arrive: the sibling's CTA goes on
-                    __threadfence();
                     const bool root = (2 << l) >= p.C1;
                     if (row < MP) {
                         const size_t dl_ = ((size_t)tr.slice * p.C1 + left) * MP + row;
@@ -1069,8 +1069,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         if (!root) p.pdelta[dl_] = dsum;
                     }
                     if (root) {
-                        __threadfence();
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        // the image is read by bulk copies: order it for the async proxy; the
+                        // flag's release (after the barrier) publishes every thread's writes
+                        fence_proxy_async_global();
                         ep_sync();
                         if (row == 0) st_release_gpu(p.flags + 32 * tr.slice, 1u);
                         return true;
