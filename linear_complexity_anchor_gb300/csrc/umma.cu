@@ -84,7 +84,11 @@ struct Layout {
     static constexpr int kUB = MP * D * 2;
     static constexpr int kAB = kT * 128 * 2;           // A tile, 128 anchor columns
     static constexpr int kWB = D * MP * 2;             // W' operand image
-    static constexpr int kOnesB = 16 * kT * 2;         // 16 x 128 ones (bf16)
+    // ones for Delta = A^T 1.  d = 64: a whole 128-token x 64-column MN-major block that the
+    // W MMA reads as columns d .. d+15 of its B operand (W and Delta in one N = d + 16 MMA);
+    // d = 128: a 16 x 128 K-major B operand of its own N = 16 MMA.
+    static constexpr bool kFoldDelta = D == 64;
+    static constexpr int kOnesB = kFoldDelta ? kT * 128 : 16 * kT * 2;
     static constexpr int kXchB = 2 * 2 * kT * 8;        // softmax halves' (max, sum), by tile parity
     static constexpr int kBarB = 1024;
     static constexpr int kMaxDyn = 227 * 1024 - 1024;  // minus the alignment slack
@@ -105,9 +109,14 @@ struct Layout {
     static constexpr int offBar = offXch + kXchB;
     static constexpr int kBytes = offBar + kBarB;
     static constexpr int kSmem = kBytes + 1024;
-    // TMEM: S0 | S1 | B0 (W in pass 1, H0 in pass 2) | B1 (Delta in pass 1, H1 in pass 2)
+    // TMEM: S0 | S1 | B0 (H0) | B1 (H1) and the pass-1 chunk accumulators W | Delta: two sets
+    // of their own when they fit (a chunk starts while the epilogue drains the last one), else
+    // one set over B0 | B1 (W at B0, Delta at B1 = B0 + D), shared with H
     static constexpr int colS0 = 0, colS1 = MP, colB0 = 2 * MP, colB1 = 2 * MP + D;
-    static constexpr int kTmemCols = (2 * MP + 2 * D) <= 256 ? 256 : 512;
+    static constexpr bool kWSep = 2 * MP + 2 * D + 2 * (D + 16) <= 512;
+    static constexpr int colW0 = kWSep ? 2 * MP + 2 * D : colB0;
+    static constexpr int colW1 = kWSep ? colW0 + D + 16 : colB0;
+    static constexpr int kTmemCols = kWSep ? 512 : ((2 * MP + 2 * D) <= 256 ? 256 : 512);
     static_assert(kNSlot >= 3, "ring too shallow");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
     static_assert(kUB % 1024 == 0 && offA % 1024 == 0 && offW % 1024 == 0 && offRing % 1024 == 0 &&
@@ -286,13 +295,15 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *a_empty = a_full + NA;             // [NA] (1)       MMA reading the A tile completed
     uint64_t *acc_full = a_empty + NA;           // [2]  (1)       W/Delta or H complete in TMEM
     uint64_t *acc_empty = acc_full + 2;          // [2]  (4)       epilogue read it
-    uint64_t *u_full = acc_empty + 2;            // [NU] (1 + tx)  U landed
+    uint64_t *wacc_full = acc_empty + 2;         // [2]  (1)       chunk W, Delta complete (separate sets)
+    uint64_t *wacc_empty = wacc_full + 2;        // [2]  (4)       epilogue read them
+    uint64_t *u_full = wacc_empty + 2;           // [NU] (1 + tx)  U landed
     uint64_t *u_empty = u_full + NU;             // [NU] (1)       MMAs on that U completed
     uint64_t *w_full = u_empty + NU;             // [NW] (1 [+ tx]) W' image in place
     uint64_t *w_empty = w_full + NW;             // [NW] (1)       MMAs reading W' completed
     uint64_t *iq_full = w_empty + NW;            // [kIQ] (1)      item queue
     uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (4)
-    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 + 2 * NA + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ;
+    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 + 2 * NA + 2 + 2 + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ;
     static_assert(kNumBars * 8 + 3 * 4 * kIQ + 16 + 4 * NS <= LY::kBarB, "barrier area");
     int *s_items = reinterpret_cast<int *>(bars + kNumBars);           // [kIQ][3]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_items + 3 * kIQ);
@@ -317,6 +328,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_init(p_full + i, 1);
             mbar_init(acc_full + i, 1);
             mbar_init(acc_empty + i, 4);
+            mbar_init(wacc_full + i, 1);
+            mbar_init(wacc_empty + i, 4);
         }
         for (int i = 0; i < NA; ++i) {
             mbar_init(a_full + i, 1);
@@ -688,6 +701,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             } else {
                 constexpr uint32_t kIdW = idesc_bf16_f32(128, D, true, true);
                 constexpr uint32_t kIdD = idesc_bf16_f32(128, 16, true, false);
+                constexpr uint32_t kIdWD = idesc_bf16_f32(128, D + 16, true, true);  // W | Delta
+                const uint32_t sOnesA = smem_u32(sOnes);
                 constexpr uint32_t kIdH = idesc_bf16_f32(128, D, false, true);
                 const uint32_t sAa = smem_u32(sA), sWa = smem_u32(sW);
                 const uint64_t odesc = smem_desc_sw128(smem_u32(sOnes), 16, 1024);
@@ -695,6 +710,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 uint32_t accuse[2] = {0u, 0u};
                 TileRef pv;
                 uint32_t xs = 0, pcnt[2] = {0u, 0u};  // S tiles seen; pass-2 A's seen per S buffer
+                uint32_t xw = 0;                      // pass-1 chunks started (separate W sets)
                 // H = A W' into the next H buffer; A at `adesc` (K-major, shared memory) or, with
                 // from_tmem, in tensor memory at a_tmem
                 auto issue_h = [&](const TileRef &tr, uint64_t adesc, uint32_t a_tmem, bool from_tmem) -> bool {
@@ -732,27 +748,50 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     if (tr.kind == 0) {
                         const int vs = (int)(vseq % NS);
                         if (!wait_slot(vseq)) return false;
+                        const int wbuf = (int)(xw & 1u);
                         if (tr.first) {
-                            if (!wait(acc_empty + 0, (accuse[0] & 1u) ^ 1u)) return false;
-                            if (!wait(acc_empty + 1, (accuse[1] & 1u) ^ 1u)) return false;
+                            if constexpr (LY::kWSep) {
+                                if (!wait(wacc_empty + wbuf, ((xw >> 1) & 1u) ^ 1u)) return false;
+                            } else {
+                                if (!wait(acc_empty + 0, (accuse[0] & 1u) ^ 1u)) return false;
+                                if (!wait(acc_empty + 1, (accuse[1] & 1u) ^ 1u)) return false;
+                            }
                         }
+                        const uint32_t wcol = wbuf ? LY::colW1 : LY::colW0;
                         tc_fence_after();
                         const uint64_t adesc = smem_desc_sw128(sAb, 16384, 1024);
-                        const uint64_t vdesc = smem_desc_sw128(sRa + vs * LY::kSlotB, 16384, 1024);
+                        if constexpr (LY::kFoldDelta) {
+                            // second 64-column block of B = the ones block: the leading-byte
+                            // offset spans from this slot to it (columns D.. of the result =
+                            // Delta)
+                            const uint32_t vbase = sRa + vs * LY::kSlotB;
+                            const uint64_t vdesc = smem_desc_sw128(vbase, sOnesA - vbase, 1024);
 #pragma unroll
-                        for (int kt = 0; kt < kT / 16; ++kt) {
-                            const uint32_t acc = (!tr.first || kt > 0) ? 1u : 0u;
-                            umma_bf16(tmem + LY::colB0, adesc + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), kIdW, acc);
-                            umma_bf16(tmem + LY::colB1, adesc + (uint64_t)(kt * 128),
-                                      odesc + (uint64_t)((((kt >> 2) * 2048) + (kt & 3) * 32) >> 4), kIdD, acc);
+                            for (int kt = 0; kt < kT / 16; ++kt)
+                                umma_bf16(tmem + wcol, adesc + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), kIdWD,
+                                          (!tr.first || kt > 0) ? 1u : 0u);
+                        } else {
+                            const uint64_t vdesc = smem_desc_sw128(sRa + vs * LY::kSlotB, 16384, 1024);
+#pragma unroll
+                            for (int kt = 0; kt < kT / 16; ++kt) {
+                                const uint32_t acc = (!tr.first || kt > 0) ? 1u : 0u;
+                                umma_bf16(tmem + wcol, adesc + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), kIdW, acc);
+                                umma_bf16(tmem + wcol + D, adesc + (uint64_t)(kt * 128),
+                                          odesc + (uint64_t)((((kt >> 2) * 2048) + (kt & 3) * 32) >> 4), kIdD, acc);
+                            }
                         }
                         umma_commit(a_empty + ab);
                         umma_commit(slot_empty + vs);
                         if (tr.last) {
-                            umma_commit(acc_full + 0);
-                            umma_commit(acc_full + 1);
-                            ++accuse[0];
-                            ++accuse[1];
+                            if constexpr (LY::kWSep) {
+                                umma_commit(wacc_full + wbuf);
+                            } else {
+                                umma_commit(acc_full + 0);
+                                umma_commit(acc_full + 1);
+                                ++accuse[0];
+                                ++accuse[1];
+                            }
+                            ++xw;
                         }
                     }
                     ++xk;
@@ -907,7 +946,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // TMEM lane: token row (H) / anchor row (W)
         const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint32_t iq = 0, p2 = 0, wuse = 0, chunks = 0, lseq = 0;
+        uint32_t iq = 0, p2 = 0, wuse = 0, chunks = 0, lseq = 0, ew = 0;
         bool lpend = false;
         uint32_t accuse[2] = {0u, 0u};
         bool ok = true;
@@ -978,11 +1017,28 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
             if (!tr.last) return true;
             // end of a pass-1 phase: W (anchor row `row`, D columns) and Delta in TMEM
-            if (!wait(acc_full + 0, accuse[0] & 1u)) return false;
-            if (!wait(acc_full + 1, accuse[1] & 1u)) return false;
+            const int wbuf = (int)(ew & 1u);
+            if constexpr (LY::kWSep) {
+                if (!wait(wacc_full + wbuf, (ew >> 1) & 1u)) return false;
+            } else {
+                if (!wait(acc_full + 0, accuse[0] & 1u)) return false;
+                if (!wait(acc_full + 1, accuse[1] & 1u)) return false;
+            }
+            const uint32_t wcol = wbuf ? LY::colW1 : LY::colW0;
+            auto release_w = [&]() {  // the chunk accumulators are read
+                if constexpr (LY::kWSep) {
+                    arrive4(wacc_empty + wbuf);
+                } else {
+                    arrive4(acc_empty + 0);
+                    arrive4(acc_empty + 1);
+                    ++accuse[0];
+                    ++accuse[1];
+                }
+                ++ew;
+            };
             tc_fence_after();
             float v[32];
-            tmem_ld32(trow + LY::colB1, v);
+            tmem_ld32(trow + wcol + D, v);
             tmem_ld_wait();
             const float dj = v[0];
             if (!tr.full) {
@@ -992,7 +1048,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     float4 *dst = reinterpret_cast<float4 *>(p.part + ((size_t)tr.slice * p.C1 + tr.chunk) * MP * D) + row;
 #pragma unroll
                     for (int q = 0; q < D / 32; ++q) {
-                        tmem_ld32(trow + LY::colB0 + q * 32, v);
+                        tmem_ld32(trow + wcol + q * 32, v);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
@@ -1001,14 +1057,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     p.pdelta[((size_t)tr.slice * p.C1 + tr.chunk) * MP + row] = dj;
                 } else {
 #pragma unroll
-                    for (int q = 0; q < D / 32; ++q) tmem_ld32(trow + LY::colB0 + q * 32, v);  // keep the warp converged
+                    for (int q = 0; q < D / 32; ++q) tmem_ld32(trow + wcol + q * 32, v);  // keep the warp converged
                     tmem_ld_wait();
                 }
                 tc_fence_before();
-                arrive4(acc_empty + 0);
-                arrive4(acc_empty + 1);
-                ++accuse[0];
-                ++accuse[1];
+                release_w();
                 ++chunks;
                 bool published = false;
                 // Fixed binary tree over the slice's chunks: node (l, i) covers chunks
@@ -1086,7 +1139,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             const float rinv = dj != 0.f ? 1.f / dj : 0.f;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
-                tmem_ld32(trow + LY::colB0 + q * 32, v);
+                tmem_ld32(trow + wcol + q * 32, v);
                 tmem_ld_wait();
                 if (row < MP) {
 #pragma unroll
@@ -1095,10 +1148,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
             }
             tc_fence_before();
-            arrive4(acc_empty + 0);
-            arrive4(acc_empty + 1);
-            ++accuse[0];
-            ++accuse[1];
+            release_w();
             fence_proxy_async_smem();
             ep_sync();
             if (row == 0) mbar_arrive(w_full + wb);
