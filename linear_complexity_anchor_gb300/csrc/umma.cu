@@ -100,6 +100,9 @@ struct Layout {
     static constexpr int kFixed = kNU * kUB + kNA * kAB + kNW * kWB + kOnesB + kXchB + kBarB;
     static constexpr int kSlotsFit = (kMaxDyn - kFixed) / kSlotB;
     static constexpr int kNSlot = kSlotsFit > 8 ? 8 : kSlotsFit;
+    // ring order per pass-1 tile: Q then V, or (a shallow ring) Q(t), then V(t-1), so that the
+    // next S is not held up behind a V that is needed only after the softmax
+    static constexpr bool kVLag = kNSlot < 5;
     static constexpr int offU = 0;
     static constexpr int offA = offU + kNU * kUB;
     static constexpr int offW = offA + kNA * kAB;
@@ -618,8 +621,12 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     has_pend_v = false;
                 }
                 if (tr.kind == 0) {
-                    pend_v = tr;
-                    has_pend_v = true;
+                    if (LY::kVLag) {
+                        pend_v = tr;
+                        has_pend_v = true;
+                    } else if (ok) {
+                        ok = load_slot(&tv, tr.slice, tr.tile, pol_stream, D);
+                    }
                 }
                 if (ok && tr.kind == 1 && tr.first) {
                     if (!tr.full) {  // W' of a split slice: published (claim checked the flag)
@@ -678,8 +685,12 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     for (int idx = 0; idx < nt && ok; ++idx) {
                         const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
                         const uint32_t mseq = lseq++;
-                        if (lpend) ++lseq;
-                        lpend = tr.kind == 0;
+                        if (LY::kVLag) {
+                            if (lpend) ++lseq;
+                            lpend = tr.kind == 0;
+                        } else if (tr.kind == 0) {
+                            ++lseq;  // this tile's V
+                        }
                         if (tr.stored) continue;
                         const int qslot = (int)(mseq % NS);
                         if (!wait_slot(mseq)) { ok = false; break; }
@@ -820,8 +831,13 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         const int sbx = (int)(xs & 1u);  // this tile's S buffer (tiles with an S only)
                         if (!tr.stored) ++xs;
                         if (tr.kind == 0) {
-                            pv = tr;
-                            lpend = true;
+                            if (LY::kVLag) {
+                                pv = tr;
+                                lpend = true;
+                            } else if (!do_x(tr, lseq++)) {  // its V is right behind its Q
+                                ok = false;
+                                break;
+                            }
                         } else if (tr.stored) {
                             // the slot holds the A tile pass 1 stored; the epilogue releases it
                             const int aslot = (int)(mseq % NS);
@@ -1175,8 +1191,12 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
                 const int aslot = (int)(lseq % NS);
                 ++lseq;
-                if (lpend) ++lseq;
-                lpend = tr.kind == 0;
+                if (LY::kVLag) {
+                    if (lpend) ++lseq;
+                    lpend = tr.kind == 0;
+                } else if (tr.kind == 0) {
+                    ++lseq;  // this tile's V
+                }
                 if (!epilogue(tr, aslot)) { ok = false; break; }
                 if (tr.kind == 1 && tr.first) ++wuse;  // W' uses started so far
             }
