@@ -294,7 +294,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *s_full = slot_empty + NS;          // [2]  (1)       scores in S buffer
     uint64_t *s_empty = s_full + 2;              // [2]  (1)       S buffer free (read, or its P consumed)
     uint64_t *p_full = s_empty + 2;              // [2]  (1)       pass-2 A (P) written over the S buffer
-    uint64_t *a_full = p_full + 2;               // [NA] (1)       A tile written
+    uint64_t *a_full = p_full + 2;               // [NA] (8)       A tile written (one arrival per softmax warp)
     uint64_t *a_empty = a_full + NA;             // [NA] (1)       MMA reading the A tile completed
     uint64_t *acc_full = a_empty + NA;           // [2]  (1)       W/Delta or H complete in TMEM
     uint64_t *acc_empty = acc_full + 2;          // [2]  (4)       epilogue read it
@@ -335,7 +335,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_init(wacc_empty + i, 4);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(a_full + i, 1);
+            mbar_init(a_full + i, 8);
             mbar_init(a_empty + i, 1);
         }
         for (int i = 0; i < NU; ++i) {
@@ -891,8 +891,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 if (p.m == MP) softmax_half<MP, false>(ts, g * HM, p.m, p.c, v, mg, zg);
                 else softmax_half<MP, true>(ts, g * HM, p.m, p.c, v, mg, zg);
                 tc_fence_before();
-                // the last A store of this group has read its rows before anyone rewrites them
-                if (g == 0 && lane == 0) bulk_wait_group_read0();
+                // this warp's last A store has read its rows before anyone rewrites them
+                if (lane == 0) bulk_wait_group_read0();
                 float2 *xc = sXch + (size_t)(sb * 2) * kT;
                 xc[g * kT + row] = make_float2(mg, zg);
                 sm_sync();  // both halves have read the S buffer
@@ -932,25 +932,28 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     *reinterpret_cast<uint4 *>(sAb + sw_off(row, g * (HM / 8) + c8, kT)) =
                         make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
                 fence_proxy_async_smem();
-                sm_sync();  // both halves of every row are in place
-                if (tid == 0) mbar_arrive(a_full + ab);
+                arrive_w(a_full + ab);
                 ++ause;
                 const bool store = tr.kind == 0 && !tr.full && p.store_a;  // pass 2 reads A back
-                if (g == 0 && store && lane == 0) {
-                    if (tr.tile * kT + quad * 32 < p.n) {
-                        // this quadrant's 32 rows; rows past the end of the slice are not written
-#pragma unroll
-                        for (int b = 0; b < MP / 64; ++b)
+                if (store) {
+                    // MP = 128: each group stores its own 64-column block of its quadrant's 32
+                    // rows; MP = 64: the block holds both halves, so the two warps of a quadrant
+                    // meet first and group 0 stores it.  Rows past the end are not written.
+                    if (MP == 64) asm volatile("bar.sync %0, 64;" ::"r"(5 + quad) : "memory");
+                    if ((MP == 128 || g == 0) && lane == 0) {
+                        if (tr.tile * kT + quad * 32 < p.n) {
+                            const int b = MP == 128 ? g : 0;
                             tma_store_3d(&ta_st, sAb + b * kT * 128 + quad * 32 * 128, 64 * b, tr.tile * kT + quad * 32,
                                          tr.slice, pol_keep);
-                        bulk_commit_group();
-                    }
-                    if (tr.last) {
-                        // end of a chunk: its A rows are in global memory before the chunk is
-                        // published (the epilogue waits for all four storing warps)
-                        bulk_wait_group0();
-                        fence_proxy_async_global();
-                        red_release_cta_add(s_ast, 1u);
+                            bulk_commit_group();
+                        }
+                        if (tr.last) {
+                            // end of a chunk: its A rows are in global memory before the chunk is
+                            // published (the epilogue waits for every storing warp)
+                            bulk_wait_group0();
+                            fence_proxy_async_global();
+                            red_release_cta_add(s_ast, 1u);
+                        }
                     }
                 }
             }
@@ -970,8 +973,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(bar);
         };
-        // bounded wait until the four softmax warps have stored the A rows of `target / 4`
-        // chunks (a monotonic counter: no phase to alias)
+        // bounded wait until the storing softmax warps (4, or 8 when MP = 128) have stored the
+        // A rows of the chunks so far (a monotonic counter: no phase to alias)
         auto wait_ast = [&](uint32_t target) -> bool {
             if (ld_acquire_cta(s_ast) >= target) return true;
             const uint64_t t0 = globaltimer_ns();
@@ -1093,7 +1096,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     if (row == 0) {
                         // this chunk's A rows must be in memory before the chunk is published;
                         // if that wait gives up (abort), stop here as if first to arrive
-                        const bool go = published || !p.store_a || wait_ast(4u * chunks);
+                        const bool go = published || !p.store_a || wait_ast((MP == 128 ? 8u : 4u) * chunks);
                         published = true;
                         *s_last = go ? (int)atom_add_acq_rel_gpu(p.tree + (size_t)tr.slice * p.C1 + (right - 1), 1u) : 0;
                     }
