@@ -53,7 +53,6 @@ constexpr int kT = 128;                         // tokens per tile (UMMA M)
 constexpr int kThreads = 480;
 constexpr int kWarpProducer = 12, kWarpMmaS = 13, kWarpMmaX = 14;
 constexpr int kIQ = 4;                          // item queue depth
-constexpr int kPrefetch = 0;                    // tiles of an item brought into L2 ahead of their load
 constexpr uint64_t kWaitNs = 2000000000ull;     // every wait gives up after 2 s
 constexpr double kL2ABudget = 256.0 * 1024 * 1024; // bytes kept for pass 2 (A or Q) of the slices in flight
 constexpr double kStoreABudget = 64.0 * 1024 * 1024; // largest A copy kept for pass 2
@@ -103,6 +102,9 @@ struct Layout {
     // ring order per pass-1 tile: Q then V, or (a shallow ring) Q(t), then V(t-1), so that the
     // next S is not held up behind a V that is needed only after the softmax
     static constexpr bool kVLag = kNSlot < 5;
+    // a single A buffer doubles as the H staging buffer of recomputed pass-2 tiles (their A is
+    // in TMEM), so their Q slot goes back right after S; with two, H is staged in the Q slot
+    static constexpr bool kStageInA = kNA == 1;
     static constexpr int offU = 0;
     static constexpr int offA = offU + kNU * kUB;
     static constexpr int offW = offA + kNA * kAB;
@@ -594,23 +596,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
             int a1, b1;
             const int nt = item_tiles(it, p, a1, b1);
-            // L2 prefetch of the tiles a few loads ahead: the ring alone holds too few bytes
-            // in flight to cover the memory latency
-            auto prefetch = [&](int j) {
-                if (!L0 || j >= nt) return;
-                const TileRef tf = tile_at(it, a1, b1, j, p.store_a != 0);
-                if (tf.stored) {
-                    for (int b = 0; b < MP / 64; ++b) tma_prefetch_l2_3d(&ta_ld, 64 * b, tf.tile * kT, tf.slice);
-                } else {
-                    for (int b = 0; b < D / 64; ++b) tma_prefetch_l2_3d(&tq, 64 * b, tf.tile * kT, tf.slice);
-                    if (tf.kind == 0)
-                        for (int b = 0; b < D / 64; ++b) tma_prefetch_l2_3d(&tv, 64 * b, tf.tile * kT, tf.slice);
-                }
-            };
-            for (int j = 0; j < kPrefetch; ++j) prefetch(j);
             for (int idx = 0; idx < nt && ok; ++idx) {
                 const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
-                prefetch(idx + kPrefetch);
                 // a pass-1 Q tile is read again by pass 2 unless pass 2 loads the stored A
                 if (tr.stored) ok = load_slot(&ta_ld, tr.slice, tr.tile, pol_stream, MP);
                 else ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 && (tr.full || !p.store_a) ? pol_keep : pol_stream, D);
@@ -704,8 +691,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                             umma_bf16(tmem + dcol, adesc + (uint64_t)((((kk >> 2) * kT * 128) + (kk & 3) * 32) >> 4),
                                       bdesc + (uint64_t)((((kk >> 2) * MP * 128) + (kk & 3) * 32) >> 4), kIdS, kk > 0);
                         umma_commit(s_full + sb);
-                        // a pass-2 tile's Q slot stays held: the epilogue stages the H tile there
-                        if (tr.kind == 0) umma_commit(slot_empty + qslot);
+                        // unless H is staged in the A buffer, a pass-2 tile's Q slot stays held: the
+                        // epilogue stages the H tile there
+                        if (tr.kind == 0 || LY::kStageInA) umma_commit(slot_empty + qslot);
                         ++sidx;
                     }
                 }
@@ -922,6 +910,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     tc_fence_before();
                     sm_sync();
                     if (tid == 0) mbar_arrive(p_full + sb);
+                    if (LY::kStageInA) ++ause;  // the epilogue stages this tile's H in the A buffer
                     continue;
                 }
                 const int ab = (int)(ause % NA);
@@ -965,7 +954,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // TMEM lane: token row (H) / anchor row (W)
         const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint32_t iq = 0, p2 = 0, wuse = 0, chunks = 0, lseq = 0, ew = 0;
+        uint32_t iq = 0, p2 = 0, wuse = 0, chunks = 0, lseq = 0, ew = 0, euse = 0;
         bool lpend = false;
         uint32_t accuse[2] = {0u, 0u};
         bool ok = true;
@@ -990,15 +979,19 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             return true;
         };
         const uint64_t pol_stream = policy_evict_first();
-        auto epilogue = [&](const TileRef &tr, int aslot) -> bool {
+        // ause: this tile's place in the sequence of A-buffer uses (see kStageInA)
+        auto epilogue = [&](const TileRef &tr, int aslot, uint32_t ause) -> bool {
             if (tr.kind == 1) {
-                // H tile -> bf16 -> the ring slot that held this tile's A or Q (the MMAs have
-                // read it) -> one TMA store per warp (32 rows), then the slot is released
+                // H tile -> bf16 -> a staging buffer (the ring slot that held this tile's A or
+                // Q, or the A buffer) -> one TMA store per warp (32 rows), then the staging
+                // buffer is released
+                const bool in_a = !tr.stored && LY::kStageInA;
                 const int hb = (int)(p2 & 1u);
                 if (!wait(acc_full + hb, accuse[hb] & 1u)) return false;
+                if (in_a && !wait(a_empty + 0, (ause & 1u) ^ 1u)) return false;  // its last user is done
                 tc_fence_after();
                 const uint32_t hcol = hb ? LY::colB1 : LY::colB0;
-                uint8_t *stage = sRing + aslot * LY::kSlotB;
+                uint8_t *stage = in_a ? sA : sRing + aslot * LY::kSlotB;
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     float v[32];
@@ -1031,7 +1024,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     for (int l = 0; l < MP * 2 / 128; ++l) discard_l2_line(arow + 128 * l);
                 }
                 ep_sync();
-                if (row == 0) mbar_arrive(slot_empty + aslot);
+                if (row == 0) mbar_arrive(in_a ? a_empty + 0 : slot_empty + aslot);
                 return true;
             }
             if (!tr.last) return true;
@@ -1200,7 +1193,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 } else if (tr.kind == 0) {
                     ++lseq;  // this tile's V
                 }
-                if (!epilogue(tr, aslot)) { ok = false; break; }
+                const uint32_t use = euse;  // A-buffer uses: pass-1 tiles, and staged pass-2 tiles
+                if (tr.kind == 0 || (!tr.stored && LY::kStageInA)) ++euse;
+                if (!epilogue(tr, aslot, use)) { ok = false; break; }
                 if (tr.kind == 1 && tr.first) ++wuse;  // W' uses started so far
             }
         }
