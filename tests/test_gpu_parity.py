@@ -80,10 +80,41 @@ def test_workload_sampled_slices(env, name, nslices):
     assert pkg.device_error() == 0
 
 
+# The tensor-core plans recompute A in pass 2 when all slices' copies of A would not fit
+# the 64 MB kept for them; each shared-memory layout stages the pass-2 H tiles differently
+# (in the Q ring slot with two A buffers, in the A buffer with one), so each gets a case.
+_RECOMPUTE = {
+    "d64_mp64": dict(B=16, heads=12, n=4200, m=64, d=64),     # 103 MB of A, two A buffers
+    "d128_mp64": dict(B=4, heads=16, n=8300, m=49, d=128),    # 68 MB of A, one A buffer, masked anchors
+    "d64_mp128": dict(B=8, heads=12, n=4200, m=100, d=64),    # 103 MB of A, one A buffer, masked anchors
+}
+
+
+@pytest.mark.parametrize("case", sorted(_RECOMPUTE))
+def test_recompute_plans(env, case):
+    pkg, torch, orc = env
+    w = gen.WORKLOADS["det_800x1344"].with_(name=case, **_RECOMPUTE[case])
+    assert 2 * w.slices * w.n * (64 if w.m <= 64 else 128) > 64 * 1024 * 1024
+    assert pkg.query_plan(w.dtype, w.B, w.heads, w.n, w.m, w.d)["variant"] == "umma"
+    x = gen.make_inputs(w, seed=7)
+    H = _run(env, w, x)
+    U = gen.to_float64(x["U"], w.dtype)
+    for s in (0, w.slices // 2, w.slices - 1):
+        b, h = divmod(s, w.heads)
+        ref = orc.slice_forward(gen.to_float64(x["Q"][b, h], w.dtype), U[h], gen.to_float64(x["V"][b, h], w.dtype),
+                                w.scale)["H"]
+        assert_parity(to_host64(H[b, h]), ref, w.dtype, f"{case} slice ({b},{h})")
+    Hs = H.double().sum(dim=2)
+    Vt = to_device(x["V"], w.dtype, torch).double()
+    assert ((Hs - Vt.sum(dim=2)).abs() <= 1e-3 * Vt.abs().sum(dim=2) + 1e-2).all()
+    assert pkg.device_error() == 0
+
+
 # ------------------------------------------------------------------ edge shapes
 
 _MD = [(1, 16), (2, 64), (15, 32), (16, 64), (30, 64), (31, 16), (32, 64), (33, 64), (49, 64), (64, 64),
-       (64, 128), (100, 128), (128, 64), (128, 128), (256, 64), (200, 32)]
+       (64, 128), (100, 128), (128, 64), (128, 128), (256, 64), (200, 32),
+       (1, 128), (15, 128), (31, 128), (33, 128), (49, 128)]
 _N = [1, 2, 7, 8, 127, 128, 129, 197, 513, 1100]
 
 
