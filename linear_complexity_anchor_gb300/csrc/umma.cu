@@ -598,9 +598,10 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             const int nt = item_tiles(it, p, a1, b1);
             for (int idx = 0; idx < nt && ok; ++idx) {
                 const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
-                // a pass-1 Q tile is read again by pass 2 unless pass 2 loads the stored A
+                // Q is kept in L2 only for a whole-slice item, whose pass 2 follows at once: across
+                // split slices too much streams through L2 before pass 2 comes back to it
                 if (tr.stored) ok = load_slot(&ta_ld, tr.slice, tr.tile, pol_stream, MP);
-                else ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 && (tr.full || !p.store_a) ? pol_keep : pol_stream, D);
+                else ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 && tr.full ? pol_keep : pol_stream, D);
                 // claim the next item now, while the ring is still full of this one's tiles
                 if (idx == 0 && !have_ahead) have_ahead = claim(ahead) == 1;
                 if (ok && has_pend_v) {
