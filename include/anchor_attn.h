@@ -124,7 +124,9 @@ enum {
     ANCHOR_ATTN_VARIANT_UMMA = 3          /* tcgen05 tensor-core path                        */
 };
 
-/* dtype: 0 = bf16 (anchor_attn_forward), 1 = fp32 (anchor_attn_forward_f32). */
+/* dtype: 0 = bf16 (anchor_attn_forward), 1 = fp32 (anchor_attn_forward_f32).  The plan is
+ * the one a call with a positive scale makes: the tensor-core variant takes bf16, d in
+ * {64, 128}, 32 <= m <= 128 and scale > 0 (a non-positive scale runs a CUDA-core variant). */
 ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, int m, int d,
                                             anchor_attn_plan_t *plan);
 
