@@ -81,12 +81,16 @@ struct Layout {
     static constexpr int kATB = kT * MP * 2;           // one stored A tile (pass-2 operand)
     static constexpr int kSlotB = kQB > kATB ? kQB : kATB;  // ring slot: any of the three
     static constexpr int kUB = MP * D * 2;
-    static constexpr int kAB = kT * 128 * 2;           // A tile, 128 anchor columns
     static constexpr int kWB = D * MP * 2;             // W' operand image
     // ones for Delta = A^T 1.  d = 64: a whole 128-token x 64-column MN-major block that the
     // W MMA reads as columns d .. d+15 of its B operand (W and Delta in one N = d + 16 MMA);
     // d = 128: a 16 x 128 K-major B operand of its own N = 16 MMA.
     static constexpr bool kFoldDelta = D == 64;
+    // A tile: the W MMA is M = 128 (anchor rows).  With MP = 64 and the ones block at hand, the
+    // tile holds only its 64 anchor columns and the MMA reads rows 64..127 from the ones block:
+    // those rows of W and Delta are never read.  Otherwise 128 anchor columns.
+    static constexpr bool kHalfA = MP == 64 && kFoldDelta;
+    static constexpr int kAB = kT * (kHalfA ? 64 : 128) * 2;
     static constexpr int kOnesB = kFoldDelta ? kT * 128 : 16 * kT * 2;
     static constexpr int kXchB = 2 * 2 * kT * 8;        // softmax halves' (max, sum), by tile parity
     static constexpr int kBarB = 1024;
@@ -123,6 +127,7 @@ struct Layout {
     static constexpr int colW1 = kWSep ? colW0 + D + 16 : colB0;
     static constexpr int kTmemCols = kWSep ? 512 : ((2 * MP + 2 * D) <= 256 ? 256 : 512);
     static_assert(kNSlot >= 3, "ring too shallow");
+    static_assert(!kStageInA || kAB >= kQB, "the single A buffer also stages H tiles");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
     static_assert(kUB % 1024 == 0 && offA % 1024 == 0 && offW % 1024 == 0 && offRing % 1024 == 0 &&
                   offOnes % 1024 == 0, "operand blocks must be 1024-byte aligned");
@@ -759,7 +764,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         }
                         const uint32_t wcol = wbuf ? LY::colW1 : LY::colW0;
                         tc_fence_after();
-                        const uint64_t adesc = smem_desc_sw128(sAb, 16384, 1024);
+                        // second 64-anchor block of A^T: the tile's own, or the ones block
+                        const uint64_t adesc = smem_desc_sw128(sAb, LY::kHalfA ? sOnesA - sAb : 16384, 1024);
                         if constexpr (LY::kFoldDelta) {
                             // second 64-column block of B = the ones block: the leading-byte
                             // offset spans from this slot to it (columns D.. of the result =
