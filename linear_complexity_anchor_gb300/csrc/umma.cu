@@ -986,6 +986,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             return true;
         };
         const uint64_t pol_stream = policy_evict_first();
+        int held = -1;  // ring slot whose H store may still be reading it (released one tile later)
         // ause: this tile's place in the sequence of A-buffer uses (see kStageInA)
         auto epilogue = [&](const TileRef &tr, int aslot, uint32_t ause) -> bool {
             if (tr.kind == 1) {
@@ -1015,12 +1016,19 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 fence_proxy_async_smem();
                 __syncwarp();
                 const int r0 = tr.tile * kT + quarter * 32;
-                if (lane == 0 && r0 < p.n) {
+                // a deep ring lets the staging slot go back one tile later, so that this tile's
+                // store reads it while the next tile is drained; the last tile of an item
+                // releases both (the tile past the end, r0 >= n, is always an item's last)
+                const bool defer = LY::kNSlot >= 6 && !in_a && !tr.last;
+                if (lane == 0) {
+                    if (r0 < p.n) {
 #pragma unroll
-                    for (int b = 0; b < D / 64; ++b)
-                        tma_store_3d(&th_st, stage + b * kT * 128 + quarter * 32 * 128, 64 * b, r0, tr.slice, pol_stream);
-                    bulk_commit_group();
-                    bulk_wait_group_read0();
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_store_3d(&th_st, stage + b * kT * 128 + quarter * 32 * 128, 64 * b, r0, tr.slice, pol_stream);
+                        bulk_commit_group();
+                    }
+                    if (defer) bulk_wait_group_read1();
+                    else bulk_wait_group_read0();  // also covers the held slot's store
                 }
                 const int tok = tr.tile * kT + row;
                 if (tr.stored && tok < p.n) {
@@ -1031,7 +1039,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     for (int l = 0; l < MP * 2 / 128; ++l) discard_l2_line(arow + 128 * l);
                 }
                 ep_sync();
-                if (row == 0) mbar_arrive(in_a ? a_empty + 0 : slot_empty + aslot);
+                if (row == 0) {
+                    if (held >= 0) mbar_arrive(slot_empty + held);  // the last tile's store has read it
+                    if (!defer) mbar_arrive(in_a ? a_empty + 0 : slot_empty + aslot);
+                }
+                held = defer ? aslot : -1;
                 return true;
             }
             if (!tr.last) return true;
