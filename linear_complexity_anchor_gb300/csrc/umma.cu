@@ -91,6 +91,9 @@ struct Layout {
     // those rows of W and Delta are never read.  Otherwise 128 anchor columns.
     static constexpr bool kHalfA = MP == 64 && kFoldDelta;
     static constexpr int kAB = kT * (kHalfA ? 64 : 128) * 2;
+    // softmax groups in ping-pong: with 64 anchors a thread holds a whole score row, so group
+    // g takes the tiles of S buffer g whole (and A buffer g) instead of half of every row
+    static constexpr bool kPP = kHalfA;
     static constexpr int kOnesB = kFoldDelta ? kT * 128 : 16 * kT * 2;
     static constexpr int kXchB = 2 * 2 * kT * 8;        // softmax halves' (max, sum), by tile parity
     static constexpr int kBarB = 1024;
@@ -128,6 +131,7 @@ struct Layout {
     static constexpr int kTmemCols = kWSep ? 512 : ((2 * MP + 2 * D) <= 256 ? 256 : 512);
     static_assert(kNSlot >= 3, "ring too shallow");
     static_assert(!kStageInA || kAB >= kQB, "the single A buffer also stages H tiles");
+    static_assert(!kPP || (kNA == 2 && !kVLag), "ping-pong softmax: one A buffer per group, V right behind Q");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
     static_assert(kUB % 1024 == 0 && offA % 1024 == 0 && offW % 1024 == 0 && offRing % 1024 == 0 &&
                   offOnes % 1024 == 0, "operand blocks must be 1024-byte aligned");
@@ -230,6 +234,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // named barriers of the two 4-warp groups (id 0 is __syncthreads)
 __device__ __forceinline__ void sm_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ void ep_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// one softmax group (ids 3, 4)
+__device__ __forceinline__ void grp_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(3 + g) : "memory"); }
 
 // Half of a row softmax: this thread's token row, anchors [col0, col0 + MP/2) of the S row.
 // A_ij = softmax_j(scale * S_ij) = 2^(c S_ij - c max_j S_ij) / sum, c = scale * log2(e) > 0.
@@ -301,7 +307,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *s_full = slot_empty + NS;          // [2]  (1)       scores in S buffer
     uint64_t *s_empty = s_full + 2;              // [2]  (1)       S buffer free (read, or its P consumed)
     uint64_t *p_full = s_empty + 2;              // [2]  (1)       pass-2 A (P) written over the S buffer
-    uint64_t *a_full = p_full + 2;               // [NA] (8)       A tile written (one arrival per softmax warp)
+    uint64_t *a_full = p_full + 2;               // [NA] (8, 4)    A tile written (one arrival per writing warp)
     uint64_t *a_empty = a_full + NA;             // [NA] (1)       MMA reading the A tile completed
     uint64_t *acc_full = a_empty + NA;           // [2]  (1)       W/Delta or H complete in TMEM
     uint64_t *acc_empty = acc_full + 2;          // [2]  (4)       epilogue read it
@@ -342,7 +348,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_init(wacc_empty + i, 4);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(a_full + i, 8);
+            mbar_init(a_full + i, LY::kPP ? 4 : 8);
             mbar_init(a_empty + i, 1);
         }
         for (int i = 0; i < NU; ++i) {
@@ -714,7 +720,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 uint32_t xk = 0, wuse = 0, p2 = 0;
                 uint32_t accuse[2] = {0u, 0u};
                 TileRef pv;
+                int pvs = 0;  // its S buffer
                 uint32_t xs = 0, pcnt[2] = {0u, 0u};  // S tiles seen; pass-2 A's seen per S buffer
+                uint32_t acnt[2] = {0u, 0u};          // ping-pong: pass-1 A's seen per A buffer
                 uint32_t xw = 0;                      // pass-1 chunks started (separate W sets)
                 // H = A W' into the next H buffer; A at `adesc` (K-major, shared memory) or, with
                 // from_tmem, in tensor memory at a_tmem
@@ -746,9 +754,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     return true;
                 };
                 // pass 1: W += A^T V, Delta += A^T 1 from the softmax's A tile (V at ring position vseq)
-                auto do_x = [&](const TileRef &tr, uint32_t vseq) -> bool {
-                    const int ab = (int)(xk % NA);
-                    if (!wait(a_full + ab, (xk / NA) & 1u)) return false;
+                // (sbx: the tile's S buffer, which names its A buffer in ping-pong)
+                auto do_x = [&](const TileRef &tr, uint32_t vseq, int sbx) -> bool {
+                    const int ab = LY::kPP ? sbx : (int)(xk % NA);
+                    if (!wait(a_full + ab, LY::kPP ? (acnt[sbx] & 1u) : ((xk / NA) & 1u))) return false;
+                    if (LY::kPP) ++acnt[sbx];
                     const uint32_t sAb = sAa + ab * LY::kAB;
                     if (tr.kind == 0) {
                         const int vs = (int)(vseq % NS);
@@ -810,7 +820,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     ++iq;
                     if (it.kind == kEnd) break;
                     if (it.kind == kFlush) {  // the producer loads the held-back V now
-                        if (lpend && !do_x(pv, lseq++)) break;
+                        if (lpend && !do_x(pv, lseq++, pvs)) break;
                         lpend = false;
                         continue;
                     }
@@ -820,7 +830,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
                         const uint32_t mseq = lseq++;
                         if (lpend) {  // the previous pass-1 tile's V follows this tile's first slot
-                            if (!do_x(pv, lseq++)) { ok = false; break; }
+                            if (!do_x(pv, lseq++, pvs)) { ok = false; break; }
                             lpend = false;
                         }
                         const int sbx = (int)(xs & 1u);  // this tile's S buffer (tiles with an S only)
@@ -828,8 +838,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         if (tr.kind == 0) {
                             if (LY::kVLag) {
                                 pv = tr;
+                                pvs = sbx;
                                 lpend = true;
-                            } else if (!do_x(tr, lseq++)) {  // its V is right behind its Q
+                            } else if (!do_x(tr, lseq++, sbx)) {  // its V is right behind its Q
                                 ok = false;
                                 break;
                             }
@@ -847,7 +858,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         }
                     }
                 }
-                if (ok && lpend) do_x(pv, lseq++);  // after the end marker the producer loads the last V
+                if (ok && lpend) do_x(pv, lseq++, pvs);  // after the end marker the producer loads the last V
             }
         }
     } else if (warp < 8) {
@@ -860,6 +871,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         constexpr int HM = MP / 2;
         const uint64_t pol_keep = policy_evict_last();
         uint32_t sidx = 0, ause = 0, iq = 0;
+        uint32_t own = 0;  // ping-pong: this group's uses of its A buffer
         bool ok = true;
         auto arrive_w = [&](uint64_t *bar) {  // one arrival per warp
             __syncwarp();
@@ -878,6 +890,70 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             for (int idx = 0; idx < nt && ok; ++idx) {
                 const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
                 if (tr.stored) continue;  // pass 2 of a split slice has no softmax
+                if constexpr (LY::kPP) {
+                    const int sb = (int)(sidx & 1u);
+                    const uint32_t sph = (sidx >> 1) & 1u;
+                    ++sidx;
+                    const bool store = tr.kind == 0 && !tr.full && p.store_a;  // pass 2 reads A back
+                    if (sb != g) {
+                        // the other group's tile.  A chunk is published once every A row of it
+                        // is stored: at its last tile this group's own stores are flushed too
+                        if (store && tr.last && lane == 0) {
+                            bulk_wait_group0();
+                            fence_proxy_async_global();
+                            red_release_cta_add(s_ast, 1u);
+                        }
+                        continue;
+                    }
+                    if (!wait(s_full + sb, sph)) { ok = false; break; }
+                    tc_fence_after();
+                    float v[MP], mg, zg;  // the whole row: both "halves" of a 2 MP-anchor softmax
+                    const uint32_t ts = trow + (sb ? LY::colS1 : LY::colS0);
+                    if (p.m == MP) softmax_half<2 * MP, false>(ts, 0, p.m, p.c, v, mg, zg);
+                    else softmax_half<2 * MP, true>(ts, 0, p.m, p.c, v, mg, zg);
+                    tc_fence_before();
+                    grp_sync(g);  // the group's four warps have read the S buffer
+                    const bool valid = tr.tile * kT + row < p.n;
+                    const uint64_t sc2 = f32x2(valid ? 1.f / zg : 0.f, valid ? 1.f / zg : 0.f);
+                    uint32_t pk[MP / 2];
+#pragma unroll
+                    for (int j = 0; j < MP / 2; ++j) {
+                        float x0, x1;
+                        f32x2_split(mul_f32x2(f32x2(v[2 * j], v[2 * j + 1]), sc2), x0, x1);
+                        pk[j] = pack_bf16x2(x0, x1);
+                    }
+                    if (tr.kind == 1) {  // recomputed pass-2 A over its S buffer (see below)
+                        tmem_st32(ts, pk);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        grp_sync(g);
+                        if (quad == 0 && lane == 0) mbar_arrive(p_full + sb);
+                        continue;
+                    }
+                    if (quad == 0 && lane == 0) mbar_arrive(s_empty + sb);
+                    if (lane == 0) bulk_wait_group_read0();  // this warp's last A store has read buffer g
+                    if (!wait(a_empty + g, (own & 1u) ^ 1u)) { ok = false; break; }
+                    uint8_t *sAb = sA + g * LY::kAB;
+#pragma unroll
+                    for (int c8 = 0; c8 < MP / 8; ++c8)
+                        *reinterpret_cast<uint4 *>(sAb + sw_off(row, c8, kT)) =
+                            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                    fence_proxy_async_smem();
+                    arrive_w(a_full + g);
+                    ++own;
+                    if (store && lane == 0) {
+                        if (tr.tile * kT + quad * 32 < p.n) {
+                            tma_store_3d(&ta_st, sAb + quad * 32 * 128, 0, tr.tile * kT + quad * 32, tr.slice, pol_keep);
+                            bulk_commit_group();
+                        }
+                        if (tr.last) {
+                            bulk_wait_group0();
+                            fence_proxy_async_global();
+                            red_release_cta_add(s_ast, 1u);
+                        }
+                    }
+                    continue;
+                }
                 const int sb = (int)(sidx & 1u);
                 if (!wait(s_full + sb, (sidx >> 1) & 1u)) { ok = false; break; }
                 tc_fence_after();
@@ -969,7 +1045,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(bar);
         };
-        // bounded wait until the storing softmax warps (4, or 8 when MP = 128) have stored the
+        // bounded wait until the storing softmax warps (4, or 8 when MP = 128 or in ping-pong) have stored the
         // A rows of the chunks so far (a monotonic counter: no phase to alias)
         auto wait_ast = [&](uint32_t target) -> bool {
             if (ld_acquire_cta(s_ast) >= target) return true;
@@ -1108,7 +1184,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     if (row == 0) {
                         // this chunk's A rows must be in memory before the chunk is published;
                         // if that wait gives up (abort), stop here as if first to arrive
-                        const bool go = published || !p.store_a || wait_ast((MP == 128 ? 8u : 4u) * chunks);
+                        const bool go = published || !p.store_a || wait_ast((MP == 128 || LY::kPP ? 8u : 4u) * chunks);
                         published = true;
                         *s_last = go ? (int)atom_add_acq_rel_gpu(p.tree + (size_t)tr.slice * p.C1 + (right - 1), 1u) : 0;
                     }
