@@ -613,8 +613,6 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 // split slices too much streams through L2 before pass 2 comes back to it
                 if (tr.stored) ok = load_slot(&ta_ld, tr.slice, tr.tile, pol_stream, MP);
                 else ok = load_slot(&tq, tr.slice, tr.tile, tr.kind == 0 && tr.full ? pol_keep : pol_stream, D);
-                // claim the next item now, while the ring is still full of this one's tiles
-                if (idx == 0 && !have_ahead) have_ahead = claim(ahead) == 1;
                 if (ok && has_pend_v) {
                     ok = load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream, D);
                     has_pend_v = false;
@@ -640,6 +638,10 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     }
                     ++wuse;
                 }
+                // claim the next item once this one's loads are all issued, so that the claim's
+                // memory round trips overlap the consumers working through the full ring; a
+                // whole-slice item is a few tiles long, and claims after its first
+                if (ok && idx == (it.kind == 2 ? 0 : nt - 1) && !have_ahead) have_ahead = claim(ahead) == 1;
             }
         }
         if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream, D);
