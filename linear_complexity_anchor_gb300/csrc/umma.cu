@@ -1078,33 +1078,54 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 tc_fence_after();
                 const uint32_t hcol = hb ? LY::colB1 : LY::colB0;
                 uint8_t *stage = in_a ? sA : sRing + aslot * LY::kSlotB;
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    float v[32];
-                    tmem_ld32(trow + hcol + q * 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(stage + sw_off(row, q * 4 + c, kT)) = pack8_scaled(v + 8 * c, 1.f);
-                }
-                tc_fence_before();
-                arrive4(acc_empty + hb);
-                ++accuse[hb];
-                ++p2;
-                fence_proxy_async_smem();
-                __syncwarp();
                 const int r0 = tr.tile * kT + quarter * 32;
                 // a deep ring lets the staging slot go back one tile later, so that this tile's
                 // store reads it while the next tile is drained; the last tile of an item
                 // releases both (the tile past the end, r0 >= n, is always an item's last)
                 const bool defer = LY::kNSlot >= 6 && !in_a && !tr.last;
-                if (lane == 0) {
-                    if (r0 < p.n) {
+                if constexpr (D == 64) {
 #pragma unroll
-                        for (int b = 0; b < D / 64; ++b)
-                            tma_store_3d(&th_st, stage + b * kT * 128 + quarter * 32 * 128, 64 * b, r0, tr.slice, pol_stream);
-                        bulk_commit_group();
+                    for (int q = 0; q < 2; ++q) {
+                        float v[32];
+                        tmem_ld32(trow + hcol + q * 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4 *>(stage + sw_off(row, q * 4 + c, kT)) = pack8_scaled(v + 8 * c, 1.f);
                     }
+                    tc_fence_before();
+                    arrive4(acc_empty + hb);
+                    ++accuse[hb];
+                    ++p2;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && r0 < p.n) tma_store_3d(&th_st, stage + quarter * 32 * 128, 0, r0, tr.slice, pol_stream);
+                } else {
+                    // per 64-column block: two TMEM loads behind one wait, then the block's
+                    // store goes out while the next block is drained
+#pragma unroll
+                    for (int b = 0; b < D / 64; ++b) {
+                        float v[64];
+                        tmem_ld32(trow + hcol + b * 64, v);
+                        tmem_ld32(trow + hcol + b * 64 + 32, v + 32);
+                        tmem_ld_wait();
+                        if (b == D / 64 - 1) {  // the accumulator is read: the next H MMA may start
+                            tc_fence_before();
+                            arrive4(acc_empty + hb);
+                            ++accuse[hb];
+                            ++p2;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(stage + sw_off(row, b * 8 + c, kT)) = pack8_scaled(v + 8 * c, 1.f);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && r0 < p.n)
+                            tma_store_3d(&th_st, stage + b * kT * 128 + quarter * 32 * 128, 64 * b, r0, tr.slice, pol_stream);
+                    }
+                }
+                if (lane == 0) {
+                    if (r0 < p.n) bulk_commit_group();
                     if (defer) bulk_wait_group_read1();
                     else bulk_wait_group_read0();  // also covers the held slot's store
                 }
