@@ -1442,9 +1442,10 @@ UmmaPlan umma_plan(const Problem &p) {
     pl.MP = MP;
     pl.NT = (p.n + kT - 1) / kT;
     const long long S = p.slices();
-    // Chunk sizes: long chunks mean fewer partials to reduce and fewer anchor reloads, but
-    // every SM needs work: halve a pass's chunk while the pass has fewer than two items per SM.
-    const long long want = 2LL * sm_count();
+    // Chunk sizes: long chunks mean fewer partials to reduce, fewer anchor reloads and fewer
+    // item switches, but every SM needs work: halve a pass's chunk while the pass has fewer
+    // than one and a half items per SM.
+    const long long want = 3LL * sm_count() / 2;
     int t1 = kUmmaP1Tiles, t2 = kUmmaP2Tiles;
     while (t1 > kUmmaMinTiles && S * ((pl.NT + t1 - 1) / t1) < want) t1 /= 2;
     while (t2 > kUmmaMinTiles && S * ((pl.NT + t2 - 1) / t2) < want) t2 /= 2;

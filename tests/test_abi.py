@@ -80,8 +80,10 @@ def test_plans(pkg):
     assert p["variant"] == "simt_split" and p["splits"] == 3 and p["workspace_bytes"] > 0
     assert pkg.query_plan("bf16", 0, 2, 100, 20, 64)["variant"] == "empty"
     # tensor-core variant: d in {64, 128}, 32 <= m <= 128, bf16 only
+    # 33 tiles of 128 tokens in chunks of at most 16: 3 chunks x 96 slices is at least 1.5
+    # items per SM of a 152-SM GPU (the count assumed without a device)
     p = pkg.query_plan("bf16", 8, 12, 4200, 64, 64)
-    assert p["variant"] == "umma" and p["kernels_per_call"] == 1 and p["splits"] == 5
+    assert p["variant"] == "umma" and p["kernels_per_call"] == 1 and p["splits"] == 3
     p = pkg.query_plan("bf16", 256, 12, 197, 49, 64)
     assert p["variant"] == "umma" and p["splits"] == 1 and p["workspace_bytes"] == 256
     assert pkg.query_plan("f32", 8, 12, 4200, 64, 64)["variant"] == "simt_split"
