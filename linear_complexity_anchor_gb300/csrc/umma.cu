@@ -5,31 +5,36 @@
 //
 // One persistent kernel per call; work is cut into items that CTAs claim at run time:
 //   P1(s, c)  pass 1 over token chunk c of slice s: per 128-token tile, S = Q U^T on the
-//             tensor core (TMEM accumulator), row softmax in registers (one thread per
+//             tensor core (TMEM accumulator), row softmax in registers (one TMEM lane = one
 //             token), A tile -> shared memory as bf16, then W += A^T V and Delta += A^T 1
-//             on the tensor core (both from the same rounded A).  The A tile also goes to
-//             a workspace copy (TMA store, kept in L2).  The chunk's (W, Delta) goes to a
-//             workspace partial; partials meet in a fixed binary tree (the second of two
-//             siblings to arrive adds them: the sums do not depend on which CTA ran what),
-//             and the root forms W' = Delta^{-1} W as a bf16 operand image and publishes it.
-//   P2(s, c)  pass 2 over token chunk c, once the slice's W' is published: the stored A
-//             tile comes back from L2, H = A W' on the tensor core, bf16 H rows to global
-//             memory; the A lines are then dropped from L2 without a write-back.
+//             on the tensor core (both from the same rounded A).  In plans that keep A for
+//             pass 2 the A tile also goes to a workspace copy (TMA store, kept in L2).  The
+//             chunk's (W, Delta) goes to a workspace partial; partials meet in a fixed binary
+//             tree (the second of two siblings to arrive adds them: the sums do not depend on
+//             which CTA ran what), and the root forms W' = Delta^{-1} W as a bf16 operand
+//             image and publishes it.
+//   P2(s, c)  pass 2 over token chunk c, once the slice's W' is published: A comes back
+//             from the L2 copy, or (when every slice's copy would not fit L2) is recomputed
+//             from Q into tensor memory; H = A W' on the tensor core, bf16 H rows to global
+//             memory.  Stored A lines are dropped from L2 after use, without a write-back.
 //   FULL(s)   short slices: P1 and P2 of a whole slice in one CTA, W' kept on chip; pass 2
 //             recomputes A instead of storing it.
 // A CTA takes a P2 chunk of a slice whose W' is ready, else a P1 chunk of a slice at most K
-// slices past the oldest slice with unclaimed P2 chunks (K: the A copies of the slices in
-// flight fit a share of L2).  A P2 chunk only waits on P1 chunks already held by running
-// CTAs, so no grid size can deadlock.
+// slices past the oldest slice with unclaimed P2 chunks (K: the pass-2 operands of the slices
+// in flight fit a share of L2; when all fit, every P1 chunk goes first).  A P2 chunk only
+// waits on P1 chunks already held by running CTAs, so no grid size can deadlock.
 //
-// Roles (warp-specialised, one CTA per SM): warps 0-3 softmax, 4-7 epilogue (H rows,
-// partials, tree, W'), warp 8 TMA producer and work claiming, warp 9 MMA issue.
+// Roles (warp-specialised, one CTA per SM): warps 0-7 softmax (two groups of four), 8-11
+// epilogue (H rows, partials, tree, W'), 12 TMA producer and work claiming, 13 issues
+// S = Q U^T, 14 issues W, Delta and H.
 //
 // Operand layouts (shared memory, 128-byte swizzle, 1024-byte aligned blocks of 64 columns):
 //   Q, V tiles     [128 tokens][D]   K-major for S = Q U^T; MN-major (N = d) for A^T V
 //   U              [MP anchors][D]   K-major
-//   A tile         [128 tokens][128 anchors] MN-major as A^T (M = anchors) in pass 1,
-//                  K-major as A (M = tokens) in pass 2; anchors >= MP stay zero
+//   A tile         [128 tokens][128 anchors] MN-major as A^T (M = anchors) for the W MMA;
+//                  anchors >= MP stay zero.  MP = 64 with d = 64: only the 64 anchor columns,
+//                  the W MMA's anchor rows 64..127 come from the ones block (never read back)
+//   stored A       [128 tokens][MP]  K-major A operand of H = A W' (pass 2, ring slot)
 //   W' image       [MP][D]           MN-major B operand of H = A W'
 #include "common.cuh"
 #include "ptx.cuh"
