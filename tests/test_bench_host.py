@@ -1,0 +1,47 @@
+"""Host logic of bench.py that needs no GPU: the recorded ncu traffic is used only for the
+kernel code it was measured on."""
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _sources(tmp_path, body):
+    p = tmp_path / "k.cu"
+    p.write_text(body)
+    return [str(p)]
+
+
+def test_source_hash_ignores_comments_and_spacing(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", _sources(tmp_path, "int a = 1;  // one\nint b = 2;\n"))
+    h0 = bench.kernel_source_hash()
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", _sources(tmp_path, "// header\nint  a = 1;\n\nint b = 2;   // two\n"))
+    assert bench.kernel_source_hash() == h0
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", _sources(tmp_path, "int a = 1;\nint b = 3;\n"))
+    assert bench.kernel_source_hash() != h0
+
+
+def test_recorded_traffic_needs_matching_code(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", _sources(tmp_path, "int a = 1;\n"))
+    rec = {"entries": {"k@w": {"dram_bytes_per_launch": 123, "source_hash": bench.kernel_source_hash()}}}
+    f = tmp_path / "t.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("w", "k") == 123
+    assert bench.recorded_traffic("other", "k") is None
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", _sources(tmp_path, "int a = 2;\n"))
+    assert bench.recorded_traffic("w", "k") is None
+
+
+def test_committed_traffic_record_matches_the_sources():
+    """The committed launch-list record was taken on the kernel code as it is committed."""
+    with open(bench.TRAFFIC_FILE) as fh:
+        rec = json.load(fh)
+    for key, e in rec["entries"].items():
+        assert e["source_hash"] == bench.kernel_source_hash(), key
+        # per-launch averages, each truncated to whole bytes
+        assert abs(e["dram_bytes_per_launch"] - e["dram_read_bytes_per_launch"] - e["dram_write_bytes_per_launch"]) <= 1
