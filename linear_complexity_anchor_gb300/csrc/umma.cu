@@ -914,7 +914,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     }
                     if (!wait(s_full + sb, sph)) { ok = false; break; }
                     tc_fence_after();
-                    float v[MP], mg, zg;  // the whole row: both "halves" of a 2 MP-anchor softmax
+                    float v[MP], mg, zg;  // the whole row: the "half" of a 2 MP-wide row is MP columns
                     const uint32_t ts = trow + (sb ? LY::colS1 : LY::colS0);
                     if (p.m == MP) softmax_half<2 * MP, false>(ts, 0, p.m, p.c, v, mg, zg);
                     else softmax_half<2 * MP, true>(ts, 0, p.m, p.c, v, mg, zg);
@@ -929,7 +929,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         f32x2_split(mul_f32x2(f32x2(v[2 * j], v[2 * j + 1]), sc2), x0, x1);
                         pk[j] = pack_bf16x2(x0, x1);
                     }
-                    if (tr.kind == 1) {  // recomputed pass-2 A over its S buffer (see below)
+                    if (tr.kind == 1) {  // pass 2: A over its S buffer, the H MMA's A operand in TMEM
                         tmem_st32(ts, pk);
                         tmem_st_wait();
                         tc_fence_before();
