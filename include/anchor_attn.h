@@ -24,7 +24,9 @@
  * NULL = the legacy default stream).  No host synchronisation happens inside.
  * Workspace, where a variant needs one, is taken with cudaMallocAsync on `stream` and
  * released with cudaFreeAsync on the same stream before the call returns.
- * Results are bit-identical from run to run on the same device and library build.
+ * Results are bit-identical from run to run with the same library build: the way the tokens
+ * of a slice are cut into chunks, and so the order of every sum, depends on the shape alone
+ * (not on the device's SM or L2 size, nor on which CTA ran what).
  *
  * Shapes: B, heads, n >= 0 (a zero makes the call a no-op that returns OK and accepts NULL
  * pointers); m >= 1; d in {16, 32, 64, 128}; m * d <= 16384 (so m <= 256 for d <= 64 and
@@ -113,9 +115,13 @@ typedef struct {
     int variant;              /* ANCHOR_ATTN_VARIANT_*                                  */
     int kernels_per_call;     /* kernel launches one call makes                        */
     int splits;               /* token chunks per slice whose partials are reduced     */
-    int reserved;
+    int flags;                /* ANCHOR_ATTN_PLAN_* (tensor-core variant)               */
     size_t workspace_bytes;   /* device workspace one call allocates (0 if none)       */
 } anchor_attn_plan_t;
+
+enum {
+    ANCHOR_ATTN_PLAN_STORED_A = 1 /* pass 2 reads the A tiles pass 1 stored (else recomputes A) */
+};
 
 enum {
     ANCHOR_ATTN_VARIANT_EMPTY = 0,        /* nothing to do                                   */
@@ -133,12 +139,31 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, in
 /*
  * Failure detection for the tensor-core variant.  Its kernel never waits without a bound:
  * a wait on the tensor-memory pipeline or on another CTA's reduction gives up after 2 s,
- * sets a bit in a device-wide error word and lets the CTA leave, so the context stays
- * usable.  This call synchronises the device, copies that word to *code and clears it
- * (bit 0: a pipeline wait timed out, bit 1: a wait for a slice's reduction timed out;
- * 0: no failure since the last read).  Returns ANCHOR_ATTN_ERR_CUDA if the copy fails.
+ * sets a bit in a device-wide error word, waits (again bounded) for the copies and MMAs it
+ * has already issued, frees its tensor memory and leaves, so the context stays usable.  The
+ * output of such a call is incomplete.  This call synchronises the device, copies that word
+ * to *code and clears it (bit 0: a pipeline wait timed out, bit 1: a wait for a slice's
+ * reduction timed out, bit 2: a wait for issued work on the way out timed out; 0: no failure
+ * since the last read).  Returns ANCHOR_ATTN_ERR_CUDA if the copy fails.
  */
 ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_device_error(unsigned *code);
+
+/*
+ * FOR TESTS OF THE FAILURE DETECTION ONLY - not part of the forward's interface.  Runs the
+ * tensor-core variant of anchor_attn_forward (ANCHOR_ATTN_ERR_UNSUPPORTED if the shape would
+ * run another variant) with:
+ *   hold_slice      >= 0: the reduction of that (batch, head) slice never publishes its W',
+ *                   so every wait for it runs out (-1: no slice is held);
+ *   wait_ns         the limit of a wait on another CTA's reduction, in ns (> 0; the
+ *                   forward uses 2e9);
+ *   force_recompute nonzero: pass 2 recomputes A from Q even where the stored-A plan
+ *                   would run (same chunks, same result bits).
+ * With a held slice the call's H is incomplete and anchor_attn_device_error reports bit 1.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_test_forward(const void *Q, const void *U, const void *V, void *H,
+                                                              int B, int heads, int n, int m, int d, float scale,
+                                                              int hold_slice, unsigned long long wait_ns,
+                                                              int force_recompute, void *stream);
 
 /* Human-readable name of a status code (static storage). */
 ANCHOR_ATTN_API const char *anchor_attn_status_string(anchor_attn_status_t status);

@@ -15,7 +15,7 @@ import threading
 __all__ = [
     "LIB_PATH", "load", "forward", "anchor_attn_forward", "anchor_attn_forward_f32",
     "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "anchor_attn_forward_static_scratch_ptr",
-    "static_scratch_bytes", "device_error", "query_plan", "status_string",
+    "static_scratch_bytes", "device_error", "query_plan", "status_string", "anchor_attn_test_forward_ptr",
     "AnchorAttnError", "STATUS", "VARIANTS",
 ]
 
@@ -37,7 +37,10 @@ class AnchorAttnError(RuntimeError):
 
 class _Plan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("kernels_per_call", ctypes.c_int), ("splits", ctypes.c_int),
-                ("reserved", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+                ("flags", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+
+
+PLAN_STORED_A = 1
 
 
 def load(path: str | None = None) -> ctypes.CDLL:
@@ -55,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
             fn.restype = ctypes.c_int
+        lib.anchor_attn_test_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.c_ulonglong, i, vp]
+        lib.anchor_attn_test_forward.restype = ctypes.c_int
         lib.anchor_attn_query_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(_Plan)]
         lib.anchor_attn_query_plan.restype = ctypes.c_int
         lib.anchor_attn_static_scratch_bytes.argtypes = []
@@ -95,6 +100,14 @@ def anchor_attn_forward_static_scratch_ptr(Q: int, U: int, V: int, H: int, B: in
     return load().anchor_attn_forward_static_scratch(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
 
 
+def anchor_attn_test_forward_ptr(Q: int, U: int, V: int, H: int, B: int, heads: int, n: int, m: int, d: int,
+                                 scale: float, hold_slice: int = -1, wait_ns: int = 2_000_000_000,
+                                 force_recompute: bool = False, stream: int = 0) -> int:
+    """Raw call of the failure-detection test entry (tests only); returns the status code."""
+    return load().anchor_attn_test_forward(Q, U, V, H, B, heads, n, m, d, float(scale), int(hold_slice),
+                                           int(wait_ns), 1 if force_recompute else 0, stream)
+
+
 def static_scratch_bytes() -> int:
     return int(load().anchor_attn_static_scratch_bytes())
 
@@ -112,7 +125,8 @@ def query_plan(dtype: str, B: int, heads: int, n: int, m: int, d: int) -> dict:
     st = load().anchor_attn_query_plan(1 if dtype == "f32" else 0, B, heads, n, m, d, ctypes.byref(pl))
     _raise(st, "query_plan")
     return {"variant": VARIANTS.get(pl.variant, pl.variant), "kernels_per_call": pl.kernels_per_call,
-            "splits": pl.splits, "workspace_bytes": pl.workspace_bytes}
+            "splits": pl.splits, "workspace_bytes": pl.workspace_bytes,
+            "stored_a": bool(pl.flags & PLAN_STORED_A)}
 
 
 def _check_tensors(Q, U, V, H, dtype):

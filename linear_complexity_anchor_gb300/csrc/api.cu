@@ -62,6 +62,7 @@ struct Plan {
     int variant = ANCHOR_ATTN_VARIANT_EMPTY;
     int kernels = 0;
     int splits = 0;
+    int flags = 0;
     size_t workspace = 0;
 };
 
@@ -73,6 +74,7 @@ Plan make_plan(const Problem &p) {
         pl.variant = ANCHOR_ATTN_VARIANT_UMMA;
         pl.kernels = 1;
         pl.splits = u.C1;
+        pl.flags = u.store_a ? ANCHOR_ATTN_PLAN_STORED_A : 0;
         pl.workspace = u.workspace_bytes;
         return pl;
     }
@@ -89,13 +91,20 @@ Plan make_plan(const Problem &p) {
     return pl;
 }
 
-anchor_attn_status_t run(const Problem &p, void *stream_v) {
+// test: options of the failure-detection test entry (NULL for the product entries)
+struct TestRun {
+    anchor::UmmaOptions opt;
+    bool force_recompute;
+};
+
+anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test = nullptr) {
     const anchor_attn_status_t st = anchor::check_problem(p);
     if (st != ANCHOR_ATTN_OK) return st;
     if (p.slices() == 0 || p.n == 0) return ANCHOR_ATTN_OK;
 
     cudaStream_t stream = (cudaStream_t)stream_v;
     const Plan pl = make_plan(p);
+    if (test && pl.variant != ANCHOR_ATTN_VARIANT_UMMA) return ANCHOR_ATTN_ERR_UNSUPPORTED;
     cudaError_t e = cudaSuccess;
     switch (pl.variant) {
     case ANCHOR_ATTN_VARIANT_SIMT_SLICE:
@@ -114,14 +123,14 @@ anchor_attn_status_t run(const Problem &p, void *stream_v) {
         break;
     }
     case ANCHOR_ATTN_VARIANT_UMMA: {
-        const anchor::UmmaPlan u = anchor::umma_plan(p);
+        const anchor::UmmaPlan u = anchor::umma_plan(p, test && test->force_recompute);
         void *ws = nullptr;
         if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
         if (cudaMallocAsync(&ws, u.workspace_bytes, stream) != cudaSuccess) {
             cudaGetLastError();
             return ANCHOR_ATTN_ERR_ALLOC;
         }
-        e = anchor::launch_umma(p, u, ws, stream);
+        e = anchor::launch_umma(p, u, test ? test->opt : anchor::UmmaOptions{}, ws, stream);
         const cudaError_t ef = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = ef;
         break;
@@ -149,6 +158,18 @@ anchor_attn_status_t anchor_attn_forward_f32(const float *Q, const float *U, con
     return run(p, stream);
 }
 
+anchor_attn_status_t anchor_attn_test_forward(const void *Q, const void *U, const void *V, void *H, int B,
+                                              int heads, int n, int m, int d, float scale, int hold_slice,
+                                              unsigned long long wait_ns, int force_recompute, void *stream) {
+    if (wait_ns == 0) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const Problem p{Q, U, V, H, B, heads, n, m, d, scale, false};
+    TestRun t;
+    t.opt.hold_slice = hold_slice;
+    t.opt.wait_ns = wait_ns;
+    t.force_recompute = force_recompute != 0;
+    return run(p, stream, &t);
+}
+
 anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, int m, int d,
                                             anchor_attn_plan_t *plan) {
     if (!plan || (dtype != 0 && dtype != 1)) return ANCHOR_ATTN_ERR_INVALID_ARG;
@@ -159,7 +180,7 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
     plan->variant = pl.variant;
     plan->kernels_per_call = pl.kernels;
     plan->splits = pl.splits;
-    plan->reserved = 0;
+    plan->flags = pl.flags;
     plan->workspace_bytes = pl.workspace;
     return ANCHOR_ATTN_OK;
 }

@@ -66,6 +66,8 @@ constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run wh
 constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)
 constexpr int kUmmaP2Tiles = 16;     // tiles per pass-2 chunk (halved while items are too few)
 constexpr int kUmmaMinTiles = 4;     // smallest chunk either pass is cut into
+constexpr int kPlanSMs = 152;        // SM count the chunking assumes on every device
+constexpr double kStoreABytes = 64.0 * 1024 * 1024;  // largest A copy (all slices) pass 2 reads back
 struct UmmaPlan {
     int MP = 0;              // anchors padded to 64 or 128
     int NT = 0;              // 128-token tiles per slice
@@ -76,9 +78,16 @@ struct UmmaPlan {
     bool store_a = false;    // pass 2 loads the A copy (else it recomputes A from Q)
     size_t workspace_bytes = 0;
 };
+// Run-time options of one tensor-core launch.
+struct UmmaOptions {
+    int hold_slice = -1;                      // failure-detection tests: never publish this slice's W'
+    unsigned long long wait_ns = 2000000000ull;  // limit of a wait on other CTAs
+};
 bool umma_supported(const Problem &p);
-UmmaPlan umma_plan(const Problem &p);
-cudaError_t launch_umma(const Problem &p, const UmmaPlan &plan, void *workspace, cudaStream_t stream);
+UmmaPlan umma_plan(const Problem &p, bool force_recompute = false);
+size_t l2_bytes();
+cudaError_t launch_umma(const Problem &p, const UmmaPlan &plan, const UmmaOptions &opt, void *workspace,
+                        cudaStream_t stream);
 cudaError_t umma_read_and_clear_error(unsigned *out);
 
 }  // namespace anchor

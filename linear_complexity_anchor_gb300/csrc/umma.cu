@@ -58,9 +58,7 @@ constexpr int kT = 128;                         // tokens per tile (UMMA M)
 constexpr int kThreads = 480;
 constexpr int kWarpProducer = 12, kWarpMmaS = 13, kWarpMmaX = 14;
 constexpr int kIQ = 4;                          // item queue depth
-constexpr uint64_t kWaitNs = 2000000000ull;     // every wait gives up after 2 s
-constexpr double kL2ABudget = 256.0 * 1024 * 1024; // bytes kept for pass 2 (A or Q) of the slices in flight
-constexpr double kStoreABudget = 64.0 * 1024 * 1024; // largest A copy kept for pass 2
+constexpr uint64_t kWaitNs = 2000000000ull;     // a wait inside the CTA gives up after 2 s
 
 struct UParams {
     int slices, heads, B, n, m;
@@ -78,6 +76,8 @@ struct UParams {
     int K;                    // P1 may run at most K slices ahead of the P2 head
     int p1first;              // take every P1 chunk before any P2 chunk
     int store_a;              // pass 2 of split slices loads pass 1's A copy (else recomputes A)
+    int hold_slice;           // failure-detection tests: this slice's W' is never published (-1: none)
+    uint64_t wait_ns;         // limit of a wait on other CTAs (a slice's reduction)
 };
 
 template <int D, int MP>
@@ -108,21 +108,25 @@ struct Layout {
     static constexpr int kNU = kRoomy ? 2 : 1;
     static constexpr int kNA = kRoomy ? 2 : 1;
     static constexpr int kNW = kRoomy ? 2 : 1;
-    static constexpr int kFixed = kNU * kUB + kNA * kAB + kNW * kWB + kOnesB + kXchB + kBarB;
+    // a single A buffer (pass 1 only): recomputed pass-2 H tiles are staged in the epilogue's
+    // own buffer (4 KB per warp: 32 rows, one 64-column block at a time), so that their Q slot
+    // goes back right after S and no pass-2 tile holds up the next pass-1 A tile; with two A
+    // buffers there is no room for it, and H is staged in the Q slot
+    static constexpr bool kStageH = kNA == 1;
+    static constexpr int kHB = kStageH ? 4 * 32 * 128 : 0;
+    static constexpr int kFixed = kNU * kUB + kNA * kAB + kNW * kWB + kOnesB + kHB + kXchB + kBarB;
     static constexpr int kSlotsFit = (kMaxDyn - kFixed) / kSlotB;
     static constexpr int kNSlot = kSlotsFit > 8 ? 8 : kSlotsFit;
     // ring order per pass-1 tile: Q then V, or (a shallow ring) Q(t), then V(t-1), so that the
     // next S is not held up behind a V that is needed only after the softmax
     static constexpr bool kVLag = kNSlot < 5;
-    // a single A buffer doubles as the H staging buffer of recomputed pass-2 tiles (their A is
-    // in TMEM), so their Q slot goes back right after S; with two, H is staged in the Q slot
-    static constexpr bool kStageInA = kNA == 1;
     static constexpr int offU = 0;
     static constexpr int offA = offU + kNU * kUB;
     static constexpr int offW = offA + kNA * kAB;
     static constexpr int offRing = offW + kNW * kWB;
     static constexpr int offOnes = offRing + kNSlot * kSlotB;
-    static constexpr int offXch = offOnes + kOnesB;
+    static constexpr int offH = offOnes + kOnesB;
+    static constexpr int offXch = offH + kHB;
     static constexpr int offBar = offXch + kXchB;
     static constexpr int kBytes = offBar + kBarB;
     static constexpr int kSmem = kBytes + 1024;
@@ -135,11 +139,10 @@ struct Layout {
     static constexpr int colW1 = kWSep ? colW0 + D + 16 : colB0;
     static constexpr int kTmemCols = kWSep ? 512 : ((2 * MP + 2 * D) <= 256 ? 256 : 512);
     static_assert(kNSlot >= 3, "ring too shallow");
-    static_assert(!kStageInA || kAB >= kQB, "the single A buffer also stages H tiles");
     static_assert(!kPP || (kNA == 2 && !kVLag), "ping-pong softmax: one A buffer per group, V right behind Q");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
     static_assert(kUB % 1024 == 0 && offA % 1024 == 0 && offW % 1024 == 0 && offRing % 1024 == 0 &&
-                  offOnes % 1024 == 0, "operand blocks must be 1024-byte aligned");
+                  offOnes % 1024 == 0 && offH % 1024 == 0, "operand blocks must be 1024-byte aligned");
 };
 
 // Work items.  kind: 0 = P1 chunk, 1 = P2 chunk, 2 = whole slice, 3 = FLUSH (no tile follows
@@ -180,12 +183,12 @@ __device__ __forceinline__ int item_tiles(const Item &it, const UParams &p, int 
     return b1 - a1;
 }
 
-__device__ __forceinline__ TileRef tile_at(const Item &it, int a1, int b1, int idx, bool store_a) {
+__device__ __forceinline__ TileRef tile_at(const Item &it, int a1, int b1, int idx, const UParams &p) {
     TileRef r;
     r.slice = it.slice;
     r.chunk = it.chunk;
     r.full = it.kind == 2;
-    r.stored = it.kind == 1 && store_a;
+    r.stored = it.kind == 1 && p.store_a;
     const int n1 = b1 - a1;
     if (it.kind == 2) {
         const bool p2 = idx >= n1;
@@ -304,6 +307,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint8_t *sW = sm + LY::offW;
     uint8_t *sRing = sm + LY::offRing;
     uint8_t *sOnes = sm + LY::offOnes;
+    uint8_t *sH = sm + LY::offH;
     float2 *sXch = reinterpret_cast<float2 *>(sm + LY::offXch);  // [tile parity][group][row]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::offBar);
     // full/empty barrier pairs (arrival counts in brackets)
@@ -324,7 +328,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *w_empty = w_full + NW;             // [NW] (1)       MMAs reading W' completed
     uint64_t *iq_full = w_empty + NW;            // [kIQ] (1)      item queue
     uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (4)
-    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 + 2 * NA + 2 + 2 + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ;
+    uint64_t *mma_done = iq_empty + kIQ;         // [2]  (1)       every MMA of an issuer completed (exit)
+    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 + 2 * NA + 2 + 2 + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ + 2;
     static_assert(kNumBars * 8 + 3 * 4 * kIQ + 16 + 4 * NS <= LY::kBarB, "barrier area");
     int *s_items = reinterpret_cast<int *>(bars + kNumBars);           // [kIQ][3]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_items + 3 * kIQ);
@@ -368,6 +373,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_init(iq_full + i, 1);
             mbar_init(iq_empty + i, 4);
         }
+        mbar_init(mma_done + 0, 1);
+        mbar_init(mma_done + 1, 1);
         *s_abort = 0;
         *s_ast = 0;
         for (int i = 0; i < NS; ++i) s_slot_seq[i] = 0xffffffffu;
@@ -402,6 +409,18 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
         }
     };
+    // Bounded wait on the way out, after a wait gave up: it ignores the abort flag, because
+    // it lets copies and MMAs that were already issued finish before the CTA leaves.
+    auto drain_wait = [&](uint64_t *bar, uint32_t parity) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, parity)) {
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                atomicOr(&g_umma_error, 4u);
+                return;
+            }
+            __nanosleep(128);
+        }
+    };
     // wait for ring load number `seq` (see s_slot_seq)
     auto wait_slot = [&](uint32_t seq) -> bool {
         uint32_t *tag = s_slot_seq + seq % NS;
@@ -432,6 +451,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const uint64_t pol_keep = policy_evict_last();
         const uint64_t pol_stream = policy_evict_first();
         uint32_t ld_seq = 0, iq = 0, wuse = 0, nu = 0;
+        uint32_t wl_use[2] = {0u, 0u};  // per W' buffer: 1 + the use its last load was for (0: none)
         int u_head = -1;
         TileRef pend_v;
         bool has_pend_v = false, ok = true, flushed = true;
@@ -576,7 +596,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     has_pend_v = false;
                     flushed = true;
                 }
-                const bool give_up = __any_sync(FULLW, *s_abort != 0 || globaltimer_ns() - idle_since > kWaitNs);
+                const bool give_up = __any_sync(FULLW, *s_abort != 0 || globaltimer_ns() - idle_since > p.wait_ns);
                 if (give_up) {
                     if (L0 && !*s_abort) {
                         *s_abort = 1;
@@ -613,7 +633,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             int a1, b1;
             const int nt = item_tiles(it, p, a1, b1);
             for (int idx = 0; idx < nt && ok; ++idx) {
-                const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                const TileRef tr = tile_at(it, a1, b1, idx, p);
                 // Q is kept in L2 only for a whole-slice item, whose pass 2 follows at once: across
                 // split slices too much streams through L2 before pass 2 comes back to it
                 if (tr.stored) ok = load_slot(&ta_ld, tr.slice, tr.tile, pol_stream, MP);
@@ -639,6 +659,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                             asm volatile("fence.proxy.async.global;" ::: "memory");
                             mbar_arrive_expect_tx(w_full + wb, LY::kWB);
                             bulk_load(sW + wb * LY::kWB, p.wimg + (size_t)tr.slice * (D * MP), LY::kWB, w_full + wb);
+                            wl_use[wb] = wuse + 1u;
                         }
                     }
                     ++wuse;
@@ -650,6 +671,13 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
         }
         if (ok && has_pend_v) load_slot(&tv, pend_v.slice, pend_v.tile, pol_stream, D);
+        // Leave no copy in flight: after a wait gave up, loads may still be landing in the
+        // ring, U and W' buffers.  Each buffer's newest load completes its own phase.
+        for (uint32_t q = ld_seq > (uint32_t)NS ? ld_seq - NS : 0u; q < ld_seq; ++q)
+            drain_wait(slot_full + q % NS, (q / NS) & 1u);
+        for (uint32_t q = nu > (uint32_t)NU ? nu - NU : 0u; q < nu; ++q) drain_wait(u_full + q % NU, (q / NU) & 1u);
+        for (int b = 0; b < NW; ++b)
+            if (wl_use[b]) drain_wait(w_full + b, ((wl_use[b] - 1u) / NW) & 1u);
     } else if (warp == kWarpMmaS || warp == kWarpMmaX) {
         // =========================================================== MMA issue
         // Two issuing threads, so that neither kind of MMA waits behind the other: warp 13
@@ -689,7 +717,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     int a1, b1;
                     const int nt = item_tiles(it, p, a1, b1);
                     for (int idx = 0; idx < nt && ok; ++idx) {
-                        const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                        const TileRef tr = tile_at(it, a1, b1, idx, p);
                         const uint32_t mseq = lseq++;
                         if (LY::kVLag) {
                             if (lpend) ++lseq;
@@ -710,9 +738,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                             umma_bf16(tmem + dcol, adesc + (uint64_t)((((kk >> 2) * kT * 128) + (kk & 3) * 32) >> 4),
                                       bdesc + (uint64_t)((((kk >> 2) * MP * 128) + (kk & 3) * 32) >> 4), kIdS, kk > 0);
                         umma_commit(s_full + sb);
-                        // unless H is staged in the A buffer, a pass-2 tile's Q slot stays held: the
-                        // epilogue stages the H tile there
-                        if (tr.kind == 0 || LY::kStageInA) umma_commit(slot_empty + qslot);
+                        // unless the epilogue has a staging buffer of its own, a pass-2 tile's Q slot
+                        // stays held: the epilogue stages the H tile there
+                        if (tr.kind == 0 || LY::kStageH) umma_commit(slot_empty + qslot);
                         ++sidx;
                     }
                 }
@@ -834,7 +862,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     int a1, b1;
                     const int nt = item_tiles(it, p, a1, b1);
                     for (int idx = 0; idx < nt && ok; ++idx) {
-                        const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                        const TileRef tr = tile_at(it, a1, b1, idx, p);
                         const uint32_t mseq = lseq++;
                         if (lpend) {  // the previous pass-1 tile's V follows this tile's first slot
                             if (!do_x(pv, lseq++, pvs)) { ok = false; break; }
@@ -867,6 +895,10 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
                 if (ok && lpend) do_x(pv, lseq++, pvs);  // after the end marker the producer loads the last V
             }
+            // every MMA this thread issued has completed before the CTA leaves (after a wait
+            // gave up, nothing else waits for them)
+            umma_commit(mma_done + (warp - kWarpMmaS));
+            drain_wait(mma_done + (warp - kWarpMmaS), 0u);
         }
     } else if (warp < 8) {
         // =========================================================== softmax (warps 0-7)
@@ -877,7 +909,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         constexpr int HM = MP / 2;
         const uint64_t pol_keep = policy_evict_last();
-        uint32_t sidx = 0, ause = 0, iq = 0;
+        uint32_t sidx = 0, ause = 0, iq = 0;  // ause: uses of the A buffers (pass-1 tiles)
         uint32_t own = 0;  // ping-pong: this group's uses of its A buffer
         bool ok = true;
         auto arrive_w = [&](uint64_t *bar) {  // one arrival per warp
@@ -895,7 +927,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             int a1, b1;
             const int nt = item_tiles(it, p, a1, b1);
             for (int idx = 0; idx < nt && ok; ++idx) {
-                const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                const TileRef tr = tile_at(it, a1, b1, idx, p);
                 if (tr.stored) continue;  // pass 2 of a split slice has no softmax
                 if constexpr (LY::kPP) {
                     const int sb = (int)(sidx & 1u);
@@ -1000,7 +1032,6 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     tc_fence_before();
                     sm_sync();
                     if (tid == 0) mbar_arrive(p_full + sb);
-                    if (LY::kStageInA) ++ause;  // the epilogue stages this tile's H in the A buffer
                     continue;
                 }
                 const int ab = (int)(ause % NA);
@@ -1037,6 +1068,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
             }
         }
+        if (lane == 0) bulk_wait_group0();  // no A store of this warp is still reading shared memory
     } else {
         // =========================================================== epilogue (warps 8-11)
         // H tiles out of TMEM to global; at the end of a pass-1 phase, the chunk partial and
@@ -1044,7 +1076,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // TMEM lane: token row (H) / anchor row (W)
         const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint32_t iq = 0, p2 = 0, wuse = 0, chunks = 0, lseq = 0, ew = 0, euse = 0;
+        uint32_t iq = 0, p2 = 0, wuse = 0, chunks = 0, lseq = 0, ew = 0;
         bool lpend = false;
         uint32_t accuse[2] = {0u, 0u};
         bool ok = true;
@@ -1070,24 +1102,56 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         };
         const uint64_t pol_stream = policy_evict_first();
         int held = -1;  // ring slot whose H store may still be reading it (released one tile later)
-        // ause: this tile's place in the sequence of A-buffer uses (see kStageInA)
-        auto epilogue = [&](const TileRef &tr, int aslot, uint32_t ause) -> bool {
+        auto epilogue = [&](const TileRef &tr, int aslot) -> bool {
             if (tr.kind == 1) {
-                // H tile -> bf16 -> a staging buffer (the ring slot that held this tile's A or
-                // Q, or the A buffer) -> one TMA store per warp (32 rows), then the staging
-                // buffer is released
-                const bool in_a = !tr.stored && LY::kStageInA;
+                // H tile -> bf16 -> a staging buffer -> TMA stores of 32 rows per warp
                 const int hb = (int)(p2 & 1u);
                 if (!wait(acc_full + hb, accuse[hb] & 1u)) return false;
-                if (in_a && !wait(a_empty + 0, (ause & 1u) ^ 1u)) return false;  // its last user is done
                 tc_fence_after();
                 const uint32_t hcol = hb ? LY::colB1 : LY::colB0;
-                uint8_t *stage = in_a ? sA : sRing + aslot * LY::kSlotB;
                 const int r0 = tr.tile * kT + quarter * 32;
+                if (LY::kStageH && !tr.stored) {
+                    // the warp's own 4 KB buffer, one 64-column block of its 32 rows at a time:
+                    // the block is read from TMEM and packed to bf16 before the wait for the
+                    // buffer's last store
+                    uint8_t *hs = sH + quarter * (32 * 128);
+#pragma unroll
+                    for (int b = 0; b < D / 64; ++b) {
+                        uint4 pk[8];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float v[32];
+                            tmem_ld32(trow + hcol + b * 64 + h * 32, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) pk[4 * h + c] = pack8_scaled(v + 8 * c, 1.f);
+                        }
+                        if (b == D / 64 - 1) {  // the accumulator is read: the next H MMA may start
+                            tc_fence_before();
+                            arrive4(acc_empty + hb);
+                            ++accuse[hb];
+                            ++p2;
+                        }
+                        if (lane == 0) bulk_wait_group_read0();
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(hs + sw_off(lane, c, 32)) = pk[c];
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && r0 < p.n) {
+                            tma_store_3d(&th_st, hs, 64 * b, r0, tr.slice, pol_stream);
+                            bulk_commit_group();
+                        }
+                    }
+                    return true;
+                }
+                // otherwise the ring slot that held this tile's A or Q, released after the stores
+                // have read it
+                uint8_t *stage = sRing + aslot * LY::kSlotB;
                 // a deep ring lets the staging slot go back one tile later, so that this tile's
                 // store reads it while the next tile is drained; the last tile of an item
                 // releases both (the tile past the end, r0 >= n, is always an item's last)
-                const bool defer = LY::kNSlot >= 6 && !in_a && !tr.last;
+                const bool defer = LY::kNSlot >= 6 && !tr.last;
                 if constexpr (D == 64) {
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
@@ -1145,7 +1209,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 ep_sync();
                 if (row == 0) {
                     if (held >= 0) mbar_arrive(slot_empty + held);  // the last tile's store has read it
-                    if (!defer) mbar_arrive(in_a ? a_empty + 0 : slot_empty + aslot);
+                    if (!defer) mbar_arrive(slot_empty + aslot);
                 }
                 held = defer ? aslot : -1;
                 return true;
@@ -1261,7 +1325,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         // flag's release (after the barrier) publishes every thread's writes
                         fence_proxy_async_global();
                         ep_sync();
-                        if (row == 0) st_release_gpu(p.flags + 32 * tr.slice, 1u);
+                        if (row == 0 && tr.slice != p.hold_slice) st_release_gpu(p.flags + 32 * tr.slice, 1u);
                         return true;
                     }
                 }
@@ -1307,7 +1371,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             int a1, b1;
             const int nt = item_tiles(it, p, a1, b1);
             for (int idx = 0; idx < nt && ok; ++idx) {
-                const TileRef tr = tile_at(it, a1, b1, idx, p.store_a != 0);
+                const TileRef tr = tile_at(it, a1, b1, idx, p);
                 const int aslot = (int)(lseq % NS);
                 ++lseq;
                 if (LY::kVLag) {
@@ -1316,12 +1380,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 } else if (tr.kind == 0) {
                     ++lseq;  // this tile's V
                 }
-                const uint32_t use = euse;  // A-buffer uses: pass-1 tiles, and staged pass-2 tiles
-                if (tr.kind == 0 || (!tr.stored && LY::kStageInA)) ++euse;
-                if (!epilogue(tr, aslot, use)) { ok = false; break; }
+                if (!epilogue(tr, aslot)) { ok = false; break; }
                 if (tr.kind == 1 && tr.first) ++wuse;  // W' uses started so far
             }
         }
+        if (lane == 0) bulk_wait_group0();  // this warp's H stores have left shared memory
     }
 
     tc_fence_before();
@@ -1360,7 +1423,7 @@ bool make_map(CUtensorMap *map, const void *base, int cols, int rows, long long 
 }
 
 template <int D, int MP>
-cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream_t stream) {
+cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, const UmmaOptions &opt, void *ws, cudaStream_t stream) {
     static_assert(Layout<D, MP>::kSmem <= 227 * 1024, "shared memory");
     using LY = Layout<D, MP>;
     auto kern = anchor_umma_kernel<D, MP>;
@@ -1404,8 +1467,10 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
     // (written in pass 1, read in pass 2) fit in a share of L2
     p.store_a = pl.store_a ? 1 : 0;
     const double kept_slice = (double)pr.n * (pl.store_a ? MP : D) * 2;  // A copy, or Q for its re-read
-    p.K = (int)std::max<double>(2.0, std::min<double>((double)S, kL2ABudget / kept_slice));
+    p.K = (int)std::max<double>(2.0, std::min<double>((double)S, 2.0 * (double)l2_bytes() / kept_slice));
     p.p1first = p.K >= S ? 1 : 0;
+    p.hold_slice = opt.hold_slice;
+    p.wait_ns = opt.wait_ns;
     uint8_t *after = w + pl.header_bytes;
     p.pdelta = reinterpret_cast<float *>(after);
     p.part = p.pdelta + (size_t)S * pl.C1 * MP;
@@ -1429,19 +1494,19 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, void *ws, cudaStream
 
 }  // namespace
 
-// SMs of the current device (152 on GB300 when no device can be queried: plans are also
-// asked for on machines without one)
-int sm_count() {
+// L2 size of the current device (126 MiB, GB300's, when no device can be queried: plans are
+// also asked for on machines without one)
+size_t l2_bytes() {
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess ||
         n <= 0) {
         cudaGetLastError();
-        return 152;
+        return size_t(126) << 20;
     }
-    return n;
+    return (size_t)n;
 }
 
-UmmaPlan umma_plan(const Problem &p) {
+UmmaPlan umma_plan(const Problem &p, bool force_recompute) {
     UmmaPlan pl;
     const int MP = p.m <= 64 ? 64 : 128;
     pl.MP = MP;
@@ -1449,12 +1514,20 @@ UmmaPlan umma_plan(const Problem &p) {
     const long long S = p.slices();
     // Chunk sizes: long chunks mean fewer partials to reduce, fewer anchor reloads and fewer
     // item switches, but every SM needs work: halve a pass's chunk while the pass has fewer
-    // than one and a half items per SM.
-    const long long want = 3LL * sm_count() / 2;
+    // than one and a half items per SM.  The SM count assumed here is a constant, not the
+    // device's, so that the chunks - and so the summation order and the result bits - depend
+    // on the shape alone.
+    const long long want = 3LL * kPlanSMs / 2;
     int t1 = kUmmaP1Tiles, t2 = kUmmaP2Tiles;
     while (t1 > kUmmaMinTiles && S * ((pl.NT + t1 - 1) / t1) < want) t1 /= 2;
     while (t2 > kUmmaMinTiles && S * ((pl.NT + t2 - 1) / t2) < want) t2 /= 2;
     pl.C1 = (pl.NT + t1 - 1) / t1;
+    // Pass 2 reuses pass 1's A only when every slice's copy fits in half of a GB300's L2
+    // together (kStoreABytes); otherwise the copy would make a round trip through memory, and
+    // recomputing A from Q costs less.  The chunking does not depend on which of the two runs
+    // (nor on a forced recompute, a test option), and the stored and the recomputed A are the
+    // same bf16 values: every plan of a shape gives the same bits.
+    const bool store_a = !force_recompute && 2.0 * (double)S * p.n * MP <= (double)kStoreABytes;
     if (pl.NT <= kUmmaFullTiles || pl.C1 == 1) {
         pl.C1 = 1;
         pl.C2 = 0;
@@ -1468,10 +1541,7 @@ UmmaPlan umma_plan(const Problem &p) {
     pl.header_bytes = (256 + 2 * 128 * (size_t)S + 4 * (size_t)S * pl.C1 + 1023) / 1024 * 1024;
     const size_t reduce_bytes = 4 * (size_t)S * pl.C1 * MP + 4 * (size_t)S * pl.C1 * p.d * MP + 2 * (size_t)S * p.d * MP;
     pl.abuf_offset = (pl.header_bytes + reduce_bytes + 1023) / 1024 * 1024;
-    // Pass 2 reuses pass 1's A only when every slice's copy fits in L2 together; otherwise
-    // the copy would make a round trip through memory, and recomputing A costs less traffic
-    // (one re-read of Q) than storing it (a write and a read of A).
-    pl.store_a = 2.0 * (double)S * p.n * MP <= kStoreABudget;
+    pl.store_a = store_a;
     pl.workspace_bytes = pl.abuf_offset + (pl.store_a ? 2 * (size_t)S * p.n * MP : 0);
     return pl;
 }
@@ -1482,11 +1552,12 @@ bool umma_supported(const Problem &p) {
            p.slices() * ((p.n + kT - 1) / kT) * 3 < 0x7fffffffLL;
 }
 
-cudaError_t launch_umma(const Problem &p, const UmmaPlan &pl, void *workspace, cudaStream_t stream) {
-    if (p.d == 64 && pl.MP == 64) return launch_t<64, 64>(p, pl, workspace, stream);
-    if (p.d == 64 && pl.MP == 128) return launch_t<64, 128>(p, pl, workspace, stream);
-    if (p.d == 128 && pl.MP == 64) return launch_t<128, 64>(p, pl, workspace, stream);
-    if (p.d == 128 && pl.MP == 128) return launch_t<128, 128>(p, pl, workspace, stream);
+cudaError_t launch_umma(const Problem &p, const UmmaPlan &pl, const UmmaOptions &opt, void *workspace,
+                        cudaStream_t stream) {
+    if (p.d == 64 && pl.MP == 64) return launch_t<64, 64>(p, pl, opt, workspace, stream);
+    if (p.d == 64 && pl.MP == 128) return launch_t<64, 128>(p, pl, opt, workspace, stream);
+    if (p.d == 128 && pl.MP == 64) return launch_t<128, 64>(p, pl, opt, workspace, stream);
+    if (p.d == 128 && pl.MP == 128) return launch_t<128, 128>(p, pl, opt, workspace, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -7,6 +7,9 @@ Parity bar (the forward's stated tolerances):
          error scales with its summands (~rms), not with itself.
   bf16 : |g - o| <= 1e-2 + 2e-2 |o| elementwise (2e-2 relative / 1e-2 absolute).
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 import gen
@@ -44,3 +47,27 @@ def assert_parity(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "") 
 
 def widen(x: dict, dtype: str) -> dict:
     return {k: gen.to_float64(v, dtype) for k, v in x.items()}
+
+
+def oracle_slices(orc, w, x: dict, slices) -> dict:
+    """Oracle H of the listed (batch, head) slices, {slice: [n][d] float64}, computed on a
+    thread pool: the oracle is plain C called through ctypes, which releases the GIL, so the
+    slices run on every host core (each call is still the single-threaded oracle)."""
+    U = gen.to_float64(x["U"], w.dtype)
+
+    def one(s):
+        b, h = divmod(s, w.heads)
+        return s, orc.slice_forward(gen.to_float64(x["Q"][b, h], w.dtype), U[h],
+                                    gen.to_float64(x["V"][b, h], w.dtype), w.scale)["H"]
+
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as ex:
+        return dict(ex.map(one, list(slices)))
+
+
+def assert_slices(got, w, refs: dict, what: str) -> float:
+    """Element-by-element parity of every slice in refs; got is the device or host H."""
+    worst = 0.0
+    for s, ref in sorted(refs.items()):
+        b, h = divmod(s, w.heads)
+        worst = max(worst, assert_parity(to_host64(got[b, h]), ref, w.dtype, f"{what} slice ({b},{h})"))
+    return worst
