@@ -2,7 +2,8 @@
 """Throughput of the anchor-attention forward H = A Delta^{-1} A^T V on GB300.
 
 One step = one forward over the whole workload (every (batch, head) slice) through the C
-ABI.  Prints ONE JSON line on rank 0.
+ABI.  Prints ONE JSON line on rank 0: the headline workload (long_16k by default) and, under
+"workloads", every other workload timed the same way in the same run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -12,10 +13,17 @@ region is bracketed by barriers and the max over ranks is reported.
 
 --impl reference times the CPU oracle (plain C, double, one thread) on a bounded sample
 of the same workload per step, on rank 0 only.
+
+Timing: W untimed calls, then K calls bracketed by a barrier and a device synchronisation,
+CUDA events around each call on the launching stream, input/output sets rotated so that
+each step's working set is larger than L2.  Clocks and throttle reasons are sampled through
+NVML (about every 0.5 ms) while the timed calls run.  A nonzero device error word after the
+timed calls marks the line invalid.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import csv
 import hashlib
 import io
@@ -37,10 +45,13 @@ METRIC = "anchor-attn tokens·heads/s at 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "tokens*heads/s"
 DEFAULT_WORKLOAD = "long_16k"
 FALLBACK_HBM_GBS = 6800.0
-L2_BYTES = 129 * 1024 * 1024
+FALLBACK_L2_BYTES = 126 * 1024 * 1024
+FMA_LANES_PER_SM = 128          # fp32 FMA lanes per SM (4 sub-partitions x 32)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "linear_complexity_anchor_gb300", "csrc", f)
                   for f in ("umma.cu", "simt.cu", "api.cu", "common.cuh", "ptx.cuh")]
+KERNEL_OF_VARIANT = {"umma": "anchor_umma_kernel", "simt_split": "simt_chunk_kernel",
+                     "simt_slice": "simt_full_kernel"}
 
 
 def parse_args(argv=None):
@@ -55,6 +66,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch count (a smaller case for profiling)")
+    ap.add_argument("--only", action="store_true", help="time the headline workload only (no sub-records)")
     return ap.parse_args(argv)
 
 
@@ -113,8 +125,66 @@ def recorded_traffic(workload: str, kernel: str):
         return None
 
 
+class NvmlClockSampler:
+    """SM clock and throttle reasons read through NVML (ctypes, no Python package needed)
+    every ~0.5 ms on a background thread while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id: str):
+        import threading
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) != 0:
+            count = ctypes.c_uint()
+            # one visible device: it is the one being timed
+            if (self.lib.nvmlDeviceGetCount_v2(ctypes.byref(count)) != 0 or count.value != 1 or
+                    self.lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)) != 0):
+                raise RuntimeError(f"no NVML device at {pci_bus_id}")
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.samples, self.reasons = [], 0
+        self.stop_ev = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self._reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _run(self):
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_ev.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(float(mhz.value))
+            if self._reason_fn(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(0.0005)
+
+    def start(self):
+        self.thread.start()
+
+    def stop(self) -> dict:
+        self.stop_ev.set()
+        self.thread.join(timeout=5)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if self.reasons & b),
+                "samples": len(self.samples), "source": "nvml"}
+
+
+def clock_sampler(dev_index: int):
+    try:
+        import torch
+        pr = torch.cuda.get_device_properties(dev_index)
+        bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        return NvmlClockSampler(bus)
+    except Exception:
+        return ClockSampler(dev_index)
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region
+    (the fallback where NVML cannot be loaded directly)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -158,27 +228,64 @@ class ClockSampler:
                 if v.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
-def cpu_baseline(w: gen.Workload, x: dict, budget_s: float) -> dict:
-    """The oracle as it stands (one thread, double) on whole slices of the same inputs until
-    the time budget is spent (at least one slice)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(w: gen.Workload, x: dict, budget_s: float, threads: int = 1) -> dict:
+    """The oracle as it stands (plain C, double, one thread per slice) on whole slices of the
+    same inputs until the time budget is spent (at least one slice per thread).  threads > 1
+    runs that many slices at once on a thread pool: the oracle is called through ctypes,
+    which releases the GIL, so each call runs on its own host core."""
+    import threading
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     oracle.build()
     U = gen.to_float64(x["U"], w.dtype)
-    done, t0 = 0, time.perf_counter()
-    while True:
-        b, h = divmod(done % w.slices, w.heads)
-        oracle.slice_forward(gen.to_float64(x["Q"][b, h], w.dtype), U[h], gen.to_float64(x["V"][b, h], w.dtype),
-                             w.scale)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or done >= w.slices:
-            break
-    return {"value": done * w.n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+    lock = threading.Lock()
+    state = {"next": 0, "done": 0}
+    t0 = time.perf_counter()
+
+    def worker():
+        while True:
+            with lock:
+                if time.perf_counter() - t0 >= budget_s and state["done"] > 0 or state["next"] >= w.slices:
+                    return
+                s = state["next"]
+                state["next"] += 1
+            b, h = divmod(s, w.heads)
+            oracle.slice_forward(gen.to_float64(x["Q"][b, h], w.dtype), U[h], gen.to_float64(x["V"][b, h], w.dtype),
+                                 w.scale)
+            with lock:
+                state["done"] += 1
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for f in [ex.submit(worker) for _ in range(threads)]:
+            f.result()
+    el = time.perf_counter() - t0
+    done = state["done"]
+    return {"value": done * w.n / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "cpu": cpu_model(),
             "sample": f"{done} of {w.slices} slices (n={w.n}, m={w.m}, d={w.d}) in {el:.2f} s, "
-                      f"single-threaded C double-precision oracle"}
+                      f"C double-precision oracle, {'one slice per thread on ' + str(threads) + ' threads' if threads > 1 else 'single-threaded'}"}
 
 
 def run_reference(args) -> None:
@@ -210,12 +317,114 @@ def run_reference(args) -> None:
         "data": "synthetic (seeded generator, value distributions of the workload)",
         "config": {"workload": w.name, "B": w.B, "heads": w.heads, "n": w.n, "m": w.m, "d": w.d,
                    "input_dtype": w.dtype, "step_sample": "one (batch, head) slice per step"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
                          "sample": f"one slice of {w.n} tokens per step, {args.steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+def l2_bytes(dev) -> int:
+    import torch
+    try:
+        n = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0))
+        return n if n > 0 else FALLBACK_L2_BYTES
+    except Exception:
+        return FALLBACK_L2_BYTES
+
+
+def host_inputs(w: gen.Workload, seed: int) -> tuple:
+    import torch
+    x = gen.make_inputs(w, seed=seed)
+
+    def host_tensor(a):
+        t = torch.from_numpy(a if w.dtype == "f32" else a.view("int16"))
+        return t if w.dtype == "f32" else t.view(torch.bfloat16)
+
+    return x, tuple(host_tensor(x[k]).pin_memory() for k in "QUV")
+
+
+def time_workload(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev, world: int, sample_clocks: bool):
+    """W untimed calls, then K timed calls (CUDA events on the launching stream around each,
+    and around all), with input/output sets rotated so that each step's working set exceeds
+    L2.  Returns a dict of the timings (max over ranks), the device error word and clocks."""
+    import torch
+    import torch.distributed as dist
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    hQ, hU, hV = hQUV
+    nsets = max(1, min(8, math.ceil(3 * l2_bytes(dev) / w.algorithmic_bytes)))
+    sets = [{"Q": hQ.to(dev), "U": hU.to(dev), "V": hV.to(dev), "H": torch.empty(hQ.shape, dtype=tdt, device=dev)}
+            for _ in range(nsets)]
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    fwd = pkg.anchor_attn_forward_f32_ptr if w.dtype == "f32" else pkg.anchor_attn_forward_ptr
+    ptrs = [(st["Q"].data_ptr(), st["U"].data_ptr(), st["V"].data_ptr(), st["H"].data_ptr()) for st in sets]
+
+    def call(st):
+        pkg.forward(st["Q"], st["U"], st["V"], H=st["H"], scale=w.scale, stream=stream)
+
+    def call_raw(i):  # the C ABI with the same pointers and stream, minus the Python tensor checks
+        st_ = fwd(*ptrs[i % nsets], w.B, w.heads, w.n, w.m, w.d, w.scale, stream.cuda_stream)
+        if st_ != 0:
+            raise RuntimeError(f"anchor_attn call failed: {pkg.status_string(st_)}")
+
+    for i in range(W):
+        call(sets[i % nsets])
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = clock_sampler(torch.cuda.current_device()) if sample_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.01)
+    # Queue the timed calls behind a short GPU sleep, so that the host enqueues them faster
+    # than the GPU runs them: the events then time the GPU work back to back, not the host's
+    # launch overhead (the sleep itself is before t_start).
+    with torch.cuda.stream(stream):
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(int(2e6))  # about a millisecond of clock cycles
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        call_raw(i)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    if world > 1:
+        dist.barrier()
+    derr = pkg.device_error()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    elapsed_ms, call_ms, derr_max = max_over_ranks([elapsed_ms, call_ms, float(derr)], dev, world)
+    return {"elapsed_ms": elapsed_ms, "call_ms": call_ms, "nsets": nsets, "sets": sets, "stream": stream,
+            "call": call, "device_error": int(derr_max), "clocks": clk}
+
+
+def roofline(w: gen.Workload, plan: dict, call_ms: float) -> dict:
+    peak, peak_src = peaks()
+    achieved = w.algorithmic_bytes / (call_ms / 1e3) / 1e9
+    kernel = KERNEL_OF_VARIANT.get(plan["variant"], plan["variant"])
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(w.name, kernel), "peak_source": f"{peak_src} hbm_gbs", "kernel": kernel,
+            "algorithmic_bytes_per_launch": w.algorithmic_bytes, "call_ms": call_ms,
+            "kernels_per_call": plan["kernels_per_call"]}
+
+
+def fma_roofline(w: gen.Workload, call_ms: float, sm_mhz, dev) -> dict:
+    """The CUDA-core variants against the fp32 FMA peak: 2 flops per FMA lane per clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = float(sm_mhz) if sm_mhz else 2070.0
+    peak = sms * FMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    achieved = w.flops / (call_ms / 1e3) / 1e12
+    return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"{sms} SMs x {FMA_LANES_PER_SM} fp32 FMA lanes x 2 flop x {mhz:.0f} MHz",
+            "flops_per_launch": w.flops}
 
 
 def run_ours(args) -> None:
@@ -229,65 +438,24 @@ def run_ours(args) -> None:
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkg.load()
+    if pkg.device_error() != 0:
+        raise RuntimeError("device error word set before the bench started")
     w = gen.WORKLOADS[args.workload]
     if args.batch is not None:
         w = w.with_(B=args.batch)
-    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     plan = pkg.query_plan(w.dtype, w.B, w.heads, w.n, w.m, w.d)
-
-    x = gen.make_inputs(w, seed=rank)
-
-    def host_tensor(a):
-        t = torch.from_numpy(a if w.dtype == "f32" else a.view("int16"))
-        return t if w.dtype == "f32" else t.view(torch.bfloat16)
-
-    hQ, hU, hV = (host_tensor(x[k]).pin_memory() for k in "QUV")
-    step_bytes = w.algorithmic_bytes
-    nsets = max(1, min(8, math.ceil(3 * L2_BYTES / step_bytes)))
-    sets = []
-    for _ in range(nsets):
-        sets.append({"Q": hQ.to(dev), "U": hU.to(dev), "V": hV.to(dev),
-                     "H": torch.empty(hQ.shape, dtype=tdt, device=dev)})
-    stream = torch.cuda.Stream(device=dev)
-    torch.cuda.synchronize()
-
-    def call(s):
-        pkg.forward(s["Q"], s["U"], s["V"], H=s["H"], scale=w.scale, stream=stream)
-
-    for i in range(args.warmup):
-        call(sets[i % nsets])
-    torch.cuda.synchronize()
-
+    x, hQUV = host_inputs(w, seed=rank)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    time.sleep(0.15)
-    t_start.record(stream)
-    for i in range(K):
-        ev[i][0].record(stream)
-        call(sets[i % nsets])
-        ev[i][1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    elapsed_ms, call_ms = max_over_ranks([elapsed_ms, call_ms], dev, world)
-
+    t = time_workload(pkg, w, hQUV, K, args.warmup, dev, world, sample_clocks=True)
     units = world * w.slices * w.n * K
-    value = units / (elapsed_ms / 1e3)
+    value = units / (t["elapsed_ms"] / 1e3)
 
     # end to end through the public API: pinned host inputs -> device, forward, H -> host
+    hQ, hU, hV = hQUV
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     E = max(1, args.e2e_steps)
     hH = torch.empty(hQ.shape, dtype=tdt).pin_memory()
-    s0 = sets[0]
+    s0, stream, call = t["sets"][0], t["stream"], t["call"]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -302,42 +470,68 @@ def run_ours(args) -> None:
             hH.copy_(s0["H"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
+    e2e_err = pkg.device_error()
     e2e_ms = e0.elapsed_time(e1)
     (e2e_ms,) = max_over_ranks([e2e_ms], dev, world)
     e2e_value = world * w.slices * w.n * E / (e2e_ms / 1e3)
     elem = 4 if w.dtype == "f32" else 2
     h2d = (hQ.numel() + hU.numel() + hV.numel()) * elem
     d2h = hH.numel() * elem
+    del t["sets"], s0
+    torch.cuda.empty_cache()
 
-    cpu = None
+    # every other workload, timed the same way in the same run
+    subs = {}
+    if not args.only:
+        for name in sorted(gen.WORKLOADS):
+            if name == w.name:
+                continue
+            ws = gen.WORKLOADS[name]
+            wplan = pkg.query_plan(ws.dtype, ws.B, ws.heads, ws.n, ws.m, ws.d)
+            _, hq = host_inputs(ws, seed=rank)
+            ts = time_workload(pkg, ws, hq, K, args.warmup, dev, world, sample_clocks=True)
+            rec = {"ms_per_step": ts["elapsed_ms"] / K,
+                   "value": world * ws.slices * ws.n * K / (ts["elapsed_ms"] / 1e3), "unit": UNIT,
+                   "dtype": ws.dtype, "variant": wplan["variant"],
+                   "config": {"B": ws.B, "heads": ws.heads, "n": ws.n, "m": ws.m, "d": ws.d},
+                   "l2": f"{ws.algorithmic_bytes / 1e6:.1f} MB per step, {ts['nsets']} rotating set(s)",
+                   "roofline": roofline(ws, wplan, ts["call_ms"]), "device_error": ts["device_error"],
+                   "clocks": ts["clocks"]}
+            if wplan["variant"] != "umma":
+                rec["fma_roofline"] = fma_roofline(ws, ts["call_ms"], (ts["clocks"] or {}).get("sm_mhz"), dev)
+            if ts["device_error"]:
+                rec["invalid"] = f"device error word {ts['device_error']:#x} after the timed calls"
+            subs[name] = rec
+            del ts
+            torch.cuda.empty_cache()
+
+    cpu = cpu_par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, x, args.cpu_seconds)
+        cpu_par = cpu_baseline(w, x, max(4.0, args.cpu_seconds / 2), threads=os.cpu_count() or 1)
 
     if rank == 0:
-        peak, peak_src = peaks()
-        achieved = w.algorithmic_bytes / (call_ms / 1e3) / 1e9
-        kernel = {"umma": "anchor_umma_kernel", "simt_split": "simt_partial_kernel",
-                  "simt_slice": "simt_slice_kernel"}.get(plan["variant"], plan["variant"])
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": t["elapsed_ms"] / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded counter-based generator; value distributions of the workload)",
             "config": {"workload": w.name, "B": w.B, "heads": w.heads, "n": w.n, "m": w.m, "d": w.d,
                        "scale": w.scale, "variant": plan["variant"],
-                       "l2": (f"inputs larger than L2: {step_bytes / 1e6:.0f} MB per step, "
-                              f"{nsets} rotating input/output set(s)")},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": recorded_traffic(w.name, kernel),
-                         "peak_source": f"{peak_src} hbm_gbs", "kernel": kernel,
-                         "algorithmic_bytes_per_launch": w.algorithmic_bytes,
-                         "call_ms": call_ms, "kernels_per_call": plan["kernels_per_call"]},
+                       "l2": (f"inputs larger than L2: {w.algorithmic_bytes / 1e6:.0f} MB per step, "
+                              f"{t['nsets']} rotating input/output set(s)")},
+            "roofline": roofline(w, plan, t["call_ms"]),
             "cpu_baseline": cpu,
+            "cpu_baseline_parallel": cpu_par,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": E},
             "gpu_launches": plan["kernels_per_call"] * K,
-            "clocks": clk,
+            "clocks": t["clocks"],
+            "device_error": t["device_error"],
+            "workloads": subs,
         }
+        if t["device_error"] or e2e_err:
+            line["invalid"] = f"device error word {t['device_error'] | e2e_err:#x} after the timed calls"
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

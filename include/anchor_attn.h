@@ -89,17 +89,20 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, con
  * engine that owns all device memory, or a loop with a fixed memory budget - and so cannot
  * use anchor_attn_forward, which takes a workspace with cudaMallocAsync on every call.
  *
- * It always runs the token-chunk CUDA-core variant (fp32 FMA, fixed-order reduction), whose
- * partial sums live in a fixed array compiled into the library:
+ * It always runs the chunked CUDA-core kernel (fp32 FMA, fixed-order reduction), whose
+ * workspace lives in a fixed array compiled into the library:
  *   - limit: anchor_attn_static_scratch_bytes() (16 MiB); a problem needing more returns
  *     ANCHOR_ATTN_ERR_SCRATCH_LIMIT before anything is launched.  It needs
- *     4 * B * heads * (ceil(n / 512) * (m * d + m) + m * d) bytes.
+ *     roundup(4 * (32 + 2 * B * heads), 256) + 4 * B * heads * (ceil(n / 512) * (m * d + m) + m * d)
+ *     bytes (a header of counters and flags, the chunk partials, W').
  *   - the array exists on every GPU that loads the library, until the process exits;
- *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture;
- *   - every call shares the array and it keeps the last call's contents (nothing needs to
- *     start at zero); calls whose kernels overlap on the GPU (other streams or host threads)
- *     race on it and must be serialised by the caller.
+ *   - the first call on a device (and the first after the device's context changed, e.g.
+ *     after cudaDeviceReset) looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture;
+ *   - every call shares the array and it keeps the last call's contents; each call clears
+ *     the header on its stream (cudaMemsetAsync, no allocation); calls whose kernels overlap
+ *     on the GPU (other streams or host threads) race on it and must be serialised by the
+ *     caller.
  * Calls no cudaMalloc, cudaMallocAsync, cudaFree or allocating library routine.
  */
 ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_static_scratch(const void *Q, const void *U,
@@ -110,7 +113,8 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_static_scratch(const vo
 /* Size in bytes of the fixed scratch array behind anchor_attn_forward_static_scratch. */
 ANCHOR_ATTN_API size_t anchor_attn_static_scratch_bytes(void);
 
-/* Static description of what one call with these arguments launches (no GPU access). */
+/* Static description of what one call with these arguments launches (no GPU access).  A shape
+ * that no variant can run returns ANCHOR_ATTN_ERR_UNSUPPORTED, as the forward would. */
 typedef struct {
     int variant;              /* ANCHOR_ATTN_VARIANT_*                                  */
     int kernels_per_call;     /* kernel launches one call makes                        */

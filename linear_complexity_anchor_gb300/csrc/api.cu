@@ -23,11 +23,12 @@ anchor_attn_status_t check_shape(int B, int heads, int n, int m, int d) {
     if (B < 0 || heads < 0 || n < 0 || m < 1 || d < 1) return ANCHOR_ATTN_ERR_INVALID_ARG;
     if (!supported_d(d) || (long long)m * d > 16384) return ANCHOR_ATTN_ERR_UNSUPPORTED;
     const long long slices = (long long)B * heads;
-    // element counts must fit in 63 bits, and the SIMT grids (slices x tiles) in 2^31 - 1
+    // element counts must fit in 63 bits, and the work items of a call (slices x 64-token
+    // blocks, and a little more) in 2^31 - 1
     if (slices > 0 && n > 0) {
         if ((long long)n * d > (1LL << 62) / slices) return ANCHOR_ATTN_ERR_INVALID_ARG;
-        const long long tiles = (n + anchor::kSimtTile - 1) / anchor::kSimtTile;
-        if (slices * tiles > 0x7fffffffLL) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+        if (slices * ((n + 63) / 64 + (n + anchor::kSimtChunk - 1) / anchor::kSimtChunk) > 0x7fffffffLL)
+            return ANCHOR_ATTN_ERR_UNSUPPORTED;
     }
     return ANCHOR_ATTN_OK;
 }
@@ -56,8 +57,6 @@ namespace {
 using anchor::Problem;
 using anchor::check_shape;
 
-constexpr size_t kMaxSmem = 227 * 1024;
-
 struct Plan {
     int variant = ANCHOR_ATTN_VARIANT_EMPTY;
     int kernels = 0;
@@ -78,16 +77,17 @@ Plan make_plan(const Problem &p) {
         pl.workspace = u.workspace_bytes;
         return pl;
     }
-    if (p.n <= 512 && anchor::simt_slice_smem_bytes(p.n, p.m, p.d) <= kMaxSmem) {
+    if (anchor::simt_full_fits(p)) {
         pl.variant = ANCHOR_ATTN_VARIANT_SIMT_SLICE;
         pl.kernels = 1;
         pl.splits = 1;
         return pl;
     }
+    if (!anchor::simt_chunk_fits(p)) return pl;  // variant EMPTY with work to do: unsupported
     pl.variant = ANCHOR_ATTN_VARIANT_SIMT_SPLIT;
-    pl.kernels = 3;
+    pl.kernels = 1;
     pl.splits = (p.n + anchor::kSimtChunk - 1) / anchor::kSimtChunk;
-    pl.workspace = anchor::simt_split_workspace_bytes(p, pl.splits);
+    pl.workspace = anchor::simt_chunk_layout(p).total_bytes;
     return pl;
 }
 
@@ -108,7 +108,7 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
     cudaError_t e = cudaSuccess;
     switch (pl.variant) {
     case ANCHOR_ATTN_VARIANT_SIMT_SLICE:
-        e = anchor::launch_simt_slice(p, stream);
+        e = anchor::launch_simt_full(p, stream);
         break;
     case ANCHOR_ATTN_VARIANT_SIMT_SPLIT: {
         void *ws = nullptr;
@@ -117,7 +117,7 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
             cudaGetLastError();
             return ANCHOR_ATTN_ERR_ALLOC;
         }
-        e = anchor::launch_simt_split(p, pl.splits, (float *)ws, stream);
+        e = anchor::launch_simt_chunk(p, ws, stream);
         const cudaError_t ef = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = ef;
         break;
@@ -138,7 +138,11 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
     default:
         return ANCHOR_ATTN_ERR_UNSUPPORTED;
     }
-    return e == cudaSuccess ? ANCHOR_ATTN_OK : ANCHOR_ATTN_ERR_CUDA;
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // a failed call leaves no error behind for the caller's next check
+        return ANCHOR_ATTN_ERR_CUDA;
+    }
+    return ANCHOR_ATTN_OK;
 }
 
 }  // namespace
@@ -177,6 +181,7 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
     if (st != ANCHOR_ATTN_OK) return st;
     const Problem p{nullptr, nullptr, nullptr, nullptr, B, heads, n, m, d, 1.f, dtype == 1};
     const Plan pl = make_plan(p);
+    if (pl.variant == ANCHOR_ATTN_VARIANT_EMPTY && p.slices() > 0 && n > 0) return ANCHOR_ATTN_ERR_UNSUPPORTED;
     plan->variant = pl.variant;
     plan->kernels_per_call = pl.kernels;
     plan->splits = pl.splits;
@@ -187,7 +192,14 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    return anchor::umma_read_and_clear_error(code) == cudaSuccess ? ANCHOR_ATTN_OK : ANCHOR_ATTN_ERR_CUDA;
+    unsigned a = 0, b = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
+        anchor::simt_read_and_clear_error(&b) != cudaSuccess) {
+        cudaGetLastError();
+        return ANCHOR_ATTN_ERR_CUDA;
+    }
+    *code = a | b;
+    return ANCHOR_ATTN_OK;
 }
 
 const char *anchor_attn_status_string(anchor_attn_status_t s) {

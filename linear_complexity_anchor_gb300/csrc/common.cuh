@@ -52,14 +52,19 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // --- SIMT (CUDA-core) variants -------------------------------------------------------
-size_t simt_slice_smem_bytes(int n, int m, int d);
-cudaError_t launch_simt_slice(const Problem &p, cudaStream_t stream);
-
-constexpr int kSimtTile = 32;        // tokens per tile in the split variant
-constexpr int kSimtChunk = 512;      // tokens per split (chunk) in the split variant
-size_t simt_split_smem_bytes(int m, int d);
-size_t simt_split_workspace_bytes(const Problem &p, int splits);
-cudaError_t launch_simt_split(const Problem &p, int splits, float *workspace, cudaStream_t stream);
+constexpr int kSimtChunk = 512;                  // tokens per pass-1 chunk of the chunked kernel
+constexpr size_t kSimtMaxSmem = 220 * 1024;      // dynamic shared memory a CUDA-core CTA may use
+// workspace of the chunked kernel: a zeroed header (ticket, per-slice arrival counters and
+// ready flags), the chunk partials [slices][chunks][m d + m] fp32 and W' [slices][m d] fp32
+struct SimtLayout {
+    size_t header_bytes = 0, part_offset = 0, wprime_offset = 0, total_bytes = 0;
+};
+bool simt_full_fits(const Problem &p);     // the whole slice fits one CTA's shared memory
+bool simt_chunk_fits(const Problem &p);    // the chunked kernel's anchors and tiles fit
+SimtLayout simt_chunk_layout(const Problem &p);
+cudaError_t launch_simt_full(const Problem &p, cudaStream_t stream);
+cudaError_t launch_simt_chunk(const Problem &p, void *workspace, cudaStream_t stream);
+cudaError_t simt_read_and_clear_error(unsigned *out);
 
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA

@@ -2,275 +2,497 @@
 //   H = A Delta^{-1} (A^T V),  A = rowsoftmax(scale * Q U^T),  Delta = diag(colsum A)
 // (AnchorFormer, arXiv 2505.16463; pith.science verdict, "key_machinery" and the referee
 // summary of Eq. 11/12).  Used for the fp32 entry point, for m < 32 (where a tensor-core
-// tile would be mostly padding) and for shapes the tensor-core path does not cover.
+// tile would be mostly padding), for d in {16, 32} and for a non-positive scale.
 //
-// Two variants:
-//   slice : one CTA holds a whole (batch, head) slice in shared memory and runs every step
-//           (scores, softmax, Delta, A^T V, Delta^{-1}, A W').  No workspace.
-//   split : the n tokens of a slice are cut into fixed 512-token chunks.  Kernel 1 gives
-//           each chunk's partial (Delta, A^T V); kernel 2 sums the partials of a slice in
-//           chunk order and divides by Delta; kernel 3 recomputes A tile by tile with the
-//           same code as kernel 1 and forms H = A W'.  The chunk count depends on n only,
-//           so the summation order - and the result - is fixed.
+// Two kernels, both one launch per call:
+//   simt_full_kernel   one CTA per (batch, head) slice with the whole slice in shared memory:
+//                      Q, V and U arrive by cp.async (16-byte copies), and every step runs
+//                      on chip (scores, softmax, Delta, A^T V, Delta^{-1}, A W').  No workspace.
+//   simt_chunk_kernel  slices too long for shared memory.  Work items are handed out by a
+//                      ticket in a fixed order: every P1 item (a 512-token chunk of a slice:
+//                      its partial Delta and A^T V), then every P2 item (64 tokens of a slice:
+//                      A recomputed with the same code, H = A W').  The last P1 chunk of a
+//                      slice to finish sums the slice's partials in chunk order and publishes
+//                      W' = Delta^{-1} A^T V; a P2 item waits for it (bounded).  A P2 item only
+//                      waits for P1 items that running CTAs already hold, so no grid size can
+//                      deadlock, and the sums do not depend on which CTA ran what.
+// Every contraction keeps one accumulator per output and adds its terms in ascending index
+// order (register tiles of outputs, 16-byte shared-memory operand loads), so results are
+// bit-identical from run to run.
 #include "common.cuh"
 
 #include <math.h>
 
 namespace anchor {
+
+// Device error word of the chunked kernel (bit 1: a wait for a slice's W' gave up).
+__device__ unsigned int g_simt_error;
+
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr uint64_t kWaitNs = 2000000000ull;  // a wait for another CTA's reduction gives up after 2 s
 
-// rows x d elements of a row-major global matrix into shared memory with row pitch `pitch`.
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer_now() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// 16-byte asynchronous copy global -> shared (cached in L2 only)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// rows x d elements of a row-major [rows][d] global matrix into shared memory with a row pitch
+// of `pitch` elements; every row is a whole number of 16-byte pieces (d * sizeof(T) >= 32)
 template <typename T>
-__device__ __forceinline__ void load_rows(const T *__restrict__ src, float *dst, int rows, int d,
-                                          int pitch) {
-    const int count = rows * d;
-    for (int e = threadIdx.x; e < count; e += blockDim.x) {
-        const int r = e / d;
-        dst[r * pitch + (e - r * d)] = to_f32(src[e]);
+__device__ __forceinline__ void stage_rows(T *dst, const T *__restrict__ src, int rows, int d, int pitch) {
+    const int per_row = d * (int)sizeof(T) / 16;
+    for (int c = threadIdx.x; c < rows * per_row; c += blockDim.x) {
+        const int r = c / per_row, k = c - r * per_row;
+        cp_async16(reinterpret_cast<char *>(dst + (size_t)r * pitch) + 16 * k,
+                   reinterpret_cast<const char *>(src + (size_t)r * d) + 16 * k);
     }
 }
 
-// As[r][j] = softmax_j(scale * Xs[r] . Us[j]) for r < rows.  Called by the whole CTA; the
-// caller synchronises before (Xs, Us ready) and after (As ready).
-__device__ __forceinline__ void scores_softmax(const float *Xs, const float *Us, float *As, int rows,
-                                               int m, int d, int dp, int mp, float scale) {
-    for (int p = threadIdx.x; p < rows * m; p += blockDim.x) {
-        const int r = p / m;
-        const int j = p - r * m;
-        const float *q = Xs + r * dp;
-        const float *u = Us + j * dp;
-        float s = 0.f;
-        for (int k = 0; k < d; ++k) s = __fmaf_rn(q[k], u[k], s);
-        As[r * mp + j] = __fmul_rn(scale, s);
+// four consecutive elements as floats (bf16 widens exactly)
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
+
+// eight outputs of one row to global memory: 16 bytes of bf16 or 32 bytes of fp32
+__device__ __forceinline__ void st8(float *dst, const float *v) {
+    reinterpret_cast<float4 *>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+__device__ __forceinline__ void st8(__nv_bfloat16 *dst, const float *v) {
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+}
+
+// As[r][j] = scale * sum_k Qs[r][k] Us[j][k] (k ascending), r < rows, j < m.  Each thread
+// takes 4 x 4 outputs: rows rt + a nrt and anchors ct + b nct (a, b < 4), so that lanes,
+// which take consecutive ct, read consecutive U rows (distinct banks) and share Q rows.
+template <typename T>
+__device__ __forceinline__ void scores(const T *Qs, const T *Us, int pitch, float *As, int ap, int rows, int m, int d,
+                                       float scale) {
+    const int nct = (m + 3) / 4, nrt = (rows + 3) / 4;
+    for (int t = threadIdx.x; t < nrt * nct; t += blockDim.x) {
+        const int rt = t / nct, ct = t - rt * nct;
+        const T *q[4], *u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[i] = Qs + (size_t)min(rt + i * nrt, rows - 1) * pitch;
+            u[i] = Us + (size_t)min(ct + i * nct, m - 1) * pitch;
+        }
+        float acc[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+        for (int k = 0; k < d; k += 4) {
+            float4 qa[4], ua[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                qa[i] = ld4(q[i] + k);
+                ua[i] = ld4(u[i] + k);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    float s = acc[a][b];
+                    s = __fmaf_rn(qa[a].x, ua[b].x, s);
+                    s = __fmaf_rn(qa[a].y, ua[b].y, s);
+                    s = __fmaf_rn(qa[a].z, ua[b].z, s);
+                    acc[a][b] = __fmaf_rn(qa[a].w, ua[b].w, s);
+                }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int r = rt + a * nrt, j = ct + b * nct;
+                if (r < rows && j < m) As[(size_t)r * ap + j] = __fmul_rn(scale, acc[a][b]);
+            }
     }
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int r = warp; r < rows; r += kWarps) {
-        float *a = As + r * mp;
+}
+
+// Row softmax of As in place, one thread per row: A_ij = exp(S_ij - max_j S_ij) / sum.
+__device__ __forceinline__ void softmax_rows(float *As, int ap, int rows, int m) {
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+        float *a = As + (size_t)r * ap;
         float mx = -INFINITY;
-        for (int j = lane; j < m; j += 32) mx = fmaxf(mx, a[j]);
-        mx = warp_max(mx);
+        for (int j = 0; j < m; ++j) mx = fmaxf(mx, a[j]);
         float z = 0.f;
-        for (int j = lane; j < m; j += 32) {
+        for (int j = 0; j < m; ++j) {
             const float e = expf(__fsub_rn(a[j], mx));
             a[j] = e;
             z = __fadd_rn(z, e);
         }
-        z = warp_sum(z);
-        for (int j = lane; j < m; j += 32) a[j] = __fdiv_rn(a[j], z);
+        for (int j = 0; j < m; ++j) a[j] = __fdiv_rn(a[j], z);
     }
 }
+
+// Wacc[j][k] += sum_r As[r][j] Vs[r][k] and Dacc[j] += sum_r As[r][j] (r ascending).  Each
+// thread takes 2 anchors x 4 columns; lanes of a warp take consecutive columns.
+template <typename T>
+__device__ __forceinline__ void accumulate(const float *As, int ap, const T *Vs, int pitch, float *Wacc, float *Dacc,
+                                           int rows, int m, int d) {
+    const int nct = d / 4, njt = (m + 1) / 2;
+    for (int t = threadIdx.x; t < njt * nct; t += blockDim.x) {
+        const int jt = t / nct, ct = t - jt * nct;
+        const int j0 = jt * 2, k0 = ct * 4;
+        const bool two = j0 + 1 < m;
+        float4 w0 = *reinterpret_cast<const float4 *>(Wacc + (size_t)j0 * d + k0);
+        float4 w1 = two ? *reinterpret_cast<const float4 *>(Wacc + (size_t)(j0 + 1) * d + k0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *a = As + j0;
+        const int j1 = two ? 1 : 0;
+        for (int r = 0; r < rows; ++r) {
+            const float a0 = a[(size_t)r * ap], a1 = a[(size_t)r * ap + j1];
+            const float4 v = ld4(Vs + (size_t)r * pitch + k0);
+            w0.x = __fmaf_rn(a0, v.x, w0.x);
+            w0.y = __fmaf_rn(a0, v.y, w0.y);
+            w0.z = __fmaf_rn(a0, v.z, w0.z);
+            w0.w = __fmaf_rn(a0, v.w, w0.w);
+            w1.x = __fmaf_rn(a1, v.x, w1.x);
+            w1.y = __fmaf_rn(a1, v.y, w1.y);
+            w1.z = __fmaf_rn(a1, v.z, w1.z);
+            w1.w = __fmaf_rn(a1, v.w, w1.w);
+        }
+        *reinterpret_cast<float4 *>(Wacc + (size_t)j0 * d + k0) = w0;
+        if (two) *reinterpret_cast<float4 *>(Wacc + (size_t)(j0 + 1) * d + k0) = w1;
+    }
+    for (int j = threadIdx.x; j < m; j += blockDim.x) {
+        float s = Dacc[j];
+        for (int r = 0; r < rows; ++r) s = __fadd_rn(s, As[(size_t)r * ap + j]);
+        Dacc[j] = s;
+    }
+}
+
+// W'[j][k] = W[j][k] / Delta_j in place (0 where Delta_j = 0: an anchor no token reaches)
+__device__ __forceinline__ void normalise(float *W, const float *Dl, int m, int d) {
+    for (int p = threadIdx.x; p < m * d; p += blockDim.x) {
+        const float dj = Dl[p / d];
+        W[p] = dj != 0.f ? __fdiv_rn(W[p], dj) : 0.f;
+    }
+}
+
+// H[r][k] = sum_j As[r][j] Ws[j][k] (j ascending) for r < rows, stored to the global rows at
+// Hg (row-major, d columns).  Each thread takes 2 rows x 8 columns (one 16-byte bf16 store,
+// or two fp32 ones, per row); lanes of a warp take consecutive columns.
+template <typename T>
+__device__ __forceinline__ void apply(const float *As, int ap, const float *Ws, T *__restrict__ Hg, int rows, int m, int d) {
+    const int nct = d / 8, nrt = (rows + 1) / 2;
+    for (int t = threadIdx.x; t < nrt * nct; t += blockDim.x) {
+        const int rt = t / nct, ct = t - rt * nct;
+        const int r0 = rt * 2, k0 = ct * 8;
+        const bool two = r0 + 1 < rows;
+        const float *a0 = As + (size_t)r0 * ap, *a1 = As + (size_t)(two ? r0 + 1 : r0) * ap;
+        float acc[2][8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[0][c] = acc[1][c] = 0.f;
+        for (int j = 0; j < m; ++j) {
+            const float x0 = a0[j], x1 = a1[j];
+            const float4 wa = *reinterpret_cast<const float4 *>(Ws + (size_t)j * d + k0);
+            const float4 wb = *reinterpret_cast<const float4 *>(Ws + (size_t)j * d + k0 + 4);
+            const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                acc[0][c] = __fmaf_rn(x0, w[c], acc[0][c]);
+                acc[1][c] = __fmaf_rn(x1, w[c], acc[1][c]);
+            }
+        }
+        st8(Hg + (size_t)r0 * d + k0, acc[0]);
+        if (two) st8(Hg + (size_t)(r0 + 1) * d + k0, acc[1]);
+    }
+}
+
+template <typename T> constexpr int pad_elems() { return 16 / (int)sizeof(T); }
 
 // ------------------------------------------------------------------ whole slice per CTA
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
-simt_slice_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__restrict__ V,
-                  T *__restrict__ H, int heads, int n, int m, int d, float scale) {
-    extern __shared__ float sm[];
-    const int dp = d + 1, mp = m + 1;
-    float *Us = sm;             // [m][dp]
-    float *Xs = Us + m * dp;    // [n][dp]  Q, then V
-    float *As = Xs + n * dp;    // [n][mp]
-    float *Ws = As + n * mp;    // [m][d]   W' = Delta^{-1} A^T V
-    float *Ds = Ws + m * d;     // [m]      Delta
+__global__ void __launch_bounds__(kThreads, 2)
+simt_full_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__restrict__ V, T *__restrict__ H,
+                 int heads, int n, int m, int d, float scale) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int pitch = d + pad_elems<T>();
+    const int ap = m + 1;
+    T *Qs = reinterpret_cast<T *>(smem);                    // [n][pitch]
+    T *Vs = Qs + (size_t)n * pitch;                         // [n][pitch]
+    T *Us = Vs + (size_t)n * pitch;                         // [m][pitch]
+    float *Ws = reinterpret_cast<float *>(Us + (size_t)m * pitch);  // [m][d]  A^T V, then W'
+    float *Ds = Ws + (size_t)m * d;                         // [m]     Delta
+    float *As = Ds + ((m + 3) & ~3);                        // [n][ap]
     const long long slice = blockIdx.x;
     const int h = (int)(slice % heads);
     const size_t off = (size_t)slice * n * d;
 
-    load_rows(U + (size_t)h * m * d, Us, m, d, dp);
-    load_rows(Q + off, Xs, n, d, dp);
+    stage_rows(Qs, Q + off, n, d, pitch);
+    stage_rows(Us, U + (size_t)h * m * d, m, d, pitch);
+    cp_async_commit();
+    stage_rows(Vs, V + off, n, d, pitch);  // lands while the scores are computed
+    cp_async_commit();
+    for (int p = threadIdx.x; p < m * d + m; p += blockDim.x) Ws[p] = 0.f;  // and Ds
+    cp_async_wait<1>();
     __syncthreads();
-    scores_softmax(Xs, Us, As, n, m, d, dp, mp, scale);
+    scores(Qs, Us, pitch, As, ap, n, m, d, scale);
     __syncthreads();
-    load_rows(V + off, Xs, n, d, dp);
-    for (int j = threadIdx.x; j < m; j += blockDim.x) {
-        float s = 0.f;
-        for (int i = 0; i < n; ++i) s = __fadd_rn(s, As[i * mp + j]);
-        Ds[j] = s;
-    }
+    softmax_rows(As, ap, n, m);
+    cp_async_wait<0>();
     __syncthreads();
-    for (int p = threadIdx.x; p < m * d; p += blockDim.x) {
-        const int j = p / d, k = p - j * d;
-        float s = 0.f;
-        for (int i = 0; i < n; ++i) s = __fmaf_rn(As[i * mp + j], Xs[i * dp + k], s);
-        Ws[p] = Ds[j] != 0.f ? __fdiv_rn(s, Ds[j]) : 0.f;
-    }
+    accumulate(As, ap, Vs, pitch, Ws, Ds, n, m, d);
     __syncthreads();
-    for (int p = threadIdx.x; p < n * d; p += blockDim.x) {
-        const int i = p / d, k = p - i * d;
-        float s = 0.f;
-        for (int j = 0; j < m; ++j) s = __fmaf_rn(As[i * mp + j], Ws[j * d + k], s);
-        H[off + p] = from_f32<T>(s);
-    }
+    normalise(Ws, Ds, m, d);
+    __syncthreads();
+    apply(As, ap, Ws, H + off, n, m, d);
 }
 
-// ------------------------------------------------------------------ split variant
-// Partial of chunk c of a slice: Delta_c[j] = sum_{i in c} A_ij and W_c[j][k] =
-// sum_{i in c} A_ij V_ik, written to part[(slice * splits + c) * (m*d + m)].
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-simt_partial_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__restrict__ V,
-                    float *__restrict__ part, int heads, int n, int m, int d, float scale,
-                    int splits) {
-    extern __shared__ float sm[];
-    const int dp = d + 1, mp = m + 1;
-    float *Us = sm;                     // [m][dp]
-    float *Xs = Us + m * dp;            // [kSimtTile][dp]
-    float *As = Xs + kSimtTile * dp;    // [kSimtTile][mp]
-    float *Wacc = As + kSimtTile * mp;  // [m][d]
-    float *Dacc = Wacc + m * d;         // [m]
-    const long long slice = blockIdx.x / splits;
-    const int c = (int)(blockIdx.x - slice * splits);
-    const int h = (int)(slice % heads);
-    const size_t off = (size_t)slice * n * d;
-    const int t_begin = c * kSimtChunk;
-    const int t_end = min(n, t_begin + kSimtChunk);
+// ------------------------------------------------------------------ chunked slices
+struct ChunkParams {
+    int heads, n, m, d;
+    float scale;
+    int slices, chunks, blocks;  // P1 chunks and P2 blocks per slice
+    int tile;                    // tokens per staged tile (64 unless the anchors need the room)
+    unsigned *ticket;            // next work item
+    unsigned *arrived;           // [slices] P1 chunks finished
+    unsigned *ready;             // [slices] W' published
+    float *part;                 // [slices][chunks][m * d + m]  A^T V and Delta partials
+    float *wprime;               // [slices][m * d]
+    uint64_t wait_ns;
+};
 
-    load_rows(U + (size_t)h * m * d, Us, m, d, dp);
-    for (int p = threadIdx.x; p < m * d + m; p += blockDim.x) Wacc[p] = 0.f;
-    for (int t0 = t_begin; t0 < t_end; t0 += kSimtTile) {
-        const int rows = min(kSimtTile, t_end - t0);
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2)
+simt_chunk_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__restrict__ V, T *__restrict__ H,
+                  const ChunkParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ unsigned s_item;
+    __shared__ int s_flag;
+    const int m = p.m, d = p.d, TR = p.tile;
+    const int pitch = d + pad_elems<T>();
+    const int ap = m + 1;
+    T *Us = reinterpret_cast<T *>(smem);                    // [m][pitch]
+    T *Qs = Us + (size_t)m * pitch;                         // [TR][pitch]
+    T *Vs = Qs + (size_t)TR * pitch;                        // [TR][pitch]
+    float *Wacc = reinterpret_cast<float *>(Vs + (size_t)TR * pitch);  // [m][d]  partial / W'
+    float *Dacc = Wacc + (size_t)m * d;                     // [m]
+    float *As = Dacc + ((m + 3) & ~3);                      // [TR][ap]
+    const unsigned n1 = (unsigned)(p.slices * p.chunks), n2 = (unsigned)(p.slices * p.blocks);
+    const size_t pstride = (size_t)m * d + m;
+
+    for (;;) {
+        __syncthreads();  // the previous item is done with shared memory and s_item
+        if (threadIdx.x == 0) s_item = atomicAdd(p.ticket, 1u);
         __syncthreads();
-        load_rows(Q + off + (size_t)t0 * d, Xs, rows, d, dp);
-        __syncthreads();
-        scores_softmax(Xs, Us, As, rows, m, d, dp, mp, scale);
-        __syncthreads();
-        load_rows(V + off + (size_t)t0 * d, Xs, rows, d, dp);
-        __syncthreads();
-        for (int j = threadIdx.x; j < m; j += blockDim.x) {
-            float s = Dacc[j];
-            for (int r = 0; r < rows; ++r) s = __fadd_rn(s, As[r * mp + j]);
-            Dacc[j] = s;
+        const unsigned item = s_item;
+        if (item >= n1 + n2) break;
+        if (item < n1) {
+            // ---------------------------------------------------------- P1: a chunk's partial
+            const int slice = (int)(item / p.chunks), c = (int)(item % p.chunks);
+            const int h = slice % p.heads;
+            const size_t off = (size_t)slice * p.n * d;
+            const int t_begin = c * kSimtChunk, t_end = min(p.n, t_begin + kSimtChunk);
+            stage_rows(Us, U + (size_t)h * m * d, m, d, pitch);
+            cp_async_commit();
+            for (int i = threadIdx.x; i < m * d + m; i += blockDim.x) Wacc[i] = 0.f;  // and Dacc
+            for (int t0 = t_begin; t0 < t_end; t0 += TR) {
+                const int rows = min(TR, t_end - t0);
+                __syncthreads();  // the last tile's Vs and As are read
+                stage_rows(Qs, Q + off + (size_t)t0 * d, rows, d, pitch);
+                stage_rows(Vs, V + off + (size_t)t0 * d, rows, d, pitch);
+                cp_async_commit();
+                cp_async_wait<0>();
+                __syncthreads();
+                scores(Qs, Us, pitch, As, ap, rows, m, d, p.scale);
+                __syncthreads();
+                softmax_rows(As, ap, rows, m);
+                __syncthreads();
+                accumulate(As, ap, Vs, pitch, Wacc, Dacc, rows, m, d);
+            }
+            __syncthreads();
+            float *dst = p.part + ((size_t)slice * p.chunks + c) * pstride;
+            for (int i = threadIdx.x; i < m * d + m; i += blockDim.x) dst[i] = Wacc[i];
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) s_flag = atomicAdd(p.arrived + slice, 1u) == (unsigned)(p.chunks - 1);
+            __syncthreads();
+            if (!s_flag) continue;
+            // the last chunk of the slice: sum every partial in chunk order, then publish W'
+            __threadfence();
+            const float *src = p.part + (size_t)slice * p.chunks * pstride;
+            for (int i = threadIdx.x; i < m * d + m; i += blockDim.x) {
+                float s = 0.f;
+                for (int cc = 0; cc < p.chunks; ++cc) s = __fadd_rn(s, __ldcg(src + cc * pstride + i));
+                Wacc[i] = s;
+            }
+            __syncthreads();
+            normalise(Wacc, Dacc, m, d);
+            __syncthreads();
+            float *wp = p.wprime + (size_t)slice * m * d;
+            for (int i = threadIdx.x; i < m * d; i += blockDim.x) wp[i] = Wacc[i];
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) atomicExch(p.ready + slice, 1u);
+        } else {
+            // ---------------------------------------------------------- P2: 64 tokens of H
+            const unsigned it2 = item - n1;
+            const int slice = (int)(it2 / p.blocks), blk = (int)(it2 % p.blocks);
+            const int h = slice % p.heads;
+            const size_t off = (size_t)slice * p.n * d;
+            if (threadIdx.x == 0) {
+                // every P1 item was handed out before this one, to CTAs that are running
+                const volatile unsigned *flag = p.ready + slice;
+                int ok = 1;
+                if (*flag == 0u) {
+                    const uint64_t t0 = globaltimer_now();
+                    while (*flag == 0u) {
+                        if (globaltimer_now() - t0 > p.wait_ns) {
+                            atomicOr(&g_simt_error, 2u);
+                            ok = 0;
+                            break;
+                        }
+                        __nanosleep(256);
+                    }
+                }
+                __threadfence();
+                s_flag = ok;
+            }
+            __syncthreads();
+            if (!s_flag) continue;  // H of this block stays unwritten; the error word says why
+            stage_rows(Us, U + (size_t)h * m * d, m, d, pitch);
+            const float *wp = p.wprime + (size_t)slice * m * d;
+            for (int i = threadIdx.x * 4; i < m * d; i += blockDim.x * 4)
+                cp_async16(Wacc + i, wp + i);
+            for (int t0 = blk * 64; t0 < min(p.n, blk * 64 + 64); t0 += TR) {
+                const int rows = min(TR, p.n - t0);
+                __syncthreads();
+                stage_rows(Qs, Q + off + (size_t)t0 * d, rows, d, pitch);
+                cp_async_commit();
+                cp_async_wait<0>();
+                __syncthreads();
+                scores(Qs, Us, pitch, As, ap, rows, m, d, p.scale);
+                __syncthreads();
+                softmax_rows(As, ap, rows, m);
+                __syncthreads();
+                apply(As, ap, Wacc, H + off + (size_t)t0 * d, rows, m, d);
+            }
         }
-        for (int p = threadIdx.x; p < m * d; p += blockDim.x) {
-            const int j = p / d, k = p - j * d;
-            float s = Wacc[p];
-            for (int r = 0; r < rows; ++r) s = __fmaf_rn(As[r * mp + j], Xs[r * dp + k], s);
-            Wacc[p] = s;
-        }
-    }
-    __syncthreads();
-    float *dst = part + ((size_t)slice * splits + c) * (size_t)(m * d + m);
-    for (int p = threadIdx.x; p < m * d + m; p += blockDim.x) dst[p] = Wacc[p];
-}
-
-// W'[slice] = (sum over chunks, in chunk order, of W_c) / (sum of Delta_c); 0 where Delta = 0.
-__global__ void __launch_bounds__(kThreads)
-simt_reduce_kernel(const float *__restrict__ part, float *__restrict__ Wp, int m, int d, int splits) {
-    extern __shared__ float Ds[];  // [m]
-    const long long slice = blockIdx.x;
-    const size_t stride = (size_t)(m * d + m);
-    const float *base = part + (size_t)slice * splits * stride;
-    for (int j = threadIdx.x; j < m; j += blockDim.x) {
-        float s = 0.f;
-        for (int c = 0; c < splits; ++c) s = __fadd_rn(s, base[c * stride + m * d + j]);
-        Ds[j] = s;
-    }
-    __syncthreads();
-    for (int p = threadIdx.x; p < m * d; p += blockDim.x) {
-        float s = 0.f;
-        for (int c = 0; c < splits; ++c) s = __fadd_rn(s, base[c * stride + p]);
-        const float dj = Ds[p / d];
-        Wp[(size_t)slice * m * d + p] = dj != 0.f ? __fdiv_rn(s, dj) : 0.f;
     }
 }
 
-// H rows of one kSimtTile-token tile: recompute A (same code as the partial kernel), then
-// H = A W'.
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-simt_apply_kernel(const T *__restrict__ Q, const T *__restrict__ U, const float *__restrict__ Wp,
-                  T *__restrict__ H, int heads, int n, int m, int d, float scale) {
-    extern __shared__ float sm[];
-    const int dp = d + 1, mp = m + 1;
-    float *Us = sm;                   // [m][dp]
-    float *Xs = Us + m * dp;          // [kSimtTile][dp]
-    float *As = Xs + kSimtTile * dp;  // [kSimtTile][mp]
-    float *Ws = As + kSimtTile * mp;  // [m][d]
-    const int tiles = (n + kSimtTile - 1) / kSimtTile;
-    const long long slice = blockIdx.x / tiles;
-    const int h = (int)(slice % heads);
-    const size_t off = (size_t)slice * n * d;
-    const int t0 = (int)(blockIdx.x - slice * tiles) * kSimtTile;
-    const int rows = min(kSimtTile, n - t0);
+template <typename T> size_t full_smem(int n, int m, int d) {
+    const size_t pitch = d + pad_elems<T>();
+    return sizeof(T) * (2 * (size_t)n + m) * pitch + 4 * ((size_t)m * d + ((m + 3) & ~3) + (size_t)n * (m + 1));
+}
 
-    load_rows(U + (size_t)h * m * d, Us, m, d, dp);
-    load_rows(Q + off + (size_t)t0 * d, Xs, rows, d, dp);
-    const float *wsrc = Wp + (size_t)slice * m * d;
-    for (int p = threadIdx.x; p < m * d; p += blockDim.x) Ws[p] = wsrc[p];
-    __syncthreads();
-    scores_softmax(Xs, Us, As, rows, m, d, dp, mp, scale);
-    __syncthreads();
-    T *out = H + off + (size_t)t0 * d;
-    for (int p = threadIdx.x; p < rows * d; p += blockDim.x) {
-        const int r = p / d, k = p - r * d;
-        float s = 0.f;
-        for (int j = 0; j < m; ++j) s = __fmaf_rn(As[r * mp + j], Ws[j * d + k], s);
-        out[p] = from_f32<T>(s);
-    }
+template <typename T> size_t chunk_smem(int m, int d, int tile) {
+    const size_t pitch = d + pad_elems<T>();
+    return sizeof(T) * ((size_t)m + 2 * tile) * pitch + 4 * ((size_t)m * d + ((m + 3) & ~3) + (size_t)tile * (m + 1));
+}
+
+template <typename T> int chunk_tile(int m, int d) {
+    for (int tile = 64; tile >= 8; tile /= 2)
+        if (chunk_smem<T>(m, d, tile) <= kSimtMaxSmem) return tile;
+    return 0;
 }
 
 template <typename T>
-cudaError_t slice_launch(const Problem &p, cudaStream_t stream) {
-    const size_t smem = simt_slice_smem_bytes(p.n, p.m, p.d);
-    cudaError_t e = cudaFuncSetAttribute(simt_slice_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+cudaError_t full_launch(const Problem &p, cudaStream_t stream) {
+    const size_t smem = full_smem<T>(p.n, p.m, p.d);
+    cudaError_t e = cudaFuncSetAttribute(simt_full_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    simt_slice_kernel<T><<<(unsigned)p.slices(), kThreads, smem, stream>>>(
+    simt_full_kernel<T><<<(unsigned)p.slices(), kThreads, smem, stream>>>(
         (const T *)p.Q, (const T *)p.U, (const T *)p.V, (T *)p.H, p.heads, p.n, p.m, p.d, p.scale);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t split_launch(const Problem &p, int splits, float *ws, cudaStream_t stream) {
-    const size_t smem = simt_split_smem_bytes(p.m, p.d);
-    cudaError_t e = cudaFuncSetAttribute(simt_partial_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+cudaError_t chunk_launch(const Problem &p, void *ws, cudaStream_t stream) {
+    const int tile = chunk_tile<T>(p.m, p.d);
+    if (tile == 0) return cudaErrorInvalidValue;
+    const size_t smem = chunk_smem<T>(p.m, p.d, tile);
+    auto kern = simt_chunk_kernel<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(simt_apply_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    float *part = ws;
-    float *Wp = ws + (size_t)p.slices() * splits * (size_t)(p.m * p.d + p.m);
-    simt_partial_kernel<T><<<(unsigned)(p.slices() * splits), kThreads, smem, stream>>>(
-        (const T *)p.Q, (const T *)p.U, (const T *)p.V, part, p.heads, p.n, p.m, p.d, p.scale, splits);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    simt_reduce_kernel<<<(unsigned)p.slices(), kThreads, sizeof(float) * p.m, stream>>>(part, Wp, p.m, p.d,
-                                                                                       splits);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const unsigned tiles = (unsigned)((p.n + kSimtTile - 1) / kSimtTile);
-    simt_apply_kernel<T><<<(unsigned)(p.slices() * tiles), kThreads, smem, stream>>>(
-        (const T *)p.Q, (const T *)p.U, Wp, (T *)p.H, p.heads, p.n, p.m, p.d, p.scale);
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem)) != cudaSuccess) return e;
+    ChunkParams cp;
+    cp.heads = p.heads;
+    cp.n = p.n;
+    cp.m = p.m;
+    cp.d = p.d;
+    cp.scale = p.scale;
+    cp.slices = (int)p.slices();
+    cp.chunks = (p.n + kSimtChunk - 1) / kSimtChunk;
+    cp.blocks = (p.n + 63) / 64;
+    cp.tile = tile;
+    cp.wait_ns = kWaitNs;
+    const SimtLayout L = simt_chunk_layout(p);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    cp.ticket = reinterpret_cast<unsigned *>(w);
+    cp.arrived = cp.ticket + 32;
+    cp.ready = cp.arrived + cp.slices;
+    cp.part = reinterpret_cast<float *>(w + L.part_offset);
+    cp.wprime = reinterpret_cast<float *>(w + L.wprime_offset);
+    const long long items = (long long)cp.slices * (cp.chunks + cp.blocks);
+    const int grid = (int)std::min<long long>((long long)sms * std::max(per_sm, 1), items);
+    if ((e = cudaMemsetAsync(ws, 0, L.header_bytes, stream)) != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, stream>>>((const T *)p.Q, (const T *)p.U, (const T *)p.V, (T *)p.H, cp);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t simt_slice_smem_bytes(int n, int m, int d) {
-    const size_t dp = d + 1, mp = m + 1;
-    return sizeof(float) * ((size_t)m * dp + (size_t)n * dp + (size_t)n * mp + (size_t)m * d + m);
+bool simt_full_fits(const Problem &p) {
+    return (p.f32 ? full_smem<float>(p.n, p.m, p.d) : full_smem<__nv_bfloat16>(p.n, p.m, p.d)) <= kSimtMaxSmem;
 }
 
-size_t simt_split_smem_bytes(int m, int d) {
-    const size_t dp = d + 1, mp = m + 1;
-    // partial: Us + Xs + As + Wacc + Dacc; apply: Us + Xs + As + Ws (smaller)
-    return sizeof(float) * ((size_t)m * dp + kSimtTile * dp + kSimtTile * mp + (size_t)m * d + m);
+bool simt_chunk_fits(const Problem &p) {
+    return (p.f32 ? chunk_tile<float>(p.m, p.d) : chunk_tile<__nv_bfloat16>(p.m, p.d)) > 0;
 }
 
-size_t simt_split_workspace_bytes(const Problem &p, int splits) {
-    const size_t per = (size_t)p.m * p.d + p.m;
-    return sizeof(float) * ((size_t)p.slices() * splits * per + (size_t)p.slices() * p.m * p.d);
+SimtLayout simt_chunk_layout(const Problem &p) {
+    SimtLayout L;
+    const size_t S = (size_t)p.slices();
+    const size_t chunks = (p.n + kSimtChunk - 1) / kSimtChunk;
+    L.header_bytes = ((32 + 2 * S) * 4 + 255) / 256 * 256;
+    L.part_offset = L.header_bytes;
+    // W' is read with 16-byte copies: its region starts on a 256-byte boundary (the partials
+    // before it are m d + m floats per chunk, not a multiple of 16 bytes for odd m)
+    L.wprime_offset = (L.part_offset + 4 * S * chunks * ((size_t)p.m * p.d + p.m) + 255) / 256 * 256;
+    L.total_bytes = L.wprime_offset + 4 * S * (size_t)p.m * p.d;
+    return L;
 }
 
-cudaError_t launch_simt_slice(const Problem &p, cudaStream_t stream) {
-    return p.f32 ? slice_launch<float>(p, stream) : slice_launch<__nv_bfloat16>(p, stream);
+cudaError_t launch_simt_full(const Problem &p, cudaStream_t stream) {
+    return p.f32 ? full_launch<float>(p, stream) : full_launch<__nv_bfloat16>(p, stream);
 }
 
-cudaError_t launch_simt_split(const Problem &p, int splits, float *workspace, cudaStream_t stream) {
-    return p.f32 ? split_launch<float>(p, splits, workspace, stream)
-                 : split_launch<__nv_bfloat16>(p, splits, workspace, stream);
+cudaError_t launch_simt_chunk(const Problem &p, void *workspace, cudaStream_t stream) {
+    return p.f32 ? chunk_launch<float>(p, workspace, stream) : chunk_launch<__nv_bfloat16>(p, workspace, stream);
+}
+
+cudaError_t simt_read_and_clear_error(unsigned *out) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_simt_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_simt_error, &zero, sizeof(unsigned));
 }
 
 }  // namespace anchor

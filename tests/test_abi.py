@@ -78,6 +78,11 @@ def test_plans(pkg):
     assert p["variant"] == "simt_slice" and p["kernels_per_call"] == 1 and p["workspace_bytes"] == 0
     p = pkg.query_plan("bf16", 1, 2, 1100, 20, 64)
     assert p["variant"] == "simt_split" and p["splits"] == 3 and p["workspace_bytes"] > 0
+    assert p["kernels_per_call"] == 1
+    # the largest anchor count per head dimension still fits the chunked kernel's tiles
+    assert pkg.query_plan("f32", 2, 2, 100000, 1024, 16)["variant"] == "simt_split"
+    assert pkg.query_plan("f32", 2, 2, 20000, 512, 32)["variant"] == "simt_split"
+    assert pkg.query_plan("bf16", 64, 6, 197, 30, 64)["variant"] == "simt_slice"
     assert pkg.query_plan("bf16", 0, 2, 100, 20, 64)["variant"] == "empty"
     # tensor-core variant: d in {64, 128}, 32 <= m <= 128, bf16 only
     # 33 tiles of 128 tokens in chunks of at most 16: 3 chunks x 96 slices is at least 1.5
