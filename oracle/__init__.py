@@ -1,4 +1,5 @@
-"""CPU oracle for the anchor-attention forward H = A Delta^{-1} A^T V (AnchorFormer).
+"""CPU oracle for the anchor-attention forward H = A Delta^{-1} A^T V (AnchorFormer) and its
+backward (the gradients with respect to Q, U and V of a loss with upstream gradient dH).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` are the only callers.  The arithmetic lives in ``anchor_oracle.c`` (plain C,
@@ -43,7 +44,10 @@ class Oracle:
         lib.oracle_anchor_slice.argtypes = [D, D, D, L, L, L, ctypes.c_double, D, D, D, D, D]
         lib.oracle_anchor_slice_rows.argtypes = [D, D, D, L, L, L, ctypes.c_double,
                                                  ctypes.POINTER(ctypes.c_long), L, D]
-        for f in (lib.oracle_anchor_forward, lib.oracle_anchor_slice, lib.oracle_anchor_slice_rows):
+        lib.oracle_anchor_backward.argtypes = [D, D, D, D, D, D, D, L, L, L, L, L, ctypes.c_double]
+        lib.oracle_anchor_slice_backward.argtypes = [D, D, D, D, L, L, L, ctypes.c_double, D, D, D]
+        for f in (lib.oracle_anchor_forward, lib.oracle_anchor_slice, lib.oracle_anchor_slice_rows,
+                  lib.oracle_anchor_backward, lib.oracle_anchor_slice_backward):
             f.restype = ctypes.c_int
         self._lib = lib
 
@@ -70,6 +74,27 @@ class Oracle:
                                              _dp(out["A"]), _dp(out["delta"]), _dp(out["W"]),
                                              _dp(out["Wp"]), _dp(out["H"])))
         return out
+
+    def backward(self, Q, U, V, dH, scale: float) -> tuple:
+        """(dQ, dU, dV) for Q, V, dH [B][heads][n][d] and U [heads][m][d]; dU sums the batch."""
+        Q, U, V, dH = _f64(Q), _f64(U), _f64(V), _f64(dH)
+        B, heads, n, d = Q.shape
+        m = U.shape[1]
+        assert U.shape == (heads, m, d) and V.shape == Q.shape and dH.shape == Q.shape
+        dQ, dU, dV = np.empty_like(Q), np.empty_like(U), np.empty_like(V)
+        _check(self._lib.oracle_anchor_backward(_dp(Q), _dp(U), _dp(V), _dp(dH), _dp(dQ), _dp(dU), _dp(dV),
+                                                B, heads, n, m, d, float(scale)))
+        return dQ, dU, dV
+
+    def slice_backward(self, Q, U, V, dH, scale: float) -> tuple:
+        """(dQ, dU, dV) of one slice (Q, V, dH [n][d], U [m][d]); dU is this slice's share."""
+        Q, U, V, dH = _f64(Q), _f64(U), _f64(V), _f64(dH)
+        n, d = Q.shape
+        m = U.shape[0]
+        dQ, dV, dU = np.empty((n, d)), np.empty((n, d)), np.zeros((m, d))
+        _check(self._lib.oracle_anchor_slice_backward(_dp(Q), _dp(U), _dp(V), _dp(dH), n, m, d, float(scale),
+                                                      _dp(dQ), _dp(dU), _dp(dV)))
+        return dQ, dU, dV
 
     def slice_rows(self, Q, U, V, scale: float, rows) -> np.ndarray:
         """H rows ``rows`` of one slice (Q, V [n][d], U [m][d])."""
@@ -117,6 +142,14 @@ def slice_forward(Q, U, V, scale: float) -> dict:
 
 def slice_rows(Q, U, V, scale: float, rows) -> np.ndarray:
     return _default().slice_rows(Q, U, V, scale, rows)
+
+
+def backward(Q, U, V, dH, scale: float) -> tuple:
+    return _default().backward(Q, U, V, dH, scale)
+
+
+def slice_backward(Q, U, V, dH, scale: float) -> tuple:
+    return _default().slice_backward(Q, U, V, dH, scale)
 
 
 def compile_variant(source_text: str, out_path: str) -> Oracle:

@@ -18,6 +18,16 @@
  * sum runs in ascending index order.  The softmax subtracts the row maximum first; that is
  * the same function mathematically and keeps exp() in range.
  *
+ * Backward (the anchors are learned by gradient descent: "core_discovery"; the arXiv abstract's
+ * anchors as "neurons in a neural layer"): for an upstream gradient dH of H, the gradients of
+ * the loss with respect to Q, U and V follow by the chain rule through the same steps, taken
+ * in reverse:
+ *   dW' = A^T dH,  dW = Delta^{-1} dW',  dDelta_j = -sum_k dW'[j][k] W'[j][k] / Delta_j,
+ *   G = dH W'^T + V dW^T + 1 dDelta^T   (dL/dA through H, through W and through Delta),
+ *   dS[i][j] = A[i][j] (G[i][j] - sum_l A[i][l] G[i][l])   (the softmax's Jacobian),
+ *   dQ = scale dS U,  dV = A dW,  dU = scale dS^T Q, summed over the batch entries that share
+ *   the head's anchors.
+ *
  * Readings where the pages are silent:
  *   - Delta_j == 0 (every A[i][j] underflowed): W'_j := 0.  Its contribution A[i][j] W'_j
  *     vanishes in the limit because every A[i][j] is 0.
@@ -135,6 +145,98 @@ int oracle_anchor_slice_rows(const double *Q, const double *U, const double *V, 
     anchor_summaries(A, V, n, m, d, delta, W, Wp);
     for (long r = 0; r < nrows; ++r) apply_row(A + rows[r] * m, Wp, m, d, Hrows + r * d);
     free(A); free(delta); free(W); free(Wp);
+    return 0;
+}
+
+/*
+ * Backward of one slice: dQ, dV [n][d] are written, dU [m][d] is ADDED to (the caller sums the
+ * batch entries of a head).  dH: [n][d].  An anchor with Delta_j == 0 (the reading above: its
+ * W'_j is 0) gets dW_j = 0 and dDelta_j = 0.
+ */
+int oracle_anchor_slice_backward(const double *Q, const double *U, const double *V, const double *dH,
+                                 long n, long m, long d, double scale, double *dQ, double *dU, double *dV)
+{
+    if (bad_shape(n, m, d)) return 1;
+    double *A = malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)m);
+    double *delta = malloc(sizeof(double) * (size_t)m);
+    double *W = malloc(sizeof(double) * (size_t)m * (size_t)d);
+    double *Wp = malloc(sizeof(double) * (size_t)m * (size_t)d);
+    double *dWp = malloc(sizeof(double) * (size_t)m * (size_t)d);
+    double *dW = malloc(sizeof(double) * (size_t)m * (size_t)d);
+    double *ddelta = malloc(sizeof(double) * (size_t)m);
+    double *G = malloc(sizeof(double) * (size_t)m);
+    if (!A || !delta || !W || !Wp || !dWp || !dW || !ddelta || !G) {
+        free(A); free(delta); free(W); free(Wp); free(dWp); free(dW); free(ddelta); free(G);
+        return 2;
+    }
+    /* the forward's intermediates */
+    token_anchor_matrix(Q, U, n, m, d, scale, A);
+    anchor_summaries(A, V, n, m, d, delta, W, Wp);
+    /* dW' = A^T dH */
+    for (long j = 0; j < m; ++j)
+        for (long k = 0; k < d; ++k) {
+            double s = 0.0;
+            for (long i = 0; i < n; ++i) s += A[i * m + j] * dH[i * d + k];
+            dWp[j * d + k] = s;
+        }
+    /* W' = W / Delta: dW = dW' / Delta and dDelta_j = -sum_k dW'_jk W_jk / Delta_j^2 */
+    for (long j = 0; j < m; ++j) {
+        double s = 0.0;
+        for (long k = 0; k < d; ++k) {
+            dW[j * d + k] = delta[j] != 0.0 ? dWp[j * d + k] / delta[j] : 0.0;
+            s += dWp[j * d + k] * W[j * d + k];
+        }
+        ddelta[j] = delta[j] != 0.0 ? -s / (delta[j] * delta[j]) : 0.0;
+    }
+    for (long i = 0; i < n; ++i) {
+        const double *a = A + i * m;
+        /* G_j = dL/dA_ij: through H = A W', through W = A^T V and through Delta = A^T 1 */
+        for (long j = 0; j < m; ++j) {
+            double g = ddelta[j];
+            for (long k = 0; k < d; ++k) g += dH[i * d + k] * Wp[j * d + k] + V[i * d + k] * dW[j * d + k];
+            G[j] = g;
+        }
+        /* softmax: dS_ij = A_ij (G_j - sum_l A_il G_l) */
+        double ag = 0.0;
+        for (long j = 0; j < m; ++j) ag += a[j] * G[j];
+        for (long j = 0; j < m; ++j) G[j] = a[j] * (G[j] - ag);  /* G now holds dS_i */
+        /* S = scale Q U^T: dQ_i = scale sum_j dS_ij U_j; dU_j += scale dS_ij Q_i */
+        for (long k = 0; k < d; ++k) {
+            double s = 0.0;
+            for (long j = 0; j < m; ++j) s += G[j] * U[j * d + k];
+            dQ[i * d + k] = scale * s;
+        }
+        for (long j = 0; j < m; ++j)
+            for (long k = 0; k < d; ++k) dU[j * d + k] += scale * G[j] * Q[i * d + k];
+        /* W = A^T V: dV_i = sum_j A_ij dW_j */
+        for (long k = 0; k < d; ++k) {
+            double s = 0.0;
+            for (long j = 0; j < m; ++j) s += a[j] * dW[j * d + k];
+            dV[i * d + k] = s;
+        }
+    }
+    free(A); free(delta); free(W); free(Wp); free(dWp); free(dW); free(ddelta); free(G);
+    return 0;
+}
+
+/*
+ * Whole backward.  Q, V, dH, dQ, dV: [B][heads][n][d]; U, dU: [heads][m][d] (dU is the sum
+ * over the batch entries of each head; it is overwritten).
+ */
+int oracle_anchor_backward(const double *Q, const double *U, const double *V, const double *dH, double *dQ,
+                           double *dU, double *dV, long B, long heads, long n, long m, long d, double scale)
+{
+    if (B < 0 || heads < 0 || bad_shape(n, m, d)) return 1;
+    for (long i = 0; i < heads * m * d; ++i) dU[i] = 0.0;
+    for (long b = 0; b < B; ++b) {
+        for (long h = 0; h < heads; ++h) {
+            size_t off = ((size_t)b * (size_t)heads + (size_t)h) * (size_t)n * (size_t)d;
+            size_t uoff = (size_t)h * (size_t)m * (size_t)d;
+            int rc = oracle_anchor_slice_backward(Q + off, U + uoff, V + off, dH + off, n, m, d, scale,
+                                                  dQ + off, dU + uoff, dV + off);
+            if (rc) return rc;
+        }
+    }
     return 0;
 }
 

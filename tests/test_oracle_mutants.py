@@ -1,10 +1,12 @@
 """Plants one mistake at a time in a copy of the oracle (on the CPU) and checks that the
-pins in test_oracle_pins.py reject every such copy."""
+pins reject every such copy: test_oracle_pins.py for the forward, and
+test_oracle_backward_pins.py for the backward."""
 import inspect
 
 import pytest
 
 import oracle
+import tests.test_oracle_backward_pins as bpins
 import tests.test_oracle_pins as pins
 
 # (name, text in anchor_oracle.c, replacement): each a plausible slip.
@@ -21,6 +23,43 @@ MUTANTS = [
     ("anchors indexed by batch", "U + (size_t)h * (size_t)m * (size_t)d", "U + (size_t)((b + h) % heads) * (size_t)m * (size_t)d"),
     ("query/anchor dims crossed", "s += Q[i * d + k] * U[j * d + k];", "s += Q[i * d + k] * U[k % m * d + j % d];"),
 ]
+
+
+# slips in the backward
+BACKWARD_MUTANTS = [
+    ("dDelta term dropped", "double g = ddelta[j];", "double g = 0.0;"),
+    ("softmax Jacobian with the wrong sign", "G[j] = a[j] * (G[j] - ag);", "G[j] = a[j] * (G[j] + ag);"),
+    ("softmax Jacobian without the row term", "G[j] = a[j] * (G[j] - ag);", "G[j] = a[j] * G[j];"),
+    ("scale dropped from dQ", "dQ[i * d + k] = scale * s;", "dQ[i * d + k] = s;"),
+    ("dU from V instead of Q", "dU[j * d + k] += scale * G[j] * Q[i * d + k];", "dU[j * d + k] += scale * G[j] * V[i * d + k];"),
+    ("Delta^-1 dropped from dW", "dW[j * d + k] = delta[j] != 0.0 ? dWp[j * d + k] / delta[j] : 0.0;",
+     "dW[j * d + k] = dWp[j * d + k];"),
+    ("dDelta with the wrong sign", "ddelta[j] = delta[j] != 0.0 ? -s / (delta[j] * delta[j]) : 0.0;",
+     "ddelta[j] = delta[j] != 0.0 ? s / (delta[j] * delta[j]) : 0.0;"),
+    ("path through W dropped", "g += dH[i * d + k] * Wp[j * d + k] + V[i * d + k] * dW[j * d + k];",
+     "g += dH[i * d + k] * Wp[j * d + k];"),
+    ("dV from dW' instead of dW", "for (long j = 0; j < m; ++j) s += a[j] * dW[j * d + k];",
+     "for (long j = 0; j < m; ++j) s += a[j] * dWp[j * d + k];"),
+    ("dU not summed over the batch", "for (long i = 0; i < heads * m * d; ++i) dU[i] = 0.0;\n    for (long b = 0; b < B; ++b) {",
+     "for (long b = 0; b < B; ++b) {\n        for (long i = 0; i < heads * m * d; ++i) dU[i] = 0.0;"),
+]
+
+
+def _run_bpins(mut) -> list:
+    failed = []
+    for name, fn in inspect.getmembers(bpins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        params = inspect.signature(fn).parameters
+        cases = [{}]
+        if "shape" in params:  # the finite-difference pin on its smallest shape keeps this quick
+            cases = [{"shape": (1, 1, 5, 3, 4), "scale": 0.5, "qscale": 1.0}]
+        for kw in cases:
+            try:
+                fn(mut, **kw)
+            except (AssertionError, ValueError, FloatingPointError, ZeroDivisionError):
+                failed.append(name)
+    return failed
 
 
 def _run_pins(mut) -> list:
@@ -46,3 +85,12 @@ def test_pins_reject_planted_mistake(tmp_path, name, old, new):
     assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
     mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
     assert _run_pins(mut), f"no pin rejects the planted mistake '{name}'"
+
+
+@pytest.mark.parametrize("name,old,new", BACKWARD_MUTANTS, ids=[m[0] for m in BACKWARD_MUTANTS])
+def test_backward_pins_reject_planted_mistake(tmp_path, name, old, new):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
+    mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    failed = _run_bpins(mut)
+    assert failed, f"no backward pin rejects the planted mistake '{name}'"
