@@ -83,6 +83,38 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, con
                                              float scale, void *stream);
 
 /*
+ * Backward of anchor_attn_forward, bf16 in and out, fp32 arithmetic on CUDA cores.  The
+ * anchors are fitted by gradient descent (pith.science verdict on arXiv 2505.16463,
+ * "core_discovery"; the arXiv abstract's anchors as "neurons in a neural layer"), so a layer
+ * built on the forward needs the gradients of a loss L with respect to Q, U and V given
+ * dH = dL/dH:
+ *   dW' = A^T dH,  dW = Delta^{-1} dW',  dDelta_j = -sum_k dW'[j][k] W'[j][k] / Delta_j,
+ *   G = dH W'^T + V dW^T + 1 dDelta^T,  dS = A o (G - rowsum(A o G)),
+ *   dQ = scale dS U,  dV = A dW,  dU = scale sum over the batch of dS^T Q.
+ * A is recomputed from Q and U (nothing is kept from the forward).
+ *
+ * Inputs Q, V, dH: [B][heads][n][d]; U: [heads][m][d].  Outputs dQ, dV: [B][heads][n][d];
+ * dU: [heads][m][d] (the sum over the batch entries, which share the anchors).  Device
+ * pointers, 16-byte aligned, caller-owned; no output may overlap an input or another output
+ * (ANCHOR_ATTN_ERR_ALIAS).  B or n = 0: dU is set to zero (dQ, dV are empty); heads = 0:
+ * nothing to do.  Shapes as for the forward; anchor counts whose fp32 summaries (2 m d
+ * floats) and tiles do not fit one CTA's shared memory return ANCHOR_ATTN_ERR_UNSUPPORTED
+ * (for fp32: d = 16 with m > about 900, d = 32 with m > about 480).  One workspace from
+ * cudaMallocAsync on `stream` per call, released on the same stream; two kernel launches.
+ * Results are bit-identical from run to run; a bounded wait that gives up is reported by
+ * anchor_attn_device_error (bit 1).
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_backward(const void *Q, const void *U, const void *V,
+                                                          const void *dH, void *dQ, void *dU, void *dV, int B,
+                                                          int heads, int n, int m, int d, float scale, void *stream);
+
+/* fp32 backward: float in, float out, same layout, shapes and errors as anchor_attn_backward. */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_backward_f32(const float *Q, const float *U, const float *V,
+                                                              const float *dH, float *dQ, float *dU, float *dV,
+                                                              int B, int heads, int n, int m, int d, float scale,
+                                                              void *stream);
+
+/*
  * Allocation-free variant of anchor_attn_forward (bf16 in and out, same layout, shapes and
  * errors).  The paper has no counterpart to this call: it exists for callers that may not
  * allocate device memory while they run - e.g. a plugin's enqueue step inside an inference

@@ -16,7 +16,7 @@ __all__ = [
     "LIB_PATH", "load", "forward", "anchor_attn_forward", "anchor_attn_forward_f32",
     "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "anchor_attn_forward_static_scratch_ptr",
     "static_scratch_bytes", "device_error", "query_plan", "status_string", "anchor_attn_test_forward_ptr",
-    "AnchorAttnError", "STATUS", "VARIANTS",
+    "AnchorAttnError", "STATUS", "VARIANTS", "backward", "anchor_attn_backward_ptr", "anchor_attn_backward_f32_ptr",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libanchor_attn.so")
@@ -57,6 +57,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         for name in ("anchor_attn_forward", "anchor_attn_forward_f32", "anchor_attn_forward_static_scratch"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
+            fn.restype = ctypes.c_int
+        for name in ("anchor_attn_backward", "anchor_attn_backward_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
             fn.restype = ctypes.c_int
         lib.anchor_attn_test_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.c_ulonglong, i, vp]
         lib.anchor_attn_test_forward.restype = ctypes.c_int
@@ -106,6 +110,18 @@ def anchor_attn_test_forward_ptr(Q: int, U: int, V: int, H: int, B: int, heads: 
     """Raw call of the failure-detection test entry (tests only); returns the status code."""
     return load().anchor_attn_test_forward(Q, U, V, H, B, heads, n, m, d, float(scale), int(hold_slice),
                                            int(wait_ns), 1 if force_recompute else 0, stream)
+
+
+def anchor_attn_backward_ptr(Q: int, U: int, V: int, dH: int, dQ: int, dU: int, dV: int, B: int, heads: int,
+                             n: int, m: int, d: int, scale: float, stream: int = 0) -> int:
+    """Raw C-ABI call of the bf16 backward (device pointers as integers); returns the status."""
+    return load().anchor_attn_backward(Q, U, V, dH, dQ, dU, dV, B, heads, n, m, d, float(scale), stream)
+
+
+def anchor_attn_backward_f32_ptr(Q: int, U: int, V: int, dH: int, dQ: int, dU: int, dV: int, B: int, heads: int,
+                                 n: int, m: int, d: int, scale: float, stream: int = 0) -> int:
+    """Raw C-ABI call of the fp32 backward (device pointers as integers); returns the status."""
+    return load().anchor_attn_backward_f32(Q, U, V, dH, dQ, dU, dV, B, heads, n, m, d, float(scale), stream)
 
 
 def static_scratch_bytes() -> int:
@@ -190,3 +206,28 @@ def anchor_attn_forward_f32(Q, U, V, H=None, scale=None, stream=None):
     if Q.dtype != torch.float32:
         raise TypeError("anchor_attn_forward_f32 takes float32 tensors")
     return forward(Q, U, V, H, scale, stream)
+
+
+def backward(Q, U, V, dH, scale: float | None = None, stream=None):
+    """(dQ, dU, dV) for torch CUDA tensors (bf16 or fp32): the gradients of a loss with
+    upstream gradient dH = dL/dH of H = forward(Q, U, V).  dU sums the batch entries (they
+    share the anchors).  scale defaults to 1/sqrt(d).  Asynchronous on ``stream`` or the
+    current stream."""
+    import torch
+    _check_tensors(Q, U, V, dH, Q.dtype)
+    B, heads, n, d = Q.shape
+    m = U.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dQ, dU, dV = torch.empty_like(Q), torch.empty_like(U), torch.empty_like(V)
+    s = stream if stream is not None else torch.cuda.current_stream(Q.device)
+    ptrs = (Q.data_ptr(), U.data_ptr(), V.data_ptr(), dH.data_ptr(), dQ.data_ptr(), dU.data_ptr(), dV.data_ptr())
+    with torch.cuda.device(Q.device):
+        if Q.dtype == torch.bfloat16:
+            st = anchor_attn_backward_ptr(*ptrs, B, heads, n, m, d, scale, s.cuda_stream)
+        elif Q.dtype == torch.float32:
+            st = anchor_attn_backward_f32_ptr(*ptrs, B, heads, n, m, d, scale, s.cuda_stream)
+        else:
+            raise TypeError("Q must be bfloat16 or float32")
+    _raise(st, "backward")
+    return dQ, dU, dV

@@ -145,6 +145,55 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
     return ANCHOR_ATTN_OK;
 }
 
+// The backward's argument checks and launch (the entry points are below).
+anchor_attn_status_t backward(const anchor::BwdProblem &p, void *stream_v) {
+    const anchor_attn_status_t st = check_shape(p.B, p.heads, p.n, p.m, p.d);
+    if (st != ANCHOR_ATTN_OK) return st;
+    if (!isfinite(p.scale)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (p.heads == 0) return ANCHOR_ATTN_OK;
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    const size_t es = p.f32 ? 4 : 2;
+    const size_t ubytes = (size_t)p.heads * p.m * p.d * es;
+    if (!p.dU || ((uintptr_t)p.dU & 15u)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (p.slices() == 0 || p.n == 0) {  // no token: dU is zero
+        if (cudaMemsetAsync(p.dU, 0, ubytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return ANCHOR_ATTN_ERR_CUDA;
+        }
+        return ANCHOR_ATTN_OK;
+    }
+    const void *in[4] = {p.Q, p.U, p.V, p.dH};
+    const void *out[3] = {p.dQ, p.dU, p.dV};
+    for (const void *q : in)
+        if (!q || ((uintptr_t)q & 15u)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    for (const void *q : out)
+        if (!q || ((uintptr_t)q & 15u)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const size_t xbytes = (size_t)p.slices() * p.n * p.d * es;
+    const size_t in_bytes[4] = {xbytes, ubytes, xbytes, xbytes};
+    const size_t out_bytes[3] = {xbytes, ubytes, xbytes};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 4; ++i)
+            if (anchor::overlaps(out[o], out_bytes[o], in[i], in_bytes[i])) return ANCHOR_ATTN_ERR_ALIAS;
+        for (int o2 = 0; o2 < o; ++o2)
+            if (anchor::overlaps(out[o], out_bytes[o], out[o2], out_bytes[o2])) return ANCHOR_ATTN_ERR_ALIAS;
+    }
+    if (!anchor::bwd_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    void *ws = nullptr;
+    if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
+    if (cudaMallocAsync(&ws, anchor::bwd_layout(p).total_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ANCHOR_ATTN_ERR_ALLOC;
+    }
+    cudaError_t e = anchor::launch_bwd(p, ws, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = ef;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ANCHOR_ATTN_ERR_CUDA;
+    }
+    return ANCHOR_ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -174,6 +223,20 @@ anchor_attn_status_t anchor_attn_test_forward(const void *Q, const void *U, cons
     return run(p, stream, &t);
 }
 
+anchor_attn_status_t anchor_attn_backward(const void *Q, const void *U, const void *V, const void *dH, void *dQ,
+                                          void *dU, void *dV, int B, int heads, int n, int m, int d, float scale,
+                                          void *stream) {
+    const anchor::BwdProblem p{Q, U, V, dH, dQ, dU, dV, B, heads, n, m, d, scale, false};
+    return backward(p, stream);
+}
+
+anchor_attn_status_t anchor_attn_backward_f32(const float *Q, const float *U, const float *V, const float *dH,
+                                              float *dQ, float *dU, float *dV, int B, int heads, int n, int m, int d,
+                                              float scale, void *stream) {
+    const anchor::BwdProblem p{Q, U, V, dH, dQ, dU, dV, B, heads, n, m, d, scale, true};
+    return backward(p, stream);
+}
+
 anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, int m, int d,
                                             anchor_attn_plan_t *plan) {
     if (!plan || (dtype != 0 && dtype != 1)) return ANCHOR_ATTN_ERR_INVALID_ARG;
@@ -192,13 +255,13 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
-        anchor::simt_read_and_clear_error(&b) != cudaSuccess) {
+        anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b;
+    *code = a | b | c;
     return ANCHOR_ATTN_OK;
 }
 

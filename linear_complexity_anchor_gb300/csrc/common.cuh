@@ -66,6 +66,26 @@ cudaError_t launch_simt_full(const Problem &p, cudaStream_t stream);
 cudaError_t launch_simt_chunk(const Problem &p, void *workspace, cudaStream_t stream);
 cudaError_t simt_read_and_clear_error(unsigned *out);
 
+// --- backward (CUDA-core) -------------------------------------------------------------
+struct BwdProblem {
+    const void *Q, *U, *V, *dH;
+    void *dQ, *dU, *dV;
+    int B, heads, n, m, d;
+    float scale;
+    bool f32;
+    long long slices() const { return (long long)B * heads; }
+};
+// workspace: a zeroed header (ticket, arrival counters, ready flags), the chunk partials
+// [slices][chunks][m + 2 m d], the published W' | dW | dDelta per slice, and the chunks' dU
+// shares [slices][chunks][m d] (all fp32)
+struct BwdLayout {
+    size_t header_bytes = 0, part_offset = 0, pub_offset = 0, dupart_offset = 0, total_bytes = 0;
+};
+bool bwd_fits(const BwdProblem &p);
+BwdLayout bwd_layout(const BwdProblem &p);
+cudaError_t launch_bwd(const BwdProblem &p, void *workspace, cudaStream_t stream);
+cudaError_t bwd_read_and_clear_error(unsigned *out);
+
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA
 constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)

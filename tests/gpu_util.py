@@ -6,6 +6,12 @@ Parity bar (the forward's stated tolerances):
          an output far below the slice's typical magnitude is a cancellation whose rounding
          error scales with its summands (~rms), not with itself.
   bf16 : |g - o| <= 1e-2 + 2e-2 |o| elementwise (2e-2 relative / 1e-2 absolute).
+  f32_bwd: the fp32 backward, |g - o| <= 1e-4 * max(|o|, rms(o)).  Its gradients pass the
+         forward's fp32 rounding through the softmax Jacobian, dS = A o (G - rowsum(A o G)),
+         a difference of nearly equal terms, and through divisions by Delta, which is small
+         for an anchor few tokens reach; a float32 evaluation in the kernel's own summation
+         order (sequential fused multiply-adds) already reaches 2.3e-5 on the worst tested
+         element, so the bar keeps the forward's form with a 10x wider constant.
 """
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -26,9 +32,9 @@ def to_host64(t) -> np.ndarray:
 
 
 def bound(ref: np.ndarray, dtype: str) -> np.ndarray:
-    if dtype == "f32":
+    if dtype in ("f32", "f32_bwd"):
         rms = float(np.sqrt((ref ** 2).mean())) if ref.size else 0.0
-        return 1e-5 * np.maximum(np.abs(ref), max(rms, 1e-30))
+        return (1e-5 if dtype == "f32" else 1e-4) * np.maximum(np.abs(ref), max(rms, 1e-30))
     return 1e-2 + 2e-2 * np.abs(ref)
 
 

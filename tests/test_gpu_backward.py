@@ -1,0 +1,89 @@
+"""GPU: the backward (dQ, dU, dV) through the C ABI against the oracle's backward, element by
+element, on the same seeded inputs (the oracle's backward is pinned by finite differences of
+the forward oracle in test_oracle_backward_pins.py)."""
+import numpy as np
+import pytest
+
+import gen
+from tests.conftest import gpu_available
+from tests.gpu_util import assert_parity, to_device, to_host64
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not gpu_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module")
+def env(oracle_mod):
+    import torch
+    import linear_complexity_anchor_gb300 as pkg
+    pkg.load()
+    assert pkg.device_error() == 0
+    return pkg, torch, oracle_mod
+
+
+def _case(env, dtype, B, heads, n, m, d, seed, dH=None, scale=None):
+    pkg, torch, orc = env
+    w = gen.WORKLOADS["vit14_f32"].with_(name="bwd", B=B, heads=heads, n=n, m=m, d=d, dtype=dtype)
+    x = gen.make_inputs(w, seed=seed)
+    if dH is None:
+        dH = gen.make_inputs(w.with_(name="bwd_dh"), seed=seed + 1000)["V"]
+    t = {k: to_device(x[k], dtype, torch) for k in "QUV"}
+    tdH = to_device(dH, dtype, torch)
+    sc = w.scale if scale is None else scale
+    dQ, dU, dV = pkg.backward(t["Q"], t["U"], t["V"], tdH, scale=sc)
+    torch.cuda.synchronize()
+    ref = orc.backward(*(gen.to_float64(a, dtype) for a in (x["Q"], x["U"], x["V"], dH)), sc)
+    return (dQ, dU, dV), ref, (t, tdH, sc)
+
+
+_SHAPES = [(1, 1, 196, 16, 64), (2, 3, 197, 30, 64), (1, 2, 700, 64, 64), (2, 2, 1100, 20, 64),
+           (1, 2, 513, 128, 128), (2, 1, 129, 49, 128), (3, 2, 7, 1, 16), (1, 1, 2, 33, 32), (1, 2, 300, 256, 64)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", _SHAPES)
+def test_backward_matches_oracle(env, dtype, shape):
+    got, ref, _ = _case(env, dtype, *shape, seed=sum(shape))
+    bar = "f32_bwd" if dtype == "f32" else dtype
+    for name, g, r in zip(("dQ", "dU", "dV"), got, ref):
+        assert_parity(to_host64(g), r, bar, f"{name} {dtype} {shape}")
+    assert env[0].device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_constant_upstream_rows(env, dtype):
+    """dH with constant rows: dQ = dU = 0 and dV = dH (S_t keeps column sums)."""
+    w = gen.WORKLOADS["vit14_f32"].with_(name="bwd", B=2, heads=2, n=600, m=40, d=64, dtype=dtype)
+    x = gen.make_inputs(w, seed=3)
+    dH = np.ascontiguousarray(np.broadcast_to(x["V"][:, :, :1, :], x["V"].shape))
+    (dQ, dU, dV), ref, _ = _case(env, dtype, 2, 2, 600, 40, 64, seed=3, dH=dH)
+    bar = "f32_bwd" if dtype == "f32" else dtype
+    for name, g, r in zip(("dQ", "dU", "dV"), (dQ, dU, dV), ref):
+        if name == "dV":
+            assert_parity(to_host64(g), r, bar, f"{name} constant rows")
+        else:  # exactly zero in exact arithmetic: rounding only, against the gradients' scale
+            scale = float(np.abs(gen.to_float64(dH, dtype)).max())
+            assert float(to_host64(g).__abs__().max()) <= (1e-5 if dtype == "f32" else 1e-2) * scale, name
+    assert_parity(to_host64(dV), gen.to_float64(dH, dtype), bar, "dV = dH")
+
+
+def test_backward_bit_stable(env):
+    pkg, torch, _ = env
+    got1, _, (t, tdH, sc) = _case(env, "bf16", 2, 3, 1500, 64, 64, seed=9)
+    got2 = pkg.backward(t["Q"], t["U"], t["V"], tdH, scale=sc)
+    torch.cuda.synchronize()
+    for a, b in zip(got1, got2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_backward_empty_and_rejected(env):
+    pkg, torch, _ = env
+    U = torch.ones((2, 4, 64), dtype=torch.bfloat16, device="cuda")
+    dU = torch.full_like(U, 5.0)
+    Q = torch.zeros((0, 2, 10, 64), dtype=torch.bfloat16, device="cuda")
+    st = pkg.anchor_attn_backward_ptr(0, U.data_ptr(), 0, 0, 0, dU.data_ptr(), 0, 0, 2, 10, 4, 64, 0.125, 0)
+    torch.cuda.synchronize()
+    assert st == 0 and bool((dU == 0).all()), "no batch entries: dU is zero"
+    Q = torch.zeros((1, 2, 10, 64), dtype=torch.bfloat16, device="cuda")
+    st = pkg.anchor_attn_backward_ptr(Q.data_ptr(), U.data_ptr(), Q.data_ptr(), Q.data_ptr(), Q.data_ptr(),
+                                      dU.data_ptr(), Q.data_ptr() + 16 * 64, 1, 2, 10, 4, 64, 0.125, 0)
+    assert st == 3, "an output over an input is rejected"
