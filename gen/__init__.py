@@ -35,7 +35,7 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "splitmix64", "uniform", "normal", "round_bf16", "bf16_to_f32",
-    "make_inputs", "slice_inputs",
+    "make_inputs", "slice_inputs", "make_keys",
 ]
 
 _G = np.uint64(0x9E3779B97F4A7C15)
@@ -180,6 +180,15 @@ def _draw_u(w: Workload, seed: int) -> np.ndarray:
             U[h] = K[h, perm[:w.m]] + 0.1 * noise[h]
         return U
     return normal(_key(seed, STREAM_U), 0, cnt).reshape(w.heads, w.m, w.d)
+
+
+def make_keys(w: Workload, seed: int = 0) -> np.ndarray:
+    """The per-head key matrix K [heads][n][d] of the workload, in its dtype: for the recipe
+    that draws the anchors from the rows of K ("u_from_k") it is that same K, so that full
+    softmax attention over K and anchor attention over U can be compared; for the others an
+    independent N(0, 1) draw on the same stream."""
+    K = normal(_key(seed, STREAM_K), 0, w.heads * w.n * w.d).reshape(w.heads, w.n, w.d)
+    return _round(K, w.dtype)
 
 
 def _round(x: np.ndarray, dtype: str) -> np.ndarray:

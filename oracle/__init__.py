@@ -45,6 +45,8 @@ class Oracle:
         lib.oracle_anchor_slice_rows.argtypes = [D, D, D, L, L, L, ctypes.c_double,
                                                  ctypes.POINTER(ctypes.c_long), L, D]
         lib.oracle_anchor_backward.argtypes = [D, D, D, D, D, D, D, L, L, L, L, L, ctypes.c_double]
+        lib.oracle_full_attention.argtypes = [D, D, D, D, L, L, L, L, ctypes.c_double]
+        lib.oracle_full_attention.restype = ctypes.c_int
         lib.oracle_anchor_slice_backward.argtypes = [D, D, D, D, L, L, L, ctypes.c_double, D, D, D]
         for f in (lib.oracle_anchor_forward, lib.oracle_anchor_slice, lib.oracle_anchor_slice_rows,
                   lib.oracle_anchor_backward, lib.oracle_anchor_slice_backward):
@@ -96,6 +98,15 @@ class Oracle:
                                                       _dp(dQ), _dp(dU), _dp(dV)))
         return dQ, dU, dV
 
+    def full_attention(self, Q, K, V, scale: float) -> np.ndarray:
+        """softmax(scale Q K^T) V for Q, V [B][heads][n][d] and K [heads][n][d] (float64)."""
+        Q, K, V = _f64(Q), _f64(K), _f64(V)
+        B, heads, n, d = Q.shape
+        assert K.shape == (heads, n, d) and V.shape == Q.shape
+        H = np.empty_like(Q)
+        _check(self._lib.oracle_full_attention(_dp(Q), _dp(K), _dp(V), _dp(H), B, heads, n, d, float(scale)))
+        return H
+
     def slice_rows(self, Q, U, V, scale: float, rows) -> np.ndarray:
         """H rows ``rows`` of one slice (Q, V [n][d], U [m][d])."""
         Q, U, V = _f64(Q), _f64(U), _f64(V)
@@ -142,6 +153,20 @@ def slice_forward(Q, U, V, scale: float) -> dict:
 
 def slice_rows(Q, U, V, scale: float, rows) -> np.ndarray:
     return _default().slice_rows(Q, U, V, scale, rows)
+
+
+def full_attention(Q, K, V, scale: float) -> np.ndarray:
+    return _default().full_attention(Q, K, V, scale)
+
+
+def relative_frobenius(Href, H) -> np.ndarray:
+    """Per (batch, head) slice: ||Href - H||_F / ||Href||_F, in float64 (the approximation
+    error of the anchor construction against full attention)."""
+    a = np.asarray(Href, dtype=np.float64)
+    b = np.asarray(H, dtype=np.float64)
+    num = np.sqrt(((a - b) ** 2).sum(axis=(-2, -1)))
+    den = np.sqrt((a ** 2).sum(axis=(-2, -1)))
+    return num / den
 
 
 def backward(Q, U, V, dH, scale: float) -> tuple:

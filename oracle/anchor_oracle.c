@@ -241,6 +241,57 @@ int oracle_anchor_backward(const double *Q, const double *U, const double *V, co
 }
 
 /*
+ * Full softmax attention, the quadratic construction the anchors approximate (the skeptic's
+ * concrete test in the pith.science verdict: compare H with softmax(Q K^T / sqrt(d)) V when
+ * the anchors come from rows of K).  One slice: Q, V [n][d], K [nk][d]:
+ *   H[i] = sum_j softmax over j of (scale q_i . k_j) v_j    (max subtracted first).
+ */
+int oracle_full_attention_slice(const double *Q, const double *K, const double *V, long n, long nk, long d,
+                                double scale, double *H)
+{
+    if (n < 0 || nk < 1 || d < 1) return 1;
+    double *p = malloc(sizeof(double) * (size_t)nk);
+    if (!p) return 2;
+    for (long i = 0; i < n; ++i) {
+        double mx = -INFINITY;
+        for (long j = 0; j < nk; ++j) {
+            double s = 0.0;
+            for (long k = 0; k < d; ++k) s += Q[i * d + k] * K[j * d + k];
+            p[j] = scale * s;
+            if (p[j] > mx) mx = p[j];
+        }
+        double z = 0.0;
+        for (long j = 0; j < nk; ++j) {
+            p[j] = exp(p[j] - mx);
+            z += p[j];
+        }
+        for (long k = 0; k < d; ++k) {
+            double s = 0.0;
+            for (long j = 0; j < nk; ++j) s += p[j] * V[j * d + k];
+            H[i * d + k] = s / z;
+        }
+    }
+    free(p);
+    return 0;
+}
+
+/* Full attention of every slice: Q, V, H [B][heads][n][d]; K [heads][n][d], one key matrix
+ * per head shared by the batch (as the anchors are). */
+int oracle_full_attention(const double *Q, const double *K, const double *V, double *H, long B, long heads,
+                          long n, long d, double scale)
+{
+    if (B < 0 || heads < 0 || n < 1 || d < 1) return 1;
+    for (long b = 0; b < B; ++b)
+        for (long h = 0; h < heads; ++h) {
+            size_t off = ((size_t)b * (size_t)heads + (size_t)h) * (size_t)n * (size_t)d;
+            int rc = oracle_full_attention_slice(Q + off, K + (size_t)h * (size_t)n * (size_t)d, V + off, n, n, d,
+                                                 scale, H + off);
+            if (rc) return rc;
+        }
+    return 0;
+}
+
+/*
  * Whole forward.  Q, V, H: [B][heads][n][d]; U: [heads][m][d] shared across the batch.
  * Each (b, h) slice is independent (the construction is per attention head).
  */

@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 import tests.test_oracle_backward_pins as bpins
+import tests.test_oracle_full_attention_pins as fpins
 import tests.test_oracle_pins as pins
 
 # (name, text in anchor_oracle.c, replacement): each a plausible slip.
@@ -43,6 +44,28 @@ BACKWARD_MUTANTS = [
     ("dU not summed over the batch", "for (long i = 0; i < heads * m * d; ++i) dU[i] = 0.0;\n    for (long b = 0; b < B; ++b) {",
      "for (long b = 0; b < B; ++b) {\n        for (long i = 0; i < heads * m * d; ++i) dU[i] = 0.0;"),
 ]
+
+
+# slips in the full attention of the approximation-error diagnostic
+FULL_MUTANTS = [
+    ("full: max subtracted with the wrong sign", "p[j] = exp(p[j] - mx);", "p[j] = exp(mx - p[j]);"),
+    ("full: not normalised", "H[i * d + k] = s / z;", "H[i * d + k] = s;"),
+    ("full: scale dropped", "p[j] = scale * s;\n            if (p[j] > mx) mx = p[j];\n        }\n        double z = 0.0;\n        for (long j = 0; j < nk; ++j) {",
+     "p[j] = s;\n            if (p[j] > mx) mx = p[j];\n        }\n        double z = 0.0;\n        for (long j = 0; j < nk; ++j) {"),
+    ("full: keys indexed per batch entry", "K + (size_t)h * (size_t)n * (size_t)d", "K + (size_t)((b + h) % heads) * (size_t)n * (size_t)d"),
+]
+
+
+def _run_module_pins(module, mut) -> list:
+    import inspect as _inspect
+    failed = []
+    for name, fn in _inspect.getmembers(module, _inspect.isfunction):
+        if name.startswith("test_"):
+            try:
+                fn(mut)
+            except (AssertionError, ValueError, FloatingPointError, ZeroDivisionError):
+                failed.append(name)
+    return failed
 
 
 def _run_bpins(mut) -> list:
@@ -94,3 +117,11 @@ def test_backward_pins_reject_planted_mistake(tmp_path, name, old, new):
     mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
     failed = _run_bpins(mut)
     assert failed, f"no backward pin rejects the planted mistake '{name}'"
+
+
+@pytest.mark.parametrize("name,old,new", FULL_MUTANTS, ids=[m[0] for m in FULL_MUTANTS])
+def test_full_attention_pins_reject_planted_mistake(tmp_path, name, old, new):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
+    mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    assert _run_module_pins(fpins, mut), f"no full-attention pin rejects the planted mistake '{name}'"
