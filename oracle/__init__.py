@@ -107,6 +107,16 @@ class Oracle:
         _check(self._lib.oracle_full_attention(_dp(Q), _dp(K), _dp(V), _dp(H), B, heads, n, d, float(scale)))
         return H
 
+    @staticmethod
+    def relative_frobenius(Href, H) -> np.ndarray:
+        """Per (batch, head) slice: ||Href - H||_F / ||Href||_F, in float64 (the approximation
+        error of the anchor construction against full attention)."""
+        a = np.asarray(Href, dtype=np.float64)
+        b = np.asarray(H, dtype=np.float64)
+        num = np.sqrt(((a - b) ** 2).sum(axis=(-2, -1)))
+        den = np.sqrt((a ** 2).sum(axis=(-2, -1)))
+        return num / den
+
     def slice_rows(self, Q, U, V, scale: float, rows) -> np.ndarray:
         """H rows ``rows`` of one slice (Q, V [n][d], U [m][d])."""
         Q, U, V = _f64(Q), _f64(U), _f64(V)
@@ -160,13 +170,7 @@ def full_attention(Q, K, V, scale: float) -> np.ndarray:
 
 
 def relative_frobenius(Href, H) -> np.ndarray:
-    """Per (batch, head) slice: ||Href - H||_F / ||Href||_F, in float64 (the approximation
-    error of the anchor construction against full attention)."""
-    a = np.asarray(Href, dtype=np.float64)
-    b = np.asarray(H, dtype=np.float64)
-    num = np.sqrt(((a - b) ** 2).sum(axis=(-2, -1)))
-    den = np.sqrt((a ** 2).sum(axis=(-2, -1)))
-    return num / den
+    return Oracle.relative_frobenius(Href, H)
 
 
 def backward(Q, U, V, dH, scale: float) -> tuple:

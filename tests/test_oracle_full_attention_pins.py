@@ -35,11 +35,16 @@ def test_constant_values_and_zero_scale(oracle_mod):
 
 
 def test_dominant_key_selects_its_value(oracle_mod):
-    Q, K, V = _rand(2, 1, 1, 6, 3)
+    """Each head's keys are shared by the batch: with key 4 of head 0 and key 1 of head 1
+    scoring far above the rest, every query of (b, 0) takes V[b, 0, 4] and of (b, 1) V[b, 1, 1]."""
+    Q, K, V = _rand(2, 2, 2, 6, 3)
     Q[..., 0] = np.abs(Q[..., 0]) + 1.0
-    K[0, 4] = [800.0, 0.0, 0.0]  # key 4 scores >= 800 * scale above every other key
+    K[0, 4] = [800.0, 0.0, 0.0]  # scores >= 800 * scale above every other key of the head
+    K[1, 1] = [800.0, 0.0, 0.0]
     H = oracle_mod.full_attention(Q, K, V, 1.0)
-    assert np.allclose(H[0, 0], np.broadcast_to(V[0, 0, 4], H[0, 0].shape), atol=1e-12, rtol=0)
+    for b in range(2):
+        assert np.allclose(H[b, 0], np.broadcast_to(V[b, 0, 4], H[b, 0].shape), atol=1e-12, rtol=0)
+        assert np.allclose(H[b, 1], np.broadcast_to(V[b, 1, 1], H[b, 1].shape), atol=1e-12, rtol=0)
 
 
 def test_permutations(oracle_mod):
