@@ -115,6 +115,35 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_backward_f32(const float *Q, co
                                                               void *stream);
 
 /*
+ * Approximation-error diagnostic (the skeptic's concrete test in the pith.science verdict on
+ * arXiv 2505.16463: compare the anchor construction with full softmax attention when the
+ * anchors are rows of the keys).
+ *
+ * anchor_attn_full_forward: full softmax attention, the quadratic construction the anchors
+ * approximate, H[i] = sum_j softmax over j of (scale q_i . k_j) v_j.  Q, V, H: [B][heads][n][d];
+ * K: [heads][n][d], one key matrix per head shared by the batch (as the anchors U are).
+ * bf16 in and out, fp32 CUDA-core arithmetic; an online softmax over 64-key tiles, so any n
+ * runs; B * heads <= 65535.  d in {16, 32, 64, 128}.  H may not overlap Q, K or V.  No
+ * workspace.  Meant for the diagnostic, not as a fast attention.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_full_forward(const void *Q, const void *K, const void *V, void *H,
+                                                              int B, int heads, int n, int d, float scale,
+                                                              void *stream);
+
+/* fp32 full attention (same layout and errors). */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_full_forward_f32(const float *Q, const float *K, const float *V,
+                                                                  float *H, int B, int heads, int n, int d,
+                                                                  float scale, void *stream);
+
+/*
+ * err[b * heads + h] = ||Href[b][h] - H[b][h]||_F / ||Href[b][h]||_F (0 where Href is all
+ * zero), for [B][heads][n][d] tensors of dtype 0 = bf16 or 1 = fp32; err is a device array of
+ * B * heads floats.  fp32 sums of squares in a fixed order.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_relative_error(const void *Href, const void *H, float *err, int B,
+                                                                int heads, int n, int d, int dtype, void *stream);
+
+/*
  * Allocation-free variant of anchor_attn_forward (bf16 in and out, same layout, shapes and
  * errors).  The paper has no counterpart to this call: it exists for callers that may not
  * allocate device memory while they run - e.g. a plugin's enqueue step inside an inference

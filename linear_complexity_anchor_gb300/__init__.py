@@ -17,6 +17,7 @@ __all__ = [
     "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "anchor_attn_forward_static_scratch_ptr",
     "static_scratch_bytes", "device_error", "query_plan", "status_string", "anchor_attn_test_forward_ptr",
     "AnchorAttnError", "STATUS", "VARIANTS", "backward", "anchor_attn_backward_ptr", "anchor_attn_backward_f32_ptr",
+    "full_forward", "relative_error",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libanchor_attn.so")
@@ -62,6 +63,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
             fn.restype = ctypes.c_int
+        for name in ("anchor_attn_full_forward", "anchor_attn_full_forward_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
+            fn.restype = ctypes.c_int
+        lib.anchor_attn_relative_error.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+        lib.anchor_attn_relative_error.restype = ctypes.c_int
         lib.anchor_attn_test_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.c_ulonglong, i, vp]
         lib.anchor_attn_test_forward.restype = ctypes.c_int
         lib.anchor_attn_query_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(_Plan)]
@@ -231,3 +238,40 @@ def backward(Q, U, V, dH, scale: float | None = None, stream=None):
             raise TypeError("Q must be bfloat16 or float32")
     _raise(st, "backward")
     return dQ, dU, dV
+
+
+def full_forward(Q, K, V, H=None, scale: float | None = None, stream=None):
+    """Full softmax attention softmax(scale Q K^T) V for torch CUDA tensors (bf16 or fp32):
+    Q, V [B, heads, n, d], K [heads, n, d] (one key matrix per head).  The reference of the
+    approximation-error diagnostic."""
+    import torch
+    if H is None:
+        H = torch.empty_like(Q)
+    _check_tensors(Q, K, V, H, Q.dtype)
+    B, heads, n, d = Q.shape
+    if K.shape[1] != n:
+        raise ValueError("K must be [heads, n, d]: one key per token of the slice")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    s = stream if stream is not None else torch.cuda.current_stream(Q.device)
+    lib = load()
+    fn = lib.anchor_attn_full_forward if Q.dtype == torch.bfloat16 else lib.anchor_attn_full_forward_f32
+    with torch.cuda.device(Q.device):
+        st = fn(Q.data_ptr(), K.data_ptr(), V.data_ptr(), H.data_ptr(), B, heads, n, d, float(scale), s.cuda_stream)
+    _raise(st, "full_forward")
+    return H
+
+
+def relative_error(Href, H, stream=None):
+    """Per (batch, head) slice ||Href - H||_F / ||Href||_F as a float32 CUDA tensor [B, heads]."""
+    import torch
+    if Href.shape != H.shape or Href.dtype != H.dtype or Href.dim() != 4:
+        raise ValueError("Href and H must be [B, heads, n, d] of one dtype")
+    B, heads, n, d = Href.shape
+    err = torch.empty((B, heads), dtype=torch.float32, device=Href.device)
+    s = stream if stream is not None else torch.cuda.current_stream(Href.device)
+    with torch.cuda.device(Href.device):
+        st = load().anchor_attn_relative_error(Href.data_ptr(), H.data_ptr(), err.data_ptr(), B, heads, n, d,
+                                               1 if Href.dtype == torch.float32 else 0, s.cuda_stream)
+    _raise(st, "relative_error")
+    return err

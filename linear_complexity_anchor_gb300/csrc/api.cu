@@ -145,6 +145,30 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
     return ANCHOR_ATTN_OK;
 }
 
+// Full attention's argument checks and launch (the diagnostic's reference).
+anchor_attn_status_t full_forward(const anchor::FullProblem &p, void *stream_v) {
+    if (p.B < 0 || p.heads < 0 || p.n < 0 || p.d < 1) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (!(p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    if (!isfinite(p.scale)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const long long S = p.slices();
+    if (S == 0 || p.n == 0) return ANCHOR_ATTN_OK;
+    if (S > 65535 || (long long)p.n * p.d > (1LL << 62) / S) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    const void *ptrs[4] = {p.Q, p.K, p.V, p.H};
+    for (const void *q : ptrs)
+        if (!q || ((uintptr_t)q & 15u)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const size_t es = p.f32 ? 4 : 2;
+    const size_t xbytes = (size_t)S * p.n * p.d * es, kbytes = (size_t)p.heads * p.n * p.d * es;
+    if (anchor::overlaps(p.H, xbytes, p.Q, xbytes) || anchor::overlaps(p.H, xbytes, p.V, xbytes) ||
+        anchor::overlaps(p.H, xbytes, p.K, kbytes))
+        return ANCHOR_ATTN_ERR_ALIAS;
+    const cudaError_t e = anchor::launch_full_attention(p, (cudaStream_t)stream_v);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ANCHOR_ATTN_ERR_CUDA;
+    }
+    return ANCHOR_ATTN_OK;
+}
+
 // The backward's argument checks and launch (the entry points are below).
 anchor_attn_status_t backward(const anchor::BwdProblem &p, void *stream_v) {
     const anchor_attn_status_t st = check_shape(p.B, p.heads, p.n, p.m, p.d);
@@ -235,6 +259,31 @@ anchor_attn_status_t anchor_attn_backward_f32(const float *Q, const float *U, co
                                               float scale, void *stream) {
     const anchor::BwdProblem p{Q, U, V, dH, dQ, dU, dV, B, heads, n, m, d, scale, true};
     return backward(p, stream);
+}
+
+anchor_attn_status_t anchor_attn_full_forward(const void *Q, const void *K, const void *V, void *H, int B, int heads,
+                                              int n, int d, float scale, void *stream) {
+    return full_forward(anchor::FullProblem{Q, K, V, H, B, heads, n, d, scale, false}, stream);
+}
+
+anchor_attn_status_t anchor_attn_full_forward_f32(const float *Q, const float *K, const float *V, float *H, int B,
+                                                  int heads, int n, int d, float scale, void *stream) {
+    return full_forward(anchor::FullProblem{Q, K, V, H, B, heads, n, d, scale, true}, stream);
+}
+
+anchor_attn_status_t anchor_attn_relative_error(const void *Href, const void *H, float *err, int B, int heads, int n,
+                                                int d, int dtype, void *stream) {
+    if ((dtype != 0 && dtype != 1) || B < 0 || heads < 0 || n < 0 || d < 1) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const long long slices = (long long)B * heads;
+    if (slices == 0) return ANCHOR_ATTN_OK;
+    if (slices > 0x7fffffffLL || (long long)n * d > (1LL << 62) / slices) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (!Href || !H || !err) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const cudaError_t e = anchor::launch_rel_error(Href, H, err, slices, (size_t)n * d, dtype == 1, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ANCHOR_ATTN_ERR_CUDA;
+    }
+    return ANCHOR_ATTN_OK;
 }
 
 anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, int m, int d,

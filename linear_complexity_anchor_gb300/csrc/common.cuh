@@ -86,6 +86,19 @@ BwdLayout bwd_layout(const BwdProblem &p);
 cudaError_t launch_bwd(const BwdProblem &p, void *workspace, cudaStream_t stream);
 cudaError_t bwd_read_and_clear_error(unsigned *out);
 
+// --- approximation-error diagnostic ------------------------------------------------------
+struct FullProblem {
+    const void *Q, *K, *V;  // K: [heads][n][d], one key matrix per head shared by the batch
+    void *H;
+    int B, heads, n, d;
+    float scale;
+    bool f32;
+    long long slices() const { return (long long)B * heads; }
+};
+cudaError_t launch_full_attention(const FullProblem &p, cudaStream_t stream);
+cudaError_t launch_rel_error(const void *Href, const void *H, float *err, long long slices, size_t per_slice, bool f32,
+                             cudaStream_t stream);
+
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA
 constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)
