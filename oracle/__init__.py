@@ -46,6 +46,8 @@ class Oracle:
                                                  ctypes.POINTER(ctypes.c_long), L, D]
         lib.oracle_anchor_backward.argtypes = [D, D, D, D, D, D, D, L, L, L, L, L, ctypes.c_double]
         lib.oracle_full_attention.argtypes = [D, D, D, D, L, L, L, L, ctypes.c_double]
+        lib.oracle_anchor_causal.argtypes = [D, D, D, D, L, L, L, L, L, ctypes.c_double]
+        lib.oracle_anchor_causal.restype = ctypes.c_int
         lib.oracle_full_attention.restype = ctypes.c_int
         lib.oracle_anchor_slice_backward.argtypes = [D, D, D, D, L, L, L, ctypes.c_double, D, D, D]
         for f in (lib.oracle_anchor_forward, lib.oracle_anchor_slice, lib.oracle_anchor_slice_rows,
@@ -107,6 +109,16 @@ class Oracle:
         _check(self._lib.oracle_full_attention(_dp(Q), _dp(K), _dp(V), _dp(H), B, heads, n, d, float(scale)))
         return H
 
+    def causal(self, Q, U, V, scale: float) -> np.ndarray:
+        """The masked (causal) variant: token i's anchor summaries use tokens j <= i only."""
+        Q, U, V = _f64(Q), _f64(U), _f64(V)
+        B, heads, n, d = Q.shape
+        m = U.shape[1]
+        assert U.shape == (heads, m, d) and V.shape == Q.shape
+        H = np.empty_like(Q)
+        _check(self._lib.oracle_anchor_causal(_dp(Q), _dp(U), _dp(V), _dp(H), B, heads, n, m, d, float(scale)))
+        return H
+
     @staticmethod
     def relative_frobenius(Href, H) -> np.ndarray:
         """Per (batch, head) slice: ||Href - H||_F / ||Href||_F, in float64 (the approximation
@@ -163,6 +175,10 @@ def slice_forward(Q, U, V, scale: float) -> dict:
 
 def slice_rows(Q, U, V, scale: float, rows) -> np.ndarray:
     return _default().slice_rows(Q, U, V, scale, rows)
+
+
+def causal(Q, U, V, scale: float) -> np.ndarray:
+    return _default().causal(Q, U, V, scale)
 
 
 def full_attention(Q, K, V, scale: float) -> np.ndarray:

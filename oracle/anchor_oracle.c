@@ -241,6 +241,57 @@ int oracle_anchor_backward(const double *Q, const double *U, const double *V, co
 }
 
 /*
+ * Masked (causal) variant: the anchors' summaries seen by token i include only tokens j <= i,
+ * so that no token draws on a later one (the "masked variant of A that forbids future
+ * tokens ... at the same O(mn) cost" of the pith.science verdict's inferences):
+ *   Delta^(i)_l = sum_{j<=i} A[j][l],  W^(i)_l = sum_{j<=i} A[j][l] v_j,
+ *   H[i] = sum_l A[i][l] W^(i)_l / Delta^(i)_l   (0 for an anchor with Delta^(i)_l = 0).
+ * Each row of the masked S_t still sums to one.  One slice, prefixes in token order.
+ */
+int oracle_anchor_causal_slice(const double *Q, const double *U, const double *V, long n, long m, long d,
+                               double scale, double *H)
+{
+    if (bad_shape(n, m, d)) return 1;
+    double *A = malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)m);
+    double *delta = calloc((size_t)m, sizeof(double));
+    double *W = calloc((size_t)m * (size_t)d, sizeof(double));
+    if (!A || !delta || !W) {
+        free(A); free(delta); free(W);
+        return 2;
+    }
+    token_anchor_matrix(Q, U, n, m, d, scale, A);
+    for (long i = 0; i < n; ++i) {
+        const double *a = A + i * m;
+        for (long l = 0; l < m; ++l) {
+            delta[l] += a[l];
+            for (long k = 0; k < d; ++k) W[l * d + k] += a[l] * V[i * d + k];
+        }
+        for (long k = 0; k < d; ++k) {
+            double s = 0.0;
+            for (long l = 0; l < m; ++l)
+                if (delta[l] != 0.0) s += a[l] * W[l * d + k] / delta[l];
+            H[i * d + k] = s;
+        }
+    }
+    free(A); free(delta); free(W);
+    return 0;
+}
+
+int oracle_anchor_causal(const double *Q, const double *U, const double *V, double *H, long B, long heads, long n,
+                         long m, long d, double scale)
+{
+    if (B < 0 || heads < 0 || bad_shape(n, m, d)) return 1;
+    for (long b = 0; b < B; ++b)
+        for (long h = 0; h < heads; ++h) {
+            size_t off = ((size_t)b * (size_t)heads + (size_t)h) * (size_t)n * (size_t)d;
+            const size_t uoff = (size_t)h * (size_t)m * (size_t)d;
+            int rc = oracle_anchor_causal_slice(Q + off, U + uoff, V + off, n, m, d, scale, H + off);
+            if (rc) return rc;
+        }
+    return 0;
+}
+
+/*
  * Full softmax attention, the quadratic construction the anchors approximate (the skeptic's
  * concrete test in the pith.science verdict: compare H with softmax(Q K^T / sqrt(d)) V when
  * the anchors come from rows of K).  One slice: Q, V [n][d], K [nk][d]:

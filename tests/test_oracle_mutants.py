@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 import tests.test_oracle_backward_pins as bpins
+import tests.test_oracle_causal_pins as cpins
 import tests.test_oracle_full_attention_pins as fpins
 import tests.test_oracle_pins as pins
 
@@ -53,6 +54,16 @@ FULL_MUTANTS = [
     ("full: scale dropped", "p[j] = scale * s;\n            if (p[j] > mx) mx = p[j];\n        }\n        double z = 0.0;\n        for (long j = 0; j < nk; ++j) {",
      "p[j] = s;\n            if (p[j] > mx) mx = p[j];\n        }\n        double z = 0.0;\n        for (long j = 0; j < nk; ++j) {"),
     ("full: keys indexed per batch entry", "K + (size_t)h * (size_t)n * (size_t)d", "K + (size_t)((b + h) % heads) * (size_t)n * (size_t)d"),
+]
+
+
+# slips in the masked (causal) variant
+CAUSAL_MUTANTS = [
+    ("causal: anchor degree counted twice", "delta[l] += a[l];", "delta[l] += 2.0 * a[l];"),
+    ("causal: summaries from the first token's value", "W[l * d + k] += a[l] * V[i * d + k];",
+     "W[l * d + k] += a[l] * V[k];"),
+    ("causal: row weights of the previous token", "if (delta[l] != 0.0) s += a[l] * W[l * d + k] / delta[l];",
+     "if (delta[l] != 0.0) s += A[(i > 0 ? i - 1 : 0) * m + l] * W[l * d + k] / delta[l];"),
 ]
 
 
@@ -125,3 +136,11 @@ def test_full_attention_pins_reject_planted_mistake(tmp_path, name, old, new):
     assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
     mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
     assert _run_module_pins(fpins, mut), f"no full-attention pin rejects the planted mistake '{name}'"
+
+
+@pytest.mark.parametrize("name,old,new", CAUSAL_MUTANTS, ids=[m[0] for m in CAUSAL_MUTANTS])
+def test_causal_pins_reject_planted_mistake(tmp_path, name, old, new):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
+    mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    assert _run_module_pins(cpins, mut), f"no causal pin rejects the planted mistake '{name}'"
