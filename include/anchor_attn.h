@@ -115,6 +115,29 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_backward_f32(const float *Q, co
                                                               void *stream);
 
 /*
+ * Masked (causal) variant of anchor_attn_forward: the anchors' summaries seen by token i
+ * include only tokens j <= i, so that no token draws on a later one (the "masked variant of
+ * A that forbids future tokens ... at the same O(mn) cost" among the inferences of the
+ * pith.science verdict on arXiv 2505.16463):
+ *   Delta^(i)_l = sum_{j<=i} A[j][l],  W^(i)_l = sum_{j<=i} A[j][l] v_j,
+ *   H[i] = sum_l A[i][l] W^(i)_l / Delta^(i)_l   (0 for an anchor with Delta^(i)_l = 0).
+ * The last row equals anchor_attn_forward's last row.  Same layout, shapes, arguments and
+ * errors as anchor_attn_forward; bf16 in and out, fp32 CUDA-core arithmetic (a chunked scan
+ * over the tokens, one launch, one workspace from cudaMallocAsync on `stream`); shapes whose
+ * tiles do not fit one CTA's shared memory return ANCHOR_ATTN_ERR_UNSUPPORTED.  Results are
+ * bit-identical from run to run; a bounded wait that gives up is reported by
+ * anchor_attn_device_error (bit 1).
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_causal_forward(const void *Q, const void *U, const void *V, void *H,
+                                                                int B, int heads, int n, int m, int d, float scale,
+                                                                void *stream);
+
+/* fp32 causal variant (same layout and errors). */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_causal_forward_f32(const float *Q, const float *U, const float *V,
+                                                                    float *H, int B, int heads, int n, int m, int d,
+                                                                    float scale, void *stream);
+
+/*
  * Approximation-error diagnostic (the skeptic's concrete test in the pith.science verdict on
  * arXiv 2505.16463: compare the anchor construction with full softmax attention when the
  * anchors are rows of the keys).

@@ -17,7 +17,7 @@ __all__ = [
     "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "anchor_attn_forward_static_scratch_ptr",
     "static_scratch_bytes", "device_error", "query_plan", "status_string", "anchor_attn_test_forward_ptr",
     "AnchorAttnError", "STATUS", "VARIANTS", "backward", "anchor_attn_backward_ptr", "anchor_attn_backward_f32_ptr",
-    "full_forward", "relative_error",
+    "full_forward", "relative_error", "causal_forward",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libanchor_attn.so")
@@ -62,6 +62,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         for name in ("anchor_attn_backward", "anchor_attn_backward_f32"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+            fn.restype = ctypes.c_int
+        for name in ("anchor_attn_causal_forward", "anchor_attn_causal_forward_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
             fn.restype = ctypes.c_int
         for name in ("anchor_attn_full_forward", "anchor_attn_full_forward_f32"):
             fn = getattr(lib, name)
@@ -275,3 +279,23 @@ def relative_error(Href, H, stream=None):
                                                1 if Href.dtype == torch.float32 else 0, s.cuda_stream)
     _raise(st, "relative_error")
     return err
+
+
+def causal_forward(Q, U, V, H=None, scale: float | None = None, stream=None):
+    """The masked (causal) variant: token i's anchor summaries use tokens j <= i only.  Same
+    tensors as ``forward`` (bf16 or fp32)."""
+    import torch
+    if H is None:
+        H = torch.empty_like(Q)
+    _check_tensors(Q, U, V, H, Q.dtype)
+    B, heads, n, d = Q.shape
+    m = U.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    s = stream if stream is not None else torch.cuda.current_stream(Q.device)
+    lib = load()
+    fn = lib.anchor_attn_causal_forward if Q.dtype == torch.bfloat16 else lib.anchor_attn_causal_forward_f32
+    with torch.cuda.device(Q.device):
+        st = fn(Q.data_ptr(), U.data_ptr(), V.data_ptr(), H.data_ptr(), B, heads, n, m, d, float(scale), s.cuda_stream)
+    _raise(st, "causal_forward")
+    return H

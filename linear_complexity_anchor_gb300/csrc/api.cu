@@ -145,6 +145,29 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
     return ANCHOR_ATTN_OK;
 }
 
+// The masked (causal) variant's launch, after the forward's argument checks.
+anchor_attn_status_t causal_forward(const Problem &p, void *stream_v) {
+    const anchor_attn_status_t st = anchor::check_problem(p);
+    if (st != ANCHOR_ATTN_OK) return st;
+    if (p.slices() == 0 || p.n == 0) return ANCHOR_ATTN_OK;
+    if (!anchor::causal_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    void *ws = nullptr;
+    if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
+    if (cudaMallocAsync(&ws, anchor::causal_layout(p).total_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ANCHOR_ATTN_ERR_ALLOC;
+    }
+    cudaError_t e = anchor::launch_causal(p, ws, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = ef;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ANCHOR_ATTN_ERR_CUDA;
+    }
+    return ANCHOR_ATTN_OK;
+}
+
 // Full attention's argument checks and launch (the diagnostic's reference).
 anchor_attn_status_t full_forward(const anchor::FullProblem &p, void *stream_v) {
     if (p.B < 0 || p.heads < 0 || p.n < 0 || p.d < 1) return ANCHOR_ATTN_ERR_INVALID_ARG;
@@ -261,6 +284,16 @@ anchor_attn_status_t anchor_attn_backward_f32(const float *Q, const float *U, co
     return backward(p, stream);
 }
 
+anchor_attn_status_t anchor_attn_causal_forward(const void *Q, const void *U, const void *V, void *H, int B,
+                                                int heads, int n, int m, int d, float scale, void *stream) {
+    return causal_forward(Problem{Q, U, V, H, B, heads, n, m, d, scale, false}, stream);
+}
+
+anchor_attn_status_t anchor_attn_causal_forward_f32(const float *Q, const float *U, const float *V, float *H, int B,
+                                                    int heads, int n, int m, int d, float scale, void *stream) {
+    return causal_forward(Problem{Q, U, V, H, B, heads, n, m, d, scale, true}, stream);
+}
+
 anchor_attn_status_t anchor_attn_full_forward(const void *Q, const void *K, const void *V, void *H, int B, int heads,
                                               int n, int d, float scale, void *stream) {
     return full_forward(anchor::FullProblem{Q, K, V, H, B, heads, n, d, scale, false}, stream);
@@ -304,13 +337,14 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0, c = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
-        anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess) {
+        anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess ||
+        anchor::causal_read_and_clear_error(&e) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b | c;
+    *code = a | b | c | e;
     return ANCHOR_ATTN_OK;
 }
 

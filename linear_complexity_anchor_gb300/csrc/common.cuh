@@ -86,6 +86,17 @@ BwdLayout bwd_layout(const BwdProblem &p);
 cudaError_t launch_bwd(const BwdProblem &p, void *workspace, cudaStream_t stream);
 cudaError_t bwd_read_and_clear_error(unsigned *out);
 
+// --- masked (causal) variant (CUDA-core) ------------------------------------------------
+// workspace: a zeroed header, the chunks' totals [slices][chunks][m + m d] and their
+// exclusive prefixes [slices][chunks][m d + m rounded up to 4] (fp32)
+struct CausalLayout {
+    size_t header_bytes = 0, part_offset = 0, pre_offset = 0, total_bytes = 0;
+};
+bool causal_fits(const Problem &p);
+CausalLayout causal_layout(const Problem &p);
+cudaError_t launch_causal(const Problem &p, void *workspace, cudaStream_t stream);
+cudaError_t causal_read_and_clear_error(unsigned *out);
+
 // --- approximation-error diagnostic ------------------------------------------------------
 struct FullProblem {
     const void *Q, *K, *V;  // K: [heads][n][d], one key matrix per head shared by the batch
