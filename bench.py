@@ -405,6 +405,139 @@ def time_workload(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev, world:
             "call": call, "device_error": int(derr_max), "clocks": clk}
 
 
+def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
+    """The backward (dQ, dU, dV for an upstream gradient dH) of one workload, timed like the
+    forward (CUDA events on the launching stream, W untimed calls first).  Algorithmic work per
+    slice: 18 n m d flops (three contractions to recompute A and the summaries, six in the
+    gradient pass) and 8 n d elements of traffic (Q, V, dH read twice, dQ and dV written)."""
+    import torch
+    hQ, hU, hV = hQUV
+    Q, U, V = hQ.to(dev), hU.to(dev), hV.to(dev)
+    dH = torch.randn(Q.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(1)).to(Q.dtype)
+    dQ, dU, dV = torch.empty_like(Q), torch.empty_like(U), torch.empty_like(V)
+    stream = torch.cuda.Stream(device=dev)
+    fn = pkg.anchor_attn_backward_f32_ptr if w.dtype == "f32" else pkg.anchor_attn_backward_ptr
+    ptrs = (Q.data_ptr(), U.data_ptr(), V.data_ptr(), dH.data_ptr(), dQ.data_ptr(), dU.data_ptr(), dV.data_ptr())
+
+    def call():
+        st = fn(*ptrs, w.B, w.heads, w.n, w.m, w.d, w.scale, stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"anchor_attn_backward failed: {pkg.status_string(st)}")
+
+    torch.cuda.synchronize()
+    for _ in range(W):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(int(2e6))
+    for i in range(K):
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    derr = pkg.device_error()
+    call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    flops = 18 * w.slices * w.n * w.m * w.d
+    hbm = (8 * w.slices * w.n * w.d + 2 * w.heads * w.m * w.d) * w.elem_bytes
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fma_peak = sms * FMA_LANES_PER_SM * 2 * 2070e6 / 1e12
+    peak, peak_src = peaks()
+    rec = {"ms_per_call": call_ms, "value": w.slices * w.n / (call_ms / 1e3), "unit": UNIT, "steps": K,
+           "kernels_per_call": 2, "device_error": derr,
+           "fma_roofline": {"bound": "alu", "achieved": flops / (call_ms / 1e3) / 1e12, "peak": fma_peak,
+                            "unit": "TFLOP/s", "frac": flops / (call_ms / 1e3) / 1e12 / fma_peak,
+                            "peak_source": f"{sms} SMs x {FMA_LANES_PER_SM} fp32 FMA lanes x 2 flop x 2070 MHz",
+                            "flops_per_call": flops},
+           "hbm": {"achieved": hbm / (call_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                   "frac": hbm / (call_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_call": hbm,
+                   "peak_source": f"{peak_src} hbm_gbs"}}
+    if derr:
+        rec["invalid"] = f"device error word {derr:#x} after the timed calls"
+    return rec
+
+
+def time_causal(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
+    """The masked (causal) variant of one workload, timed like the forward.  Algorithmic
+    traffic as the forward's (Q, V and H once, U once); work about 4 n m d flops for A and the
+    summaries plus 2 n m d + 2 n TR (m + d) for the rows, counted here as 6 n m d."""
+    import torch
+    hQ, hU, hV = hQUV
+    Q, U, V = hQ.to(dev), hU.to(dev), hV.to(dev)
+    H = torch.empty_like(Q)
+    stream = torch.cuda.Stream(device=dev)
+    lib = pkg.load()
+    fn = lib.anchor_attn_causal_forward_f32 if w.dtype == "f32" else lib.anchor_attn_causal_forward
+    args = (Q.data_ptr(), U.data_ptr(), V.data_ptr(), H.data_ptr(), w.B, w.heads, w.n, w.m, w.d, float(w.scale))
+
+    def call():
+        st = fn(*args, stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"anchor_attn_causal_forward failed: {pkg.status_string(st)}")
+
+    torch.cuda.synchronize()
+    for _ in range(W):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(int(2e6))
+    for i in range(K):
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    derr = pkg.device_error()
+    call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    peak, peak_src = peaks()
+    rec = {"ms_per_call": call_ms, "value": w.slices * w.n / (call_ms / 1e3), "unit": UNIT, "steps": K,
+           "kernels_per_call": 1, "device_error": derr,
+           "hbm": {"achieved": w.algorithmic_bytes / (call_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                   "frac": w.algorithmic_bytes / (call_ms / 1e3) / 1e9 / peak,
+                   "algorithmic_bytes_per_call": w.algorithmic_bytes, "peak_source": f"{peak_src} hbm_gbs"},
+           "fma_roofline": fma_roofline(w, call_ms, None, dev)}
+    if derr:
+        rec["invalid"] = f"device error word {derr:#x} after the timed calls"
+    return rec
+
+
+def approx_error(pkg, w: gen.Workload, dev, K: int) -> dict:
+    """The approximation-error diagnostic on a workload whose anchors are rows of the keys:
+    ||H_full - H_anchor||_F / ||H_full||_F per slice (mean and max), with the time of the
+    full-attention reference and of the anchor forward on the same inputs."""
+    import torch
+    x = gen.make_inputs(w, seed=0)
+    x["K"] = gen.make_keys(w, seed=0)
+
+    def dev_t(a):
+        t = torch.from_numpy(a if w.dtype == "f32" else a.view("int16"))
+        return (t if w.dtype == "f32" else t.view(torch.bfloat16)).to(dev)
+
+    t = {k: dev_t(x[k]) for k in "QUVK"}
+    Hf, Ha = torch.empty_like(t["Q"]), torch.empty_like(t["Q"])
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(K):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
+
+    ms_full = timed(lambda: pkg.full_forward(t["Q"], t["K"], t["V"], H=Hf, scale=w.scale))
+    ms_anchor = timed(lambda: pkg.forward(t["Q"], t["U"], t["V"], H=Ha, scale=w.scale))
+    err = pkg.relative_error(Hf, Ha).double().cpu()
+    return {"workload": w.name, "rel_frobenius_mean": float(err.mean()), "rel_frobenius_max": float(err.max()),
+            "slices": w.slices, "full_attention_ms": ms_full, "anchor_ms": ms_anchor,
+            "note": "anchors are rows of the keys plus N(0, 0.1^2) noise; full attention is the CUDA-core "
+                    "reference of the diagnostic, not a tuned attention"}
+
+
 def roofline(w: gen.Workload, plan: dict, call_ms: float) -> dict:
     peak, peak_src = peaks()
     achieved = w.algorithmic_bytes / (call_ms / 1e3) / 1e9
@@ -505,6 +638,24 @@ def run_ours(args) -> None:
             del ts
             torch.cuda.empty_cache()
 
+    # the backward of every workload (fewer steps: it runs on CUDA cores)
+    bwd = {}
+    if not args.only and world == 1:
+        for name in sorted(gen.WORKLOADS):
+            ws = gen.WORKLOADS[name]
+            _, hq = host_inputs(ws, seed=rank) if name != w.name else (None, hQUV)
+            bwd[name] = time_backward(pkg, ws, hq, min(K, 10), min(args.warmup, 3), dev)
+            torch.cuda.empty_cache()
+
+    diag = approx_error(pkg, gen.WORKLOADS["deit_base"], dev, min(K, 10)) if not args.only and world == 1 else None
+    causal = {}
+    if not args.only and world == 1:
+        for name in sorted(gen.WORKLOADS):
+            ws = gen.WORKLOADS[name]
+            _, hq = host_inputs(ws, seed=rank) if name != w.name else (None, hQUV)
+            causal[name] = time_causal(pkg, ws, hq, min(K, 10), min(args.warmup, 3), dev)
+            torch.cuda.empty_cache()
+
     cpu = cpu_par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, x, args.cpu_seconds)
@@ -529,6 +680,9 @@ def run_ours(args) -> None:
             "clocks": t["clocks"],
             "device_error": t["device_error"],
             "workloads": subs,
+            "backward": bwd,
+            "approx_error": diag,
+            "causal": causal,
         }
         if t["device_error"] or e2e_err:
             line["invalid"] = f"device error word {t['device_error'] | e2e_err:#x} after the timed calls"
