@@ -85,7 +85,7 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, con
 /*
  * Backward of anchor_attn_forward, bf16 in and out, fp32 arithmetic on CUDA cores.  The
  * anchors are fitted by gradient descent (pith.science verdict on arXiv 2505.16463,
- * "core_discovery"; the arXiv abstract's anchors as "neurons in a neural layer"), so a layer
+ * "core_discovery"; the arXiv abstract, where the anchors are weights of a trainable layer), so a layer
  * built on the forward needs the gradients of a loss L with respect to Q, U and V given
  * dH = dL/dH:
  *   dW' = A^T dH,  dW = Delta^{-1} dW',  dDelta_j = -sum_k dW'[j][k] W'[j][k] / Delta_j,
@@ -116,9 +116,9 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_backward_f32(const float *Q, co
 
 /*
  * Masked (causal) variant of anchor_attn_forward: the anchors' summaries seen by token i
- * include only tokens j <= i, so that no token draws on a later one (the "masked variant of
- * A that forbids future tokens ... at the same O(mn) cost" among the inferences of the
- * pith.science verdict on arXiv 2505.16463):
+ * include only tokens j <= i, so that no token draws on a later one (one of the inferences of
+ * the pith.science verdict on arXiv 2505.16463: A can be masked against later tokens without
+ * giving up the O(mn) cost):
  *   Delta^(i)_l = sum_{j<=i} A[j][l],  W^(i)_l = sum_{j<=i} A[j][l] v_j,
  *   H[i] = sum_l A[i][l] W^(i)_l / Delta^(i)_l   (0 for an anchor with Delta^(i)_l = 0).
  * The last row equals anchor_attn_forward's last row.  Same layout, shapes, arguments and

@@ -4,7 +4,7 @@
 //   G = dH W'^T + V dW^T + 1 dDelta^T,  dS = A o (G - rowsum(A o G)),
 //   dQ = scale dS U,  dV = A dW,  dU = scale dS^T Q summed over the batch entries of a head.
 // (The anchors are fitted by gradient descent: pith.science verdict on arXiv 2505.16463,
-// "core_discovery"; the arXiv abstract's anchors as neurons in a neural layer.)
+// "core_discovery"; the arXiv abstract, where the anchors are weights of a trainable layer.)
 //
 // Two launches:
 //   anchor_bwd_kernel    work items from a ticket, in a fixed order: every B1 item (a

@@ -1,7 +1,7 @@
 // Masked (causal) variant of the anchor-attention forward: the anchors' summaries seen by
-// token i include only tokens j <= i, so that no token draws on a later one (the "masked
-// variant of A that forbids future tokens ... at the same O(mn) cost" among the inferences of
-// the pith.science verdict on arXiv 2505.16463):
+// token i include only tokens j <= i, so that no token draws on a later one (one of the
+// inferences of the pith.science verdict on arXiv 2505.16463: A can be masked against later
+// tokens without giving up the O(mn) cost):
 //   Delta^(i)_l = sum_{j<=i} A[j][l],  W^(i)_l = sum_{j<=i} A[j][l] v_j,
 //   H[i] = sum_l A[i][l] W^(i)_l / Delta^(i)_l   (0 for an anchor with Delta^(i)_l = 0).
 //

@@ -18,8 +18,8 @@
  * sum runs in ascending index order.  The softmax subtracts the row maximum first; that is
  * the same function mathematically and keeps exp() in range.
  *
- * Backward (the anchors are learned by gradient descent: "core_discovery"; the arXiv abstract's
- * anchors as "neurons in a neural layer"): for an upstream gradient dH of H, the gradients of
+ * Backward (the anchors are learned by gradient descent: "core_discovery"; the arXiv abstract,
+ * where the anchors are weights of a trainable layer): for an upstream gradient dH of H, the gradients of
  * the loss with respect to Q, U and V follow by the chain rule through the same steps, taken
  * in reverse:
  *   dW' = A^T dH,  dW = Delta^{-1} dW',  dDelta_j = -sum_k dW'[j][k] W'[j][k] / Delta_j,
@@ -242,8 +242,8 @@ int oracle_anchor_backward(const double *Q, const double *U, const double *V, co
 
 /*
  * Masked (causal) variant: the anchors' summaries seen by token i include only tokens j <= i,
- * so that no token draws on a later one (the "masked variant of A that forbids future
- * tokens ... at the same O(mn) cost" of the pith.science verdict's inferences):
+ * so that no token draws on a later one (one of the pith.science verdict's inferences: A
+ * can be masked against later tokens without giving up the O(mn) cost):
  *   Delta^(i)_l = sum_{j<=i} A[j][l],  W^(i)_l = sum_{j<=i} A[j][l] v_j,
  *   H[i] = sum_l A[i][l] W^(i)_l / Delta^(i)_l   (0 for an anchor with Delta^(i)_l = 0).
  * Each row of the masked S_t still sums to one.  One slice, prefixes in token order.

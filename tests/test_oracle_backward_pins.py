@@ -14,7 +14,7 @@ backward's own formula retyped:
   dU of a head is the sum over the batch entries that share its anchors; linearity in dH.
 
 Source: the anchors are fitted by gradient descent (pith.science verdict on arXiv 2505.16463,
-"core_discovery"; the arXiv abstract's anchors as neurons in a neural layer).
+"core_discovery"; the arXiv abstract, where the anchors are weights of a trainable layer).
 """
 import numpy as np
 import pytest

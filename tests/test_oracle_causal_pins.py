@@ -1,6 +1,6 @@
 """Pins for the oracle's masked (causal) variant of the anchor construction: token i's anchor
-summaries include only tokens j <= i (the "masked variant of A that forbids future tokens" of
-the pith.science verdict's inferences on arXiv 2505.16463).  Checked against what the
+summaries include only tokens j <= i (one of the pith.science verdict's inferences on arXiv
+2505.16463: A can be masked against later tokens).  Checked against what the
 definition fixes, not against the prefix loop retyped:
 
   the last token sees every token: its row equals the unmasked forward's last row;
