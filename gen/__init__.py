@@ -10,7 +10,8 @@ Counter-based, so that any element (or any slice of a tensor) can be drawn on it
   generators", OOPSLA 2014): output k of a stream with state ``key`` is
   ``mix(key + (k + 1) * 0x9E3779B97F4A7C15)`` with the published 64-bit finaliser ``mix``.
 * Stream key for (seed, stream id): ``mix(mix(seed + G) + stream * G)``, G the golden-ratio
-  constant above.  Stream ids: Q=1, V=2, U=3, K=4, row choice=5, noise=6.
+  constant above.  Stream ids: Q=1, V=2, U=3, K=4, row choice=5, noise=6; for the block
+  front end X=7, Wq=8, Wv=9.
 * Uniform in (0, 1): ``((x >> 11) + 0.5) * 2**-53``.
 * Normal: Box-Muller on the pair (2p, 2p+1) of uniforms: element 2p takes the cosine
   branch and element 2p+1 the sine branch.
@@ -35,7 +36,7 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "splitmix64", "uniform", "normal", "round_bf16", "bf16_to_f32",
-    "make_inputs", "slice_inputs", "make_keys",
+    "make_inputs", "slice_inputs", "make_keys", "BlockWorkload", "BLOCK_WORKLOADS", "make_block_inputs",
 ]
 
 _G = np.uint64(0x9E3779B97F4A7C15)
@@ -43,6 +44,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 STREAM_Q, STREAM_V, STREAM_U, STREAM_K, STREAM_ROWS, STREAM_NOISE = 1, 2, 3, 4, 5, 6
+STREAM_X, STREAM_WQ, STREAM_WV = 7, 8, 9
 
 _CHUNK = 1 << 22
 
@@ -247,3 +249,51 @@ def to_float64(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "f32":
         return np.asarray(x, dtype=np.float32).astype(np.float64)
     return bf16_to_f32(x).astype(np.float64)
+
+
+@dataclass(frozen=True)
+class BlockWorkload:
+    """The block front end: token embeddings X [B][n][dm] projected per head to Q and V by
+    Wq, Wv [heads][d][dm], then the forward with the anchors of ``base`` (same B, heads, n,
+    m, d).  X ~ N(0, 1) and W ~ N(0, 1/dm), so that Q and V are about N(0, 1) as in the
+    forward's workloads."""
+    name: str
+    base: str           # the forward workload whose shape and anchor recipe this block uses
+    dm: int
+    about: str
+
+    @property
+    def w(self) -> Workload:
+        return WORKLOADS[self.base]
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """X, the two projection matrices and U read once, H written once."""
+        w = self.w
+        return (w.B * w.n * self.dm + 2 * w.heads * w.d * self.dm + w.heads * w.m * w.d
+                + w.slices * w.n * w.d) * w.elem_bytes
+
+    @property
+    def flops(self) -> int:
+        """The two projections (2 n dm d flop each per slice) plus the forward's 6 n m d."""
+        w = self.w
+        return w.slices * w.n * (4 * self.dm * w.d + 6 * w.m * w.d)
+
+
+BLOCK_WORKLOADS: dict[str, BlockWorkload] = {b.name: b for b in [
+    BlockWorkload("deit_base_block", "deit_base", 768,
+                  "DeiT-Base block: 197 tokens of width 768 projected to 12 heads of 64"),
+    BlockWorkload("deit_small_block", "deit_small", 384,
+                  "DeiT-Small block: 197 tokens of width 384 projected to 6 heads of 64"),
+]}
+
+
+def make_block_inputs(bw: BlockWorkload, seed: int = 0) -> dict:
+    """X [B][n][dm], Wq, Wv [heads][d][dm] and U [heads][m][d] in the base workload's dtype."""
+    w = bw.w
+    X = _draw_big(w, seed, STREAM_X, 1.0, 0, w.B * w.n * bw.dm).reshape(w.B, w.n, bw.dm)
+    wmult = 1.0 / math.sqrt(bw.dm)
+    Wq = _draw_big(w, seed, STREAM_WQ, wmult, 0, w.heads * w.d * bw.dm).reshape(w.heads, w.d, bw.dm)
+    Wv = _draw_big(w, seed, STREAM_WV, wmult, 0, w.heads * w.d * bw.dm).reshape(w.heads, w.d, bw.dm)
+    U = _round(_draw_u(w, seed), w.dtype).reshape(w.heads, w.m, w.d)
+    return {"X": X, "Wq": Wq, "Wv": Wv, "U": U}

@@ -1,5 +1,7 @@
-"""CPU oracle for the anchor-attention forward H = A Delta^{-1} A^T V (AnchorFormer) and its
-backward (the gradients with respect to Q, U and V of a loss with upstream gradient dH).
+"""CPU oracle for the anchor-attention forward H = A Delta^{-1} A^T V (AnchorFormer), its
+backward (the gradients with respect to Q, U and V of a loss with upstream gradient dH), the
+masked variant, full softmax attention for the approximation-error diagnostic, and the block
+front end (Q and V projected from the token embeddings, then the forward).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` are the only callers.  The arithmetic lives in ``anchor_oracle.c`` (plain C,
@@ -50,6 +52,10 @@ class Oracle:
         lib.oracle_anchor_causal.restype = ctypes.c_int
         lib.oracle_full_attention.restype = ctypes.c_int
         lib.oracle_anchor_slice_backward.argtypes = [D, D, D, D, L, L, L, ctypes.c_double, D, D, D]
+        lib.oracle_anchor_block.argtypes = [D, D, D, D, D, L, L, L, L, L, L, ctypes.c_double]
+        lib.oracle_anchor_block.restype = ctypes.c_int
+        lib.oracle_anchor_block_slice.argtypes = [D, D, D, D, L, L, L, L, ctypes.c_double, D]
+        lib.oracle_anchor_block_slice.restype = ctypes.c_int
         for f in (lib.oracle_anchor_forward, lib.oracle_anchor_slice, lib.oracle_anchor_slice_rows,
                   lib.oracle_anchor_backward, lib.oracle_anchor_slice_backward):
             f.restype = ctypes.c_int
@@ -117,6 +123,29 @@ class Oracle:
         assert U.shape == (heads, m, d) and V.shape == Q.shape
         H = np.empty_like(Q)
         _check(self._lib.oracle_anchor_causal(_dp(Q), _dp(U), _dp(V), _dp(H), B, heads, n, m, d, float(scale)))
+        return H
+
+    def block(self, X, Wq, Wv, U, scale: float) -> np.ndarray:
+        """The block front end: Q = X Wq^T and V = X Wv^T per head, then the forward.
+        X [B][n][dm]; Wq, Wv [heads][d][dm]; U [heads][m][d]; returns H [B][heads][n][d]."""
+        X, Wq, Wv, U = _f64(X), _f64(Wq), _f64(Wv), _f64(U)
+        B, n, dm = X.shape
+        heads, m, d = U.shape
+        assert Wq.shape == (heads, d, dm) and Wv.shape == Wq.shape
+        H = np.empty((B, heads, n, d))
+        _check(self._lib.oracle_anchor_block(_dp(X), _dp(Wq), _dp(Wv), _dp(U), _dp(H), B, heads, n, m, d, dm,
+                                             float(scale)))
+        return H
+
+    def block_slice(self, X, Wq, Wv, U, scale: float) -> np.ndarray:
+        """One slice of the block front end: X [n][dm], Wq, Wv [d][dm], U [m][d] -> H [n][d]."""
+        X, Wq, Wv, U = _f64(X), _f64(Wq), _f64(Wv), _f64(U)
+        n, dm = X.shape
+        m, d = U.shape
+        assert Wq.shape == (d, dm) and Wv.shape == Wq.shape
+        H = np.empty((n, d))
+        _check(self._lib.oracle_anchor_block_slice(_dp(X), _dp(Wq), _dp(Wv), _dp(U), n, m, d, dm, float(scale),
+                                                   _dp(H)))
         return H
 
     @staticmethod
@@ -187,6 +216,14 @@ def full_attention(Q, K, V, scale: float) -> np.ndarray:
 
 def relative_frobenius(Href, H) -> np.ndarray:
     return Oracle.relative_frobenius(Href, H)
+
+
+def block(X, Wq, Wv, U, scale: float) -> np.ndarray:
+    return _default().block(X, Wq, Wv, U, scale)
+
+
+def block_slice(X, Wq, Wv, U, scale: float) -> np.ndarray:
+    return _default().block_slice(X, Wq, Wv, U, scale)
 
 
 def backward(Q, U, V, dH, scale: float) -> tuple:

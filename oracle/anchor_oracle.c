@@ -360,3 +360,54 @@ int oracle_anchor_forward(const double *Q, const double *U, const double *V, dou
     }
     return 0;
 }
+
+/*
+ * Block front end: in an AnchorFormer layer the anchor attention takes the place of a ViT
+ * block's self-attention, so its per-head queries and values are linear projections of the
+ * token embeddings X (no bias: the pages give none):
+ *   Q[i][k] = sum_c X[i][c] Wq[k][c],   V[i][k] = sum_c X[i][c] Wv[k][c],
+ * followed by the forward above on (Q, U, V).  One slice: X [n][dm] (the batch entry's
+ * tokens), Wq, Wv [d][dm] (the head's rows of the projection matrices), U [m][d], H [n][d].
+ */
+int oracle_anchor_block_slice(const double *X, const double *Wq, const double *Wv, const double *U, long n,
+                              long m, long d, long dm, double scale, double *H)
+{
+    if (bad_shape(n, m, d) || dm < 1) return 1;
+    double *Qp = malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)d);
+    double *Vp = malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)d);
+    if (!Qp || !Vp) {
+        free(Qp); free(Vp);
+        return 2;
+    }
+    for (long i = 0; i < n; ++i)
+        for (long k = 0; k < d; ++k) {
+            double sq = 0.0, sv = 0.0;
+            for (long c = 0; c < dm; ++c) {
+                sq += X[i * dm + c] * Wq[k * dm + c];
+                sv += X[i * dm + c] * Wv[k * dm + c];
+            }
+            Qp[i * d + k] = sq;
+            Vp[i * d + k] = sv;
+        }
+    int rc = oracle_anchor_slice(Qp, U, Vp, n, m, d, scale, NULL, NULL, NULL, NULL, H);
+    free(Qp); free(Vp);
+    return rc;
+}
+
+/* Every slice: X [B][n][dm]; Wq, Wv [heads][d][dm]; U [heads][m][d]; H [B][heads][n][d]. */
+int oracle_anchor_block(const double *X, const double *Wq, const double *Wv, const double *U, double *H, long B,
+                        long heads, long n, long m, long d, long dm, double scale)
+{
+    if (B < 0 || heads < 0 || bad_shape(n, m, d) || dm < 1) return 1;
+    for (long b = 0; b < B; ++b)
+        for (long h = 0; h < heads; ++h) {
+            const size_t xoff = (size_t)b * (size_t)n * (size_t)dm;
+            const size_t woff = (size_t)h * (size_t)d * (size_t)dm;
+            const size_t hoff = ((size_t)b * (size_t)heads + (size_t)h) * (size_t)n * (size_t)d;
+            const size_t uoff = (size_t)h * (size_t)m * (size_t)d;
+            int rc = oracle_anchor_block_slice(X + xoff, Wq + woff, Wv + woff, U + uoff, n, m, d, dm, scale,
+                                               H + hoff);
+            if (rc) return rc;
+        }
+    return 0;
+}

@@ -1,12 +1,13 @@
 """Plants one mistake at a time in a copy of the oracle (on the CPU) and checks that the
-pins reject every such copy: test_oracle_pins.py for the forward, and
-test_oracle_backward_pins.py for the backward."""
+pins reject every such copy: test_oracle_pins.py for the forward, test_oracle_backward_pins.py
+for the backward, and the full-attention, masked-variant and block-front-end pins for theirs."""
 import inspect
 
 import pytest
 
 import oracle
 import tests.test_oracle_backward_pins as bpins
+import tests.test_oracle_block_pins as blpins
 import tests.test_oracle_causal_pins as cpins
 import tests.test_oracle_full_attention_pins as fpins
 import tests.test_oracle_pins as pins
@@ -64,6 +65,20 @@ CAUSAL_MUTANTS = [
      "W[l * d + k] += a[l] * V[k];"),
     ("causal: row weights of the previous token", "if (delta[l] != 0.0) s += a[l] * W[l * d + k] / delta[l];",
      "if (delta[l] != 0.0) s += A[(i > 0 ? i - 1 : 0) * m + l] * W[l * d + k] / delta[l];"),
+]
+
+
+# slips in the block front end (the Q and V projections)
+BLOCK_MUTANTS = [
+    ("block: Q projected with the value weights", "sq += X[i * dm + c] * Wq[k * dm + c];",
+     "sq += X[i * dm + c] * Wv[k * dm + c];"),
+    ("block: query weights read transposed", "sq += X[i * dm + c] * Wq[k * dm + c];",
+     "sq += X[i * dm + c] * Wq[(c % d) * dm + (k * dm + c) / d % dm];"),
+    ("block: head offset of the weights dropped", "const size_t woff = (size_t)h * (size_t)d * (size_t)dm;",
+     "const size_t woff = 0;"),
+    ("block: batch offset of the tokens dropped", "const size_t xoff = (size_t)b * (size_t)n * (size_t)dm;",
+     "const size_t xoff = 0;"),
+    ("block: last embedding column skipped", "for (long c = 0; c < dm; ++c) {", "for (long c = 0; c + 1 < dm; ++c) {"),
 ]
 
 
@@ -144,3 +159,11 @@ def test_causal_pins_reject_planted_mistake(tmp_path, name, old, new):
     assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
     mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
     assert _run_module_pins(cpins, mut), f"no causal pin rejects the planted mistake '{name}'"
+
+
+@pytest.mark.parametrize("name,old,new", BLOCK_MUTANTS, ids=[m[0] for m in BLOCK_MUTANTS])
+def test_block_pins_reject_planted_mistake(tmp_path, name, old, new):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
+    mut = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    assert _run_module_pins(blpins, mut), f"no block pin rejects the planted mistake '{name}'"
