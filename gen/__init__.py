@@ -258,13 +258,13 @@ class BlockWorkload:
     m, d).  X ~ N(0, 1) and W ~ N(0, 1/dm), so that Q and V are about N(0, 1) as in the
     forward's workloads."""
     name: str
-    base: str           # the forward workload whose shape and anchor recipe this block uses
+    base: Workload      # the forward workload whose shape, dtype and anchor recipe this block uses
     dm: int
     about: str
 
     @property
     def w(self) -> Workload:
-        return WORKLOADS[self.base]
+        return self.base
 
     @property
     def algorithmic_bytes(self) -> int:
@@ -281,9 +281,9 @@ class BlockWorkload:
 
 
 BLOCK_WORKLOADS: dict[str, BlockWorkload] = {b.name: b for b in [
-    BlockWorkload("deit_base_block", "deit_base", 768,
+    BlockWorkload("deit_base_block", WORKLOADS["deit_base"], 768,
                   "DeiT-Base block: 197 tokens of width 768 projected to 12 heads of 64"),
-    BlockWorkload("deit_small_block", "deit_small", 384,
+    BlockWorkload("deit_small_block", WORKLOADS["deit_small"], 384,
                   "DeiT-Small block: 197 tokens of width 384 projected to 6 heads of 64"),
 ]}
 

@@ -167,6 +167,30 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_relative_error(const void *Href
                                                                 int heads, int n, int d, int dtype, void *stream);
 
 /*
+ * Block front end: an AnchorFormer layer puts the anchor attention where a ViT block has its
+ * self-attention, so the per-head queries and values are projections of the token embeddings
+ * (pith.science verdict on arXiv 2505.16463, "key_machinery" and the referee summary of
+ * Eq. 11/12; the arXiv abstract, where the anchors are weights of a trainable layer):
+ *
+ *   Q[b][h][i][k] = sum_c X[b][i][c] Wq[h][k][c],   V[b][h][i][k] = sum_c X[b][i][c] Wv[h][k][c]
+ *   H[b][h] = anchor_attn_forward of (Q[b][h], U[h], V[b][h])
+ *
+ * computed in one kernel: the projections run on the tensor cores into tensor memory and are
+ * used from there (rounded to bf16 operands), so X is read once and Q, V never reach global
+ * memory.  Layout: X [B][n][dm]; Wq, Wv [heads][d][dm] (each head's rows of the projection
+ * matrices, i.e. a [heads*d][dm] weight); U [heads][m][d]; H [B][heads][n][d]; all bf16,
+ * device pointers, 16-byte aligned, caller-owned.  No bias (the pages give none).
+ * Shapes: d = 64, 1 <= m <= 64, 1 <= n <= 256 (a ViT classification block: 196 patches and
+ * a class token), dm a positive multiple of 64; B, heads >= 0 (zero, or n = 0, is a no-op);
+ * anything else returns ANCHOR_ATTN_ERR_UNSUPPORTED.  H may not overlap X, Wq, Wv or U
+ * (ANCHOR_ATTN_ERR_ALIAS).  No workspace; one launch; results are bit-identical from run to
+ * run.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_block_forward(const void *X, const void *Wq, const void *Wv,
+                                                               const void *U, void *H, int B, int heads, int n, int m,
+                                                               int d, int dm, float scale, void *stream);
+
+/*
  * Allocation-free variant of anchor_attn_forward (bf16 in and out, same layout, shapes and
  * errors).  The paper has no counterpart to this call: it exists for callers that may not
  * allocate device memory while they run - e.g. a plugin's enqueue step inside an inference

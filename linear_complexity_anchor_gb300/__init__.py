@@ -17,7 +17,7 @@ __all__ = [
     "anchor_attn_forward_ptr", "anchor_attn_forward_f32_ptr", "anchor_attn_forward_static_scratch_ptr",
     "static_scratch_bytes", "device_error", "query_plan", "status_string", "anchor_attn_test_forward_ptr",
     "AnchorAttnError", "STATUS", "VARIANTS", "backward", "anchor_attn_backward_ptr", "anchor_attn_backward_f32_ptr",
-    "full_forward", "relative_error", "causal_forward",
+    "full_forward", "relative_error", "causal_forward", "block_forward", "anchor_attn_block_forward_ptr",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libanchor_attn.so")
@@ -71,6 +71,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
             fn.restype = ctypes.c_int
+        lib.anchor_attn_block_forward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+        lib.anchor_attn_block_forward.restype = ctypes.c_int
         lib.anchor_attn_relative_error.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.anchor_attn_relative_error.restype = ctypes.c_int
         lib.anchor_attn_test_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, ctypes.c_ulonglong, i, vp]
@@ -298,4 +300,37 @@ def causal_forward(Q, U, V, H=None, scale: float | None = None, stream=None):
     with torch.cuda.device(Q.device):
         st = fn(Q.data_ptr(), U.data_ptr(), V.data_ptr(), H.data_ptr(), B, heads, n, m, d, float(scale), s.cuda_stream)
     _raise(st, "causal_forward")
+    return H
+
+
+def anchor_attn_block_forward_ptr(X: int, Wq: int, Wv: int, U: int, H: int, B: int, heads: int, n: int, m: int,
+                                  d: int, dm: int, scale: float, stream: int = 0) -> int:
+    """Raw C-ABI call of the block front end (bf16 device pointers); returns the status code."""
+    return load().anchor_attn_block_forward(X, Wq, Wv, U, H, B, heads, n, m, d, dm, float(scale), stream)
+
+
+def block_forward(X, Wq, Wv, U, H=None, scale: float | None = None, stream=None):
+    """The block front end for bf16 torch CUDA tensors: Q = X Wq^T and V = X Wv^T per head,
+    then the forward, in one kernel.  X [B, n, dm]; Wq, Wv [heads, d, dm]; U [heads, m, d];
+    returns H [B, heads, n, d]."""
+    import torch
+    if X.dim() != 3 or Wq.dim() != 3 or Wv.shape != Wq.shape or U.dim() != 3:
+        raise ValueError("X must be [B, n, dm], Wq and Wv [heads, d, dm], U [heads, m, d]")
+    B, n, dm = X.shape
+    heads, d, _ = Wq.shape
+    m = U.shape[1]
+    if Wq.shape[2] != dm or U.shape[0] != heads or U.shape[2] != d:
+        raise ValueError("inconsistent shapes")
+    for t in (X, Wq, Wv, U):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous bfloat16 CUDA tensors")
+    if H is None:
+        H = torch.empty((B, heads, n, d), dtype=torch.bfloat16, device=X.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    s = stream if stream is not None else torch.cuda.current_stream(X.device)
+    with torch.cuda.device(X.device):
+        st = anchor_attn_block_forward_ptr(X.data_ptr(), Wq.data_ptr(), Wv.data_ptr(), U.data_ptr(), H.data_ptr(),
+                                           B, heads, n, m, d, dm, scale, s.cuda_stream)
+    _raise(st, "block_forward")
     return H

@@ -192,6 +192,31 @@ anchor_attn_status_t full_forward(const anchor::FullProblem &p, void *stream_v) 
     return ANCHOR_ATTN_OK;
 }
 
+// The block front end's argument checks and launch.
+anchor_attn_status_t block_forward(const anchor::BlockProblem &p, void *stream_v) {
+    if (p.B < 0 || p.heads < 0 || p.n < 0 || p.m < 1 || p.d < 1 || p.dm < 1) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    if (!isfinite(p.scale)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const long long S = (long long)p.B * p.heads;
+    if (S == 0 || p.n == 0) return ANCHOR_ATTN_OK;
+    if (!anchor::block_supported(p) || S > 0x7fffffffLL) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    if ((long long)p.n * p.dm > (1LL << 62) / p.B || (long long)p.n * p.d > (1LL << 62) / S)
+        return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const void *ptrs[5] = {p.X, p.Wq, p.Wv, p.U, p.H};
+    for (const void *q : ptrs)
+        if (!q || ((uintptr_t)q & 15u)) return ANCHOR_ATTN_ERR_INVALID_ARG;
+    const size_t xbytes = (size_t)p.B * p.n * p.dm * 2, wbytes = (size_t)p.heads * p.d * p.dm * 2;
+    const size_t ubytes = (size_t)p.heads * p.m * p.d * 2, hbytes = (size_t)S * p.n * p.d * 2;
+    if (anchor::overlaps(p.H, hbytes, p.X, xbytes) || anchor::overlaps(p.H, hbytes, p.Wq, wbytes) ||
+        anchor::overlaps(p.H, hbytes, p.Wv, wbytes) || anchor::overlaps(p.H, hbytes, p.U, ubytes))
+        return ANCHOR_ATTN_ERR_ALIAS;
+    const cudaError_t e = anchor::launch_block(p, (cudaStream_t)stream_v);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ANCHOR_ATTN_ERR_CUDA;
+    }
+    return ANCHOR_ATTN_OK;
+}
+
 // The backward's argument checks and launch (the entry points are below).
 anchor_attn_status_t backward(const anchor::BwdProblem &p, void *stream_v) {
     const anchor_attn_status_t st = check_shape(p.B, p.heads, p.n, p.m, p.d);
@@ -304,6 +329,12 @@ anchor_attn_status_t anchor_attn_full_forward_f32(const float *Q, const float *K
     return full_forward(anchor::FullProblem{Q, K, V, H, B, heads, n, d, scale, true}, stream);
 }
 
+anchor_attn_status_t anchor_attn_block_forward(const void *X, const void *Wq, const void *Wv, const void *U, void *H,
+                                               int B, int heads, int n, int m, int d, int dm, float scale,
+                                               void *stream) {
+    return block_forward(anchor::BlockProblem{X, Wq, Wv, U, H, B, heads, n, m, d, dm, scale}, stream);
+}
+
 anchor_attn_status_t anchor_attn_relative_error(const void *Href, const void *H, float *err, int B, int heads, int n,
                                                 int d, int dtype, void *stream) {
     if ((dtype != 0 && dtype != 1) || B < 0 || heads < 0 || n < 0 || d < 1) return ANCHOR_ATTN_ERR_INVALID_ARG;
@@ -337,14 +368,14 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0, c = 0, e = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0, f = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
         anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess ||
-        anchor::causal_read_and_clear_error(&e) != cudaSuccess) {
+        anchor::causal_read_and_clear_error(&e) != cudaSuccess || anchor::block_read_and_clear_error(&f) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b | c | e;
+    *code = a | b | c | e | f;
     return ANCHOR_ATTN_OK;
 }
 

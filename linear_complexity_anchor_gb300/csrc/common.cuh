@@ -1,6 +1,7 @@
 // Shared device helpers and the internal launch interface of the anchor-attention kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -109,6 +110,22 @@ struct FullProblem {
 cudaError_t launch_full_attention(const FullProblem &p, cudaStream_t stream);
 cudaError_t launch_rel_error(const void *Href, const void *H, float *err, long long slices, size_t per_slice, bool f32,
                              cudaStream_t stream);
+
+// --- block front end (tensor core): Q and V projected from the token embeddings -------------
+struct BlockProblem {
+    const void *X;          // [B][n][dm] bf16 token embeddings
+    const void *Wq, *Wv;    // [heads][d][dm] bf16 rows of the query / value projections
+    const void *U;          // [heads][m][d] bf16 anchors
+    void *H;                // [B][heads][n][d] bf16
+    int B, heads, n, m, d, dm;
+    float scale;
+};
+bool block_supported(const BlockProblem &p);
+cudaError_t launch_block(const BlockProblem &p, cudaStream_t stream);
+cudaError_t block_read_and_clear_error(unsigned *out);
+
+// 3-D bf16 tensor map [outer][rows][cols], box 64 columns x box_rows rows x 1, 128-byte swizzle
+bool make_bf16_map(CUtensorMap *map, const void *base, int cols, int rows, long long outer, int box_rows);
 
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA

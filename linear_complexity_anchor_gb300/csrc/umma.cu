@@ -1494,6 +1494,10 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, const UmmaOptions &o
 
 }  // namespace
 
+bool make_bf16_map(CUtensorMap *map, const void *base, int cols, int rows, long long outer, int box_rows) {
+    return make_map(map, base, cols, rows, outer, box_rows);
+}
+
 // L2 size of the current device (126 MiB, GB300's, when no device can be queried: plans are
 // also asked for on machines without one)
 size_t l2_bytes() {

@@ -110,3 +110,24 @@ def test_missing_library_fails_loudly(tmp_path):
     import linear_complexity_anchor_gb300 as p
     with pytest.raises(RuntimeError, match="not built"):
         p.load(str(tmp_path / "nope.so"))
+
+
+def test_block_argument_validation(pkg):
+    """The block front end rejects bad arguments before touching the device."""
+    def c(X=A, Wq=2 * A, Wv=3 * A, U=4 * A, H=5 * A, B=2, heads=3, n=197, m=49, d=64, dm=768, scale=0.125):
+        return pkg.anchor_attn_block_forward_ptr(X, Wq, Wv, U, H, B, heads, n, m, d, dm, scale, 0)
+    INVALID, UNSUP, ALIAS = 1, 2, 3
+    assert c(X=0) == INVALID
+    assert c(U=4 * A + 8) == INVALID
+    assert c(m=0) == INVALID
+    assert c(dm=0) == INVALID
+    assert c(B=-1) == INVALID
+    assert c(scale=float("nan")) == INVALID
+    assert c(d=32) == UNSUP
+    assert c(m=65) == UNSUP
+    assert c(n=257) == UNSUP
+    assert c(dm=96) == UNSUP                    # not a multiple of 64
+    assert c(H=A + 64) == ALIAS                 # overlaps X
+    assert c(H=2 * A) == ALIAS                  # overlaps Wq
+    assert c(B=0) == 0 and c(heads=0) == 0 and c(n=0) == 0   # no-ops (no device access)
+    assert c(B=0, X=0, H=0) == 0
