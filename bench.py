@@ -2,8 +2,10 @@
 """Throughput of the anchor-attention forward H = A Delta^{-1} A^T V on GB300.
 
 One step = one forward over the whole workload (every (batch, head) slice) through the C
-ABI.  Prints ONE JSON line on rank 0: the headline workload (long_16k by default) and, under
-"workloads", every other workload timed the same way in the same run.
+ABI.  Prints ONE JSON line on rank 0: the headline workload (long_16k by default) and, timed
+in the same run, every other workload ("workloads"), the backward of each ("backward"), the
+masked variant ("causal"), the approximation-error diagnostic ("approx_error") and the block
+front end with its projections ("block"); --only keeps the headline alone.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -45,6 +47,7 @@ METRIC = "anchor-attn tokens·heads/s at 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "tokens*heads/s"
 DEFAULT_WORKLOAD = "long_16k"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_L2_BYTES = 126 * 1024 * 1024
 FMA_LANES_PER_SM = 128          # fp32 FMA lanes per SM (4 sub-partitions x 32)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -503,6 +506,95 @@ def time_causal(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
     return rec
 
 
+def bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the burst figure of MEASURED_PEAKS.json, for a kernel
+    timed alone."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def time_block(pkg, bw: gen.BlockWorkload, K: int, W: int, dev) -> dict:
+    """The block front end (projections + forward in one kernel) on one ViT block workload,
+    timed like the forward (GPU sleep, CUDA events on the launching stream, two rotating
+    input/output sets so that every call reads its X from HBM).  Its work is dominated by the
+    projections (4 n dm d flops per slice against the forward's 6 n m d), so the roofline is
+    the bf16 tensor peak.  For context, the same block unfused: one library GEMM for both
+    projections, the head-major layout copy of Q and V, and anchor_attn_forward."""
+    import numpy as np
+    import torch
+    w = bw.w
+    x = gen.make_block_inputs(bw, seed=0)
+
+    def dev_t(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    base = {k: dev_t(v) for k, v in x.items()}
+    sets = [base, {k: v.clone() for k, v in base.items()}]
+    for st in sets:
+        st["H"] = torch.empty((w.B, w.heads, w.n, w.d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    lib = pkg.load()
+
+    def call(i):
+        st = sets[i % len(sets)]
+        rc = lib.anchor_attn_block_forward(st["X"].data_ptr(), st["Wq"].data_ptr(), st["Wv"].data_ptr(),
+                                           st["U"].data_ptr(), st["H"].data_ptr(), w.B, w.heads, w.n, w.m, w.d,
+                                           bw.dm, float(w.scale), stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"anchor_attn_block_forward failed: {pkg.status_string(rc)}")
+
+    Wqv = torch.cat([base["Wq"].reshape(-1, bw.dm), base["Wv"].reshape(-1, bw.dm)], 0)
+    hd = w.heads * w.d
+
+    def unfused(i):
+        st = sets[i % len(sets)]
+        P = st["X"] @ Wqv.t()
+        Q = P[..., :hd].reshape(w.B, w.n, w.heads, w.d).permute(0, 2, 1, 3).contiguous()
+        V = P[..., hd:].reshape(w.B, w.n, w.heads, w.d).permute(0, 2, 1, 3).contiguous()
+        pkg.forward(Q, st["U"], V, H=st["H"], scale=w.scale, stream=stream)
+
+    def timed(fn, k):
+        torch.cuda.synchronize()
+        for i in range(W):
+            with torch.cuda.stream(stream):
+                fn(i)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        with torch.cuda.stream(stream):
+            if hasattr(torch.cuda, "_sleep"):
+                torch.cuda._sleep(int(2e6))
+            for i in range(k):
+                ev[i][0].record(stream)
+                fn(i)
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / k
+
+    call_ms = timed(call, K)
+    derr = pkg.device_error()
+    unfused_ms = timed(unfused, min(K, 10))
+    tpeak, tsrc = bf16_peak()
+    hpeak, hsrc = peaks()
+    tflops = bw.flops / (call_ms / 1e3) / 1e12
+    rec = {"ms_per_call": call_ms, "value": w.slices * w.n / (call_ms / 1e3), "unit": UNIT, "steps": K,
+           "kernels_per_call": 1, "device_error": derr,
+           "config": {"B": w.B, "heads": w.heads, "n": w.n, "m": w.m, "d": w.d, "dm": bw.dm},
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+                        "frac": tflops / tpeak, "kernel": "anchor_block_kernel",
+                        "flops_per_launch": bw.flops, "peak_source": f"{tsrc} bf16_tflops (burst)"},
+           "hbm": {"achieved": bw.algorithmic_bytes / (call_ms / 1e3) / 1e9, "peak": hpeak, "unit": "GB/s",
+                   "frac": bw.algorithmic_bytes / (call_ms / 1e3) / 1e9 / hpeak,
+                   "algorithmic_bytes_per_call": bw.algorithmic_bytes},
+           "unfused_ms_per_call": unfused_ms,
+           "unfused": "torch GEMM of X with [Wq; Wv], head-major copies of Q and V, anchor_attn_forward"}
+    if derr:
+        rec["invalid"] = f"device error word {derr:#x} after the timed calls"
+    return rec
+
+
 def approx_error(pkg, w: gen.Workload, dev, K: int) -> dict:
     """The approximation-error diagnostic on a workload whose anchors are rows of the keys:
     ||H_full - H_anchor||_F / ||H_full||_F per slice (mean and max), with the time of the
@@ -656,6 +748,12 @@ def run_ours(args) -> None:
             causal[name] = time_causal(pkg, ws, hq, min(K, 10), min(args.warmup, 3), dev)
             torch.cuda.empty_cache()
 
+    block = {}
+    if not args.only and world == 1:
+        for name in sorted(gen.BLOCK_WORKLOADS):
+            block[name] = time_block(pkg, gen.BLOCK_WORKLOADS[name], K, min(args.warmup, 3), dev)
+            torch.cuda.empty_cache()
+
     cpu = cpu_par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, x, args.cpu_seconds)
@@ -683,6 +781,7 @@ def run_ours(args) -> None:
             "backward": bwd,
             "approx_error": diag,
             "causal": causal,
+            "block": block,
         }
         if t["device_error"] or e2e_err:
             line["invalid"] = f"device error word {t['device_error'] | e2e_err:#x} after the timed calls"
