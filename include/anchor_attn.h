@@ -83,7 +83,7 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, con
                                              float scale, void *stream);
 
 /*
- * Backward of anchor_attn_forward, bf16 in and out, fp32 arithmetic on CUDA cores.  The
+ * Backward of anchor_attn_forward, bf16 in and out, fp32 accumulation.  The
  * anchors are fitted by gradient descent (pith.science verdict on arXiv 2505.16463,
  * "core_discovery"; the arXiv abstract, where the anchors are weights of a trainable layer), so a layer
  * built on the forward needs the gradients of a loss L with respect to Q, U and V given
@@ -92,6 +92,9 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, con
  *   G = dH W'^T + V dW^T + 1 dDelta^T,  dS = A o (G - rowsum(A o G)),
  *   dQ = scale dS U,  dV = A dW,  dU = scale sum over the batch of dS^T Q.
  * A is recomputed from Q and U (nothing is kept from the forward).
+ * With d = 64 and m <= 64 the contractions run on the tensor cores (tcgen05: bf16 operands -
+ * A, W', dW, dS rounded to bf16 as the forward rounds A - with fp32 accumulators), one CTA per
+ * slice; otherwise on CUDA-core fp32 FMA.
  *
  * Inputs Q, V, dH: [B][heads][n][d]; U: [heads][m][d].  Outputs dQ, dV: [B][heads][n][d];
  * dU: [heads][m][d] (the sum over the batch entries, which share the anchors).  Device
@@ -102,7 +105,7 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, con
  * (for fp32: d = 16 with m > about 900, d = 32 with m > about 480).  One workspace from
  * cudaMallocAsync on `stream` per call, released on the same stream; two kernel launches.
  * Results are bit-identical from run to run; a bounded wait that gives up is reported by
- * anchor_attn_device_error (bit 1).
+ * anchor_attn_device_error (bit 1 on the CUDA-core path, bit 0 on the tensor-core path).
  */
 ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_backward(const void *Q, const void *U, const void *V,
                                                           const void *dH, void *dQ, void *dU, void *dV, int B,

@@ -249,14 +249,16 @@ anchor_attn_status_t backward(const anchor::BwdProblem &p, void *stream_v) {
         for (int o2 = 0; o2 < o; ++o2)
             if (anchor::overlaps(out[o], out_bytes[o], out[o2], out_bytes[o2])) return ANCHOR_ATTN_ERR_ALIAS;
     }
-    if (!anchor::bwd_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    const bool tc = anchor::bwd_tc_supported(p);
+    if (!tc && !anchor::bwd_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
     void *ws = nullptr;
     if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
-    if (cudaMallocAsync(&ws, anchor::bwd_layout(p).total_bytes, stream) != cudaSuccess) {
+    const size_t wsb = tc ? anchor::bwd_tc_workspace(p) : anchor::bwd_layout(p).total_bytes;
+    if (cudaMallocAsync(&ws, wsb, stream) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_ALLOC;
     }
-    cudaError_t e = anchor::launch_bwd(p, ws, stream);
+    cudaError_t e = tc ? anchor::launch_bwd_tc(p, ws, stream) : anchor::launch_bwd(p, ws, stream);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = ef;
     if (e != cudaSuccess) {
@@ -368,14 +370,15 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0, c = 0, e = 0, f = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
         anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess ||
-        anchor::causal_read_and_clear_error(&e) != cudaSuccess || anchor::block_read_and_clear_error(&f) != cudaSuccess) {
+        anchor::causal_read_and_clear_error(&e) != cudaSuccess || anchor::block_read_and_clear_error(&f) != cudaSuccess ||
+        anchor::bwd_tc_read_and_clear_error(&g) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b | c | e | f;
+    *code = a | b | c | e | f | g;
     return ANCHOR_ATTN_OK;
 }
 

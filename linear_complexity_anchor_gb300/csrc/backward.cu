@@ -328,20 +328,41 @@ anchor_bwd_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__r
     }
 }
 
-// dU[h][e] = sum over batch entries b, then chunks c, of dupart[b heads + h][c][e]
+// dU[h][e] = sum over the K = B chunks shares k = (b, c) (b-major) of dupart[b heads + h][c][e],
+// in a fixed order: a CTA takes 32 consecutive e (one coalesced 128-byte row per share) and 8
+// groups of shares; group g adds shares g, g + 8, g + 16, ... in that order (loads issued 8 at
+// a time), then group 0 adds the 8 group sums in group order.
+constexpr int kDuGroups = 8, kDuBatch = 8;
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(32 * kDuGroups)
 anchor_bwd_du_kernel(const float *__restrict__ dupart, T *__restrict__ dU, int B, int heads, int chunks, int md) {
-    const int h = blockIdx.y;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= md) return;
+    __shared__ float part[kDuGroups][32];
+    const int h = blockIdx.y, lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + lane;
+    const int K = B * chunks;
     float s = 0.f;
-    for (int b = 0; b < B; ++b) {
-        const float *src = dupart + ((size_t)(b * heads + h) * chunks) * md + e;
-        for (int c = 0; c < chunks; ++c) s = __fadd_rn(s, src[(size_t)c * md]);
+    if (e < md) {
+        for (int k0 = g; k0 < K; k0 += kDuGroups * kDuBatch) {
+            float x[kDuBatch];
+#pragma unroll
+            for (int u = 0; u < kDuBatch; ++u) {
+                const int k = k0 + u * kDuGroups;
+                const int b = k / chunks, c = k - b * chunks;
+                x[u] = k < K ? __ldg(dupart + ((size_t)(b * heads + h) * chunks + c) * md + e) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kDuBatch; ++u)
+                if (k0 + u * kDuGroups < K) s = __fadd_rn(s, x[u]);
+        }
     }
-    float v[1] = {s};
-    dU[(size_t)h * md + e] = from_f32<T>(v[0]);
+    part[g][lane] = s;
+    __syncthreads();
+    if (g == 0 && e < md) {
+        float t = part[0][lane];
+#pragma unroll
+        for (int q = 1; q < kDuGroups; ++q) t = __fadd_rn(t, part[q][lane]);
+        dU[(size_t)h * md + e] = from_f32<T>(t);
+    }
 }
 
 template <typename T>
@@ -380,10 +401,7 @@ cudaError_t bwd_launch(const BwdProblem &p, void *ws, cudaStream_t stream) {
     kern<<<grid, kThreads, smem, stream>>>((const T *)p.Q, (const T *)p.U, (const T *)p.V, (const T *)p.dH, (T *)p.dQ,
                                            (T *)p.dV, bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int md = p.m * p.d;
-    anchor_bwd_du_kernel<T><<<dim3((md + kThreads - 1) / kThreads, p.heads), kThreads, 0, stream>>>(
-        bp.dupart, (T *)p.dU, p.B, p.heads, bp.chunks, md);
-    return cudaGetLastError();
+    return launch_bwd_du_sum(bp.dupart, p.dU, p.B, p.heads, bp.chunks, p.m * p.d, p.f32, stream);
 }
 
 }  // namespace
@@ -408,6 +426,17 @@ BwdLayout bwd_layout(const BwdProblem &p) {
 
 cudaError_t launch_bwd(const BwdProblem &p, void *workspace, cudaStream_t stream) {
     return p.f32 ? bwd_launch<float>(p, workspace, stream) : bwd_launch<__nv_bfloat16>(p, workspace, stream);
+}
+
+cudaError_t launch_bwd_du_sum(const float *dupart, void *dU, int B, int heads, int chunks, int md, bool f32,
+                              cudaStream_t stream) {
+    const dim3 grid((md + 31) / 32, heads);
+    if (f32)
+        anchor_bwd_du_kernel<float><<<grid, 32 * kDuGroups, 0, stream>>>(dupart, (float *)dU, B, heads, chunks, md);
+    else
+        anchor_bwd_du_kernel<__nv_bfloat16><<<grid, 32 * kDuGroups, 0, stream>>>(dupart, (__nv_bfloat16 *)dU, B,
+                                                                                 heads, chunks, md);
+    return cudaGetLastError();
 }
 
 cudaError_t bwd_read_and_clear_error(unsigned *out) {

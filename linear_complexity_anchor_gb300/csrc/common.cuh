@@ -86,6 +86,14 @@ bool bwd_fits(const BwdProblem &p);
 BwdLayout bwd_layout(const BwdProblem &p);
 cudaError_t launch_bwd(const BwdProblem &p, void *workspace, cudaStream_t stream);
 cudaError_t bwd_read_and_clear_error(unsigned *out);
+// dU[h] = sum over batch entries b, then chunks c, of dupart[b heads + h][c] ([m d] fp32 blocks)
+cudaError_t launch_bwd_du_sum(const float *dupart, void *dU, int B, int heads, int chunks, int md, bool f32,
+                              cudaStream_t stream);
+// the backward on the tensor cores (bf16, d = 64, m <= 64): workspace = the slices' dU blocks
+bool bwd_tc_supported(const BwdProblem &p);
+size_t bwd_tc_workspace(const BwdProblem &p);
+cudaError_t launch_bwd_tc(const BwdProblem &p, void *workspace, cudaStream_t stream);
+cudaError_t bwd_tc_read_and_clear_error(unsigned *out);
 
 // --- masked (causal) variant (CUDA-core) ------------------------------------------------
 // workspace: a zeroed header, the chunks' totals [slices][chunks][m + m d] and their

@@ -1,6 +1,10 @@
 """GPU: the backward (dQ, dU, dV) through the C ABI against the oracle's backward, element by
 element, on the same seeded inputs (the oracle's backward is pinned by finite differences of
-the forward oracle in test_oracle_backward_pins.py)."""
+the forward oracle in test_oracle_backward_pins.py).  bf16 with d = 64 and m <= 64 runs on the
+tensor cores; the rest, and fp32, on CUDA cores."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 
@@ -66,13 +70,58 @@ def test_backward_constant_upstream_rows(env, dtype):
     assert_parity(to_host64(dV), gen.to_float64(dH, dtype), bar, "dV = dH")
 
 
+# tensor-core path: one token; exactly one tile; a second tile of one token; a long slice;
+# one anchor; many batch entries summed into dU
+_TC_SHAPES = [(3, 2, 1, 7, 64), (2, 2, 128, 64, 64), (1, 3, 129, 49, 64), (1, 1, 2000, 64, 64), (2, 2, 300, 1, 64),
+              (16, 2, 197, 33, 64)]
+
+
+@pytest.mark.parametrize("shape", _TC_SHAPES)
+def test_backward_tensor_core_shapes(env, shape):
+    got, ref, _ = _case(env, "bf16", *shape, seed=sum(shape) + 1)
+    for name, g, r in zip(("dQ", "dU", "dV"), got, ref):
+        assert_parity(to_host64(g), r, "bf16", f"{name} {shape}")
+    assert env[0].device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["deit_small", "deit_base", "det_800x1344"])
+def test_backward_workload_every_slice(env, name):
+    """Full size: every slice's dQ and dV against the oracle element by element, and dU
+    against the sum of every slice's share (the oracle runs one slice per host core)."""
+    pkg, torch, orc = env
+    w = gen.WORKLOADS[name]
+    x = gen.make_inputs(w, seed=0)
+    dH = gen.make_inputs(w.with_(name="bwd_dh"), seed=1000)["V"]
+    t = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    dQ, dU, dV = pkg.backward(t["Q"], t["U"], t["V"], to_device(dH, w.dtype, torch), scale=w.scale)
+    torch.cuda.synchronize()
+    assert pkg.device_error() == 0
+    dQh, dVh, dUh = to_host64(dQ), to_host64(dV), to_host64(dU)
+    U = gen.to_float64(x["U"], w.dtype)
+
+    def one(s):
+        b, h = divmod(s, w.heads)
+        f = lambda a: gen.to_float64(a[b, h], w.dtype)
+        return s, orc.slice_backward(f(x["Q"]), U[h], f(x["V"]), f(dH), w.scale)
+
+    dU_ref = np.zeros(U.shape)
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as ex:
+        for s, (rq, ru, rv) in ex.map(one, range(w.slices)):
+            b, h = divmod(s, w.heads)
+            assert_parity(dQh[b, h], rq, w.dtype, f"{name} dQ slice ({b},{h})")
+            assert_parity(dVh[b, h], rv, w.dtype, f"{name} dV slice ({b},{h})")
+            dU_ref[h] += ru
+    assert_parity(dUh, dU_ref, w.dtype, f"{name} dU")
+
+
 def test_backward_bit_stable(env):
     pkg, torch, _ = env
-    got1, _, (t, tdH, sc) = _case(env, "bf16", 2, 3, 1500, 64, 64, seed=9)
-    got2 = pkg.backward(t["Q"], t["U"], t["V"], tdH, scale=sc)
-    torch.cuda.synchronize()
-    for a, b in zip(got1, got2):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for shape in [(2, 3, 1500, 64, 64), (2, 3, 1500, 100, 64)]:  # tensor-core and CUDA-core paths
+        got1, _, (t, tdH, sc) = _case(env, "bf16", *shape, seed=9)
+        got2 = pkg.backward(t["Q"], t["U"], t["V"], tdH, scale=sc)
+        torch.cuda.synchronize()
+        for a, b in zip(got1, got2):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 def test_backward_empty_and_rejected(env):
