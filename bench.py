@@ -412,7 +412,9 @@ def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dic
     """The backward (dQ, dU, dV for an upstream gradient dH) of one workload, timed like the
     forward (CUDA events on the launching stream, W untimed calls first).  Algorithmic work per
     slice: 18 n m d flops (three contractions to recompute A and the summaries, six in the
-    gradient pass) and 8 n d elements of traffic (Q, V, dH read twice, dQ and dV written)."""
+    gradient pass) and 5 n d elements of traffic (Q, V, dH read, dQ and dV written; U read and
+    dU written once per head).  bf16 with d = 64 and m <= 64 runs on the tensor cores (roofline:
+    the measured bf16 peak, and HBM), the rest on CUDA cores (roofline: the fp32 FMA peak)."""
     import torch
     hQ, hU, hV = hQUV
     Q, U, V = hQ.to(dev), hU.to(dev), hV.to(dev)
@@ -443,19 +445,26 @@ def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dic
     derr = pkg.device_error()
     call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     flops = 18 * w.slices * w.n * w.m * w.d
-    hbm = (8 * w.slices * w.n * w.d + 2 * w.heads * w.m * w.d) * w.elem_bytes
+    hbm = (5 * w.slices * w.n * w.d + 2 * w.heads * w.m * w.d) * w.elem_bytes
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fma_peak = sms * FMA_LANES_PER_SM * 2 * 2070e6 / 1e12
     peak, peak_src = peaks()
+    tensor = w.dtype == "bf16" and w.d == 64 and w.m <= 64
     rec = {"ms_per_call": call_ms, "value": w.slices * w.n / (call_ms / 1e3), "unit": UNIT, "steps": K,
-           "kernels_per_call": 2, "device_error": derr,
-           "fma_roofline": {"bound": "alu", "achieved": flops / (call_ms / 1e3) / 1e12, "peak": fma_peak,
-                            "unit": "TFLOP/s", "frac": flops / (call_ms / 1e3) / 1e12 / fma_peak,
-                            "peak_source": f"{sms} SMs x {FMA_LANES_PER_SM} fp32 FMA lanes x 2 flop x 2070 MHz",
-                            "flops_per_call": flops},
+           "kernels_per_call": 2, "device_error": derr, "path": "tensor" if tensor else "cuda_core",
            "hbm": {"achieved": hbm / (call_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                    "frac": hbm / (call_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_call": hbm,
                    "peak_source": f"{peak_src} hbm_gbs"}}
+    if tensor:
+        tpeak, tsrc = bf16_peak()
+        rec["tensor_roofline"] = {"bound": "tensor", "achieved": flops / (call_ms / 1e3) / 1e12, "peak": tpeak,
+                                  "unit": "TFLOP/s", "frac": flops / (call_ms / 1e3) / 1e12 / tpeak,
+                                  "peak_source": f"{tsrc} bf16_tflops (burst)", "flops_per_call": flops}
+    else:
+        rec["fma_roofline"] = {"bound": "alu", "achieved": flops / (call_ms / 1e3) / 1e12, "peak": fma_peak,
+                               "unit": "TFLOP/s", "frac": flops / (call_ms / 1e3) / 1e12 / fma_peak,
+                               "peak_source": f"{sms} SMs x {FMA_LANES_PER_SM} fp32 FMA lanes x 2 flop x 2070 MHz",
+                               "flops_per_call": flops}
     if derr:
         rec["invalid"] = f"device error word {derr:#x} after the timed calls"
     return rec

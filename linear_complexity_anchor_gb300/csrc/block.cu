@@ -15,7 +15,9 @@
 //   4    producer: TMA loads of U and of the projection operands (a two-stage ring of
 //        [X tile 0 | X tile 1 | Wq_h rows | Wv_h rows] 64-column chunks)
 //   5    MMA issuer (one thread): [Q|V]_t += X_t [Wq_h; Wv_h]^T (M = 128, N = 128, K = dm),
-//        S_t = Q_t U^T, W += A_t^T V_t and Delta += A_t^T 1, H_t = A_t W'
+//        S_t = Q_t U^T, [W | Delta] += A_t^T [V_t | 1], H_t = A_t W'
+// After the projection the steps go tile by tile (tile 0's S and W MMAs run while the row
+// warps convert and take the softmax of tile 1).
 // Tensor memory (256 columns): projections P_t = [Q_t | V_t] at 128 t; then S_t and H_t at
 // 64 t, W at 128, Delta at 192.  Every wait is bounded; a wait that gives up sets bit 0 of the
 // block error word and the CTA drains what it has in flight and leaves.
@@ -44,14 +46,13 @@ constexpr uint32_t kTmemCols = 256;
 constexpr int kTileB = kT * 64 * 2;                 // one 128 x 64 bf16 tile: 16 KB
 constexpr int kStageB = 3 * kTileB;                 // X tile 0 | X tile 1 | Wq rows | Wv rows
 constexpr int kRingB = 2 * kStageB;                 // 96 KB
-// after the projection the ring holds: Q_t / A_t at t * 16 KB, V_t at 32 KB + t * 16 KB, the
-// ones block and then the W' image at 64 KB, the H staging at 64 KB + (warp * 2 + t) * 4 KB
+// after the projection the ring holds: Q_t / A_t at t * 16 KB, V_t (then the H_t staging) at
+// 32 KB + t * 16 KB, the ones block [128][64] (16 KB) and then the W' image at 64 KB
 constexpr int kOffV = 2 * kTileB;
 constexpr int kOffW = 4 * kTileB;
-constexpr int kOffStage = 4 * kTileB;
 constexpr int kOffU = kRingB;                       // U [64][64] bf16, 8 KB
 constexpr int kOffBar = kOffU + kMP * kD * 2;
-constexpr int kBars = 15;
+constexpr int kBars = 20;
 constexpr int kSmem = kOffBar + kBars * 8 + 16 + 1024;  // + alignment slack
 
 struct BlockParams {
@@ -107,9 +108,10 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
     uint64_t *full = bars + 0, *empty = bars + 2;
-    uint64_t *proj_done = bars + 4, *qv_full = bars + 5, *u_full = bars + 6, *s_full = bars + 7;
-    uint64_t *a_full = bars + 8, *w_full = bars + 9, *wp_full = bars + 10, *h_full = bars + 11;
-    uint64_t *mma_done = bars + 12;
+    uint64_t *proj_done = bars + 4, *u_full = bars + 5, *w_full = bars + 6, *wp_full = bars + 7;
+    uint64_t *mma_done = bars + 8;
+    // per token tile t: qv_full + t (Q_t, V_t written), s_full + t, a_full + t, h_full + t
+    uint64_t *qv_full = bars + 9, *s_full = bars + 11, *a_full = bars + 13, *h_full = bars + 15;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + kBars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,14 +126,16 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
             mbar_init(empty + i, 1);
         }
         mbar_init(proj_done, 1);
-        mbar_init(qv_full, 4);
         mbar_init(u_full, 1);
-        mbar_init(s_full, 1);
-        mbar_init(a_full, 4);
         mbar_init(w_full, 1);
         mbar_init(wp_full, 4);
-        mbar_init(h_full, 1);
         mbar_init(mma_done, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(qv_full + t, 4);
+            mbar_init(s_full + t, 1);
+            mbar_init(a_full + t, 4);
+            mbar_init(h_full + t, 1);
+        }
         fence_mbar_init();
     }
     if (warp == kWarpMma) tmem_alloc(s_tmem, kTmemCols);
@@ -173,8 +177,7 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
         if (lane == 0) {
             const uint32_t kIdP = idesc_bf16_f32(kT, 2 * kD, false, false);  // [Q|V] += X [Wq; Wv]^T
             const uint32_t kIdS = idesc_bf16_f32(kT, kMP, false, false);     // S = Q U^T
-            const uint32_t kIdW = idesc_bf16_f32(kT, kD, true, true);        // W += A^T V
-            const uint32_t kIdDl = idesc_bf16_f32(kT, 16, true, false);      // Delta += A^T 1
+            const uint32_t kIdWD = idesc_bf16_f32(kT, kD + 16, true, true);  // [W | Delta] += A^T [V | 1]
             const uint32_t kIdH = idesc_bf16_f32(kT, kD, false, true);       // H = A W'
             bool ok = true;
             for (int kc = 0; kc < KC; ++kc) {
@@ -193,37 +196,33 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
                 umma_commit(empty + s);
             }
             if (ok) umma_commit(proj_done);
-            ok = ok && bwait(qv_full, 0u, p.wait_ns) && bwait(u_full, 0u, p.wait_ns);
-            if (ok) {
+            // tile by tile, so that tile 0's S and W run while the row warps work on tile 1
+            ok = ok && bwait(u_full, 0u, p.wait_ns);
+            const uint64_t udesc = smem_desc_sw128(sbase + kOffU, 16, 1024);
+            for (int t = 0; t < T && ok; ++t) {
+                if (!bwait(qv_full + t, 0u, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t udesc = smem_desc_sw128(sbase + kOffU, 16, 1024);
-                for (int t = 0; t < T; ++t) {
-                    const uint64_t qdesc = smem_desc_sw128(sbase + t * kTileB, 16, 1024);
+                const uint64_t qdesc = smem_desc_sw128(sbase + t * kTileB, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk)
-                        umma_bf16(tmem + t * 64, qdesc + (uint64_t)(kk * 2), udesc + (uint64_t)(kk * 2), kIdS,
-                                  kk > 0 ? 1u : 0u);
-                }
-                umma_commit(s_full);
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    umma_bf16(tmem + t * 64, qdesc + (uint64_t)(kk * 2), udesc + (uint64_t)(kk * 2), kIdS,
+                              kk > 0 ? 1u : 0u);
+                umma_commit(s_full + t);
             }
-            ok = ok && bwait(a_full, 0u, p.wait_ns);
-            if (ok) {
+            for (int t = 0; t < T && ok; ++t) {
+                if (!bwait(a_full + t, 0u, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t odesc = smem_desc_sw128(sbase + kOffW, 16, 1024);
-                for (int t = 0; t < T; ++t) {
-                    // A^T as the M = 128 operand: anchors 64..127 read the next 16 KB (never used)
-                    const uint64_t adesc = smem_desc_sw128(sbase + t * kTileB, kTileB, 1024);
-                    const uint64_t vdesc = smem_desc_sw128(sbase + kOffV + t * kTileB, kTileB, 1024);
+                // A^T as the M = 128 operand: anchors 64..127 read the next 16 KB (never used);
+                // [V | 1]: the ones block is the B operand's second 64-column block
+                const uint32_t va = sbase + kOffV + t * kTileB;
+                const uint64_t adesc = smem_desc_sw128(sbase + t * kTileB, kTileB, 1024);
+                const uint64_t vdesc = smem_desc_sw128(va, sbase + kOffW - va, 1024);
 #pragma unroll
-                    for (int kt = 0; kt < kT / 16; ++kt) {
-                        const uint32_t acc = (t > 0 || kt > 0) ? 1u : 0u;
-                        umma_bf16(tmem + 128, adesc + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), kIdW, acc);
-                        umma_bf16(tmem + 192, adesc + (uint64_t)(kt * 128),
-                                  odesc + (uint64_t)((((kt >> 2) * 2048) + (kt & 3) * 32) >> 4), kIdDl, acc);
-                    }
-                }
-                umma_commit(w_full);
+                for (int kt = 0; kt < kT / 16; ++kt)
+                    umma_bf16(tmem + 128, adesc + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), kIdWD,
+                              (t > 0 || kt > 0) ? 1u : 0u);
             }
+            if (ok) umma_commit(w_full);
             ok = ok && bwait(wp_full, 0u, p.wait_ns);
             if (ok) {
                 tc_fence_after();
@@ -234,8 +233,8 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
                     for (int kj = 0; kj < kMP / 16; ++kj)
                         umma_bf16(tmem + t * 64, adesc + (uint64_t)(kj * 2), wdesc + (uint64_t)(kj * 128), kIdH,
                                   kj > 0 ? 1u : 0u);
+                    umma_commit(h_full + t);
                 }
-                umma_commit(h_full);
             }
             // every MMA issued has completed before the CTA leaves
             umma_commit(mma_done);
@@ -264,45 +263,44 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8)
                     *reinterpret_cast<uint4 *>(sm + kOffV + t * kTileB + sw_off(row, c8, kT)) = pack8(v + 8 * c8, 1.f);
+                if (t == 0) {  // the ones block of [V | 1] ([128][64] bf16 ones, 16 KB)
+                    const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+                    for (int i = row; i < kTileB / 16; i += 128) reinterpret_cast<uint4 *>(sm + kOffW)[i] = ones;
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qv_full + t);
             }
-            // the ones block of the Delta MMA: [16][128] bf16 ones (4 KB)
-            const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-            for (int i = row; i < 256; i += 128) *reinterpret_cast<uint4 *>(sm + kOffW + i * 16) = ones;
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qv_full);
         }
-        ok = ok && bwait(s_full, 0u, p.wait_ns);
-        if (ok) {
+        for (int t = 0; t < T && ok; ++t) {
+            if (!bwait(s_full + t, 0u, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             float v[64];
-            for (int t = 0; t < T; ++t) {
-                tmem_ld32(trow + t * 64, v);
-                tmem_ld32(trow + t * 64 + 32, v + 32);
-                tmem_ld_wait();
-                // A_ij = 2^(c S_ij - max_j c S_ij) / sum; anchors >= m get 0; tokens >= n a zero row
-                float mx = -INFINITY;
+            tmem_ld32(trow + t * 64, v);
+            tmem_ld32(trow + t * 64 + 32, v + 32);
+            tmem_ld_wait();
+            // A_ij = 2^(c S_ij - max_j c S_ij) / sum; anchors >= m get 0; tokens >= n a zero row
+            float mx = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    v[j] = j < p.m ? v[j] * p.c : -INFINITY;
-                    mx = fmaxf(mx, v[j]);
-                }
-                float z = 0.f;
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    v[j] = ex2(v[j] - mx);
-                    z += v[j];
-                }
-                const float r = t * kT + row < p.n ? 1.f / z : 0.f;
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    *reinterpret_cast<uint4 *>(sm + t * kTileB + sw_off(row, c8, kT)) = pack8(v + 8 * c8, r);
+            for (int j = 0; j < 64; ++j) {
+                v[j] = j < p.m ? v[j] * p.c : -INFINITY;
+                mx = fmaxf(mx, v[j]);
             }
+            float z = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                v[j] = ex2(v[j] - mx);
+                z += v[j];
+            }
+            const float r = t * kT + row < p.n ? 1.f / z : 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                *reinterpret_cast<uint4 *>(sm + t * kTileB + sw_off(row, c8, kT)) = pack8(v + 8 * c8, r);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(a_full);
+            if (lane == 0) mbar_arrive(a_full + t);
         }
         ok = ok && bwait(w_full, 0u, p.wait_ns);
         if (ok) {
@@ -323,16 +321,18 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
             __syncwarp();
             if (lane == 0) mbar_arrive(wp_full);
         }
-        ok = ok && bwait(h_full, 0u, p.wait_ns);
         if (ok) {
-            tc_fence_after();
             const uint64_t pol_out = policy_evict_first();
             float v[64];
             for (int t = 0; t < T; ++t) {
+                if (!bwait(h_full + t, 0u, p.wait_ns)) break;
+                tc_fence_after();
                 tmem_ld32(trow + t * 64, v);
                 tmem_ld32(trow + t * 64 + 32, v + 32);
                 tmem_ld_wait();
-                uint8_t *stage = sm + kOffStage + (warp * 2 + t) * 4096;
+                // staged over V_t (free since the W MMAs; the H MMA of the other tile may still
+                // be reading A and W')
+                uint8_t *stage = sm + kOffV + t * kTileB + warp * 4096;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8)
                     *reinterpret_cast<uint4 *>(stage + sw_off(lane, c8, 32)) = pack8(v + 8 * c8, 1.f);
