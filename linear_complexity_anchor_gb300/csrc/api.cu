@@ -150,8 +150,16 @@ anchor_attn_status_t causal_forward(const Problem &p, void *stream_v) {
     const anchor_attn_status_t st = anchor::check_problem(p);
     if (st != ANCHOR_ATTN_OK) return st;
     if (p.slices() == 0 || p.n == 0) return ANCHOR_ATTN_OK;
-    if (!anchor::causal_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
     cudaStream_t stream = (cudaStream_t)stream_v;
+    if (anchor::causal_tc_supported(p)) {
+        if (p.slices() > 0x7fffffffLL) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+        if (anchor::launch_causal_tc(p, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return ANCHOR_ATTN_ERR_CUDA;
+        }
+        return ANCHOR_ATTN_OK;
+    }
+    if (!anchor::causal_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
     void *ws = nullptr;
     if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
     if (cudaMallocAsync(&ws, anchor::causal_layout(p).total_bytes, stream) != cudaSuccess) {
@@ -370,15 +378,15 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
         anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess ||
         anchor::causal_read_and_clear_error(&e) != cudaSuccess || anchor::block_read_and_clear_error(&f) != cudaSuccess ||
-        anchor::bwd_tc_read_and_clear_error(&g) != cudaSuccess) {
+        anchor::bwd_tc_read_and_clear_error(&g) != cudaSuccess || anchor::causal_tc_read_and_clear_error(&k) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b | c | e | f | g;
+    *code = a | b | c | e | f | g | k;
     return ANCHOR_ATTN_OK;
 }
 

@@ -105,6 +105,10 @@ bool causal_fits(const Problem &p);
 CausalLayout causal_layout(const Problem &p);
 cudaError_t launch_causal(const Problem &p, void *workspace, cudaStream_t stream);
 cudaError_t causal_read_and_clear_error(unsigned *out);
+// the masked variant on the tensor cores (bf16, d = 64, m <= 64; no workspace)
+bool causal_tc_supported(const Problem &p);
+cudaError_t launch_causal_tc(const Problem &p, cudaStream_t stream);
+cudaError_t causal_tc_read_and_clear_error(unsigned *out);
 
 // --- approximation-error diagnostic ------------------------------------------------------
 struct FullProblem {

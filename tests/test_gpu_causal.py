@@ -1,6 +1,10 @@
 """GPU: the masked (causal) variant through the C ABI against the oracle's, element by element,
 plus the properties that hold at any size: the last row equals the unmasked forward's, the
-first row is its own value, and changing later tokens leaves earlier rows unchanged."""
+first row is its own value, and changing later tokens leaves earlier rows unchanged.  bf16 with
+d = 64 and m <= 64 runs on the tensor cores; the rest, and fp32, on CUDA cores."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 
@@ -58,3 +62,51 @@ def test_causal_ignores_later_tokens(env):
     torch.cuda.synchronize()
     assert torch.equal(H1[:, :, :900].view(torch.int16), H2[:, :, :900].view(torch.int16))
     assert not torch.equal(H1[:, :, 900:], H2[:, :, 900:])
+
+
+# tensor-core path: one token; exactly one tile; a second tile of one token; a long slice; one
+# anchor; a scale of either sign
+_TC_SHAPES = [(3, 2, 1, 5, 64, None), (2, 2, 128, 64, 64, None), (1, 2, 129, 33, 64, None), (1, 1, 2000, 64, 64, None),
+              (2, 2, 300, 1, 64, None), (1, 2, 250, 40, 64, -0.2), (2, 1, 400, 64, 64, 0.0)]
+
+
+@pytest.mark.parametrize("shape", _TC_SHAPES)
+def test_causal_tensor_core_shapes(env, shape):
+    pkg, torch, orc = env
+    *dims, scale = shape
+    w = _w("bf16", *dims)
+    sc = w.scale if scale is None else scale
+    x = gen.make_inputs(w, seed=sum(dims) + 3)
+    t = {k: to_device(x[k], "bf16", torch) for k in "QUV"}
+    H = pkg.causal_forward(t["Q"], t["U"], t["V"], scale=sc)
+    torch.cuda.synchronize()
+    xx = widen(x, "bf16")
+    assert_parity(to_host64(H), orc.causal(xx["Q"], xx["U"], xx["V"], sc), "bf16", f"causal {shape}")
+    assert pkg.device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["deit_base", "det_800x1344"])
+def test_causal_workload_every_slice(env, name):
+    """Full size, every slice against the oracle (one slice per host core), and bit-stable."""
+    pkg, torch, orc = env
+    w = gen.WORKLOADS[name]
+    x = gen.make_inputs(w, seed=0)
+    t = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    H = pkg.causal_forward(t["Q"], t["U"], t["V"], scale=w.scale)
+    H2 = pkg.causal_forward(t["Q"], t["U"], t["V"], scale=w.scale)
+    torch.cuda.synchronize()
+    assert pkg.device_error() == 0
+    assert torch.equal(H.view(torch.int16), H2.view(torch.int16))
+    Hh = to_host64(H)
+    U = gen.to_float64(x["U"], w.dtype)
+
+    def one(s):
+        b, h = divmod(s, w.heads)
+        q = gen.to_float64(x["Q"][b, h], w.dtype)[None, None]
+        v = gen.to_float64(x["V"][b, h], w.dtype)[None, None]
+        return s, orc.causal(q, U[h:h + 1], v, w.scale)[0, 0]
+
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as ex:
+        for s, ref in ex.map(one, range(w.slices)):
+            b, h = divmod(s, w.heads)
+            assert_parity(Hh[b, h], ref, w.dtype, f"{name} causal slice ({b},{h})")
