@@ -472,8 +472,9 @@ def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dic
 
 def time_causal(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
     """The masked (causal) variant of one workload, timed like the forward.  Algorithmic
-    traffic as the forward's (Q, V and H once, U once); work about 4 n m d flops for A and the
-    summaries plus 2 n m d + 2 n TR (m + d) for the rows, counted here as 6 n m d."""
+    traffic as the forward's (Q, V and H once, U once), the roofline of the tensor-core path
+    (bf16, d = 64, m <= 64); the CUDA-core path also reports its FMA rate, counting the work as
+    the forward's 6 n m d."""
     import torch
     hQ, hU, hV = hQUV
     Q, U, V = hQ.to(dev), hU.to(dev), hV.to(dev)
@@ -504,12 +505,14 @@ def time_causal(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
     derr = pkg.device_error()
     call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     peak, peak_src = peaks()
+    tensor = w.dtype == "bf16" and w.d == 64 and w.m <= 64
     rec = {"ms_per_call": call_ms, "value": w.slices * w.n / (call_ms / 1e3), "unit": UNIT, "steps": K,
-           "kernels_per_call": 1, "device_error": derr,
+           "kernels_per_call": 1, "device_error": derr, "path": "tensor" if tensor else "cuda_core",
            "hbm": {"achieved": w.algorithmic_bytes / (call_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                    "frac": w.algorithmic_bytes / (call_ms / 1e3) / 1e9 / peak,
-                   "algorithmic_bytes_per_call": w.algorithmic_bytes, "peak_source": f"{peak_src} hbm_gbs"},
-           "fma_roofline": fma_roofline(w, call_ms, None, dev)}
+                   "algorithmic_bytes_per_call": w.algorithmic_bytes, "peak_source": f"{peak_src} hbm_gbs"}}
+    if not tensor:
+        rec["fma_roofline"] = fma_roofline(w, call_ms, None, dev)
     if derr:
         rec["invalid"] = f"device error word {derr:#x} after the timed calls"
     return rec

@@ -65,9 +65,22 @@ struct Plan {
     size_t workspace = 0;
 };
 
+// The slice-streaming variant takes bf16 problems with d = 64 and 32 <= m <= 64 whose slices are
+// long (n > 512): one CTA per slice needs no cross-CTA reduction there; short slices go to
+// the persistent tensor-core variant, which packs several into one CTA.
+bool stream_plan(const Problem &p) { return anchor::stream_supported(p) && p.m >= 32 && p.n > 512; }
+
 Plan make_plan(const Problem &p) {
     Plan pl;
     if (p.slices() == 0 || p.n == 0) return pl;
+    if (stream_plan(p) && p.slices() <= 0x7fffffffLL) {
+        pl.variant = ANCHOR_ATTN_VARIANT_STREAM;
+        pl.kernels = 1;
+        pl.splits = 1;
+        pl.flags = ANCHOR_ATTN_PLAN_STORED_A;
+        pl.workspace = anchor::stream_workspace(p);
+        return pl;
+    }
     if (anchor::umma_supported(p)) {
         const anchor::UmmaPlan u = anchor::umma_plan(p);
         pl.variant = ANCHOR_ATTN_VARIANT_UMMA;
@@ -103,8 +116,11 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
     if (p.slices() == 0 || p.n == 0) return ANCHOR_ATTN_OK;
 
     cudaStream_t stream = (cudaStream_t)stream_v;
-    const Plan pl = make_plan(p);
-    if (test && pl.variant != ANCHOR_ATTN_VARIANT_UMMA) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    Plan pl = make_plan(p);
+    if (test) {  // the failure-detection test entry always runs the persistent tensor-core variant
+        if (!anchor::umma_supported(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+        pl.variant = ANCHOR_ATTN_VARIANT_UMMA;
+    }
     cudaError_t e = cudaSuccess;
     switch (pl.variant) {
     case ANCHOR_ATTN_VARIANT_SIMT_SLICE:
@@ -118,6 +134,18 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
             return ANCHOR_ATTN_ERR_ALLOC;
         }
         e = anchor::launch_simt_chunk(p, ws, stream);
+        const cudaError_t ef = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess) e = ef;
+        break;
+    }
+    case ANCHOR_ATTN_VARIANT_STREAM: {
+        void *ws = nullptr;
+        if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
+        if (cudaMallocAsync(&ws, pl.workspace, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return ANCHOR_ATTN_ERR_ALLOC;
+        }
+        e = anchor::launch_stream(p, ws, stream);
         const cudaError_t ef = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = ef;
         break;
@@ -378,15 +406,16 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0, l = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
         anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess ||
         anchor::causal_read_and_clear_error(&e) != cudaSuccess || anchor::block_read_and_clear_error(&f) != cudaSuccess ||
-        anchor::bwd_tc_read_and_clear_error(&g) != cudaSuccess || anchor::causal_tc_read_and_clear_error(&k) != cudaSuccess) {
+        anchor::bwd_tc_read_and_clear_error(&g) != cudaSuccess || anchor::causal_tc_read_and_clear_error(&k) != cudaSuccess ||
+        anchor::stream_read_and_clear_error(&l) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b | c | e | f | g | k;
+    *code = a | b | c | e | f | g | k | l;
     return ANCHOR_ATTN_OK;
 }
 

@@ -139,6 +139,13 @@ cudaError_t block_read_and_clear_error(unsigned *out);
 // 3-D bf16 tensor map [outer][rows][cols], box 64 columns x box_rows rows x 1, 128-byte swizzle
 bool make_bf16_map(CUtensorMap *map, const void *base, int cols, int rows, long long outer, int box_rows);
 
+// --- slice-streaming tensor-core variant (d = 64, m <= 64): one CTA per slice ----------------
+// workspace: the A tiles of pass 1, [slices][n][64] bf16
+bool stream_supported(const Problem &p);
+size_t stream_workspace(const Problem &p);
+cudaError_t launch_stream(const Problem &p, void *workspace, cudaStream_t stream);
+cudaError_t stream_read_and_clear_error(unsigned *out);
+
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA
 constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)

@@ -59,7 +59,7 @@ def test_recompute_plan_matches_oracle_and_stored_plan(env, shape):
     pkg, torch, orc = env
     w = _w(*shape)
     plan = pkg.query_plan("bf16", *shape)
-    assert plan["variant"] == "umma"
+    assert plan["variant"] in ("umma", "stream")
     x = gen.make_inputs(w, seed=sum(shape))
     t = {k: to_device(x[k], "bf16", torch) for k in "QUV"}
     H = torch.full_like(t["Q"], float("nan"))
@@ -68,8 +68,11 @@ def test_recompute_plan_matches_oracle_and_stored_plan(env, shape):
     _oracle_slices(orc, x, w, H, range(w.slices), "recompute")
     H2 = pkg.forward(t["Q"], t["U"], t["V"], scale=w.scale)
     torch.cuda.synchronize()
-    assert torch.equal(H.view(torch.int16), H2.view(torch.int16)), \
-        f"recompute and {'stored' if plan['stored_a'] else 'default'} plans differ"
+    if plan["variant"] == "umma":
+        assert torch.equal(H.view(torch.int16), H2.view(torch.int16)), \
+            f"recompute and {'stored' if plan['stored_a'] else 'default'} plans differ"
+    else:  # another kernel and summation order: against the oracle instead
+        _oracle_slices(orc, x, w, H2, range(w.slices), "stream")
 
 
 def test_workload_plans(env):
