@@ -27,6 +27,7 @@
 // backward's error word and the CTA drains what it has in flight and leaves.
 #include "common.cuh"
 #include "ptx.cuh"
+#include "rowops.cuh"
 
 #include <math.h>
 
@@ -92,11 +93,6 @@ __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
     hi = pack8(x, 1.f);
     lo = pack8(r, 1.f);
 }
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limit_ns) {
     if (mbar_try_wait(bar, par)) return true;
@@ -112,21 +108,8 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limi
 
 // row softmax of 64 scores (anchors >= m masked), in place; a row past the slice is all zero
 __device__ __forceinline__ void softmax64(float (&v)[64], int m, float c, bool valid) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-        v[j] = j < m ? v[j] * c : -INFINITY;
-        mx = fmaxf(mx, v[j]);
-    }
-    float z = 0.f;
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-        v[j] = ex2(v[j] - mx);
-        z += v[j];
-    }
-    const float r = valid ? 1.f / z : 0.f;
-#pragma unroll
-    for (int j = 0; j < 64; ++j) v[j] *= r;
+    const float z = rowops::softmax64_unnormalised(v, m, c);
+    rowops::scale64(v, valid ? 1.f / z : 0.f);
 }
 
 // a row of 64 fp32 values as hi and lo bf16 rows of a swizzled [rows][64] tile
@@ -443,12 +426,9 @@ anchor_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             }
             softmax64(v, p.m, p.c, t * kT + row < p.n);
             // dS_j = A_j (G_j + dDelta_j - sum_l A_l (G_l + dDelta_l))
-            float rs = 0.f;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                g[j] += sDD[j];
-                rs = fmaf(v[j], g[j], rs);
-            }
+            for (int j = 0; j < 64; ++j) g[j] += sDD[j];
+            const float rs = rowops::dot64(v, g);
 #pragma unroll
             for (int j = 0; j < 64; ++j) g[j] = v[j] * (g[j] - rs);
             if (t >= 1 && !bwait(ds_empty, (uint32_t)((t - 1) & 1), p.wait_ns)) { ok = false; break; }

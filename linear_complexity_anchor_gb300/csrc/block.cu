@@ -23,6 +23,7 @@
 // block error word and the CTA drains what it has in flight and leaves.
 #include "common.cuh"
 #include "ptx.cuh"
+#include "rowops.cuh"
 
 #include <math.h>
 
@@ -75,11 +76,6 @@ __device__ __forceinline__ uint4 pack8(const float *x, float r) {
                       pack2(x[6] * r, x[7] * r));
 }
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 __device__ __forceinline__ uint64_t policy_evict_normal() {
     uint64_t p;
@@ -281,22 +277,11 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
             tmem_ld32(trow + t * 64 + 32, v + 32);
             tmem_ld_wait();
             // A_ij = 2^(c S_ij - max_j c S_ij) / sum; anchors >= m get 0; tokens >= n a zero row
-            float mx = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                v[j] = j < p.m ? v[j] * p.c : -INFINITY;
-                mx = fmaxf(mx, v[j]);
-            }
-            float z = 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                v[j] = ex2(v[j] - mx);
-                z += v[j];
-            }
-            const float r = t * kT + row < p.n ? 1.f / z : 0.f;
+            const float z = rowops::softmax64_unnormalised(v, p.m, p.c);
+            rowops::scale64(v, t * kT + row < p.n ? 1.f / z : 0.f);
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
-                *reinterpret_cast<uint4 *>(sm + t * kTileB + sw_off(row, c8, kT)) = pack8(v + 8 * c8, r);
+                *reinterpret_cast<uint4 *>(sm + t * kTileB + sw_off(row, c8, kT)) = pack8(v + 8 * c8, 1.f);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();

@@ -22,6 +22,7 @@
 // what it has in flight and leaves.
 #include "common.cuh"
 #include "ptx.cuh"
+#include "rowops.cuh"
 
 #include <math.h>
 
@@ -71,11 +72,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 }
 __device__ __forceinline__ uint4 pack8(const float *x) {
     return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
-}
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limit_ns) {
@@ -276,21 +272,8 @@ anchor_causal_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty + s);
             {
-                float mx = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    a[j] = j < p.m ? a[j] * p.c : -INFINITY;
-                    mx = fmaxf(mx, a[j]);
-                }
-                float z = 0.f;
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    a[j] = ex2(a[j] - mx);
-                    z += a[j];
-                }
-                const float r = valid ? 1.f / z : 0.f;
-#pragma unroll
-                for (int j = 0; j < 64; ++j) a[j] *= r;
+                const float z = rowops::softmax64_unnormalised(a, p.m, p.c);
+                rowops::scale64(a, valid ? 1.f / z : 0.f);
             }
             // the tile before has finished with A, B, P and has added itself to W_pre: the
             // W_pre image for this tile (anchor rows, warps 0 and 1)
@@ -329,7 +312,7 @@ anchor_causal_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     cr[j] = __fadd_rn(dp[j], cr[j]);
-                    a[j] = cr[j] != 0.f ? __fdiv_rn(a[j], cr[j]) : 0.f;
+                    a[j] = cr[j] != 0.f ? __fdividef(a[j], cr[j]) : 0.f;  // rounded to bf16 next
                 }
                 if (row == kT - 1)  // the whole tile: the next tile's Delta_pre
 #pragma unroll

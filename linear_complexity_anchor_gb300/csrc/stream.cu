@@ -6,17 +6,21 @@
 //
 // Pass 1 walks the slice's 128-token tiles: S_t = Q_t U^T, A_t = softmax (row warps, bf16),
 // [W | Delta] += A_t^T [V_t | 1]; each A_t tile also goes to a workspace by TMA (it stays in
-// L2).  Then W' = Delta^{-1} W.  Pass 2 loads the A tiles back and forms H_t = A_t W', stored
+// L2).  With one CTA per slice only as many SMs as slices stream, so each CTA keeps as many
+// bytes in flight as its shared memory allows (eight 16 KB ring slots).  Then W' = Delta^{-1} W.  Pass 2 loads the A tiles back and forms H_t = A_t W', stored
 // by TMA.  No other CTA takes part in a slice, so nothing waits on another CTA: the whole
 // slice's sums run in one tensor-memory accumulator in tile order (bit-identical from run to
 // run).
 // Warps: 0-7 row warps in two groups that take alternate tiles (group g = warp / 4 owns TMEM
-// lanes 32 (warp % 4) + [0, 32) of its own S and H buffers); 8 producer (a four-slot TMA
-// ring: [Q_t | V_t] in pass 1, A_t in pass 2); 9 MMA issuer.  Every wait is bounded; one that
-// gives up sets bit 0 of this kernel's error word and the CTA drains what it has in flight
-// and leaves.
+// lanes 32 (warp % 4) + [0, 32) of its own S and H buffers); 8 and 10 producers, each with
+// its own four-slot TMA ring (warp 8: Q_t in pass 1, then A_t in pass 2; warp 10: V_t): a Q
+// slot is free again as soon as S_t has read it, so the Q loads run further ahead of their
+// use than a shared [Q | V] slot, which only the later W MMA frees, would allow; 9 MMA
+// issuer.  Every wait is bounded; one that gives up sets bit 0 of this kernel's error word
+// and the CTA drains what it has in flight and leaves.
 #include "common.cuh"
 #include "ptx.cuh"
+#include "rowops.cuh"
 
 #include <math.h>
 
@@ -29,25 +33,27 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 128, kD = 64, kMP = 64;
-constexpr int kThreads = 320;
-constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr int kThreads = 352;
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpProducerV = 10;
 constexpr int kSlots = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTileB = kT * 64 * 2;   // a [128][64] bf16 tile (16 KB)
-constexpr int kSlotB = 2 * kTileB;    // Q_t | V_t (pass 1), A_t (pass 2)
+
 constexpr int kImgB = kMP * kD * 2;
-// shared memory
-constexpr int kOffOnes = kSlots * kSlotB;      // [128][64] bf16 ones: the second block of [V | 1]
-constexpr int kOffU = kOffOnes + kTileB;       // U [64][64]
-constexpr int kOffA = kOffU + kImgB;           // A tiles of the two groups; the second one's unused
-                                               // M block (W MMA) reads the W' image and staging
-constexpr int kOffW = kOffA + 2 * kTileB;      // W' image [64][64]
-constexpr int kOffStage = kOffW + kImgB;       // H staging: 4 KB per row warp
-constexpr int kOffBar = kOffStage + 8 * 4096;
-constexpr int kBars = 32;
+// shared memory (an MN-major M = 128 operand reads an unused second 64-row block 16 KB on:
+// A tile 1's is the first Q slot)
+constexpr int kOffA = 0;                             // A tiles of the two row-warp groups
+constexpr int kOffQRing = kOffA + 2 * kTileB;        // Q ring: Q_t in pass 1, then A_t in pass 2
+constexpr int kOffVRing = kOffQRing + kSlots * kTileB;  // V ring; in pass 2 the H staging (4 KB per row warp)
+constexpr int kOffOnes = kOffVRing + kSlots * kTileB;   // [128][64] bf16 ones: the second block of [V | 1]
+constexpr int kOffU = kOffOnes + kTileB;             // U [64][64]
+constexpr int kOffW = kOffU + kImgB;                 // W' image [64][64]
+constexpr int kOffStage = kOffVRing;
+constexpr int kOffBar = kOffW + kImgB;
+constexpr int kBars = 4 * kSlots + 20;
 constexpr int kSmem = kOffBar + kBars * 8 + 16 + 1024;
 static_assert(kSmem <= 227 * 1024, "shared memory");
-// tensor memory: S_g at 64 g, [W | Delta] at 128, H_g at 256 + 64 g
+// tensor memory: S_g at 64 g, [W | Delta] at 128, H of group g, buffer b at 256 + 64 (2 g + b)
 constexpr uint32_t kColS = 0, kColW = 128, kColDelta = 192, kColH = 256;
 
 struct StParams {
@@ -63,14 +69,12 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
+}
 __device__ __forceinline__ uint4 pack8(const float *x, float r) {
     return make_uint4(pack2(x[0] * r, x[1] * r), pack2(x[2] * r, x[3] * r), pack2(x[4] * r, x[5] * r),
                       pack2(x[6] * r, x[7] * r));
-}
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limit_ns) {
@@ -93,10 +97,10 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
-    uint64_t *full = bars + 0, *empty = bars + kSlots;
-    uint64_t *s_full = bars + 8, *s_empty = bars + 10, *a_full = bars + 12, *a_empty = bars + 14;
-    uint64_t *h_full = bars + 16, *h_empty = bars + 18;
-    uint64_t *u_full = bars + 20, *w_full = bars + 21, *wp_full = bars + 22, *mma_done = bars + 23;
+    uint64_t *full = bars, *empty = full + kSlots, *vfull = empty + kSlots, *vempty = vfull + kSlots;
+    uint64_t *s_full = vempty + kSlots, *s_empty = s_full + 2, *a_full = s_full + 4, *a_empty = s_full + 6;
+    uint64_t *u_full = s_full + 8, *w_full = s_full + 9, *wp_full = s_full + 10, *mma_done = s_full + 11;
+    uint64_t *h_full = s_full + 12, *h_empty = s_full + 16;  // [2 g + b]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + kBars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,14 +112,18 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(full + i, 1);
             mbar_init(empty + i, 1);
+            mbar_init(vfull + i, 1);
+            mbar_init(vempty + i, 1);
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(s_full + g, 1);
             mbar_init(s_empty + g, 4);
             mbar_init(a_full + g, 4);
             mbar_init(a_empty + g, 1);
-            mbar_init(h_full + g, 1);
-            mbar_init(h_empty + g, 4);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(h_full + i, 1);
+            mbar_init(h_empty + i, 4);
         }
         mbar_init(u_full, 1);
         mbar_init(w_full, 1);
@@ -138,26 +146,23 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     if (warp == kWarpProducer) {
         if (lane == 0) {
             tma_prefetch_desc(&tq);
-            tma_prefetch_desc(&tv);
             tma_prefetch_desc(&tu);
             tma_prefetch_desc(&ta_ld);
             const uint64_t pol_once = policy_evict_first(), pol_keep = policy_evict_last();
             mbar_arrive_expect_tx(u_full, kImgB);
             tma_load_3d(sm + kOffU, &tu, u_full, 0, 0, h, pol_keep);
             int issued = 0;
-            bool ok = true;
-            for (int seq = 0; seq < 2 * T && ok; ++seq) {
+            for (int seq = 0; seq < 2 * T; ++seq) {
                 const int s = seq % kSlots;
                 if (seq >= kSlots && !bwait(empty + s, (uint32_t)(((seq / kSlots) - 1) & 1), p.wait_ns)) break;
-                uint8_t *st = sm + s * kSlotB;
+                uint8_t *st = sm + kOffQRing + s * kTileB;
                 if (seq < T) {
-                    mbar_arrive_expect_tx(full + s, 2 * kTileB);
+                    mbar_arrive_expect_tx(full + s, kTileB);
                     tma_load_3d(st, &tq, full + s, 0, seq * kT, slice, pol_once);
-                    tma_load_3d(st + kTileB, &tv, full + s, 0, seq * kT, slice, pol_once);
                 } else {
                     // pass 2: every A tile has been stored (the row warps finish their stores
                     // before they arrive on wp_full)
-                    if (seq == T && !bwait(wp_full, 0u, p.wait_ns)) { ok = false; break; }
+                    if (seq == T && !bwait(wp_full, 0u, p.wait_ns)) break;
                     mbar_arrive_expect_tx(full + s, kTileB);
                     tma_load_3d(st, &ta_ld, full + s, 0, (seq - T) * kT, slice, pol_once);
                 }
@@ -168,6 +173,24 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 if (loads > 0) bwait(full + s, (uint32_t)((loads - 1) & 1), p.wait_ns);
             }
             bwait(u_full, 0u, p.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == kWarpProducerV) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tv);
+            const uint64_t pol_once = policy_evict_first();
+            int issued = 0;
+            for (int t = 0; t < T; ++t) {
+                const int s = t % kSlots;
+                if (t >= kSlots && !bwait(vempty + s, (uint32_t)(((t / kSlots) - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(vfull + s, kTileB);
+                tma_load_3d(sm + kOffVRing + s * kTileB, &tv, vfull + s, 0, t * kT, slice, pol_once);
+                ++issued;
+            }
+            for (int s = 0; s < kSlots; ++s) {
+                const int loads = issued > s ? (issued - s + kSlots - 1) / kSlots : 0;
+                if (loads > 0) bwait(vfull + s, (uint32_t)((loads - 1) & 1), p.wait_ns);
+            }
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -183,45 +206,53 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 if (!bwait(full + s, (uint32_t)((t / kSlots) & 1), p.wait_ns)) return false;
                 if (t >= 2 && !bwait(s_empty + g, (uint32_t)(((t >> 1) - 1) & 1), p.wait_ns)) return false;
                 tc_fence_after();
-                const uint64_t qdesc = smem_desc_sw128(sbase + s * kSlotB, 16, 1024);
+                const uint64_t qdesc = smem_desc_sw128(sbase + kOffQRing + s * kTileB, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     umma_bf16(tmem + kColS + g * 64, qdesc + (uint64_t)(kk * 2), udesc + (uint64_t)(kk * 2), idS,
                               kk > 0 ? 1u : 0u);
                 umma_commit(s_full + g);
+                umma_commit(empty + s);  // Q_t has been read
                 return true;
             };
-            // pass 1: S two tiles ahead of the W MMAs (one S buffer per row-warp group)
+            // pass 1: S two tiles ahead of the W MMAs (one S buffer per row-warp group); S_{t+2}
+            // needs only its group's S buffer read, which happens before the group's softmax
+            // of tile t, so it goes in ahead of W_t
             for (int t = 0; t < 2 && t < T && ok; ++t) ok = issue_s(t);
             for (int t = 0; t < T && ok; ++t) {
                 const int s = t % kSlots, g = t & 1;
-                if (!bwait(a_full + g, (uint32_t)((t >> 1) & 1), p.wait_ns)) { ok = false; break; }
+                if (t + 2 < T && !issue_s(t + 2)) { ok = false; break; }
+                if (!bwait(a_full + g, (uint32_t)((t >> 1) & 1), p.wait_ns) ||
+                    !bwait(vfull + s, (uint32_t)((t / kSlots) & 1), p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t va = sbase + s * kSlotB + kTileB;
+                const uint32_t va = sbase + kOffVRing + s * kTileB;
                 const uint64_t adesc = smem_desc_sw128(sbase + kOffA + g * kTileB, kTileB, 1024);
+                // [V | 1]: the ones block is the B operand's second 64-column block
                 const uint64_t vdesc = smem_desc_sw128(va, sbase + kOffOnes - va, 1024);
 #pragma unroll
                 for (int kt = 0; kt < kT / 16; ++kt)
                     umma_bf16(tmem + kColW, adesc + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), idWD,
                               (t > 0 || kt > 0) ? 1u : 0u);
                 umma_commit(a_empty + g);
-                umma_commit(empty + s);
-                if (t + 2 < T && !issue_s(t + 2)) { ok = false; break; }
+                umma_commit(vempty + s);
             }
             if (ok) umma_commit(w_full);
             // pass 2: H_t = A_t W'
             ok = ok && bwait(wp_full, 0u, p.wait_ns);
             for (int t = 0; t < T && ok; ++t) {
-                const int seq = T + t, s = seq % kSlots, g = t & 1;
+                const int seq = T + t, s = seq % kSlots, hb = 2 * (t & 1) + ((t >> 1) & 1);  // H buffer (g, b)
                 if (!bwait(full + s, (uint32_t)((seq / kSlots) & 1), p.wait_ns)) { ok = false; break; }
-                if (t >= 2 && !bwait(h_empty + g, (uint32_t)(((t >> 1) - 1) & 1), p.wait_ns)) { ok = false; break; }
+                if (t >= 4 && !bwait(h_empty + hb, (uint32_t)(((t >> 2) - 1) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t adesc = smem_desc_sw128(sbase + s * kSlotB, 16, 1024);
+                const uint64_t adesc = smem_desc_sw128(sbase + kOffQRing + s * kTileB, 16, 1024);
 #pragma unroll
                 for (int kj = 0; kj < kMP / 16; ++kj)
-                    umma_bf16(tmem + kColH + g * 64, adesc + (uint64_t)(kj * 2), wdesc + (uint64_t)(kj * 128), idH,
+                    umma_bf16(tmem + kColH + hb * 64, adesc + (uint64_t)(kj * 2), wdesc + (uint64_t)(kj * 128), idH,
                               kj > 0 ? 1u : 0u);
-                umma_commit(h_full + g);
+                umma_commit(h_full + hb);
                 umma_commit(empty + s);
             }
             umma_commit(mma_done);
@@ -247,26 +278,15 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty + g);
             // A_ij = 2^(c S_ij - max_j c S_ij) / sum; anchors >= m get 0; tokens >= n a zero row
-            float mx = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                v[j] = j < p.m ? v[j] * p.c : -INFINITY;
-                mx = fmaxf(mx, v[j]);
-            }
-            float z = 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                v[j] = ex2(v[j] - mx);
-                z += v[j];
-            }
-            const float r = t * kT + row < p.n ? 1.f / z : 0.f;
+            const float z = rowops::softmax64_unnormalised(v, p.m, p.c);
+            rowops::scale64(v, t * kT + row < p.n ? 1.f / z : 0.f);
             // the group's A buffer: the W MMA of its previous tile has read it, and so has
             // this warp's TMA store of it
             if (k >= 1 && !bwait(a_empty + g, (uint32_t)((k - 1) & 1), p.wait_ns)) { ok = false; break; }
             if (lane == 0) bulk_wait_group_read0();
             __syncwarp();
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(sA + sw_off(row, c8, kT)) = pack8(v + 8 * c8, r);
+            for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4 *>(sA + sw_off(row, c8, kT)) = pack8(v + 8 * c8);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -306,21 +326,22 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         // pass 2: H tiles out
         uint8_t *stage = sm + kOffStage + warp * 4096;
         for (int t = g, k = 0; t < T && ok; t += 2, ++k) {
-            if (!bwait(h_full + g, (uint32_t)(k & 1), p.wait_ns)) { ok = false; break; }
+            const int hb = 2 * g + (k & 1);
+            if (!bwait(h_full + hb, (uint32_t)((k >> 1) & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
-            tmem_ld32(trow + kColH + g * 64, v);
-            tmem_ld32(trow + kColH + g * 64 + 32, v + 32);
+            tmem_ld32(trow + kColH + hb * 64, v);
+            tmem_ld32(trow + kColH + hb * 64 + 32, v + 32);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(h_empty + g);
+                mbar_arrive(h_empty + hb);
                 bulk_wait_group_read0();  // the last store has read the staging
             }
             __syncwarp();
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
-                *reinterpret_cast<uint4 *>(stage + sw_off(lane, c8, 32)) = pack8(v + 8 * c8, 1.f);
+                *reinterpret_cast<uint4 *>(stage + sw_off(lane, c8, 32)) = pack8(v + 8 * c8);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && t * kT + q * 32 < p.n) {
