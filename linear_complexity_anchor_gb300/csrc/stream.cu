@@ -6,11 +6,11 @@
 //
 // Pass 1 walks the slice's 128-token tiles: S_t = Q_t U^T, A_t = softmax (row warps, bf16),
 // [W | Delta] += A_t^T [V_t | 1]; each A_t tile also goes to a workspace by TMA (it stays in
-// L2).  With one CTA per slice only as many SMs as slices stream, so each CTA keeps as many
-// bytes in flight as its shared memory allows (eight 16 KB ring slots).  Then W' = Delta^{-1} W.  Pass 2 loads the A tiles back and forms H_t = A_t W', stored
-// by TMA.  No other CTA takes part in a slice, so nothing waits on another CTA: the whole
-// slice's sums run in one tensor-memory accumulator in tile order (bit-identical from run to
-// run).
+// L2).  Then W' = Delta^{-1} W.  Pass 2 loads the A tiles back and forms H_t = A_t W',
+// stored by TMA.  No other CTA takes part in a slice, so nothing waits on another CTA: the
+// whole slice's sums run in one tensor-memory accumulator in tile order (bit-identical from
+// run to run).  With one CTA per slice only as many SMs as slices stream; each keeps eight
+// 16 KB ring slots in flight.
 // Warps: 0-7 row warps in two groups that take alternate tiles (group g = warp / 4 owns TMEM
 // lanes 32 (warp % 4) + [0, 32) of its own S and H buffers); 8 and 10 producers, each with
 // its own four-slot TMA ring (warp 8: Q_t in pass 1, then A_t in pass 2; warp 10: V_t): a Q
