@@ -246,14 +246,18 @@ enum {
     ANCHOR_ATTN_VARIANT_SIMT_SLICE = 1,   /* one CTA per slice, CUDA-core FMA                */
     ANCHOR_ATTN_VARIANT_SIMT_SPLIT = 2,   /* token chunks + fixed-order reduction, FMA       */
     ANCHOR_ATTN_VARIANT_UMMA = 3,         /* tcgen05 tensor-core path, persistent CTAs       */
-    ANCHOR_ATTN_VARIANT_STREAM = 4        /* tcgen05 tensor-core path, one CTA per slice     */
+    ANCHOR_ATTN_VARIANT_STREAM = 4,       /* tcgen05 tensor-core path, one CTA per slice     */
+    ANCHOR_ATTN_VARIANT_SPLIT_TC = 5      /* tcgen05, the tile list cut over 152 CTAs        */
 };
 
 /* dtype: 0 = bf16 (anchor_attn_forward), 1 = fp32 (anchor_attn_forward_f32).  The plan is
  * the one a call with a positive scale makes: bf16 with d = 64, 32 <= m <= 64 and n > 512 runs
- * the slice-streaming tensor-core variant (any scale); otherwise the persistent tensor-core
- * variant takes bf16, d in {64, 128}, 32 <= m <= 128 and scale > 0 (a non-positive scale runs
- * a CUDA-core variant). */
+ * a slice-streaming tensor-core variant (any scale): one CTA per slice when there are at most
+ * 152 slices, else the slices' 128-token tiles cut into 152 contiguous ranges, one per CTA,
+ * all resident at once (a device that cannot hold 152 such CTAs runs one CTA per slice
+ * instead, in another summation order); otherwise the persistent tensor-core variant takes
+ * bf16, d in {64, 128}, 32 <= m <= 128 and scale > 0 (a non-positive scale runs a CUDA-core
+ * variant). */
 ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, int m, int d,
                                             anchor_attn_plan_t *plan);
 

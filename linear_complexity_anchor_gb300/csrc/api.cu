@@ -65,20 +65,22 @@ struct Plan {
     size_t workspace = 0;
 };
 
-// The slice-streaming variant takes bf16 problems with d = 64 and 32 <= m <= 64 whose slices are
-// long (n > 512): one CTA per slice needs no cross-CTA reduction there; short slices go to
-// the persistent tensor-core variant, which packs several into one CTA.
-bool stream_plan(const Problem &p) { return anchor::stream_supported(p) && p.m >= 32 && p.n > 512; }
+// bf16 problems with d = 64 and 32 <= m <= 64 whose slices are long (n > 512) stream each slice
+// through one CTA; with more slices than kPlanSMs (a second wave of CTAs) the slices' tiles are
+// cut into kPlanSMs contiguous ranges instead, one per resident CTA.  Short slices go to the
+// persistent tensor-core variant, which packs several into one CTA.
+bool long_plan(const Problem &p) { return anchor::split_supported(p) && p.m >= 32 && p.n > 512; }
 
 Plan make_plan(const Problem &p) {
     Plan pl;
     if (p.slices() == 0 || p.n == 0) return pl;
-    if (stream_plan(p) && p.slices() <= 0x7fffffffLL) {
-        pl.variant = ANCHOR_ATTN_VARIANT_STREAM;
+    if (long_plan(p) && p.slices() <= 0x7fffffffLL) {
+        const bool split = p.slices() > anchor::kPlanSMs;
+        pl.variant = split ? ANCHOR_ATTN_VARIANT_SPLIT_TC : ANCHOR_ATTN_VARIANT_STREAM;
         pl.kernels = 1;
-        pl.splits = 1;
+        pl.splits = split ? 0 : 1;  // split: ranges of the tile list, not chunks of each slice
         pl.flags = ANCHOR_ATTN_PLAN_STORED_A;
-        pl.workspace = anchor::stream_workspace(p);
+        pl.workspace = split ? anchor::split_workspace(p) : anchor::stream_workspace(p);
         return pl;
     }
     if (anchor::umma_supported(p)) {
@@ -138,14 +140,20 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
         if (e == cudaSuccess) e = ef;
         break;
     }
-    case ANCHOR_ATTN_VARIANT_STREAM: {
+    case ANCHOR_ATTN_VARIANT_STREAM:
+    case ANCHOR_ATTN_VARIANT_SPLIT_TC: {
         void *ws = nullptr;
         if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
         if (cudaMallocAsync(&ws, pl.workspace, stream) != cudaSuccess) {
             cudaGetLastError();
             return ANCHOR_ATTN_ERR_ALLOC;
         }
-        e = anchor::launch_stream(p, ws, stream);
+        e = pl.variant == ANCHOR_ATTN_VARIANT_SPLIT_TC ? anchor::launch_split(p, ws, stream)
+                                                        : anchor::launch_stream(p, ws, stream);
+        if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer resident CTAs: one CTA per slice
+            cudaGetLastError();
+            e = anchor::launch_stream(p, ws, stream);
+        }
         const cudaError_t ef = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = ef;
         break;
@@ -406,16 +414,16 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0, l = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0, l = 0, q = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
         anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess ||
         anchor::causal_read_and_clear_error(&e) != cudaSuccess || anchor::block_read_and_clear_error(&f) != cudaSuccess ||
         anchor::bwd_tc_read_and_clear_error(&g) != cudaSuccess || anchor::causal_tc_read_and_clear_error(&k) != cudaSuccess ||
-        anchor::stream_read_and_clear_error(&l) != cudaSuccess) {
+        anchor::stream_read_and_clear_error(&l) != cudaSuccess || anchor::split_read_and_clear_error(&q) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b | c | e | f | g | k | l;
+    *code = a | b | c | e | f | g | k | l | q;
     return ANCHOR_ATTN_OK;
 }
 

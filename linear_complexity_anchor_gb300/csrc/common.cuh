@@ -146,6 +146,16 @@ size_t stream_workspace(const Problem &p);
 cudaError_t launch_stream(const Problem &p, void *workspace, cudaStream_t stream);
 cudaError_t stream_read_and_clear_error(unsigned *out);
 
+// --- split tensor-core variant (d = 64, m <= 64): the slices' tiles cut over kPlanSMs CTAs --------
+// workspace: the A tiles [slices][n][64] bf16 first (so that launch_stream can run on it),
+// then a zeroed header (per-slice counters and flags), the parts' (W, Delta) partials and the
+// slices' W' images.  launch_split returns cudaErrorCooperativeLaunchTooLarge when the device
+// cannot hold all kPlanSMs CTAs at once.
+bool split_supported(const Problem &p);
+size_t split_workspace(const Problem &p);
+cudaError_t launch_split(const Problem &p, void *workspace, cudaStream_t stream);
+cudaError_t split_read_and_clear_error(unsigned *out);
+
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA
 constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)

@@ -84,11 +84,14 @@ def test_plans(pkg):
     assert pkg.query_plan("f32", 2, 2, 20000, 512, 32)["variant"] == "simt_split"
     assert pkg.query_plan("bf16", 64, 6, 197, 30, 64)["variant"] == "simt_slice"
     assert pkg.query_plan("bf16", 0, 2, 100, 20, 64)["variant"] == "empty"
-    # slice-streaming tensor-core variant: bf16, d = 64, 32 <= m <= 64, n > 512; one CTA per
-    # slice, the A tiles of pass 1 in a workspace
+    # slice-streaming tensor-core variants: bf16, d = 64, 32 <= m <= 64, n > 512; one CTA per
+    # slice up to 152 slices (workspace: the A tiles of pass 1), the tile list cut over 152
+    # CTAs beyond (the A tiles first, then counters, partials and W' images)
     p = pkg.query_plan("bf16", 8, 12, 4200, 64, 64)
-    assert p["variant"] == "stream" and p["kernels_per_call"] == 1 and p["splits"] == 1 and p["stored_a"]
+    assert p["variant"] == "stream" and p["kernels_per_call"] == 1 and p["stored_a"]
     assert p["workspace_bytes"] == 8 * 12 * 4200 * 64 * 2
+    p = pkg.query_plan("bf16", 16, 12, 4200, 64, 64)
+    assert p["variant"] == "split_tc" and p["stored_a"] and p["workspace_bytes"] > 16 * 12 * 4200 * 64 * 2
     assert pkg.query_plan("bf16", 8, 12, 512, 64, 64)["variant"] == "umma"
     # persistent tensor-core variant: d in {64, 128}, 32 <= m <= 128, bf16 only
     # 33 tiles of 128 tokens in chunks of at most 16: 3 chunks x 96 slices is at least 1.5

@@ -261,3 +261,21 @@ def test_runs_on_the_given_stream(env):
     s.synchronize()
     xx = widen(x, "bf16")
     assert_parity(to_host64(H), orc.forward(xx["Q"], xx["U"], xx["V"], w.scale), "bf16", "side stream")
+
+
+# More slices than 152: the tile list cut over 152 resident CTAs (slices shared by two or
+# more CTAs, partials summed in part order by the last arriver).
+@pytest.mark.parametrize("shape", [(16, 12, 700, 64, 64), (40, 4, 1000, 40, 64), (2, 80, 600, 33, 64)])
+def test_split_tiles_every_slice(env, shape):
+    pkg, torch, orc = env
+    B, heads, n, m, d = shape
+    w = gen.WORKLOADS["det_800x1344"].with_(name="split", B=B, heads=heads, n=n, m=m, d=d)
+    assert pkg.query_plan("bf16", B, heads, n, m, d)["variant"] == "split_tc"
+    x = gen.make_inputs(w, seed=sum(shape))
+    H = _run(env, w, x)
+    H2 = _run(env, w, x)
+    assert pkg.device_error() == 0
+    assert torch.equal(H.view(torch.int16), H2.view(torch.int16))
+    Hc = H.cpu()
+    for s0 in range(0, w.slices, 64):
+        assert_slices(Hc, w, oracle_slices(orc, w, x, range(s0, min(w.slices, s0 + 64))), "split")

@@ -59,7 +59,7 @@ def test_recompute_plan_matches_oracle_and_stored_plan(env, shape):
     pkg, torch, orc = env
     w = _w(*shape)
     plan = pkg.query_plan("bf16", *shape)
-    assert plan["variant"] in ("umma", "stream")
+    assert plan["variant"] in ("umma", "stream", "split_tc")
     x = gen.make_inputs(w, seed=sum(shape))
     t = {k: to_device(x[k], "bf16", torch) for k in "QUV"}
     H = torch.full_like(t["Q"], float("nan"))
@@ -72,7 +72,7 @@ def test_recompute_plan_matches_oracle_and_stored_plan(env, shape):
         assert torch.equal(H.view(torch.int16), H2.view(torch.int16)), \
             f"recompute and {'stored' if plan['stored_a'] else 'default'} plans differ"
     else:  # another kernel and summation order: against the oracle instead
-        _oracle_slices(orc, x, w, H2, range(w.slices), "stream")
+        _oracle_slices(orc, x, w, H2, range(w.slices), plan["variant"])
 
 
 def test_workload_plans(env):
