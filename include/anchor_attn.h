@@ -247,11 +247,13 @@ enum {
     ANCHOR_ATTN_VARIANT_SIMT_SPLIT = 2,   /* token chunks + fixed-order reduction, FMA       */
     ANCHOR_ATTN_VARIANT_UMMA = 3,         /* tcgen05 tensor-core path, persistent CTAs       */
     ANCHOR_ATTN_VARIANT_STREAM = 4,       /* tcgen05 tensor-core path, one CTA per slice     */
-    ANCHOR_ATTN_VARIANT_SPLIT_TC = 5      /* tcgen05, the tile list cut over 152 CTAs        */
+    ANCHOR_ATTN_VARIANT_SPLIT_TC = 5,     /* tcgen05, the tile list cut over 152 CTAs        */
+    ANCHOR_ATTN_VARIANT_SHORT_TC = 6      /* tcgen05, one CTA per short slice, two per SM    */
 };
 
 /* dtype: 0 = bf16 (anchor_attn_forward), 1 = fp32 (anchor_attn_forward_f32).  The plan is
- * the one a call with a positive scale makes: bf16 with d = 64, 32 <= m <= 64 and n > 512 runs
+ * the one a call with a positive scale makes: bf16 with d = 64, 32 <= m <= 64 and n <= 256
+ * runs one CTA per slice with the slice's tiles in shared memory (any scale); with n > 512 it runs
  * a slice-streaming tensor-core variant (any scale): one CTA per slice when there are at most
  * 152 slices, else the slices' 128-token tiles cut into 152 contiguous ranges, one per CTA,
  * all resident at once (a device that cannot hold 152 such CTAs runs one CTA per slice

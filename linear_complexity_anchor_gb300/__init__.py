@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libanchor_a
 
 STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_ALIAS", 4: "ERR_ALLOC", 5: "ERR_CUDA",
           6: "ERR_SCRATCH_LIMIT"}
-VARIANTS = {0: "empty", 1: "simt_slice", 2: "simt_split", 3: "umma", 4: "stream", 5: "split_tc"}
+VARIANTS = {0: "empty", 1: "simt_slice", 2: "simt_split", 3: "umma", 4: "stream", 5: "split_tc", 6: "short_tc"}
 
 _lock = threading.Lock()
 _lib = None

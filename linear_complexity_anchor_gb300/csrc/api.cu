@@ -74,6 +74,12 @@ bool long_plan(const Problem &p) { return anchor::split_supported(p) && p.m >= 3
 Plan make_plan(const Problem &p) {
     Plan pl;
     if (p.slices() == 0 || p.n == 0) return pl;
+    if (anchor::short_supported(p) && p.m >= 32 && p.slices() <= 0x7fffffffLL) {
+        pl.variant = ANCHOR_ATTN_VARIANT_SHORT_TC;
+        pl.kernels = 1;
+        pl.splits = 1;
+        return pl;
+    }
     if (long_plan(p) && p.slices() <= 0x7fffffffLL) {
         const bool split = p.slices() > anchor::kPlanSMs;
         pl.variant = split ? ANCHOR_ATTN_VARIANT_SPLIT_TC : ANCHOR_ATTN_VARIANT_STREAM;
@@ -140,6 +146,9 @@ anchor_attn_status_t run(const Problem &p, void *stream_v, const TestRun *test =
         if (e == cudaSuccess) e = ef;
         break;
     }
+    case ANCHOR_ATTN_VARIANT_SHORT_TC:
+        e = anchor::launch_short(p, stream);
+        break;
     case ANCHOR_ATTN_VARIANT_STREAM:
     case ANCHOR_ATTN_VARIANT_SPLIT_TC: {
         void *ws = nullptr;

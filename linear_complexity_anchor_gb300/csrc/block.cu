@@ -51,10 +51,14 @@ constexpr int kRingB = 2 * kStageB;                 // 96 KB
 // 32 KB + t * 16 KB, the ones block [128][64] (16 KB) and then the W' image at 64 KB
 constexpr int kOffV = 2 * kTileB;
 constexpr int kOffW = 4 * kTileB;
-constexpr int kOffU = kRingB;                       // U [64][64] bf16, 8 KB
-constexpr int kOffBar = kOffU + kMP * kD * 2;
+// The same kernel runs the plain forward on short slices (kProj = false): Q and V then arrive
+// by TMA straight into the tiles at 0 and 32 KB, and shared memory ends after the ones block.
+template <bool kProj> struct BlockLayout {
+    static constexpr int kOffU = kProj ? kRingB : 5 * kTileB;   // U [64][64] bf16, 8 KB
+    static constexpr int kOffBar = kOffU + kMP * kD * 2;
+    static constexpr int kSmem = kOffBar + 20 * 8 + 16 + 1024;  // + alignment slack
+};
 constexpr int kBars = 20;
-constexpr int kSmem = kOffBar + kBars * 8 + 16 + 1024;  // + alignment slack
 
 struct BlockParams {
     int heads, n, m, dm, tiles;
@@ -96,13 +100,15 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limi
     return true;
 }
 
+template <bool kProj>
 __global__ void __launch_bounds__(kThreads, 2)
 anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap twq,
                     const __grid_constant__ CUtensorMap twv, const __grid_constant__ CUtensorMap tu,
                     const __grid_constant__ CUtensorMap th, const BlockParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
+    using LY = BlockLayout<kProj>;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::kOffBar);
     uint64_t *full = bars + 0, *empty = bars + 2;
     uint64_t *proj_done = bars + 4, *u_full = bars + 5, *w_full = bars + 6, *wp_full = bars + 7;
     uint64_t *mma_done = bars + 8;
@@ -149,21 +155,30 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
             tma_prefetch_desc(&tu);
             const uint64_t pol_keep = policy_evict_last(), pol_x = policy_evict_normal();
             mbar_arrive_expect_tx(u_full, kMP * kD * 2);
-            tma_load_3d(sm + kOffU, &tu, u_full, 0, 0, h, pol_keep);
+            tma_load_3d(sm + LY::kOffU, &tu, u_full, 0, 0, h, pol_keep);
             int issued = 0;
-            for (int kc = 0; kc < KC; ++kc) {
-                const int s = kc & 1;
-                if (kc >= 2 && !bwait(empty + s, ((kc >> 1) + 1) & 1u, p.wait_ns)) break;
-                uint8_t *st = sm + s * kStageB;
-                mbar_arrive_expect_tx(full + s, (uint32_t)(T * kTileB + kTileB));
-                for (int t = 0; t < T; ++t) tma_load_3d(st + t * kTileB, &tx, full + s, kc * kKC, t * kT, b, pol_x);
-                tma_load_3d(st + 2 * kTileB, &twq, full + s, kc * kKC, 0, h, pol_keep);
-                tma_load_3d(st + 2 * kTileB + kTileB / 2, &twv, full + s, kc * kKC, 0, h, pol_keep);
-                ++issued;
+            if constexpr (kProj) {
+                for (int kc = 0; kc < KC; ++kc) {
+                    const int s = kc & 1;
+                    if (kc >= 2 && !bwait(empty + s, ((kc >> 1) + 1) & 1u, p.wait_ns)) break;
+                    uint8_t *st = sm + s * kStageB;
+                    mbar_arrive_expect_tx(full + s, (uint32_t)(T * kTileB + kTileB));
+                    for (int t = 0; t < T; ++t) tma_load_3d(st + t * kTileB, &tx, full + s, kc * kKC, t * kT, b, pol_x);
+                    tma_load_3d(st + 2 * kTileB, &twq, full + s, kc * kKC, 0, h, pol_keep);
+                    tma_load_3d(st + 2 * kTileB + kTileB / 2, &twv, full + s, kc * kKC, 0, h, pol_keep);
+                    ++issued;
+                }
+            } else {  // Q_t and V_t of the slice (tx: the Q map, twq: the V map), one barrier per tile
+                for (int t = 0; t < T; ++t) {
+                    mbar_arrive_expect_tx(full + t, 2 * kTileB);
+                    tma_load_3d(sm + t * kTileB, &tx, full + t, 0, t * kT, slice, pol_x);
+                    tma_load_3d(sm + kOffV + t * kTileB, &twq, full + t, 0, t * kT, slice, pol_x);
+                }
+                issued = T;
             }
-            // the last loads of each stage and of U have landed before the CTA leaves
+            // the last loads of each stage (each tile) and of U have landed before the CTA leaves
             for (int s = 0; s < 2; ++s) {
-                const int loads = issued > s ? (issued - s + 1) / 2 : 0;
+                const int loads = kProj ? (issued > s ? (issued - s + 1) / 2 : 0) : (issued > s ? 1 : 0);
                 if (loads > 0) bwait(full + s, (uint32_t)((loads - 1) & 1), p.wait_ns);
             }
             bwait(u_full, 0u, p.wait_ns);
@@ -176,7 +191,7 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
             const uint32_t kIdWD = idesc_bf16_f32(kT, kD + 16, true, true);  // [W | Delta] += A^T [V | 1]
             const uint32_t kIdH = idesc_bf16_f32(kT, kD, false, true);       // H = A W'
             bool ok = true;
-            for (int kc = 0; kc < KC; ++kc) {
+            for (int kc = 0; kProj && kc < KC; ++kc) {
                 const int s = kc & 1;
                 if (!bwait(full + s, (uint32_t)((kc >> 1) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
@@ -191,12 +206,13 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
                 }
                 umma_commit(empty + s);
             }
-            if (ok) umma_commit(proj_done);
+            if (kProj && ok) umma_commit(proj_done);
             // tile by tile, so that tile 0's S and W run while the row warps work on tile 1
             ok = ok && bwait(u_full, 0u, p.wait_ns);
-            const uint64_t udesc = smem_desc_sw128(sbase + kOffU, 16, 1024);
+            const uint64_t udesc = smem_desc_sw128(sbase + LY::kOffU, 16, 1024);
             for (int t = 0; t < T && ok; ++t) {
-                if (!bwait(qv_full + t, 0u, p.wait_ns)) { ok = false; break; }
+                // the tile's Q and V: written by the row warps from the projection, or loaded
+                if (!bwait(kProj ? qv_full + t : full + t, 0u, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t qdesc = smem_desc_sw128(sbase + t * kTileB, 16, 1024);
 #pragma unroll
@@ -205,6 +221,8 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
                               kk > 0 ? 1u : 0u);
                 umma_commit(s_full + t);
             }
+            // the ones block is written (by the row warps, before qv_full + 0)
+            if (!kProj) ok = ok && bwait(qv_full, 0u, p.wait_ns);
             for (int t = 0; t < T && ok; ++t) {
                 if (!bwait(a_full + t, 0u, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
@@ -241,8 +259,16 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
         // ------------------------------------------------------------------ row warps
         const int row = warp * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        bool ok = bwait(proj_done, 0u, p.wait_ns);
-        if (ok) {
+        bool ok = true;
+        if (!kProj) {  // the ones block of [V | 1] ([128][64] bf16 ones, 16 KB)
+            const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+            for (int i = row; i < kTileB / 16; i += 128) reinterpret_cast<uint4 *>(sm + kOffW)[i] = ones;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qv_full);
+        }
+        if (kProj) ok = bwait(proj_done, 0u, p.wait_ns);
+        if (kProj && ok) {
             tc_fence_after();
             float v[64];
             for (int t = 0; t < T; ++t) {
@@ -353,7 +379,8 @@ cudaError_t launch_block(const BlockProblem &p, cudaStream_t stream) {
         !make_bf16_map(&twv, p.Wv, p.dm, kD, p.heads, kD) || !make_bf16_map(&tu, p.U, kD, p.m, p.heads, kMP) ||
         !make_bf16_map(&th, p.H, kD, p.n, slices, 32))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(anchor_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    constexpr int kSmem = BlockLayout<true>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(anchor_block_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     BlockParams bp;
     bp.heads = p.heads;
@@ -363,7 +390,33 @@ cudaError_t launch_block(const BlockProblem &p, cudaStream_t stream) {
     bp.tiles = (p.n + kT - 1) / kT;
     bp.c = p.scale * 1.4426950408889634f;
     bp.wait_ns = 2000000000ull;
-    anchor_block_kernel<<<(unsigned)slices, kThreads, kSmem, stream>>>(tx, twq, twv, tu, th, bp);
+    anchor_block_kernel<true><<<(unsigned)slices, kThreads, kSmem, stream>>>(tx, twq, twv, tu, th, bp);
+    return cudaGetLastError();
+}
+
+bool short_supported(const Problem &p) {
+    return !p.f32 && p.d == kD && p.m >= 1 && p.m <= kMP && p.n >= 1 && p.n <= 2 * kT;
+}
+
+// The plain forward on slices of up to 256 tokens: the same kernel with Q and V loaded.
+cudaError_t launch_short(const Problem &p, cudaStream_t stream) {
+    CUtensorMap tq, tv, tu, th;
+    const long long slices = p.slices();
+    if (!make_bf16_map(&tq, p.Q, kD, p.n, slices, kT) || !make_bf16_map(&tv, p.V, kD, p.n, slices, kT) ||
+        !make_bf16_map(&tu, p.U, kD, p.m, p.heads, kMP) || !make_bf16_map(&th, p.H, kD, p.n, slices, 32))
+        return cudaErrorInvalidValue;
+    constexpr int kSmem = BlockLayout<false>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(anchor_block_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    BlockParams bp;
+    bp.heads = p.heads;
+    bp.n = p.n;
+    bp.m = p.m;
+    bp.dm = kKC;
+    bp.tiles = (p.n + kT - 1) / kT;
+    bp.c = p.scale * 1.4426950408889634f;
+    bp.wait_ns = 2000000000ull;
+    anchor_block_kernel<false><<<(unsigned)slices, kThreads, kSmem, stream>>>(tq, tv, tq, tu, th, bp);
     return cudaGetLastError();
 }
 

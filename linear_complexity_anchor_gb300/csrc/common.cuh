@@ -134,6 +134,10 @@ struct BlockProblem {
 };
 bool block_supported(const BlockProblem &p);
 cudaError_t launch_block(const BlockProblem &p, cudaStream_t stream);
+// the plain forward on short slices (bf16, d = 64, m <= 64, n <= 256) with the same kernel:
+// one CTA per slice, two per SM, no workspace
+bool short_supported(const Problem &p);
+cudaError_t launch_short(const Problem &p, cudaStream_t stream);
 cudaError_t block_read_and_clear_error(unsigned *out);
 
 // 3-D bf16 tensor map [outer][rows][cols], box 64 columns x box_rows rows x 1, 128-byte swizzle

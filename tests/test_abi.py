@@ -98,7 +98,9 @@ def test_plans(pkg):
     # items per SM of a 152-SM GPU (the count assumed without a device)
     p = pkg.query_plan("bf16", 8, 12, 4200, 100, 64)
     assert p["variant"] == "umma" and p["kernels_per_call"] == 1 and p["splits"] == 3
-    p = pkg.query_plan("bf16", 256, 12, 197, 49, 64)
+    p = pkg.query_plan("bf16", 256, 12, 197, 49, 64)   # short slices, d = 64: one CTA per slice
+    assert p["variant"] == "short_tc" and p["splits"] == 1 and p["workspace_bytes"] == 0
+    p = pkg.query_plan("bf16", 256, 12, 197, 49, 128)  # d = 128: the persistent variant, whole slices
     assert p["variant"] == "umma" and p["splits"] == 1 and p["workspace_bytes"] == 256
     assert pkg.query_plan("f32", 8, 12, 4200, 64, 64)["variant"] == "simt_split"
     assert pkg.query_plan("bf16", 1, 1, 4200, 31, 64)["variant"] == "simt_split"

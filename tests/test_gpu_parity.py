@@ -39,7 +39,7 @@ def _check_full(env, w, seed=0, x=None, scale=None):
 
 # ------------------------------------------------------------------ the five workloads
 
-EXPECTED_VARIANT = {"vit14_f32": "simt_slice", "deit_small": "simt_slice", "deit_base": "umma",
+EXPECTED_VARIANT = {"vit14_f32": "simt_slice", "deit_small": "simt_slice", "deit_base": "short_tc",
                     "det_800x1344": "stream", "long_16k": "umma"}
 
 
