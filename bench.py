@@ -51,10 +51,17 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_L2_BYTES = 126 * 1024 * 1024
 FMA_LANES_PER_SM = 128          # fp32 FMA lanes per SM (4 sub-partitions x 32)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-KERNEL_SOURCES = [os.path.join(ROOT, "linear_complexity_anchor_gb300", "csrc", f)
-                  for f in ("umma.cu", "simt.cu", "api.cu", "common.cuh", "ptx.cuh")]
+CSRC = os.path.join(ROOT, "linear_complexity_anchor_gb300", "csrc")
+# the files whose code makes each kernel (a recorded ncu capture stays valid while they hold)
+KERNEL_SOURCES = {"anchor_umma_kernel": ("umma.cu", "ptx.cuh"),
+                  "anchor_stream_kernel": ("stream.cu", "ptx.cuh", "rowops.cuh"),
+                  "anchor_split_kernel": ("split.cu", "ptx.cuh", "rowops.cuh"),
+                  "anchor_block_kernel": ("block.cu", "ptx.cuh", "rowops.cuh"),
+                  "simt_full_kernel": ("simt.cu", "simt_ops.cuh"),
+                  "simt_chunk_kernel": ("simt.cu", "simt_ops.cuh")}
 KERNEL_OF_VARIANT = {"umma": "anchor_umma_kernel", "simt_split": "simt_chunk_kernel",
-                     "simt_slice": "simt_full_kernel"}
+                     "simt_slice": "simt_full_kernel", "stream": "anchor_stream_kernel",
+                     "split_tc": "anchor_split_kernel", "short_tc": "anchor_block_kernel"}
 
 
 def parse_args(argv=None):
@@ -99,12 +106,12 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources' code: line comments and spacing are left out, so that an
-    edit to comments alone keeps a recorded ncu capture valid (the sources hold no string
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of a kernel's source files' code: line comments and spacing are left out, so that
+    an edit to comments alone keeps a recorded ncu capture valid (the sources hold no string
     literal with "//" in it)."""
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in (os.path.join(CSRC, f) for f in KERNEL_SOURCES.get(kernel, ())):
         if os.path.exists(p):
             with open(p) as f:
                 for line in f:
@@ -121,7 +128,7 @@ def recorded_traffic(workload: str, kernel: str):
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
         e = t["entries"][f"{kernel}@{workload}"]
-        if e.get("source_hash") != kernel_source_hash():
+        if e.get("source_hash") != kernel_source_hash(kernel):
             return None
         return int(e["dram_bytes_per_launch"])
     except Exception:
@@ -734,7 +741,7 @@ def run_ours(args) -> None:
                    "l2": f"{ws.algorithmic_bytes / 1e6:.1f} MB per step, {ts['nsets']} rotating set(s)",
                    "roofline": roofline(ws, wplan, ts["call_ms"]), "device_error": ts["device_error"],
                    "clocks": ts["clocks"]}
-            if wplan["variant"] != "umma":
+            if wplan["variant"].startswith("simt"):
                 rec["fma_roofline"] = fma_roofline(ws, ts["call_ms"], (ts["clocks"] or {}).get("sm_mhz"), dev)
             if ts["device_error"]:
                 rec["invalid"] = f"device error word {ts['device_error']:#x} after the timed calls"
