@@ -109,24 +109,29 @@ static __device__ __forceinline__ void scores(const T *Qs, const T *Us, int pitc
     }
 }
 
-// Row softmax of As in place, one thread per row: A_ij = exp(S_ij - max_j S_ij) / sum.
+// Row softmax of As in place, one thread per row: A_ij = exp(S_ij - max_j S_ij) * (1 / sum).
 static __device__ __forceinline__ void softmax_rows(float *As, int ap, int rows, int m) {
     for (int r = threadIdx.x; r < rows; r += blockDim.x) {
         float *a = As + (size_t)r * ap;
         float mx = -INFINITY;
+#pragma unroll 4
         for (int j = 0; j < m; ++j) mx = fmaxf(mx, a[j]);
         float z = 0.f;
+#pragma unroll 4
         for (int j = 0; j < m; ++j) {
             const float e = expf(__fsub_rn(a[j], mx));
             a[j] = e;
             z = __fadd_rn(z, e);
         }
-        for (int j = 0; j < m; ++j) a[j] = __fdiv_rn(a[j], z);
+        const float rz = __frcp_rn(z);
+#pragma unroll 4
+        for (int j = 0; j < m; ++j) a[j] = __fmul_rn(a[j], rz);
     }
 }
 
 // Wacc[j][k] += sum_r As[r][j] Vs[r][k] and Dacc[j] += sum_r As[r][j] (r ascending).  Each
-// thread takes 2 anchors x 4 columns; lanes of a warp take consecutive columns.
+// thread takes 2 anchors x 4 columns; lanes of a warp take consecutive columns; the threads of
+// column block 0 also sum the two anchors' Delta from the A values they already hold.
 template <typename T>
 static __device__ __forceinline__ void accumulate(const float *As, int ap, const T *Vs, int pitch, float *Wacc, float *Dacc,
                                            int rows, int m, int d) {
@@ -137,8 +142,11 @@ static __device__ __forceinline__ void accumulate(const float *As, int ap, const
         const bool two = j0 + 1 < m;
         float4 w0 = *reinterpret_cast<const float4 *>(Wacc + (size_t)j0 * d + k0);
         float4 w1 = two ? *reinterpret_cast<const float4 *>(Wacc + (size_t)(j0 + 1) * d + k0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool delta = Dacc != nullptr && ct == 0;
+        float d0 = delta ? Dacc[j0] : 0.f, d1 = delta && two ? Dacc[j0 + 1] : 0.f;
         const float *a = As + j0;
         const int j1 = two ? 1 : 0;
+#pragma unroll 4
         for (int r = 0; r < rows; ++r) {
             const float a0 = a[(size_t)r * ap], a1 = a[(size_t)r * ap + j1];
             const float4 v = ld4(Vs + (size_t)r * pitch + k0);
@@ -150,15 +158,15 @@ static __device__ __forceinline__ void accumulate(const float *As, int ap, const
             w1.y = __fmaf_rn(a1, v.y, w1.y);
             w1.z = __fmaf_rn(a1, v.z, w1.z);
             w1.w = __fmaf_rn(a1, v.w, w1.w);
+            d0 = __fadd_rn(d0, a0);
+            d1 = __fadd_rn(d1, a1);
         }
         *reinterpret_cast<float4 *>(Wacc + (size_t)j0 * d + k0) = w0;
         if (two) *reinterpret_cast<float4 *>(Wacc + (size_t)(j0 + 1) * d + k0) = w1;
-    }
-    if (Dacc == nullptr) return;  // W only
-    for (int j = threadIdx.x; j < m; j += blockDim.x) {
-        float s = Dacc[j];
-        for (int r = 0; r < rows; ++r) s = __fadd_rn(s, As[(size_t)r * ap + j]);
-        Dacc[j] = s;
+        if (delta) {
+            Dacc[j0] = d0;
+            if (two) Dacc[j0 + 1] = d1;
+        }
     }
 }
 
@@ -196,6 +204,7 @@ static __device__ __forceinline__ void apply(const float *As, int ap, const TW *
         float acc[2][8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) acc[0][c] = acc[1][c] = 0.f;
+#pragma unroll 4
         for (int j = 0; j < m; ++j) {
             const float x0 = a0[j], x1 = a1[j];
             float w[8];
