@@ -114,7 +114,16 @@ struct Layout {
     // buffers there is no room for it, and H is staged in the Q slot
     static constexpr bool kStageH = kNA == 1;
     static constexpr int kHB = kStageH ? 4 * 32 * 128 : 0;
-    static constexpr int kFixed = kNU * kUB + kNA * kAB + kNW * kWB + kOnesB + kHB + kXchB + kBarB;
+    // Single-buffered layouts can keep the pass-1 A tile and the pass-2 W' image in one buffer
+    // (each pass uses only one of them) when that frees room for another ring slot; the two
+    // uses then wait for each other's MMAs (barriers aw_w and aw_a below).
+    static constexpr int kAWB = kAB > kWB ? kAB : kWB;
+    static constexpr int kRest = kOnesB + kHB + kXchB + kBarB;
+    static constexpr int kFixedSplit = kNU * kUB + kNA * kAB + kNW * kWB + kRest;
+    static constexpr int kFixedUnion = kNU * kUB + kAWB + kRest;
+    static constexpr bool kAW =
+        kNA == 1 && kNW == 1 && (kMaxDyn - kFixedUnion) / kSlotB > (kMaxDyn - kFixedSplit) / kSlotB;
+    static constexpr int kFixed = kAW ? kFixedUnion : kFixedSplit;
     static constexpr int kSlotsFit = (kMaxDyn - kFixed) / kSlotB;
     static constexpr int kNSlot = kSlotsFit > 8 ? 8 : kSlotsFit;
     // ring order per pass-1 tile: Q then V, or (a shallow ring) Q(t), then V(t-1), so that the
@@ -122,8 +131,8 @@ struct Layout {
     static constexpr bool kVLag = kNSlot < 5;
     static constexpr int offU = 0;
     static constexpr int offA = offU + kNU * kUB;
-    static constexpr int offW = offA + kNA * kAB;
-    static constexpr int offRing = offW + kNW * kWB;
+    static constexpr int offW = kAW ? offA : offA + kNA * kAB;
+    static constexpr int offRing = kAW ? offA + kAWB : offW + kNW * kWB;
     static constexpr int offOnes = offRing + kNSlot * kSlotB;
     static constexpr int offH = offOnes + kOnesB;
     static constexpr int offXch = offH + kHB;
@@ -329,7 +338,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint64_t *iq_full = w_empty + NW;            // [kIQ] (1)      item queue
     uint64_t *iq_empty = iq_full + kIQ;          // [kIQ] (4)
     uint64_t *mma_done = iq_empty + kIQ;         // [2]  (1)       every MMA of an issuer completed (exit)
-    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 + 2 * NA + 2 + 2 + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ + 2;
+    // one A / W' buffer (LY::kAW): the MMAs before a W' load, or before a pass-1 A tile that
+    // follows a pass-2 phase, have completed (committed by the W/H issuer at those points)
+    uint64_t *aw_w = mma_done + 2;               // (1)
+    uint64_t *aw_a = aw_w + 1;                   // (1)
+    constexpr int kNumBars = 2 * NS + 2 + 2 + 2 + 2 * NA + 2 + 2 + 2 + 2 + 2 * NU + 2 * NW + 2 * kIQ + 2 + 2;
     static_assert(kNumBars * 8 + 3 * 4 * kIQ + 16 + 4 * NS <= LY::kBarB, "barrier area");
     int *s_items = reinterpret_cast<int *>(bars + kNumBars);           // [kIQ][3]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_items + 3 * kIQ);
@@ -375,6 +388,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         mbar_init(mma_done + 0, 1);
         mbar_init(mma_done + 1, 1);
+        mbar_init(aw_w, 1);
+        mbar_init(aw_a, 1);
         *s_abort = 0;
         *s_ast = 0;
         for (int i = 0; i < NS; ++i) s_slot_seq[i] = 0xffffffffu;
@@ -450,7 +465,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const bool L0 = lane == 0;
         const uint64_t pol_keep = policy_evict_last();
         const uint64_t pol_stream = policy_evict_first();
-        uint32_t ld_seq = 0, iq = 0, wuse = 0, nu = 0;
+        uint32_t ld_seq = 0, iq = 0, wuse = 0, nu = 0, nww = 0;  // nww: W' loads (aw_w phases)
         uint32_t wl_use[2] = {0u, 0u};  // per W' buffer: 1 + the use its last load was for (0: none)
         int u_head = -1;
         TileRef pend_v;
@@ -654,6 +669,9 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     if (!tr.full) {  // W' of a split slice: published (claim checked the flag)
                         const int wb = (int)(wuse % NW);
                         ok = wwait(w_empty + wb, ((wuse / NW) & 1u) ^ 1u);
+                        // one A / W' buffer: the last pass-1 tile's MMAs have read its A
+                        if (LY::kAW) ok = ok && wwait(aw_w, nww & 1u);
+                        ++nww;
                         if (ok && L0) {
                             (void)ld_acquire_gpu(p.flags + 32 * tr.slice);  // orders the image reads
                             asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -759,11 +777,13 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 uint32_t xs = 0, pcnt[2] = {0u, 0u};  // S tiles seen; pass-2 A's seen per S buffer
                 uint32_t acnt[2] = {0u, 0u};          // ping-pong: pass-1 A's seen per A buffer
                 uint32_t xw = 0;                      // pass-1 chunks started (separate W sets)
+                bool after_p2 = false;                // a pass-2 tile since the last pass-1 tile
                 // H = A W' into the next H buffer; A at `adesc` (K-major, shared memory) or, with
                 // from_tmem, in tensor memory at a_tmem
                 auto issue_h = [&](const TileRef &tr, uint64_t adesc, uint32_t a_tmem, bool from_tmem) -> bool {
                     const int wb = (int)((tr.first ? wuse : wuse - 1u) % NW);  // this pass-2 phase's W'
                     if (tr.first) {
+                        if (LY::kAW && !tr.full) umma_commit(aw_w);  // the producer may load W' over A
                         if (!wait(w_full + wb, (wuse / NW) & 1u)) return false;
                         ++wuse;
                     }
@@ -863,6 +883,10 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     const int nt = item_tiles(it, p, a1, b1);
                     for (int idx = 0; idx < nt && ok; ++idx) {
                         const TileRef tr = tile_at(it, a1, b1, idx, p);
+                        if (LY::kAW) {  // one A / W' buffer: the softmax may write A once W' is read
+                            if (tr.kind == 0 && after_p2) umma_commit(aw_a);
+                            after_p2 = tr.kind == 1;
+                        }
                         const uint32_t mseq = lseq++;
                         if (lpend) {  // the previous pass-1 tile's V follows this tile's first slot
                             if (!do_x(pv, lseq++, pvs)) { ok = false; break; }
@@ -911,6 +935,8 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const uint64_t pol_keep = policy_evict_last();
         uint32_t sidx = 0, ause = 0, iq = 0;  // ause: uses of the A buffers (pass-1 tiles)
         uint32_t own = 0;  // ping-pong: this group's uses of its A buffer
+        uint32_t naw = 0;  // one A / W' buffer: pass-2 to pass-1 switches waited for
+        bool after_p2 = false;
         bool ok = true;
         auto arrive_w = [&](uint64_t *bar) {  // one arrival per warp
             __syncwarp();
@@ -928,6 +954,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             const int nt = item_tiles(it, p, a1, b1);
             for (int idx = 0; idx < nt && ok; ++idx) {
                 const TileRef tr = tile_at(it, a1, b1, idx, p);
+                if (LY::kAW && tr.kind == 1) after_p2 = true;
                 if (tr.stored) continue;  // pass 2 of a split slice has no softmax
                 if constexpr (LY::kPP) {
                     const int sb = (int)(sidx & 1u);
@@ -1036,6 +1063,11 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
                 const int ab = (int)(ause % NA);
                 if (!wait(a_empty + ab, ((ause / NA) & 1u) ^ 1u)) { ok = false; break; }
+                if (LY::kAW && after_p2) {  // the buffer held W': its pass-2 MMAs have completed
+                    if (!wait(aw_a, naw & 1u)) { ok = false; break; }
+                    ++naw;
+                    after_p2 = false;
+                }
                 uint8_t *sAb = sA + ab * LY::kAB;
 #pragma unroll
                 for (int c8 = 0; c8 < HM / 8; ++c8)
