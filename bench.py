@@ -382,7 +382,6 @@ def time_workload(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev, world:
     for i in range(W):
         call(sets[i % nsets])
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -397,11 +396,11 @@ def time_workload(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev, world:
     with torch.cuda.stream(stream):
         if hasattr(torch.cuda, "_sleep"):
             torch.cuda._sleep(int(2e6))  # about a millisecond of clock cycles
+    # no event between the calls: an event recorded between two launches adds a few
+    # microseconds of its own to each gap, so the calls are timed as one batch
     t_start.record(stream)
     for i in range(K):
-        ev[i][0].record(stream)
         call_raw(i)
-        ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
@@ -409,10 +408,28 @@ def time_workload(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev, world:
         dist.barrier()
     derr = pkg.device_error()
     elapsed_ms = t_start.elapsed_time(t_end)
-    call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    call_ms = elapsed_ms / K  # one launch per call: the average launch duration, gaps included
     elapsed_ms, call_ms, derr_max = max_over_ranks([elapsed_ms, call_ms, float(derr)], dev, world)
     return {"elapsed_ms": elapsed_ms, "call_ms": call_ms, "nsets": nsets, "sets": sets, "stream": stream,
             "call": call, "device_error": int(derr_max), "clocks": clk}
+
+
+def batch_ms(stream, fn, k: int) -> float:
+    """Average milliseconds of k calls of fn(i) queued back to back on `stream` behind a short
+    GPU sleep (so that the host enqueues them faster than the GPU runs them), timed by two CUDA
+    events around the whole batch (an event between two launches adds to the gap)."""
+    import torch
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(int(2e6))
+        t0.record(stream)
+        for i in range(k):
+            fn(i)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / k
 
 
 def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
@@ -440,17 +457,8 @@ def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dic
     for _ in range(W):
         call()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    with torch.cuda.stream(stream):
-        if hasattr(torch.cuda, "_sleep"):
-            torch.cuda._sleep(int(2e6))
-    for i in range(K):
-        ev[i][0].record(stream)
-        call()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    call_ms = batch_ms(stream, lambda i: call(), K)
     derr = pkg.device_error()
-    call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     flops = 18 * w.slices * w.n * w.m * w.d
     hbm = (5 * w.slices * w.n * w.d + 2 * w.heads * w.m * w.d) * w.elem_bytes
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -500,17 +508,8 @@ def time_causal(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
     for _ in range(W):
         call()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    with torch.cuda.stream(stream):
-        if hasattr(torch.cuda, "_sleep"):
-            torch.cuda._sleep(int(2e6))
-    for i in range(K):
-        ev[i][0].record(stream)
-        call()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    call_ms = batch_ms(stream, lambda i: call(), K)
     derr = pkg.device_error()
-    call_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     peak, peak_src = peaks()
     tensor = w.dtype == "bf16" and w.d == 64 and w.m <= 64
     rec = {"ms_per_call": call_ms, "value": w.slices * w.n / (call_ms / 1e3), "unit": UNIT, "steps": K,
@@ -580,17 +579,7 @@ def time_block(pkg, bw: gen.BlockWorkload, K: int, W: int, dev) -> dict:
         for i in range(W):
             with torch.cuda.stream(stream):
                 fn(i)
-        torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
-        with torch.cuda.stream(stream):
-            if hasattr(torch.cuda, "_sleep"):
-                torch.cuda._sleep(int(2e6))
-            for i in range(k):
-                ev[i][0].record(stream)
-                fn(i)
-                ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in ev) / k
+        return batch_ms(stream, fn, k)
 
     call_ms = timed(call, K)
     derr = pkg.device_error()

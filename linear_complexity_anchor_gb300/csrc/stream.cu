@@ -15,9 +15,11 @@
 // lanes 32 (warp % 4) + [0, 32) of its own S and H buffers); 8 and 10 producers, each with
 // its own four-slot TMA ring (warp 8: Q_t in pass 1, then A_t in pass 2; warp 10: V_t): a Q
 // slot is free again as soon as S_t has read it, so the Q loads run further ahead of their
-// use than a shared [Q | V] slot, which only the later W MMA frees, would allow; 9 MMA
-// issuer.  Every wait is bounded; one that gives up sets bit 0 of this kernel's error word
-// and the CTA drains what it has in flight and leaves.
+// use than a shared [Q | V] slot, which only the later W MMA frees, would allow; 9 issues
+// S_t (and the pass-2 H MMAs), 11 issues the W MMAs: each tcgen05.mma holds its issuing
+// thread for a while, so one thread issuing both kinds (12 per tile) set the tile rate.
+// Every wait is bounded; one that gives up sets bit 0 of this kernel's error word and the
+// CTA drains what it has in flight and leaves.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "rowops.cuh"
@@ -33,8 +35,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 128, kD = 64, kMP = 64;
-constexpr int kThreads = 352;
-constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpProducerV = 10;
+constexpr int kThreads = 384;
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpProducerV = 10, kWarpMmaW = 11;
 constexpr int kSlots = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTileB = kT * 64 * 2;   // a [128][64] bf16 tile (16 KB)
@@ -50,7 +52,7 @@ constexpr int kOffU = kOffOnes + kTileB;             // U [64][64]
 constexpr int kOffW = kOffU + kImgB;                 // W' image [64][64]
 constexpr int kOffStage = kOffVRing;
 constexpr int kOffBar = kOffW + kImgB;
-constexpr int kBars = 4 * kSlots + 20;
+constexpr int kBars = 4 * kSlots + 21;
 constexpr int kSmem = kOffBar + kBars * 8 + 16 + 1024;
 static_assert(kSmem <= 227 * 1024, "shared memory");
 // tensor memory: S_g at 64 g, [W | Delta] at 128, H of group g, buffer b at 256 + 64 (2 g + b)
@@ -101,6 +103,7 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     uint64_t *s_full = vempty + kSlots, *s_empty = s_full + 2, *a_full = s_full + 4, *a_empty = s_full + 6;
     uint64_t *u_full = s_full + 8, *w_full = s_full + 9, *wp_full = s_full + 10, *mma_done = s_full + 11;
     uint64_t *h_full = s_full + 12, *h_empty = s_full + 16;  // [2 g + b]
+    uint64_t *mma_done_w = s_full + 20;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + kBars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -129,6 +132,7 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         mbar_init(w_full, 1);
         mbar_init(wp_full, 8);
         mbar_init(mma_done, 1);
+        mbar_init(mma_done_w, 1);
         fence_mbar_init();
     }
     if (warp < 8) {  // the ones block
@@ -196,15 +200,15 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);       // S = Q U^T
-            const uint32_t idWD = idesc_bf16_f32(kT, kD + 16, true, true);    // [W | Delta] += A^T [V | 1]
             const uint32_t idH = idesc_bf16_f32(kT, kD, false, true);         // H = A W'
             const uint64_t udesc = smem_desc_sw128(sbase + kOffU, 16, 1024);
             const uint64_t wdesc = smem_desc_sw128(sbase + kOffW, kMP * 128, 1024);
             bool ok = bwait(u_full, 0u, p.wait_ns);
-            auto issue_s = [&](int t) -> bool {
+            // pass 1: S_t as soon as Q_t is in and its group has read S_{t-2}
+            for (int t = 0; t < T && ok; ++t) {
                 const int s = t % kSlots, g = t & 1;
-                if (!bwait(full + s, (uint32_t)((t / kSlots) & 1), p.wait_ns)) return false;
-                if (t >= 2 && !bwait(s_empty + g, (uint32_t)(((t >> 1) - 1) & 1), p.wait_ns)) return false;
+                if (!bwait(full + s, (uint32_t)((t / kSlots) & 1), p.wait_ns)) { ok = false; break; }
+                if (t >= 2 && !bwait(s_empty + g, (uint32_t)(((t >> 1) - 1) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t qdesc = smem_desc_sw128(sbase + kOffQRing + s * kTileB, 16, 1024);
 #pragma unroll
@@ -213,15 +217,32 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                               kk > 0 ? 1u : 0u);
                 umma_commit(s_full + g);
                 umma_commit(empty + s);  // Q_t has been read
-                return true;
-            };
-            // pass 1: S two tiles ahead of the W MMAs (one S buffer per row-warp group); S_{t+2}
-            // needs only its group's S buffer read, which happens before the group's softmax
-            // of tile t, so it goes in ahead of W_t
-            for (int t = 0; t < 2 && t < T && ok; ++t) ok = issue_s(t);
+            }
+            // pass 2: H_t = A_t W'
+            ok = ok && bwait(wp_full, 0u, p.wait_ns);
+            for (int t = 0; t < T && ok; ++t) {
+                const int seq = T + t, s = seq % kSlots, hb = 2 * (t & 1) + ((t >> 1) & 1);  // H buffer (g, b)
+                if (!bwait(full + s, (uint32_t)((seq / kSlots) & 1), p.wait_ns)) { ok = false; break; }
+                if (t >= 4 && !bwait(h_empty + hb, (uint32_t)(((t >> 2) - 1) & 1), p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t adesc = smem_desc_sw128(sbase + kOffQRing + s * kTileB, 16, 1024);
+#pragma unroll
+                for (int kj = 0; kj < kMP / 16; ++kj)
+                    umma_bf16(tmem + kColH + hb * 64, adesc + (uint64_t)(kj * 2), wdesc + (uint64_t)(kj * 128), idH,
+                              kj > 0 ? 1u : 0u);
+                umma_commit(h_full + hb);
+                umma_commit(empty + s);
+            }
+            umma_commit(mma_done);
+            bwait(mma_done, 0u, p.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMmaW) {
+        if (lane == 0) {
+            const uint32_t idWD = idesc_bf16_f32(kT, kD + 16, true, true);    // [W | Delta] += A^T [V | 1]
+            bool ok = true;
             for (int t = 0; t < T && ok; ++t) {
                 const int s = t % kSlots, g = t & 1;
-                if (t + 2 < T && !issue_s(t + 2)) { ok = false; break; }
                 if (!bwait(a_full + g, (uint32_t)((t >> 1) & 1), p.wait_ns) ||
                     !bwait(vfull + s, (uint32_t)((t / kSlots) & 1), p.wait_ns)) {
                     ok = false;
@@ -240,23 +261,8 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 umma_commit(vempty + s);
             }
             if (ok) umma_commit(w_full);
-            // pass 2: H_t = A_t W'
-            ok = ok && bwait(wp_full, 0u, p.wait_ns);
-            for (int t = 0; t < T && ok; ++t) {
-                const int seq = T + t, s = seq % kSlots, hb = 2 * (t & 1) + ((t >> 1) & 1);  // H buffer (g, b)
-                if (!bwait(full + s, (uint32_t)((seq / kSlots) & 1), p.wait_ns)) { ok = false; break; }
-                if (t >= 4 && !bwait(h_empty + hb, (uint32_t)(((t >> 2) - 1) & 1), p.wait_ns)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t adesc = smem_desc_sw128(sbase + kOffQRing + s * kTileB, 16, 1024);
-#pragma unroll
-                for (int kj = 0; kj < kMP / 16; ++kj)
-                    umma_bf16(tmem + kColH + hb * 64, adesc + (uint64_t)(kj * 2), wdesc + (uint64_t)(kj * 128), idH,
-                              kj > 0 ? 1u : 0u);
-                umma_commit(h_full + hb);
-                umma_commit(empty + s);
-            }
-            umma_commit(mma_done);
-            bwait(mma_done, 0u, p.wait_ns);
+            umma_commit(mma_done_w);
+            bwait(mma_done_w, 0u, p.wait_ns);
         }
         __syncwarp();
     } else {
