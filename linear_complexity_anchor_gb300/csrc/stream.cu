@@ -9,15 +9,18 @@
 // L2).  Then W' = Delta^{-1} W.  Pass 2 loads the A tiles back and forms H_t = A_t W',
 // stored by TMA.  No other CTA takes part in a slice, so nothing waits on another CTA: the
 // whole slice's sums run in one tensor-memory accumulator in tile order (bit-identical from
-// run to run).  With one CTA per slice only as many SMs as slices stream; each keeps eight
+// run to run).  With one CTA per slice only as many SMs as slices stream; each keeps ten
 // 16 KB ring slots in flight.
-// Warps: 0-7 row warps in two groups that take alternate tiles (group g = warp / 4 owns TMEM
+// Warps: 0-7 row warps in two groups taking alternate tiles (group g = warp / 4 owns TMEM
 // lanes 32 (warp % 4) + [0, 32) of its own S and H buffers); 8 and 10 producers, each with
-// its own four-slot TMA ring (warp 8: Q_t in pass 1, then A_t in pass 2; warp 10: V_t): a Q
+// its own five-slot TMA ring (warp 8: Q_t in pass 1, then A_t in pass 2; warp 10: V_t): a Q
 // slot is free again as soon as S_t has read it, so the Q loads run further ahead of their
 // use than a shared [Q | V] slot, which only the later W MMA frees, would allow; 9 issues
-// S_t (and the pass-2 H MMAs), 11 issues the W MMAs: each tcgen05.mma holds its issuing
-// thread for a while, so one thread issuing both kinds (12 per tile) set the tile rate.
+// S_t (and the pass-2 H MMAs), 11 issues the W MMAs: a tcgen05.mma holds its issuing thread
+// until the tensor pipe takes it (about 48 cycles at N = 64, 52 at N = 80, whatever the
+// work), so one thread issuing both kinds (12 per tile) set the tile rate.  Pass 1 is then
+// bound by the bytes in flight: the deepest rings that fit shared memory (five slots each,
+// with two row-warp groups; a third group, and so four slots, was slower).
 // Every wait is bounded; one that gives up sets bit 0 of this kernel's error word and the
 // CTA drains what it has in flight and leaves.
 #include "common.cuh"
@@ -35,28 +38,34 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 128, kD = 64, kMP = 64;
-constexpr int kThreads = 384;
-constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpProducerV = 10, kWarpMmaW = 11;
-constexpr int kSlots = 4;
+constexpr int kNG = 2;                 // row-warp groups, taking tiles t = g (mod kNG)
+constexpr int kRowWarps = 4 * kNG;
+constexpr int kThreads = 32 * (kRowWarps + 4);
+constexpr int kWarpProducer = kRowWarps, kWarpMma = kRowWarps + 1, kWarpProducerV = kRowWarps + 2,
+              kWarpMmaW = kRowWarps + 3;
+constexpr int kSlots = 5;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTileB = kT * 64 * 2;   // a [128][64] bf16 tile (16 KB)
 
 constexpr int kImgB = kMP * kD * 2;
 // shared memory (an MN-major M = 128 operand reads an unused second 64-row block 16 KB on:
-// A tile 1's is the first Q slot)
-constexpr int kOffA = 0;                             // A tiles of the two row-warp groups
-constexpr int kOffQRing = kOffA + 2 * kTileB;        // Q ring: Q_t in pass 1, then A_t in pass 2
+// the last A tile's is the first Q slot)
+constexpr int kOffA = 0;                             // A tiles of the row-warp groups
+constexpr int kOffQRing = kOffA + kNG * kTileB;      // Q ring: Q_t in pass 1, then A_t in pass 2
 constexpr int kOffVRing = kOffQRing + kSlots * kTileB;  // V ring; in pass 2 the H staging (4 KB per row warp)
 constexpr int kOffOnes = kOffVRing + kSlots * kTileB;   // [128][64] bf16 ones: the second block of [V | 1]
 constexpr int kOffU = kOffOnes + kTileB;             // U [64][64]
 constexpr int kOffW = kOffU + kImgB;                 // W' image [64][64]
 constexpr int kOffStage = kOffVRing;
 constexpr int kOffBar = kOffW + kImgB;
-constexpr int kBars = 4 * kSlots + 21;
+constexpr int kBars = 4 * kSlots + 4 * kNG + 2 * kNG * 2 + 6;
 constexpr int kSmem = kOffBar + kBars * 8 + 16 + 1024;
 static_assert(kSmem <= 227 * 1024, "shared memory");
-// tensor memory: S_g at 64 g, [W | Delta] at 128, H of group g, buffer b at 256 + 64 (2 g + b)
-constexpr uint32_t kColS = 0, kColW = 128, kColDelta = 192, kColH = 256;
+static_assert(kOffStage + kRowWarps * 4096 <= kOffOnes, "pass-2 staging inside the V ring");
+// tensor memory: pass 1 S_g at 64 g and [W | Delta] after them; pass 2 (W read out by then)
+// H of group g, buffer b at 64 (2 g + b)
+constexpr uint32_t kColS = 0, kColW = 64 * kNG, kColDelta = kColW + 64, kColH = 0;
+static_assert(kColDelta + 16 <= 512 && 64 * 2 * kNG <= 512, "tensor memory columns");
 
 struct StParams {
     int heads, n, m, tiles;
@@ -100,10 +109,10 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
     uint64_t *full = bars, *empty = full + kSlots, *vfull = empty + kSlots, *vempty = vfull + kSlots;
-    uint64_t *s_full = vempty + kSlots, *s_empty = s_full + 2, *a_full = s_full + 4, *a_empty = s_full + 6;
-    uint64_t *u_full = s_full + 8, *w_full = s_full + 9, *wp_full = s_full + 10, *mma_done = s_full + 11;
-    uint64_t *h_full = s_full + 12, *h_empty = s_full + 16;  // [2 g + b]
-    uint64_t *mma_done_w = s_full + 20;
+    uint64_t *s_full = vempty + kSlots, *s_empty = s_full + kNG, *a_full = s_empty + kNG, *a_empty = a_full + kNG;
+    uint64_t *h_full = a_empty + kNG, *h_empty = h_full + 2 * kNG;  // [2 g + b]
+    uint64_t *u_full = h_empty + 2 * kNG, *w_full = u_full + 1, *wp_full = u_full + 2, *mma_done = u_full + 3;
+    uint64_t *mma_done_w = u_full + 4;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + kBars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -118,26 +127,26 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             mbar_init(vfull + i, 1);
             mbar_init(vempty + i, 1);
         }
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < kNG; ++g) {
             mbar_init(s_full + g, 1);
             mbar_init(s_empty + g, 4);
             mbar_init(a_full + g, 4);
             mbar_init(a_empty + g, 1);
         }
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2 * kNG; ++i) {
             mbar_init(h_full + i, 1);
             mbar_init(h_empty + i, 4);
         }
         mbar_init(u_full, 1);
         mbar_init(w_full, 1);
-        mbar_init(wp_full, 8);
+        mbar_init(wp_full, kRowWarps);
         mbar_init(mma_done, 1);
         mbar_init(mma_done_w, 1);
         fence_mbar_init();
     }
-    if (warp < 8) {  // the ones block
+    if (warp < kRowWarps) {  // the ones block
         const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        for (int i = threadIdx.x; i < kTileB / 16; i += 256) reinterpret_cast<uint4 *>(sm + kOffOnes)[i] = ones;
+        for (int i = threadIdx.x; i < kTileB / 16; i += 32 * kRowWarps) reinterpret_cast<uint4 *>(sm + kOffOnes)[i] = ones;
         fence_proxy_async_smem();
     }
     if (warp == kWarpMma) tmem_alloc(s_tmem, kTmemCols);
@@ -206,9 +215,9 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             bool ok = bwait(u_full, 0u, p.wait_ns);
             // pass 1: S_t as soon as Q_t is in and its group has read S_{t-2}
             for (int t = 0; t < T && ok; ++t) {
-                const int s = t % kSlots, g = t & 1;
+                const int s = t % kSlots, g = t % kNG, k = t / kNG;
                 if (!bwait(full + s, (uint32_t)((t / kSlots) & 1), p.wait_ns)) { ok = false; break; }
-                if (t >= 2 && !bwait(s_empty + g, (uint32_t)(((t >> 1) - 1) & 1), p.wait_ns)) { ok = false; break; }
+                if (k >= 1 && !bwait(s_empty + g, (uint32_t)((k - 1) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t qdesc = smem_desc_sw128(sbase + kOffQRing + s * kTileB, 16, 1024);
 #pragma unroll
@@ -221,9 +230,10 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             // pass 2: H_t = A_t W'
             ok = ok && bwait(wp_full, 0u, p.wait_ns);
             for (int t = 0; t < T && ok; ++t) {
-                const int seq = T + t, s = seq % kSlots, hb = 2 * (t & 1) + ((t >> 1) & 1);  // H buffer (g, b)
+                // H buffer (g, b) of tile t = g + kNG k: b = k & 1, its use number k >> 1
+                const int seq = T + t, s = seq % kSlots, k = t / kNG, hb = 2 * (t % kNG) + (k & 1), u = k >> 1;
                 if (!bwait(full + s, (uint32_t)((seq / kSlots) & 1), p.wait_ns)) { ok = false; break; }
-                if (t >= 4 && !bwait(h_empty + hb, (uint32_t)(((t >> 2) - 1) & 1), p.wait_ns)) { ok = false; break; }
+                if (u >= 1 && !bwait(h_empty + hb, (uint32_t)((u - 1) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t adesc = smem_desc_sw128(sbase + kOffQRing + s * kTileB, 16, 1024);
 #pragma unroll
@@ -242,8 +252,8 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             const uint32_t idWD = idesc_bf16_f32(kT, kD + 16, true, true);    // [W | Delta] += A^T [V | 1]
             bool ok = true;
             for (int t = 0; t < T && ok; ++t) {
-                const int s = t % kSlots, g = t & 1;
-                if (!bwait(a_full + g, (uint32_t)((t >> 1) & 1), p.wait_ns) ||
+                const int s = t % kSlots, g = t % kNG;
+                if (!bwait(a_full + g, (uint32_t)((t / kNG) & 1), p.wait_ns) ||
                     !bwait(vfull + s, (uint32_t)((t / kSlots) & 1), p.wait_ns)) {
                     ok = false;
                     break;
@@ -274,7 +284,7 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         const uint64_t pol_a = policy_evict_last(), pol_out = policy_evict_first();
         bool ok = true;
         float v[64];
-        for (int t = g, k = 0; t < T && ok; t += 2, ++k) {
+        for (int t = g, k = 0; t < T && ok; t += kNG, ++k) {
             if (!bwait(s_full + g, (uint32_t)(k & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             tmem_ld32(trow + kColS + g * 64, v);
@@ -331,7 +341,7 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         }
         // pass 2: H tiles out
         uint8_t *stage = sm + kOffStage + warp * 4096;
-        for (int t = g, k = 0; t < T && ok; t += 2, ++k) {
+        for (int t = g, k = 0; t < T && ok; t += kNG, ++k) {
             const int hb = 2 * g + (k & 1);
             if (!bwait(h_full + hb, (uint32_t)((k >> 1) & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
