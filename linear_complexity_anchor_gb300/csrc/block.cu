@@ -146,6 +146,9 @@ anchor_block_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t sbase = smem_u32(sm);
+    // launched with programmatic stream serialization: global memory only from here on
+    grid_dependency_wait();
+    grid_dependents_launch();
 
     if (warp == kWarpProducer) {
         if (lane == 0) {
@@ -390,8 +393,8 @@ cudaError_t launch_block(const BlockProblem &p, cudaStream_t stream) {
     bp.tiles = (p.n + kT - 1) / kT;
     bp.c = p.scale * 1.4426950408889634f;
     bp.wait_ns = 2000000000ull;
-    anchor_block_kernel<true><<<(unsigned)slices, kThreads, kSmem, stream>>>(tx, twq, twv, tu, th, bp);
-    return cudaGetLastError();
+    return launch_pdl(anchor_block_kernel<true>, dim3((unsigned)slices), dim3(kThreads), kSmem, stream, tx, twq, twv, tu,
+                      th, bp);
 }
 
 bool short_supported(const Problem &p) {
@@ -416,8 +419,8 @@ cudaError_t launch_short(const Problem &p, cudaStream_t stream) {
     bp.tiles = (p.n + kT - 1) / kT;
     bp.c = p.scale * 1.4426950408889634f;
     bp.wait_ns = 2000000000ull;
-    anchor_block_kernel<false><<<(unsigned)slices, kThreads, kSmem, stream>>>(tq, tv, tq, tu, th, bp);
-    return cudaGetLastError();
+    return launch_pdl(anchor_block_kernel<false>, dim3((unsigned)slices), dim3(kThreads), kSmem, stream, tq, tv, tq, tu,
+                      th, bp);
 }
 
 cudaError_t block_read_and_clear_error(unsigned *out) {

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <utility>
 
 #include "anchor_attn.h"
 
@@ -141,6 +142,32 @@ cudaError_t launch_short(const Problem &p, cudaStream_t stream);
 cudaError_t block_read_and_clear_error(unsigned *out);
 
 // 3-D bf16 tensor map [outer][rows][cols], box 64 columns x box_rows rows x 1, 128-byte swizzle
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization
+// may start while the kernel before it in the stream is still running.  It touches global
+// memory only after grid_dependency_wait() (which returns once that kernel has completed and
+// its writes are visible), and lets the next such launch start early with
+// grid_dependents_launch().
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Launch with programmatic stream serialization: the kernel's setup may overlap the end of the
+// previous kernel in the stream; the kernel itself waits (grid_dependency_wait) before it
+// touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 bool make_bf16_map(CUtensorMap *map, const void *base, int cols, int rows, long long outer, int box_rows);
 
 // --- slice-streaming tensor-core variant (d = 64, m <= 64): one CTA per slice ----------------

@@ -54,6 +54,9 @@ simt_full_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__re
     const int h = (int)(slice % heads);
     const size_t off = (size_t)slice * n * d;
 
+    // launched with programmatic stream serialization: global memory only from here on
+    grid_dependency_wait();
+    grid_dependents_launch();
     stage_rows(Qs, Q + off, n, d, pitch);
     stage_rows(Us, U + (size_t)h * m * d, m, d, pitch);
     cp_async_commit();
@@ -228,9 +231,8 @@ cudaError_t full_launch(const Problem &p, cudaStream_t stream) {
     const size_t smem = full_smem<T>(p.n, p.m, p.d);
     cudaError_t e = cudaFuncSetAttribute(simt_full_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    simt_full_kernel<T><<<(unsigned)p.slices(), kThreads, smem, stream>>>(
-        (const T *)p.Q, (const T *)p.U, (const T *)p.V, (T *)p.H, p.heads, p.n, p.m, p.d, p.scale);
-    return cudaGetLastError();
+    return launch_pdl(simt_full_kernel<T>, dim3((unsigned)p.slices()), dim3(kThreads), smem, stream, (const T *)p.Q,
+                      (const T *)p.U, (const T *)p.V, (T *)p.H, p.heads, p.n, p.m, p.d, p.scale);
 }
 
 template <typename T>

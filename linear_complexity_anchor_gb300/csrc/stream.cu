@@ -155,6 +155,10 @@ anchor_stream_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t sbase = smem_u32(sm);
+    // launched with programmatic stream serialization: the setup above may run while the
+    // previous kernel in the stream finishes; global memory only from here on
+    grid_dependency_wait();
+    grid_dependents_launch();
 
     if (warp == kWarpProducer) {
         if (lane == 0) {
@@ -397,8 +401,8 @@ cudaError_t launch_stream(const Problem &p, void *workspace, cudaStream_t stream
     sp.tiles = (p.n + kT - 1) / kT;
     sp.c = p.scale * 1.4426950408889634f;
     sp.wait_ns = 2000000000ull;
-    anchor_stream_kernel<<<(unsigned)S, kThreads, kSmem, stream>>>(tq, tv, tu, ta_st, ta_ld, th, sp);
-    return cudaGetLastError();
+    return launch_pdl(anchor_stream_kernel, dim3((unsigned)S), dim3(kThreads), kSmem, stream, tq, tv, tu, ta_st, ta_ld,
+                      th, sp);
 }
 
 cudaError_t stream_read_and_clear_error(unsigned *out) {
