@@ -488,7 +488,7 @@ def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dic
 def time_causal(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
     """The masked (causal) variant of one workload, timed like the forward.  Algorithmic
     traffic as the forward's (Q, V and H once, U once), the roofline of the tensor-core path
-    (bf16, d = 64, m <= 64); the CUDA-core path also reports its FMA rate, counting the work as
+    (bf16, d = 64 or 128, m <= 128); the CUDA-core path also reports its FMA rate, counting the work as
     the forward's 6 n m d."""
     import torch
     hQ, hU, hV = hQUV
@@ -511,7 +511,8 @@ def time_causal(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dict:
     call_ms = batch_ms(stream, lambda i: call(), K)
     derr = pkg.device_error()
     peak, peak_src = peaks()
-    tensor = w.dtype == "bf16" and w.d == 64 and w.m <= 64
+    # the tensor-core kernels: 64 anchors at d = 64, 128 anchors at d = 128 (and d = 64, m > 64)
+    tensor = w.dtype == "bf16" and w.d in (64, 128) and w.m <= 128
     rec = {"ms_per_call": call_ms, "value": w.slices * w.n / (call_ms / 1e3), "unit": UNIT, "steps": K,
            "kernels_per_call": 1, "device_error": derr, "path": "tensor" if tensor else "cuda_core",
            "hbm": {"achieved": w.algorithmic_bytes / (call_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",

@@ -196,9 +196,11 @@ anchor_attn_status_t causal_forward(const Problem &p, void *stream_v) {
     if (st != ANCHOR_ATTN_OK) return st;
     if (p.slices() == 0 || p.n == 0) return ANCHOR_ATTN_OK;
     cudaStream_t stream = (cudaStream_t)stream_v;
-    if (anchor::causal_tc_supported(p)) {
+    if (anchor::causal_tc_supported(p) || anchor::causal_wide_supported(p)) {
         if (p.slices() > 0x7fffffffLL) return ANCHOR_ATTN_ERR_UNSUPPORTED;
-        if (anchor::launch_causal_tc(p, stream) != cudaSuccess) {
+        const cudaError_t e = anchor::causal_tc_supported(p) ? anchor::launch_causal_tc(p, stream)
+                                                             : anchor::launch_causal_wide(p, stream);
+        if (e != cudaSuccess) {
             cudaGetLastError();
             return ANCHOR_ATTN_ERR_CUDA;
         }
@@ -423,16 +425,17 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0, l = 0, q = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0, l = 0, q = 0, r = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
         anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess ||
         anchor::causal_read_and_clear_error(&e) != cudaSuccess || anchor::block_read_and_clear_error(&f) != cudaSuccess ||
         anchor::bwd_tc_read_and_clear_error(&g) != cudaSuccess || anchor::causal_tc_read_and_clear_error(&k) != cudaSuccess ||
-        anchor::stream_read_and_clear_error(&l) != cudaSuccess || anchor::split_read_and_clear_error(&q) != cudaSuccess) {
+        anchor::stream_read_and_clear_error(&l) != cudaSuccess || anchor::split_read_and_clear_error(&q) != cudaSuccess ||
+        anchor::causal_wide_read_and_clear_error(&r) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b | c | e | f | g | k | l | q;
+    *code = a | b | c | e | f | g | k | l | q | r;
     return ANCHOR_ATTN_OK;
 }
 

@@ -110,6 +110,10 @@ cudaError_t causal_read_and_clear_error(unsigned *out);
 bool causal_tc_supported(const Problem &p);
 cudaError_t launch_causal_tc(const Problem &p, cudaStream_t stream);
 cudaError_t causal_tc_read_and_clear_error(unsigned *out);
+// the masked variant on the tensor cores for up to 128 anchors (d = 128, or d = 64 with m > 64)
+bool causal_wide_supported(const Problem &p);
+cudaError_t launch_causal_wide(const Problem &p, cudaStream_t stream);
+cudaError_t causal_wide_read_and_clear_error(unsigned *out);
 
 // --- approximation-error diagnostic ------------------------------------------------------
 struct FullProblem {

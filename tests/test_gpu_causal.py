@@ -1,7 +1,8 @@
 """GPU: the masked (causal) variant through the C ABI against the oracle's, element by element,
 plus the properties that hold at any size: the last row equals the unmasked forward's, the
-first row is its own value, and changing later tokens leaves earlier rows unchanged.  bf16 with
-d = 64 and m <= 64 runs on the tensor cores; the rest, and fp32, on CUDA cores."""
+first row is its own value, and changing later tokens leaves earlier rows unchanged.  bf16 runs
+on the tensor cores (the 64-anchor kernel for d = 64, m <= 64; the 128-anchor kernel for
+d = 128, m <= 128 and d = 64, 64 < m <= 128); the rest, and fp32, on CUDA cores."""
 import os
 from concurrent.futures import ThreadPoolExecutor
 
@@ -110,3 +111,66 @@ def test_causal_workload_every_slice(env, name):
         for s, ref in ex.map(one, range(w.slices)):
             b, h = divmod(s, w.heads)
             assert_parity(Hh[b, h], ref, w.dtype, f"{name} causal slice ({b},{h})")
+
+
+# 128-anchor tensor-core path (d = 128, or d = 64 with m > 64): the same edge cases
+_WIDE_SHAPES = [(3, 2, 1, 5, 128, None), (2, 2, 128, 128, 128, None), (1, 2, 129, 33, 128, None),
+                (1, 1, 2000, 128, 128, None), (2, 2, 300, 1, 128, None), (1, 2, 250, 40, 128, -0.2),
+                (2, 1, 400, 128, 128, 0.0), (2, 2, 300, 65, 64, None), (1, 2, 513, 128, 64, None)]
+
+
+@pytest.mark.parametrize("shape", _WIDE_SHAPES)
+def test_causal_wide_shapes(env, shape):
+    pkg, torch, orc = env
+    *dims, scale = shape
+    w = _w("bf16", *dims)
+    sc = w.scale if scale is None else scale
+    x = gen.make_inputs(w, seed=sum(dims) + 5)
+    t = {k: to_device(x[k], "bf16", torch) for k in "QUV"}
+    H = pkg.causal_forward(t["Q"], t["U"], t["V"], scale=sc)
+    torch.cuda.synchronize()
+    xx = widen(x, "bf16")
+    assert_parity(to_host64(H), orc.causal(xx["Q"], xx["U"], xx["V"], sc), "bf16", f"causal {shape}")
+    assert pkg.device_error() == 0
+
+
+def test_causal_wide_ignores_later_tokens(env):
+    pkg, torch, _ = env
+    w = _w("bf16", 1, 2, 1000, 128, 128)
+    x = gen.make_inputs(w, seed=23)
+    t = {k: to_device(x[k], "bf16", torch) for k in "QUV"}
+    H1 = pkg.causal_forward(t["Q"], t["U"], t["V"], scale=w.scale)
+    Q2, V2 = t["Q"].clone(), t["V"].clone()
+    Q2[:, :, 700:] += 1.0
+    V2[:, :, 700:] -= 1.0
+    H2 = pkg.causal_forward(Q2, t["U"], V2, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(H1[:, :, :700].view(torch.int16), H2[:, :, :700].view(torch.int16))
+    assert not torch.equal(H1[:, :, 700:], H2[:, :, 700:])
+
+
+def test_causal_long_16k_sampled_slices(env):
+    """long_16k at full size (the 128-anchor kernel): 16 of the 64 slices against the oracle,
+    and bit-stable from run to run."""
+    pkg, torch, orc = env
+    w = gen.WORKLOADS["long_16k"]
+    x = gen.make_inputs(w, seed=0)
+    t = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    H = pkg.causal_forward(t["Q"], t["U"], t["V"], scale=w.scale)
+    H2 = pkg.causal_forward(t["Q"], t["U"], t["V"], scale=w.scale)
+    torch.cuda.synchronize()
+    assert pkg.device_error() == 0
+    assert torch.equal(H.view(torch.int16), H2.view(torch.int16))
+    Hh = to_host64(H)
+    U = gen.to_float64(x["U"], w.dtype)
+
+    def one(s):
+        b, h = divmod(s, w.heads)
+        q = gen.to_float64(x["Q"][b, h], w.dtype)[None, None]
+        v = gen.to_float64(x["V"][b, h], w.dtype)[None, None]
+        return s, orc.causal(q, U[h:h + 1], v, w.scale)[0, 0]
+
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as ex:
+        for s, ref in ex.map(one, range(0, w.slices, 4)):
+            b, h = divmod(s, w.heads)
+            assert_parity(Hh[b, h], ref, w.dtype, f"long_16k causal slice ({b},{h})")
