@@ -26,10 +26,11 @@
 // goes over B_t (every MMA reading B_t has completed by then).  Shared memory (D = 128): Q, V,
 // U, L, A, B / P, W_pre image, 32 KB each.  Tensor memory: S / C at 0, P at 128, H at 256,
 // W_pre at 384.
-// Warps: 0-3 row warps (TMEM lanes 32w..32w+31: tokens, or anchors for the W_pre image), 4
-// producer (TMA), 5 MMA issuer.  Sums run in a fixed order: results are bit-identical from run
-// to run.  Every wait is bounded; one that gives up sets bit 0 of this kernel's error word and
-// the CTA drains what it has in flight and leaves.
+// Warps: 0-3 row warps (TMEM lanes 32w..32w+31: tokens, or anchors for the W_pre image; a
+// tile's H goes out while the next tile's C runs), 4 producer (TMA), 5 MMA issuer.  Sums run
+// in a fixed order: results are bit-identical from run to run.  Every wait is bounded; one
+// that gives up sets bit 0 of this kernel's error word and the CTA drains what it has in
+// flight and leaves.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "rowops.cuh"
@@ -277,6 +278,26 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
         float a[kMP];
+        // H of tile u out of tensor memory to global (rows past the slice are not stored)
+        auto store_h = [&](int u) -> bool {
+            if (!bwait(h_full, (uint32_t)(u & 1), p.wait_ns)) return false;
+            tc_fence_after();
+            const bool valid_u = u * kT + row < p.n;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.H + ((size_t)slice * p.n + (size_t)(u * kT + row)) * D);
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                float o[32];
+                tmem_ld32(trow + kColH + q * 32, o);
+                tmem_ld_wait();
+                if (valid_u)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) dst[q * 4 + c] = pack8(o + 8 * c);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(h_empty);
+            return true;
+        };
         for (int t = 0; t < T && ok; ++t) {
             const uint32_t ph = (uint32_t)(t & 1);
             const bool valid = t * kT + row < p.n;
@@ -290,11 +311,21 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 const float z = rowops::softmax_unnormalised<kMP>(a, p.m, p.c);
                 rowops::scale_row<kMP>(a, valid ? 1.f / z : 0.f);
             }
-            // the tile before has finished with A, B, P and has added itself to W_pre: the
-            // W_pre image for this tile (anchor rows)
+            // the tile before has finished with A, B, P and has added itself to W_pre
             if (t >= 1) {
                 if (!bwait(w_full, ph ^ 1u, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < kMP / 8; ++c8)
+                *reinterpret_cast<uint4 *>(sm + LY::kOffA + sw_off(row, c8, kT)) = pack8(a + 8 * c8);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full);
+            // while C_t runs: the tile before's H out, and the W_pre image for this tile (anchor rows)
+            if (t >= 1) {
+                if (!store_h(t - 1)) { ok = false; break; }
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     float w[32];
@@ -309,13 +340,6 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 __syncwarp();
                 if (lane == 0) mbar_arrive(wi_full);
             }
-#pragma unroll
-            for (int c8 = 0; c8 < kMP / 8; ++c8)
-                *reinterpret_cast<uint4 *>(sm + LY::kOffA + sw_off(row, c8, kT)) = pack8(a + 8 * c8);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(a_full);
             // Delta^(i) = Delta_pre + C_t[i]; B = A / Delta^(i)
             if (!bwait(c_full, ph, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
@@ -367,25 +391,8 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pm_full);
-            // H_t out
-            if (!bwait(h_full, ph, p.wait_ns)) { ok = false; break; }
-            tc_fence_after();
-            {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.H + ((size_t)slice * p.n + (size_t)(t * kT + row)) * D);
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    float o[32];
-                    tmem_ld32(trow + kColH + q * 32, o);
-                    tmem_ld_wait();
-                    if (valid)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) dst[q * 4 + c] = pack8(o + 8 * c);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(h_empty);
-            }
         }
+        if (ok) store_h(T - 1);  // the last tile's H
         __syncwarp();
     }
     __syncthreads();
