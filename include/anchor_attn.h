@@ -125,10 +125,11 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_backward_f32(const float *Q, co
  *   Delta^(i)_l = sum_{j<=i} A[j][l],  W^(i)_l = sum_{j<=i} A[j][l] v_j,
  *   H[i] = sum_l A[i][l] W^(i)_l / Delta^(i)_l   (0 for an anchor with Delta^(i)_l = 0).
  * The last row equals anchor_attn_forward's last row.  Same layout, shapes, arguments and
- * errors as anchor_attn_forward; bf16 in and out.  With d = 64 and m <= 64 it runs on the
- * tensor cores (bf16 operands, fp32 accumulators; one CTA per slice walks its tiles in order,
- * the running sums inside a tile taken as an MMA with a lower-triangular ones matrix; no
- * workspace); otherwise fp32 CUDA-core arithmetic (a chunked scan over the tokens, one launch,
+ * errors as anchor_attn_forward; bf16 in and out.  With d = 64 and m <= 64, d = 64 and
+ * 64 < m <= 128, or d = 128 and m <= 128 it runs on the tensor cores (bf16 operands, fp32
+ * accumulators; one CTA per slice walks its tiles in order, the running sums inside a tile
+ * taken as an MMA with a lower-triangular ones matrix; no workspace); otherwise fp32 CUDA-core
+ * arithmetic (a chunked scan over the tokens, one launch,
  * one workspace from cudaMallocAsync on `stream`), where shapes whose tiles do not fit one
  * CTA's shared memory return ANCHOR_ATTN_ERR_UNSUPPORTED.  Results are bit-identical from run
  * to run; a bounded wait that gives up is reported by anchor_attn_device_error (bit 0 on the
