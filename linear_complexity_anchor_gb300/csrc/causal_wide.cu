@@ -72,6 +72,7 @@ struct WideLayout {
 
 struct CwParams {
     int heads, n, m, tiles;
+    int chunks;  // CTAs per slice (token chunks); chunk c first sums the tiles before it
     float c;  // scale * log2(e)
     __nv_bfloat16 *H;
     uint64_t wait_ns;
@@ -120,9 +121,13 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     float *sDP = reinterpret_cast<float *>(sm + LY::kOffDP);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int slice = blockIdx.x;
+    const int slice = blockIdx.x / p.chunks, chunk = blockIdx.x - slice * p.chunks;
     const int h = slice % p.heads;
-    const int T = p.tiles;
+    // this CTA's tiles: [t0, t1) of the slice; tiles [0, t0) run first as summary tiles (S,
+    // softmax, C for Delta, W only), which leave W_pre and Delta_pre exactly as a CTA that
+    // ran them in full would (the same MMAs and additions in the same order)
+    const int t0 = (int)((long long)chunk * p.tiles / p.chunks), t1 = (int)((long long)(chunk + 1) * p.tiles / p.chunks);
+    const int T = t1;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -217,7 +222,8 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             bool ok = bwait(u_full, 0u, p.wait_ns);
             auto issue_s = [&](int t) -> bool {  // S_t into the S / C columns
                 if (!bwait(q_full, (uint32_t)(t & 1), p.wait_ns)) return false;
-                if (t >= 1 && !bwait(b_full, (uint32_t)((t - 1) & 1), p.wait_ns)) return false;  // C_{t-1} read
+                // C_{t-1} read (a full tile's C shares S's columns; a summary tile's is in P's)
+                if (t - 1 >= t0 && !bwait(b_full, (uint32_t)((t - 1) & 1), p.wait_ns)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
@@ -229,38 +235,50 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             if (ok) ok = issue_s(0);
             for (int t = 0; t < T && ok; ++t) {
                 const uint32_t ph = (uint32_t)(t & 1);
-                // C_t = L A_t over S_t's columns
+                const bool full = t >= t0;
+                const int u = t - t0;                         // full tile index
+                const int img = u - (t0 == 0 ? 1 : 0);        // W_pre image index (full tiles with t >= 1)
+                // C_t = L A_t over S_t's columns (a summary tile's over P's, so that S_{t+1} need
+                // not wait for it to be read)
                 if (!bwait(a_full, ph, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t ccol = full ? kColSC : kColP;
 #pragma unroll
                 for (int kt = 0; kt < kT / 16; ++kt)
-                    umma_bf16(tmem + kColSC, ldesc + kstep(kt, kT), amn + (uint64_t)(kt * 128), idC, kt > 0 ? 1u : 0u);
+                    umma_bf16(tmem + ccol, ldesc + kstep(kt, kT), amn + (uint64_t)(kt * 128), idC, kt > 0 ? 1u : 0u);
                 umma_commit(c_full);
-                // P_t = B_t A_t^T and H_t = B_t W_pre
-                if (!bwait(b_full, ph, p.wait_ns)) { ok = false; break; }
-                if (t >= 1 && !(bwait(h_empty, ph ^ 1u, p.wait_ns) && bwait(wi_full, ph ^ 1u, p.wait_ns))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                if (full) {
+                    // P_t = B_t A_t^T and H_t = B_t W_pre
+                    if (!bwait(b_full, ph, p.wait_ns)) { ok = false; break; }
+                    if (u >= 1 && !bwait(h_empty, (uint32_t)((u - 1) & 1), p.wait_ns)) { ok = false; break; }
+                    if (t >= 1 && !bwait(wi_full, (uint32_t)(img & 1), p.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kMP / 16; ++kk)
-                    umma_bf16(tmem + kColP, bk + kstep(kk, kT), ak + kstep(kk, kT), idP, kk > 0 ? 1u : 0u);
-                if (t >= 1) {
+                    for (int kk = 0; kk < kMP / 16; ++kk)
+                        umma_bf16(tmem + kColP, bk + kstep(kk, kT), ak + kstep(kk, kT), idP, kk > 0 ? 1u : 0u);
+                    if (t >= 1) {
 #pragma unroll
-                    for (int kj = 0; kj < kMP / 16; ++kj)
-                        umma_bf16(tmem + kColH, bk + kstep(kj, kT), wim + (uint64_t)(kj * 128), idH, kj > 0 ? 1u : 0u);
+                        for (int kj = 0; kj < kMP / 16; ++kj)
+                            umma_bf16(tmem + kColH, bk + kstep(kj, kT), wim + (uint64_t)(kj * 128), idH, kj > 0 ? 1u : 0u);
+                    }
+                    umma_commit(p_full);
                 }
-                umma_commit(p_full);
-                // the next tile's scores while the row warps mask P_t
+                // the next tile's scores while the row warps mask P_t (or once they have read C_t)
                 if (t + 1 < T && !issue_s(t + 1)) { ok = false; break; }
-                // H_t += P_t V_t, then W_pre += A_t^T V_t
-                if (!bwait(pm_full, ph, p.wait_ns) || !bwait(v_full, ph, p.wait_ns)) { ok = false; break; }
-                tc_fence_after();
+                if (full) {
+                    // H_t += P_t V_t
+                    if (!bwait(pm_full, (uint32_t)(u & 1), p.wait_ns) || !bwait(v_full, ph, p.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int kt = 0; kt < kT / 16; ++kt)
-                    umma_bf16(tmem + kColH, bk + kstep(kt, kT), vmn + (uint64_t)(kt * 128), idH, (t > 0 || kt > 0) ? 1u : 0u);
-                umma_commit(h_full);
+                    for (int kt = 0; kt < kT / 16; ++kt)
+                        umma_bf16(tmem + kColH, bk + kstep(kt, kT), vmn + (uint64_t)(kt * 128), idH,
+                                  (t > 0 || kt > 0) ? 1u : 0u);
+                    umma_commit(h_full);
+                } else {
+                    if (!bwait(v_full, ph, p.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                // W_pre += A_t^T V_t
 #pragma unroll
                 for (int kt = 0; kt < kT / 16; ++kt)
                     umma_bf16(tmem + kColW, amn + (uint64_t)(kt * 128), vmn + (uint64_t)(kt * 128), idW,
@@ -278,12 +296,14 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
         float a[kMP];
-        // H of tile u out of tensor memory to global (rows past the slice are not stored)
+        // H of full tile u (slice tile t0 + u) out of tensor memory to global (rows past the
+        // slice are not stored)
         auto store_h = [&](int u) -> bool {
             if (!bwait(h_full, (uint32_t)(u & 1), p.wait_ns)) return false;
             tc_fence_after();
-            const bool valid_u = u * kT + row < p.n;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.H + ((size_t)slice * p.n + (size_t)(u * kT + row)) * D);
+            const int tok = (t0 + u) * kT + row;
+            const bool valid_u = tok < p.n;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.H + ((size_t)slice * p.n + (size_t)tok) * D);
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 float o[32];
@@ -301,6 +321,8 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         for (int t = 0; t < T && ok; ++t) {
             const uint32_t ph = (uint32_t)(t & 1);
             const bool valid = t * kT + row < p.n;
+            const bool full = t >= t0;
+            const int u = t - t0;  // full tile index
             // A_t (fp32, in registers)
             if (!bwait(s_full, ph, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
@@ -323,9 +345,36 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full);
+            if (!full) {
+                // a summary tile: Delta_pre += the tile's column sums (the last row of C_t, in
+                // the P columns), by the last row's warp (tensor-memory loads are warp-wide);
+                // the other warps go on to the next tile
+                if (warp == (kT - 1) / 32) {
+                    if (!bwait(c_full, ph, p.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    const float *dp = sDP + (t & 1) * kMP;
+#pragma unroll
+                    for (int q = 0; q < kMP / 32; ++q) {
+                        float cr[32];
+                        tmem_ld32(trow + kColP + q * 32, cr);
+                        tmem_ld_wait();
+                        if (row == kT - 1)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                sDP[((t + 1) & 1) * kMP + q * 32 + j] = __fadd_rn(dp[q * 32 + j], cr[j]);
+                    }
+                    tc_fence_before();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(b_full);
+                    mbar_arrive(dp_full);
+                }
+                continue;
+            }
             // while C_t runs: the tile before's H out, and the W_pre image for this tile (anchor rows)
             if (t >= 1) {
-                if (!store_h(t - 1)) { ok = false; break; }
+                if (u >= 1 && !store_h(u - 1)) { ok = false; break; }
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     float w[32];
@@ -340,7 +389,9 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 __syncwarp();
                 if (lane == 0) mbar_arrive(wi_full);
             }
-            // Delta^(i) = Delta_pre + C_t[i]; B = A / Delta^(i)
+            // Delta^(i) = Delta_pre + C_t[i]; B = A / Delta^(i).  The first full tile after
+            // summary tiles reads the Delta_pre the last of them wrote.
+            if (u == 0 && t0 > 0 && !bwait(dp_full, (uint32_t)((t0 - 1) & 1), p.wait_ns)) { ok = false; break; }
             if (!bwait(c_full, ph, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             {
@@ -373,7 +424,7 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             // every row warp has read this tile's Delta_pre, and the next tile's is written
             if (!bwait(dp_full, ph, p.wait_ns)) { ok = false; break; }
             // P_t masked to j <= i, over B_t, as the A operand of P V
-            if (!bwait(p_full, ph, p.wait_ns)) { ok = false; break; }
+            if (!bwait(p_full, (uint32_t)(u & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int q = 0; q < kT / 32; ++q) {
@@ -392,7 +443,7 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive(pm_full);
         }
-        if (ok) store_h(T - 1);  // the last tile's H
+        if (ok && t1 > t0) store_h(t1 - t0 - 1);  // the last tile's H
         __syncwarp();
     }
     __syncthreads();
@@ -400,6 +451,16 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// CTAs per slice: with fewer slices than SMs, the tokens of a slice are cut into up to four
+// chunks of at least four tiles, one CTA each (one CTA per SM).  The chunk boundaries do not
+// change the results (each chunk first sums the tiles before it in the same order).
+int causal_wide_chunks(long long slices, int tiles) {
+    long long k = kPlanSMs / (slices > 0 ? slices : 1);
+    k = k < 1 ? 1 : (k > 4 ? 4 : k);
+    while (k > 1 && tiles / k < 4) --k;
+    return (int)k;
 }
 
 template <int D>
@@ -417,10 +478,11 @@ cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     cp.n = p.n;
     cp.m = p.m;
     cp.tiles = (p.n + kT - 1) / kT;
+    cp.chunks = causal_wide_chunks(S, cp.tiles);
     cp.c = p.scale * 1.4426950408889634f;
     cp.H = static_cast<__nv_bfloat16 *>(p.H);
     cp.wait_ns = 2000000000ull;
-    anchor_causal_wide_kernel<D><<<(unsigned)S, kThreads, LY::kSmem, stream>>>(tq, tv, tu, cp);
+    anchor_causal_wide_kernel<D><<<(unsigned)(S * cp.chunks), kThreads, LY::kSmem, stream>>>(tq, tv, tu, cp);
     return cudaGetLastError();
 }
 

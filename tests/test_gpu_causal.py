@@ -174,3 +174,19 @@ def test_causal_long_16k_sampled_slices(env):
         for s, ref in ex.map(one, range(0, w.slices, 4)):
             b, h = divmod(s, w.heads)
             assert_parity(Hh[b, h], ref, w.dtype, f"long_16k causal slice ({b},{h})")
+
+
+def test_causal_wide_chunks_do_not_change_bits(env):
+    """With few slices the 128-anchor kernel cuts each slice's tokens over up to four CTAs (each
+    first sums the tiles before its chunk); with many slices one CTA takes a slice whole.  The
+    same slice gives the same bits either way."""
+    pkg, torch, _ = env
+    w = _w("bf16", 80, 1, 2000, 128, 128)  # 80 slices: one CTA per slice
+    x = gen.make_inputs(w, seed=31)
+    t = {k: to_device(x[k], "bf16", torch) for k in "QUV"}
+    Hall = pkg.causal_forward(t["Q"], t["U"], t["V"], scale=w.scale)
+    for b in (0, 37, 79):  # alone: four chunks of four tiles
+        H1 = pkg.causal_forward(t["Q"][b:b + 1].contiguous(), t["U"], t["V"][b:b + 1].contiguous(), scale=w.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(H1[0].view(torch.int16), Hall[b].view(torch.int16)), f"slice {b}"
+    assert pkg.device_error() == 0
