@@ -196,12 +196,14 @@ constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run wh
 constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)
 constexpr int kUmmaP2Tiles = 16;     // tiles per pass-2 chunk (halved while items are too few)
 constexpr int kUmmaMinTiles = 4;     // smallest chunk either pass is cut into
+constexpr int kUmmaFineSplit = 2;    // pass-2 chunks of the last slices: this many times finer
 constexpr int kPlanSMs = 152;        // SM count the chunking assumes on every device
 constexpr double kStoreABytes = 64.0 * 1024 * 1024;  // largest A copy (all slices) pass 2 reads back
 struct UmmaPlan {
     int MP = 0;              // anchors padded to 64 or 128
     int NT = 0;              // 128-token tiles per slice
     int C1 = 0, C2 = 0;      // chunks per slice in pass 1 / pass 2 (C1 == 1: whole slice per CTA)
+    int S2f = 0, C2f = 0;    // slices from schedule index S2f on take C2f pass-2 chunks
     int total_items = 0;
     size_t header_bytes = 0; // zeroed part of the workspace (ticket, counters, flags)
     size_t abuf_offset = 0;  // the A copy pass 2 reads: [slices][n][MP] bf16 (split slices only)

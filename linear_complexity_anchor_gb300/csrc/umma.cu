@@ -64,6 +64,7 @@ struct UParams {
     int slices, heads, B, n, m;
     float c;                  // scale * log2(e)
     int NT, C1, C2;           // tiles per slice, P1 / P2 chunks per slice (C1 == 1: whole slices)
+    int S2f, C2f;             // slices from schedule index S2f on cut pass 2 into C2f (finer) chunks
     float *part;              // [slices][C1][D/4][MP][4]  W partials (anchor-interleaved float4)
     float *pdelta;            // [slices][C1][MP]     Delta partials
     uint16_t *wimg;           // [slices][D * MP]     W' operand images (bf16, swizzled)
@@ -181,12 +182,19 @@ struct TileRef {
     int chunk;      // pass-1 chunk (partials)
 };
 
+// P2 chunks of a slice: the last slices in schedule order take finer ones, so that the last
+// round of pass-2 items spreads over every SM (the chunking of pass 2 does not change any sum)
+__device__ __forceinline__ int c2_of(int slice, const UParams &p) {
+    const int so = (slice % p.heads) * p.B + slice / p.heads;
+    return so >= p.S2f ? p.C2f : p.C2;
+}
+
 __device__ __forceinline__ int item_tiles(const Item &it, const UParams &p, int &a1, int &b1) {
     if (it.kind == 2) {
         a1 = 0, b1 = p.NT;
         return 2 * p.NT;
     }
-    const int C = it.kind == 0 ? p.C1 : p.C2;
+    const int C = it.kind == 0 ? p.C1 : c2_of(it.slice, p);
     a1 = (int)((long long)it.chunk * p.NT / C);
     b1 = (int)((long long)(it.chunk + 1) * p.NT / C);
     return b1 - a1;
@@ -550,7 +558,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 int sl = 0;
                 if (so < S) {
                     sl = slice_of((int)so, p);
-                    exhausted = vload(p.p2c + 32 * sl) >= (unsigned)p.C2;
+                    exhausted = vload(p.p2c + 32 * sl) >= (unsigned)c2_of(sl, p);
                     ready = !exhausted && vload(p.flags + 32 * sl) != 0u;
                 }
                 const unsigned ex = __ballot_sync(FULLW, exhausted);
@@ -573,7 +581,7 @@ anchor_umma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         if (lane == ln) got = atomicAdd(p.p2c + 32 * sl, 1u);
                         got = __shfl_sync(FULLW, got, ln);
                         const int slr = __shfl_sync(FULLW, sl, ln);
-                        if (got < (unsigned)p.C2) {
+                        if (got < (unsigned)c2_of(slr, p)) {
                             it = {1, slr, (int)got};
                             return 1;
                         }
@@ -1486,6 +1494,8 @@ cudaError_t launch_t(const Problem &pr, const UmmaPlan &pl, const UmmaOptions &o
     p.NT = pl.NT;
     p.C1 = pl.C1;
     p.C2 = pl.C2;
+    p.S2f = pl.S2f;
+    p.C2f = pl.C2f;
     const int grid = (int)std::min<long long>((long long)sms * per_sm, pl.total_items);
     uint8_t *w = static_cast<uint8_t *>(ws);
     // header (zeroed each call): next | head | flags[S] and P2 claim counters[S], one 128-byte
@@ -1573,7 +1583,14 @@ UmmaPlan umma_plan(const Problem &p, bool force_recompute) {
         return pl;
     }
     pl.C2 = (pl.NT + t2 - 1) / t2;
-    pl.total_items = (int)(S * (pl.C1 + pl.C2));
+    // the last slices' pass 2 in chunks kUmmaFineSplit times finer: about a quarter of a round
+    // of pass-2 items' worth of slices, which the SMs freed first share out at the end
+    // (long_16k: 207.0 -> 203.5 us; half a round 204.8, a whole round 207.0, four times finer
+    // 208.4)
+    pl.C2f = std::min(pl.NT, pl.C2 * kUmmaFineSplit);
+    const long long fine = std::min<long long>(S, ((long long)kPlanSMs * t2 / 4 + pl.NT - 1) / pl.NT);
+    pl.S2f = (int)(S - (pl.C2f > pl.C2 ? fine : 0));
+    pl.total_items = (int)(S * pl.C1 + (long long)pl.S2f * pl.C2 + (S - pl.S2f) * (long long)pl.C2f);
     pl.header_bytes = (256 + 2 * 128 * (size_t)S + 4 * (size_t)S * pl.C1 + 1023) / 1024 * 1024;
     const size_t reduce_bytes = 4 * (size_t)S * pl.C1 * MP + 4 * (size_t)S * pl.C1 * p.d * MP + 2 * (size_t)S * p.d * MP;
     pl.abuf_offset = (pl.header_bytes + reduce_bytes + 1023) / 1024 * 1024;
