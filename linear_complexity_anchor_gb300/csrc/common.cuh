@@ -56,6 +56,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // --- SIMT (CUDA-core) variants -------------------------------------------------------
 constexpr int kSimtChunk = 512;                  // tokens per pass-1 chunk of the chunked kernel
 constexpr size_t kSimtMaxSmem = 220 * 1024;      // dynamic shared memory a CUDA-core CTA may use
+constexpr size_t kSimtThirdSmem = 72 * 1024;     // ... when three such CTAs are to share an SM
 // workspace of the chunked kernel: a zeroed header (ticket, per-slice arrival counters and
 // ready flags), the chunk partials [slices][chunks][m d + m] fp32 and W' [slices][m d] fp32
 struct SimtLayout {

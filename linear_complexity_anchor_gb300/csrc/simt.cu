@@ -37,19 +37,27 @@ constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;  // a wait for another CTA's reduction gives up after 2 s
 
 // ------------------------------------------------------------------ whole slice per CTA
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 2)
+// Shared memory of a whole slice: Qs | Vs | Us | Ws | Ds | As, or (kOver) with As laid over Qs
+// (the scores are formed in registers first), small enough for three CTAs per SM.
+template <typename T, bool kOver>
+__device__ __host__ __forceinline__ size_t full_qa_bytes(int n, int m, int d) {
+    const size_t q = sizeof(T) * (size_t)n * (d + pad_elems<T>()), a = 4 * (size_t)n * (m + 1);
+    return kOver ? ((q > a ? q : a) + 15) / 16 * 16 : q;
+}
+
+template <typename T, bool kOver>
+__global__ void __launch_bounds__(kThreads, kOver ? 3 : 2)
 simt_full_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__restrict__ V, T *__restrict__ H,
                  int heads, int n, int m, int d, float scale) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int pitch = d + pad_elems<T>();
     const int ap = m + 1;
     T *Qs = reinterpret_cast<T *>(smem);                    // [n][pitch]
-    T *Vs = Qs + (size_t)n * pitch;                         // [n][pitch]
+    T *Vs = reinterpret_cast<T *>(smem + full_qa_bytes<T, kOver>(n, m, d));  // [n][pitch]
     T *Us = Vs + (size_t)n * pitch;                         // [m][pitch]
     float *Ws = reinterpret_cast<float *>(Us + (size_t)m * pitch);  // [m][d]  A^T V, then W'
     float *Ds = Ws + (size_t)m * d;                         // [m]     Delta
-    float *As = Ds + ((m + 3) & ~3);                        // [n][ap]
+    float *As = kOver ? reinterpret_cast<float *>(smem) : Ds + ((m + 3) & ~3);  // [n][ap]
     const long long slice = blockIdx.x;
     const int h = (int)(slice % heads);
     const size_t off = (size_t)slice * n * d;
@@ -65,7 +73,8 @@ simt_full_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__re
     for (int p = threadIdx.x; p < m * d + m; p += blockDim.x) Ws[p] = 0.f;  // and Ds
     cp_async_wait<1>();
     __syncthreads();
-    scores(Qs, Us, pitch, As, ap, n, m, d, scale);
+    if (kOver) scores_over(Qs, Us, pitch, As, ap, n, m, d, scale);
+    else scores(Qs, Us, pitch, As, ap, n, m, d, scale);
     __syncthreads();
     softmax_rows(As, ap, n, m);
     cp_async_wait<0>();
@@ -210,9 +219,15 @@ simt_chunk_kernel(const T *__restrict__ Q, const T *__restrict__ U, const T *__r
     }
 }
 
-template <typename T> size_t full_smem(int n, int m, int d) {
+template <typename T, bool kOver = false> size_t full_smem(int n, int m, int d) {
     const size_t pitch = d + pad_elems<T>();
-    return sizeof(T) * (2 * (size_t)n + m) * pitch + 4 * ((size_t)m * d + ((m + 3) & ~3) + (size_t)n * (m + 1));
+    return full_qa_bytes<T, kOver>(n, m, d) + sizeof(T) * ((size_t)n + m) * pitch +
+           4 * ((size_t)m * d + ((m + 3) & ~3) + (kOver ? 0 : (size_t)n * (m + 1)));
+}
+// the compact layout when it fits three CTAs per SM and the scores' tiles two per thread
+template <typename T> bool full_over(int n, int m, int d) {
+    return full_smem<T, true>(n, m, d) <= kSimtThirdSmem &&
+           (long long)((n + 3) / 4) * ((m + 3) / 4) <= 2LL * kThreads;
 }
 
 template <typename T> size_t chunk_smem(int m, int d, int tile) {
@@ -226,13 +241,18 @@ template <typename T> int chunk_tile(int m, int d) {
     return 0;
 }
 
+template <typename T, bool kOver>
+cudaError_t full_launch_t(const Problem &p, cudaStream_t stream) {
+    const size_t smem = full_smem<T, kOver>(p.n, p.m, p.d);
+    cudaError_t e =
+        cudaFuncSetAttribute(simt_full_kernel<T, kOver>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(simt_full_kernel<T, kOver>, dim3((unsigned)p.slices()), dim3(kThreads), smem, stream,
+                      (const T *)p.Q, (const T *)p.U, (const T *)p.V, (T *)p.H, p.heads, p.n, p.m, p.d, p.scale);
+}
 template <typename T>
 cudaError_t full_launch(const Problem &p, cudaStream_t stream) {
-    const size_t smem = full_smem<T>(p.n, p.m, p.d);
-    cudaError_t e = cudaFuncSetAttribute(simt_full_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(simt_full_kernel<T>, dim3((unsigned)p.slices()), dim3(kThreads), smem, stream, (const T *)p.Q,
-                      (const T *)p.U, (const T *)p.V, (T *)p.H, p.heads, p.n, p.m, p.d, p.scale);
+    return full_over<T>(p.n, p.m, p.d) ? full_launch_t<T, true>(p, stream) : full_launch_t<T, false>(p, stream);
 }
 
 template <typename T>

@@ -109,6 +109,65 @@ static __device__ __forceinline__ void scores(const T *Qs, const T *Us, int pitc
     }
 }
 
+// scores() for an As laid over Qs: each thread first computes its (at most two) 4 x 4 tiles
+// into registers, then every thread of the CTA meets (all have read Qs), then the tiles are
+// written.  The same sums in the same order as scores().  Needs ceil(rows / 4) ceil(m / 4)
+// <= 2 blockDim.x; every thread of the CTA must call it.
+template <typename T>
+static __device__ __forceinline__ void scores_over(const T *Qs, const T *Us, int pitch, float *As, int ap, int rows, int m,
+                                                   int d, float scale) {
+    const int nct = (m + 3) / 4, nrt = (rows + 3) / 4;
+    float acc[2][4][4];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int t = threadIdx.x + it * blockDim.x;
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[it][a][b] = 0.f;
+        if (t >= nrt * nct) continue;
+        const int rt = t / nct, ct = t - rt * nct;
+        const T *q[4], *u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[i] = Qs + (size_t)min(rt + i * nrt, rows - 1) * pitch;
+            u[i] = Us + (size_t)min(ct + i * nct, m - 1) * pitch;
+        }
+        for (int k = 0; k < d; k += 4) {
+            float4 qa[4], ua[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                qa[i] = ld4(q[i] + k);
+                ua[i] = ld4(u[i] + k);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    float s = acc[it][a][b];
+                    s = __fmaf_rn(qa[a].x, ua[b].x, s);
+                    s = __fmaf_rn(qa[a].y, ua[b].y, s);
+                    s = __fmaf_rn(qa[a].z, ua[b].z, s);
+                    acc[it][a][b] = __fmaf_rn(qa[a].w, ua[b].w, s);
+                }
+        }
+    }
+    __syncthreads();  // Qs is read: As may overwrite it
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int t = threadIdx.x + it * blockDim.x;
+        if (t >= nrt * nct) continue;
+        const int rt = t / nct, ct = t - rt * nct;
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int r = rt + a * nrt, j = ct + b * nct;
+                if (r < rows && j < m) As[(size_t)r * ap + j] = __fmul_rn(scale, acc[it][a][b]);
+            }
+    }
+}
+
 // Row softmax of As in place, one thread per row: A_ij = exp(S_ij - max_j S_ij) * (1 / sum).
 static __device__ __forceinline__ void softmax_rows(float *As, int ap, int rows, int m) {
     for (int r = threadIdx.x; r < rows; r += blockDim.x) {
