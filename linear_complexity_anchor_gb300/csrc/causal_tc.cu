@@ -16,7 +16,8 @@
 //   W_pre += A_t^T V_t, Delta_pre += the tile's column sums (the last row of C_t)
 // The sums over j use the bf16 A_t in every place (C_t, P_t, W_pre), so Delta and W stay
 // consistent; B on the i side is formed from the fp32 A.  Warps: 0-3 row warps (TMEM lanes
-// 32w..32w+31: tokens, or anchors for the W_pre image), 4 producer (TMA ring of [Q_t | V_t]),
+// 32w..32w+31: tokens, or anchors for the W_pre image; a tile's H goes out, and the next W_pre
+// image is written, while the next tile's C runs), 4 producer (TMA ring of [Q_t | V_t]),
 // 5 MMA issuer.  Sums run in a fixed order: results are bit-identical from run to run.  Every
 // wait is bounded; one that gives up sets bit 0 of this kernel's error word and the CTA drains
 // what it has in flight and leaves.
@@ -258,6 +259,24 @@ anchor_causal_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
         float a[64];
+        // H of tile u out of tensor memory to global (rows past the slice are not stored)
+        auto store_h = [&](int u) -> bool {
+            if (!bwait(h_full, (uint32_t)(u & 1), p.wait_ns)) return false;
+            tc_fence_after();
+            float o[64];
+            tmem_ld32(trow + kColH, o);
+            tmem_ld32(trow + kColH + 32, o + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(h_empty);
+            if (u * kT + row < p.n) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.H + ((size_t)slice * p.n + (size_t)(u * kT + row)) * kD);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) dst[c8] = pack8(o + 8 * c8);
+            }
+            return true;
+        };
         for (int t = 0; t < T && ok; ++t) {
             const int s = t & 1;
             const uint32_t ph = (uint32_t)(t & 1);
@@ -275,11 +294,21 @@ anchor_causal_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
                 const float z = rowops::softmax64_unnormalised(a, p.m, p.c);
                 rowops::scale64(a, valid ? 1.f / z : 0.f);
             }
-            // the tile before has finished with A, B, P and has added itself to W_pre: the
-            // W_pre image for this tile (anchor rows, warps 0 and 1)
+            // the tile before has finished with A, B, P and has added itself to W_pre
             if (t >= 1) {
                 if (!bwait(w_full, ph ^ 1u, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                *reinterpret_cast<uint4 *>(sm + kOffA + sw_off(row, c8, kT)) = pack8(a + 8 * c8);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full);
+            // while C_t runs: the tile before's H out, and the W_pre image for this tile (anchor
+            // rows, warps 0 and 1)
+            if (t >= 1) {
+                if (!store_h(t - 1)) { ok = false; break; }
                 if (warp < 2) {
                     float w[64];
                     tmem_ld32(trow + kColW, w);
@@ -294,12 +323,6 @@ anchor_causal_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
                 __syncwarp();
                 if (lane == 0) mbar_arrive(wi_full);
             }
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                *reinterpret_cast<uint4 *>(sm + kOffA + sw_off(row, c8, kT)) = pack8(a + 8 * c8);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(a_full);
             // Delta^(i) = Delta_pre + C_t[i]; B = A / Delta^(i)
             if (!bwait(c_full, ph, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
@@ -350,24 +373,8 @@ anchor_causal_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pm_full);
-            // H_t out
-            if (!bwait(h_full, ph, p.wait_ns)) { ok = false; break; }
-            tc_fence_after();
-            {
-                float o[64];
-                tmem_ld32(trow + kColH, o);
-                tmem_ld32(trow + kColH + 32, o + 32);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(h_empty);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.H + ((size_t)slice * p.n + (size_t)(t * kT + row)) * kD);
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) dst[c8] = pack8(o + 8 * c8);
-                }
-            }
         }
+        if (ok && T > 0) store_h(T - 1);  // the last tile's H
         __syncwarp();
     }
     __syncthreads();
