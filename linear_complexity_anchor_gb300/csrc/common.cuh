@@ -194,7 +194,7 @@ cudaError_t split_read_and_clear_error(unsigned *out);
 
 // --- tensor-core (tcgen05) variant ---------------------------------------------------
 constexpr int kUmmaFullTiles = 4;    // slices of <= 4 tiles (512 tokens) run whole in one CTA
-constexpr int kUmmaP1Tiles = 16;     // tiles per pass-1 chunk (halved while items are too few)
+constexpr int kUmmaP1Tiles = 32;     // tiles per pass-1 chunk (halved while items are too few)
 constexpr int kUmmaP2Tiles = 16;     // tiles per pass-2 chunk (halved while items are too few)
 constexpr int kUmmaMinTiles = 4;     // smallest chunk either pass is cut into
 constexpr int kUmmaFineSplit = 2;    // pass-2 chunks of the last slices: this many times finer
