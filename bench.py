@@ -53,7 +53,7 @@ FMA_LANES_PER_SM = 128          # fp32 FMA lanes per SM (4 sub-partitions x 32)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CSRC = os.path.join(ROOT, "linear_complexity_anchor_gb300", "csrc")
 # the files whose code makes each kernel (a recorded ncu capture stays valid while they hold)
-KERNEL_SOURCES = {"anchor_umma_kernel": ("umma.cu", "ptx.cuh"),
+KERNEL_SOURCES = {"anchor_umma_kernel": ("umma.cu", "ptx.cuh", "common.cuh"),
                   "anchor_stream_kernel": ("stream.cu", "ptx.cuh", "rowops.cuh"),
                   "anchor_split_kernel": ("split.cu", "ptx.cuh", "rowops.cuh"),
                   "anchor_block_kernel": ("block.cu", "ptx.cuh", "rowops.cuh"),
