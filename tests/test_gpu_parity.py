@@ -279,3 +279,34 @@ def test_split_tiles_every_slice(env, shape):
     Hc = H.cpu()
     for s0 in range(0, w.slices, 64):
         assert_slices(Hc, w, oracle_slices(orc, w, x, range(s0, min(w.slices, s0 + 64))), "split")
+
+
+@pytest.mark.parametrize("name", ["det_800x1344", "deit_base", "deit_small"])
+def test_dependent_calls_back_to_back(env, name):
+    """Kernels launched with programmatic stream serialization start while the previous kernel
+    in the stream finishes; each waits for it before touching global memory.  A chain of calls
+    that each read the previous call's output (H as the next Q and V), queued back to back on
+    one stream, gives the same bits as the same calls with a full synchronisation between them."""
+    pkg, torch, _ = env
+    w = gen.WORKLOADS[name]
+    x = gen.make_inputs(w, seed=41)
+    t = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def chain(sync):
+        q, v = t["Q"], t["V"]
+        outs = []
+        for _ in range(4):
+            h = pkg.forward(q, t["U"], v, scale=w.scale, stream=stream)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append(h)
+            q, v = h, h
+        torch.cuda.synchronize()
+        return outs
+
+    queued, synced = chain(False), chain(True)
+    for i, (a, b) in enumerate(zip(queued, synced)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{name}: call {i} differs"
+    assert pkg.device_error() == 0
