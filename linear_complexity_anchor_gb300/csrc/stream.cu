@@ -17,10 +17,13 @@
 // slot is free again as soon as S_t has read it, so the Q loads run further ahead of their
 // use than a shared [Q | V] slot, which only the later W MMA frees, would allow; 9 issues
 // S_t (and the pass-2 H MMAs), 11 issues the W MMAs: a tcgen05.mma holds its issuing thread
-// until the tensor pipe takes it (about 48 cycles at N = 64, 52 at N = 80, whatever the
-// work), so one thread issuing both kinds (12 per tile) set the tile rate.  Pass 1 is then
-// bound by the bytes in flight: the deepest rings that fit shared memory (five slots each,
-// with two row-warp groups; a third group, and so four slots, was slower).
+// until the tensor pipe takes it (about 48 cycles at N = 64, 52 at N = 80), so one thread
+// issuing both kinds (12 per tile) between its waits set the tile rate.  Pass 1 is then bound
+// by the bytes in flight: the deepest rings that fit shared memory (five slots each, with two
+// row-warp groups; a third group, which leaves room for four slots only, was slower, and so
+// was Delta as an MMA of its own over a smaller ones block).  Launched with programmatic
+// stream serialization: the setup overlaps the previous kernel, global memory comes after
+// griddepcontrol.wait.
 // Every wait is bounded; one that gives up sets bit 0 of this kernel's error word and the
 // CTA drains what it has in flight and leaves.
 #include "common.cuh"
