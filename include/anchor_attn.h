@@ -83,6 +83,28 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, con
                                              float scale, void *stream);
 
 /*
+ * Forward from host buffers: Q, U, V and H are host pointers (pinned memory, e.g. from
+ * cudaHostAlloc, for the copies to run asynchronously; pageable memory works but the copies
+ * then hold the calling thread), same layout, shapes, numbers and errors as
+ * anchor_attn_forward (bit-identical results: the same kernels run on device copies).  The
+ * batch is cut into chunks of whole batch entries; chunk by chunk Q and V are copied to the
+ * device on an internal stream, the forward runs on `stream`, and H is copied back on a
+ * second internal stream, over two device buffer sets, so that copies in, forward and copies
+ * out of neighbouring chunks overlap.  Asynchronous: H is complete once `stream` has reached
+ * this point (every internal copy is ordered before it); work already on `stream` is ordered
+ * before the copies.  The device workspace (U and two chunks of Q, V, H) comes from
+ * cudaMallocAsync on `stream` and goes back on it (ANCHOR_ATTN_ERR_ALLOC if it cannot be
+ * had).  Calls on one device take a lock while they enqueue.
+ */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_host(const void *Q, const void *U, const void *V, void *H,
+                                                              int B, int heads, int n, int m, int d, float scale,
+                                                              void *stream);
+/* fp32 forward from host buffers (as anchor_attn_forward_f32, same pipeline). */
+ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_host_f32(const float *Q, const float *U, const float *V,
+                                                                  float *H, int B, int heads, int n, int m, int d,
+                                                                  float scale, void *stream);
+
+/*
  * Backward of anchor_attn_forward, bf16 in and out, fp32 accumulation.  The
  * anchors are fitted by gradient descent (pith.science verdict on arXiv 2505.16463,
  * "core_discovery"; the arXiv abstract, where the anchors are weights of a trainable layer), so a layer

@@ -18,6 +18,7 @@ __all__ = [
     "static_scratch_bytes", "device_error", "query_plan", "status_string", "anchor_attn_test_forward_ptr",
     "AnchorAttnError", "STATUS", "VARIANTS", "backward", "anchor_attn_backward_ptr", "anchor_attn_backward_f32_ptr",
     "full_forward", "relative_error", "causal_forward", "block_forward", "anchor_attn_block_forward_ptr",
+    "forward_host", "anchor_attn_forward_host_ptr", "anchor_attn_forward_host_f32_ptr",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libanchor_attn.so")
@@ -55,7 +56,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             raise RuntimeError(f"anchor_attn CUDA library not built ({p}); run __graft_entry__.build()")
         lib = ctypes.CDLL(p)
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        for name in ("anchor_attn_forward", "anchor_attn_forward_f32", "anchor_attn_forward_static_scratch"):
+        for name in ("anchor_attn_forward", "anchor_attn_forward_f32", "anchor_attn_forward_static_scratch",
+                     "anchor_attn_forward_host", "anchor_attn_forward_host_f32"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
             fn.restype = ctypes.c_int
@@ -109,6 +111,19 @@ def anchor_attn_forward_f32_ptr(Q: int, U: int, V: int, H: int, B: int, heads: i
                                 d: int, scale: float, stream: int = 0) -> int:
     """Raw C-ABI call (fp32 device pointers as integers); returns the status code."""
     return load().anchor_attn_forward_f32(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
+
+
+def anchor_attn_forward_host_ptr(Q: int, U: int, V: int, H: int, B: int, heads: int, n: int, m: int, d: int,
+                                 scale: float, stream: int = 0) -> int:
+    """Raw C-ABI call of the host-buffer forward (bf16 host pointers as integers); returns the
+    status code.  Asynchronous on `stream` (a CUDA stream handle)."""
+    return load().anchor_attn_forward_host(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
+
+
+def anchor_attn_forward_host_f32_ptr(Q: int, U: int, V: int, H: int, B: int, heads: int, n: int, m: int,
+                                     d: int, scale: float, stream: int = 0) -> int:
+    """Raw C-ABI call of the fp32 host-buffer forward; returns the status code."""
+    return load().anchor_attn_forward_host_f32(Q, U, V, H, B, heads, n, m, d, float(scale), stream)
 
 
 def anchor_attn_forward_static_scratch_ptr(Q: int, U: int, V: int, H: int, B: int, heads: int, n: int,
@@ -202,6 +217,43 @@ def forward(Q, U, V, H=None, scale: float | None = None, stream=None):
         else:
             raise TypeError("Q must be bfloat16 or float32")
     _raise(st, "forward")
+    return H
+
+
+def forward_host(Q, U, V, H=None, scale: float | None = None, stream=None, device=None):
+    """The forward on host (CPU) torch tensors (bf16 or fp32; pinned memory for asynchronous
+    copies): the library copies chunks of the batch to the device, runs the forward and copies
+    H back, overlapping the three.  Q, V: [B, heads, n, d]; U: [heads, m, d].  Runs on
+    ``stream`` (a torch.cuda.Stream of ``device``, default the current device's current
+    stream); asynchronous: H is complete once the stream reaches this point."""
+    import torch
+    if H is None:
+        H = torch.empty(Q.shape, dtype=Q.dtype).pin_memory() if Q.is_pinned() else torch.empty_like(Q)
+    for name, t in (("Q", Q), ("U", U), ("V", V), ("H", H)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise TypeError(f"{name} must be a host (CPU) torch.Tensor")
+        if t.dtype != Q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous and of Q's dtype")
+    if Q.dim() != 4 or U.dim() != 3 or V.shape != Q.shape or H.shape != Q.shape:
+        raise ValueError("Q, V, H are [B, heads, n, d]; U is [heads, m, d]")
+    if U.shape[0] != Q.shape[1] or U.shape[2] != Q.shape[3]:
+        raise ValueError("U must be [heads, m, d] matching Q")
+    B, heads, n, d = Q.shape
+    m = U.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        if Q.dtype == torch.bfloat16:
+            st = anchor_attn_forward_host_ptr(Q.data_ptr(), U.data_ptr(), V.data_ptr(), H.data_ptr(), B, heads, n,
+                                              m, d, scale, s.cuda_stream)
+        elif Q.dtype == torch.float32:
+            st = anchor_attn_forward_host_f32_ptr(Q.data_ptr(), U.data_ptr(), V.data_ptr(), H.data_ptr(), B, heads,
+                                                  n, m, d, scale, s.cuda_stream)
+        else:
+            raise TypeError("Q must be bfloat16 or float32")
+    _raise(st, "forward_host")
     return H
 
 

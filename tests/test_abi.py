@@ -142,3 +142,16 @@ def test_block_argument_validation(pkg):
     assert c(H=2 * A) == ALIAS                  # overlaps Wq
     assert c(B=0) == 0 and c(heads=0) == 0 and c(n=0) == 0   # no-ops (no device access)
     assert c(B=0, X=0, H=0) == 0
+
+
+def test_forward_host_validates_before_any_device_call(pkg):
+    """The host-buffer entry checks its arguments as the device entry does, before it touches
+    a device (so these run without one)."""
+    lib = pkg.load()
+    buf = (ctypes.c_uint16 * 1024)()
+    p = ctypes.addressof(buf)
+    assert lib.anchor_attn_forward_host(p, p, p, p, -1, 2, 100, 20, 64, 0.125, None) == 1   # negative B
+    assert lib.anchor_attn_forward_host(p, p, p, p, 1, 1, 10, 4, 48, 0.125, None) == 2      # d = 48
+    assert lib.anchor_attn_forward_host(p, p, p, p, 0, 2, 100, 20, 64, 0.125, None) == 0    # empty: a no-op
+    assert lib.anchor_attn_forward_host(None, p, p, p, 1, 2, 100, 20, 64, 0.125, None) == 1  # null Q
+    assert lib.anchor_attn_forward_host_f32(p, p, p, p, 1, 1, 10, 4, 64, float("nan"), None) == 1
