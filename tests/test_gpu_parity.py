@@ -310,3 +310,32 @@ def test_dependent_calls_back_to_back(env, name):
     for i, (a, b) in enumerate(zip(queued, synced)):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{name}: call {i} differs"
     assert pkg.device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["det_800x1344", "deit_base", "deit_small", "long_16k"])
+def test_graph_capture_replays_the_same_bits(env, name):
+    """The forward calls can be captured in a CUDA graph (the stream-ordered workspace becomes
+    graph allocation nodes, programmatic launches become programmatic edges) and replayed:
+    every replay gives the bits of the eager call."""
+    pkg, torch, _ = env
+    w = gen.WORKLOADS[name]
+    x = gen.make_inputs(w, seed=61)
+    t = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    ref = pkg.forward(t["Q"], t["U"], t["V"], scale=w.scale, stream=stream)
+    ref2 = pkg.forward(ref, t["U"], ref, scale=w.scale, stream=stream)
+    torch.cuda.synchronize()
+    H1, H2 = torch.empty_like(ref), torch.empty_like(ref)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        pkg.forward(t["Q"], t["U"], t["V"], H=H1, scale=w.scale, stream=stream)
+        pkg.forward(H1, t["U"], H1, H=H2, scale=w.scale, stream=stream)
+    for _ in range(3):
+        H1.zero_()
+        H2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(H1.view(torch.int16), ref.view(torch.int16)), name
+        assert torch.equal(H2.view(torch.int16), ref2.view(torch.int16)), name
+    assert pkg.device_error() == 0
