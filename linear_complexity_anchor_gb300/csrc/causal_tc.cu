@@ -148,6 +148,9 @@ anchor_causal_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t sbase = smem_u32(sm);
+    // launched with programmatic stream serialization: global memory only from here on
+    grid_dependency_wait();
+    grid_dependents_launch();
 
     if (warp == kWarpProducer) {
         if (lane == 0) {
@@ -404,8 +407,7 @@ cudaError_t launch_causal_tc(const Problem &p, cudaStream_t stream) {
     cp.c = p.scale * 1.4426950408889634f;
     cp.H = static_cast<__nv_bfloat16 *>(p.H);
     cp.wait_ns = 2000000000ull;
-    anchor_causal_tc_kernel<<<(unsigned)S, kThreads, kSmem, stream>>>(tq, tv, tu, cp);
-    return cudaGetLastError();
+    return launch_pdl(anchor_causal_tc_kernel, dim3((unsigned)S), dim3(kThreads), kSmem, stream, tq, tv, tu, cp);
 }
 
 cudaError_t causal_tc_read_and_clear_error(unsigned *out) {

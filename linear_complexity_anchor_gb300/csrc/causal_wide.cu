@@ -171,6 +171,9 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t sbase = smem_u32(sm);
+    // launched with programmatic stream serialization: global memory only from here on
+    grid_dependency_wait();
+    grid_dependents_launch();
 
     if (warp == kWarpProducer) {
         if (lane == 0) {
@@ -482,8 +485,8 @@ cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     cp.c = p.scale * 1.4426950408889634f;
     cp.H = static_cast<__nv_bfloat16 *>(p.H);
     cp.wait_ns = 2000000000ull;
-    anchor_causal_wide_kernel<D><<<(unsigned)(S * cp.chunks), kThreads, LY::kSmem, stream>>>(tq, tv, tu, cp);
-    return cudaGetLastError();
+    return launch_pdl(anchor_causal_wide_kernel<D>, dim3((unsigned)(S * cp.chunks)), dim3(kThreads), LY::kSmem, stream,
+                      tq, tv, tu, cp);
 }
 
 }  // namespace

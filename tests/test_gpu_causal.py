@@ -190,3 +190,32 @@ def test_causal_wide_chunks_do_not_change_bits(env):
         torch.cuda.synchronize()
         assert torch.equal(H1[0].view(torch.int16), Hall[b].view(torch.int16)), f"slice {b}"
     assert pkg.device_error() == 0
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 700, 49, 64), (1, 2, 2100, 100, 128)])
+def test_causal_dependent_calls_back_to_back(env, shape):
+    """The masked kernels start while the previous kernel in the stream finishes and wait for
+    it before touching global memory: a chain of calls that each read the previous output
+    gives the same bits queued back to back as with a synchronisation between them."""
+    pkg, torch, _ = env
+    w = _w("bf16", *shape)
+    x = gen.make_inputs(w, seed=71)
+    t = {k: to_device(x[k], "bf16", torch) for k in "QUV"}
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def chain(sync):
+        q, v, outs = t["Q"], t["V"], []
+        for _ in range(4):
+            with torch.cuda.stream(stream):
+                h = pkg.causal_forward(q, t["U"], v, scale=w.scale)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append(h)
+            q, v = h, h
+        torch.cuda.synchronize()
+        return outs
+
+    for a, b in zip(chain(False), chain(True)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert pkg.device_error() == 0
