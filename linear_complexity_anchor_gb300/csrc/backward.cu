@@ -337,6 +337,9 @@ template <typename T>
 __global__ void __launch_bounds__(32 * kDuGroups)
 anchor_bwd_du_kernel(const float *__restrict__ dupart, T *__restrict__ dU, int B, int heads, int chunks, int md) {
     __shared__ float part[kDuGroups][32];
+    // launched with programmatic stream serialization after the kernel that writes dupart
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int h = blockIdx.y, lane = threadIdx.x & 31, g = threadIdx.x >> 5;
     const int e = blockIdx.x * 32 + lane;
     const int K = B * chunks;
@@ -432,11 +435,10 @@ cudaError_t launch_bwd_du_sum(const float *dupart, void *dU, int B, int heads, i
                               cudaStream_t stream) {
     const dim3 grid((md + 31) / 32, heads);
     if (f32)
-        anchor_bwd_du_kernel<float><<<grid, 32 * kDuGroups, 0, stream>>>(dupart, (float *)dU, B, heads, chunks, md);
-    else
-        anchor_bwd_du_kernel<__nv_bfloat16><<<grid, 32 * kDuGroups, 0, stream>>>(dupart, (__nv_bfloat16 *)dU, B,
-                                                                                 heads, chunks, md);
-    return cudaGetLastError();
+        return launch_pdl(anchor_bwd_du_kernel<float>, grid, dim3(32 * kDuGroups), 0, stream, dupart, (float *)dU, B,
+                          heads, chunks, md);
+    return launch_pdl(anchor_bwd_du_kernel<__nv_bfloat16>, grid, dim3(32 * kDuGroups), 0, stream, dupart,
+                      (__nv_bfloat16 *)dU, B, heads, chunks, md);
 }
 
 cudaError_t bwd_read_and_clear_error(unsigned *out) {

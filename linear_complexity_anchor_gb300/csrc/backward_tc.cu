@@ -171,6 +171,9 @@ anchor_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t sbase = smem_u32(sm);
+    // launched with programmatic stream serialization: global memory only from here on
+    grid_dependency_wait();
+    grid_dependents_launch();
 
     if (warp == kWarpProducer) {
         if (lane == 0) {
@@ -492,8 +495,9 @@ cudaError_t launch_bwd_tc(const BwdProblem &p, void *workspace, cudaStream_t str
     bp.dQ = static_cast<__nv_bfloat16 *>(p.dQ);
     bp.dV = static_cast<__nv_bfloat16 *>(p.dV);
     bp.wait_ns = 2000000000ull;
-    anchor_bwd_tc_kernel<<<(unsigned)S, kThreads, kSmem, stream>>>(tq, tv, tdh, tu, bp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(anchor_bwd_tc_kernel, dim3((unsigned)S), dim3(kThreads), kSmem, stream, tq, tv, tdh, tu, bp)) !=
+        cudaSuccess)
+        return e;
     return launch_bwd_du_sum(bp.dupart, p.dU, p.B, p.heads, 1, p.m * kD, false, stream);
 }
 

@@ -136,3 +136,35 @@ def test_backward_empty_and_rejected(env):
     st = pkg.anchor_attn_backward_ptr(Q.data_ptr(), U.data_ptr(), Q.data_ptr(), Q.data_ptr(), Q.data_ptr(),
                                       dU.data_ptr(), Q.data_ptr() + 16 * 64, 1, 2, 10, 4, 64, 0.125, 0)
     assert st == 3, "an output over an input is rejected"
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 197, 30, 64), (1, 2, 700, 64, 64)])
+def test_backward_dependent_calls_back_to_back(env, shape):
+    """The backward's two kernels (and the next call's) start while the kernel before them in
+    the stream finishes and wait for it before touching global memory: calls that each take the
+    previous call's dQ as their upstream gradient give the same bits queued back to back as
+    with a synchronisation between them."""
+    pkg, torch, _ = env
+    B, heads, n, m, d = shape
+    w = gen.WORKLOADS["vit14_f32"].with_(name="bwd_chain", B=B, heads=heads, n=n, m=m, d=d, dtype="bf16")
+    x = gen.make_inputs(w, seed=81)
+    t = {k: to_device(x[k], "bf16", torch) for k in "QUV"}
+    dH0 = to_device(gen.make_inputs(w.with_(name="bwd_dh"), seed=82)["V"], "bf16", torch)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def chain(sync):
+        dh, outs = dH0, []
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                dQ, dU, dV = pkg.backward(t["Q"], t["U"], t["V"], dh, scale=w.scale)
+            if sync:
+                torch.cuda.synchronize()
+            outs += [dQ, dU, dV]
+            dh = dQ
+        torch.cuda.synchronize()
+        return outs
+
+    for a, b in zip(chain(False), chain(True)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert pkg.device_error() == 0
