@@ -305,15 +305,20 @@ anchor_attn_status_t backward(const anchor::BwdProblem &p, void *stream_v) {
             if (anchor::overlaps(out[o], out_bytes[o], out[o2], out_bytes[o2])) return ANCHOR_ATTN_ERR_ALIAS;
     }
     const bool tc = anchor::bwd_tc_supported(p);
-    if (!tc && !anchor::bwd_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
+    const bool wide = !tc && anchor::bwd_wide_supported(p);
+    if (!tc && !wide && !anchor::bwd_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
     void *ws = nullptr;
     if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
-    const size_t wsb = tc ? anchor::bwd_tc_workspace(p) : anchor::bwd_layout(p).total_bytes;
+    const size_t wsb = tc     ? anchor::bwd_tc_workspace(p)
+                       : wide ? anchor::bwd_wide_workspace(p)
+                              : anchor::bwd_layout(p).total_bytes;
     if (cudaMallocAsync(&ws, wsb, stream) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_ALLOC;
     }
-    cudaError_t e = tc ? anchor::launch_bwd_tc(p, ws, stream) : anchor::launch_bwd(p, ws, stream);
+    cudaError_t e = tc     ? anchor::launch_bwd_tc(p, ws, stream)
+                    : wide ? anchor::launch_bwd_wide(p, ws, stream)
+                           : anchor::launch_bwd(p, ws, stream);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = ef;
     if (e != cudaSuccess) {
@@ -425,17 +430,18 @@ anchor_attn_status_t anchor_attn_query_plan(int dtype, int B, int heads, int n, 
 
 anchor_attn_status_t anchor_attn_device_error(unsigned *code) {
     if (!code) return ANCHOR_ATTN_ERR_INVALID_ARG;
-    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0, l = 0, q = 0, r = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0, f = 0, g = 0, k = 0, l = 0, q = 0, r = 0, w = 0;
     if (cudaDeviceSynchronize() != cudaSuccess || anchor::umma_read_and_clear_error(&a) != cudaSuccess ||
         anchor::simt_read_and_clear_error(&b) != cudaSuccess || anchor::bwd_read_and_clear_error(&c) != cudaSuccess ||
         anchor::causal_read_and_clear_error(&e) != cudaSuccess || anchor::block_read_and_clear_error(&f) != cudaSuccess ||
         anchor::bwd_tc_read_and_clear_error(&g) != cudaSuccess || anchor::causal_tc_read_and_clear_error(&k) != cudaSuccess ||
         anchor::stream_read_and_clear_error(&l) != cudaSuccess || anchor::split_read_and_clear_error(&q) != cudaSuccess ||
-        anchor::causal_wide_read_and_clear_error(&r) != cudaSuccess) {
+        anchor::causal_wide_read_and_clear_error(&r) != cudaSuccess ||
+        anchor::bwd_wide_read_and_clear_error(&w) != cudaSuccess) {
         cudaGetLastError();
         return ANCHOR_ATTN_ERR_CUDA;
     }
-    *code = a | b | c | e | f | g | k | l | q | r;
+    *code = a | b | c | e | f | g | k | l | q | r | w;
     return ANCHOR_ATTN_OK;
 }
 

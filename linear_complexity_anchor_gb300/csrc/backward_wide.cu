@@ -1,0 +1,772 @@
+// Backward of the anchor-attention forward on the tensor cores for d = 128 and m <= 128 (bf16
+// operands, fp32 accumulators in tensor memory), any n.  For an upstream gradient dH of
+// H = A Delta^{-1} (A^T V), A = rowsoftmax(scale Q U^T):
+//   dW' = A^T dH,  dW = Delta^{-1} dW',  dDelta_j = -sum_k dW_jk W'_jk,
+//   G = dH W'^T + V dW^T + 1 dDelta^T,  dS = A o (G - rowsum(A o G)),
+//   dQ = scale dS U,  dV = A dW,  dU = scale dS^T Q summed over the batch entries of a head
+// (the anchors are fitted by gradient descent: pith.science verdict on arXiv 2505.16463,
+// "core_discovery"; the arXiv abstract, where the anchors are weights of a trainable layer).
+//
+// At d = m = 128 one CTA cannot hold a slice's whole backward (the four W', dW images alone
+// take 128 KB of shared memory, and the accumulators S, G, dQ, dV and dU 640 tensor-memory
+// columns), so the work runs as three kernels over items (a slice's run of consecutive
+// 128-token tiles; the chunking depends on the shape alone, so the sums and the bits do too):
+//   pass 1   S_t = Q_t U^T, A_t = softmax; [W | dW'] += A_t^T [V_t | dH_t] (one N = 256 MMA)
+//            and Delta += A_t^T 1, with A as hi + lo bf16 parts; the item's W, dW', Delta go
+//            to a workspace row block
+//   reduce   per slice: the items' blocks summed in order; W' = W / Delta, dW = dW' / Delta
+//            as hi + lo bf16 images [4][128][128], and dDelta (fp32)
+//   pass 2   S_t and A_t again; G_t = dH_t (W'_hi + W'_lo)^T + V_t (dW_hi + dW_lo)^T with the
+//            images streamed through a two-slot ring (from L2: every item of a slice reads
+//            the same 128 KB); dS_t on CUDA cores in fp32; dV_t = A_t dW, dQ_t = dS_t U,
+//            dU += dS_t^T Q_t; the item's dU to a workspace block, summed per head by the
+//            backward's dU kernel in (batch entry, item) order
+// The fp32 operands that the gradients sum over many terms - A in pass 1, W' and dW in G, dS
+// in dQ and dU - enter the MMAs as two bf16 parts, hi = bf16(x) and lo = bf16(x - hi): with
+// any one of them rounded once to bf16, dU of the 16384-token workload (four batch entries)
+// comes out at 0.8 to 1.1 of the bf16 tolerance in a float64 emulation; with all of them split
+// at 0.003.
+// Pass 2's shared memory (U | two Q-or-A buffers | V, dH or dS | image ring) fills 224 KB:
+// tile t's Q and A_t take turns in the two buffers (A_t goes where Q_{t-1} was; Q_{t+1} goes
+// where A_t was, once dV_t is done), and dS_t is written over V_t and dH_t once G_t is done.
+// Tensor memory (512 columns): S | G, then dQ | dV | dU.
+// Warps: 0-3 row warps (TMEM lanes 32w..32w+31: tokens, or anchors for the item's sums),
+// 4 producer (TMA), 5 MMA issuer.  Every wait is bounded; one that gives up sets bit 0 of the
+// error word and the CTA drains what it has in flight and leaves.
+#include "common.cuh"
+#include "ptx.cuh"
+#include "rowops.cuh"
+
+#include <math.h>
+
+namespace anchor {
+
+__device__ unsigned int g_bwd_wide_error;  // bit 0: a pipeline wait gave up
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kT = 128, kD = 128, kMP = 128;
+constexpr int kThreads = 192;
+constexpr int kWarpProducer = 4, kWarpMma = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBlkB = kT * 128;   // one 64-column block of a 128-row bf16 tile (16 KB)
+constexpr int kTileB = 2 * kBlkB; // a [128][128] bf16 tile (32 KB)
+constexpr int kPartF = kMP * 2 * kD + kMP;  // an item's pass-1 block: [W | dW'] rows, then Delta
+
+// pass 1: U | Q | V dH | A_hi | A_lo | ones [16][128] | barriers
+constexpr int k1U = 0, k1Q = k1U + kTileB, k1VH = k1Q + kTileB, k1AH = k1VH + 2 * kTileB, k1AL = k1AH + kTileB;
+constexpr int k1Ones = k1AL + kTileB, k1Bar = k1Ones + 4096;
+constexpr int k1Bars = 10;
+constexpr int k1Smem = k1Bar + k1Bars * 8 + 16 + 1024;
+static_assert(k1Smem <= 227 * 1024, "pass 1 shared memory");
+constexpr uint32_t k1ColS = 0, k1ColWD = 128, k1ColDelta = 384;
+
+// pass 2: U | X0 X1 (Q or A) | V dH, then dS_hi dS_lo | image ring (2 x 32 KB) | dDelta | barriers
+constexpr int k2U = 0, k2X = k2U + kTileB, k2VH = k2X + 2 * kTileB, k2Img = k2VH + 2 * kTileB;
+constexpr int k2DD = k2Img + 2 * kTileB, k2Bar = k2DD + kMP * 4;
+constexpr int k2Bars = 24;
+constexpr int k2Smem = k2Bar + k2Bars * 8 + 16 + 1024;
+static_assert(k2Smem <= 227 * 1024, "pass 2 shared memory");
+constexpr uint32_t k2ColS = 0, k2ColG = 128, k2ColDV = 256, k2ColDU = 384;  // dQ_t reuses G's columns
+
+struct BwParams {
+    int heads, n, m, tiles, chunks;
+    float c;      // scale * log2(e)
+    float scale;
+    float *part;           // pass 1: [slices * chunks][kPartF]
+    const float *ddelta;   // pass 2: [slices][kMP]
+    float *dupart;         // pass 2: [slices][chunks][m][kD]
+    __nv_bfloat16 *dQ, *dV;
+    uint64_t wait_ns;
+};
+
+// byte offset of 16-byte chunk c (0..15) of row r in a swizzled [rows][128] bf16 tile stored as
+// two 64-column blocks of rows x 128 bytes (the layout a TMA load of the tile produces)
+__device__ __forceinline__ uint32_t sw_off(int r, int c, int rows) {
+    return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+// descriptor advance for K step kk (16 elements) of a K-major [128 rows][128] swizzled tile
+__device__ __forceinline__ uint64_t kstep(int kk) { return (uint64_t)((((kk >> 2) * kT * 128) + (kk & 3) * 32) >> 4); }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 pack8(const float *x, float r) {
+    return make_uint4(pack2(x[0] * r, x[1] * r), pack2(x[2] * r, x[3] * r), pack2(x[4] * r, x[5] * r),
+                      pack2(x[6] * r, x[7] * r));
+}
+// bf16 parts of 8 floats: hi = round(x), lo = round(x - hi)
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+    float r[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = x[i] - __bfloat162float(__float2bfloat16_rn(x[i]));
+    hi = pack8(x, 1.f);
+    lo = pack8(r, 1.f);
+}
+
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, par)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(bar, par, 2000)) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(&g_bwd_wide_error, 1u);
+            return false;
+        }
+    }
+    return true;
+}
+
+// the two TMA boxes (64 columns each) of a [128][128] bf16 tile
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int row, int outer,
+                                          uint64_t pol) {
+    tma_load_3d(dst, map, bar, 0, row, outer, pol);
+    tma_load_3d(dst + kBlkB, map, bar, 64, row, outer, pol);
+}
+
+// the item's tiles: [t0, t1) of slice `slice` (chunks of balanced integer length)
+struct Item {
+    int slice, chunk, t0, nt;
+};
+__device__ __forceinline__ Item item_of(int b, int tiles, int chunks) {
+    Item it;
+    it.slice = b / chunks;
+    it.chunk = b - it.slice * chunks;
+    it.t0 = (int)((long long)it.chunk * tiles / chunks);
+    it.nt = (int)((long long)(it.chunk + 1) * tiles / chunks) - it.t0;
+    return it;
+}
+
+// the row softmax of 128 scores in place (anchors >= m masked); a row past the slice is zero
+__device__ __forceinline__ void softmax128(float (&v)[128], int m, float c, bool valid) {
+    const float z = rowops::softmax_unnormalised<128>(v, m, c);
+    rowops::scale_row<128>(v, valid ? 1.f / z : 0.f);
+}
+
+// a row of 128 fp32 values as hi and lo bf16 rows of two swizzled [128][128] tiles
+__device__ __forceinline__ void store_split128(uint8_t *hi, uint8_t *lo, int row, const float *x) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        uint4 h, l;
+        split8(x + 8 * c, h, l);
+        *reinterpret_cast<uint4 *>(hi + sw_off(row, c, kT)) = h;
+        *reinterpret_cast<uint4 *>(lo + sw_off(row, c, kT)) = l;
+    }
+}
+
+// ------------------------------------------------------------------------------ pass 1
+__global__ void __launch_bounds__(kThreads, 1)
+anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
+                          const __grid_constant__ CUtensorMap tdh, const __grid_constant__ CUtensorMap tu,
+                          const BwParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k1Bar);
+    uint64_t *u_full = bars + 0, *q_full = bars + 1, *q_empty = bars + 2, *vh_full = bars + 3, *vh_empty = bars + 4;
+    uint64_t *s_full = bars + 5, *a_full = bars + 6, *a_empty = bars + 7, *acc_full = bars + 8, *mma_done = bars + 9;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k1Bars);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Item it = item_of(blockIdx.x, p.tiles, p.chunks);
+    const int h = it.slice % p.heads;
+
+    if (threadIdx.x == 0) {
+        mbar_init(u_full, 1);
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        mbar_init(vh_full, 1);
+        mbar_init(vh_empty, 1);
+        mbar_init(s_full, 1);
+        mbar_init(a_full, 4);
+        mbar_init(a_empty, 1);
+        mbar_init(acc_full, 1);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) tmem_alloc(s_tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t sbase = smem_u32(sm);
+    // launched with programmatic stream serialization: global memory only from here on
+    grid_dependency_wait();
+    grid_dependents_launch();
+
+    if (warp == kWarpProducer) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tv);
+            tma_prefetch_desc(&tdh);
+            tma_prefetch_desc(&tu);
+            const uint64_t pol_keep = policy_evict_last();
+            mbar_arrive_expect_tx(u_full, kTileB);
+            load_tile(sm + k1U, &tu, u_full, 0, h, pol_keep);
+            int nq = 0, nvh = 0;
+            for (int i = 0; i < it.nt; ++i) {
+                const int row = (it.t0 + i) * kT;
+                if (i >= 1 && !bwait(q_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(q_full, kTileB);
+                load_tile(sm + k1Q, &tq, q_full, row, it.slice, pol_keep);
+                ++nq;
+                if (i >= 1 && !bwait(vh_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(vh_full, 2 * kTileB);
+                load_tile(sm + k1VH, &tv, vh_full, row, it.slice, pol_keep);
+                load_tile(sm + k1VH + kTileB, &tdh, vh_full, row, it.slice, pol_keep);
+                ++nvh;
+            }
+            // the CTA leaves only once its copies have landed
+            if (nq > 0) bwait(q_full, (uint32_t)((nq - 1) & 1), p.wait_ns);
+            if (nvh > 0) bwait(vh_full, (uint32_t)((nvh - 1) & 1), p.wait_ns);
+            bwait(u_full, 0u, p.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);       // [tokens x anchors], K = d
+            const uint32_t idWD = idesc_bf16_f32(kMP, 2 * kD, true, true);     // A^T [V | dH], K = tokens
+            const uint32_t idDl = idesc_bf16_f32(kMP, 16, true, false);        // A^T 1
+            const uint64_t udesc = smem_desc_sw128(sbase + k1U, 16, 1024);
+            const uint64_t qdesc = smem_desc_sw128(sbase + k1Q, 16, 1024);
+            const uint64_t vhdesc = smem_desc_sw128(sbase + k1VH, kBlkB, 1024);  // N = 256: V | dH blocks
+            const uint64_t odesc = smem_desc_sw128(sbase + k1Ones, 16, 1024);
+            bool ok = bwait(u_full, 0u, p.wait_ns);
+            auto issue_s = [&](int i) -> bool {
+                if (!bwait(q_full, (uint32_t)(i & 1), p.wait_ns)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    umma_bf16(tmem + k1ColS, qdesc + kstep(kk), udesc + kstep(kk), idS, kk > 0 ? 1u : 0u);
+                umma_commit(s_full);
+                umma_commit(q_empty);
+                return true;
+            };
+            if (ok && it.nt > 0) ok = issue_s(0);
+            for (int i = 0; i < it.nt && ok; ++i) {
+                // the row warps have read S_i and written A_i
+                if (!bwait(a_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                if (i + 1 < it.nt && !issue_s(i + 1)) { ok = false; break; }
+                if (!bwait(vh_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint64_t adesc = smem_desc_sw128(sbase + (part ? k1AL : k1AH), kBlkB, 1024);  // A^T, MN-major
+#pragma unroll
+                    for (int kt = 0; kt < kT / 16; ++kt) {
+                        const uint32_t acc = (i > 0 || part > 0 || kt > 0) ? 1u : 0u;
+                        const uint64_t ak = adesc + (uint64_t)(kt * 128);
+                        umma_bf16(tmem + k1ColWD, ak, vhdesc + (uint64_t)(kt * 128), idWD, acc);
+                        umma_bf16(tmem + k1ColDelta, ak, odesc + (uint64_t)((((kt >> 2) * 2048) + (kt & 3) * 32) >> 4),
+                                  idDl, acc);
+                    }
+                }
+                umma_commit(a_empty);
+                umma_commit(vh_empty);
+            }
+            if (ok) umma_commit(acc_full);
+            umma_commit(mma_done);
+            bwait(mma_done, 0u, p.wait_ns);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ row warps
+        const int row = warp * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        {   // the ones operand [16][128] (every element 1)
+            const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+            for (int i = row; i < 4096 / 16; i += 128) reinterpret_cast<uint4 *>(sm + k1Ones)[i] = ones;
+        }
+        bool ok = true;
+        float v[128];
+        for (int i = 0; i < it.nt && ok; ++i) {
+            if (!bwait(s_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(trow + k1ColS + 32 * q, v + 32 * q);
+            tmem_ld_wait();
+            softmax128(v, p.m, p.c, (it.t0 + i) * kT + row < p.n);
+            if (i >= 1 && !bwait(a_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
+            store_split128(sm + k1AH, sm + k1AL, row, v);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full);
+        }
+        // the item's W | dW' | Delta: anchor j = row
+        ok = ok && it.nt > 0 && bwait(acc_full, 0u, p.wait_ns);
+        if (ok) {
+            tc_fence_after();
+            float *dst = p.part + (size_t)blockIdx.x * kPartF;
+#pragma unroll 1
+            for (int q = 0; q < 8; ++q) {
+                tmem_ld32(trow + k1ColWD + 32 * q, v);
+                tmem_ld_wait();
+                float4 *o = reinterpret_cast<float4 *>(dst + (size_t)row * 2 * kD + 32 * q);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            }
+            tmem_ld32(trow + k1ColDelta, v);
+            tmem_ld_wait();
+            dst[kMP * 2 * kD + row] = v[0];
+            tc_fence_before();
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------------ reduce
+// One CTA per slice, thread k = column k: W, dW' and Delta summed over the slice's items in
+// item order; W' = W / Delta and dW = dW' / Delta as hi + lo bf16 images (rows >= m and anchors
+// with Delta = 0 are zero), dDelta_j = -sum_k dW_jk W'_jk in fp32 (a fixed warp tree, then the
+// four warps in order).
+__global__ void __launch_bounds__(kD)
+anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m, __nv_bfloat16 *__restrict__ img,
+                              float *__restrict__ ddelta) {
+    __shared__ float s_rinv[kMP];
+    __shared__ float s_red[kD / 32][kMP];
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int slice = blockIdx.x, k = threadIdx.x, lane = k & 31, warp = k >> 5;
+    const float *P = part + (size_t)slice * chunks * kPartF;
+    {
+        float dl = 0.f;
+        for (int c = 0; c < chunks; ++c) dl = __fadd_rn(dl, P[(size_t)c * kPartF + kMP * 2 * kD + k]);
+        s_rinv[k] = (k < m && dl != 0.f) ? 1.f / dl : 0.f;
+    }
+    __syncthreads();
+    __nv_bfloat16 *I = img + (size_t)slice * 4 * kMP * kD;
+    for (int j = 0; j < kMP; ++j) {
+        float w = 0.f, dw = 0.f;
+        for (int c = 0; c < chunks; ++c) {
+            const float *r = P + (size_t)c * kPartF + (size_t)j * 2 * kD;
+            w = __fadd_rn(w, r[k]);
+            dw = __fadd_rn(dw, r[kD + k]);
+        }
+        const float rinv = s_rinv[j];
+        const float wp = w * rinv, dwv = dw * rinv;
+        const __nv_bfloat16 wh = __float2bfloat16_rn(wp), dh = __float2bfloat16_rn(dwv);
+        I[(size_t)(0 * kMP + j) * kD + k] = wh;
+        I[(size_t)(1 * kMP + j) * kD + k] = __float2bfloat16_rn(wp - __bfloat162float(wh));
+        I[(size_t)(2 * kMP + j) * kD + k] = dh;
+        I[(size_t)(3 * kMP + j) * kD + k] = __float2bfloat16_rn(dwv - __bfloat162float(dh));
+        float pr = dwv * wp;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) pr += __shfl_xor_sync(0xffffffffu, pr, o);
+        if (lane == 0) s_red[warp][j] = pr;
+    }
+    __syncthreads();
+    if (k < kMP) {
+        float dd = s_red[0][k];
+#pragma unroll
+        for (int w = 1; w < kD / 32; ++w) dd = __fadd_rn(dd, s_red[w][k]);
+        ddelta[(size_t)slice * kMP + k] = s_rinv[k] != 0.f ? -dd : 0.f;
+    }
+}
+
+// ------------------------------------------------------------------------------ pass 2
+__global__ void __launch_bounds__(kThreads, 1)
+anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
+                          const __grid_constant__ CUtensorMap tdh, const __grid_constant__ CUtensorMap tu,
+                          const __grid_constant__ CUtensorMap timg, const BwParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k2Bar);
+    uint64_t *u_full = bars + 0, *q_full = bars + 1 /* [2] */, *xq_free = bars + 3 /* [2] */,
+             *xa_free = bars + 5 /* [2] */, *vh_full = bars + 7, *vh_free = bars + 8, *img_full = bars + 9 /* [2] */,
+             *img_empty = bars + 11 /* [2] */, *s_full = bars + 13, *s_empty = bars + 14, *g_full = bars + 15,
+             *g_empty = bars + 16, *a_full = bars + 17, *dv_full = bars + 18, *dv_empty = bars + 19,
+             *ds_full = bars + 20, *dq_full = bars + 21, *du_full = bars + 22, *mma_done = bars + 23;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k2Bars);
+    float *sDD = reinterpret_cast<float *>(sm + k2DD);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Item it = item_of(blockIdx.x, p.tiles, p.chunks);
+    const int h = it.slice % p.heads;
+
+    if (threadIdx.x == 0) {
+        mbar_init(u_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(q_full + b, 1);
+            mbar_init(xq_free + b, 1);
+            mbar_init(xa_free + b, 1);
+            mbar_init(img_full + b, 1);
+            mbar_init(img_empty + b, 1);
+        }
+        mbar_init(vh_full, 1);
+        mbar_init(vh_free, 1);
+        mbar_init(s_full, 1);
+        mbar_init(s_empty, 4);
+        mbar_init(g_full, 1);
+        mbar_init(g_empty, 4);
+        mbar_init(a_full, 4);
+        mbar_init(dv_full, 1);
+        mbar_init(dv_empty, 4);
+        mbar_init(ds_full, 4);
+        mbar_init(dq_full, 1);
+        mbar_init(du_full, 1);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) tmem_alloc(s_tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t sbase = smem_u32(sm);
+    grid_dependency_wait();
+    grid_dependents_launch();
+
+    if (warp == kWarpProducer) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tv);
+            tma_prefetch_desc(&tdh);
+            tma_prefetch_desc(&tu);
+            tma_prefetch_desc(&timg);
+            const uint64_t pol_keep = policy_evict_last(), pol_once = policy_evict_first();
+            mbar_arrive_expect_tx(u_full, kTileB);
+            load_tile(sm + k2U, &tu, u_full, 0, h, pol_keep);
+            int nq[2] = {0, 0}, nvh = 0, nimg[2] = {0, 0};
+            bool ok = true;
+            for (int i = 0; i < it.nt && ok; ++i) {
+                const int row = (it.t0 + i) * kT, b = i & 1;
+                // Q_i into X[b] once dV_{i-1} has read A_{i-1} there
+                if (i >= 1 && !bwait(xq_free + b, (uint32_t)(((i - 1) >> 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(q_full + b, kTileB);
+                load_tile(sm + k2X + b * kTileB, &tq, q_full + b, row, it.slice, pol_once);
+                ++nq[b];
+                // V_i, dH_i once dQ_{i-1} and dU have read dS_{i-1} there
+                if (i >= 1 && !bwait(vh_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(vh_full, 2 * kTileB);
+                load_tile(sm + k2VH, &tv, vh_full, row, it.slice, pol_once);
+                load_tile(sm + k2VH + kTileB, &tdh, vh_full, row, it.slice, pol_once);
+                ++nvh;
+                // the images W'_hi, W'_lo, dW_hi, dW_lo (unit u = 4 i + part, slot u & 1)
+                for (int part = 0; part < 4; ++part) {
+                    const int u = 4 * i + part, s = u & 1;
+                    if (u >= 2 && !bwait(img_empty + s, (uint32_t)(((u >> 1) - 1) & 1), p.wait_ns)) { ok = false; break; }
+                    mbar_arrive_expect_tx(img_full + s, kTileB);
+                    load_tile(sm + k2Img + s * kTileB, &timg, img_full + s, 0, it.slice * 4 + part, pol_keep);
+                    ++nimg[s];
+                }
+            }
+            for (int b = 0; b < 2; ++b) {
+                if (nq[b] > 0) bwait(q_full + b, (uint32_t)((nq[b] - 1) & 1), p.wait_ns);
+                if (nimg[b] > 0) bwait(img_full + b, (uint32_t)((nimg[b] - 1) & 1), p.wait_ns);
+            }
+            if (nvh > 0) bwait(vh_full, (uint32_t)((nvh - 1) & 1), p.wait_ns);
+            bwait(u_full, 0u, p.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);  // [tokens x anchors], K = d
+            const uint32_t idR = idesc_bf16_f32(kT, kD, false, true);    // [tokens x d], K = anchors
+            const uint32_t idU = idesc_bf16_f32(kMP, kD, true, true);    // dS^T Q: anchors x d, K = tokens
+            const uint64_t udesc = smem_desc_sw128(sbase + k2U, 16, 1024);      // U, K-major (N = anchors)
+            const uint64_t umn = smem_desc_sw128(sbase + k2U, kBlkB, 1024);     // U, MN-major (N = d)
+            const uint64_t vk = smem_desc_sw128(sbase + k2VH, 16, 1024);
+            const uint64_t hk = smem_desc_sw128(sbase + k2VH + kTileB, 16, 1024);
+            bool ok = bwait(u_full, 0u, p.wait_ns);
+            for (int i = 0; i < it.nt && ok; ++i) {
+                const int b = i & 1;
+                const uint32_t xq = sbase + k2X + b * kTileB, xa = sbase + k2X + (b ^ 1) * kTileB;
+                // S_i = Q_i U^T
+                if (!bwait(q_full + b, (uint32_t)((i >> 1) & 1), p.wait_ns)) { ok = false; break; }
+                if (i >= 1 && !bwait(s_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+                {
+                    const uint64_t qd = smem_desc_sw128(xq, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        umma_bf16(tmem + k2ColS, qd + kstep(kk), udesc + kstep(kk), idS, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(s_full);
+                // G_i = dH_i (W'_hi + W'_lo)^T + V_i (dW_hi + dW_lo)^T, once dQ_{i-1} left G's columns
+                if (!bwait(vh_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                if (i >= 1 && !bwait(g_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
+                for (int part = 0; part < 4 && ok; ++part) {
+                    const int u = 4 * i + part, s = u & 1;
+                    if (!bwait(img_full + s, (uint32_t)((u >> 1) & 1), p.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = part < 2 ? hk : vk;
+                    const uint64_t bd = smem_desc_sw128(sbase + k2Img + s * kTileB, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        umma_bf16(tmem + k2ColG, ad + kstep(kk), bd + kstep(kk), idS, (part > 0 || kk > 0) ? 1u : 0u);
+                    if (part < 2) umma_commit(img_empty + s);  // W' parts: the slot takes a dW part next
+                }
+                if (!ok) break;
+                umma_commit(g_full);
+                // dV_i = A_i (dW_hi + dW_lo) (the dW parts are in slots 0 and 1)
+                if (!bwait(a_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                if (i >= 1 && !bwait(dv_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+                {
+                    const uint64_t ak = smem_desc_sw128(xa, 16, 1024);
+#pragma unroll
+                    for (int s = 0; s < 2; ++s) {
+                        const uint64_t dwm = smem_desc_sw128(sbase + k2Img + s * kTileB, kBlkB, 1024);
+#pragma unroll
+                        for (int kj = 0; kj < kMP / 16; ++kj)
+                            umma_bf16(tmem + k2ColDV, ak + kstep(kj), dwm + (uint64_t)(kj * 128), idR,
+                                      (s > 0 || kj > 0) ? 1u : 0u);
+                    }
+                }
+                umma_commit(dv_full);
+                umma_commit(img_empty + 0);
+                umma_commit(img_empty + 1);
+                umma_commit(xq_free + (b ^ 1));  // A_i read: Q_{i+1} may load there
+                // dQ_i = dS_i U (into G's columns) and dU += dS_i^T Q_i, dS_i over V_i and dH_i
+                if (!bwait(ds_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+                {
+                    const uint64_t qm = smem_desc_sw128(xq, kBlkB, 1024);  // Q_i, MN-major (N = d)
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t da = sbase + k2VH + part * kTileB;
+                        const uint64_t dsk = smem_desc_sw128(da, 16, 1024);
+                        const uint64_t dsm = smem_desc_sw128(da, kBlkB, 1024);  // dS^T: anchors x tokens
+#pragma unroll
+                        for (int kj = 0; kj < kMP / 16; ++kj)
+                            umma_bf16(tmem + k2ColG, dsk + kstep(kj), umn + (uint64_t)(kj * 128), idR,
+                                      (part > 0 || kj > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int kt = 0; kt < kT / 16; ++kt)
+                            umma_bf16(tmem + k2ColDU, dsm + (uint64_t)(kt * 128), qm + (uint64_t)(kt * 128), idU,
+                                      (i > 0 || part > 0 || kt > 0) ? 1u : 0u);
+                    }
+                }
+                umma_commit(dq_full);
+                umma_commit(vh_free);
+                umma_commit(xa_free + b);  // Q_i read: A_{i+1} may be written there
+            }
+            if (ok && it.nt > 0) umma_commit(du_full);
+            umma_commit(mma_done);
+            bwait(mma_done, 0u, p.wait_ns);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ row warps
+        const int row = warp * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        sDD[row] = p.ddelta[(size_t)it.slice * kMP + row];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        bool ok = true;
+        float a[128];
+        // dQ_i and dV_i from tensor memory to global memory (16-byte stores from the row)
+        auto drain = [&](int i) -> bool {
+            if (!bwait(dq_full, (uint32_t)(i & 1), p.wait_ns)) return false;
+            tc_fence_after();
+            const bool valid = (it.t0 + i) * kT + row < p.n;
+            const size_t off = ((size_t)it.slice * p.n + (size_t)((it.t0 + i) * kT + row)) * kD;
+            float o[32];
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                tmem_ld32(trow + k2ColG + 32 * q, o);
+                tmem_ld_wait();
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + off + 32 * q);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) dst[c8] = pack8(o + 8 * c8, p.scale);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(g_empty);
+            if (!bwait(dv_full, (uint32_t)(i & 1), p.wait_ns)) return false;
+            tc_fence_after();
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                tmem_ld32(trow + k2ColDV + 32 * q, o);
+                tmem_ld_wait();
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.dV + off + 32 * q);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) dst[c8] = pack8(o + 8 * c8, 1.f);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dv_empty);
+            return true;
+        };
+        for (int i = 0; i < it.nt && ok; ++i) {
+            const int b = i & 1;
+            if (!bwait(s_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(trow + k2ColS + 32 * q, a + 32 * q);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty);
+            softmax128(a, p.m, p.c, (it.t0 + i) * kT + row < p.n);
+            // A_i (bf16) into X[b ^ 1], once dU has read Q_{i-1} there
+            if (i >= 1 && !bwait(xa_free + (b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), p.wait_ns)) { ok = false; break; }
+            {
+                uint8_t *xa = sm + k2X + (b ^ 1) * kTileB;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4 *>(xa + sw_off(row, c, kT)) = pack8(a + 8 * c, 1.f);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full);
+            if (i >= 1 && !drain(i - 1)) { ok = false; break; }
+            // dS_j = A_j (G_j + dDelta_j - sum_l A_l (G_l + dDelta_l)), over V_i and dH_i
+            if (!bwait(g_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+            tc_fence_after();
+            float g[32];
+            float rs = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                tmem_ld32(trow + k2ColG + 32 * q, g);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) rs = fmaf(a[32 * q + j], g[j] + sDD[32 * q + j], rs);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                tmem_ld32(trow + k2ColG + 32 * q, g);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) g[j] = a[32 * q + j] * (g[j] + sDD[32 * q + j] - rs);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 hi, lo;
+                    split8(g + 8 * c, hi, lo);
+                    *reinterpret_cast<uint4 *>(sm + k2VH + sw_off(row, 4 * q + c, kT)) = hi;
+                    *reinterpret_cast<uint4 *>(sm + k2VH + kTileB + sw_off(row, 4 * q + c, kT)) = lo;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ds_full);
+        }
+        if (ok && it.nt >= 1) ok = drain(it.nt - 1);
+        // the item's dU (scale dS^T Q): anchor j = row
+        ok = ok && it.nt > 0 && bwait(du_full, 0u, p.wait_ns);
+        if (ok) {
+            tc_fence_after();
+            float o[32];
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                tmem_ld32(trow + k2ColDU + 32 * q, o);
+                tmem_ld_wait();
+                if (row < p.m) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        p.dupart + ((size_t)blockIdx.x * p.m + row) * kD + 32 * q);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(o[4 * k] * p.scale, o[4 * k + 1] * p.scale, o[4 * k + 2] * p.scale,
+                                             o[4 * k + 3] * p.scale);
+                }
+            }
+            tc_fence_before();
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// items per slice: the split of the slice's tiles into `chunks` runs that keeps the most
+// loaded SM's work (whole waves of kPlanSMs one-CTA-per-SM items, each its tiles plus about
+// one tile's worth of setup and partial traffic) smallest; from the shape alone
+int wide_chunks(long long slices, int tiles) {
+    int best = 1;
+    long long best_cost = -1;
+    for (int c = 1; c <= tiles && c <= 64; ++c) {
+        const long long waves = (slices * c + kPlanSMs - 1) / kPlanSMs;
+        const long long cost = waves * ((tiles + c - 1) / c + 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = c;
+        }
+    }
+    return best;
+}
+
+struct WideWs {
+    size_t part = 0, img = 0, dd = 0, du = 0, total = 0;
+};
+WideWs wide_ws(const BwdProblem &p, int chunks) {
+    auto up = [](size_t x) { return (x + 1023) / 1024 * 1024; };
+    const size_t S = (size_t)p.slices();
+    WideWs w;
+    w.part = 0;
+    w.img = up(w.part + 4 * S * chunks * (size_t)kPartF);
+    w.dd = up(w.img + 2 * S * 4 * kMP * kD);
+    w.du = up(w.dd + 4 * S * kMP);
+    w.total = w.du + 4 * S * chunks * (size_t)p.m * kD;
+    return w;
+}
+
+}  // namespace
+
+bool bwd_wide_supported(const BwdProblem &p) { return !p.f32 && p.d == kD && p.m >= 1 && p.m <= kMP && p.n >= 1; }
+
+size_t bwd_wide_workspace(const BwdProblem &p) {
+    return wide_ws(p, wide_chunks(p.slices(), (p.n + kT - 1) / kT)).total;
+}
+
+cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t stream) {
+    const long long S = p.slices();
+    const int tiles = (p.n + kT - 1) / kT;
+    const int chunks = wide_chunks(S, tiles);
+    const WideWs L = wide_ws(p, chunks);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    CUtensorMap tq, tv, tdh, tu, timg;
+    if (!make_bf16_map(&tq, p.Q, kD, p.n, S, kT) || !make_bf16_map(&tv, p.V, kD, p.n, S, kT) ||
+        !make_bf16_map(&tdh, p.dH, kD, p.n, S, kT) || !make_bf16_map(&tu, p.U, kD, p.m, p.heads, kMP) ||
+        !make_bf16_map(&timg, ws + L.img, kD, kMP, S * 4, kMP))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(anchor_bwd_wide_p1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, k1Smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(anchor_bwd_wide_p2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, k2Smem);
+    if (e != cudaSuccess) return e;
+    BwParams bp;
+    bp.heads = p.heads;
+    bp.n = p.n;
+    bp.m = p.m;
+    bp.tiles = tiles;
+    bp.chunks = chunks;
+    bp.c = p.scale * 1.4426950408889634f;
+    bp.scale = p.scale;
+    bp.part = reinterpret_cast<float *>(ws + L.part);
+    bp.ddelta = reinterpret_cast<const float *>(ws + L.dd);
+    bp.dupart = reinterpret_cast<float *>(ws + L.du);
+    bp.dQ = static_cast<__nv_bfloat16 *>(p.dQ);
+    bp.dV = static_cast<__nv_bfloat16 *>(p.dV);
+    bp.wait_ns = 2000000000ull;
+    const dim3 grid((unsigned)(S * chunks));
+    if ((e = launch_pdl(anchor_bwd_wide_p1_kernel, grid, dim3(kThreads), k1Smem, stream, tq, tv, tdh, tu, bp)) !=
+        cudaSuccess)
+        return e;
+    if ((e = launch_pdl(anchor_bwd_wide_reduce_kernel, dim3((unsigned)S), dim3(kD), 0, stream,
+                        (const float *)bp.part, chunks, p.m, reinterpret_cast<__nv_bfloat16 *>(ws + L.img),
+                        reinterpret_cast<float *>(ws + L.dd))) != cudaSuccess)
+        return e;
+    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel, grid, dim3(kThreads), k2Smem, stream, tq, tv, tdh, tu, timg, bp)) !=
+        cudaSuccess)
+        return e;
+    return launch_bwd_du_sum(bp.dupart, p.dU, p.B, p.heads, chunks, p.m * kD, false, stream);
+}
+
+cudaError_t bwd_wide_read_and_clear_error(unsigned *out) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_bwd_wide_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_bwd_wide_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace anchor

@@ -96,6 +96,13 @@ bool bwd_tc_supported(const BwdProblem &p);
 size_t bwd_tc_workspace(const BwdProblem &p);
 cudaError_t launch_bwd_tc(const BwdProblem &p, void *workspace, cudaStream_t stream);
 cudaError_t bwd_tc_read_and_clear_error(unsigned *out);
+// the backward on the tensor cores for d = 128, m <= 128 (bf16): pass 1, a per-slice reduce,
+// pass 2 and the dU sum; workspace = the items' pass-1 blocks, the slices' W' and dW images,
+// dDelta and the items' dU blocks
+bool bwd_wide_supported(const BwdProblem &p);
+size_t bwd_wide_workspace(const BwdProblem &p);
+cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t stream);
+cudaError_t bwd_wide_read_and_clear_error(unsigned *out);
 
 // --- masked (causal) variant (CUDA-core) ------------------------------------------------
 // workspace: a zeroed header, the chunks' totals [slices][chunks][m + m d] and their

@@ -1,7 +1,7 @@
 """GPU: the backward (dQ, dU, dV) through the C ABI against the oracle's backward, element by
 element, on the same seeded inputs (the oracle's backward is pinned by finite differences of
-the forward oracle in test_oracle_backward_pins.py).  bf16 with d = 64 and m <= 64 runs on the
-tensor cores; the rest, and fp32, on CUDA cores."""
+the forward oracle in test_oracle_backward_pins.py).  bf16 with d = 64 and m <= 64, and bf16
+with d = 128 and m <= 128, run on the tensor cores; the rest, and fp32, on CUDA cores."""
 import os
 from concurrent.futures import ThreadPoolExecutor
 
@@ -84,6 +84,53 @@ def test_backward_tensor_core_shapes(env, shape):
     assert env[0].device_error() == 0
 
 
+# d = 128 tensor-core path: one token; exactly one tile; a ragged second tile; a long slice
+# cut into many items; one anchor; many batch entries summed into dU; fewer anchors than 64
+_WIDE_SHAPES = [(3, 2, 1, 7, 128), (2, 2, 128, 128, 128), (1, 3, 129, 49, 128), (1, 1, 2000, 128, 128),
+                (2, 2, 300, 1, 128), (16, 2, 197, 100, 128), (1, 2, 5000, 40, 128)]
+
+
+@pytest.mark.parametrize("shape", _WIDE_SHAPES)
+def test_backward_wide_tensor_core_shapes(env, shape):
+    got, ref, _ = _case(env, "bf16", *shape, seed=sum(shape) + 2)
+    for name, g, r in zip(("dQ", "dU", "dV"), got, ref):
+        assert_parity(to_host64(g), r, "bf16", f"{name} {shape}")
+    assert env[0].device_error() == 0
+
+
+def test_backward_long_16k_sampled_heads(env):
+    """Full size (4 x 16 slices of 16384 tokens, 128 anchors, d = 128): dQ and dV of every
+    batch entry of three heads element by element, and those heads' dU against the sum of
+    their four slices' shares."""
+    pkg, torch, orc = env
+    w = gen.WORKLOADS["long_16k"]
+    x = gen.make_inputs(w, seed=0)
+    dH = gen.make_inputs(w.with_(name="bwd_dh"), seed=1000)["V"]
+    t = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    dQ, dU, dV = pkg.backward(t["Q"], t["U"], t["V"], to_device(dH, w.dtype, torch), scale=w.scale)
+    torch.cuda.synchronize()
+    assert pkg.device_error() == 0
+    heads = [0, 7, w.heads - 1]
+    dQh = {(b, h): to_host64(dQ[b, h]) for b in range(w.B) for h in heads}
+    dVh = {(b, h): to_host64(dV[b, h]) for b in range(w.B) for h in heads}
+    dUh = to_host64(dU)
+    U = gen.to_float64(x["U"], w.dtype)
+
+    def one(bh):
+        b, h = bh
+        f = lambda a: gen.to_float64(a[b, h], w.dtype)
+        return bh, orc.slice_backward(f(x["Q"]), U[h], f(x["V"]), f(dH), w.scale)
+
+    dU_ref = {h: np.zeros(U.shape[1:]) for h in heads}
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as ex:
+        for (b, h), (rq, ru, rv) in ex.map(one, [(b, h) for b in range(w.B) for h in heads]):
+            assert_parity(dQh[b, h], rq, w.dtype, f"long_16k dQ slice ({b},{h})")
+            assert_parity(dVh[b, h], rv, w.dtype, f"long_16k dV slice ({b},{h})")
+            dU_ref[h] += ru
+    for h in heads:
+        assert_parity(dUh[h], dU_ref[h], w.dtype, f"long_16k dU head {h}")
+
+
 @pytest.mark.parametrize("name", ["deit_small", "deit_base", "det_800x1344"])
 def test_backward_workload_every_slice(env, name):
     """Full size: every slice's dQ and dV against the oracle element by element, and dU
@@ -116,7 +163,8 @@ def test_backward_workload_every_slice(env, name):
 
 def test_backward_bit_stable(env):
     pkg, torch, _ = env
-    for shape in [(2, 3, 1500, 64, 64), (2, 3, 1500, 100, 64)]:  # tensor-core and CUDA-core paths
+    # tensor-core paths (d = 64, d = 128) and the CUDA-core path
+    for shape in [(2, 3, 1500, 64, 64), (2, 3, 1500, 100, 128), (2, 3, 1500, 100, 64)]:
         got1, _, (t, tdH, sc) = _case(env, "bf16", *shape, seed=9)
         got2 = pkg.backward(t["Q"], t["U"], t["V"], tdH, scale=sc)
         torch.cuda.synchronize()
@@ -138,7 +186,7 @@ def test_backward_empty_and_rejected(env):
     assert st == 3, "an output over an input is rejected"
 
 
-@pytest.mark.parametrize("shape", [(2, 3, 197, 30, 64), (1, 2, 700, 64, 64)])
+@pytest.mark.parametrize("shape", [(2, 3, 197, 30, 64), (1, 2, 700, 64, 64), (2, 2, 900, 128, 128)])
 def test_backward_dependent_calls_back_to_back(env, shape):
     """The backward's two kernels (and the next call's) start while the kernel before them in
     the stream finishes and wait for it before touching global memory: calls that each take the
