@@ -11,9 +11,10 @@
 // take 128 KB of shared memory, and the accumulators S, G, dQ, dV and dU 640 tensor-memory
 // columns), so the work runs as three kernels over items (a slice's run of consecutive
 // 128-token tiles; the chunking depends on the shape alone, so the sums and the bits do too):
-//   pass 1   S_t = Q_t U^T, A_t = softmax; [W | dW'] += A_t^T [V_t | dH_t] (one N = 256 MMA)
-//            and Delta += A_t^T 1, with A as hi + lo bf16 parts; the item's W, dW', Delta go
-//            to a workspace row block
+//   pass 1   S_t = Q_t U^T, A_t = softmax; W += A_t^T V_t with Delta += A_t^T 1, then
+//            dW' += A_t^T dH_t, with A as hi + lo bf16 parts (Q, V, dH in buffers of their own,
+//            each refilled as soon as its products are done); the item's W, dW', Delta go to
+//            a workspace row block
 //   reduce   per slice: the items' blocks summed in order; W' = W / Delta, dW = dW' / Delta
 //            as hi + lo bf16 images [4][128][128], and dDelta (fp32)
 //   pass 2   S_t and A_t again; G_t = dH_t (W'_hi + W'_lo)^T + V_t (dW_hi + dW_lo)^T with the
@@ -26,10 +27,10 @@
 // any one of them rounded once to bf16, dU of the 16384-token workload (four batch entries)
 // comes out at 0.8 to 1.1 of the bf16 tolerance in a float64 emulation; with all of them split
 // at 0.003.
-// Pass 2's shared memory (U | two Q-or-A buffers | V, dH or dS | image ring) fills 224 KB:
-// tile t's Q and A_t take turns in the two buffers (A_t goes where Q_{t-1} was; Q_{t+1} goes
-// where A_t was, once dV_t is done), and dS_t is written over V_t and dH_t once G_t is done.
-// Tensor memory (512 columns): S | G, then dQ | dV | dU.
+// Pass 2's shared memory (U | two Q buffers | V or dS_hi | dH or dS_lo | image ring) fills
+// 224 KB: dS_t is written over V_t and dH_t once G_t is done, and A_t (bf16) over S_t in
+// tensor memory, where dV_t reads it.  Tensor memory (512 columns): S then A | G then dQ | dV |
+// dU.
 // Warps: 0-3 row warps (TMEM lanes 32w..32w+31: tokens, or anchors for the item's sums),
 // 4 producer (TMA), 5 MMA issuer.  Every wait is bounded; one that gives up sets bit 0 of the
 // error word and the CTA drains what it has in flight and leaves.
@@ -55,10 +56,10 @@ constexpr int kBlkB = kT * 128;   // one 64-column block of a 128-row bf16 tile 
 constexpr int kTileB = 2 * kBlkB; // a [128][128] bf16 tile (32 KB)
 constexpr int kPartF = kMP * 2 * kD + kMP;  // an item's pass-1 block: [W | dW'] rows, then Delta
 
-// pass 1: U | Q | V dH | A_hi | A_lo | ones [16][128] | barriers
+// pass 1: U | Q | V | dH | A_hi | A_lo | ones [16][128] | barriers
 constexpr int k1U = 0, k1Q = k1U + kTileB, k1VH = k1Q + kTileB, k1AH = k1VH + 2 * kTileB, k1AL = k1AH + kTileB;
 constexpr int k1Ones = k1AL + kTileB, k1Bar = k1Ones + 4096;
-constexpr int k1Bars = 10;
+constexpr int k1Bars = 12;
 constexpr int k1Smem = k1Bar + k1Bars * 8 + 16 + 1024;
 static_assert(k1Smem <= 227 * 1024, "pass 1 shared memory");
 constexpr uint32_t k1ColS = 0, k1ColWD = 128, k1ColDelta = 384;
@@ -66,10 +67,13 @@ constexpr uint32_t k1ColS = 0, k1ColWD = 128, k1ColDelta = 384;
 // pass 2: U | X0 X1 (Q or A) | V dH, then dS_hi dS_lo | image ring (2 x 32 KB) | dDelta | barriers
 constexpr int k2U = 0, k2X = k2U + kTileB, k2VH = k2X + 2 * kTileB, k2Img = k2VH + 2 * kTileB;
 constexpr int k2DD = k2Img + 2 * kTileB, k2Bar = k2DD + kMP * 4;
-constexpr int k2Bars = 24;
+constexpr int k2Bars = 27;
 constexpr int k2Smem = k2Bar + k2Bars * 8 + 16 + 1024;
 static_assert(k2Smem <= 227 * 1024, "pass 2 shared memory");
 constexpr uint32_t k2ColS = 0, k2ColG = 128, k2ColDV = 256, k2ColDU = 384;  // dQ_t reuses G's columns
+// pass 2 warps: 0-7 row warps (two per TMEM lane quarter, one per half of the columns), 8
+// producer, 9 MMA issuer
+constexpr int k2Threads = 320, kWarp2Producer = 8, kWarp2Mma = 9;
 
 struct BwParams {
     int heads, n, m, tiles, chunks;
@@ -119,11 +123,35 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limi
     return true;
 }
 
+// two TMEM columns of this warp's 32 lanes from / to two registers of each lane
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, float a, float b) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(__float_as_uint(a)),
+                 "r"(__float_as_uint(b))
+                 : "memory");
+}
+__device__ __forceinline__ float2 tmem_ld2(uint32_t taddr) {
+    uint32_t x, y;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(taddr));
+    return make_float2(__uint_as_float(x), __uint_as_float(y));
+}
+
 // the two TMA boxes (64 columns each) of a [128][128] bf16 tile
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int row, int outer,
                                           uint64_t pol) {
     tma_load_3d(dst, map, bar, 0, row, outer, pol);
     tma_load_3d(dst + kBlkB, map, bar, 64, row, outer, pol);
+}
+
+// an L2 prefetch of the two boxes of a [128][128] bf16 tile (no shared memory, no completion):
+// the kernels keep one tile of each input in shared memory, so the load of the next one is
+// issued late and would otherwise wait out the full memory latency
+__device__ __forceinline__ void prefetch_tile(const CUtensorMap *map, int row, int outer) {
+#pragma unroll
+    for (int c0 = 0; c0 < 128; c0 += 64)
+        asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                         reinterpret_cast<uint64_t>(map)),
+                     "r"(c0), "r"(row), "r"(outer)
+                     : "memory");
 }
 
 // the item's tiles: [t0, t1) of slice `slice` (chunks of balanced integer length)
@@ -164,8 +192,9 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k1Bar);
-    uint64_t *u_full = bars + 0, *q_full = bars + 1, *q_empty = bars + 2, *vh_full = bars + 3, *vh_empty = bars + 4;
-    uint64_t *s_full = bars + 5, *a_full = bars + 6, *a_empty = bars + 7, *acc_full = bars + 8, *mma_done = bars + 9;
+    uint64_t *u_full = bars + 0, *q_full = bars + 1, *q_empty = bars + 2, *v_full = bars + 3, *v_empty = bars + 4;
+    uint64_t *h_full = bars + 5, *h_empty = bars + 6, *s_full = bars + 7, *a_full = bars + 8, *a_empty = bars + 9;
+    uint64_t *acc_full = bars + 10, *mma_done = bars + 11;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k1Bars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Item it = item_of(blockIdx.x, p.tiles, p.chunks);
@@ -175,8 +204,10 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         mbar_init(u_full, 1);
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        mbar_init(vh_full, 1);
-        mbar_init(vh_empty, 1);
+        mbar_init(v_full, 1);
+        mbar_init(v_empty, 1);
+        mbar_init(h_full, 1);
+        mbar_init(h_empty, 1);
         mbar_init(s_full, 1);
         mbar_init(a_full, 4);
         mbar_init(a_empty, 1);
@@ -203,33 +234,45 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             const uint64_t pol_keep = policy_evict_last();
             mbar_arrive_expect_tx(u_full, kTileB);
             load_tile(sm + k1U, &tu, u_full, 0, h, pol_keep);
-            int nq = 0, nvh = 0;
+            int nq = 0, nv = 0, nh = 0;
             for (int i = 0; i < it.nt; ++i) {
                 const int row = (it.t0 + i) * kT;
+                // the tiles two ahead (and, at the start, the next) into L2
+                for (int k = i == 0 ? 1 : 2; k <= 2; ++k)
+                    if (i + k < it.nt) {
+                        prefetch_tile(&tq, row + k * kT, it.slice);
+                        prefetch_tile(&tv, row + k * kT, it.slice);
+                        prefetch_tile(&tdh, row + k * kT, it.slice);
+                    }
                 if (i >= 1 && !bwait(q_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
                 mbar_arrive_expect_tx(q_full, kTileB);
                 load_tile(sm + k1Q, &tq, q_full, row, it.slice, pol_keep);
                 ++nq;
-                if (i >= 1 && !bwait(vh_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(vh_full, 2 * kTileB);
-                load_tile(sm + k1VH, &tv, vh_full, row, it.slice, pol_keep);
-                load_tile(sm + k1VH + kTileB, &tdh, vh_full, row, it.slice, pol_keep);
-                ++nvh;
+                if (i >= 1 && !bwait(v_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(v_full, kTileB);
+                load_tile(sm + k1VH, &tv, v_full, row, it.slice, pol_keep);
+                ++nv;
+                if (i >= 1 && !bwait(h_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(h_full, kTileB);
+                load_tile(sm + k1VH + kTileB, &tdh, h_full, row, it.slice, pol_keep);
+                ++nh;
             }
             // the CTA leaves only once its copies have landed
             if (nq > 0) bwait(q_full, (uint32_t)((nq - 1) & 1), p.wait_ns);
-            if (nvh > 0) bwait(vh_full, (uint32_t)((nvh - 1) & 1), p.wait_ns);
+            if (nv > 0) bwait(v_full, (uint32_t)((nv - 1) & 1), p.wait_ns);
+            if (nh > 0) bwait(h_full, (uint32_t)((nh - 1) & 1), p.wait_ns);
             bwait(u_full, 0u, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);       // [tokens x anchors], K = d
-            const uint32_t idWD = idesc_bf16_f32(kMP, 2 * kD, true, true);     // A^T [V | dH], K = tokens
+            const uint32_t idW = idesc_bf16_f32(kMP, kD, true, true);          // A^T V or A^T dH, K = tokens
             const uint32_t idDl = idesc_bf16_f32(kMP, 16, true, false);        // A^T 1
             const uint64_t udesc = smem_desc_sw128(sbase + k1U, 16, 1024);
             const uint64_t qdesc = smem_desc_sw128(sbase + k1Q, 16, 1024);
-            const uint64_t vhdesc = smem_desc_sw128(sbase + k1VH, kBlkB, 1024);  // N = 256: V | dH blocks
+            const uint64_t vdesc = smem_desc_sw128(sbase + k1VH, kBlkB, 1024);
+            const uint64_t hdesc = smem_desc_sw128(sbase + k1VH + kTileB, kBlkB, 1024);
             const uint64_t odesc = smem_desc_sw128(sbase + k1Ones, 16, 1024);
             bool ok = bwait(u_full, 0u, p.wait_ns);
             auto issue_s = [&](int i) -> bool {
@@ -247,7 +290,9 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 // the row warps have read S_i and written A_i
                 if (!bwait(a_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 if (i + 1 < it.nt && !issue_s(i + 1)) { ok = false; break; }
-                if (!bwait(vh_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                // W += A^T V and Delta += A^T 1, then dW' += A^T dH (V's buffer is refilled
+                // while the dH products run)
+                if (!bwait(v_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
@@ -256,13 +301,24 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                     for (int kt = 0; kt < kT / 16; ++kt) {
                         const uint32_t acc = (i > 0 || part > 0 || kt > 0) ? 1u : 0u;
                         const uint64_t ak = adesc + (uint64_t)(kt * 128);
-                        umma_bf16(tmem + k1ColWD, ak, vhdesc + (uint64_t)(kt * 128), idWD, acc);
+                        umma_bf16(tmem + k1ColWD, ak, vdesc + (uint64_t)(kt * 128), idW, acc);
                         umma_bf16(tmem + k1ColDelta, ak, odesc + (uint64_t)((((kt >> 2) * 2048) + (kt & 3) * 32) >> 4),
                                   idDl, acc);
                     }
                 }
+                umma_commit(v_empty);
+                if (!bwait(h_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint64_t adesc = smem_desc_sw128(sbase + (part ? k1AL : k1AH), kBlkB, 1024);
+#pragma unroll
+                    for (int kt = 0; kt < kT / 16; ++kt)
+                        umma_bf16(tmem + k1ColWD + kD, adesc + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idW,
+                                  (i > 0 || part > 0 || kt > 0) ? 1u : 0u);
+                }
                 umma_commit(a_empty);
-                umma_commit(vh_empty);
+                umma_commit(h_empty);
             }
             if (ok) umma_commit(acc_full);
             umma_commit(mma_done);
@@ -321,35 +377,39 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
 }
 
 // ------------------------------------------------------------------------------ reduce
-// One CTA per slice, thread k = column k: W, dW' and Delta summed over the slice's items in
-// item order; W' = W / Delta and dW = dW' / Delta as hi + lo bf16 images (rows >= m and anchors
-// with Delta = 0 are zero), dDelta_j = -sum_k dW_jk W'_jk in fp32 (a fixed warp tree, then the
-// four warps in order).
+// Per slice and run of kRJ anchors (one CTA; thread k = column k): W, dW' and Delta summed over
+// the slice's items in item order; W' = W / Delta and dW = dW' / Delta as hi + lo bf16 images
+// (rows >= m and anchors with Delta = 0 are zero), dDelta_j = -sum_k dW_jk W'_jk in fp32 (a
+// fixed warp tree, then the four warps in order).
+constexpr int kRJ = 8;
 __global__ void __launch_bounds__(kD)
 anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m, __nv_bfloat16 *__restrict__ img,
                               float *__restrict__ ddelta) {
-    __shared__ float s_rinv[kMP];
-    __shared__ float s_red[kD / 32][kMP];
+    __shared__ float s_red[kD / 32][kRJ];
+    __shared__ float s_rinv[kRJ];
     grid_dependency_wait();
     grid_dependents_launch();
-    const int slice = blockIdx.x, k = threadIdx.x, lane = k & 31, warp = k >> 5;
+    const int slice = blockIdx.x, j0 = blockIdx.y * kRJ, k = threadIdx.x, lane = k & 31, warp = k >> 5;
     const float *P = part + (size_t)slice * chunks * kPartF;
-    {
-        float dl = 0.f;
-        for (int c = 0; c < chunks; ++c) dl = __fadd_rn(dl, P[(size_t)c * kPartF + kMP * 2 * kD + k]);
-        s_rinv[k] = (k < m && dl != 0.f) ? 1.f / dl : 0.f;
-    }
-    __syncthreads();
-    __nv_bfloat16 *I = img + (size_t)slice * 4 * kMP * kD;
-    for (int j = 0; j < kMP; ++j) {
-        float w = 0.f, dw = 0.f;
-        for (int c = 0; c < chunks; ++c) {
-            const float *r = P + (size_t)c * kPartF + (size_t)j * 2 * kD;
-            w = __fadd_rn(w, r[k]);
-            dw = __fadd_rn(dw, r[kD + k]);
+    float w[kRJ], dw[kRJ], dl[kRJ];
+#pragma unroll
+    for (int r = 0; r < kRJ; ++r) w[r] = dw[r] = dl[r] = 0.f;
+    for (int c = 0; c < chunks; ++c) {
+        const float *pc = P + (size_t)c * kPartF;
+#pragma unroll
+        for (int r = 0; r < kRJ; ++r) {
+            w[r] = __fadd_rn(w[r], __ldg(pc + (size_t)(j0 + r) * 2 * kD + k));
+            dw[r] = __fadd_rn(dw[r], __ldg(pc + (size_t)(j0 + r) * 2 * kD + kD + k));
+            dl[r] = __fadd_rn(dl[r], __ldg(pc + kMP * 2 * kD + j0 + r));
         }
-        const float rinv = s_rinv[j];
-        const float wp = w * rinv, dwv = dw * rinv;
+    }
+    __nv_bfloat16 *I = img + (size_t)slice * 4 * kMP * kD;
+#pragma unroll
+    for (int r = 0; r < kRJ; ++r) {
+        const int j = j0 + r;
+        const float rinv = (j < m && dl[r] != 0.f) ? 1.f / dl[r] : 0.f;
+        if (k == 0) s_rinv[r] = rinv;
+        const float wp = w[r] * rinv, dwv = dw[r] * rinv;
         const __nv_bfloat16 wh = __float2bfloat16_rn(wp), dh = __float2bfloat16_rn(dwv);
         I[(size_t)(0 * kMP + j) * kD + k] = wh;
         I[(size_t)(1 * kMP + j) * kD + k] = __float2bfloat16_rn(wp - __bfloat162float(wh));
@@ -358,30 +418,32 @@ anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m,
         float pr = dwv * wp;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) pr += __shfl_xor_sync(0xffffffffu, pr, o);
-        if (lane == 0) s_red[warp][j] = pr;
+        if (lane == 0) s_red[warp][r] = pr;
     }
     __syncthreads();
-    if (k < kMP) {
+    if (k < kRJ) {
         float dd = s_red[0][k];
 #pragma unroll
-        for (int w = 1; w < kD / 32; ++w) dd = __fadd_rn(dd, s_red[w][k]);
-        ddelta[(size_t)slice * kMP + k] = s_rinv[k] != 0.f ? -dd : 0.f;
+        for (int q = 1; q < kD / 32; ++q) dd = __fadd_rn(dd, s_red[q][k]);
+        const int j = j0 + k;
+        ddelta[(size_t)slice * kMP + j] = s_rinv[k] != 0.f ? -dd : 0.f;
     }
 }
 
 // ------------------------------------------------------------------------------ pass 2
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(k2Threads, 1)
 anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ CUtensorMap tdh, const __grid_constant__ CUtensorMap tu,
                           const __grid_constant__ CUtensorMap timg, const BwParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k2Bar);
-    uint64_t *u_full = bars + 0, *q_full = bars + 1 /* [2] */, *xq_free = bars + 3 /* [2] */,
-             *xa_free = bars + 5 /* [2] */, *vh_full = bars + 7, *vh_free = bars + 8, *img_full = bars + 9 /* [2] */,
+    uint64_t *u_full = bars + 0, *q_full = bars + 1 /* [2] */, *x_free = bars + 3 /* [2] */,
+             *s_free = bars + 5, *v_full = bars + 7, *v_free = bars + 8, *img_full = bars + 9 /* [2] */,
              *img_empty = bars + 11 /* [2] */, *s_full = bars + 13, *s_empty = bars + 14, *g_full = bars + 15,
              *g_empty = bars + 16, *a_full = bars + 17, *dv_full = bars + 18, *dv_empty = bars + 19,
-             *ds_full = bars + 20, *dq_full = bars + 21, *du_full = bars + 22, *mma_done = bars + 23;
+             *ds_full = bars + 20, *dq_full = bars + 21, *du_full = bars + 22, *mma_done = bars + 23,
+             *x_ex = bars + 24, *h_full = bars + 25, *h_free = bars + 26;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k2Bars);
     float *sDD = reinterpret_cast<float *>(sm + k2DD);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,27 +454,30 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         mbar_init(u_full, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(q_full + b, 1);
-            mbar_init(xq_free + b, 1);
-            mbar_init(xa_free + b, 1);
+            mbar_init(x_free + b, 1);
             mbar_init(img_full + b, 1);
             mbar_init(img_empty + b, 1);
         }
-        mbar_init(vh_full, 1);
-        mbar_init(vh_free, 1);
+        mbar_init(s_free, 1);
+        mbar_init(v_full, 1);
+        mbar_init(v_free, 1);
+        mbar_init(h_full, 1);
+        mbar_init(h_free, 1);
         mbar_init(s_full, 1);
-        mbar_init(s_empty, 4);
+        mbar_init(s_empty, 8);
         mbar_init(g_full, 1);
-        mbar_init(g_empty, 4);
-        mbar_init(a_full, 4);
+        mbar_init(g_empty, 8);
+        mbar_init(a_full, 8);
         mbar_init(dv_full, 1);
-        mbar_init(dv_empty, 4);
-        mbar_init(ds_full, 4);
+        mbar_init(dv_empty, 8);
+        mbar_init(ds_full, 8);
         mbar_init(dq_full, 1);
         mbar_init(du_full, 1);
         mbar_init(mma_done, 1);
+        mbar_init(x_ex, 8);
         fence_mbar_init();
     }
-    if (warp == kWarpMma) tmem_alloc(s_tmem, kTmemCols);
+    if (warp == kWarp2Mma) tmem_alloc(s_tmem, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -421,7 +486,7 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     grid_dependency_wait();
     grid_dependents_launch();
 
-    if (warp == kWarpProducer) {
+    if (warp == kWarp2Producer) {
         if (lane == 0) {
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tv);
@@ -431,21 +496,31 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             const uint64_t pol_keep = policy_evict_last(), pol_once = policy_evict_first();
             mbar_arrive_expect_tx(u_full, kTileB);
             load_tile(sm + k2U, &tu, u_full, 0, h, pol_keep);
-            int nq[2] = {0, 0}, nvh = 0, nimg[2] = {0, 0};
+            int nq[2] = {0, 0}, nv = 0, nh = 0, nimg[2] = {0, 0};
             bool ok = true;
             for (int i = 0; i < it.nt && ok; ++i) {
                 const int row = (it.t0 + i) * kT, b = i & 1;
-                // Q_i into X[b] once dV_{i-1} has read A_{i-1} there
-                if (i >= 1 && !bwait(xq_free + b, (uint32_t)(((i - 1) >> 1) & 1), p.wait_ns)) break;
+                for (int k = i == 0 ? 1 : 2; k <= 2; ++k)
+                    if (i + k < it.nt) {
+                        prefetch_tile(&tq, row + k * kT, it.slice);
+                        prefetch_tile(&tv, row + k * kT, it.slice);
+                        prefetch_tile(&tdh, row + k * kT, it.slice);
+                    }
+                // Q_i into X[b] once dU has read Q_{i-2} there
+                if (i >= 2 && !bwait(x_free + b, (uint32_t)(((i >> 1) - 1) & 1), p.wait_ns)) break;
                 mbar_arrive_expect_tx(q_full + b, kTileB);
                 load_tile(sm + k2X + b * kTileB, &tq, q_full + b, row, it.slice, pol_once);
                 ++nq[b];
-                // V_i, dH_i once dQ_{i-1} and dU have read dS_{i-1} there
-                if (i >= 1 && !bwait(vh_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(vh_full, 2 * kTileB);
-                load_tile(sm + k2VH, &tv, vh_full, row, it.slice, pol_once);
-                load_tile(sm + k2VH + kTileB, &tdh, vh_full, row, it.slice, pol_once);
-                ++nvh;
+                // dH_i once dU has read dS_lo of tile i - 1 there, then V_i once dQ and dU have
+                // read dS_hi
+                if (i >= 1 && !bwait(h_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(h_full, kTileB);
+                load_tile(sm + k2VH + kTileB, &tdh, h_full, row, it.slice, pol_once);
+                ++nh;
+                if (i >= 1 && !bwait(v_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(v_full, kTileB);
+                load_tile(sm + k2VH, &tv, v_full, row, it.slice, pol_once);
+                ++nv;
                 // the images W'_hi, W'_lo, dW_hi, dW_lo (unit u = 4 i + part, slot u & 1)
                 for (int part = 0; part < 4; ++part) {
                     const int u = 4 * i + part, s = u & 1;
@@ -459,11 +534,12 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 if (nq[b] > 0) bwait(q_full + b, (uint32_t)((nq[b] - 1) & 1), p.wait_ns);
                 if (nimg[b] > 0) bwait(img_full + b, (uint32_t)((nimg[b] - 1) & 1), p.wait_ns);
             }
-            if (nvh > 0) bwait(vh_full, (uint32_t)((nvh - 1) & 1), p.wait_ns);
+            if (nh > 0) bwait(h_full, (uint32_t)((nh - 1) & 1), p.wait_ns);
+            if (nv > 0) bwait(v_full, (uint32_t)((nv - 1) & 1), p.wait_ns);
             bwait(u_full, 0u, p.wait_ns);
         }
         __syncwarp();
-    } else if (warp == kWarpMma) {
+    } else if (warp == kWarp2Mma) {
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);  // [tokens x anchors], K = d
             const uint32_t idR = idesc_bf16_f32(kT, kD, false, true);    // [tokens x d], K = anchors
@@ -475,10 +551,10 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             bool ok = bwait(u_full, 0u, p.wait_ns);
             for (int i = 0; i < it.nt && ok; ++i) {
                 const int b = i & 1;
-                const uint32_t xq = sbase + k2X + b * kTileB, xa = sbase + k2X + (b ^ 1) * kTileB;
-                // S_i = Q_i U^T
+                const uint32_t xq = sbase + k2X + b * kTileB;
+                // S_i = Q_i U^T, once dV_{i-1} has read A_{i-1} over S's columns
                 if (!bwait(q_full + b, (uint32_t)((i >> 1) & 1), p.wait_ns)) { ok = false; break; }
-                if (i >= 1 && !bwait(s_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
+                if (i >= 1 && !bwait(s_free, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 {
                     const uint64_t qd = smem_desc_sw128(xq, 16, 1024);
@@ -488,10 +564,11 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 }
                 umma_commit(s_full);
                 // G_i = dH_i (W'_hi + W'_lo)^T + V_i (dW_hi + dW_lo)^T, once dQ_{i-1} left G's columns
-                if (!bwait(vh_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                if (!bwait(h_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 if (i >= 1 && !bwait(g_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
                 for (int part = 0; part < 4 && ok; ++part) {
                     const int u = 4 * i + part, s = u & 1;
+                    if (part == 2 && !bwait(v_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                     if (!bwait(img_full + s, (uint32_t)((u >> 1) & 1), p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = part < 2 ? hk : vk;
@@ -503,48 +580,48 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 }
                 if (!ok) break;
                 umma_commit(g_full);
-                // dV_i = A_i (dW_hi + dW_lo) (the dW parts are in slots 0 and 1)
+                // dV_i = A_i (dW_hi + dW_lo), A_i (bf16) in tensor memory over S's columns (the dW
+                // parts are in slots 0 and 1)
                 if (!bwait(a_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 if (i >= 1 && !bwait(dv_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
-                {
-                    const uint64_t ak = smem_desc_sw128(xa, 16, 1024);
 #pragma unroll
-                    for (int s = 0; s < 2; ++s) {
-                        const uint64_t dwm = smem_desc_sw128(sbase + k2Img + s * kTileB, kBlkB, 1024);
+                for (int s = 0; s < 2; ++s) {
+                    const uint64_t dwm = smem_desc_sw128(sbase + k2Img + s * kTileB, kBlkB, 1024);
 #pragma unroll
-                        for (int kj = 0; kj < kMP / 16; ++kj)
-                            umma_bf16(tmem + k2ColDV, ak + kstep(kj), dwm + (uint64_t)(kj * 128), idR,
-                                      (s > 0 || kj > 0) ? 1u : 0u);
-                    }
+                    for (int kj = 0; kj < kMP / 16; ++kj)
+                        umma_bf16_tmem_a(tmem + k2ColDV, tmem + k2ColS + kj * 8, dwm + (uint64_t)(kj * 128), idR,
+                                         (s > 0 || kj > 0) ? 1u : 0u);
                 }
                 umma_commit(dv_full);
                 umma_commit(img_empty + 0);
                 umma_commit(img_empty + 1);
-                umma_commit(xq_free + (b ^ 1));  // A_i read: Q_{i+1} may load there
-                // dQ_i = dS_i U (into G's columns) and dU += dS_i^T Q_i, dS_i over V_i and dH_i
+                umma_commit(s_free);  // A_i read: S_{i+1} may be written there
+                // dU += dS_lo^T Q_i first (dS_lo is over dH_i, whose buffer then takes dH_{i+1}),
+                // then dQ_i = dS_hi U (into G's columns; dQ sums over the m anchors only, so one
+                // bf16 part is enough) and dU += dS_hi^T Q_i (dS_hi over V_i)
                 if (!bwait(ds_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 {
                     const uint64_t qm = smem_desc_sw128(xq, kBlkB, 1024);  // Q_i, MN-major (N = d)
+                    const uint64_t dsml = smem_desc_sw128(sbase + k2VH + kTileB, kBlkB, 1024);  // dS_lo^T
 #pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        const uint32_t da = sbase + k2VH + part * kTileB;
-                        const uint64_t dsk = smem_desc_sw128(da, 16, 1024);
-                        const uint64_t dsm = smem_desc_sw128(da, kBlkB, 1024);  // dS^T: anchors x tokens
+                    for (int kt = 0; kt < kT / 16; ++kt)
+                        umma_bf16(tmem + k2ColDU, dsml + (uint64_t)(kt * 128), qm + (uint64_t)(kt * 128), idU,
+                                  (i > 0 || kt > 0) ? 1u : 0u);
+                    umma_commit(h_free);
+                    const uint64_t dsk = smem_desc_sw128(sbase + k2VH, 16, 1024);
+                    const uint64_t dsm = smem_desc_sw128(sbase + k2VH, kBlkB, 1024);  // dS_hi^T: anchors x tokens
 #pragma unroll
-                        for (int kj = 0; kj < kMP / 16; ++kj)
-                            umma_bf16(tmem + k2ColG, dsk + kstep(kj), umn + (uint64_t)(kj * 128), idR,
-                                      (part > 0 || kj > 0) ? 1u : 0u);
+                    for (int kj = 0; kj < kMP / 16; ++kj)
+                        umma_bf16(tmem + k2ColG, dsk + kstep(kj), umn + (uint64_t)(kj * 128), idR, kj > 0 ? 1u : 0u);
 #pragma unroll
-                        for (int kt = 0; kt < kT / 16; ++kt)
-                            umma_bf16(tmem + k2ColDU, dsm + (uint64_t)(kt * 128), qm + (uint64_t)(kt * 128), idU,
-                                      (i > 0 || part > 0 || kt > 0) ? 1u : 0u);
-                    }
+                    for (int kt = 0; kt < kT / 16; ++kt)
+                        umma_bf16(tmem + k2ColDU, dsm + (uint64_t)(kt * 128), qm + (uint64_t)(kt * 128), idU, 1u);
                 }
                 umma_commit(dq_full);
-                umma_commit(vh_free);
-                umma_commit(xa_free + b);  // Q_i read: A_{i+1} may be written there
+                umma_commit(v_free);
+                umma_commit(x_free + b);  // Q_i read: Q_{i+2} may load there
             }
             if (ok && it.nt > 0) umma_commit(du_full);
             umma_commit(mma_done);
@@ -553,127 +630,177 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ row warps
-        const int row = warp * 32 + lane;
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        sDD[row] = p.ddelta[(size_t)it.slice * kMP + row];
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        // warp w: TMEM lanes 32 (w % 4) .. + 31 (tokens; anchors for dU), column group
+        // g = w / 4 (anchors, or d columns, 64 g .. 64 g + 63)
+        const int row = (warp & 3) * 32 + lane, g = warp >> 2;
+        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        if (g == 0) sDD[row] = p.ddelta[(size_t)it.slice * kMP + row];
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         bool ok = true;
-        float a[128];
-        // dQ_i and dV_i from tensor memory to global memory (16-byte stores from the row)
-        auto drain = [&](int i) -> bool {
+        float e[64];          // 2^(c s_j - max) of this group's anchors (A = e / z)
+        float zinv_prev = 0.f;
+        // dQ_i, then dV_i (as (e dW) / z), from tensor memory to global memory
+        auto drain_dq = [&](int i) -> bool {
             if (!bwait(dq_full, (uint32_t)(i & 1), p.wait_ns)) return false;
             tc_fence_after();
             const bool valid = (it.t0 + i) * kT + row < p.n;
-            const size_t off = ((size_t)it.slice * p.n + (size_t)((it.t0 + i) * kT + row)) * kD;
-            float o[32];
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                tmem_ld32(trow + k2ColG + 32 * q, o);
-                tmem_ld_wait();
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + off + 32 * q);
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) dst[c8] = pack8(o + 8 * c8, p.scale);
-                }
-            }
+            const size_t off = ((size_t)it.slice * p.n + (size_t)((it.t0 + i) * kT + row)) * kD + 64 * g;
+            float o[64];
+            tmem_ld32(trow + k2ColG + 64 * g, o);
+            tmem_ld32(trow + k2ColG + 64 * g + 32, o + 32);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(g_empty);
+            if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + off);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) dst[c8] = pack8(o + 8 * c8, p.scale);
+            }
+            return true;
+        };
+        auto drain_dv = [&](int i, float zinv) -> bool {
             if (!bwait(dv_full, (uint32_t)(i & 1), p.wait_ns)) return false;
             tc_fence_after();
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                tmem_ld32(trow + k2ColDV + 32 * q, o);
-                tmem_ld_wait();
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.dV + off + 32 * q);
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) dst[c8] = pack8(o + 8 * c8, 1.f);
-                }
-            }
+            const bool valid = (it.t0 + i) * kT + row < p.n;
+            const size_t off = ((size_t)it.slice * p.n + (size_t)((it.t0 + i) * kT + row)) * kD + 64 * g;
+            float o[64];
+            tmem_ld32(trow + k2ColDV + 64 * g, o);
+            tmem_ld32(trow + k2ColDV + 64 * g + 32, o + 32);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dv_empty);
+            if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.dV + off);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) dst[c8] = pack8(o + 8 * c8, zinv);
+            }
             return true;
         };
         for (int i = 0; i < it.nt && ok; ++i) {
             const int b = i & 1;
+            const bool valid = (it.t0 + i) * kT + row < p.n;
+            // dQ of the tile before first: it holds G's columns, which G_i needs
+            if (i >= 1 && !drain_dq(i - 1)) { ok = false; break; }
             if (!bwait(s_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
+            float mx;
+            {   // the row maximum over all 128 scores (each group reads the whole row), then
+                // this group's exponentials and their sum
+                float sv[128];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(trow + k2ColS + 32 * q, a + 32 * q);
-            tmem_ld_wait();
+                for (int q = 0; q < 4; ++q) tmem_ld32(trow + k2ColS + 32 * q, sv + 32 * q);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty);
+#pragma unroll
+                for (int j = 0; j < 128; ++j) sv[j] = j < p.m ? sv[j] * p.c : -INFINITY;
+                float m8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = sv[k];
+#pragma unroll
+                for (int j = 8; j < 128; j += 8)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[j + k]);
+                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                if (g == 0) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(sv[j] - mx);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(sv[64 + j] - mx);
+                }
+            }
+            float zg = 0.f;
+            {
+                float z4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < 64; ++j) z4[j & 3] += e[j];
+                zg = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+            }
+            // e (bf16 pairs) over S's columns 32 g .. 32 g + 31 (dV's A operand), once all eight
+            // row warps have read S_i
+            if (!bwait(s_empty, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) pk[j] = pack2(e[2 * j], e[2 * j + 1]);
+                tmem_st32(trow + k2ColS + 32 * g, pk);
+                tmem_st_wait();
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty);
-            softmax128(a, p.m, p.c, (it.t0 + i) * kT + row < p.n);
-            // A_i (bf16) into X[b ^ 1], once dU has read Q_{i-1} there
-            if (i >= 1 && !bwait(xa_free + (b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), p.wait_ns)) { ok = false; break; }
-            {
-                uint8_t *xa = sm + k2X + (b ^ 1) * kTileB;
-#pragma unroll
-                for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4 *>(xa + sw_off(row, c, kT)) = pack8(a + 8 * c, 1.f);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
             if (lane == 0) mbar_arrive(a_full);
-            if (i >= 1 && !drain(i - 1)) { ok = false; break; }
-            // dS_j = A_j (G_j + dDelta_j - sum_l A_l (G_l + dDelta_l)), over V_i and dH_i
+            if (i >= 1 && !drain_dv(i - 1, zinv_prev)) { ok = false; break; }
+            // dS_j = A_j (G_j + dDelta_j - sum_l A_l (G_l + dDelta_l)), A = e / z, over V_i and dH_i
             if (!bwait(g_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
-            float g[32];
-            float rs = 0.f;
+            float gv[64];
+            tmem_ld32(trow + k2ColG + 64 * g, gv);
+            tmem_ld32(trow + k2ColG + 64 * g + 32, gv + 32);
+            tmem_ld_wait();
+            float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                tmem_ld32(trow + k2ColG + 32 * q, g);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) rs = fmaf(a[32 * q + j], g[j] + sDD[32 * q + j], rs);
+            for (int j = 0; j < 64; ++j) {
+                gv[j] += sDD[64 * g + j];
+                r4[j & 3] = fmaf(e[j], gv[j], r4[j & 3]);
             }
+            const float rg = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+            // the two groups' (z, r) through tensor memory: each writes them into the first two
+            // of its own (already read) G columns and reads the other group's (G's columns
+            // take dQ_i only after every row warp has passed ds_full)
+            tmem_st2(trow + k2ColG + 64 * g, zg, rg);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x_ex);
+            if (!bwait(x_ex, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+            tc_fence_after();
+            const float2 other = tmem_ld2(trow + k2ColG + 64 * (1 - g));
+            tmem_ld_wait();
+            const float z = g == 0 ? zg + other.x : other.x + zg;
+            const float rr = g == 0 ? rg + other.y : other.y + rg;
+            const float zinv = valid ? 1.f / z : 0.f;
+            const float rs = rr * zinv;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                tmem_ld32(trow + k2ColG + 32 * q, g);
-                tmem_ld_wait();
+            for (int j = 0; j < 64; ++j) gv[j] = e[j] * zinv * (gv[j] - rs);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) g[j] = a[32 * q + j] * (g[j] + sDD[32 * q + j] - rs);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint4 hi, lo;
-                    split8(g + 8 * c, hi, lo);
-                    *reinterpret_cast<uint4 *>(sm + k2VH + sw_off(row, 4 * q + c, kT)) = hi;
-                    *reinterpret_cast<uint4 *>(sm + k2VH + kTileB + sw_off(row, 4 * q + c, kT)) = lo;
-                }
+            for (int c = 0; c < 8; ++c) {
+                uint4 hi, lo;
+                split8(gv + 8 * c, hi, lo);
+                *reinterpret_cast<uint4 *>(sm + k2VH + sw_off(row, 8 * g + c, kT)) = hi;
+                *reinterpret_cast<uint4 *>(sm + k2VH + kTileB + sw_off(row, 8 * g + c, kT)) = lo;
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
+            zinv_prev = zinv;
         }
-        if (ok && it.nt >= 1) ok = drain(it.nt - 1);
-        // the item's dU (scale dS^T Q): anchor j = row
+        if (ok && it.nt >= 1) ok = drain_dq(it.nt - 1) && drain_dv(it.nt - 1, zinv_prev);
+        // the item's dU (scale dS^T Q): anchor j = row, d columns 64 g ..
         ok = ok && it.nt > 0 && bwait(du_full, 0u, p.wait_ns);
         if (ok) {
             tc_fence_after();
-            float o[32];
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                tmem_ld32(trow + k2ColDU + 32 * q, o);
-                tmem_ld_wait();
-                if (row < p.m) {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        p.dupart + ((size_t)blockIdx.x * p.m + row) * kD + 32 * q);
+            float o[64];
+            tmem_ld32(trow + k2ColDU + 64 * g, o);
+            tmem_ld32(trow + k2ColDU + 64 * g + 32, o + 32);
+            tmem_ld_wait();
+            if (row < p.m) {
+                float4 *dst = reinterpret_cast<float4 *>(p.dupart + ((size_t)blockIdx.x * p.m + row) * kD + 64 * g);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(o[4 * k] * p.scale, o[4 * k + 1] * p.scale, o[4 * k + 2] * p.scale,
-                                             o[4 * k + 3] * p.scale);
-                }
+                for (int k = 0; k < 16; ++k)
+                    dst[k] = make_float4(o[4 * k] * p.scale, o[4 * k + 1] * p.scale, o[4 * k + 2] * p.scale,
+                                         o[4 * k + 3] * p.scale);
             }
             tc_fence_before();
         }
         __syncwarp();
     }
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kWarp2Mma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -752,11 +879,11 @@ cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t s
     if ((e = launch_pdl(anchor_bwd_wide_p1_kernel, grid, dim3(kThreads), k1Smem, stream, tq, tv, tdh, tu, bp)) !=
         cudaSuccess)
         return e;
-    if ((e = launch_pdl(anchor_bwd_wide_reduce_kernel, dim3((unsigned)S), dim3(kD), 0, stream,
+    if ((e = launch_pdl(anchor_bwd_wide_reduce_kernel, dim3((unsigned)S, kMP / kRJ), dim3(kD), 0, stream,
                         (const float *)bp.part, chunks, p.m, reinterpret_cast<__nv_bfloat16 *>(ws + L.img),
                         reinterpret_cast<float *>(ws + L.dd))) != cudaSuccess)
         return e;
-    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel, grid, dim3(kThreads), k2Smem, stream, tq, tv, tdh, tu, timg, bp)) !=
+    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel, grid, dim3(k2Threads), k2Smem, stream, tq, tv, tdh, tu, timg, bp)) !=
         cudaSuccess)
         return e;
     return launch_bwd_du_sum(bp.dupart, p.dU, p.B, p.heads, chunks, p.m * kD, false, stream);
