@@ -64,8 +64,9 @@ constexpr int k1Smem = k1Bar + k1Bars * 8 + 16 + 1024;
 static_assert(k1Smem <= 227 * 1024, "pass 1 shared memory");
 constexpr uint32_t k1ColS = 0, k1ColWD = 128, k1ColDelta = 384;
 
-// pass 2: U | X0 X1 (Q or A) | V dH, then dS_hi dS_lo | image ring (2 x 32 KB) | dDelta | barriers
-constexpr int k2U = 0, k2X = k2U + kTileB, k2VH = k2X + 2 * kTileB, k2Img = k2VH + 2 * kTileB;
+// pass 2: U | Q | dQ, dV staging (4 KB per row warp) | V dH, then dS_hi dS_lo | image ring
+// (2 x 32 KB) | dDelta | barriers
+constexpr int k2U = 0, k2X = k2U + kTileB, k2Stage = k2X + kTileB, k2VH = k2X + 2 * kTileB, k2Img = k2VH + 2 * kTileB;
 constexpr int k2DD = k2Img + 2 * kTileB, k2Bar = k2DD + kMP * 4;
 constexpr int k2Bars = 27;
 constexpr int k2Smem = k2Bar + k2Bars * 8 + 16 + 1024;
@@ -434,11 +435,12 @@ anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m,
 __global__ void __launch_bounds__(k2Threads, 1)
 anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ CUtensorMap tdh, const __grid_constant__ CUtensorMap tu,
-                          const __grid_constant__ CUtensorMap timg, const BwParams p) {
+                          const __grid_constant__ CUtensorMap timg, const __grid_constant__ CUtensorMap tdq,
+                          const __grid_constant__ CUtensorMap tdv, const BwParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k2Bar);
-    uint64_t *u_full = bars + 0, *q_full = bars + 1 /* [2] */, *x_free = bars + 3 /* [2] */,
+    uint64_t *u_full = bars + 0, *q_full = bars + 1, *x_free = bars + 3,
              *s_free = bars + 5, *v_full = bars + 7, *v_free = bars + 8, *img_full = bars + 9 /* [2] */,
              *img_empty = bars + 11 /* [2] */, *s_full = bars + 13, *s_empty = bars + 14, *g_full = bars + 15,
              *g_empty = bars + 16, *a_full = bars + 17, *dv_full = bars + 18, *dv_empty = bars + 19,
@@ -453,11 +455,12 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     if (threadIdx.x == 0) {
         mbar_init(u_full, 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(q_full + b, 1);
-            mbar_init(x_free + b, 1);
+
             mbar_init(img_full + b, 1);
             mbar_init(img_empty + b, 1);
         }
+        mbar_init(q_full, 1);
+        mbar_init(x_free, 1);
         mbar_init(s_free, 1);
         mbar_init(v_full, 1);
         mbar_init(v_free, 1);
@@ -493,24 +496,26 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             tma_prefetch_desc(&tdh);
             tma_prefetch_desc(&tu);
             tma_prefetch_desc(&timg);
+            tma_prefetch_desc(&tdq);
+            tma_prefetch_desc(&tdv);
             const uint64_t pol_keep = policy_evict_last(), pol_once = policy_evict_first();
             mbar_arrive_expect_tx(u_full, kTileB);
             load_tile(sm + k2U, &tu, u_full, 0, h, pol_keep);
-            int nq[2] = {0, 0}, nv = 0, nh = 0, nimg[2] = {0, 0};
+            int nq = 0, nv = 0, nh = 0, nimg[2] = {0, 0};
             bool ok = true;
             for (int i = 0; i < it.nt && ok; ++i) {
-                const int row = (it.t0 + i) * kT, b = i & 1;
+                const int row = (it.t0 + i) * kT;
                 for (int k = i == 0 ? 1 : 2; k <= 2; ++k)
                     if (i + k < it.nt) {
                         prefetch_tile(&tq, row + k * kT, it.slice);
                         prefetch_tile(&tv, row + k * kT, it.slice);
                         prefetch_tile(&tdh, row + k * kT, it.slice);
                     }
-                // Q_i into X[b] once dU has read Q_{i-2} there
-                if (i >= 2 && !bwait(x_free + b, (uint32_t)(((i >> 1) - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(q_full + b, kTileB);
-                load_tile(sm + k2X + b * kTileB, &tq, q_full + b, row, it.slice, pol_once);
-                ++nq[b];
+                // Q_i once dU has read Q_{i-1} (it comes from L2: the tiles ahead are prefetched)
+                if (i >= 1 && !bwait(x_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(q_full, kTileB);
+                load_tile(sm + k2X, &tq, q_full, row, it.slice, pol_once);
+                ++nq;
                 // dH_i once dU has read dS_lo of tile i - 1 there, then V_i once dQ and dU have
                 // read dS_hi
                 if (i >= 1 && !bwait(h_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
@@ -530,8 +535,8 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                     ++nimg[s];
                 }
             }
+            if (nq > 0) bwait(q_full, (uint32_t)((nq - 1) & 1), p.wait_ns);
             for (int b = 0; b < 2; ++b) {
-                if (nq[b] > 0) bwait(q_full + b, (uint32_t)((nq[b] - 1) & 1), p.wait_ns);
                 if (nimg[b] > 0) bwait(img_full + b, (uint32_t)((nimg[b] - 1) & 1), p.wait_ns);
             }
             if (nh > 0) bwait(h_full, (uint32_t)((nh - 1) & 1), p.wait_ns);
@@ -550,10 +555,9 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             const uint64_t hk = smem_desc_sw128(sbase + k2VH + kTileB, 16, 1024);
             bool ok = bwait(u_full, 0u, p.wait_ns);
             for (int i = 0; i < it.nt && ok; ++i) {
-                const int b = i & 1;
-                const uint32_t xq = sbase + k2X + b * kTileB;
+                const uint32_t xq = sbase + k2X;
                 // S_i = Q_i U^T, once dV_{i-1} has read A_{i-1} over S's columns
-                if (!bwait(q_full + b, (uint32_t)((i >> 1) & 1), p.wait_ns)) { ok = false; break; }
+                if (!bwait(q_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 if (i >= 1 && !bwait(s_free, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 {
@@ -621,7 +625,7 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 }
                 umma_commit(dq_full);
                 umma_commit(v_free);
-                umma_commit(x_free + b);  // Q_i read: Q_{i+2} may load there
+                umma_commit(x_free);  // Q_i read: Q_{i+1} may load there
             }
             if (ok && it.nt > 0) umma_commit(du_full);
             umma_commit(mma_done);
@@ -638,48 +642,42 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         asm volatile("bar.sync 1, 256;" ::: "memory");
         bool ok = true;
         float e[64];          // 2^(c s_j - max) of this group's anchors (A = e / z)
+        const uint64_t pol_out = policy_evict_first();
         float zinv_prev = 0.f;
-        // dQ_i, then dV_i (as (e dW) / z), from tensor memory to global memory
-        auto drain_dq = [&](int i) -> bool {
-            if (!bwait(dq_full, (uint32_t)(i & 1), p.wait_ns)) return false;
+        // dQ_i, then dV_i (as (e dW) / z): tensor memory -> this warp's staging [32 rows][64]
+        // (swizzled like a TMA box) -> one TMA store of the warp's 32 rows and 64 columns (rows
+        // past the slice are not written); the staging is reused once the previous store has
+        // read it
+        uint8_t *stage = sm + k2Stage + warp * 4096;
+        auto drain = [&](int i, uint64_t *full, uint64_t *empty, uint32_t col, const CUtensorMap *map,
+                         float r) -> bool {
+            if (!bwait(full, (uint32_t)(i & 1), p.wait_ns)) return false;
             tc_fence_after();
-            const bool valid = (it.t0 + i) * kT + row < p.n;
-            const size_t off = ((size_t)it.slice * p.n + (size_t)((it.t0 + i) * kT + row)) * kD + 64 * g;
             float o[64];
-            tmem_ld32(trow + k2ColG + 64 * g, o);
-            tmem_ld32(trow + k2ColG + 64 * g + 32, o + 32);
+            tmem_ld32(trow + col + 64 * g, o);
+            tmem_ld32(trow + col + 64 * g + 32, o + 32);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(g_empty);
-            if (valid) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.dQ + off);
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) dst[c8] = pack8(o + 8 * c8, p.scale);
+            if (lane == 0) {
+                mbar_arrive(empty);
+                bulk_wait_group_read0();
             }
-            return true;
-        };
-        auto drain_dv = [&](int i, float zinv) -> bool {
-            if (!bwait(dv_full, (uint32_t)(i & 1), p.wait_ns)) return false;
-            tc_fence_after();
-            const bool valid = (it.t0 + i) * kT + row < p.n;
-            const size_t off = ((size_t)it.slice * p.n + (size_t)((it.t0 + i) * kT + row)) * kD + 64 * g;
-            float o[64];
-            tmem_ld32(trow + k2ColDV + 64 * g, o);
-            tmem_ld32(trow + k2ColDV + 64 * g + 32, o + 32);
-            tmem_ld_wait();
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(dv_empty);
-            if (valid) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.dV + off);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) dst[c8] = pack8(o + 8 * c8, zinv);
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(stage + sw_off(lane, c, 32)) = pack8(o + 8 * c, r);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(map, stage, 64 * g, (it.t0 + i) * kT + (warp & 3) * 32, it.slice, pol_out);
+                bulk_commit_group();
             }
             return true;
         };
+        auto drain_dq = [&](int i) -> bool { return drain(i, dq_full, g_empty, k2ColG, &tdq, p.scale); };
+        auto drain_dv = [&](int i, float zinv) -> bool { return drain(i, dv_full, dv_empty, k2ColDV, &tdv, zinv); };
         for (int i = 0; i < it.nt && ok; ++i) {
-            const int b = i & 1;
             const bool valid = (it.t0 + i) * kT + row < p.n;
             // dQ of the tile before first: it holds G's columns, which G_i needs
             if (i >= 1 && !drain_dq(i - 1)) { ok = false; break; }
@@ -780,6 +778,8 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             zinv_prev = zinv;
         }
         if (ok && it.nt >= 1) ok = drain_dq(it.nt - 1) && drain_dv(it.nt - 1, zinv_prev);
+        if (lane == 0) bulk_wait_group0();  // the stores have read the staging and landed
+        __syncwarp();
         // the item's dU (scale dS^T Q): anchor j = row, d columns 64 g ..
         ok = ok && it.nt > 0 && bwait(du_full, 0u, p.wait_ns);
         if (ok) {
@@ -852,10 +852,11 @@ cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t s
     const int chunks = wide_chunks(S, tiles);
     const WideWs L = wide_ws(p, chunks);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    CUtensorMap tq, tv, tdh, tu, timg;
+    CUtensorMap tq, tv, tdh, tu, timg, tdq, tdv;
     if (!make_bf16_map(&tq, p.Q, kD, p.n, S, kT) || !make_bf16_map(&tv, p.V, kD, p.n, S, kT) ||
         !make_bf16_map(&tdh, p.dH, kD, p.n, S, kT) || !make_bf16_map(&tu, p.U, kD, p.m, p.heads, kMP) ||
-        !make_bf16_map(&timg, ws + L.img, kD, kMP, S * 4, kMP))
+        !make_bf16_map(&timg, ws + L.img, kD, kMP, S * 4, kMP) || !make_bf16_map(&tdq, p.dQ, kD, p.n, S, 32) ||
+        !make_bf16_map(&tdv, p.dV, kD, p.n, S, 32))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(anchor_bwd_wide_p1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, k1Smem);
     if (e == cudaSuccess)
@@ -883,7 +884,7 @@ cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t s
                         (const float *)bp.part, chunks, p.m, reinterpret_cast<__nv_bfloat16 *>(ws + L.img),
                         reinterpret_cast<float *>(ws + L.dd))) != cudaSuccess)
         return e;
-    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel, grid, dim3(k2Threads), k2Smem, stream, tq, tv, tdh, tu, timg, bp)) !=
+    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel, grid, dim3(k2Threads), k2Smem, stream, tq, tv, tdh, tu, timg, tdq, tdv, bp)) !=
         cudaSuccess)
         return e;
     return launch_bwd_du_sum(bp.dupart, p.dU, p.B, p.heads, chunks, p.m * kD, false, stream);
