@@ -11,8 +11,8 @@
 // take 128 KB of shared memory, and the accumulators S, G, dQ, dV and dU 640 tensor-memory
 // columns), so the work runs as three kernels over items (a slice's run of consecutive
 // 128-token tiles; the chunking depends on the shape alone, so the sums and the bits do too):
-//   pass 1   S_t = Q_t U^T, A_t = softmax; W += A_t^T V_t with Delta += A_t^T 1, then
-//            dW' += A_t^T dH_t, with A as hi + lo bf16 parts (Q, V, dH in buffers of their own,
+//   pass 1   S_t = Q_t U^T, A_t = softmax; W += A_t^T V_t, then [dW' | Delta] +=
+//            A_t^T [dH_t | 1] (one N = 144 product), with A as hi + lo bf16 parts (Q, V, dH in buffers of their own,
 //            each refilled as soon as its products are done); the item's W, dW', Delta go to
 //            a workspace row block
 //   reduce   per slice: the items' blocks summed in order; W' = W / Delta, dW = dW' / Delta
@@ -49,20 +49,25 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 128, kD = 128, kMP = 128;
-constexpr int kThreads = 192;
-constexpr int kWarpProducer = 4, kWarpMma = 5;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBlkB = kT * 128;   // one 64-column block of a 128-row bf16 tile (16 KB)
 constexpr int kTileB = 2 * kBlkB; // a [128][128] bf16 tile (32 KB)
 constexpr int kPartF = kMP * 2 * kD + kMP;  // an item's pass-1 block: [W | dW'] rows, then Delta
 
-// pass 1: U | Q | V | dH | A_hi | A_lo | ones [16][128] | barriers
-constexpr int k1U = 0, k1Q = k1U + kTileB, k1VH = k1Q + kTileB, k1AH = k1VH + 2 * kTileB, k1AL = k1AH + kTileB;
-constexpr int k1Ones = k1AL + kTileB, k1Bar = k1Ones + 4096;
-constexpr int k1Bars = 12;
+// pass 1: U | Q | V | dH | ones [128][64] (dH's third 64-column block: [dH | 1] is one N = 144
+// operand) | A_hi | A_lo | row-sum exchange [2][128] | barriers
+constexpr int k1U = 0, k1Q = k1U + kTileB, k1VH = k1Q + kTileB, k1Ones = k1VH + 2 * kTileB;
+constexpr int k1AH = k1Ones + kBlkB, k1AL = k1AH + kTileB, k1Ex = k1AL + kTileB, k1Bar = k1Ex + 2 * kT * 4;
+constexpr int k1Bars = 13;
 constexpr int k1Smem = k1Bar + k1Bars * 8 + 16 + 1024;
 static_assert(k1Smem <= 227 * 1024, "pass 1 shared memory");
 constexpr uint32_t k1ColS = 0, k1ColWD = 128, k1ColDelta = 384;
+// row warps 0-7 in both passes (two per TMEM lane quarter, one per half of the columns), then
+// producer warps (one per input in pass 1: Q, V, dH; in pass 2 one for Q, dH, V and one for the
+// image ring: a lane that sleeps in an mbarrier wait holds up its whole warp), then the MMA warp
+constexpr int kRowWarps = 8, kWarpProd = kRowWarps;
+constexpr int kP1Threads = 32 * (kRowWarps + 4), kP1Issue = kRowWarps + 3;
+constexpr int kP2Threads = 32 * (kRowWarps + 3), kP2Issue = kRowWarps + 2;
 
 // pass 2: U | Q | dQ, dV staging (4 KB per row warp) | V dH, then dS_hi dS_lo | image ring
 // (2 x 32 KB) | dDelta | barriers
@@ -72,9 +77,7 @@ constexpr int k2Bars = 27;
 constexpr int k2Smem = k2Bar + k2Bars * 8 + 16 + 1024;
 static_assert(k2Smem <= 227 * 1024, "pass 2 shared memory");
 constexpr uint32_t k2ColS = 0, k2ColG = 128, k2ColDV = 256, k2ColDU = 384;  // dQ_t reuses G's columns
-// pass 2 warps: 0-7 row warps (two per TMEM lane quarter, one per half of the columns), 8
-// producer, 9 MMA issuer
-constexpr int k2Threads = 320, kWarp2Producer = 8, kWarp2Mma = 9;
+
 
 struct BwParams {
     int heads, n, m, tiles, chunks;
@@ -168,25 +171,8 @@ __device__ __forceinline__ Item item_of(int b, int tiles, int chunks) {
     return it;
 }
 
-// the row softmax of 128 scores in place (anchors >= m masked); a row past the slice is zero
-__device__ __forceinline__ void softmax128(float (&v)[128], int m, float c, bool valid) {
-    const float z = rowops::softmax_unnormalised<128>(v, m, c);
-    rowops::scale_row<128>(v, valid ? 1.f / z : 0.f);
-}
-
-// a row of 128 fp32 values as hi and lo bf16 rows of two swizzled [128][128] tiles
-__device__ __forceinline__ void store_split128(uint8_t *hi, uint8_t *lo, int row, const float *x) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        uint4 h, l;
-        split8(x + 8 * c, h, l);
-        *reinterpret_cast<uint4 *>(hi + sw_off(row, c, kT)) = h;
-        *reinterpret_cast<uint4 *>(lo + sw_off(row, c, kT)) = l;
-    }
-}
-
 // ------------------------------------------------------------------------------ pass 1
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kP1Threads, 1)
 anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ CUtensorMap tdh, const __grid_constant__ CUtensorMap tu,
                           const BwParams p) {
@@ -195,7 +181,8 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k1Bar);
     uint64_t *u_full = bars + 0, *q_full = bars + 1, *q_empty = bars + 2, *v_full = bars + 3, *v_empty = bars + 4;
     uint64_t *h_full = bars + 5, *h_empty = bars + 6, *s_full = bars + 7, *a_full = bars + 8, *a_empty = bars + 9;
-    uint64_t *acc_full = bars + 10, *mma_done = bars + 11;
+    uint64_t *acc_full = bars + 10, *mma_done = bars + 11, *x_ex = bars + 12;
+    float *s_z = reinterpret_cast<float *>(sm + k1Ex);  // [2][128]: each column half's row sums
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k1Bars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Item it = item_of(blockIdx.x, p.tiles, p.chunks);
@@ -210,13 +197,14 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         mbar_init(h_full, 1);
         mbar_init(h_empty, 1);
         mbar_init(s_full, 1);
-        mbar_init(a_full, 4);
+        mbar_init(a_full, kRowWarps);
+        mbar_init(x_ex, kRowWarps);
         mbar_init(a_empty, 1);
         mbar_init(acc_full, 1);
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
-    if (warp == kWarpMma) tmem_alloc(s_tmem, kTmemCols);
+    if (warp == kP1Issue) tmem_alloc(s_tmem, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -226,55 +214,46 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     grid_dependency_wait();
     grid_dependents_launch();
 
-    if (warp == kWarpProducer) {
+    if (warp >= kWarpProd && warp < kP1Issue) {
+        // one warp per input (U and Q, V, dH), so that no refill waits behind another
         if (lane == 0) {
-            tma_prefetch_desc(&tq);
-            tma_prefetch_desc(&tv);
-            tma_prefetch_desc(&tdh);
-            tma_prefetch_desc(&tu);
+            const int w = warp - kWarpProd;
             const uint64_t pol_keep = policy_evict_last();
-            mbar_arrive_expect_tx(u_full, kTileB);
-            load_tile(sm + k1U, &tu, u_full, 0, h, pol_keep);
-            int nq = 0, nv = 0, nh = 0;
+            const CUtensorMap *map = w == 0 ? &tq : (w == 1 ? &tv : &tdh);
+            uint64_t *full = w == 0 ? q_full : (w == 1 ? v_full : h_full);
+            uint64_t *empty = w == 0 ? q_empty : (w == 1 ? v_empty : h_empty);
+            uint8_t *dst = sm + (w == 0 ? k1Q : (w == 1 ? k1VH : k1VH + kTileB));
+            tma_prefetch_desc(map);
+            if (w == 0) {
+                tma_prefetch_desc(&tu);
+                mbar_arrive_expect_tx(u_full, kTileB);
+                load_tile(sm + k1U, &tu, u_full, 0, h, pol_keep);
+            }
+            int n = 0;
             for (int i = 0; i < it.nt; ++i) {
                 const int row = (it.t0 + i) * kT;
-                // the tiles two ahead (and, at the start, the next) into L2
+                // this input's tiles two ahead (and, at the start, the next) into L2
                 for (int k = i == 0 ? 1 : 2; k <= 2; ++k)
-                    if (i + k < it.nt) {
-                        prefetch_tile(&tq, row + k * kT, it.slice);
-                        prefetch_tile(&tv, row + k * kT, it.slice);
-                        prefetch_tile(&tdh, row + k * kT, it.slice);
-                    }
-                if (i >= 1 && !bwait(q_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(q_full, kTileB);
-                load_tile(sm + k1Q, &tq, q_full, row, it.slice, pol_keep);
-                ++nq;
-                if (i >= 1 && !bwait(v_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(v_full, kTileB);
-                load_tile(sm + k1VH, &tv, v_full, row, it.slice, pol_keep);
-                ++nv;
-                if (i >= 1 && !bwait(h_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(h_full, kTileB);
-                load_tile(sm + k1VH + kTileB, &tdh, h_full, row, it.slice, pol_keep);
-                ++nh;
+                    if (i + k < it.nt) prefetch_tile(map, row + k * kT, it.slice);
+                if (i >= 1 && !bwait(empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(full, kTileB);
+                load_tile(dst, map, full, row, it.slice, pol_keep);
+                ++n;
             }
             // the CTA leaves only once its copies have landed
-            if (nq > 0) bwait(q_full, (uint32_t)((nq - 1) & 1), p.wait_ns);
-            if (nv > 0) bwait(v_full, (uint32_t)((nv - 1) & 1), p.wait_ns);
-            if (nh > 0) bwait(h_full, (uint32_t)((nh - 1) & 1), p.wait_ns);
-            bwait(u_full, 0u, p.wait_ns);
+            if (n > 0) bwait(full, (uint32_t)((n - 1) & 1), p.wait_ns);
+            if (w == 0) bwait(u_full, 0u, p.wait_ns);
         }
         __syncwarp();
-    } else if (warp == kWarpMma) {
+    } else if (warp == kP1Issue) {
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);       // [tokens x anchors], K = d
-            const uint32_t idW = idesc_bf16_f32(kMP, kD, true, true);          // A^T V or A^T dH, K = tokens
-            const uint32_t idDl = idesc_bf16_f32(kMP, 16, true, false);        // A^T 1
+            const uint32_t idW = idesc_bf16_f32(kMP, kD, true, true);          // A^T V, K = tokens
+            const uint32_t idWD = idesc_bf16_f32(kMP, kD + 16, true, true);    // A^T [dH | 1]
             const uint64_t udesc = smem_desc_sw128(sbase + k1U, 16, 1024);
             const uint64_t qdesc = smem_desc_sw128(sbase + k1Q, 16, 1024);
             const uint64_t vdesc = smem_desc_sw128(sbase + k1VH, kBlkB, 1024);
-            const uint64_t hdesc = smem_desc_sw128(sbase + k1VH + kTileB, kBlkB, 1024);
-            const uint64_t odesc = smem_desc_sw128(sbase + k1Ones, 16, 1024);
+            const uint64_t hdesc = smem_desc_sw128(sbase + k1VH + kTileB, kBlkB, 1024);  // dH | ones
             bool ok = bwait(u_full, 0u, p.wait_ns);
             auto issue_s = [&](int i) -> bool {
                 if (!bwait(q_full, (uint32_t)(i & 1), p.wait_ns)) return false;
@@ -291,8 +270,8 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 // the row warps have read S_i and written A_i
                 if (!bwait(a_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 if (i + 1 < it.nt && !issue_s(i + 1)) { ok = false; break; }
-                // W += A^T V and Delta += A^T 1, then dW' += A^T dH (V's buffer is refilled
-                // while the dH products run)
+                // W += A^T V, then [dW' | Delta] += A^T [dH | 1] (V's buffer is refilled while
+                // the dH products run)
                 if (!bwait(v_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
@@ -303,8 +282,6 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                         const uint32_t acc = (i > 0 || part > 0 || kt > 0) ? 1u : 0u;
                         const uint64_t ak = adesc + (uint64_t)(kt * 128);
                         umma_bf16(tmem + k1ColWD, ak, vdesc + (uint64_t)(kt * 128), idW, acc);
-                        umma_bf16(tmem + k1ColDelta, ak, odesc + (uint64_t)((((kt >> 2) * 2048) + (kt & 3) * 32) >> 4),
-                                  idDl, acc);
                     }
                 }
                 umma_commit(v_empty);
@@ -315,7 +292,7 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                     const uint64_t adesc = smem_desc_sw128(sbase + (part ? k1AL : k1AH), kBlkB, 1024);
 #pragma unroll
                     for (int kt = 0; kt < kT / 16; ++kt)
-                        umma_bf16(tmem + k1ColWD + kD, adesc + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idW,
+                        umma_bf16(tmem + k1ColWD + kD, adesc + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idWD,
                                   (i > 0 || part > 0 || kt > 0) ? 1u : 0u);
                 }
                 umma_commit(a_empty);
@@ -328,50 +305,93 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ row warps
-        const int row = warp * 32 + lane;
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        {   // the ones operand [16][128] (every element 1)
+        // warp w: TMEM lanes 32 (w % 4) .. + 31 (tokens; anchors for the item's sums), column
+        // group g = w / 4 (anchors 64 g .. 64 g + 63; W or dW' for the item's sums)
+        const int row = (warp & 3) * 32 + lane, g = warp >> 2;
+        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        {   // the ones block (every element 1; the MMA reads its first 16 columns)
             const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-            for (int i = row; i < 4096 / 16; i += 128) reinterpret_cast<uint4 *>(sm + k1Ones)[i] = ones;
+            for (int i = warp * 32 + lane; i < kBlkB / 16; i += 32 * kRowWarps) reinterpret_cast<uint4 *>(sm + k1Ones)[i] = ones;
         }
         bool ok = true;
-        float v[128];
+        float e[64];
         for (int i = 0; i < it.nt && ok; ++i) {
+            const bool valid = (it.t0 + i) * kT + row < p.n;
             if (!bwait(s_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
+            {   // the row maximum over all 128 scores, then this half's exponentials and sum
+                float sv[128];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(trow + k1ColS + 32 * q, v + 32 * q);
-            tmem_ld_wait();
-            softmax128(v, p.m, p.c, (it.t0 + i) * kT + row < p.n);
+                for (int q = 0; q < 4; ++q) tmem_ld32(trow + k1ColS + 32 * q, sv + 32 * q);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 128; ++j) sv[j] = j < p.m ? sv[j] * p.c : -INFINITY;
+                float m8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = sv[k];
+#pragma unroll
+                for (int j = 8; j < 128; j += 8)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[j + k]);
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                if (g == 0) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(sv[j] - mx);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(sv[64 + j] - mx);
+                }
+            }
+            float z4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 64; ++j) z4[j & 3] += e[j];
+            s_z[g * kT + row] = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x_ex);
+            if (!bwait(x_ex, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+            const float z = s_z[row] + s_z[kT + row];
+            const float zinv = valid ? 1.f / z : 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) e[j] *= zinv;
             if (i >= 1 && !bwait(a_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
-            store_split128(sm + k1AH, sm + k1AL, row, v);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 hi, lo;
+                split8(e + 8 * c, hi, lo);
+                *reinterpret_cast<uint4 *>(sm + k1AH + sw_off(row, 8 * g + c, kT)) = hi;
+                *reinterpret_cast<uint4 *>(sm + k1AL + sw_off(row, 8 * g + c, kT)) = lo;
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full);
         }
-        // the item's W | dW' | Delta: anchor j = row
+        // the item's W | dW' | Delta: anchor j = row; group 0 W and Delta, group 1 dW'
         ok = ok && it.nt > 0 && bwait(acc_full, 0u, p.wait_ns);
         if (ok) {
             tc_fence_after();
             float *dst = p.part + (size_t)blockIdx.x * kPartF;
+            float o[32];
 #pragma unroll 1
-            for (int q = 0; q < 8; ++q) {
-                tmem_ld32(trow + k1ColWD + 32 * q, v);
+            for (int q = 0; q < 4; ++q) {
+                tmem_ld32(trow + k1ColWD + 128 * g + 32 * q, o);
                 tmem_ld_wait();
-                float4 *o = reinterpret_cast<float4 *>(dst + (size_t)row * 2 * kD + 32 * q);
+                float4 *d4 = reinterpret_cast<float4 *>(dst + (size_t)row * 2 * kD + 128 * g + 32 * q);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                for (int k = 0; k < 8; ++k) d4[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
             }
-            tmem_ld32(trow + k1ColDelta, v);
-            tmem_ld_wait();
-            dst[kMP * 2 * kD + row] = v[0];
+            if (g == 0) {
+                tmem_ld32(trow + k1ColDelta, o);
+                tmem_ld_wait();
+                dst[kMP * 2 * kD + row] = o[0];
+            }
             tc_fence_before();
         }
         __syncwarp();
     }
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kP1Issue) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -432,7 +452,7 @@ anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m,
 }
 
 // ------------------------------------------------------------------------------ pass 2
-__global__ void __launch_bounds__(k2Threads, 1)
+__global__ void __launch_bounds__(kP2Threads, 1)
 anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ CUtensorMap tdh, const __grid_constant__ CUtensorMap tu,
                           const __grid_constant__ CUtensorMap timg, const __grid_constant__ CUtensorMap tdq,
@@ -480,7 +500,7 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         mbar_init(x_ex, 8);
         fence_mbar_init();
     }
-    if (warp == kWarp2Mma) tmem_alloc(s_tmem, kTmemCols);
+    if (warp == kP2Issue) tmem_alloc(s_tmem, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -489,21 +509,22 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     grid_dependency_wait();
     grid_dependents_launch();
 
-    if (warp == kWarp2Producer) {
+    if (warp == kWarpProd) {
         if (lane == 0) {
+            // Q_i once dU has read Q_{i-1}; dH_i once dU has read dS_lo of tile i - 1 over
+            // dH_{i-1}; V_i once dQ and dU have read dS_hi over V_{i-1} (the tiles ahead are
+            // prefetched to L2)
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tv);
             tma_prefetch_desc(&tdh);
             tma_prefetch_desc(&tu);
-            tma_prefetch_desc(&timg);
             tma_prefetch_desc(&tdq);
             tma_prefetch_desc(&tdv);
             const uint64_t pol_keep = policy_evict_last(), pol_once = policy_evict_first();
             mbar_arrive_expect_tx(u_full, kTileB);
             load_tile(sm + k2U, &tu, u_full, 0, h, pol_keep);
-            int nq = 0, nv = 0, nh = 0, nimg[2] = {0, 0};
-            bool ok = true;
-            for (int i = 0; i < it.nt && ok; ++i) {
+            int nq = 0, nh = 0, nv = 0;
+            for (int i = 0; i < it.nt; ++i) {
                 const int row = (it.t0 + i) * kT;
                 for (int k = i == 0 ? 1 : 2; k <= 2; ++k)
                     if (i + k < it.nt) {
@@ -511,13 +532,10 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                         prefetch_tile(&tv, row + k * kT, it.slice);
                         prefetch_tile(&tdh, row + k * kT, it.slice);
                     }
-                // Q_i once dU has read Q_{i-1} (it comes from L2: the tiles ahead are prefetched)
                 if (i >= 1 && !bwait(x_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
                 mbar_arrive_expect_tx(q_full, kTileB);
                 load_tile(sm + k2X, &tq, q_full, row, it.slice, pol_once);
                 ++nq;
-                // dH_i once dU has read dS_lo of tile i - 1 there, then V_i once dQ and dU have
-                // read dS_hi
                 if (i >= 1 && !bwait(h_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
                 mbar_arrive_expect_tx(h_full, kTileB);
                 load_tile(sm + k2VH + kTileB, &tdh, h_full, row, it.slice, pol_once);
@@ -526,25 +544,31 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 mbar_arrive_expect_tx(v_full, kTileB);
                 load_tile(sm + k2VH, &tv, v_full, row, it.slice, pol_once);
                 ++nv;
-                // the images W'_hi, W'_lo, dW_hi, dW_lo (unit u = 4 i + part, slot u & 1)
-                for (int part = 0; part < 4; ++part) {
-                    const int u = 4 * i + part, s = u & 1;
-                    if (u >= 2 && !bwait(img_empty + s, (uint32_t)(((u >> 1) - 1) & 1), p.wait_ns)) { ok = false; break; }
-                    mbar_arrive_expect_tx(img_full + s, kTileB);
-                    load_tile(sm + k2Img + s * kTileB, &timg, img_full + s, 0, it.slice * 4 + part, pol_keep);
-                    ++nimg[s];
-                }
             }
             if (nq > 0) bwait(q_full, (uint32_t)((nq - 1) & 1), p.wait_ns);
-            for (int b = 0; b < 2; ++b) {
-                if (nimg[b] > 0) bwait(img_full + b, (uint32_t)((nimg[b] - 1) & 1), p.wait_ns);
-            }
             if (nh > 0) bwait(h_full, (uint32_t)((nh - 1) & 1), p.wait_ns);
             if (nv > 0) bwait(v_full, (uint32_t)((nv - 1) & 1), p.wait_ns);
             bwait(u_full, 0u, p.wait_ns);
         }
         __syncwarp();
-    } else if (warp == kWarp2Mma) {
+    } else if (warp == kWarpProd + 1) {
+        if (lane == 0) {
+            // the images W'_hi, W'_lo, dW_hi, dW_lo of every tile (unit u = 4 i + part, slot u & 1)
+            tma_prefetch_desc(&timg);
+            const uint64_t pol_keep = policy_evict_last();
+            int nimg[2] = {0, 0};
+            for (int u = 0; u < 4 * it.nt; ++u) {
+                const int s = u & 1;
+                if (u >= 2 && !bwait(img_empty + s, (uint32_t)(((u >> 1) - 1) & 1), p.wait_ns)) break;
+                mbar_arrive_expect_tx(img_full + s, kTileB);
+                load_tile(sm + k2Img + s * kTileB, &timg, img_full + s, 0, it.slice * 4 + (u & 3), pol_keep);
+                ++nimg[s];
+            }
+            for (int b = 0; b < 2; ++b)
+                if (nimg[b] > 0) bwait(img_full + b, (uint32_t)((nimg[b] - 1) & 1), p.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == kP2Issue) {
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);  // [tokens x anchors], K = d
             const uint32_t idR = idesc_bf16_f32(kT, kD, false, true);    // [tokens x d], K = anchors
@@ -800,7 +824,7 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         __syncwarp();
     }
     __syncthreads();
-    if (warp == kWarp2Mma) {
+    if (warp == kP2Issue) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -877,14 +901,14 @@ cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t s
     bp.dV = static_cast<__nv_bfloat16 *>(p.dV);
     bp.wait_ns = 2000000000ull;
     const dim3 grid((unsigned)(S * chunks));
-    if ((e = launch_pdl(anchor_bwd_wide_p1_kernel, grid, dim3(kThreads), k1Smem, stream, tq, tv, tdh, tu, bp)) !=
+    if ((e = launch_pdl(anchor_bwd_wide_p1_kernel, grid, dim3(kP1Threads), k1Smem, stream, tq, tv, tdh, tu, bp)) !=
         cudaSuccess)
         return e;
     if ((e = launch_pdl(anchor_bwd_wide_reduce_kernel, dim3((unsigned)S, kMP / kRJ), dim3(kD), 0, stream,
                         (const float *)bp.part, chunks, p.m, reinterpret_cast<__nv_bfloat16 *>(ws + L.img),
                         reinterpret_cast<float *>(ws + L.dd))) != cudaSuccess)
         return e;
-    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel, grid, dim3(k2Threads), k2Smem, stream, tq, tv, tdh, tu, timg, tdq, tdv, bp)) !=
+    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel, grid, dim3(kP2Threads), k2Smem, stream, tq, tv, tdh, tu, timg, tdq, tdv, bp)) !=
         cudaSuccess)
         return e;
     return launch_bwd_du_sum(bp.dupart, p.dU, p.B, p.heads, chunks, p.m * kD, false, stream);
