@@ -703,8 +703,9 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         auto drain_dv = [&](int i, float zinv) -> bool { return drain(i, dv_full, dv_empty, k2ColDV, &tdv, zinv); };
         for (int i = 0; i < it.nt && ok; ++i) {
             const bool valid = (it.t0 + i) * kT + row < p.n;
-            // dQ of the tile before first: it holds G's columns, which G_i needs
-            if (i >= 1 && !drain_dq(i - 1)) { ok = false; break; }
+            // dQ and dV of the tile before first (dQ holds G's columns, which G_i needs, and the
+            // rows would otherwise wait here for S_i)
+            if (i >= 1 && !(drain_dq(i - 1) && drain_dv(i - 1, zinv_prev))) { ok = false; break; }
             if (!bwait(s_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             float mx;
@@ -755,7 +756,6 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full);
-            if (i >= 1 && !drain_dv(i - 1, zinv_prev)) { ok = false; break; }
             // dS_j = A_j (G_j + dDelta_j - sum_l A_l (G_l + dDelta_l)), A = e / z, over V_i and dH_i
             if (!bwait(g_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
