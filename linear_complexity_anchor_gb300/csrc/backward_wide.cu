@@ -626,8 +626,9 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 umma_commit(img_empty + 1);
                 umma_commit(s_free);  // A_i read: S_{i+1} may be written there
                 // dU += dS_lo^T Q_i first (dS_lo is over dH_i, whose buffer then takes dH_{i+1}),
-                // then dQ_i = dS_hi U (into G's columns; dQ sums over the m anchors only, so one
-                // bf16 part is enough) and dU += dS_hi^T Q_i (dS_hi over V_i)
+                // then dU += dS_hi^T Q_i (Q's buffer then takes Q_{i+1}), then dQ_i = dS_hi U
+                // (into G's columns; dQ sums over the m anchors only, so one bf16 part is enough;
+                // V's buffer, under dS_hi, then takes V_{i+1})
                 if (!bwait(ds_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 {
@@ -641,15 +642,15 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                     const uint64_t dsk = smem_desc_sw128(sbase + k2VH, 16, 1024);
                     const uint64_t dsm = smem_desc_sw128(sbase + k2VH, kBlkB, 1024);  // dS_hi^T: anchors x tokens
 #pragma unroll
-                    for (int kj = 0; kj < kMP / 16; ++kj)
-                        umma_bf16(tmem + k2ColG, dsk + kstep(kj), umn + (uint64_t)(kj * 128), idR, kj > 0 ? 1u : 0u);
-#pragma unroll
                     for (int kt = 0; kt < kT / 16; ++kt)
                         umma_bf16(tmem + k2ColDU, dsm + (uint64_t)(kt * 128), qm + (uint64_t)(kt * 128), idU, 1u);
+                    umma_commit(x_free);  // Q_i read: Q_{i+1} may load there
+#pragma unroll
+                    for (int kj = 0; kj < kMP / 16; ++kj)
+                        umma_bf16(tmem + k2ColG, dsk + kstep(kj), umn + (uint64_t)(kj * 128), idR, kj > 0 ? 1u : 0u);
                 }
                 umma_commit(dq_full);
                 umma_commit(v_free);
-                umma_commit(x_free);  // Q_i read: Q_{i+1} may load there
             }
             if (ok && it.nt > 0) umma_commit(du_full);
             umma_commit(mma_done);
