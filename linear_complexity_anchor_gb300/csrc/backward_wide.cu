@@ -58,7 +58,7 @@ constexpr int kPartF = kMP * 2 * kD + kMP;  // an item's pass-1 block: [W | dW']
 // operand) | A_hi | A_lo | row-sum exchange [2][128] | barriers
 constexpr int k1U = 0, k1Q = k1U + kTileB, k1VH = k1Q + kTileB, k1Ones = k1VH + 2 * kTileB;
 constexpr int k1AH = k1Ones + kBlkB, k1AL = k1AH + kTileB, k1Ex = k1AL + kTileB, k1Bar = k1Ex + 2 * kT * 4;
-constexpr int k1Bars = 13;
+constexpr int k1Bars = 15;
 constexpr int k1Smem = k1Bar + k1Bars * 8 + 16 + 1024;
 static_assert(k1Smem <= 227 * 1024, "pass 1 shared memory");
 constexpr uint32_t k1ColS = 0, k1ColWD = 128, k1ColDelta = 384;
@@ -181,7 +181,8 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k1Bar);
     uint64_t *u_full = bars + 0, *q_full = bars + 1, *q_empty = bars + 2, *v_full = bars + 3, *v_empty = bars + 4;
     uint64_t *h_full = bars + 5, *h_empty = bars + 6, *s_full = bars + 7, *a_full = bars + 8, *a_empty = bars + 9;
-    uint64_t *acc_full = bars + 10, *mma_done = bars + 11, *x_ex = bars + 12;
+    uint64_t *acc_full = bars + 10, *mma_done = bars + 11, *x_ex = bars + 12, *al_full = bars + 13,
+             *al_empty = bars + 14;  // a_full / a_empty: A_hi's
     float *s_z = reinterpret_cast<float *>(sm + k1Ex);  // [2][128]: each column half's row sums
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k1Bars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -198,6 +199,8 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         mbar_init(h_empty, 1);
         mbar_init(s_full, 1);
         mbar_init(a_full, kRowWarps);
+        mbar_init(al_full, kRowWarps);
+        mbar_init(al_empty, 1);
         mbar_init(x_ex, kRowWarps);
         mbar_init(a_empty, 1);
         mbar_init(acc_full, 1);
@@ -267,35 +270,36 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             };
             if (ok && it.nt > 0) ok = issue_s(0);
             for (int i = 0; i < it.nt && ok; ++i) {
-                // the row warps have read S_i and written A_i
+                // the row warps have read S_i and written A_hi of tile i
                 if (!bwait(a_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 if (i + 1 < it.nt && !issue_s(i + 1)) { ok = false; break; }
-                // W += A^T V, then [dW' | Delta] += A^T [dH | 1] (V's buffer is refilled while
-                // the dH products run)
+                // W += A_hi^T V + A_lo^T V (then V's buffer is refilled), [dW' | Delta] +=
+                // A_hi^T [dH | 1] (then A_hi's buffer takes the next tile's) + A_lo^T [dH | 1]
+                const uint64_t ahd = smem_desc_sw128(sbase + k1AH, kBlkB, 1024);  // A^T, MN-major
+                const uint64_t ald = smem_desc_sw128(sbase + k1AL, kBlkB, 1024);
                 if (!bwait(v_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint64_t adesc = smem_desc_sw128(sbase + (part ? k1AL : k1AH), kBlkB, 1024);  // A^T, MN-major
+                for (int kt = 0; kt < kT / 16; ++kt)
+                    umma_bf16(tmem + k1ColWD, ahd + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), idW,
+                              (i > 0 || kt > 0) ? 1u : 0u);
+                if (!bwait(al_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll
-                    for (int kt = 0; kt < kT / 16; ++kt) {
-                        const uint32_t acc = (i > 0 || part > 0 || kt > 0) ? 1u : 0u;
-                        const uint64_t ak = adesc + (uint64_t)(kt * 128);
-                        umma_bf16(tmem + k1ColWD, ak, vdesc + (uint64_t)(kt * 128), idW, acc);
-                    }
-                }
+                for (int kt = 0; kt < kT / 16; ++kt)
+                    umma_bf16(tmem + k1ColWD, ald + (uint64_t)(kt * 128), vdesc + (uint64_t)(kt * 128), idW, 1u);
                 umma_commit(v_empty);
                 if (!bwait(h_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint64_t adesc = smem_desc_sw128(sbase + (part ? k1AL : k1AH), kBlkB, 1024);
-#pragma unroll
-                    for (int kt = 0; kt < kT / 16; ++kt)
-                        umma_bf16(tmem + k1ColWD + kD, adesc + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idWD,
-                                  (i > 0 || part > 0 || kt > 0) ? 1u : 0u);
-                }
+                for (int kt = 0; kt < kT / 16; ++kt)
+                    umma_bf16(tmem + k1ColWD + kD, ahd + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idWD,
+                              (i > 0 || kt > 0) ? 1u : 0u);
                 umma_commit(a_empty);
+#pragma unroll
+                for (int kt = 0; kt < kT / 16; ++kt)
+                    umma_bf16(tmem + k1ColWD + kD, ald + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idWD, 1u);
+                umma_commit(al_empty);
                 umma_commit(h_empty);
             }
             if (ok) umma_commit(acc_full);
@@ -354,18 +358,23 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             const float zinv = valid ? 1.f / z : 0.f;
 #pragma unroll
             for (int j = 0; j < 64; ++j) e[j] *= zinv;
+            uint4 hi[8], lo[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) split8(e + 8 * c, hi[c], lo[c]);
+            // A_hi once the previous tile's products have read it, then A_lo likewise
             if (i >= 1 && !bwait(a_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 hi, lo;
-                split8(e + 8 * c, hi, lo);
-                *reinterpret_cast<uint4 *>(sm + k1AH + sw_off(row, 8 * g + c, kT)) = hi;
-                *reinterpret_cast<uint4 *>(sm + k1AL + sw_off(row, 8 * g + c, kT)) = lo;
-            }
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(sm + k1AH + sw_off(row, 8 * g + c, kT)) = hi[c];
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full);
+            if (i >= 1 && !bwait(al_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(sm + k1AL + sw_off(row, 8 * g + c, kT)) = lo[c];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(al_full);
         }
         // the item's W | dW' | Delta: anchor j = row; group 0 W and Delta, group 1 dW'
         ok = ok && it.nt > 0 && bwait(acc_full, 0u, p.wait_ns);
