@@ -57,7 +57,7 @@ constexpr int kPartF = kMP * 2 * kD + kMP;  // an item's pass-1 block: [W | dW']
 // pass 1: U | Q | V | dH | ones [128][64] (dH's third 64-column block: [dH | 1] is one N = 144
 // operand) | A_hi | A_lo | row-sum exchange [2][128] | barriers
 constexpr int k1U = 0, k1Q = k1U + kTileB, k1VH = k1Q + kTileB, k1Ones = k1VH + 2 * kTileB;
-constexpr int k1AH = k1Ones + kBlkB, k1AL = k1AH + kTileB, k1Ex = k1AL + kTileB, k1Bar = k1Ex + 2 * kT * 4;
+constexpr int k1AH = k1Ones + kBlkB, k1AL = k1AH + kTileB, k1Ex = k1AL + kTileB, k1Bar = k1Ex + 2 * kT * 8;
 constexpr int k1Bars = 15;
 constexpr int k1Smem = k1Bar + k1Bars * 8 + 16 + 1024;
 static_assert(k1Smem <= 227 * 1024, "pass 1 shared memory");
@@ -106,13 +106,18 @@ __device__ __forceinline__ uint4 pack8(const float *x, float r) {
     return make_uint4(pack2(x[0] * r, x[1] * r), pack2(x[2] * r, x[3] * r), pack2(x[4] * r, x[5] * r),
                       pack2(x[6] * r, x[7] * r));
 }
-// bf16 parts of 8 floats: hi = round(x), lo = round(x - hi)
+// bf16 parts of 8 floats: hi = round(x), lo = round(x - hi) (hi read back from its packed pair:
+// the low bf16 of a pair is the even element)
 __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
-    float r[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) r[i] = x[i] - __bfloat162float(__float2bfloat16_rn(x[i]));
-    hi = pack8(x, 1.f);
-    lo = pack8(r, 1.f);
+    for (int k = 0; k < 4; ++k) {
+        h[k] = pack2(x[2 * k], x[2 * k + 1]);
+        const float h0 = __uint_as_float(h[k] << 16), h1 = __uint_as_float(h[k] & 0xffff0000u);
+        l[k] = pack2(x[2 * k] - h0, x[2 * k + 1] - h1);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limit_ns) {
@@ -183,7 +188,7 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     uint64_t *h_full = bars + 5, *h_empty = bars + 6, *s_full = bars + 7, *a_full = bars + 8, *a_empty = bars + 9;
     uint64_t *acc_full = bars + 10, *mma_done = bars + 11, *x_ex = bars + 12, *al_full = bars + 13,
              *al_empty = bars + 14;  // a_full / a_empty: A_hi's
-    float *s_z = reinterpret_cast<float *>(sm + k1Ex);  // [2][128]: each column half's row sums
+    float2 *s_mz = reinterpret_cast<float2 *>(sm + k1Ex);  // [2][128]: each column half's (max, sum)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k1Bars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Item it = item_of(blockIdx.x, p.tiles, p.chunks);
@@ -323,39 +328,41 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             const bool valid = (it.t0 + i) * kT + row < p.n;
             if (!bwait(s_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
-            {   // the row maximum over all 128 scores, then this half's exponentials and sum
-                float sv[128];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) tmem_ld32(trow + k1ColS + 32 * q, sv + 32 * q);
+            // this half's maximum, exponentials and sum; the halves' (max, sum) exchanged, and
+            // both scaled to the row's maximum: A_j = e_j 2^(m_g - M) / (z_0 2^(m_0 - M) + z_1 2^(m_1 - M))
+            float mg;
+            {
+                tmem_ld32(trow + k1ColS + 64 * g, e);
+                tmem_ld32(trow + k1ColS + 64 * g + 32, e + 32);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 128; ++j) sv[j] = j < p.m ? sv[j] * p.c : -INFINITY;
+                for (int j = 0; j < 64; ++j) e[j] = 64 * g + j < p.m ? e[j] * p.c : -INFINITY;
                 float m8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) m8[k] = sv[k];
+                for (int k = 0; k < 8; ++k) m8[k] = e[k];
 #pragma unroll
-                for (int j = 8; j < 128; j += 8)
+                for (int j = 8; j < 64; j += 8)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[j + k]);
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                if (g == 0) {
+                    for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], e[j + k]);
+                mg = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                // a half with every anchor masked (m <= 64) has no maximum: its terms are zero
+                const float ms = mg == -INFINITY ? 0.f : mg;
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(sv[j] - mx);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(sv[64 + j] - mx);
-                }
+                for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(e[j] - ms);
             }
             float z4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 64; ++j) z4[j & 3] += e[j];
-            s_z[g * kT + row] = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+            s_mz[g * kT + row] = make_float2(mg, (z4[0] + z4[1]) + (z4[2] + z4[3]));
             __syncwarp();
             if (lane == 0) mbar_arrive(x_ex);
             if (!bwait(x_ex, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
-            const float z = s_z[row] + s_z[kT + row];
-            const float zinv = valid ? 1.f / z : 0.f;
+            const float2 h0 = s_mz[row], h1 = s_mz[kT + row];
+            const float M = fmaxf(h0.x, h1.x);  // finite: half 0 holds anchor 0
+            const float f0 = h0.x == -INFINITY ? 0.f : rowops::ex2_approx(h0.x - M);
+            const float f1 = h1.x == -INFINITY ? 0.f : rowops::ex2_approx(h1.x - M);
+            const float z = h0.y * f0 + h1.y * f1;
+            const float zinv = valid ? (g == 0 ? f0 : f1) / z : 0.f;
 #pragma unroll
             for (int j = 0; j < 64; ++j) e[j] *= zinv;
             uint4 hi[8], lo[8];
