@@ -725,44 +725,54 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             if (i >= 1 && !(drain_dq(i - 1) && drain_dv(i - 1, zinv_prev))) { ok = false; break; }
             if (!bwait(s_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
-            float mx;
-            {   // the row maximum over all 128 scores (each group reads the whole row), then
-                // this group's exponentials and their sum
-                float sv[128];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) tmem_ld32(trow + k2ColS + 32 * q, sv + 32 * q);
+            // this half's maximum, exponentials and sum; the halves' (max, sum) exchanged through
+            // the last two of each half's own (already read) S columns, and e scaled to the row's
+            // maximum M (both halves of dV's A operand must share it): A = e / z with
+            // z = z_0 2^(m_0 - M) + z_1 2^(m_1 - M)
+            float zinv;
+            {
+                tmem_ld32(trow + k2ColS + 64 * g, e);
+                tmem_ld32(trow + k2ColS + 64 * g + 32, e + 32);
                 tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_empty);
 #pragma unroll
-                for (int j = 0; j < 128; ++j) sv[j] = j < p.m ? sv[j] * p.c : -INFINITY;
+                for (int j = 0; j < 64; ++j) e[j] = 64 * g + j < p.m ? e[j] * p.c : -INFINITY;
                 float m8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) m8[k] = sv[k];
+                for (int k = 0; k < 8; ++k) m8[k] = e[k];
 #pragma unroll
-                for (int j = 8; j < 128; j += 8)
+                for (int j = 8; j < 64; j += 8)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[j + k]);
-                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                if (g == 0) {
+                    for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], e[j + k]);
+                const float mg = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                const float ms = mg == -INFINITY ? 0.f : mg;  // a half with every anchor masked
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(sv[j] - mx);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(sv[64 + j] - mx);
-                }
-            }
-            float zg = 0.f;
-            {
+                for (int j = 0; j < 64; ++j) e[j] = rowops::ex2_approx(e[j] - ms);
                 float z4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < 64; ++j) z4[j & 3] += e[j];
-                zg = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+                const float2 mine = make_float2(mg, (z4[0] + z4[1]) + (z4[2] + z4[3]));
+                tmem_st2(trow + k2ColS + 64 * g + 62, mine.x, mine.y);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty);  // this warp has read S_i and written its pair
+                if (!bwait(s_empty, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+                // (the other half's pair only: half 1 writes its A over half 0's pair columns
+                // once it has read them)
+                const float2 other = tmem_ld2(trow + k2ColS + 64 * (1 - g) + 62);
+                tmem_ld_wait();
+                const float2 h0 = g == 0 ? mine : other, h1 = g == 0 ? other : mine;
+                const float M = fmaxf(h0.x, h1.x);  // finite: half 0 holds anchor 0
+                const float f0 = h0.x == -INFINITY ? 0.f : rowops::ex2_approx(h0.x - M);
+                const float f1 = h1.x == -INFINITY ? 0.f : rowops::ex2_approx(h1.x - M);
+                const float fg = g == 0 ? f0 : f1;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) e[j] *= fg;
+                zinv = valid ? 1.f / (h0.y * f0 + h1.y * f1) : 0.f;
             }
-            // e (bf16 pairs) over S's columns 32 g .. 32 g + 31 (dV's A operand), once all eight
-            // row warps have read S_i
-            if (!bwait(s_empty, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
+            // e (bf16 pairs) over S's columns 32 g .. 32 g + 31 (dV's A operand)
             {
                 uint32_t pk[32];
 #pragma unroll
@@ -787,10 +797,10 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 r4[j & 3] = fmaf(e[j], gv[j], r4[j & 3]);
             }
             const float rg = (r4[0] + r4[1]) + (r4[2] + r4[3]);
-            // the two groups' (z, r) through tensor memory: each writes them into the first two
-            // of its own (already read) G columns and reads the other group's (G's columns
-            // take dQ_i only after every row warp has passed ds_full)
-            tmem_st2(trow + k2ColG + 64 * g, zg, rg);
+            // the two halves' r through tensor memory: each writes it into the first of its own
+            // (already read) G columns and reads the other half's (G's columns take dQ_i only
+            // after every row warp has passed ds_full)
+            tmem_st2(trow + k2ColG + 64 * g, rg, 0.f);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -799,9 +809,7 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             tc_fence_after();
             const float2 other = tmem_ld2(trow + k2ColG + 64 * (1 - g));
             tmem_ld_wait();
-            const float z = g == 0 ? zg + other.x : other.x + zg;
-            const float rr = g == 0 ? rg + other.y : other.y + rg;
-            const float zinv = valid ? 1.f / z : 0.f;
+            const float rr = g == 0 ? rg + other.x : other.x + rg;
             const float rs = rr * zinv;
 #pragma unroll
             for (int j = 0; j < 64; ++j) gv[j] = e[j] * zinv * (gv[j] - rs);
