@@ -100,8 +100,8 @@ def test_backward_wide_tensor_core_shapes(env, shape):
 
 def test_backward_long_16k_sampled_heads(env):
     """Full size (4 x 16 slices of 16384 tokens, 128 anchors, d = 128): dQ and dV of every
-    batch entry of three heads element by element, and those heads' dU against the sum of
-    their four slices' shares."""
+    batch entry of four heads (16 of the 64 slices) element by element, and those heads' dU
+    against the sum of their four slices' shares."""
     pkg, torch, orc = env
     w = gen.WORKLOADS["long_16k"]
     x = gen.make_inputs(w, seed=0)
@@ -110,7 +110,7 @@ def test_backward_long_16k_sampled_heads(env):
     dQ, dU, dV = pkg.backward(t["Q"], t["U"], t["V"], to_device(dH, w.dtype, torch), scale=w.scale)
     torch.cuda.synchronize()
     assert pkg.device_error() == 0
-    heads = [0, 7, w.heads - 1]
+    heads = [0, 5, 10, w.heads - 1]
     dQh = {(b, h): to_host64(dQ[b, h]) for b in range(w.B) for h in heads}
     dVh = {(b, h): to_host64(dV[b, h]) for b in range(w.B) for h in heads}
     dUh = to_host64(dU)
