@@ -27,7 +27,8 @@
 // U, L, A, B / P, W_pre image, 32 KB each.  Tensor memory: S / C at 0, P at 128, H at 256,
 // W_pre at 384.
 // Warps: 0-3 row warps (TMEM lanes 32w..32w+31: tokens, or anchors for the W_pre image; a
-// tile's H goes out while the next tile's C runs), 4 producer (TMA), 5 MMA issuer.  Sums run
+// tile's H goes out while the next tile's C runs, staged in the warp's own rows of the B / P
+// tile and written by TMA stores), 4 producer (TMA), 5 MMA issuer.  Sums run
 // in a fixed order: results are bit-identical from run to run.  Every wait is bounded; one
 // that gives up sets bit 0 of this kernel's error word and the CTA drains what it has in
 // flight and leaves.
@@ -108,7 +109,8 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limi
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
-                          const __grid_constant__ CUtensorMap tu, const CwParams p) {
+                          const __grid_constant__ CUtensorMap tu, const __grid_constant__ CUtensorMap th,
+                          const CwParams p) {
     using LY = WideLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -180,6 +182,7 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tv);
             tma_prefetch_desc(&tu);
+            tma_prefetch_desc(&th);
             const uint64_t pol_keep = policy_evict_last(), pol_once = policy_evict_first();
             mbar_arrive_expect_tx(u_full, LY::kQB);
 #pragma unroll
@@ -299,27 +302,41 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
         float a[kMP];
-        // H of full tile u (slice tile t0 + u) out of tensor memory to global (rows past the
-        // slice are not stored)
+        // H of full tile u (slice tile t0 + u): tensor memory -> this warp's own rows of the
+        // B / P tile (free: the tile's H products have read P; the same swizzled layout as a
+        // [32][64] TMA box) -> TMA stores (rows past the slice are not written).  The warp's
+        // next B rows are written once the stores have read them.
+        const uint64_t pol_out = policy_evict_first();
         auto store_h = [&](int u) -> bool {
             if (!bwait(h_full, (uint32_t)(u & 1), p.wait_ns)) return false;
             tc_fence_after();
-            const int tok = (t0 + u) * kT + row;
-            const bool valid_u = tok < p.n;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.H + ((size_t)slice * p.n + (size_t)tok) * D);
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 float o[32];
                 tmem_ld32(trow + kColH + q * 32, o);
                 tmem_ld_wait();
-                if (valid_u)
+                uint8_t *box = sm + LY::kOffB + (q >> 1) * kBlkB + warp * 4096;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) dst[q * 4 + c] = pack8(o + 8 * c);
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(box + sw_off(lane, (q & 1) * 4 + c, 32)) = pack8(o + 8 * c);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(h_empty);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(h_empty);
+#pragma unroll
+                for (int k = 0; k < D / 64; ++k)
+                    tma_store_3d(&th, sm + LY::kOffB + k * kBlkB + warp * 4096, 64 * k, (t0 + u) * kT + warp * 32,
+                                 slice, pol_out);
+                bulk_commit_group();
+            }
             return true;
+        };
+        auto stores_read = [&]() {  // this warp's H stores have read its B rows
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
         };
         for (int t = 0; t < T && ok; ++t) {
             const uint32_t ph = (uint32_t)(t & 1);
@@ -392,6 +409,7 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 __syncwarp();
                 if (lane == 0) mbar_arrive(wi_full);
             }
+            stores_read();
             // Delta^(i) = Delta_pre + C_t[i]; B = A / Delta^(i).  The first full tile after
             // summary tiles reads the Delta_pre the last of them wrote.
             if (u == 0 && t0 > 0 && !bwait(dp_full, (uint32_t)((t0 - 1) & 1), p.wait_ns)) { ok = false; break; }
@@ -447,6 +465,7 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             if (lane == 0) mbar_arrive(pm_full);
         }
         if (ok && t1 > t0) store_h(t1 - t0 - 1);  // the last tile's H
+        if (lane == 0) bulk_wait_group0();       // the stores have landed
         __syncwarp();
     }
     __syncthreads();
@@ -469,10 +488,10 @@ int causal_wide_chunks(long long slices, int tiles) {
 template <int D>
 cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     using LY = WideLayout<D>;
-    CUtensorMap tq, tv, tu;
+    CUtensorMap tq, tv, tu, th;
     const long long S = p.slices();
     if (!make_bf16_map(&tq, p.Q, D, p.n, S, kT) || !make_bf16_map(&tv, p.V, D, p.n, S, kT) ||
-        !make_bf16_map(&tu, p.U, D, p.m, p.heads, kMP))
+        !make_bf16_map(&tu, p.U, D, p.m, p.heads, kMP) || !make_bf16_map(&th, p.H, D, p.n, S, 32))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(anchor_causal_wide_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem);
     if (e != cudaSuccess) return e;
@@ -486,7 +505,7 @@ cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     cp.H = static_cast<__nv_bfloat16 *>(p.H);
     cp.wait_ns = 2000000000ull;
     return launch_pdl(anchor_causal_wide_kernel<D>, dim3((unsigned)(S * cp.chunks)), dim3(kThreads), LY::kSmem, stream,
-                      tq, tv, tu, cp);
+                      tq, tv, tu, th, cp);
 }
 
 }  // namespace
