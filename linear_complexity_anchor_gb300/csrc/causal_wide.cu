@@ -106,6 +106,23 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limi
     return true;
 }
 
+// First tile of chunk c of a slice's `tiles` tiles.  A chunk first walks the tiles before it
+// as summary tiles (S, A and the summaries' products only), which cost about kSummaryCost of a
+// full tile, so later chunks get fewer full tiles: the boundaries equalise
+// (full tiles) + kSummaryCost * (summary tiles) over the chunks.
+constexpr float kSummaryCost = 0.5f;
+__host__ __device__ __forceinline__ int chunk_bound(int c, int tiles, int chunks) {
+    if (c <= 0) return 0;
+    if (c >= chunks) return tiles;
+    if (kSummaryCost <= 0.f) return (int)((long long)c * tiles / chunks);
+    const float r = 1.f - kSummaryCost;
+    float rc = 1.f, rk = 1.f;
+    for (int i = 0; i < c; ++i) rc *= r;
+    for (int i = 0; i < chunks; ++i) rk *= r;
+    const int b = (int)((float)tiles * (1.f - rc) / (1.f - rk) + 0.5f);
+    return b < c ? c : (b > tiles - (chunks - c) ? tiles - (chunks - c) : b);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
@@ -128,7 +145,7 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     // this CTA's tiles: [t0, t1) of the slice; tiles [0, t0) run first as summary tiles (S,
     // softmax, C for Delta, W only), which leave W_pre and Delta_pre exactly as a CTA that
     // ran them in full would (the same MMAs and additions in the same order)
-    const int t0 = (int)((long long)chunk * p.tiles / p.chunks), t1 = (int)((long long)(chunk + 1) * p.tiles / p.chunks);
+    const int t0 = chunk_bound(chunk, p.tiles, p.chunks), t1 = chunk_bound(chunk + 1, p.tiles, p.chunks);
     const int T = t1;
 
     if (threadIdx.x == 0) {
@@ -476,8 +493,9 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
 }
 
 // CTAs per slice: with fewer slices than SMs, the tokens of a slice are cut into up to four
-// chunks of at least four tiles, one CTA each (one CTA per SM).  The chunk boundaries do not
-// change the results (each chunk first sums the tiles before it in the same order).
+// chunks of at least four tiles, one CTA each (one CTA per SM), at the boundaries
+// chunk_bound gives.  The chunk boundaries do not change the results (each chunk first sums
+// the tiles before it in the same order).
 int causal_wide_chunks(long long slices, int tiles) {
     long long k = kPlanSMs / (slices > 0 ? slices : 1);
     k = k < 1 ? 1 : (k > 4 ? 4 : k);
