@@ -37,6 +37,7 @@
 #include "common.cuh"
 #include "ptx.cuh"
 #include "rowops.cuh"
+#include "tmem_pair.cuh"
 
 #include <math.h>
 
@@ -130,18 +131,6 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limi
         }
     }
     return true;
-}
-
-// two TMEM columns of this warp's 32 lanes from / to two registers of each lane
-__device__ __forceinline__ void tmem_st2(uint32_t taddr, float a, float b) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(__float_as_uint(a)),
-                 "r"(__float_as_uint(b))
-                 : "memory");
-}
-__device__ __forceinline__ float2 tmem_ld2(uint32_t taddr) {
-    uint32_t x, y;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(taddr));
-    return make_float2(__uint_as_float(x), __uint_as_float(y));
 }
 
 // the two TMA boxes (64 columns each) of a [128][128] bf16 tile

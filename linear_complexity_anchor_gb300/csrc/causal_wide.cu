@@ -26,15 +26,17 @@
 // goes over B_t (every MMA reading B_t has completed by then).  Shared memory (D = 128): Q, V,
 // U, L, A, B / P, W_pre image, 32 KB each.  Tensor memory: S / C at 0, P at 128, H at 256,
 // W_pre at 384.
-// Warps: 0-3 row warps (TMEM lanes 32w..32w+31: tokens, or anchors for the W_pre image; a
-// tile's H goes out while the next tile's C runs, staged in the warp's own rows of the B / P
-// tile and written by TMA stores), 4 producer (TMA), 5 MMA issuer.  Sums run
+// Warps: 0-7 row warps (warp w: TMEM lanes 32 (w % 4) .. + 31, tokens or anchors for the
+// W_pre image; half w / 4 of the columns, the softmax's (max, sum) pairs exchanged through
+// tensor memory; a tile's H goes out while the next tile's C runs, staged in the warp's own
+// rows of the B / P tile and written by TMA stores), 8 producer (TMA), 9 MMA issuer.  Sums run
 // in a fixed order: results are bit-identical from run to run.  Every wait is bounded; one
 // that gives up sets bit 0 of this kernel's error word and the CTA drains what it has in
 // flight and leaves.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "rowops.cuh"
+#include "tmem_pair.cuh"
 
 #include <math.h>
 
@@ -47,8 +49,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 128, kMP = 128;
-constexpr int kThreads = 192;
-constexpr int kWarpProducer = 4, kWarpMma = 5;
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8, kWarpMma = 9;  // warps 0-7: row warps
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBlkB = kT * 64 * 2;  // a [128][64] bf16 block (16 KB)
 constexpr uint32_t kColSC = 0, kColP = 128, kColH = 256, kColW = 384;
@@ -136,6 +138,7 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     uint64_t *u_full = bars + 4, *s_full = bars + 5, *a_full = bars + 6, *c_full = bars + 7, *b_full = bars + 8;
     uint64_t *p_full = bars + 9, *pm_full = bars + 10, *h_full = bars + 11, *h_empty = bars + 12;
     uint64_t *w_full = bars + 13, *wi_full = bars + 14, *mma_done = bars + 15, *dp_full = bars + 16;
+    uint64_t *x_sm = bars + 17;  // the two halves' (max, sum) pairs written
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + LY::kBars);
     float *sDP = reinterpret_cast<float *>(sm + LY::kOffDP);
 
@@ -155,17 +158,18 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         mbar_init(v_empty, 1);
         mbar_init(u_full, 1);
         mbar_init(s_full, 1);
-        mbar_init(a_full, 4);
+        mbar_init(a_full, 8);
         mbar_init(c_full, 1);
-        mbar_init(b_full, 4);
+        mbar_init(b_full, 8);
         mbar_init(p_full, 1);
-        mbar_init(pm_full, 4);
+        mbar_init(pm_full, 8);
         mbar_init(h_full, 1);
-        mbar_init(h_empty, 4);
+        mbar_init(h_empty, 8);
         mbar_init(w_full, 1);
-        mbar_init(wi_full, 4);
+        mbar_init(wi_full, 8);
         mbar_init(mma_done, 1);
-        mbar_init(dp_full, 4);
+        mbar_init(dp_full, 8);
+        mbar_init(x_sm, 8);
         fence_mbar_init();
     }
     if (warp < 4) {  // row warps: L[i][j] = 1 for j <= i (row i = this thread), Delta_pre = 0
@@ -315,27 +319,37 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ row warps
-        const int row = warp * 32 + lane;
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        // warp w: TMEM lanes 32 (w % 4) .. + 31 (tokens; anchors for the W_pre image), column
+        // half g = w / 4 (anchors 64 g .. 64 g + 63 of S, C and B; tokens 64 g .. of P; the
+        // columns D/2 g .. of H and of the W_pre image)
+        const int q4 = warp & 3, g = warp >> 2;
+        const int row = q4 * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        constexpr int DH = D / 2;  // this half's columns of H and of the W_pre image
         bool ok = true;
-        float a[kMP];
+        float a[64];
         // H of full tile u (slice tile t0 + u): tensor memory -> this warp's own rows of the
         // B / P tile (free: the tile's H products have read P; the same swizzled layout as a
-        // [32][64] TMA box) -> TMA stores (rows past the slice are not written).  The warp's
-        // next B rows are written once the stores have read them.
+        // [32][64] TMA box) -> a TMA store (rows past the slice are not written).  At D = 128
+        // each half stores its 64 columns; at D = 64 half 0 stores all of them.  The warp's
+        // next B rows are written once its stores have read them.
         const uint64_t pol_out = policy_evict_first();
         auto store_h = [&](int u) -> bool {
             if (!bwait(h_full, (uint32_t)(u & 1), p.wait_ns)) return false;
             tc_fence_after();
+            const bool mine = D == 128 || g == 0;
+            if (mine) {
+                const int c0 = D == 128 ? 64 * g : 0;  // this warp's 64 columns of H
+                uint8_t *box = sm + LY::kOffB + g * kBlkB + q4 * 4096;
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                float o[32];
-                tmem_ld32(trow + kColH + q * 32, o);
-                tmem_ld_wait();
-                uint8_t *box = sm + LY::kOffB + (q >> 1) * kBlkB + warp * 4096;
+                for (int q = 0; q < 2; ++q) {
+                    float o[32];
+                    tmem_ld32(trow + kColH + c0 + q * 32, o);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(box + sw_off(lane, (q & 1) * 4 + c, 32)) = pack8(o + 8 * c);
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(box + sw_off(lane, q * 4 + c, 32)) = pack8(o + 8 * c);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -343,11 +357,11 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(h_empty);
-#pragma unroll
-                for (int k = 0; k < D / 64; ++k)
-                    tma_store_3d(&th, sm + LY::kOffB + k * kBlkB + warp * 4096, 64 * k, (t0 + u) * kT + warp * 32,
-                                 slice, pol_out);
-                bulk_commit_group();
+                if (mine) {
+                    tma_store_3d(&th, sm + LY::kOffB + g * kBlkB + q4 * 4096, D == 128 ? 64 * g : 0,
+                                 (t0 + u) * kT + q4 * 32, slice, pol_out);
+                    bulk_commit_group();
+                }
             }
             return true;
         };
@@ -360,15 +374,51 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             const bool valid = t * kT + row < p.n;
             const bool full = t >= t0;
             const int u = t - t0;  // full tile index
-            // A_t (fp32, in registers)
+            // A_t (fp32, in registers): this half's maximum, exponentials and sum; the halves'
+            // (max, sum) pairs exchanged through the last two of each half's own S columns (C_t
+            // goes there only once every row warp has passed a_full); both halves scaled to the
+            // row's maximum M: A_j = e_j 2^(m_g - M) / (z_0 2^(m_0 - M) + z_1 2^(m_1 - M))
             if (!bwait(s_full, ph, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int q = 0; q < kMP / 32; ++q) tmem_ld32(trow + kColSC + q * 32, a + q * 32);
-            tmem_ld_wait();
             {
-                const float z = rowops::softmax_unnormalised<kMP>(a, p.m, p.c);
-                rowops::scale_row<kMP>(a, valid ? 1.f / z : 0.f);
+                tmem_ld32(trow + kColSC + 64 * g, a);
+                tmem_ld32(trow + kColSC + 64 * g + 32, a + 32);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 64; ++j) a[j] = 64 * g + j < p.m ? a[j] * p.c : -INFINITY;
+                float m8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = a[k];
+#pragma unroll
+                for (int j = 8; j < 64; j += 8)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], a[j + k]);
+                const float mg = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                const float ms = mg == -INFINITY ? 0.f : mg;  // a half with every anchor masked
+                float z4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    a[j] = rowops::ex2_approx(a[j] - ms);
+                    z4[j & 3] += a[j];
+                }
+                const float2 mine = make_float2(mg, (z4[0] + z4[1]) + (z4[2] + z4[3]));
+                tmem_st2(trow + kColSC + 64 * g + 62, mine.x, mine.y);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_sm);
+                if (!bwait(x_sm, ph, p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+                const float2 other = tmem_ld2(trow + kColSC + 64 * (1 - g) + 62);
+                tmem_ld_wait();
+                const float2 h0 = g == 0 ? mine : other, h1 = g == 0 ? other : mine;
+                const float M = fmaxf(h0.x, h1.x);  // finite: half 0 holds anchor 0
+                const float f0 = h0.x == -INFINITY ? 0.f : rowops::ex2_approx(h0.x - M);
+                const float f1 = h1.x == -INFINITY ? 0.f : rowops::ex2_approx(h1.x - M);
+                const float r = valid ? (g == 0 ? f0 : f1) / (h0.y * f0 + h1.y * f1) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) a[j] *= r;
             }
             // the tile before has finished with A, B, P and has added itself to W_pre
             if (t >= 1) {
@@ -376,29 +426,29 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 tc_fence_after();
             }
 #pragma unroll
-            for (int c8 = 0; c8 < kMP / 8; ++c8)
-                *reinterpret_cast<uint4 *>(sm + LY::kOffA + sw_off(row, c8, kT)) = pack8(a + 8 * c8);
+            for (int c8 = 0; c8 < 8; ++c8)
+                *reinterpret_cast<uint4 *>(sm + LY::kOffA + sw_off(row, 8 * g + c8, kT)) = pack8(a + 8 * c8);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full);
             if (!full) {
                 // a summary tile: Delta_pre += the tile's column sums (the last row of C_t, in
-                // the P columns), by the last row's warp (tensor-memory loads are warp-wide);
+                // the P columns), by the last rows' warps (tensor-memory loads are warp-wide);
                 // the other warps go on to the next tile
-                if (warp == (kT - 1) / 32) {
+                if (q4 == (kT - 1) / 32) {
                     if (!bwait(c_full, ph, p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
-                    const float *dp = sDP + (t & 1) * kMP;
+                    const float *dp = sDP + (t & 1) * kMP + 64 * g;
 #pragma unroll
-                    for (int q = 0; q < kMP / 32; ++q) {
+                    for (int q = 0; q < 2; ++q) {
                         float cr[32];
-                        tmem_ld32(trow + kColP + q * 32, cr);
+                        tmem_ld32(trow + kColP + 64 * g + q * 32, cr);
                         tmem_ld_wait();
                         if (row == kT - 1)
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
-                                sDP[((t + 1) & 1) * kMP + q * 32 + j] = __fadd_rn(dp[q * 32 + j], cr[j]);
+                                sDP[((t + 1) & 1) * kMP + 64 * g + q * 32 + j] = __fadd_rn(dp[q * 32 + j], cr[j]);
                     }
                     tc_fence_before();
                 }
@@ -409,17 +459,19 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 }
                 continue;
             }
-            // while C_t runs: the tile before's H out, and the W_pre image for this tile (anchor rows)
+            // while C_t runs: the tile before's H out, and this half of the W_pre image for
+            // this tile (anchor rows)
             if (t >= 1) {
                 if (u >= 1 && !store_h(u - 1)) { ok = false; break; }
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
+                for (int q = 0; q < DH / 32; ++q) {
                     float w[32];
-                    tmem_ld32(trow + kColW + q * 32, w);
+                    tmem_ld32(trow + kColW + DH * g + q * 32, w);
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(sm + LY::kOffWI + sw_off(row, q * 4 + c, kMP)) = pack8(w + 8 * c);
+                        *reinterpret_cast<uint4 *>(sm + LY::kOffWI + sw_off(row, (DH * g) / 8 + q * 4 + c, kMP)) =
+                            pack8(w + 8 * c);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -433,11 +485,11 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             if (!bwait(c_full, ph, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             {
-                const float *dp = sDP + (t & 1) * kMP;
+                const float *dp = sDP + (t & 1) * kMP + 64 * g;
 #pragma unroll
-                for (int q = 0; q < kMP / 32; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     float cr[32];
-                    tmem_ld32(trow + kColSC + q * 32, cr);
+                    tmem_ld32(trow + kColSC + 64 * g + q * 32, cr);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -446,12 +498,12 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                     }
                     if (row == kT - 1)  // the whole tile: the next tile's Delta_pre
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sDP[((t + 1) & 1) * kMP + q * 32 + j] = cr[j];
+                        for (int j = 0; j < 32; ++j) sDP[((t + 1) & 1) * kMP + 64 * g + q * 32 + j] = cr[j];
                 }
             }
 #pragma unroll
-            for (int c8 = 0; c8 < kMP / 8; ++c8)
-                *reinterpret_cast<uint4 *>(sm + LY::kOffB + sw_off(row, c8, kT)) = pack8(a + 8 * c8);
+            for (int c8 = 0; c8 < 8; ++c8)
+                *reinterpret_cast<uint4 *>(sm + LY::kOffB + sw_off(row, 8 * g + c8, kT)) = pack8(a + 8 * c8);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -461,20 +513,20 @@ anchor_causal_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             }
             // every row warp has read this tile's Delta_pre, and the next tile's is written
             if (!bwait(dp_full, ph, p.wait_ns)) { ok = false; break; }
-            // P_t masked to j <= i, over B_t, as the A operand of P V
+            // P_t masked to j <= i, over B_t, as the A operand of P V (this half: tokens 64 g ..)
             if (!bwait(p_full, (uint32_t)(u & 1), p.wait_ns)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
-            for (int q = 0; q < kT / 32; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float pr[32];
-                tmem_ld32(trow + kColP + q * 32, pr);
+                tmem_ld32(trow + kColP + 64 * g + q * 32, pr);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (q * 32 + j > row) pr[j] = 0.f;
+                    if (64 * g + q * 32 + j > row) pr[j] = 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(sm + LY::kOffB + sw_off(row, q * 4 + c, kT)) = pack8(pr + 8 * c);
+                    *reinterpret_cast<uint4 *>(sm + LY::kOffB + sw_off(row, 8 * g + q * 4 + c, kT)) = pack8(pr + 8 * c);
             }
             fence_proxy_async_smem();
             tc_fence_before();
