@@ -9,31 +9,35 @@
 //
 // At d = m = 128 one CTA cannot hold a slice's whole backward (the four W', dW images alone
 // take 128 KB of shared memory, and the accumulators S, G, dQ, dV and dU 640 tensor-memory
-// columns), so the work runs as three kernels over items (a slice's run of consecutive
-// 128-token tiles; the chunking depends on the shape alone, so the sums and the bits do too):
+// columns), so the work runs as four launches over items (a slice's run of consecutive 128-token
+// tiles; the chunking depends on the shape alone, so the sums and the bits do too):
 //   pass 1   S_t = Q_t U^T, A_t = softmax; W += A_t^T V_t, then [dW' | Delta] +=
-//            A_t^T [dH_t | 1] (one N = 144 product), with A as hi + lo bf16 parts (Q, V, dH in buffers of their own,
-//            each refilled as soon as its products are done); the item's W, dW', Delta go to
-//            a workspace row block
+//            A_t^T [dH_t | 1] (one N = 144 product), with A as hi + lo bf16 parts released
+//            one after the other; Q, V, dH in buffers of their own, each refilled by its own
+//            producer warp as soon as its products are done; the item's W, dW', Delta go to a
+//            workspace row block
 //   reduce   per slice: the items' blocks summed in order; W' = W / Delta, dW = dW' / Delta
 //            as hi + lo bf16 images [4][128][128], and dDelta (fp32)
-//   pass 2   S_t and A_t again; G_t = dH_t (W'_hi + W'_lo)^T + V_t (dW_hi + dW_lo)^T with the
-//            images streamed through a two-slot ring (from L2: every item of a slice reads
-//            the same 128 KB); dS_t on CUDA cores in fp32; dV_t = A_t dW, dQ_t = dS_t U,
-//            dU += dS_t^T Q_t; the item's dU to a workspace block, summed per head by the
-//            backward's dU kernel in (batch entry, item) order
+//   pass 2   S_t again and e = 2^(c s - M) (A = e / z); G_t = dH_t (W'_hi + W'_lo)^T +
+//            V_t (dW_hi + dW_lo)^T with the images streamed through a two-slot ring (from L2:
+//            every item of a slice reads the same 128 KB); dS_t on CUDA cores in fp32;
+//            dV_t = e dW (scaled by 1/z on the way out), dU += dS_t^T Q_t, dQ_t = dS_hi U;
+//            the item's dU to a workspace block
+//   dU sum   per head, the items' blocks in (batch entry, item) order (the backward's dU
+//            kernel)
 // The fp32 operands that the gradients sum over many terms - A in pass 1, W' and dW in G, dS
-// in dQ and dU - enter the MMAs as two bf16 parts, hi = bf16(x) and lo = bf16(x - hi): with
-// any one of them rounded once to bf16, dU of the 16384-token workload (four batch entries)
-// comes out at 0.8 to 1.1 of the bf16 tolerance in a float64 emulation; with all of them split
-// at 0.003.
-// Pass 2's shared memory (U | two Q buffers | V or dS_hi | dH or dS_lo | image ring) fills
-// 224 KB: dS_t is written over V_t and dH_t once G_t is done, and A_t (bf16) over S_t in
-// tensor memory, where dV_t reads it.  Tensor memory (512 columns): S then A | G then dQ | dV |
-// dU.
-// Warps: 0-3 row warps (TMEM lanes 32w..32w+31: tokens, or anchors for the item's sums),
-// 4 producer (TMA), 5 MMA issuer.  Every wait is bounded; one that gives up sets bit 0 of the
-// error word and the CTA drains what it has in flight and leaves.
+// in dU - enter the MMAs as two bf16 parts, hi = bf16(x) and lo = bf16(x - hi): with any one of
+// them rounded once to bf16, dU of the 16384-token workload (four batch entries) comes out at
+// 0.8 to 1.1 of the bf16 tolerance in a float64 emulation; with all of them split at 0.003
+// (dQ, a sum over the m anchors only, stays at 0.06 with dS_hi alone).
+// Pass 2's shared memory (U | Q | dQ, dV staging | V or dS_hi | dH or dS_lo | image ring) fills
+// 224 KB: dS_t is written over V_t and dH_t once G_t is done, and e (bf16) over S_t in tensor
+// memory, where dV_t reads it.  Tensor memory (512 columns): S then e | G then dQ | dV | dU.
+// Warps: row warps 0-7 (warp w: TMEM lanes 32 (w % 4) .. + 31, tokens or anchors for the
+// item's sums; half w / 4 of the columns, the halves' row sums exchanged through shared or
+// tensor memory), then the producer warps and the MMA warp (see kP1Issue, kP2Issue).  Every
+// wait is bounded; one that gives up sets bit 0 of the error word and the CTA drains what it
+// has in flight and leaves.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "rowops.cuh"
