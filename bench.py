@@ -447,9 +447,9 @@ def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dic
     forward (CUDA events on the launching stream, W untimed calls first).  Algorithmic work per
     slice: 18 n m d flops (three contractions to recompute A and the summaries, six in the
     gradient pass) and 5 n d elements of traffic (Q, V, dH read, dQ and dV written; U read and
-    dU written once per head).  bf16 with d = 64 and m <= 64, or d = 128 and m <= 128, runs on
-    the tensor cores (roofline: the measured bf16 peak, and HBM), the rest on CUDA cores
-    (roofline: the fp32 FMA peak)."""
+    dU written once per head).  bf16 with d = 64 or 128 and m <= 128 runs on the tensor cores
+    (roofline: the measured bf16 peak, and HBM), the rest on CUDA cores (roofline: the fp32 FMA
+    peak)."""
     import torch
     hQ, hU, hV = hQUV
     check_shapes(w, hQ, hU, hV)
@@ -476,9 +476,12 @@ def time_backward(pkg, w: gen.Workload, hQUV: tuple, K: int, W: int, dev) -> dic
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fma_peak = sms * FMA_LANES_PER_SM * 2 * 2070e6 / 1e12
     peak, peak_src = peaks()
-    tensor = w.dtype == "bf16" and ((w.d == 64 and w.m <= 64) or (w.d == 128 and w.m <= 128))
+    tensor = w.dtype == "bf16" and w.d in (64, 128) and w.m <= 128
+    # the library's choice: four launches (two passes, the reduce, the dU sum) at d = 128 and at
+    # d = 64 with m > 64; two (one CTA per slice, the dU sum) at d = 64 with m <= 64
+    wide = tensor and (w.d == 128 or w.m > 64)
     rec = {"ms_per_call": call_ms, "value": w.slices * w.n / (call_ms / 1e3), "unit": UNIT, "steps": K,
-           "kernels_per_call": 4 if tensor and w.d == 128 else 2, "device_error": derr, "path": "tensor" if tensor else "cuda_core",
+           "kernels_per_call": 4 if wide else 2, "device_error": derr, "path": "tensor" if tensor else "cuda_core",
            "hbm": {"achieved": hbm / (call_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                    "frac": hbm / (call_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_call": hbm,
                    "peak_source": f"{peak_src} hbm_gbs"}}

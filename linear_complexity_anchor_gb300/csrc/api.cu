@@ -304,8 +304,8 @@ anchor_attn_status_t backward(const anchor::BwdProblem &p, void *stream_v) {
         for (int o2 = 0; o2 < o; ++o2)
             if (anchor::overlaps(out[o], out_bytes[o], out[o2], out_bytes[o2])) return ANCHOR_ATTN_ERR_ALIAS;
     }
-    const bool tc = anchor::bwd_tc_supported(p);
-    const bool wide = !tc && anchor::bwd_wide_supported(p);
+    const bool wide = anchor::bwd_wide_preferred(p);
+    const bool tc = !wide && anchor::bwd_tc_supported(p);
     if (!tc && !wide && !anchor::bwd_fits(p)) return ANCHOR_ATTN_ERR_UNSUPPORTED;
     void *ws = nullptr;
     if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;

@@ -53,44 +53,50 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kT = 128, kD = 128, kMP = 128;
+constexpr int kT = 128, kMP = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBlkB = kT * 128;   // one 64-column block of a 128-row bf16 tile (16 KB)
-constexpr int kTileB = 2 * kBlkB; // a [128][128] bf16 tile (32 KB)
-constexpr int kPartF = kMP * 2 * kD + kMP;  // an item's pass-1 block: [W | dW'] rows, then Delta
-
-// pass 1: U | Q | V | dH | ones [128][64] (dH's third 64-column block: [dH | 1] is one N = 144
-// operand) | A_hi | A_lo | row-sum exchange [2][128] | barriers
-constexpr int k1U = 0, k1Q = k1U + kTileB, k1VH = k1Q + kTileB, k1Ones = k1VH + 2 * kTileB;
-constexpr int k1AH = k1Ones + kBlkB, k1AL = k1AH + kTileB, k1Ex = k1AL + kTileB, k1Bar = k1Ex + 2 * kT * 8;
-constexpr int k1Bars = 15;
-constexpr int k1Smem = k1Bar + k1Bars * 8 + 16 + 1024;
-static_assert(k1Smem <= 227 * 1024, "pass 1 shared memory");
-constexpr uint32_t k1ColS = 0, k1ColWD = 128, k1ColDelta = 384;
+constexpr int kAB = kT * kMP * 2; // a [128 tokens][128 anchors] bf16 tile (A, dS: 32 KB)
+constexpr int kStageB = 8 * 4096; // pass 2's dQ / dV staging: 4 KB per row warp
+constexpr int k1Bars = 15, k2Bars = 27;
 // row warps 0-7 in both passes (two per TMEM lane quarter, one per half of the columns), then
 // producer warps (one per input in pass 1: Q, V, dH; in pass 2 one for Q, dH, V and one for the
 // image ring: a lane that sleeps in an mbarrier wait holds up its whole warp), then the MMA warp
 constexpr int kRowWarps = 8, kWarpProd = kRowWarps;
 constexpr int kP1Threads = 32 * (kRowWarps + 4), kP1Issue = kRowWarps + 3;
 constexpr int kP2Threads = 32 * (kRowWarps + 3), kP2Issue = kRowWarps + 2;
-
-// pass 2: U | Q | dQ, dV staging (4 KB per row warp) | V dH, then dS_hi dS_lo | image ring
-// (2 x 32 KB) | dDelta | barriers
-constexpr int k2U = 0, k2X = k2U + kTileB, k2Stage = k2X + kTileB, k2VH = k2X + 2 * kTileB, k2Img = k2VH + 2 * kTileB;
-constexpr int k2DD = k2Img + 2 * kTileB, k2Bar = k2DD + kMP * 4;
-constexpr int k2Bars = 27;
-constexpr int k2Smem = k2Bar + k2Bars * 8 + 16 + 1024;
-static_assert(k2Smem <= 227 * 1024, "pass 2 shared memory");
+constexpr uint32_t k1ColS = 0, k1ColWD = 128;
 constexpr uint32_t k2ColS = 0, k2ColG = 128, k2ColDV = 256, k2ColDU = 384;  // dQ_t reuses G's columns
 
+// Sizes and shared-memory layouts for head dimension D (64 or 128).
+template <int D>
+struct Geo {
+    static constexpr int kNB = D / 64;               // 64-column blocks of a [rows][D] tile
+    static constexpr int kQB = kT * D * 2;           // a [128 tokens][D] bf16 tile (Q, V, dH)
+    static constexpr int kUB = kMP * D * 2;          // a [128 anchors][D] bf16 tile (U, an image)
+    static constexpr int kPartF = kMP * 2 * D + kMP; // an item's pass-1 block: [W | dW'] rows, then Delta
+    static constexpr uint32_t k1ColDelta = k1ColWD + 2 * D;
+    // pass 1: U | Q | V | dH | ones [128][64] (dH's block after its last: [dH | 1] is one
+    // N = D + 16 operand) | A_hi | A_lo | row-sum exchange [2][128] | barriers
+    static constexpr int k1U = 0, k1Q = k1U + kUB, k1V = k1Q + kQB, k1H = k1V + kQB, k1Ones = k1H + kQB;
+    static constexpr int k1AH = k1Ones + kBlkB, k1AL = k1AH + kAB, k1Ex = k1AL + kAB, k1Bar = k1Ex + 2 * kT * 8;
+    static constexpr int k1Smem = k1Bar + k1Bars * 8 + 16 + 1024;
+    // pass 2: U | Q | dQ, dV staging | V or dS_hi | dH or dS_lo | image ring (2 slots) | dDelta |
+    // barriers (V and dH each sit at the start of a 32 KB dS tile)
+    static constexpr int k2U = 0, k2X = k2U + kUB, k2Stage = k2X + kQB, k2VH = k2Stage + kStageB;
+    static constexpr int k2Img = k2VH + 2 * kAB, k2DD = k2Img + 2 * kUB, k2Bar = k2DD + kMP * 4;
+    static constexpr int k2Smem = k2Bar + k2Bars * 8 + 16 + 1024;
+    static_assert(k1Smem <= 227 * 1024 && k2Smem <= 227 * 1024, "shared memory");
+    static_assert(k1ColWD + 2 * D + 16 <= kTmemCols, "tensor memory");
+};
 
 struct BwParams {
     int heads, n, m, tiles, chunks;
     float c;      // scale * log2(e)
     float scale;
-    float *part;           // pass 1: [slices * chunks][kPartF]
+    float *part;           // pass 1: [slices * chunks][kPartF of D]
     const float *ddelta;   // pass 2: [slices][kMP]
-    float *dupart;         // pass 2: [slices][chunks][m][kD]
+    float *dupart;         // pass 2: [slices][chunks][m][D]
     __nv_bfloat16 *dQ, *dV;
     uint64_t wait_ns;
 };
@@ -137,19 +143,21 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t par, uint64_t limi
     return true;
 }
 
-// the two TMA boxes (64 columns each) of a [128][128] bf16 tile
+// the TMA boxes (64 columns each) of a [128][64 NB] bf16 tile
+template <int NB>
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int row, int outer,
                                           uint64_t pol) {
-    tma_load_3d(dst, map, bar, 0, row, outer, pol);
-    tma_load_3d(dst + kBlkB, map, bar, 64, row, outer, pol);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) tma_load_3d(dst + b * kBlkB, map, bar, 64 * b, row, outer, pol);
 }
 
-// an L2 prefetch of the two boxes of a [128][128] bf16 tile (no shared memory, no completion):
+// an L2 prefetch of the boxes of a [128][64 NB] bf16 tile (no shared memory, no completion):
 // the kernels keep one tile of each input in shared memory, so the load of the next one is
 // issued late and would otherwise wait out the full memory latency
+template <int NB>
 __device__ __forceinline__ void prefetch_tile(const CUtensorMap *map, int row, int outer) {
 #pragma unroll
-    for (int c0 = 0; c0 < 128; c0 += 64)
+    for (int c0 = 0; c0 < 64 * NB; c0 += 64)
         asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                          reinterpret_cast<uint64_t>(map)),
                      "r"(c0), "r"(row), "r"(outer)
@@ -170,18 +178,20 @@ __device__ __forceinline__ Item item_of(int b, int tiles, int chunks) {
 }
 
 // ------------------------------------------------------------------------------ pass 1
+template <int D>
 __global__ void __launch_bounds__(kP1Threads, 1)
 anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ CUtensorMap tdh, const __grid_constant__ CUtensorMap tu,
                           const BwParams p) {
+    using GE = Geo<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k1Bar);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + GE::k1Bar);
     uint64_t *u_full = bars + 0, *q_full = bars + 1, *q_empty = bars + 2, *v_full = bars + 3, *v_empty = bars + 4;
     uint64_t *h_full = bars + 5, *h_empty = bars + 6, *s_full = bars + 7, *a_full = bars + 8, *a_empty = bars + 9;
     uint64_t *acc_full = bars + 10, *mma_done = bars + 11, *x_ex = bars + 12, *al_full = bars + 13,
              *al_empty = bars + 14;  // a_full / a_empty: A_hi's
-    float2 *s_mz = reinterpret_cast<float2 *>(sm + k1Ex);  // [2][128]: each column half's (max, sum)
+    float2 *s_mz = reinterpret_cast<float2 *>(sm + GE::k1Ex);  // [2][128]: each column half's (max, sum)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k1Bars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Item it = item_of(blockIdx.x, p.tiles, p.chunks);
@@ -223,22 +233,22 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             const CUtensorMap *map = w == 0 ? &tq : (w == 1 ? &tv : &tdh);
             uint64_t *full = w == 0 ? q_full : (w == 1 ? v_full : h_full);
             uint64_t *empty = w == 0 ? q_empty : (w == 1 ? v_empty : h_empty);
-            uint8_t *dst = sm + (w == 0 ? k1Q : (w == 1 ? k1VH : k1VH + kTileB));
+            uint8_t *dst = sm + (w == 0 ? GE::k1Q : (w == 1 ? GE::k1V : GE::k1H));
             tma_prefetch_desc(map);
             if (w == 0) {
                 tma_prefetch_desc(&tu);
-                mbar_arrive_expect_tx(u_full, kTileB);
-                load_tile(sm + k1U, &tu, u_full, 0, h, pol_keep);
+                mbar_arrive_expect_tx(u_full, GE::kUB);
+                load_tile<GE::kNB>(sm + GE::k1U, &tu, u_full, 0, h, pol_keep);
             }
             int n = 0;
             for (int i = 0; i < it.nt; ++i) {
                 const int row = (it.t0 + i) * kT;
                 // this input's tiles two ahead (and, at the start, the next) into L2
                 for (int k = i == 0 ? 1 : 2; k <= 2; ++k)
-                    if (i + k < it.nt) prefetch_tile(map, row + k * kT, it.slice);
+                    if (i + k < it.nt) prefetch_tile<GE::kNB>(map, row + k * kT, it.slice);
                 if (i >= 1 && !bwait(empty, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(full, kTileB);
-                load_tile(dst, map, full, row, it.slice, pol_keep);
+                mbar_arrive_expect_tx(full, GE::kQB);
+                load_tile<GE::kNB>(dst, map, full, row, it.slice, pol_keep);
                 ++n;
             }
             // the CTA leaves only once its copies have landed
@@ -249,18 +259,18 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     } else if (warp == kP1Issue) {
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);       // [tokens x anchors], K = d
-            const uint32_t idW = idesc_bf16_f32(kMP, kD, true, true);          // A^T V, K = tokens
-            const uint32_t idWD = idesc_bf16_f32(kMP, kD + 16, true, true);    // A^T [dH | 1]
-            const uint64_t udesc = smem_desc_sw128(sbase + k1U, 16, 1024);
-            const uint64_t qdesc = smem_desc_sw128(sbase + k1Q, 16, 1024);
-            const uint64_t vdesc = smem_desc_sw128(sbase + k1VH, kBlkB, 1024);
-            const uint64_t hdesc = smem_desc_sw128(sbase + k1VH + kTileB, kBlkB, 1024);  // dH | ones
+            const uint32_t idW = idesc_bf16_f32(kMP, D, true, true);          // A^T V, K = tokens
+            const uint32_t idWD = idesc_bf16_f32(kMP, D + 16, true, true);    // A^T [dH | 1]
+            const uint64_t udesc = smem_desc_sw128(sbase + GE::k1U, 16, 1024);
+            const uint64_t qdesc = smem_desc_sw128(sbase + GE::k1Q, 16, 1024);
+            const uint64_t vdesc = smem_desc_sw128(sbase + GE::k1V, kBlkB, 1024);
+            const uint64_t hdesc = smem_desc_sw128(sbase + GE::k1H, kBlkB, 1024);  // dH | ones
             bool ok = bwait(u_full, 0u, p.wait_ns);
             auto issue_s = [&](int i) -> bool {
                 if (!bwait(q_full, (uint32_t)(i & 1), p.wait_ns)) return false;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
+                for (int kk = 0; kk < D / 16; ++kk)
                     umma_bf16(tmem + k1ColS, qdesc + kstep(kk), udesc + kstep(kk), idS, kk > 0 ? 1u : 0u);
                 umma_commit(s_full);
                 umma_commit(q_empty);
@@ -273,8 +283,8 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 if (i + 1 < it.nt && !issue_s(i + 1)) { ok = false; break; }
                 // W += A_hi^T V + A_lo^T V (then V's buffer is refilled), [dW' | Delta] +=
                 // A_hi^T [dH | 1] (then A_hi's buffer takes the next tile's) + A_lo^T [dH | 1]
-                const uint64_t ahd = smem_desc_sw128(sbase + k1AH, kBlkB, 1024);  // A^T, MN-major
-                const uint64_t ald = smem_desc_sw128(sbase + k1AL, kBlkB, 1024);
+                const uint64_t ahd = smem_desc_sw128(sbase + GE::k1AH, kBlkB, 1024);  // A^T, MN-major
+                const uint64_t ald = smem_desc_sw128(sbase + GE::k1AL, kBlkB, 1024);
                 if (!bwait(v_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
@@ -291,12 +301,12 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 tc_fence_after();
 #pragma unroll
                 for (int kt = 0; kt < kT / 16; ++kt)
-                    umma_bf16(tmem + k1ColWD + kD, ahd + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idWD,
+                    umma_bf16(tmem + k1ColWD + D, ahd + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idWD,
                               (i > 0 || kt > 0) ? 1u : 0u);
                 umma_commit(a_empty);
 #pragma unroll
                 for (int kt = 0; kt < kT / 16; ++kt)
-                    umma_bf16(tmem + k1ColWD + kD, ald + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idWD, 1u);
+                    umma_bf16(tmem + k1ColWD + D, ald + (uint64_t)(kt * 128), hdesc + (uint64_t)(kt * 128), idWD, 1u);
                 umma_commit(al_empty);
                 umma_commit(h_empty);
             }
@@ -313,7 +323,7 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         {   // the ones block (every element 1; the MMA reads its first 16 columns)
             const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-            for (int i = warp * 32 + lane; i < kBlkB / 16; i += 32 * kRowWarps) reinterpret_cast<uint4 *>(sm + k1Ones)[i] = ones;
+            for (int i = warp * 32 + lane; i < kBlkB / 16; i += 32 * kRowWarps) reinterpret_cast<uint4 *>(sm + GE::k1Ones)[i] = ones;
         }
         bool ok = true;
         float e[64];
@@ -364,14 +374,14 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             // A_hi once the previous tile's products have read it, then A_lo likewise
             if (i >= 1 && !bwait(a_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(sm + k1AH + sw_off(row, 8 * g + c, kT)) = hi[c];
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(sm + GE::k1AH + sw_off(row, 8 * g + c, kT)) = hi[c];
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full);
             if (i >= 1 && !bwait(al_empty, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(sm + k1AL + sw_off(row, 8 * g + c, kT)) = lo[c];
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(sm + GE::k1AL + sw_off(row, 8 * g + c, kT)) = lo[c];
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(al_full);
@@ -380,20 +390,20 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         ok = ok && it.nt > 0 && bwait(acc_full, 0u, p.wait_ns);
         if (ok) {
             tc_fence_after();
-            float *dst = p.part + (size_t)blockIdx.x * kPartF;
+            float *dst = p.part + (size_t)blockIdx.x * GE::kPartF;
             float o[32];
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                tmem_ld32(trow + k1ColWD + 128 * g + 32 * q, o);
+            for (int q = 0; q < D / 32; ++q) {
+                tmem_ld32(trow + k1ColWD + D * g + 32 * q, o);
                 tmem_ld_wait();
-                float4 *d4 = reinterpret_cast<float4 *>(dst + (size_t)row * 2 * kD + 128 * g + 32 * q);
+                float4 *d4 = reinterpret_cast<float4 *>(dst + (size_t)row * 2 * D + D * g + 32 * q);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) d4[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
             }
             if (g == 0) {
-                tmem_ld32(trow + k1ColDelta, o);
+                tmem_ld32(trow + GE::k1ColDelta, o);
                 tmem_ld_wait();
-                dst[kMP * 2 * kD + row] = o[0];
+                dst[kMP * 2 * D + row] = o[0];
             }
             tc_fence_before();
         }
@@ -407,15 +417,17 @@ anchor_bwd_wide_p1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
 }
 
 // ------------------------------------------------------------------------------ reduce
-// Per slice and run of kRJ anchors (one CTA; thread k = column k): W, dW' and Delta summed over
+// Per slice and run of kRJ anchors (one CTA of D threads; thread k = column k): W, dW' and Delta summed over
 // the slice's items in item order; W' = W / Delta and dW = dW' / Delta as hi + lo bf16 images
 // (rows >= m and anchors with Delta = 0 are zero), dDelta_j = -sum_k dW_jk W'_jk in fp32 (a
-// fixed warp tree, then the four warps in order).
+// fixed warp tree, then the warps in order).
 constexpr int kRJ = 8;
-__global__ void __launch_bounds__(kD)
+template <int D>
+__global__ void __launch_bounds__(D)
 anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m, __nv_bfloat16 *__restrict__ img,
                               float *__restrict__ ddelta) {
-    __shared__ float s_red[kD / 32][kRJ];
+    constexpr int kPartF = Geo<D>::kPartF;
+    __shared__ float s_red[D / 32][kRJ];
     __shared__ float s_rinv[kRJ];
     grid_dependency_wait();
     grid_dependents_launch();
@@ -428,12 +440,12 @@ anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m,
         const float *pc = P + (size_t)c * kPartF;
 #pragma unroll
         for (int r = 0; r < kRJ; ++r) {
-            w[r] = __fadd_rn(w[r], __ldg(pc + (size_t)(j0 + r) * 2 * kD + k));
-            dw[r] = __fadd_rn(dw[r], __ldg(pc + (size_t)(j0 + r) * 2 * kD + kD + k));
-            dl[r] = __fadd_rn(dl[r], __ldg(pc + kMP * 2 * kD + j0 + r));
+            w[r] = __fadd_rn(w[r], __ldg(pc + (size_t)(j0 + r) * 2 * D + k));
+            dw[r] = __fadd_rn(dw[r], __ldg(pc + (size_t)(j0 + r) * 2 * D + D + k));
+            dl[r] = __fadd_rn(dl[r], __ldg(pc + kMP * 2 * D + j0 + r));
         }
     }
-    __nv_bfloat16 *I = img + (size_t)slice * 4 * kMP * kD;
+    __nv_bfloat16 *I = img + (size_t)slice * 4 * kMP * D;
 #pragma unroll
     for (int r = 0; r < kRJ; ++r) {
         const int j = j0 + r;
@@ -441,10 +453,10 @@ anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m,
         if (k == 0) s_rinv[r] = rinv;
         const float wp = w[r] * rinv, dwv = dw[r] * rinv;
         const __nv_bfloat16 wh = __float2bfloat16_rn(wp), dh = __float2bfloat16_rn(dwv);
-        I[(size_t)(0 * kMP + j) * kD + k] = wh;
-        I[(size_t)(1 * kMP + j) * kD + k] = __float2bfloat16_rn(wp - __bfloat162float(wh));
-        I[(size_t)(2 * kMP + j) * kD + k] = dh;
-        I[(size_t)(3 * kMP + j) * kD + k] = __float2bfloat16_rn(dwv - __bfloat162float(dh));
+        I[(size_t)(0 * kMP + j) * D + k] = wh;
+        I[(size_t)(1 * kMP + j) * D + k] = __float2bfloat16_rn(wp - __bfloat162float(wh));
+        I[(size_t)(2 * kMP + j) * D + k] = dh;
+        I[(size_t)(3 * kMP + j) * D + k] = __float2bfloat16_rn(dwv - __bfloat162float(dh));
         float pr = dwv * wp;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) pr += __shfl_xor_sync(0xffffffffu, pr, o);
@@ -454,21 +466,23 @@ anchor_bwd_wide_reduce_kernel(const float *__restrict__ part, int chunks, int m,
     if (k < kRJ) {
         float dd = s_red[0][k];
 #pragma unroll
-        for (int q = 1; q < kD / 32; ++q) dd = __fadd_rn(dd, s_red[q][k]);
+        for (int q = 1; q < D / 32; ++q) dd = __fadd_rn(dd, s_red[q][k]);
         const int j = j0 + k;
         ddelta[(size_t)slice * kMP + j] = s_rinv[k] != 0.f ? -dd : 0.f;
     }
 }
 
 // ------------------------------------------------------------------------------ pass 2
+template <int D>
 __global__ void __launch_bounds__(kP2Threads, 1)
 anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ CUtensorMap tdh, const __grid_constant__ CUtensorMap tu,
                           const __grid_constant__ CUtensorMap timg, const __grid_constant__ CUtensorMap tdq,
                           const __grid_constant__ CUtensorMap tdv, const BwParams p) {
+    using GE = Geo<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + k2Bar);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + GE::k2Bar);
     uint64_t *u_full = bars + 0, *q_full = bars + 1, *x_free = bars + 3,
              *s_free = bars + 5, *v_full = bars + 7, *v_free = bars + 8, *img_full = bars + 9 /* [2] */,
              *img_empty = bars + 11 /* [2] */, *s_full = bars + 13, *s_empty = bars + 14, *g_full = bars + 15,
@@ -476,7 +490,7 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
              *ds_full = bars + 20, *dq_full = bars + 21, *du_full = bars + 22, *mma_done = bars + 23,
              *x_ex = bars + 24, *h_full = bars + 25, *h_free = bars + 26;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + k2Bars);
-    float *sDD = reinterpret_cast<float *>(sm + k2DD);
+    float *sDD = reinterpret_cast<float *>(sm + GE::k2DD);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Item it = item_of(blockIdx.x, p.tiles, p.chunks);
     const int h = it.slice % p.heads;
@@ -530,28 +544,28 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             tma_prefetch_desc(&tdq);
             tma_prefetch_desc(&tdv);
             const uint64_t pol_keep = policy_evict_last(), pol_once = policy_evict_first();
-            mbar_arrive_expect_tx(u_full, kTileB);
-            load_tile(sm + k2U, &tu, u_full, 0, h, pol_keep);
+            mbar_arrive_expect_tx(u_full, GE::kUB);
+            load_tile<GE::kNB>(sm + GE::k2U, &tu, u_full, 0, h, pol_keep);
             int nq = 0, nh = 0, nv = 0;
             for (int i = 0; i < it.nt; ++i) {
                 const int row = (it.t0 + i) * kT;
                 for (int k = i == 0 ? 1 : 2; k <= 2; ++k)
                     if (i + k < it.nt) {
-                        prefetch_tile(&tq, row + k * kT, it.slice);
-                        prefetch_tile(&tv, row + k * kT, it.slice);
-                        prefetch_tile(&tdh, row + k * kT, it.slice);
+                        prefetch_tile<GE::kNB>(&tq, row + k * kT, it.slice);
+                        prefetch_tile<GE::kNB>(&tv, row + k * kT, it.slice);
+                        prefetch_tile<GE::kNB>(&tdh, row + k * kT, it.slice);
                     }
                 if (i >= 1 && !bwait(x_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(q_full, kTileB);
-                load_tile(sm + k2X, &tq, q_full, row, it.slice, pol_once);
+                mbar_arrive_expect_tx(q_full, GE::kQB);
+                load_tile<GE::kNB>(sm + GE::k2X, &tq, q_full, row, it.slice, pol_once);
                 ++nq;
                 if (i >= 1 && !bwait(h_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(h_full, kTileB);
-                load_tile(sm + k2VH + kTileB, &tdh, h_full, row, it.slice, pol_once);
+                mbar_arrive_expect_tx(h_full, GE::kQB);
+                load_tile<GE::kNB>(sm + GE::k2VH + kAB, &tdh, h_full, row, it.slice, pol_once);
                 ++nh;
                 if (i >= 1 && !bwait(v_free, (uint32_t)((i - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(v_full, kTileB);
-                load_tile(sm + k2VH, &tv, v_full, row, it.slice, pol_once);
+                mbar_arrive_expect_tx(v_full, GE::kQB);
+                load_tile<GE::kNB>(sm + GE::k2VH, &tv, v_full, row, it.slice, pol_once);
                 ++nv;
             }
             if (nq > 0) bwait(q_full, (uint32_t)((nq - 1) & 1), p.wait_ns);
@@ -569,8 +583,8 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             for (int u = 0; u < 4 * it.nt; ++u) {
                 const int s = u & 1;
                 if (u >= 2 && !bwait(img_empty + s, (uint32_t)(((u >> 1) - 1) & 1), p.wait_ns)) break;
-                mbar_arrive_expect_tx(img_full + s, kTileB);
-                load_tile(sm + k2Img + s * kTileB, &timg, img_full + s, 0, it.slice * 4 + (u & 3), pol_keep);
+                mbar_arrive_expect_tx(img_full + s, GE::kUB);
+                load_tile<GE::kNB>(sm + GE::k2Img + s * GE::kUB, &timg, img_full + s, 0, it.slice * 4 + (u & 3), pol_keep);
                 ++nimg[s];
             }
             for (int b = 0; b < 2; ++b)
@@ -580,15 +594,15 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
     } else if (warp == kP2Issue) {
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(kT, kMP, false, false);  // [tokens x anchors], K = d
-            const uint32_t idR = idesc_bf16_f32(kT, kD, false, true);    // [tokens x d], K = anchors
-            const uint32_t idU = idesc_bf16_f32(kMP, kD, true, true);    // dS^T Q: anchors x d, K = tokens
-            const uint64_t udesc = smem_desc_sw128(sbase + k2U, 16, 1024);      // U, K-major (N = anchors)
-            const uint64_t umn = smem_desc_sw128(sbase + k2U, kBlkB, 1024);     // U, MN-major (N = d)
-            const uint64_t vk = smem_desc_sw128(sbase + k2VH, 16, 1024);
-            const uint64_t hk = smem_desc_sw128(sbase + k2VH + kTileB, 16, 1024);
+            const uint32_t idR = idesc_bf16_f32(kT, D, false, true);    // [tokens x d], K = anchors
+            const uint32_t idU = idesc_bf16_f32(kMP, D, true, true);    // dS^T Q: anchors x d, K = tokens
+            const uint64_t udesc = smem_desc_sw128(sbase + GE::k2U, 16, 1024);      // U, K-major (N = anchors)
+            const uint64_t umn = smem_desc_sw128(sbase + GE::k2U, kBlkB, 1024);     // U, MN-major (N = d)
+            const uint64_t vk = smem_desc_sw128(sbase + GE::k2VH, 16, 1024);
+            const uint64_t hk = smem_desc_sw128(sbase + GE::k2VH + kAB, 16, 1024);
             bool ok = bwait(u_full, 0u, p.wait_ns);
             for (int i = 0; i < it.nt && ok; ++i) {
-                const uint32_t xq = sbase + k2X;
+                const uint32_t xq = sbase + GE::k2X;
                 // S_i = Q_i U^T, once dV_{i-1} has read A_{i-1} over S's columns
                 if (!bwait(q_full, (uint32_t)(i & 1), p.wait_ns)) { ok = false; break; }
                 if (i >= 1 && !bwait(s_free, (uint32_t)((i - 1) & 1), p.wait_ns)) { ok = false; break; }
@@ -596,7 +610,7 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 {
                     const uint64_t qd = smem_desc_sw128(xq, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk)
+                    for (int kk = 0; kk < D / 16; ++kk)
                         umma_bf16(tmem + k2ColS, qd + kstep(kk), udesc + kstep(kk), idS, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(s_full);
@@ -609,9 +623,9 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                     if (!bwait(img_full + s, (uint32_t)((u >> 1) & 1), p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = part < 2 ? hk : vk;
-                    const uint64_t bd = smem_desc_sw128(sbase + k2Img + s * kTileB, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(sbase + GE::k2Img + s * GE::kUB, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk)
+                    for (int kk = 0; kk < D / 16; ++kk)
                         umma_bf16(tmem + k2ColG, ad + kstep(kk), bd + kstep(kk), idS, (part > 0 || kk > 0) ? 1u : 0u);
                     if (part < 2) umma_commit(img_empty + s);  // W' parts: the slot takes a dW part next
                 }
@@ -624,7 +638,7 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < 2; ++s) {
-                    const uint64_t dwm = smem_desc_sw128(sbase + k2Img + s * kTileB, kBlkB, 1024);
+                    const uint64_t dwm = smem_desc_sw128(sbase + GE::k2Img + s * GE::kUB, kBlkB, 1024);
 #pragma unroll
                     for (int kj = 0; kj < kMP / 16; ++kj)
                         umma_bf16_tmem_a(tmem + k2ColDV, tmem + k2ColS + kj * 8, dwm + (uint64_t)(kj * 128), idR,
@@ -642,14 +656,14 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 tc_fence_after();
                 {
                     const uint64_t qm = smem_desc_sw128(xq, kBlkB, 1024);  // Q_i, MN-major (N = d)
-                    const uint64_t dsml = smem_desc_sw128(sbase + k2VH + kTileB, kBlkB, 1024);  // dS_lo^T
+                    const uint64_t dsml = smem_desc_sw128(sbase + GE::k2VH + kAB, kBlkB, 1024);  // dS_lo^T
 #pragma unroll
                     for (int kt = 0; kt < kT / 16; ++kt)
                         umma_bf16(tmem + k2ColDU, dsml + (uint64_t)(kt * 128), qm + (uint64_t)(kt * 128), idU,
                                   (i > 0 || kt > 0) ? 1u : 0u);
                     umma_commit(h_free);
-                    const uint64_t dsk = smem_desc_sw128(sbase + k2VH, 16, 1024);
-                    const uint64_t dsm = smem_desc_sw128(sbase + k2VH, kBlkB, 1024);  // dS_hi^T: anchors x tokens
+                    const uint64_t dsk = smem_desc_sw128(sbase + GE::k2VH, 16, 1024);
+                    const uint64_t dsm = smem_desc_sw128(sbase + GE::k2VH, kBlkB, 1024);  // dS_hi^T: anchors x tokens
 #pragma unroll
                     for (int kt = 0; kt < kT / 16; ++kt)
                         umma_bf16(tmem + k2ColDU, dsm + (uint64_t)(kt * 128), qm + (uint64_t)(kt * 128), idU, 1u);
@@ -682,12 +696,14 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         // (swizzled like a TMA box) -> one TMA store of the warp's 32 rows and 64 columns (rows
         // past the slice are not written); the staging is reused once the previous store has
         // read it
-        uint8_t *stage = sm + k2Stage + warp * 4096;
+        // (at D = 64 column half 0 drains all 64 columns, half 1 only arrives)
+        uint8_t *stage = sm + GE::k2Stage + warp * 4096;
+        const bool drains = D == 128 || g == 0;
         auto drain = [&](int i, uint64_t *full, uint64_t *empty, uint32_t col, const CUtensorMap *map,
                          float r) -> bool {
             if (!bwait(full, (uint32_t)(i & 1), p.wait_ns)) return false;
             tc_fence_after();
-            float o[64];
+            float o[64];  // (at D = 64 half 1 reads columns past the tile's and stores nothing)
             tmem_ld32(trow + col + 64 * g, o);
             tmem_ld32(trow + col + 64 * g + 32, o + 32);
             tmem_ld_wait();
@@ -698,14 +714,16 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
                 bulk_wait_group_read0();
             }
             __syncwarp();
+            if (drains) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(stage + sw_off(lane, c, 32)) = pack8(o + 8 * c, r);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_3d(map, stage, 64 * g, (it.t0 + i) * kT + (warp & 3) * 32, it.slice, pol_out);
-                bulk_commit_group();
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(stage + sw_off(lane, c, 32)) = pack8(o + 8 * c, r);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(map, stage, 64 * g, (it.t0 + i) * kT + (warp & 3) * 32, it.slice, pol_out);
+                    bulk_commit_group();
+                }
             }
             return true;
         };
@@ -810,8 +828,8 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
             for (int c = 0; c < 8; ++c) {
                 uint4 hi, lo;
                 split8(gv + 8 * c, hi, lo);
-                *reinterpret_cast<uint4 *>(sm + k2VH + sw_off(row, 8 * g + c, kT)) = hi;
-                *reinterpret_cast<uint4 *>(sm + k2VH + kTileB + sw_off(row, 8 * g + c, kT)) = lo;
+                *reinterpret_cast<uint4 *>(sm + GE::k2VH + sw_off(row, 8 * g + c, kT)) = hi;
+                *reinterpret_cast<uint4 *>(sm + GE::k2VH + kAB + sw_off(row, 8 * g + c, kT)) = lo;
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -827,13 +845,14 @@ anchor_bwd_wide_p2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_c
         if (ok) {
             tc_fence_after();
             float o[64];
-            tmem_ld32(trow + k2ColDU + 64 * g, o);
-            tmem_ld32(trow + k2ColDU + 64 * g + 32, o + 32);
+            constexpr int DH = D / 2;  // this half's columns of dU
+#pragma unroll
+            for (int q = 0; q < DH / 32; ++q) tmem_ld32(trow + k2ColDU + DH * g + 32 * q, o + 32 * q);
             tmem_ld_wait();
             if (row < p.m) {
-                float4 *dst = reinterpret_cast<float4 *>(p.dupart + ((size_t)blockIdx.x * p.m + row) * kD + 64 * g);
+                float4 *dst = reinterpret_cast<float4 *>(p.dupart + ((size_t)blockIdx.x * p.m + row) * D + DH * g);
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
+                for (int k = 0; k < DH / 4; ++k)
                     dst[k] = make_float4(o[4 * k] * p.scale, o[4 * k + 1] * p.scale, o[4 * k + 2] * p.scale,
                                          o[4 * k + 3] * p.scale);
             }
@@ -870,39 +889,34 @@ struct WideWs {
 };
 WideWs wide_ws(const BwdProblem &p, int chunks) {
     auto up = [](size_t x) { return (x + 1023) / 1024 * 1024; };
-    const size_t S = (size_t)p.slices();
+    const size_t S = (size_t)p.slices(), D = (size_t)p.d;
     WideWs w;
     w.part = 0;
-    w.img = up(w.part + 4 * S * chunks * (size_t)kPartF);
-    w.dd = up(w.img + 2 * S * 4 * kMP * kD);
+    w.img = up(w.part + 4 * S * chunks * (kMP * 2 * D + kMP));
+    w.dd = up(w.img + 2 * S * 4 * kMP * D);
     w.du = up(w.dd + 4 * S * kMP);
-    w.total = w.du + 4 * S * chunks * (size_t)p.m * kD;
+    w.total = w.du + 4 * S * chunks * (size_t)p.m * D;
     return w;
 }
 
-}  // namespace
-
-bool bwd_wide_supported(const BwdProblem &p) { return !p.f32 && p.d == kD && p.m >= 1 && p.m <= kMP && p.n >= 1; }
-
-size_t bwd_wide_workspace(const BwdProblem &p) {
-    return wide_ws(p, wide_chunks(p.slices(), (p.n + kT - 1) / kT)).total;
-}
-
-cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_wide(const BwdProblem &p, void *workspace, cudaStream_t stream) {
+    using GE = Geo<D>;
     const long long S = p.slices();
     const int tiles = (p.n + kT - 1) / kT;
     const int chunks = wide_chunks(S, tiles);
     const WideWs L = wide_ws(p, chunks);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     CUtensorMap tq, tv, tdh, tu, timg, tdq, tdv;
-    if (!make_bf16_map(&tq, p.Q, kD, p.n, S, kT) || !make_bf16_map(&tv, p.V, kD, p.n, S, kT) ||
-        !make_bf16_map(&tdh, p.dH, kD, p.n, S, kT) || !make_bf16_map(&tu, p.U, kD, p.m, p.heads, kMP) ||
-        !make_bf16_map(&timg, ws + L.img, kD, kMP, S * 4, kMP) || !make_bf16_map(&tdq, p.dQ, kD, p.n, S, 32) ||
-        !make_bf16_map(&tdv, p.dV, kD, p.n, S, 32))
+    if (!make_bf16_map(&tq, p.Q, D, p.n, S, kT) || !make_bf16_map(&tv, p.V, D, p.n, S, kT) ||
+        !make_bf16_map(&tdh, p.dH, D, p.n, S, kT) || !make_bf16_map(&tu, p.U, D, p.m, p.heads, kMP) ||
+        !make_bf16_map(&timg, ws + L.img, D, kMP, S * 4, kMP) || !make_bf16_map(&tdq, p.dQ, D, p.n, S, 32) ||
+        !make_bf16_map(&tdv, p.dV, D, p.n, S, 32))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(anchor_bwd_wide_p1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, k1Smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(anchor_bwd_wide_p1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, GE::k1Smem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(anchor_bwd_wide_p2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, k2Smem);
+        e = cudaFuncSetAttribute(anchor_bwd_wide_p2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, GE::k2Smem);
     if (e != cudaSuccess) return e;
     BwParams bp;
     bp.heads = p.heads;
@@ -919,17 +933,39 @@ cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t s
     bp.dV = static_cast<__nv_bfloat16 *>(p.dV);
     bp.wait_ns = 2000000000ull;
     const dim3 grid((unsigned)(S * chunks));
-    if ((e = launch_pdl(anchor_bwd_wide_p1_kernel, grid, dim3(kP1Threads), k1Smem, stream, tq, tv, tdh, tu, bp)) !=
-        cudaSuccess)
+    if ((e = launch_pdl(anchor_bwd_wide_p1_kernel<D>, grid, dim3(kP1Threads), GE::k1Smem, stream, tq, tv, tdh, tu,
+                        bp)) != cudaSuccess)
         return e;
-    if ((e = launch_pdl(anchor_bwd_wide_reduce_kernel, dim3((unsigned)S, kMP / kRJ), dim3(kD), 0, stream,
+    if ((e = launch_pdl(anchor_bwd_wide_reduce_kernel<D>, dim3((unsigned)S, kMP / kRJ), dim3(D), 0, stream,
                         (const float *)bp.part, chunks, p.m, reinterpret_cast<__nv_bfloat16 *>(ws + L.img),
                         reinterpret_cast<float *>(ws + L.dd))) != cudaSuccess)
         return e;
-    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel, grid, dim3(kP2Threads), k2Smem, stream, tq, tv, tdh, tu, timg, tdq, tdv, bp)) !=
-        cudaSuccess)
+    if ((e = launch_pdl(anchor_bwd_wide_p2_kernel<D>, grid, dim3(kP2Threads), GE::k2Smem, stream, tq, tv, tdh, tu, timg,
+                        tdq, tdv, bp)) != cudaSuccess)
         return e;
-    return launch_bwd_du_sum(bp.dupart, p.dU, p.B, p.heads, chunks, p.m * kD, false, stream);
+    return launch_bwd_du_sum(bp.dupart, p.dU, p.B, p.heads, chunks, p.m * D, false, stream);
+}
+
+}  // namespace
+
+bool bwd_wide_supported(const BwdProblem &p) {
+    return !p.f32 && (p.d == 64 || p.d == 128) && p.m >= 1 && p.m <= kMP && p.n >= 1;
+}
+
+// d = 128 always; d = 64 when the one-CTA-per-slice kernel cannot take it (m > 64).  (At
+// d = 64 with m <= 64 these kernels still pad the anchors to 128 and came out slower than the
+// one-CTA-per-slice kernel even on long slices: 0.225 against 0.202 ms on 96 slices of 33 tiles.)
+bool bwd_wide_preferred(const BwdProblem &p) {
+    if (!bwd_wide_supported(p)) return false;
+    return p.d == 128 || p.m > 64;
+}
+
+size_t bwd_wide_workspace(const BwdProblem &p) {
+    return wide_ws(p, wide_chunks(p.slices(), (p.n + kT - 1) / kT)).total;
+}
+
+cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t stream) {
+    return p.d == 64 ? launch_wide<64>(p, workspace, stream) : launch_wide<128>(p, workspace, stream);
 }
 
 cudaError_t bwd_wide_read_and_clear_error(unsigned *out) {

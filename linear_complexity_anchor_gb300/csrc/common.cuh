@@ -96,10 +96,12 @@ bool bwd_tc_supported(const BwdProblem &p);
 size_t bwd_tc_workspace(const BwdProblem &p);
 cudaError_t launch_bwd_tc(const BwdProblem &p, void *workspace, cudaStream_t stream);
 cudaError_t bwd_tc_read_and_clear_error(unsigned *out);
-// the backward on the tensor cores for d = 128, m <= 128 (bf16): pass 1, a per-slice reduce,
-// pass 2 and the dU sum; workspace = the items' pass-1 blocks, the slices' W' and dW images,
-// dDelta and the items' dU blocks
+// the backward on the tensor cores for d = 64 or 128, m <= 128 (bf16): pass 1, a per-slice
+// reduce, pass 2 and the dU sum over runs of each slice's tiles; workspace = the items' pass-1
+// blocks, the slices' W' and dW images, dDelta and the items' dU blocks.  Preferred for d = 128
+// and for d = 64 with m > 64; d = 64 with m <= 64 takes bwd_tc.
 bool bwd_wide_supported(const BwdProblem &p);
+bool bwd_wide_preferred(const BwdProblem &p);
 size_t bwd_wide_workspace(const BwdProblem &p);
 cudaError_t launch_bwd_wide(const BwdProblem &p, void *workspace, cudaStream_t stream);
 cudaError_t bwd_wide_read_and_clear_error(unsigned *out);

@@ -1,7 +1,8 @@
 """GPU: the backward (dQ, dU, dV) through the C ABI against the oracle's backward, element by
 element, on the same seeded inputs (the oracle's backward is pinned by finite differences of
-the forward oracle in test_oracle_backward_pins.py).  bf16 with d = 64 and m <= 64, and bf16
-with d = 128 and m <= 128, run on the tensor cores; the rest, and fp32, on CUDA cores."""
+the forward oracle in test_oracle_backward_pins.py).  bf16 with d = 64 or 128 and m <= 128 runs
+on the tensor cores (one CTA per slice at d = 64 with m <= 64, runs of tiles over every SM
+otherwise); the rest, and fp32, on CUDA cores."""
 import os
 from concurrent.futures import ThreadPoolExecutor
 
@@ -90,6 +91,20 @@ _WIDE_SHAPES = [(3, 2, 1, 7, 128), (2, 2, 128, 128, 128), (1, 3, 129, 49, 128), 
                 (2, 2, 300, 1, 128), (16, 2, 197, 100, 128), (1, 2, 5000, 40, 128)]
 
 
+# the same kernels at d = 64 with more than 64 anchors (one token; a ragged second tile; a long
+# slice cut into many runs; the most anchors)
+_WIDE64_SHAPES = [(3, 1, 1, 70, 64), (2, 2, 300, 100, 64), (2, 2, 1100, 65, 64), (1, 3, 2000, 128, 64),
+                  (1, 2, 129, 128, 64)]
+
+
+@pytest.mark.parametrize("shape", _WIDE64_SHAPES)
+def test_backward_wide_d64_shapes(env, shape):
+    got, ref, _ = _case(env, "bf16", *shape, seed=sum(shape) + 3)
+    for name, g, r in zip(("dQ", "dU", "dV"), got, ref):
+        assert_parity(to_host64(g), r, "bf16", f"{name} {shape}")
+    assert env[0].device_error() == 0
+
+
 @pytest.mark.parametrize("shape", _WIDE_SHAPES)
 def test_backward_wide_tensor_core_shapes(env, shape):
     got, ref, _ = _case(env, "bf16", *shape, seed=sum(shape) + 2)
@@ -163,8 +178,9 @@ def test_backward_workload_every_slice(env, name):
 
 def test_backward_bit_stable(env):
     pkg, torch, _ = env
-    # tensor-core paths (d = 64, d = 128) and the CUDA-core path
-    for shape in [(2, 3, 1500, 64, 64), (2, 3, 1500, 100, 128), (2, 3, 1500, 100, 64)]:
+    # tensor-core paths (one CTA per slice at d = 64, m <= 64; runs of tiles at d = 64 with more
+    # anchors and at d = 128) and the CUDA-core path (more than 128 anchors)
+    for shape in [(2, 3, 1500, 64, 64), (2, 3, 1500, 100, 64), (2, 3, 1500, 100, 128), (2, 3, 1500, 200, 64)]:
         got1, _, (t, tdH, sc) = _case(env, "bf16", *shape, seed=9)
         got2 = pkg.backward(t["Q"], t["U"], t["V"], tdH, scale=sc)
         torch.cuda.synchronize()
