@@ -116,9 +116,9 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_host_f32(const float *Q
  * A is recomputed from Q and U (nothing is kept from the forward).
  * With d = 64 and m <= 64 the contractions run on the tensor cores (tcgen05: bf16 operands,
  * fp32 accumulators; A, W', dW and dS enter as hi + lo bf16 pairs), one CTA per slice; with
- * d = 128 and m <= 128 also on the tensor cores, as a first pass over runs of tiles, a
- * per-slice reduce, a second pass and the dU sum (the split into runs depends on the shape
- * alone); otherwise on CUDA-core fp32 FMA.
+ * d = 128 and m <= 128, or d = 64 and 64 < m <= 128, also on the tensor cores, as a first pass
+ * over runs of tiles, a per-slice reduce, a second pass and the dU sum (the split into runs
+ * depends on the shape alone); otherwise on CUDA-core fp32 FMA.
  *
  * Inputs Q, V, dH: [B][heads][n][d]; U: [heads][m][d].  Outputs dQ, dV: [B][heads][n][d];
  * dU: [heads][m][d] (the sum over the batch entries, which share the anchors).  Device
@@ -128,7 +128,7 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_host_f32(const float *Q
  * floats) and tiles do not fit one CTA's shared memory return ANCHOR_ATTN_ERR_UNSUPPORTED
  * (for fp32: d = 16 with m > about 900, d = 32 with m > about 480).  One workspace from
  * cudaMallocAsync on `stream` per call, released on the same stream; two kernel launches
- * (four at d = 128 on the tensor cores).
+ * (four on the two-pass tensor-core path).
  * Results are bit-identical from run to run; a bounded wait that gives up is reported by
  * anchor_attn_device_error (bit 1 on the CUDA-core path, bit 0 on the tensor-core paths).
  */
