@@ -86,11 +86,15 @@ ANCHOR_ATTN_API anchor_attn_status_t anchor_attn_forward_f32(const float *Q, con
  * Forward from host buffers: Q, U, V and H are host pointers (pinned memory, e.g. from
  * cudaHostAlloc, for the copies to run asynchronously; pageable memory works but the copies
  * then hold the calling thread), same layout, shapes, numbers and errors as
- * anchor_attn_forward (bit-identical results: the same kernels run on device copies).  The
- * batch is cut into chunks of whole batch entries; chunk by chunk Q and V are copied to the
- * device on an internal stream, the forward runs on `stream`, and H is copied back on a
+ * anchor_attn_forward.  The batch is cut into chunks of whole batch entries, or of head ranges
+ * of single batch entries when that gives too few chunks; chunk by chunk Q and V are copied to
+ * the device on an internal stream, the forward runs on `stream`, and H is copied back on a
  * second internal stream, over two device buffer sets, so that copies in, forward and copies
- * out of neighbouring chunks overlap.  Asynchronous: H is complete once `stream` has reached
+ * out of neighbouring chunks overlap.  The results are bit-identical to anchor_attn_forward's
+ * (the same kernels, planned for the whole problem), except where the whole problem has more
+ * than 152 slices at d = 64 with 32 <= m <= 64 and n > 512: there the device entry cuts the
+ * tile list over the SMs and the chunks do not, so sums run in another order (the same values
+ * within rounding).  Asynchronous: H is complete once `stream` has reached
  * this point (every internal copy is ordered before it); work already on `stream` is ordered
  * before the copies.  The device workspace (U and two chunks of Q, V, H) comes from
  * cudaMallocAsync on `stream` and goes back on it (ANCHOR_ATTN_ERR_ALLOC if it cannot be

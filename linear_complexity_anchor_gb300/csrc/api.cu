@@ -330,6 +330,10 @@ anchor_attn_status_t backward(const anchor::BwdProblem &p, void *stream_v) {
 
 }  // namespace
 
+namespace anchor {
+anchor_attn_status_t forward_problem(const Problem &p, void *stream) { return run(p, stream); }
+}  // namespace anchor
+
 extern "C" {
 
 anchor_attn_status_t anchor_attn_forward(const void *Q, const void *U, const void *V, void *H, int B,

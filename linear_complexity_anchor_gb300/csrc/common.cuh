@@ -23,8 +23,16 @@ struct Problem {
     int B, heads, n, m, d;
     float scale;
     bool f32;  // element type of Q, U, V, H: float (true) or bf16 (false)
+    // the slice count the persistent tensor-core plan cuts a slice's pass 1 by (its chunks set
+    // the summation order of W): 0 = this problem's own.  A part of a larger problem run on its
+    // own (the host entry's chunks) passes the whole problem's, so that its bits match the
+    // whole problem's.
+    long long plan_slices = 0;
     long long slices() const { return (long long)B * heads; }
+    long long plan_S() const { return plan_slices > 0 ? plan_slices : slices(); }
 };
+// the forward of a problem (the C ABI's checks, plan and launch; used by the host entry)
+anchor_attn_status_t forward_problem(const Problem &p, void *stream);
 
 // Argument checks of the C ABI (see include/anchor_attn.h); no device access.
 anchor_attn_status_t check_shape(int B, int heads, int n, int m, int d);

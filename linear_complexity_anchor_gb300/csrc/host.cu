@@ -1,6 +1,8 @@
-// Forward from host buffers.  The batch is cut into chunks of whole batch entries (each chunk
-// covers every head, so U is copied once and every chunk is an ordinary forward problem);
-// chunk k's Q and V are copied in on one stream, its forward runs on the caller's stream and
+// Forward from host buffers.  The batch is cut into chunks of whole batch entries, or, when that
+// gives too few chunks to overlap well, of head ranges of single batch entries (U is copied
+// once; a chunk is an ordinary forward problem on a range of U's rows, planned with the whole
+// problem's slice count so that its result bits are the whole problem's); chunk k's Q and V
+// are copied in on one stream, its forward runs on the caller's stream and
 // its H is copied out on a third stream, over two device buffer sets, so that the copies of
 // one chunk overlap the forward of the next and the copies in and out run at the same time
 // (Q and V on two streams of their own were no faster: the host link, not a copy engine, sets
@@ -64,14 +66,28 @@ anchor_attn_status_t forward_host(const void *hQ, const void *hU, const void *hV
     }
     Pipe &P = *pp;
     const size_t elem = f32 ? 4 : 2;
-    const size_t entry = (size_t)heads * n * d * elem;  // one batch entry of Q, V or H
+    const size_t sbytes = (size_t)n * d * elem;  // one slice of Q, V or H
     const size_t ubytes = (size_t)heads * m * d * elem;
-    const long long want = (long long)((3 * entry * (size_t)B + kChunkBytes - 1) / kChunkBytes);
-    const int chunks = (int)std::max<long long>(1, std::min<long long>({(long long)B, (long long)kMaxChunks, want}));
-    const int per = (B + chunks - 1) / chunks;  // batch entries of the largest chunk
+    const long long S = whole.slices();
+    const long long want = (long long)((3 * sbytes * (size_t)S + kChunkBytes - 1) / kChunkBytes);
+    // Chunks: whole batch entries while that gives enough of them; else each batch entry cut
+    // into head ranges (a chunk is always slices of one head range of whole batch entries, so
+    // that it is an ordinary problem: its U is a range of rows of U)
+    int chunks, hsplit, per_b = 1;
+    if (want <= B) {
+        hsplit = 1;
+        chunks = (int)std::max<long long>(1, std::min<long long>({(long long)B, (long long)kMaxChunks, want}));
+        per_b = (B + chunks - 1) / chunks;
+    } else {
+        hsplit = (int)std::max<long long>(1, std::min<long long>({(long long)heads, (long long)(kMaxChunks / B),
+                                                                    (want + B - 1) / B}));
+        chunks = B * hsplit;
+    }
+    const int per_h = (heads + hsplit - 1) / hsplit;
+    const size_t per = (size_t)(hsplit == 1 ? per_b * heads : per_h);  // slices of the largest chunk
     const int sets = chunks > 1 ? 2 : 1;
     // device workspace: U | sets x (Q | V | H) of the largest chunk
-    const size_t setb = 3 * entry * (size_t)per;
+    const size_t setb = 3 * sbytes * per;
     const size_t ubytes_al = (ubytes + 255) / 256 * 256;
     uint8_t *ws = nullptr;
     if (getenv("ANCHOR_ATTN_TEST_FAIL_ALLOC") != nullptr) return ANCHOR_ATTN_ERR_ALLOC;
@@ -88,21 +104,35 @@ anchor_attn_status_t forward_host(const void *hQ, const void *hU, const void *hV
     if (e == cudaSuccess) e = cudaMemcpyAsync(ws, hU, ubytes, cudaMemcpyHostToDevice, P.in);
     int issued_out = 0;
     for (int k = 0; k < chunks && e == cudaSuccess && status == ANCHOR_ATTN_OK; ++k) {
-        const int b0 = (int)((long long)k * B / chunks), b1 = (int)((long long)(k + 1) * B / chunks);
-        const size_t bytes = entry * (size_t)(b1 - b0), off = entry * (size_t)b0;
-        uint8_t *dQ = ws + ubytes_al + (k % sets) * setb, *dV = dQ + entry * per, *dH = dV + entry * per;
+        // this chunk: batch entries [b0, b1) x heads [h0, h1), contiguous in memory
+        int b0, b1, h0, h1;
+        if (hsplit == 1) {
+            b0 = (int)((long long)k * B / chunks);
+            b1 = (int)((long long)(k + 1) * B / chunks);
+            h0 = 0;
+            h1 = heads;
+        } else {
+            b0 = k / hsplit;
+            b1 = b0 + 1;
+            const int j = k - b0 * hsplit;
+            h0 = (int)((long long)j * heads / hsplit);
+            h1 = (int)((long long)(j + 1) * heads / hsplit);
+        }
+        const size_t off = ((size_t)b0 * heads + h0) * sbytes;
+        const size_t bytes = (size_t)(b1 - b0) * (h1 - h0) * sbytes;
+        uint8_t *dQ = ws + ubytes_al + (k % sets) * setb, *dV = dQ + sbytes * per, *dH = dV + sbytes * per;
         // copy in (after the copy out of the chunk that last used this buffer set)
         if (k >= sets) e = cudaStreamWaitEvent(P.in, ev_out[k - sets], 0);
         if (e == cudaSuccess) e = cudaMemcpyAsync(dQ, static_cast<const uint8_t *>(hQ) + off, bytes, cudaMemcpyHostToDevice, P.in);
         if (e == cudaSuccess) e = cudaMemcpyAsync(dV, static_cast<const uint8_t *>(hV) + off, bytes, cudaMemcpyHostToDevice, P.in);
         if (e == cudaSuccess) e = cudaEventRecord(ev_in[k], P.in);
-        // the forward of the chunk on the caller's stream
+        // the forward of the chunk on the caller's stream, planned as the whole problem would be
+        // (the same result bits)
         if (e == cudaSuccess) e = cudaStreamWaitEvent(user, ev_in[k], 0);
         if (e != cudaSuccess) break;
-        status = f32 ? anchor_attn_forward_f32(reinterpret_cast<const float *>(dQ), reinterpret_cast<const float *>(ws),
-                                               reinterpret_cast<const float *>(dV), reinterpret_cast<float *>(dH),
-                                               b1 - b0, heads, n, m, d, scale, user)
-                     : anchor_attn_forward(dQ, ws, dV, dH, b1 - b0, heads, n, m, d, scale, user);
+        Problem cp{dQ, ws + (size_t)h0 * m * d * elem, dV, dH, b1 - b0, h1 - h0, n, m, d, scale, f32};
+        cp.plan_slices = S;
+        status = forward_problem(cp, user);
         if (status != ANCHOR_ATTN_OK) break;
         e = cudaEventRecord(ev_comp[k], user);
         // copy out

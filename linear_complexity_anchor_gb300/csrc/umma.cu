@@ -1565,7 +1565,8 @@ UmmaPlan umma_plan(const Problem &p, bool force_recompute) {
     // on the shape alone.
     const long long want = 3LL * kPlanSMs / 2;
     int t1 = kUmmaP1Tiles, t2 = kUmmaP2Tiles;
-    while (t1 > kUmmaMinTiles && S * ((pl.NT + t1 - 1) / t1) < want) t1 /= 2;
+    // (pass 1's chunks set the summation order of W: they follow the plan's slice count)
+    while (t1 > kUmmaMinTiles && p.plan_S() * ((pl.NT + t1 - 1) / t1) < want) t1 /= 2;
     while (t2 > kUmmaMinTiles && S * ((pl.NT + t2 - 1) / t2) < want) t2 /= 2;
     pl.C1 = (pl.NT + t1 - 1) / t1;
     // Pass 2 reuses pass 1's A only when every slice's copy fits in half of a GB300's L2

@@ -43,6 +43,23 @@ def test_host_entry_matches_device_entry(env, name, pinned):
     assert pkg.device_error() == 0
 
 
+def test_host_entry_head_chunks_persistent_plan(env):
+    """One batch entry of 8 heads of 16384 tokens at d = m = 128 (100 MB of Q, V and H): two
+    chunks of four heads each; the persistent tensor-core plan of each chunk follows the whole
+    problem's slice count, so the bits are the device entry's."""
+    pkg, torch = env
+    w = gen.WORKLOADS["long_16k"].with_(name="host_heads", B=1, heads=8)
+    x = gen.make_inputs(w, seed=53)
+    h = {k: _host(x[k], w.dtype, torch, True) for k in "QUV"}
+    d = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    Hh = pkg.forward_host(h["Q"], h["U"], h["V"], scale=w.scale)
+    torch.cuda.current_stream().synchronize()
+    Hd = pkg.forward(d["Q"], d["U"], d["V"], scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(Hh.view(torch.int16), Hd.cpu().view(torch.int16))
+    assert pkg.device_error() == 0
+
+
 def test_host_entry_chunks_of_a_large_batch(env):
     """B = 5 entries, 184 MB of Q, V and H: three chunks (1, 2 and 2 entries) over two buffer
     sets; every entry against the device entry."""
