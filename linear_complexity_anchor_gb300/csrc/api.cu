@@ -84,7 +84,8 @@ Plan make_plan(const Problem &p) {
         const bool split = p.slices() > anchor::kPlanSMs;
         pl.variant = split ? ANCHOR_ATTN_VARIANT_SPLIT_TC : ANCHOR_ATTN_VARIANT_STREAM;
         pl.kernels = 1;
-        pl.splits = split ? 0 : 1;  // split: ranges of the tile list, not chunks of each slice
+        pl.splits = 0;  // split: ranges of the tile list, not chunks of each slice
+        if (!split) pl.splits = anchor::stream_cluster(p);  // stream: CTAs per slice
         pl.flags = ANCHOR_ATTN_PLAN_STORED_A;
         pl.workspace = split ? anchor::split_workspace(p) : anchor::stream_workspace(p);
         return pl;
@@ -332,6 +333,12 @@ anchor_attn_status_t backward(const anchor::BwdProblem &p, void *stream_v) {
 
 namespace anchor {
 anchor_attn_status_t forward_problem(const Problem &p, void *stream) { return run(p, stream); }
+
+int forward_stream_cluster(const Problem &p) {
+    if (p.slices() == 0 || p.n == 0 || make_plan(p).variant != ANCHOR_ATTN_VARIANT_STREAM) return 0;
+    return stream_cluster(p);
+}
+
 }  // namespace anchor
 
 extern "C" {

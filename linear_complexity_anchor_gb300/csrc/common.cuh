@@ -28,11 +28,17 @@ struct Problem {
     // own (the host entry's chunks) passes the whole problem's, so that its bits match the
     // whole problem's.
     long long plan_slices = 0;
+    // the slice-streaming kernel's CTAs per slice; 0 = what this problem's shape gives.  The
+    // host entry's chunks pass the whole problem's.
+    int plan_cl_c = 0;
     long long slices() const { return (long long)B * heads; }
     long long plan_S() const { return plan_slices > 0 ? plan_slices : slices(); }
 };
 // the forward of a problem (the C ABI's checks, plan and launch; used by the host entry)
 anchor_attn_status_t forward_problem(const Problem &p, void *stream);
+// the CTAs per slice the forward of `p` runs the slice-streaming kernel with; 0 when it takes
+// another kernel
+int forward_stream_cluster(const Problem &p);
 
 // Argument checks of the C ABI (see include/anchor_attn.h); no device access.
 anchor_attn_status_t check_shape(int B, int heads, int n, int m, int d);
@@ -195,6 +201,7 @@ bool make_bf16_map(CUtensorMap *map, const void *base, int cols, int rows, long 
 // --- slice-streaming tensor-core variant (d = 64, m <= 64): one CTA per slice ----------------
 // workspace: the A tiles of pass 1, [slices][n][64] bf16
 bool stream_supported(const Problem &p);
+int stream_cluster(const Problem &p);  // CTAs per slice (a cluster when more than 1)
 size_t stream_workspace(const Problem &p);
 cudaError_t launch_stream(const Problem &p, void *workspace, cudaStream_t stream);
 cudaError_t stream_read_and_clear_error(unsigned *out);

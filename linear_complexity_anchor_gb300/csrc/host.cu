@@ -1,7 +1,9 @@
 // Forward from host buffers.  The batch is cut into chunks of whole batch entries, or, when that
-// gives too few chunks to overlap well, of head ranges of single batch entries (U is copied
-// once; a chunk is an ordinary forward problem on a range of U's rows, planned with the whole
-// problem's slice count so that its result bits are the whole problem's); chunk k's Q and V
+// gives too few chunks to overlap well (and there are fewer batch entries than chunks allowed),
+// of head ranges of single batch entries.  U is copied once; a chunk is an ordinary forward
+// problem on a range of U's rows, planned as the whole problem is (its slice count, the
+// slice-streaming kernel's CTAs per slice), so that its result bits are the whole problem's.
+// Chunk k's Q and V
 // are copied in on one stream, its forward runs on the caller's stream and
 // its H is copied out on a third stream, over two device buffer sets, so that the copies of
 // one chunk overlap the forward of the next and the copies in and out run at the same time
@@ -70,11 +72,13 @@ anchor_attn_status_t forward_host(const void *hQ, const void *hU, const void *hV
     const size_t ubytes = (size_t)heads * m * d * elem;
     const long long S = whole.slices();
     const long long want = (long long)((3 * sbytes * (size_t)S + kChunkBytes - 1) / kChunkBytes);
-    // Chunks: whole batch entries while that gives enough of them; else each batch entry cut
-    // into head ranges (a chunk is always slices of one head range of whole batch entries, so
-    // that it is an ordinary problem: its U is a range of rows of U)
+    const int cl_c = forward_stream_cluster(whole);
+    // Chunks: whole batch entries while that gives enough of them (or there are kMaxChunks
+    // entries or more); else each batch entry cut into head ranges (a chunk is always slices of
+    // one head range of whole batch entries, so that it is an ordinary problem: its U is a range
+    // of rows of U, its Q, V and H one run of memory)
     int chunks, hsplit, per_b = 1;
-    if (want <= B) {
+    if (want <= B || B >= kMaxChunks) {
         hsplit = 1;
         chunks = (int)std::max<long long>(1, std::min<long long>({(long long)B, (long long)kMaxChunks, want}));
         per_b = (B + chunks - 1) / chunks;
@@ -132,6 +136,7 @@ anchor_attn_status_t forward_host(const void *hQ, const void *hU, const void *hV
         if (e != cudaSuccess) break;
         Problem cp{dQ, ws + (size_t)h0 * m * d * elem, dV, dH, b1 - b0, h1 - h0, n, m, d, scale, f32};
         cp.plan_slices = S;
+        cp.plan_cl_c = cl_c;
         status = forward_problem(cp, user);
         if (status != ANCHOR_ATTN_OK) break;
         e = cudaEventRecord(ev_comp[k], user);

@@ -87,9 +87,14 @@ def test_plans(pkg):
     # slice-streaming tensor-core variants: bf16, d = 64, 32 <= m <= 64, n > 512; one CTA per
     # slice up to 152 slices (workspace: the A tiles of pass 1), the tile list cut over 152
     # CTAs beyond (the A tiles first, then counters, partials and W' images)
+    # (CTAs per slice: 96 slices of 33 tiles: one; 1 slice of 33 tiles: a cluster of 8; 16
+    # slices of 128 tiles: clusters of 6; 40 slices of 5 tiles: one)
     p = pkg.query_plan("bf16", 8, 12, 4200, 64, 64)
-    assert p["variant"] == "stream" and p["kernels_per_call"] == 1 and p["stored_a"]
+    assert p["variant"] == "stream" and p["kernels_per_call"] == 1 and p["stored_a"] and p["splits"] == 1
     assert p["workspace_bytes"] == 8 * 12 * 4200 * 64 * 2
+    assert pkg.query_plan("bf16", 1, 1, 4200, 64, 64)["splits"] == 8
+    assert pkg.query_plan("bf16", 1, 16, 16384, 64, 64)["splits"] == 6
+    assert pkg.query_plan("bf16", 4, 10, 600, 40, 64)["splits"] == 1
     p = pkg.query_plan("bf16", 16, 12, 4200, 64, 64)
     assert p["variant"] == "split_tc" and p["stored_a"] and p["workspace_bytes"] > 16 * 12 * 4200 * 64 * 2
     assert pkg.query_plan("bf16", 8, 12, 512, 64, 64)["variant"] == "umma"

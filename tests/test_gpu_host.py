@@ -60,6 +60,26 @@ def test_host_entry_head_chunks_persistent_plan(env):
     assert pkg.device_error() == 0
 
 
+def test_host_entry_head_chunks_keep_the_cluster_plan(env):
+    """One batch entry of 16 heads of 16384 tokens at d = m = 64: the device entry runs the
+    slice-streaming kernel in clusters of 6 CTAs per slice (8 slices alone would take 8); the
+    host entry cuts the heads into two chunks of 8 and runs each with clusters of 6, so the bits
+    are the device entry's."""
+    pkg, torch = env
+    w = gen.WORKLOADS["det_800x1344"].with_(name="host_cluster", B=1, heads=16, n=16384, m=64, d=64)
+    assert pkg.query_plan("bf16", 1, 16, 16384, 64, 64)["splits"] == 6
+    assert pkg.query_plan("bf16", 1, 8, 16384, 64, 64)["splits"] == 8
+    x = gen.make_inputs(w, seed=57)
+    h = {k: _host(x[k], w.dtype, torch, True) for k in "QUV"}
+    d = {k: to_device(x[k], w.dtype, torch) for k in "QUV"}
+    Hh = pkg.forward_host(h["Q"], h["U"], h["V"], scale=w.scale)
+    torch.cuda.current_stream().synchronize()
+    Hd = pkg.forward(d["Q"], d["U"], d["V"], scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(Hh.view(torch.int16), Hd.cpu().view(torch.int16))
+    assert pkg.device_error() == 0
+
+
 def test_host_entry_chunks_of_a_large_batch(env):
     """B = 5 entries, 184 MB of Q, V and H: three chunks (1, 2 and 2 entries) over two buffer
     sets; every entry against the device entry."""

@@ -281,6 +281,27 @@ def test_split_tiles_every_slice(env, shape):
         assert_slices(Hc, w, oracle_slices(orc, w, x, range(s0, min(w.slices, s0 + 64))), "split")
 
 
+# A few slices of many tiles: a cluster of c CTAs per slice, the c partial sums added over
+# distributed shared memory in rank order.  (B, heads, n, m, d, CTAs per slice): ragged
+# tails, padded anchors, clusters of 4, 6 and 8.
+@pytest.mark.parametrize("shape", [(1, 1, 4200, 64, 64, 8), (2, 3, 8000, 50, 64, 8), (1, 8, 16384, 64, 64, 8),
+                                   (4, 8, 8000, 33, 64, 4), (1, 16, 16384, 40, 64, 6)])
+def test_stream_clusters_every_slice(env, shape):
+    pkg, torch, orc = env
+    B, heads, n, m, d, per_slice = shape
+    w = gen.WORKLOADS["det_800x1344"].with_(name="clusters", B=B, heads=heads, n=n, m=m, d=d)
+    plan = pkg.query_plan("bf16", B, heads, n, m, d)
+    assert plan["variant"] == "stream" and plan["splits"] == per_slice
+    x = gen.make_inputs(w, seed=sum(shape))
+    H = _run(env, w, x)
+    H2 = _run(env, w, x)
+    assert pkg.device_error() == 0
+    assert torch.equal(H.view(torch.int16), H2.view(torch.int16))
+    Hc = H.cpu()
+    for s0 in range(0, w.slices, 64):
+        assert_slices(Hc, w, oracle_slices(orc, w, x, range(s0, min(w.slices, s0 + 64))), "clusters")
+
+
 @pytest.mark.parametrize("name", ["det_800x1344", "deit_base", "deit_small"])
 def test_dependent_calls_back_to_back(env, name):
     """Kernels launched with programmatic stream serialization start while the previous kernel
