@@ -262,7 +262,7 @@ ANCHOR_ATTN_API size_t anchor_attn_static_scratch_bytes(void);
 typedef struct {
     int variant;              /* ANCHOR_ATTN_VARIANT_*                                  */
     int kernels_per_call;     /* kernel launches one call makes                        */
-    int splits;               /* token chunks per slice whose partials are reduced     */
+    int splits;               /* token chunks (CTAs) per slice whose partials are reduced */
     int flags;                /* ANCHOR_ATTN_PLAN_* (tensor-core variant)               */
     size_t workspace_bytes;   /* device workspace one call allocates (0 if none)       */
 } anchor_attn_plan_t;
@@ -285,7 +285,9 @@ enum {
  * the one a call with a positive scale makes: bf16 with d = 64, 32 <= m <= 64 and n <= 256
  * runs one CTA per slice with the slice's tiles in shared memory (any scale); with n > 512 it runs
  * a slice-streaming tensor-core variant (any scale): one CTA per slice when there are at most
- * 152 slices, else the slices' 128-token tiles cut into 152 contiguous ranges, one per CTA,
+ * 152 slices (with at most 38 slices of many tiles, a thread-block cluster of 2 to 8 CTAs per
+ * slice, the CTAs' partial sums added in rank order; `splits` = CTAs per slice, chosen from the
+ * shape alone), else the slices' 128-token tiles cut into 152 contiguous ranges, one per CTA,
  * all resident at once (a device that cannot hold 152 such CTAs runs one CTA per slice
  * instead, in another summation order); otherwise the persistent tensor-core variant takes
  * bf16, d in {64, 128}, 32 <= m <= 128 and scale > 0 (a non-positive scale runs a CUDA-core
