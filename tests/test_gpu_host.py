@@ -80,6 +80,24 @@ def test_host_entry_head_chunks_keep_the_cluster_plan(env):
     assert pkg.device_error() == 0
 
 
+def test_host_entry_more_large_entries_than_chunks(env):
+    """17 batch entries of 72 MB of Q, V and H each (6 heads of 16384 tokens at d = m = 128):
+    more entries than the 16 chunks a call overlaps, each larger than a chunk's aim; the
+    chunks stay whole-entry groups (16 of them) and the bits are the device entry's."""
+    pkg, torch = env
+    w = gen.WORKLOADS["long_16k"].with_(name="host_many", B=17, heads=6)
+    x = gen.make_inputs(w, seed=59)
+    h = {k: _host(x[k], w.dtype, torch, True) for k in "QUV"}
+    del x
+    Hh = pkg.forward_host(h["Q"], h["U"], h["V"], scale=w.scale)
+    torch.cuda.current_stream().synchronize()
+    d = {k: h[k].to("cuda") for k in "QUV"}
+    Hd = pkg.forward(d["Q"], d["U"], d["V"], scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(Hh.view(torch.int16), Hd.cpu().view(torch.int16))
+    assert pkg.device_error() == 0
+
+
 def test_host_entry_chunks_of_a_large_batch(env):
     """B = 5 entries, 184 MB of Q, V and H: three chunks (1, 2 and 2 entries) over two buffer
     sets; every entry against the device entry."""
