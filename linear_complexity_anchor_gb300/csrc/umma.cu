@@ -1584,9 +1584,9 @@ UmmaPlan umma_plan(const Problem &p, bool force_recompute) {
         return pl;
     }
     pl.C2 = (pl.NT + t2 - 1) / t2;
-    // the last slices' pass 2 in chunks kUmmaFineSplit times finer: about a quarter of a round
-    // of pass-2 items' worth of slices, which the SMs freed first share out at the end
-    // (long_16k: 207.0 -> 203.5 us; half a round 204.8, a whole round 207.0, four times finer
+    // the last slices' pass 2 in chunks kUmmaFineSplit times finer: about a quarter of a wave
+    // (one pass-2 item per SM) of slices, which the SMs freed first share out at the end
+    // (long_16k: 207.0 -> 203.5 us; half a wave 204.8, a whole wave 207.0, four times finer
     // 208.4)
     pl.C2f = std::min(pl.NT, pl.C2 * kUmmaFineSplit);
     const long long fine = std::min<long long>(S, ((long long)kPlanSMs * t2 / 4 + pl.NT - 1) / pl.NT);
