@@ -94,6 +94,11 @@ def test_plans(pkg):
     assert p["workspace_bytes"] == 8 * 12 * 4200 * 64 * 2
     assert pkg.query_plan("bf16", 1, 1, 4200, 64, 64)["splits"] == 8
     assert pkg.query_plan("bf16", 1, 16, 16384, 64, 64)["splits"] == 6
+    # clusters up to 38 slices (38 of 128 tiles: 3 CTAs; 39: one CTA per slice) and only with
+    # four tiles or more per CTA (1 slice of 5 tiles: one CTA)
+    assert pkg.query_plan("bf16", 1, 38, 16384, 64, 64)["splits"] == 3
+    assert pkg.query_plan("bf16", 1, 39, 16384, 64, 64)["splits"] == 1
+    assert pkg.query_plan("bf16", 1, 1, 600, 64, 64)["splits"] == 1
     assert pkg.query_plan("bf16", 4, 10, 600, 40, 64)["splits"] == 1
     p = pkg.query_plan("bf16", 16, 12, 4200, 64, 64)
     assert p["variant"] == "split_tc" and p["stored_a"] and p["workspace_bytes"] > 16 * 12 * 4200 * 64 * 2
